@@ -1,0 +1,338 @@
+#!/usr/bin/env python3
+"""Benchmark of the SSD forward pass (one JSON line on rank 0).
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+                    [--workload 27b|sweep:B:L:S|long|varlen|tiny]
+
+A step is one ssd_fwd call over one batch of the workload (default: the
+Mamba-2 2.7B-like layer, batch 8 x 2048 tokens, 80 heads, P 64, N 128, bf16).
+Inputs are synthetic (seeded), resident in HBM before timing; L2 is flushed
+(a 256 MiB write) before every timed step.  Under torchrun each rank runs its
+own copy of the workload (independent batch rows: weak scaling) and rank 0
+reports the aggregate over ranks with the slowest rank's time.
+
+--impl reference times the fp64 CPU oracle recurrence on the host cores on a
+bounded sample of the same workload (one batch row per step).
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import numpy as np  # noqa: E402
+
+from mamba_ssd_chunked_scan_gb300 import synth  # noqa: E402
+
+METRIC = "SSD fwd tokens/s and achieved HBM GB/s (% of GB300 roofline) vs L, 1 GPU"
+FALLBACK_HBM_GBS = 6800.0
+
+
+def workload(name: str):
+    if name == "27b":
+        return synth.config_27b()
+    if name == "tiny":
+        return synth.config_tiny_f32()
+    if name == "long":
+        return synth.config_long()
+    if name == "varlen":
+        return synth.config_varlen()
+    if name.startswith("sweep"):
+        _, b, L, s = name.split(":")
+        return synth.config_sweep(int(b), int(L), int(s))
+    raise ValueError(name)
+
+
+def compulsory_bytes(p) -> int:
+    """x + dt + B + C + y: the bytes the operator must move at least once."""
+    e = 2 if p.dtype == "bf16" else 4
+    T = p.batch * p.seqlen
+    return T * (2 * p.nheads * p.headdim * e + p.nheads * 4 + 2 * p.ngroups * p.dstate * e)
+
+
+def peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        try:
+            d = json.load(open(path))
+            for k in ("hbm_gbs", "hbm_GBs", "hbm_copy_gbs"):
+                if k in d:
+                    return float(d[k]), "measured"
+        except Exception:
+            pass
+    return FALLBACK_HBM_GBS, "fallback"
+
+
+def dist_env():
+    return int(os.environ.get("RANK", 0)), int(os.environ.get("LOCAL_RANK", 0)), int(os.environ.get("WORLD_SIZE", 1))
+
+
+class ClockSampler:
+    """nvidia-smi clocks / throttle reasons sampled during the timed region."""
+
+    def __init__(self, index: int):
+        self.index = index
+        self.rows = []
+        self.proc = None
+
+    def __enter__(self):
+        q = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+             "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+             "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+        try:
+            self.proc = subprocess.Popen(["nvidia-smi", "-i", str(self.index), f"--query-gpu={q}",
+                                          "--format=csv,noheader,nounits", "-lms", "100"],
+                                         stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.t = threading.Thread(target=self._read, daemon=True)
+            self.t.start()
+        except Exception:
+            self.proc = None
+        return self
+
+    def _read(self):
+        for line in self.proc.stdout:
+            parts = [s.strip() for s in line.split(",")]
+            if len(parts) >= 8:
+                self.rows.append(parts)
+
+    def __exit__(self, *a):
+        if self.proc:
+            time.sleep(0.25)
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except Exception:
+                self.proc.kill()
+
+    def summary(self):
+        if not self.rows:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unsampled"]}
+        def num(v):
+            try:
+                return float(v)
+            except ValueError:
+                return None
+        sm = [num(r[0]) for r in self.rows if num(r[0]) is not None]
+        mx = [num(r[1]) for r in self.rows if num(r[1]) is not None]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for r in self.rows for i in range(4) if r[4 + i].lower() == "active"})
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(mx) if mx else None,
+                "reasons": reasons, "samples": len(self.rows)}
+
+
+def kernel_traffic(family: int):
+    """DRAM bytes per launch of the dominant kernel from the committed ncu
+    summary, used only while the kernel source is unchanged since capture."""
+    path = os.path.join(ROOT, "profiles", "traffic.json")
+    if not os.path.exists(path):
+        return None
+    try:
+        d = json.load(open(path))
+        ent = d.get(str(family))
+        if not ent:
+            return None
+        src = os.path.join(ROOT, "mamba_ssd_chunked_scan_gb300", "csrc", ent["source"])
+        sha = hashlib.sha256(open(src, "rb").read()).hexdigest()[:16]
+        return ent["dram_bytes_per_launch"] if sha == ent["source_sha"] else None
+    except Exception:
+        return None
+
+
+def run_reference(args):
+    import oracle
+    rank, _, world = dist_env()
+    if rank != 0:
+        return
+    p = workload(args.workload)
+    # bounded sample: one batch row of the workload per step
+    q = synth.SSDProblem(1, p.seqlen, p.nheads, p.headdim, p.dstate, p.ngroups, p.chunk, p.split_len,
+                         p.dtype, p.x[:1].copy(), p.dt[:1].copy(), p.A, p.B[:1].copy(), p.C[:1].copy(), p.D,
+                         None if p.initial_states is None else p.initial_states[:1].copy(), p.cu_seqlens,
+                         p.name)
+    for _ in range(args.warmup):
+        oracle.ssd_recurrence(q, want_final=p.initial_states is not None)
+    times = []
+    for _ in range(args.steps):
+        t0 = time.perf_counter()
+        oracle.ssd_recurrence(q, want_final=p.initial_states is not None)
+        times.append(time.perf_counter() - t0)
+    ms = 1e3 * sum(times) / len(times)
+    tok = q.batch * q.seqlen
+    value = tok / (ms / 1e3)
+    cores = oracle.max_threads()
+    line = {"impl": "reference", "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": {"workload": p.name, "sample": f"1 of {p.batch} batch rows per step"},
+            "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": cores, "kind": "oracle",
+                             "sample": f"fp64 sequential recurrence, batch row 0 of {p.name} per step"},
+            "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+
+
+def cpu_baseline(p):
+    import oracle
+    q = synth.SSDProblem(1, p.seqlen, p.nheads, p.headdim, p.dstate, p.ngroups, p.chunk, p.split_len,
+                         p.dtype, p.x[:1].copy(), p.dt[:1].copy(), p.A, p.B[:1].copy(), p.C[:1].copy(), p.D,
+                         None if p.initial_states is None else p.initial_states[:1].copy(), p.cu_seqlens,
+                         p.name)
+    reps, t_all = 0, 0.0
+    while t_all < 10.0 and reps < 16:
+        t0 = time.perf_counter()
+        oracle.ssd_recurrence(q, want_final=False)
+        t_all += time.perf_counter() - t0
+        reps += 1
+    tok = q.batch * q.seqlen * reps
+    return {"value": tok / t_all, "unit": "tokens/s", "cores": oracle.max_threads(), "kind": "oracle",
+            "sample": f"fp64 recurrence on batch row 0 of {p.name}, {reps} passes, {t_all:.1f} s wall"}
+
+
+def run_ours(args):
+    import torch
+    import torch.distributed as dist
+    import mamba_ssd_chunked_scan_gb300 as ssd
+
+    rank, local_rank, world = dist_env()
+    torch.cuda.set_device(local_rank)
+    dev = torch.device("cuda", local_rank)
+    if world > 1:
+        dist.init_process_group("nccl", device_id=dev)
+    p = workload(args.workload)
+    dtype = torch.bfloat16 if p.dtype == "bf16" else torch.float32
+
+    def dev_io(name):
+        if p.dtype == "bf16":
+            return torch.from_numpy(p.storage(name).view(np.int16).copy()).to(dev).view(torch.bfloat16)
+        return torch.from_numpy(getattr(p, name)).to(dev)
+
+    x, B, C = dev_io("x"), dev_io("B"), dev_io("C")
+    dt = torch.from_numpy(p.dt).to(dev)
+    A = torch.from_numpy(p.A).to(dev)
+    D = None if p.D is None else torch.from_numpy(p.D).to(dev)
+    init = None if p.initial_states is None else torch.from_numpy(p.initial_states).to(dev)
+    cu = None if p.cu_seqlens is None else torch.from_numpy(p.cu_seqlens).to(dev)
+    want_final = init is not None
+    f = ssd.SSDForward(p.batch, p.seqlen, p.nheads, p.headdim, p.dstate, p.ngroups, p.chunk, p.split_len,
+                       p.ndocs, dtype, dev)
+    family, launches, nsplit = f.plan(init is not None, want_final)
+    y = torch.empty_like(x)
+    fin = torch.empty((f.nstates, p.nheads, p.headdim, p.dstate), dtype=torch.float32, device=dev) \
+        if want_final else None
+    flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
+    stream = torch.cuda.current_stream()
+
+    def step():
+        f(x, dt, A, B, C, D, init, cu, y=y, final_states=fin, stream=stream)
+
+    for _ in range(args.warmup):
+        flush.zero_()
+        step()
+    assert f.check_status() == 0
+    torch.cuda.synchronize()
+    if world > 1:
+        dist.barrier()
+    torch.cuda.synchronize()
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
+    with ClockSampler(local_rank) as clk:
+        for i in range(args.steps):
+            flush.zero_()
+            ev[i][0].record(stream)
+            step()
+            ev[i][1].record(stream)
+        torch.cuda.synchronize()
+    if world > 1:
+        dist.barrier()
+    st = f.check_status()
+    assert st == 0, f"device status {st}"
+    kt = [a.elapsed_time(b) for a, b in ev]
+    ms = sum(kt) / len(kt)
+
+    # end to end through the public API: pinned host inputs -> device -> ssd_fwd -> host y
+    hx, hB, hC = x.cpu().pin_memory(), B.cpu().pin_memory(), C.cpu().pin_memory()
+    hdt = dt.cpu().pin_memory()
+    hy = torch.empty(y.shape, dtype=y.dtype).pin_memory()
+    hfin = torch.empty(fin.shape, dtype=torch.float32).pin_memory() if fin is not None else None
+    h2d = sum(t.numel() * t.element_size() for t in (hx, hB, hC, hdt))
+    d2h = hy.numel() * hy.element_size() + (hfin.numel() * 4 if hfin is not None else 0)
+    e2e_t = []
+    for i in range(args.warmup + args.steps):
+        torch.cuda.synchronize()
+        s0, s1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        s0.record(stream)
+        x.copy_(hx, non_blocking=True); B.copy_(hB, non_blocking=True); C.copy_(hC, non_blocking=True)
+        dt.copy_(hdt, non_blocking=True)
+        step()
+        hy.copy_(y, non_blocking=True)
+        if hfin is not None:
+            hfin.copy_(fin, non_blocking=True)
+        s1.record(stream)
+        s1.synchronize()
+        if i >= args.warmup:
+            e2e_t.append(s0.elapsed_time(s1))
+    e2e_ms = sum(e2e_t) / len(e2e_t)
+
+    t_tensor = torch.tensor([ms, e2e_ms], dtype=torch.float64, device=dev)
+    if world > 1:
+        dist.all_reduce(t_tensor, op=dist.ReduceOp.MAX)
+        dist.barrier()
+    ms_max, e2e_max = float(t_tensor[0]), float(t_tensor[1])
+    tokens = p.batch * p.seqlen
+    value = world * tokens / (ms_max / 1e3)
+    e2e_value = world * tokens / (e2e_max / 1e3)
+    if rank == 0:
+        nbytes = compulsory_bytes(p)
+        peak, peak_kind = peaks()
+        achieved = nbytes / (ms / 1e3) / 1e9
+        traffic = kernel_traffic(family) if nsplit == 1 else None
+        line = {
+            "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": ms_max, "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "bf16" if family == 1 else "f32", "data": "synthetic",
+            "config": {"workload": p.name, "batch": p.batch, "seq_len": p.seqlen, "nheads": p.nheads,
+                       "headdim": p.headdim, "dstate": p.dstate, "ngroups": p.ngroups, "chunk": p.chunk,
+                       "split_len": p.split_len, "nsplits": nsplit, "storage": p.dtype,
+                       "kernel": "tcgen05" if family == 1 else "simt",
+                       "l2": "256 MiB write before every timed step; inputs larger than L2",
+                       "compulsory_bytes": nbytes, "achieved_GBps": achieved,
+                       "pct_of_8TBps_spec": 100.0 * achieved / 8000.0},
+            "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
+                         "frac": achieved / peak, "peak_source": peak_kind, "traffic": traffic},
+            "e2e": {"value": e2e_value, "unit": "tokens/s", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
+            "gpu_launches": launches * args.steps,
+            "clocks": clk.summary(),
+        }
+        if world == 1 and not args.no_cpu_baseline:
+            line["cpu_baseline"] = cpu_baseline(p)
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        dist.destroy_process_group()
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--workload", default="27b")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    if args.warmup < 3 and args.impl == "ours":
+        args.warmup = 3
+    if args.impl == "reference":
+        run_reference(args)
+    else:
+        run_ours(args)
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,139 @@
+/*
+ * libssd: Mamba-2 structured-state-space-duality (SSD) chunked-scan forward
+ * pass for NVIDIA GB300 (sm_103a).  C ABI: plain pointers and sizes only.
+ *
+ * The operation ("State Space Duality and Mamba-2", sections "The
+ * Mathematical Bridge" and "The SSD Block Decomposition Algorithm"; the
+ * discretisation is the selective-scan one of "NVIDIA Accelerates Mamba-2
+ * Forward Kernel with CUDA Tile", where the decay and input matrices depend
+ * on the step size dt):  per batch row b and head h, with group
+ * g = h / (H / G),
+ *
+ *     h_t = exp(dt_t * A_h) * h_{t-1} + dt_t * x_t B_t^T        (P x N state)
+ *     y_t = h_t C_t + D_h * x_t
+ *
+ * computed chunk by chunk: the intra-chunk block ((C B^T) o L) X with the
+ * 1-semiseparable decay mask L_ij = exp(sum_{k=j+1..i} dt_k A_h), chunk
+ * states B^T (decay o X), inter-chunk state passing and the off-diagonal
+ * output C * state.  A sequence may also be cut into splits of split_len
+ * tokens that run in parallel and are joined by composing their states
+ * ("GPU Hierarchy Meets Structured Matrices", abstract: the split-sequence
+ * algorithm; "Parallel Scan and Hardware-Aware SSM Kernels", "The scan": the
+ * affine-step composition).  Packed documents (cu_seqlens) restart the state
+ * at every document start (same page, "When it breaks").
+ *
+ * Layouts (all row-major, contiguous, device memory, 16-byte aligned bases):
+ *   x, y            (batch, seqlen, nheads, headdim)      dtype
+ *   dt              (batch, seqlen, nheads)               fp32, >= 0 (post-softplus)
+ *   A, D            (nheads)                              fp32 (A <= 0; D optional)
+ *   B, C            (batch, seqlen, ngroups, dstate)      dtype
+ *   initial_states  (nstates, nheads, headdim, dstate)    fp32, optional (zeros)
+ *   final_states    (nstates, nheads, headdim, dstate)    fp32, optional
+ *   cu_seqlens      (ndocs + 1) int32, cu[0] = 0, cu[ndocs] = seqlen, optional
+ *   nstates = ndocs when cu_seqlens is given (then batch must be 1), else batch.
+ *
+ * Ownership: the caller owns every buffer; the library keeps no pointer past
+ * a call and allocates no device memory.  Calls are asynchronous on the given
+ * stream (a cudaStream_t passed as void*; NULL = legacy default stream).
+ *
+ * Errors: argument errors return a status before anything is launched and
+ * nothing is written.  A failed launch returns SSD_ERR_CUDA.  Errors found on
+ * the device (a bounded wait that ran out) are recorded in a status word at
+ * the start of the workspace and are read by ssd_check_status().
+ */
+#ifndef SSD_H_
+#define SSD_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#if defined(__GNUC__)
+#define SSD_API __attribute__((visibility("default")))
+#else
+#define SSD_API
+#endif
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+    SSD_OK = 0,
+    SSD_ERR_INVALID_ARG = 1,   /* bad pointer, size, alignment or layout */
+    SSD_ERR_UNSUPPORTED = 2,   /* valid but not implemented (e.g. chunk 256) */
+    SSD_ERR_WORKSPACE = 3,     /* workspace missing or smaller than required */
+    SSD_ERR_CUDA = 4,          /* a CUDA runtime call or launch failed */
+    SSD_ERR_TIMEOUT = 5,       /* a device-side bounded wait ran out */
+    SSD_ERR_DEVICE_CHECK = 6   /* a device-side consistency check failed */
+} ssd_status_t;
+
+typedef enum { SSD_F32 = 0, SSD_BF16 = 1 } ssd_dtype_t;
+
+typedef struct {
+    int64_t batch;      /* batch rows (1 when cu_seqlens is given)                  */
+    int64_t seqlen;     /* tokens per row (total packed length with cu_seqlens)      */
+    int32_t nheads;     /* H                                                         */
+    int32_t headdim;    /* P                                                         */
+    int32_t dstate;     /* N                                                         */
+    int32_t ngroups;    /* G, H % G == 0; head h reads B, C of group h / (H / G)     */
+    int32_t chunk;      /* Q: 64 or 128                                              */
+    int32_t split_len;  /* tokens per split: a multiple of chunk; 0 = automatic;
+                           >= seqlen = one split.  Never changes the result beyond
+                           rounding.                                                 */
+    int32_t ndocs;      /* documents when cu_seqlens is given, else 0                */
+    int32_t dtype;      /* ssd_dtype_t of x, B, C and y                              */
+} ssd_params_t;
+
+/* Bytes of device workspace ssd_fwd() needs for these parameters (>= 256:
+ * the first 256 bytes hold the device status word).  0 on invalid params. */
+SSD_API size_t ssd_fwd_workspace_size(const ssd_params_t* p);
+
+/* Zero the workspace's status word (async on `stream`).  Call once after
+ * allocating a workspace; the status word then stays zero until a device
+ * error is recorded, and ssd_check_status() clears it again. */
+SSD_API int ssd_workspace_init(void* workspace, size_t workspace_bytes, void* stream);
+
+/* The SSD forward pass: y (and optionally final_states) from x, dt, A, B, C
+ * and the optional D, initial_states and cu_seqlens, as defined above.
+ * `workspace` is device scratch of at least ssd_fwd_workspace_size(p) bytes,
+ * initialised once by ssd_workspace_init(); calls that share a workspace must
+ * be ordered on one stream.  y must not alias any input.  final_states may
+ * alias initial_states.  Bitwise deterministic for fixed inputs and params. */
+SSD_API int ssd_fwd(const ssd_params_t* p,
+            const void* x, const float* dt, const float* A,
+            const void* B, const void* C, const float* D,
+            const float* initial_states, const int32_t* cu_seqlens,
+            void* y, float* final_states,
+            void* workspace, size_t workspace_bytes, void* stream);
+
+/* Synchronise `stream`, read the device status word of `workspace`, clear it,
+ * and return it (SSD_OK when no device error was recorded). */
+SSD_API int ssd_check_status(void* workspace, void* stream);
+
+/* Human-readable name of a status code (static storage). */
+SSD_API const char* ssd_status_string(int status);
+
+/* Which kernel family ssd_fwd() uses for these params:
+ * 0 = SIMT fp32 kernel, 1 = tcgen05 tensor-core kernel; -1 on invalid params.
+ * *launches (if not NULL) receives the number of kernel launches per call. */
+SSD_API int ssd_fwd_plan(const ssd_params_t* p, int has_initial_states, int has_final_states,
+                 int* launches, int* nsplits);
+
+/* The hierarchy-aware segsum device routine on its own (test aid).
+ * log2decay: (nrows, chunk) fp32 log2-domain log-decays (<= 0, may be -inf),
+ * chunk 64 or 128.  For each row, writes seg (chunk x chunk, fp32):
+ * seg[i][j] = sum_{k=j+1..i} log2decay[k] for j <= i as the kernels compute
+ * it (no prefix subtraction), -inf above the diagonal; and L (chunk x chunk):
+ * the decay-mask values 2^seg the tensor-core kernel multiplies in (on
+ * off-diagonal 32 x 32 blocks as the rank-one product of a row and a column
+ * factor), 0 above the diagonal.  Either output may be NULL.
+ * Device pointers; async on `stream`.
+ * Source: "GPU Hierarchy Meets Structured Matrices" (abstract): the 1-SS mask
+ * as 1-SS diagonal blocks plus rank-one off-diagonal blocks. */
+SSD_API int ssd_segsum_dump(const float* log2decay, int64_t nrows, int32_t chunk,
+                    float* seg_out, float* L_out, void* stream);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* SSD_H_ */

@@ -1,0 +1,153 @@
+"""Mamba-2 SSD chunked-scan forward pass for GB300 (sm_103a).
+
+Thin PyTorch-facing wrapper over the C ABI of ``libssd.so`` (include/ssd.h):
+it checks tensor shapes, takes device pointers and the current CUDA stream,
+and calls the library.  PyTorch provides device memory and streams only;
+every arithmetic step runs in the library's CUDA kernels.
+"""
+from __future__ import annotations
+
+import ctypes
+from typing import Optional
+
+import importlib
+
+import torch
+
+SSD_F32, SSD_BF16 = 0, 1
+
+
+class _LazyLib:
+    """Loads libssd.so on first use; raises ImportError if it is not built."""
+
+    def __getattr__(self, name):
+        mod = importlib.import_module(__name__ + "._lib")
+        return getattr(mod, name)
+
+
+_lib = _LazyLib()
+
+
+def __getattr__(name):
+    if name == "SSDError":
+        return _lib.SSDError
+    raise AttributeError(name)
+
+__all__ = ["ssd_fwd", "SSDForward", "segsum_dump", "check_status", "SSDError", "plan"]
+
+
+def _ptr(t: Optional[torch.Tensor]):
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+def _stream_handle(stream: Optional[torch.cuda.Stream]):
+    s = stream if stream is not None else torch.cuda.current_stream()
+    return ctypes.c_void_p(s.cuda_stream)
+
+
+def _dtype_code(t: torch.Tensor) -> int:
+    if t.dtype == torch.bfloat16:
+        return SSD_BF16
+    if t.dtype == torch.float32:
+        return SSD_F32
+    raise TypeError(f"x/B/C must be bf16 or fp32, got {t.dtype}")
+
+
+class SSDForward:
+    """A reusable SSD forward call with fixed shapes: owns its workspace.
+
+    shapes: x (batch, L, H, P), dt (batch, L, H), A (H), B/C (batch, L, G, N),
+    D (H) or None, initial/final states (nstates, H, P, N) fp32, cu_seqlens
+    (ndocs + 1) int32 or None.
+    """
+
+    def __init__(self, batch, seqlen, nheads, headdim, dstate, ngroups=1, chunk=128, split_len=0,
+                 ndocs=0, dtype=torch.bfloat16, device="cuda"):
+        self.params = _lib.make_params(batch, seqlen, nheads, headdim, dstate, ngroups, chunk,
+                                       split_len, ndocs, SSD_BF16 if dtype == torch.bfloat16 else SSD_F32)
+        self.dtype = dtype
+        nbytes = _lib.workspace_size(self.params)
+        if nbytes == 0:
+            raise _lib.SSDError(1, "invalid SSD parameters")
+        self.device = torch.device(device)
+        self.workspace = torch.zeros(nbytes, dtype=torch.uint8, device=self.device)
+        self.nstates = ndocs if ndocs > 0 else batch
+
+    @property
+    def workspace_bytes(self) -> int:
+        return self.workspace.numel()
+
+    def plan(self, has_init=False, has_final=False):
+        return _lib.plan(self.params, has_init, has_final)
+
+    def __call__(self, x, dt, A, B, C, D=None, initial_states=None, cu_seqlens=None, y=None,
+                 final_states=None, stream=None):
+        p = self.params
+        shp_x = (p.batch, p.seqlen, p.nheads, p.headdim)
+        shp_bc = (p.batch, p.seqlen, p.ngroups, p.dstate)
+        shp_s = (self.nstates, p.nheads, p.headdim, p.dstate)
+        for name, t, shp, dt_ in (("x", x, shp_x, self.dtype), ("dt", dt, shp_x[:3], torch.float32),
+                                  ("A", A, (p.nheads,), torch.float32), ("B", B, shp_bc, self.dtype),
+                                  ("C", C, shp_bc, self.dtype), ("D", D, (p.nheads,), torch.float32),
+                                  ("initial_states", initial_states, shp_s, torch.float32),
+                                  ("final_states", final_states, shp_s, torch.float32),
+                                  ("y", y, shp_x, self.dtype)):
+            if t is None:
+                continue
+            if tuple(t.shape) != shp or t.dtype != dt_ or not t.is_contiguous() or t.device != self.device:
+                raise ValueError(f"{name}: expected contiguous {dt_} {shp} on {self.device}, got "
+                                 f"{t.dtype} {tuple(t.shape)} on {t.device}")
+        if (cu_seqlens is None) != (p.ndocs == 0):
+            raise ValueError("cu_seqlens must be given exactly when ndocs > 0")
+        if cu_seqlens is not None and (cu_seqlens.dtype != torch.int32 or cu_seqlens.numel() != p.ndocs + 1
+                                       or cu_seqlens.device != self.device):
+            raise ValueError("cu_seqlens: expected int32 (ndocs + 1) on the device")
+        if y is None:
+            y = torch.empty(shp_x, dtype=self.dtype, device=self.device)
+        rc = _lib.lib.ssd_fwd(ctypes.byref(p), _ptr(x), _ptr(dt), _ptr(A), _ptr(B), _ptr(C), _ptr(D),
+                              _ptr(initial_states), _ptr(cu_seqlens), _ptr(y), _ptr(final_states),
+                              _ptr(self.workspace), self.workspace.numel(), _stream_handle(stream))
+        _lib.check(rc, "ssd_fwd")
+        return y
+
+    def check_status(self, stream=None) -> int:
+        return check_status(self.workspace, stream)
+
+
+def ssd_fwd(x, dt, A, B, C, D=None, initial_states=None, cu_seqlens=None, *, chunk=128, split_len=0,
+            return_final_states=False, stream=None):
+    """One SSD forward call.  Returns y, or (y, final_states) when asked."""
+    batch, seqlen, nheads, headdim = x.shape
+    ngroups, dstate = B.shape[2], B.shape[3]
+    ndocs = 0 if cu_seqlens is None else cu_seqlens.numel() - 1
+    f = SSDForward(batch, seqlen, nheads, headdim, dstate, ngroups, chunk, split_len, ndocs,
+                   x.dtype, x.device)
+    fin = None
+    if return_final_states:
+        fin = torch.empty((f.nstates, nheads, headdim, dstate), dtype=torch.float32, device=x.device)
+    y = f(x, dt, A, B, C, D, initial_states, cu_seqlens, final_states=fin, stream=stream)
+    st = f.check_status(stream)
+    if st != 0:
+        raise _lib.SSDError(st, "ssd_fwd device status")
+    return (y, fin) if return_final_states else y
+
+
+def check_status(workspace: torch.Tensor, stream=None) -> int:
+    return int(_lib.lib.ssd_check_status(_ptr(workspace), _stream_handle(stream)))
+
+
+def plan(params) -> tuple:
+    return _lib.plan(params)
+
+
+def segsum_dump(log2decay: torch.Tensor, want_seg=True, want_L=True, stream=None):
+    """Run the hierarchy-aware segsum device routine on rows of log2-decays
+    (nrows, chunk) fp32; returns (seg, L), each (nrows, chunk, chunk) or None."""
+    if log2decay.dtype != torch.float32 or log2decay.dim() != 2 or not log2decay.is_contiguous():
+        raise ValueError("log2decay: contiguous fp32 (nrows, chunk)")
+    nrows, q = log2decay.shape
+    seg = torch.empty((nrows, q, q), dtype=torch.float32, device=log2decay.device) if want_seg else None
+    L = torch.empty((nrows, q, q), dtype=torch.float32, device=log2decay.device) if want_L else None
+    rc = _lib.lib.ssd_segsum_dump(_ptr(log2decay), nrows, q, _ptr(seg), _ptr(L), _stream_handle(stream))
+    _lib.check(rc, "ssd_segsum_dump")
+    return seg, L

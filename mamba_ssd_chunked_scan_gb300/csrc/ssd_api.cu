@@ -1,0 +1,174 @@
+// C ABI of libssd: argument checks, the split plan, and kernel dispatch.
+// Nothing here allocates device memory; every launch is asynchronous on the
+// caller's stream.
+#include <stdio.h>
+#include <string.h>
+
+#include "ssd_common.cuh"
+#include "ssd_kernels.h"
+
+using namespace ssd;
+
+namespace {
+
+constexpr int kSmemLimit = 227 * 1024;
+constexpr int64_t kAutoTargetUnits = 2 * 152;   // independent (row, head, split) units wanted
+
+bool aligned(const void* p, size_t a) { return ((uintptr_t)p % a) == 0; }
+
+int check_params(const ssd_params_t* p) {
+    if (!p) return SSD_ERR_INVALID_ARG;
+    if (p->batch < 1 || p->seqlen < 1 || p->nheads < 1 || p->headdim < 1 || p->dstate < 1 ||
+        p->ngroups < 1)
+        return SSD_ERR_INVALID_ARG;
+    if (p->nheads % p->ngroups != 0) return SSD_ERR_INVALID_ARG;
+    if (p->dtype != SSD_F32 && p->dtype != SSD_BF16) return SSD_ERR_INVALID_ARG;
+    if (p->chunk != 64 && p->chunk != 128) return (p->chunk > 0) ? SSD_ERR_UNSUPPORTED : SSD_ERR_INVALID_ARG;
+    if (p->split_len < 0 || (p->split_len % p->chunk) != 0) return SSD_ERR_INVALID_ARG;
+    if (p->ndocs < 0) return SSD_ERR_INVALID_ARG;
+    if (p->ndocs > 0 && p->batch != 1) return SSD_ERR_INVALID_ARG;
+    // element counts must fit the 32-bit grid and index arithmetic
+    if (p->batch * p->nheads > (int64_t)1 << 30) return SSD_ERR_UNSUPPORTED;
+    // x/y rows must keep 16-byte alignment (vector and bulk copies)
+    const int esz = p->dtype == SSD_BF16 ? 2 : 4;
+    if ((p->headdim * esz) % 16 != 0 || (p->dstate * esz) % 16 != 0) return SSD_ERR_UNSUPPORTED;
+    return SSD_OK;
+}
+
+int64_t plan_split_len(const ssd_params_t* p) {
+    const int64_t L = p->seqlen;
+    int64_t sl = p->split_len;
+    if (sl == 0) {
+        const int64_t bh = p->batch * p->nheads;
+        if (bh >= kAutoTargetUnits) {
+            sl = L;
+        } else {
+            const int64_t want = (kAutoTargetUnits + bh - 1) / bh;
+            sl = (L + want - 1) / want;
+            sl = (sl + p->chunk - 1) / p->chunk * p->chunk;
+            if (sl < 4 * p->chunk) sl = 4 * p->chunk;   // keep boundary-state traffic small
+        }
+    }
+    if (sl >= L) sl = (L + p->chunk - 1) / p->chunk * p->chunk;
+    return sl;
+}
+
+int plan_nsplit(const ssd_params_t* p) {
+    const int64_t sl = plan_split_len(p);
+    return (int)((p->seqlen + sl - 1) / sl);
+}
+
+// SIMT kernel chunk: the caller's chunk when its shared-memory tiles fit,
+// else 64 (the chunk size changes only the rounding, not the result).
+int simt_chunk(const ssd_params_t* p) {
+    if (simt_smem_bytes(p->chunk, p->headdim, p->dstate) <= (size_t)kSmemLimit) return p->chunk;
+    if (simt_smem_bytes(64, p->headdim, p->dstate) <= (size_t)kSmemLimit) return 64;
+    return 0;
+}
+
+}  // namespace
+
+extern "C" {
+
+const char* ssd_status_string(int s) {
+    switch (s) {
+        case SSD_OK: return "SSD_OK";
+        case SSD_ERR_INVALID_ARG: return "SSD_ERR_INVALID_ARG";
+        case SSD_ERR_UNSUPPORTED: return "SSD_ERR_UNSUPPORTED";
+        case SSD_ERR_WORKSPACE: return "SSD_ERR_WORKSPACE";
+        case SSD_ERR_CUDA: return "SSD_ERR_CUDA";
+        case SSD_ERR_TIMEOUT: return "SSD_ERR_TIMEOUT";
+        case SSD_ERR_DEVICE_CHECK: return "SSD_ERR_DEVICE_CHECK";
+        default: return "SSD_ERR_UNKNOWN";
+    }
+}
+
+size_t ssd_fwd_workspace_size(const ssd_params_t* p) {
+    if (check_params(p) != SSD_OK) return 0;
+    const int ns = plan_nsplit(p);
+    return ws_layout(p->batch, p->nheads, p->headdim, p->dstate, ns).total;
+}
+
+int ssd_fwd_plan(const ssd_params_t* p, int has_init, int has_final, int* launches, int* nsplits) {
+    (void)has_init; (void)has_final;
+    if (check_params(p) != SSD_OK) return -1;
+    const int ns = plan_nsplit(p);
+    if (launches) *launches = (ns > 1) ? 3 : 1;
+    if (nsplits) *nsplits = ns;
+    return 0;
+}
+
+int ssd_workspace_init(void* workspace, size_t bytes, void* stream) {
+    if (!workspace || bytes < sizeof(WsHeader)) return SSD_ERR_WORKSPACE;
+    if (cudaMemsetAsync(workspace, 0, sizeof(WsHeader), (cudaStream_t)stream) != cudaSuccess)
+        return SSD_ERR_CUDA;
+    return SSD_OK;
+}
+
+int ssd_check_status(void* workspace, void* stream) {
+    if (!workspace) return SSD_ERR_WORKSPACE;
+    cudaStream_t st = (cudaStream_t)stream;
+    WsHeader h;
+    if (cudaMemcpyAsync(&h, workspace, sizeof(h), cudaMemcpyDeviceToHost, st) != cudaSuccess) return SSD_ERR_CUDA;
+    if (cudaStreamSynchronize(st) != cudaSuccess) return SSD_ERR_CUDA;
+    if (h.status != 0) {
+        if (cudaMemsetAsync(workspace, 0, sizeof(WsHeader), st) != cudaSuccess) return SSD_ERR_CUDA;
+        if (cudaStreamSynchronize(st) != cudaSuccess) return SSD_ERR_CUDA;
+    }
+    return (int)h.status;
+}
+
+int ssd_fwd(const ssd_params_t* p, const void* x, const float* dt, const float* A, const void* B,
+            const void* C, const float* D, const float* init, const int32_t* cu, void* y,
+            float* fin, void* workspace, size_t workspace_bytes, void* stream) {
+    int rc = check_params(p);
+    if (rc != SSD_OK) return rc;
+    if (!x || !dt || !A || !B || !C || !y) return SSD_ERR_INVALID_ARG;
+    if (!aligned(x, 16) || !aligned(B, 16) || !aligned(C, 16) || !aligned(y, 16) || !aligned(dt, 16))
+        return SSD_ERR_INVALID_ARG;
+    if (!aligned(A, 4) || (D && !aligned(D, 4)) || (init && !aligned(init, 16)) || (fin && !aligned(fin, 16)))
+        return SSD_ERR_INVALID_ARG;
+    if ((cu == nullptr) != (p->ndocs == 0)) return SSD_ERR_INVALID_ARG;
+    if (cu && !aligned(cu, 4)) return SSD_ERR_INVALID_ARG;
+    if ((const void*)y == x || (const void*)y == B || (const void*)y == C) return SSD_ERR_INVALID_ARG;
+    const size_t need = ssd_fwd_workspace_size(p);
+    if (!workspace || workspace_bytes < need || !aligned(workspace, 256)) return SSD_ERR_WORKSPACE;
+
+    const int ns = plan_nsplit(p);
+    const WsLayout wl = ws_layout(p->batch, p->nheads, p->headdim, p->dstate, ns);
+    FwdArgs a;
+    memset(&a, 0, sizeof(a));
+    a.batch = p->batch; a.L = p->seqlen;
+    a.H = p->nheads; a.P = p->headdim; a.N = p->dstate; a.G = p->ngroups;
+    a.split_len = plan_split_len(p);
+    a.nsplit = ns;
+    a.dtype = p->dtype;
+    a.x = x; a.dt = dt; a.A = A; a.B = B; a.C = C; a.D = D; a.init = init;
+    a.cu = cu; a.ndocs = p->ndocs;
+    a.y = y; a.fin = fin;
+    a.ws = (WsHeader*)workspace;
+    a.ws_tau = (float*)((char*)workspace + wl.tau_off);
+    a.ws_state = (float*)((char*)workspace + wl.state_off);
+    cudaStream_t st = (cudaStream_t)stream;
+
+    a.Q = simt_chunk(p);
+    if (a.Q == 0) return SSD_ERR_UNSUPPORTED;
+    cudaError_t e;
+    if (ns > 1) {
+        a.mode = kModeAggregate;
+        if ((e = launch_simt(a, st)) != cudaSuccess) return SSD_ERR_CUDA;
+        if ((e = launch_split_scan(a, st)) != cudaSuccess) return SSD_ERR_CUDA;
+    }
+    a.mode = kModeFull;
+    if ((e = launch_simt(a, st)) != cudaSuccess) return SSD_ERR_CUDA;
+    return SSD_OK;
+}
+
+int ssd_segsum_dump(const float* l2, int64_t nrows, int32_t chunk, float* seg, float* L, void* stream) {
+    if (!l2 || nrows < 0 || (chunk != 64 && chunk != 128)) return SSD_ERR_INVALID_ARG;
+    if (nrows == 0) return SSD_OK;
+    if (launch_segsum_dump(l2, nrows, chunk, seg, L, (cudaStream_t)stream) != cudaSuccess) return SSD_ERR_CUDA;
+    return SSD_OK;
+}
+
+}  // extern "C"

@@ -1,0 +1,66 @@
+// Shared definitions of the libssd CUDA sources (sm_103a).
+#pragma once
+#include <cuda_runtime.h>
+#include <cuda_bf16.h>
+#include <stdint.h>
+
+#include "../../include/ssd.h"
+
+namespace ssd {
+
+// Workspace layout: [0, 256) status header, then the split buffers.
+struct WsHeader {
+    uint32_t status;       // first device error recorded (0 = none)
+    uint32_t where;        // kernel-specific code of the failing wait
+    uint32_t pad[62];
+};
+static_assert(sizeof(WsHeader) == 256, "workspace header is 256 bytes");
+
+constexpr float kLog2e = 1.4426950408889634f;
+
+// Record a device-side error once (first writer wins).
+__device__ __forceinline__ void record_error(WsHeader* ws, uint32_t code, uint32_t where) {
+    if (ws && atomicCAS(&ws->status, 0u, code) == 0u) ws->where = where;
+}
+
+template <typename T> struct Elem;
+template <> struct Elem<float> {
+    static __device__ __forceinline__ float load(const float* p) { return *p; }
+    static __device__ __forceinline__ void store(float* p, float v) { *p = v; }
+};
+template <> struct Elem<__nv_bfloat16> {
+    static __device__ __forceinline__ float load(const __nv_bfloat16* p) { return __bfloat162float(*p); }
+    static __device__ __forceinline__ void store(__nv_bfloat16* p, float v) { *p = __float2bfloat16_rn(v); }
+};
+
+// Split plan shared by host and device: splits of `split_len` tokens over
+// each batch row; unit u = ((b * H) + h) * nsplit + s.
+struct SplitPlan {
+    int64_t split_len;
+    int32_t nsplit;
+};
+
+// Offsets (in bytes) of the split buffers inside the workspace.
+struct WsLayout {
+    size_t tau_off;     // float   [batch * H * nsplit]
+    size_t state_off;   // float   [batch * H * nsplit * P * N]  aggregates, then incoming states
+    size_t total;
+};
+
+__host__ __device__ inline size_t align_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
+
+__host__ __device__ inline WsLayout ws_layout(int64_t batch, int H, int P, int N, int nsplit) {
+    WsLayout l;
+    l.tau_off = sizeof(WsHeader);
+    if (nsplit <= 1) {
+        l.state_off = l.tau_off;
+        l.total = sizeof(WsHeader);
+        return l;
+    }
+    size_t units = (size_t)batch * H * nsplit;
+    l.state_off = align_up(l.tau_off + units * sizeof(float), 256);
+    l.total = align_up(l.state_off + units * (size_t)P * N * sizeof(float), 256);
+    return l;
+}
+
+}  // namespace ssd

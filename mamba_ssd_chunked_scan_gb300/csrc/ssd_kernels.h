@@ -1,0 +1,44 @@
+// Host-side declarations shared by the libssd CUDA sources.
+#pragma once
+#include <cuda_runtime.h>
+#include <stddef.h>
+#include <stdint.h>
+
+namespace ssd {
+
+struct WsHeader;
+
+enum { kModeFull = 0, kModeAggregate = 1 };
+
+// Everything one launch of a chunk kernel needs (passed by value).
+struct FwdArgs {
+    int64_t batch, L;
+    int H, P, N, G;
+    int Q;                 // chunk the kernel uses
+    int64_t split_len;     // tokens per split (== L rounded up when one split)
+    int nsplit;
+    int dtype;             // ssd_dtype_t
+    int mode;              // kModeFull or kModeAggregate
+    const void* x;
+    const float* dt;
+    const float* A;
+    const void* B;
+    const void* C;
+    const float* D;
+    const float* init;
+    const int32_t* cu;
+    int ndocs;
+    void* y;
+    float* fin;
+    float* ws_tau;         // [batch * H * nsplit] natural-log split decays
+    float* ws_state;       // [batch * H * nsplit * P * N] split states
+    WsHeader* ws;
+};
+
+size_t simt_smem_bytes(int Q, int P, int N);
+cudaError_t launch_simt(const FwdArgs& a, cudaStream_t st);
+cudaError_t launch_split_scan(const FwdArgs& a, cudaStream_t st);
+cudaError_t launch_segsum_dump(const float* l2, int64_t nrows, int chunk, float* seg, float* L,
+                               cudaStream_t st);
+
+}  // namespace ssd

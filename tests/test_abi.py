@@ -1,0 +1,91 @@
+"""The C ABI without a GPU: the library builds and loads, exports every
+symbol include/ssd.h declares, and rejects bad arguments before launching
+anything (these calls never touch the device)."""
+import ctypes
+import os
+import re
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def L():
+    from mamba_ssd_chunked_scan_gb300 import build
+    build.build()
+    from mamba_ssd_chunked_scan_gb300 import _lib
+    return _lib
+
+
+def declared_symbols():
+    src = open(os.path.join(ROOT, "include", "ssd.h")).read()
+    return re.findall(r"SSD_API\s+[\w\s\*]+?\b(ssd_\w+)\s*\(", src)
+
+
+def test_exports_every_declared_symbol(L):
+    names = declared_symbols()
+    assert len(names) >= 7
+    assert set(names) == set(L.EXPORTS)
+    for n in names:
+        assert hasattr(L.lib, n), n
+
+
+def params(L, **kw):
+    d = dict(batch=8, seqlen=2048, nheads=80, headdim=64, dstate=128, ngroups=1, chunk=128,
+             split_len=0, ndocs=0, dtype=1)
+    d.update(kw)
+    return L.make_params(**d)
+
+
+def test_workspace_size_and_plan(L):
+    p = params(L)
+    assert L.workspace_size(p) == 256          # one split: status header only
+    fam, launches, ns = L.plan(p)
+    assert ns == 1 and launches >= 1
+    p = params(L, batch=1, seqlen=65536, nheads=32, split_len=2048)
+    fam, launches, ns = L.plan(p)
+    assert ns == 32
+    assert L.workspace_size(p) >= 256 + 32 * 32 * (4 + 64 * 128 * 4)
+    # split_len >= seqlen is one split
+    assert L.plan(params(L, batch=1, seqlen=1000, nheads=2, split_len=1024))[2] == 1
+
+
+@pytest.mark.parametrize("kw,code", [
+    (dict(chunk=256), 2), (dict(chunk=0), 1), (dict(chunk=100), 2), (dict(ngroups=3), 1),
+    (dict(split_len=100), 1), (dict(batch=0), 1), (dict(dtype=7), 1), (dict(ndocs=3, batch=2), 1),
+    (dict(headdim=12), 2),
+])
+def test_invalid_params(L, kw, code):
+    p = params(L, **kw)
+    assert L.workspace_size(p) == 0
+    rc = L.lib.ssd_fwd(ctypes.byref(p), *([ctypes.c_void_p(0x1000)] * 10), ctypes.c_void_p(0x1000),
+                       1 << 20, None)
+    assert rc == code
+
+
+def test_invalid_pointers_rejected_before_launch(L):
+    p = params(L, batch=1, seqlen=256, nheads=2)
+    ok = ctypes.c_void_p(0x10000)
+    ws = ctypes.c_void_p(0x20000)
+    args = [ok, ok, ok, ok, ok, None, None, None, ctypes.c_void_p(0x30000), None]
+    def call(a, wsb=4096, w=ws):
+        return L.lib.ssd_fwd(ctypes.byref(p), *a, w, wsb, None)
+    bad = list(args); bad[0] = None                       # x missing
+    assert call(bad) == 1
+    bad = list(args); bad[0] = ctypes.c_void_p(0x10008)   # x not 16-byte aligned
+    assert call(bad) == 1
+    bad = list(args); bad[8] = ok                         # y aliases x
+    assert call(bad) == 1
+    bad = list(args); bad[7] = ok                         # cu_seqlens with ndocs == 0
+    assert call(bad) == 1
+    assert call(args, wsb=100) == 3                       # workspace too small
+    assert call(args, w=None) == 3                        # workspace missing
+    assert L.lib.ssd_segsum_dump(None, 10, 128, None, None, None) == 1
+    assert L.lib.ssd_segsum_dump(ok, 10, 96, None, None, None) == 1
+
+
+def test_status_strings(L):
+    assert L.lib.ssd_status_string(0) == b"SSD_OK"
+    assert L.lib.ssd_status_string(5) == b"SSD_ERR_TIMEOUT"
+    assert L.lib.ssd_status_string(99) == b"SSD_ERR_UNKNOWN"

@@ -1,0 +1,55 @@
+"""Full-size parity on the five SSD workloads, whole output tensors compared
+with the fp64 oracle recurrence (which runs in seconds on the host cores)."""
+import numpy as np
+import pytest
+
+import oracle
+from mamba_ssd_chunked_scan_gb300 import synth
+
+from gpu_helpers import TOL, rel_err, run
+
+pytestmark = [pytest.mark.gpu, pytest.mark.slow]
+
+
+def _check(p, y_o, f_o, split_len=None, want_final=True):
+    y_g, f_g, _ = run(p, want_final=want_final, split_len=split_len)
+    tol = TOL[p.dtype]
+    ey = rel_err(y_g, y_o)
+    assert np.isfinite(y_g).all()
+    assert ey <= tol, f"{p.name} split={split_len}: y err {ey:.3e}"
+    if want_final:
+        ef = rel_err(f_g, f_o)
+        assert ef <= tol, f"{p.name} split={split_len}: final err {ef:.3e}"
+    print(f"{p.name} split={split_len}: err_y={ey:.3e}")
+
+
+def test_config_tiny_fp32():
+    p = synth.config_tiny_f32()
+    y_o, f_o = oracle.ssd_recurrence(p)
+    _check(p, y_o, f_o)
+
+
+def test_config_27b_layer():
+    p = synth.config_27b()
+    y_o, f_o = oracle.ssd_recurrence(p)
+    _check(p, y_o, f_o)
+
+
+@pytest.mark.parametrize("batch,seqlen", synth.SWEEP_POINTS)
+def test_config_sweep(batch, seqlen):
+    p = synth.config_sweep(batch, seqlen)
+    y_o, f_o = oracle.ssd_recurrence(p)
+    for sc in synth.SWEEP_SPLITS:
+        _check(p, y_o, f_o, split_len=128 * sc)
+
+
+def test_config_long_context():
+    p = synth.config_long()
+    y_o, f_o = oracle.ssd_recurrence(p)
+    _check(p, y_o, f_o)
+
+
+def test_config_varlen_stress():
+    p = synth.config_varlen()
+    y_o, f_o = oracle.ssd_recurrence(p)
+    _check(p, y_o, f_o)
