@@ -70,6 +70,8 @@ class SSDForward:
         if nbytes == 0:
             raise _lib.SSDError(1, "invalid SSD parameters")
         self.device = torch.device(device)
+        if self.device.type == "cuda" and self.device.index is None:
+            self.device = torch.device("cuda", torch.cuda.current_device())
         self.workspace = torch.zeros(nbytes, dtype=torch.uint8, device=self.device)
         self.nstates = ndocs if ndocs > 0 else batch
 

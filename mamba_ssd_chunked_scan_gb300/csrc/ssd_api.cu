@@ -66,6 +66,14 @@ int simt_chunk(const ssd_params_t* p) {
     return 0;
 }
 
+// The tcgen05 kernel covers the Mamba-2 head shape in bf16; packed documents
+// with their own initial states go to the SIMT kernel.
+bool use_tc(const ssd_params_t* p, bool has_init) {
+    if (!tc_supported(p->headdim, p->dstate, p->chunk, p->dtype)) return false;
+    if (p->ndocs > 0 && has_init) return false;
+    return true;
+}
+
 }  // namespace
 
 extern "C" {
@@ -90,12 +98,12 @@ size_t ssd_fwd_workspace_size(const ssd_params_t* p) {
 }
 
 int ssd_fwd_plan(const ssd_params_t* p, int has_init, int has_final, int* launches, int* nsplits) {
-    (void)has_init; (void)has_final;
+    (void)has_final;
     if (check_params(p) != SSD_OK) return -1;
     const int ns = plan_nsplit(p);
     if (launches) *launches = (ns > 1) ? 3 : 1;
     if (nsplits) *nsplits = ns;
-    return 0;
+    return use_tc(p, has_init != 0) ? 1 : 0;
 }
 
 int ssd_workspace_init(void* workspace, size_t bytes, void* stream) {
@@ -151,16 +159,17 @@ int ssd_fwd(const ssd_params_t* p, const void* x, const float* dt, const float* 
     a.ws_state = (float*)((char*)workspace + wl.state_off);
     cudaStream_t st = (cudaStream_t)stream;
 
-    a.Q = simt_chunk(p);
+    const bool tc = use_tc(p, init != nullptr);
+    a.Q = tc ? p->chunk : simt_chunk(p);
     if (a.Q == 0) return SSD_ERR_UNSUPPORTED;
-    cudaError_t e;
+    auto launch = [&](const FwdArgs& aa) { return tc ? launch_tc(aa, st) : launch_simt(aa, st); };
     if (ns > 1) {
         a.mode = kModeAggregate;
-        if ((e = launch_simt(a, st)) != cudaSuccess) return SSD_ERR_CUDA;
-        if ((e = launch_split_scan(a, st)) != cudaSuccess) return SSD_ERR_CUDA;
+        if (launch(a) != cudaSuccess) return SSD_ERR_CUDA;
+        if (launch_split_scan(a, st) != cudaSuccess) return SSD_ERR_CUDA;
     }
     a.mode = kModeFull;
-    if ((e = launch_simt(a, st)) != cudaSuccess) return SSD_ERR_CUDA;
+    if (launch(a) != cudaSuccess) return SSD_ERR_CUDA;
     return SSD_OK;
 }
 

@@ -38,6 +38,9 @@ struct FwdArgs {
 size_t simt_smem_bytes(int Q, int P, int N);
 cudaError_t launch_simt(const FwdArgs& a, cudaStream_t st);
 cudaError_t launch_split_scan(const FwdArgs& a, cudaStream_t st);
+size_t tc_smem_bytes();
+bool tc_supported(int P, int N, int Q, int dtype);
+cudaError_t launch_tc(const FwdArgs& a, cudaStream_t st);
 cudaError_t launch_segsum_dump(const float* l2, int64_t nrows, int chunk, float* seg, float* L,
                                cudaStream_t st);
 

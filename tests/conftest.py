@@ -20,6 +20,9 @@ def pytest_collection_modifyitems(config, items):
     except Exception:  # pragma: no cover
         have_gpu = False
     if have_gpu:
+        if any("gpu" in it.keywords for it in items):
+            from mamba_ssd_chunked_scan_gb300 import build
+            build.build()
         return
     skip = pytest.mark.skip(reason="no CUDA device")
     for it in items:

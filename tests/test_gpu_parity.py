@@ -124,3 +124,12 @@ def test_deterministic():
     y1, f1, _ = run(p, split_len=256)
     y2, f2, _ = run(p, split_len=256)
     assert np.array_equal(y1, y2) and np.array_equal(f1, f2)
+
+
+def test_mamba2_shape_uses_tensor_core_kernel():
+    import mamba_ssd_chunked_scan_gb300 as ssd
+    f = ssd.SSDForward(2, 256, 4, 64, 128, 2, 128, 0, 0)
+    fam, launches, ns = f.plan()
+    assert fam == 1 and launches == 1 and ns == 1
+    f32 = ssd.SSDForward(2, 256, 4, 16, 16, 2, 64, 0, 0, dtype=__import__("torch").float32)
+    assert f32.plan()[0] == 0
