@@ -24,6 +24,7 @@
 #include <cuda.h>
 #include <cudaTypedefs.h>
 #include <cuda_bf16.h>
+#include <stddef.h>
 
 #include "ssd_common.cuh"
 #include "segsum.cuh"
@@ -51,9 +52,9 @@ enum : uint32_t { kWhereEmpty = 1, kWhereFullMma = 2, kWhereBarM = 3, kWhereFull
 
 struct TcSmall {
     SegsumShared<4> seg;
-    float dtv[Q];
-    float colfac[Q];
-    float wv[Q];
+    alignas(16) float dtv[Q];      // read as float4
+    alignas(16) float colfac[Q];   // read as float4
+    alignas(16) float wv[Q];
     float pexp_e;
     int rowflag[Q];     // bit0: a document starts at this token, bit1: a document ends here
     int rowdoc[Q];      // state index (document, or batch row) of this token
@@ -63,6 +64,11 @@ struct TcSmall {
     int abort;
     int never;          // stays 0: lets drain waits ignore the abort flag
 };
+
+static_assert(offsetof(TcSmall, dtv) % 16 == 0 && offsetof(TcSmall, colfac) % 16 == 0,
+              "vector-loaded arrays must be 16-byte aligned");
+static_assert(offsetof(TcSmall, full) % 8 == 0, "mbarriers are 8-byte aligned");
+static_assert(kTiles % 1024 == 0, "swizzled tiles start on 1024-byte boundaries");
 
 struct TcParams {
     CUtensorMap tm_x, tm_B, tm_C, tm_y;
