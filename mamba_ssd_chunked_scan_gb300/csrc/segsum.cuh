@@ -38,7 +38,7 @@ namespace ssd {
 
 template <int NW>
 struct SegsumShared {
-    float ell[32 * NW];    // input: log2-domain log-decays of the chunk
+    alignas(16) float ell[32 * NW];    // input: log2-domain log-decays of the chunk
     float colS[32 * NW];   // seg(end of j's block, j)
     float tot[NW];         // block totals
     float rlast[NW];       // R[r] of the chunk's last row, r < NW - 1
@@ -64,17 +64,28 @@ __device__ __forceinline__ float ex2_approx(float v) {
 template <int NW>
 __device__ __forceinline__ void segsum_phase1(SegsumShared<NW>& sh, SegsumRow<NW>& row, int w,
                                               int lane) {
+    // the block's log-decays, read once (broadcast) into registers
+    float e[32];
+    const float4* src = reinterpret_cast<const float4*>(sh.ell + 32 * w);
+#pragma unroll
+    for (int q = 0; q < 8; ++q) {
+        const float4 v = src[q];
+        e[4 * q] = v.x;
+        e[4 * q + 1] = v.y;
+        e[4 * q + 2] = v.z;
+        e[4 * q + 3] = v.w;
+    }
     float r = 0.f;
     row.d[31] = 0.f;
 #pragma unroll
     for (int c = 30; c >= 0; --c) {
-        if (c < lane) r += sh.ell[32 * w + c + 1];
+        if (c < lane) r += e[c + 1];
         row.d[c] = r;
     }
     if (lane == 31) {
 #pragma unroll
         for (int c = 0; c < 32; ++c) sh.colS[32 * w + c] = row.d[c];
-        sh.tot[w] = row.d[0] + sh.ell[32 * w];
+        sh.tot[w] = row.d[0] + e[0];
     }
 }
 

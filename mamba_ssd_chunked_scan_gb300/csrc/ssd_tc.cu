@@ -9,23 +9,24 @@
 // recurrent, state resident on chip).  Per chunk c:
 //
 //   G     = C B^T                        (UMMA 128x128x128 -> TMEM)
-//   M     = G o L o dt                   (hierarchy-aware segsum mask, bf16 -> TMEM)
+//   M     = G o L o dt + D I             (hierarchy-aware segsum mask, bf16,
+//                                         written over G in TMEM; the skip
+//                                         term D x rides on the diagonal)
 //   Ydiag = M X                          (UMMA, A operand from TMEM)
 //   dS    = B^T (exp(s_j) dt_j x_j)      (UMMA, chunk state summary)
 //   Yoff  = C S_in^T                     (UMMA; the row decay exp(p_i) is applied in the epilogue)
 //   S     = exp(tau) S + dS              (state carried in registers)
-//   y     = Ydiag + exp(p_i) Yoff + D x  (epilogue, TMA store)
+//   y     = Ydiag + exp(p_i) Yoff        (epilogue, stored from registers)
 //
-// Warp roles (320 threads):
-//   warp 0      TMA producer (two-stage ring of C, B, X tiles)
-//   warp 1      TMEM owner and MMA issuer
-//   warps 2-5   mask group: log-decays, segsum, scaled X tile, mask M
-//   warps 6-9   state group: state update, incoming-state tile, epilogue
-// One thread of each math group owns one chunk row (= TMEM lane).  The MMA
-// issue order G(c), Ydiag(c), dS(c), G(c+1), Yoff(c) keeps the tensor pipe
-// fed while the state group closes the state recurrence of chunk c; the Y
-// accumulators are double-buffered in TMEM so the epilogue of chunk c
-// overlaps the products of chunk c+1.
+// Warpgroups (512 threads; register budgets rebalanced with setmaxnreg):
+//   WG0  warp 0: TMA producer; warp 1: issues Ydiag and dS; warp 2: issues G
+//   WG1  mask group for even chunks, WG2 mask group for odd chunks:
+//        log-decays, segsum, scaled X tile, mask M, and the chunk's epilogue
+//   WG3  state group: state update, incoming-state tile, issues Yoff
+// Chunk c uses input stage, G/M buffer and scaled-X buffer c & 1, so the two
+// mask groups work on consecutive chunks concurrently; the only serial
+// dependency, the state recurrence, is a short loop through the state group.
+// One thread of each math group owns one chunk row (= TMEM lane).
 //
 // Every wait is bounded; a wait that runs out records SSD_ERR_TIMEOUT in the
 // workspace status word, and the CTA drains its copies, frees TMEM and exits.
@@ -43,27 +44,28 @@ namespace ssd {
 namespace {
 
 constexpr int Q = 128, P = 64, N = 128;
-constexpr int NS = 2;                        // input stages
-constexpr int kThreads = 320;
+constexpr int NMETA = 3;                     // per-chunk value buffers between the math groups
+constexpr int kThreads = 512;
+constexpr int kRegsIssue = 56, kRegsMath = 152;   // 128 * (56 + 3 * 152) = 65536 = 512 * 128
+static_assert(128 * (kRegsIssue + 3 * kRegsMath) == kThreads * 128, "register split must equal the launch total");
 constexpr uint32_t kTileC = 0, kTileB = 32768, kTileX = 65536, kStageBytes = 81920;
-constexpr uint32_t kXt = NS * kStageBytes;   // scaled X for the state summary
-constexpr uint32_t kSin = kXt + 16384;       // incoming state, bf16, (n rows, p)
-constexpr uint32_t kYs = kSin + 16384;       // y staging for the TMA store
-constexpr uint32_t kTiles = kYs + 16384;
-// TMEM columns: G | M (bf16 pairs) | dS | Ydiag[2] | Yoff[2]
-constexpr uint32_t kTmG = 0, kTmM = 128, kTmDS = 192, kTmYd = 256, kTmYo = 384, kTmCols = 512;
+constexpr uint32_t kXt = 2 * kStageBytes;    // scaled X for the state summary, two buffers
+constexpr uint32_t kSin = kXt + 2 * 16384;   // incoming state, bf16, (n rows, p)
+constexpr uint32_t kTiles = kSin + 16384;
+// TMEM columns: G/M/Ydiag [2] (G, then M in cols 0-63 and Ydiag in 64-127) | Yoff [2] | dS
+constexpr uint32_t kTmGM = 0, kTmYo = 256, kTmDS = 384, kTmCols = 512;
 constexpr uint64_t kWaitNs = 2000000000ull;  // 2 s: far beyond any legitimate wait
 constexpr float kLn2 = 0.6931471805599453f;
-constexpr int kBarMask = 1, kBarState = 2;   // named barriers of the two math groups
+constexpr int kBarMask0 = 1, kBarState = 3;  // named barriers: mask groups 1 and 2, state group 3
 
 // codes of the wait that gave up (WsHeader::where)
 enum : uint32_t {
-    kWhereEmpty = 1, kWhereFull = 2, kWhereBarM = 3, kWhereYFree = 4, kWhereDsFree = 5, kWhereBarS = 6,
+    kWhereEmpty = 1, kWhereFull = 2, kWhereBarM = 3, kWhereYFree = 4, kWhereDsFree = 5,
     kWhereMetaFree = 7, kWhereBarDS = 8, kWhereBarG = 9, kWhereMetaFull = 10, kWhereBarY = 11,
-    kWhereDrain = 12
+    kWhereDrain = 12, kWhereBarYd = 13
 };
 
-// Per-chunk values handed from the mask group to the state group.
+// Per-chunk values handed from a mask group to the state group.
 struct ChunkMeta {
     alignas(16) float pexp[Q];   // 2^{p_i}: decay of the incoming state at row i
     alignas(16) float ell[Q];    // log2-decays
@@ -73,29 +75,40 @@ struct ChunkMeta {
     float tau;                   // whole-chunk log2-decay
 };
 
-struct TcSmall {
+// Scratch of one mask group.
+struct MaskScratch {
     SegsumShared<4> seg;
     alignas(16) float dtv[Q];      // read as float4
     alignas(16) float colfac[Q];   // read as float4
-    alignas(16) float wv[Q];
-    ChunkMeta meta[2];
     int doc_cursor;
-    uint64_t full[NS], empty[NS];
-    uint64_t barG, barM, barDS, barS, barY, dsFree, barDrain;
-    uint64_t yFree[2], metaFull[2], metaFree[2];
+};
+
+struct TcSmall {
+    MaskScratch mask[2];
+    ChunkMeta meta[NMETA];
+    alignas(16) float wv[Q];
+    uint64_t full[2], empty[2];
+    uint64_t barG[2], barM[2], barYd[2], barDS[2], barY[2], yFree[2];
+    uint64_t dsFree;
+    uint64_t metaFull[NMETA], metaFree[NMETA];
+    uint64_t drain[3];
     uint32_t tmem_base;
     int abort;
     int never;                     // stays 0: lets drain waits ignore the abort flag
 };
 
-static_assert(offsetof(TcSmall, dtv) % 16 == 0 && offsetof(TcSmall, colfac) % 16 == 0,
+static_assert(offsetof(MaskScratch, seg) == 0 && sizeof(MaskScratch) % 16 == 0, "segsum inputs are read as float4");
+static_assert(offsetof(MaskScratch, dtv) % 16 == 0 && offsetof(MaskScratch, colfac) % 16 == 0,
               "vector-loaded arrays must be 16-byte aligned");
 static_assert(offsetof(TcSmall, meta) % 16 == 0 && sizeof(ChunkMeta) % 16 == 0, "meta alignment");
 static_assert(offsetof(TcSmall, full) % 8 == 0, "mbarriers are 8-byte aligned");
 static_assert(kTiles % 1024 == 0, "swizzled tiles start on 1024-byte boundaries");
 
+constexpr size_t kSmemBytes = 1024 + kTiles + sizeof(TcSmall);
+static_assert(kSmemBytes <= 227 * 1024, "shared memory per CTA");
+
 struct TcParams {
-    CUtensorMap tm_x, tm_B, tm_C, tm_y;
+    CUtensorMap tm_x, tm_B, tm_C;
     FwdArgs a;
 };
 
@@ -184,6 +197,7 @@ __global__ void __launch_bounds__(kThreads, 1) ssd_chunk_tc(const __grid_constan
     TcSmall& sh = *reinterpret_cast<TcSmall*>(sm + kTiles);
     const FwdArgs& a = prm.a;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int wg = warp >> 2;
     const bool full_mode = (a.mode == kModeFull);
 
     // unit: heads of one (row, split) are adjacent so they share B / C in L2
@@ -198,32 +212,34 @@ __global__ void __launch_bounds__(kThreads, 1) ssd_chunk_tc(const __grid_constan
     const int nch = (int)((t1 - t0 + Q - 1) / Q);
 
     if (threadIdx.x == 0) {
-        for (int i = 0; i < NS; ++i) {
-            ptx::mbar_init(&sh.full[i], 1);
-            ptx::mbar_init(&sh.empty[i], 3);   // MMA commit + mask group + state group
-        }
-        ptx::mbar_init(&sh.barG, 1);
-        ptx::mbar_init(&sh.barM, 4);
-        ptx::mbar_init(&sh.barDS, 1);
-        ptx::mbar_init(&sh.barS, 4);
-        ptx::mbar_init(&sh.barY, 1);
-        ptx::mbar_init(&sh.dsFree, 4);
-        ptx::mbar_init(&sh.barDrain, 1);
         for (int i = 0; i < 2; ++i) {
+            ptx::mbar_init(&sh.full[i], 1);
+            // stage readers: dS issuer, mask group, state group (+ Yoff issuer)
+            ptx::mbar_init(&sh.empty[i], full_mode ? 4 : 3);
+            ptx::mbar_init(&sh.barG[i], 1);
+            ptx::mbar_init(&sh.barM[i], 4);
+            ptx::mbar_init(&sh.barYd[i], 1);
+            ptx::mbar_init(&sh.barDS[i], 1);
+            ptx::mbar_init(&sh.barY[i], 1);
             ptx::mbar_init(&sh.yFree[i], 4);
+        }
+        ptx::mbar_init(&sh.dsFree, 4);
+        for (int i = 0; i < NMETA; ++i) {
             ptx::mbar_init(&sh.metaFull[i], 4);
             ptx::mbar_init(&sh.metaFree[i], 1);
         }
+        for (int i = 0; i < 3; ++i) ptx::mbar_init(&sh.drain[i], 1);
         sh.abort = 0;
         sh.never = 0;
-        sh.doc_cursor = a.cu ? find_doc_tc(a.cu, a.ndocs, t0) : 0;
+        const int dc = a.cu ? find_doc_tc(a.cu, a.ndocs, t0) : 0;
+        sh.mask[0].doc_cursor = dc;
+        sh.mask[1].doc_cursor = dc;
         ptx::mbar_fence_init();
     }
     if (warp == 0 && lane == 0) {
         ptx::prefetch_tmap(&prm.tm_x);
         ptx::prefetch_tmap(&prm.tm_B);
         ptx::prefetch_tmap(&prm.tm_C);
-        ptx::prefetch_tmap(&prm.tm_y);
     }
     if (warp == 1) ptx::tmem_alloc(&sh.tmem_base, kTmCols);
     ptx::tc_fence_before();
@@ -231,13 +247,14 @@ __global__ void __launch_bounds__(kThreads, 1) ssd_chunk_tc(const __grid_constan
     ptx::tc_fence_after();
     const uint32_t tb = sh.tmem_base;
 
-    if (warp == 0) {
-        // ================================================================ TMA producer
-        if (lane == 0) {
+    if (wg == 0) {
+        ptx::regs_dec<kRegsIssue>();
+        if (warp == 0 && lane == 0) {
+            // ============================================================ TMA producer
             int issued = 0;
             for (int c = 0; c < nch; ++c) {
-                const int st = c % NS, k = c / NS;
-                if (c >= NS && !wait_or_fail(sh, a, &sh.empty[st], (k - 1) & 1, kWhereEmpty)) break;
+                const int st = c & 1;
+                if (c >= 2 && !wait_or_fail(sh, a, &sh.empty[st], ((c >> 1) - 1) & 1, kWhereEmpty)) break;
                 const int t = (int)(t0 + (int64_t)c * Q);
                 uint8_t* stg = sm + st * kStageBytes;
                 ptx::mbar_expect_tx(&sh.full[st], full_mode ? 81920u : 49152u);
@@ -251,108 +268,87 @@ __global__ void __launch_bounds__(kThreads, 1) ssd_chunk_tc(const __grid_constan
                 ++issued;
             }
             // drain: the last load issued into each stage has landed
-            for (int st = 0; st < NS && st < issued; ++st) {
-                const int last = ((issued - 1 - st) / NS) * NS + st;
-                if (!ptx::mbar_wait(&sh.full[st], (last / NS) & 1, &sh.never, kWaitNs)) fail(sh, a, kWhereDrain);
+            for (int st = 0; st < 2 && st < issued; ++st) {
+                const int last = ((issued - 1 - st) >> 1) * 2 + st;
+                if (!ptx::mbar_wait(&sh.full[st], (last >> 1) & 1, &sh.never, kWaitNs)) fail(sh, a, kWhereDrain);
             }
-        }
-    } else if (warp == 1) {
-        // ================================================================ MMA issuer
-        if (lane == 0) {
-            constexpr uint32_t idG = ptx::idesc_bf16(128, 128, 0, 0);
+        } else if (warp == 1 && lane == 0) {
+            // ============================================================ Ydiag / dS issuer
             constexpr uint32_t idYd = ptx::idesc_bf16(128, 64, 0, 1);
-            constexpr uint32_t idYo = ptx::idesc_bf16(128, 64, 0, 1);
             constexpr uint32_t idDS = ptx::idesc_bf16(128, 64, 1, 1);
-            const uint32_t xt = ptx::smem_u32(sm + kXt), sin = ptx::smem_u32(sm + kSin);
-            auto stage = [&](int c) { return ptx::smem_u32(sm + (c % NS) * kStageBytes); };
-            auto issue_G = [&](int c) {
-                const uint32_t stg = stage(c);
-#pragma unroll
-                for (int kk = 0; kk < 8; ++kk)
-                    ptx::mma_ss(tb + kTmG, desc_k(stg + kTileC, kk), desc_k(stg + kTileB, kk), idG, kk > 0);
-                ptx::mma_commit(&sh.barG);
-            };
-            bool ok = true;
-            if (nch > 0 && full_mode) {
-                ok = wait_or_fail(sh, a, &sh.full[0], 0, kWhereFull);
-                ptx::tc_fence_after();
-                if (ok) issue_G(0);
-            }
-            for (int c = 0; ok && c < nch; ++c) {
-                const int st = c % NS;
-                const uint32_t stg = stage(c);
-                if (!full_mode && !wait_or_fail(sh, a, &sh.full[st], (c / NS) & 1, kWhereFull)) break;
-                if (!wait_or_fail(sh, a, &sh.barM, c & 1, kWhereBarM)) break;
+            for (int c = 0; c < nch; ++c) {
+                const int X = c & 1, j = c >> 1;
+                const uint32_t stg = ptx::smem_u32(sm + X * kStageBytes);
+                if (!wait_or_fail(sh, a, &sh.barM[X], j & 1, kWhereBarM)) break;
                 ptx::tc_fence_after();
                 if (full_mode) {
-                    if (c >= 2 && !wait_or_fail(sh, a, &sh.yFree[c & 1], ((c >> 1) - 1) & 1, kWhereYFree)) break;
-                    ptx::tc_fence_after();
+                    const uint32_t gm = tb + kTmGM + 128 * X;
 #pragma unroll
                     for (int kk = 0; kk < 8; ++kk)
-                        ptx::mma_ts(tb + kTmYd + 64 * (c & 1), tb + kTmM + 8 * kk, desc_mn1(stg + kTileX, kk), idYd,
-                                    kk > 0);
+                        ptx::mma_ts(gm + 64, gm + 8 * kk, desc_mn1(stg + kTileX, kk), idYd, kk > 0);
+                    ptx::mma_commit(&sh.barYd[X]);
                 }
                 if (c >= 1 && !wait_or_fail(sh, a, &sh.dsFree, (c - 1) & 1, kWhereDsFree)) break;
                 ptx::tc_fence_after();
+                const uint32_t xt = ptx::smem_u32(sm + kXt + 16384 * X);
 #pragma unroll
                 for (int kk = 0; kk < 8; ++kk)
                     ptx::mma_ss(tb + kTmDS, desc_mn2(stg + kTileB, kk), desc_mn1(xt, kk), idDS, kk > 0);
-                ptx::mma_commit(&sh.barDS);
-                if (full_mode) {
-                    if (c + 1 < nch) {
-                        if (!wait_or_fail(sh, a, &sh.full[(c + 1) % NS], ((c + 1) / NS) & 1, kWhereFull)) break;
-                        ptx::tc_fence_after();
-                        issue_G(c + 1);
-                    }
-                    if (!wait_or_fail(sh, a, &sh.barS, c & 1, kWhereBarS)) break;
-                    ptx::tc_fence_after();
-#pragma unroll
-                    for (int kk = 0; kk < 8; ++kk)
-                        ptx::mma_ss(tb + kTmYo + 64 * (c & 1), desc_k(stg + kTileC, kk), desc_mn1(sin, kk), idYo,
-                                    kk > 0);
-                    ptx::mma_commit(&sh.barY);
-                }
-                ptx::mma_commit(&sh.empty[st]);
+                ptx::mma_commit(&sh.barDS[X]);
+                ptx::mma_commit(&sh.empty[X]);
             }
-            // drain: every MMA issued so far has completed
-            ptx::mma_commit(&sh.barDrain);
-            if (!ptx::mbar_wait(&sh.barDrain, 0, &sh.never, kWaitNs)) fail(sh, a, kWhereDrain);
+            ptx::mma_commit(&sh.drain[0]);
+            if (!ptx::mbar_wait(&sh.drain[0], 0, &sh.never, kWaitNs)) fail(sh, a, kWhereDrain);
+        } else if (warp == 2 && lane == 0 && full_mode) {
+            // ============================================================ G issuer
+            constexpr uint32_t idG = ptx::idesc_bf16(128, 128, 0, 0);
+            for (int c = 0; c < nch; ++c) {
+                const int X = c & 1, j = c >> 1;
+                const uint32_t stg = ptx::smem_u32(sm + X * kStageBytes);
+                if (!wait_or_fail(sh, a, &sh.full[X], j & 1, kWhereFull)) break;
+                // G/M buffer X is free once the epilogue of chunk c-2 has read its Ydiag
+                if (j >= 1 && !wait_or_fail(sh, a, &sh.yFree[X], (j - 1) & 1, kWhereYFree)) break;
+                ptx::tc_fence_after();
+                const uint32_t d = tb + kTmGM + 128 * X;
+#pragma unroll
+                for (int kk = 0; kk < 8; ++kk)
+                    ptx::mma_ss(d, desc_k(stg + kTileC, kk), desc_k(stg + kTileB, kk), idG, kk > 0);
+                ptx::mma_commit(&sh.barG[X]);
+            }
+            ptx::mma_commit(&sh.drain[1]);
+            if (!ptx::mbar_wait(&sh.drain[1], 0, &sh.never, kWaitNs)) fail(sh, a, kWhereDrain);
         }
-    } else if (warp < 6) {
-        // ================================================================ mask group
-        const int mt = threadIdx.x - 64;          // 0..127
+    } else if (wg <= 2) {
+        // ================================================================ mask groups
+        ptx::regs_inc<kRegsMath>();
+        const int X = wg - 1;                     // this group takes chunks c with c & 1 == X
+        const int nb = kBarMask0 + X;
+        MaskScratch& ms = sh.mask[X];
+        const int mt = threadIdx.x - 128 * wg;    // 0..127
         const int rb = warp & 3;                  // TMEM lane quarter = row block
         const int i = 32 * rb + lane;             // chunk row = TMEM lane
         const uint32_t lane_addr = tb + ((uint32_t)(32 * rb) << 16);
         const float A2 = a.A[h] * kLog2e;
-        if (full_mode) {
-            // the mask above the diagonal blocks is zero in every chunk: write it once
-            uint32_t z[16];
-#pragma unroll
-            for (int q = 0; q < 16; ++q) z[q] = 0u;
-#pragma unroll
-            for (int r = 1; r < 4; ++r)
-                if (r > rb) ptx::tmem_st16(lane_addr + kTmM + 16 * r, z);
-            ptx::tmem_st_wait();
-        }
+        const float Dh = a.D ? a.D[h] : 0.f;
+        __nv_bfloat16* yg = (__nv_bfloat16*)a.y;
         auto load_dt = [&](int c) -> float {
             const int64_t t = t0 + (int64_t)c * Q;
             return (c < nch && t + i < t1) ? __ldg(a.dt + ((size_t)b * a.L + t + i) * a.H + h) : 0.f;
         };
-        float dt_next = load_dt(0);
-        for (int c = 0; c < nch; ++c) {
-            const int st = c % NS, k = c / NS, mb = c & 1;
-            uint8_t* stg = sm + st * kStageBytes;
+        float dt_next = load_dt(X);
+        for (int c = X; c < nch; c += 2) {
+            const int j = c >> 1, mb = c % NMETA;
+            uint8_t* stg = sm + X * kStageBytes;
             const int64_t t = t0 + (int64_t)c * Q;
             const int nv = (int)((t + Q < t1) ? Q : t1 - t);
             const float dti = dt_next;
-            dt_next = load_dt(c + 1);
-            if (c >= 2) wait_or_fail(sh, a, &sh.metaFree[mb], ((c >> 1) - 1) & 1, kWhereMetaFree);
-            // document boundaries: walk forward from the chunk's first document
+            dt_next = load_dt(c + 2);
+            if (c >= NMETA) wait_or_fail(sh, a, &sh.metaFree[mb], ((c / NMETA) - 1) & 1, kWhereMetaFree);
+            // document boundaries: walk forward from this group's cursor
             int flag = 0, doc = (int)b;
             if (i < nv) {
                 if (a.cu) {
-                    int d = sh.doc_cursor;
+                    int d = ms.doc_cursor;
                     while (d + 1 < a.ndocs && __ldg(a.cu + d + 1) <= t + i) ++d;
                     doc = d;
                     if (d > 0 && __ldg(a.cu + d) == t + i) flag |= 1;
@@ -363,31 +359,32 @@ __global__ void __launch_bounds__(kThreads, 1) ssd_chunk_tc(const __grid_constan
             }
             const float l2 = (flag & 1) ? -INFINITY : dti * A2;
             ChunkMeta& m = sh.meta[mb];
-            sh.seg.ell[i] = l2;
-            sh.dtv[i] = dti;
+            ms.seg.ell[i] = l2;
+            ms.dtv[i] = dti;
             m.ell[i] = l2;
             m.dtv[i] = dti;
             m.rowflag[i] = flag;
             m.rowdoc[i] = doc;
-            ptx::named_bar(kBarMask, 128);
-            if (mt == Q - 1 && a.cu) sh.doc_cursor = doc;   // the next chunk starts in (or after) this document
+            ptx::named_bar(nb, 128);
+            if (mt == Q - 1 && a.cu) ms.doc_cursor = doc;   // later chunks start in (or after) this document
             SegsumRow<4> row;
-            segsum_phase1<4>(sh.seg, row, rb, lane);
-            ptx::named_bar(kBarMask, 128);
-            segsum_phase2<4>(sh.seg, row, rb, lane);
-            ptx::named_bar(kBarMask, 128);
-            sh.colfac[i] = ex2_approx(sh.seg.colS[i]) * dti;
-            const float xf = ex2_approx(segsum_chunk_suffix<4>(sh.seg, i)) * dti;
-            m.pexp[i] = ex2_approx(row.p);
-            if (mt == 0) m.tau = sh.seg.tau;
+            segsum_phase1<4>(ms.seg, row, rb, lane);
+            ptx::named_bar(nb, 128);
+            segsum_phase2<4>(ms.seg, row, rb, lane);
+            ptx::named_bar(nb, 128);
+            ms.colfac[i] = ex2_approx(ms.seg.colS[i]) * dti;
+            const float xf = ex2_approx(segsum_chunk_suffix<4>(ms.seg, i)) * dti;
+            const float pe = ex2_approx(row.p);
+            m.pexp[i] = pe;
+            if (mt == 0) m.tau = ms.seg.tau;
             __syncwarp();
             if (lane == 0) ptx::mbar_arrive(&sh.metaFull[mb]);
-            // scaled X (state-summary operand); its buffer and M's are free once dS(c-1) is done
-            wait_or_fail(sh, a, &sh.full[st], k & 1, kWhereFull);
-            if (c >= 1) wait_or_fail(sh, a, &sh.barDS, (c - 1) & 1, kWhereBarDS);
+            // scaled X (state-summary operand): buffer X is free once dS(c-2) is done
+            wait_or_fail(sh, a, &sh.full[X], j & 1, kWhereFull);
+            if (j >= 1) wait_or_fail(sh, a, &sh.barDS[X], (j - 1) & 1, kWhereBarDS);
             {
                 const uint8_t* xrow = stg + kTileX;
-                uint8_t* xt = sm + kXt;
+                uint8_t* xt = sm + kXt + 16384 * X;
 #pragma unroll
                 for (int q = 0; q < 8; ++q) {
                     const uint4 v = *reinterpret_cast<const uint4*>(xrow + sw128_off(i, 8 * q));
@@ -400,19 +397,21 @@ __global__ void __launch_bounds__(kThreads, 1) ssd_chunk_tc(const __grid_constan
                 }
                 ptx::fence_proxy_async();
             }
-            ptx::named_bar(kBarMask, 128);        // colfac complete; X tile reads done
-            if (mt == 0) ptx::mbar_arrive(&sh.empty[st]);
+            ptx::named_bar(nb, 128);              // colfac complete; X tile reads done
+            if (mt == 0) ptx::mbar_arrive(&sh.empty[X]);
             if (full_mode) {
-                wait_or_fail(sh, a, &sh.barG, c & 1, kWhereBarG);
+                // M is written over G (block r of M occupies G columns already consumed)
+                wait_or_fail(sh, a, &sh.barG[X], j & 1, kWhereBarG);
                 ptx::tc_fence_after();
+                const uint32_t gm = lane_addr + kTmGM + 128 * X;
                 // rank-one off-diagonal blocks r < rb: row factor x column factor
 #pragma unroll 1
                 for (int r = 0; r < rb; ++r) {
                     uint32_t gr[32];
-                    ptx::tmem_ld32(lane_addr + kTmG + 32 * r, gr);
+                    ptx::tmem_ld32(gm + 32 * r, gr);
                     const float Rr = (r == 0) ? row.R[0] : (r == 1) ? row.R[1] : row.R[2];
                     const float rf = ex2_approx(Rr);
-                    const float4* cf = reinterpret_cast<const float4*>(sh.colfac + 32 * r);
+                    const float4* cf = reinterpret_cast<const float4*>(ms.colfac + 32 * r);
                     ptx::tmem_ld_wait();
                     uint32_t pk[16];
 #pragma unroll
@@ -423,45 +422,83 @@ __global__ void __launch_bounds__(kThreads, 1) ssd_chunk_tc(const __grid_constan
                         pk[2 * q + 1] = pack_bf16(__uint_as_float(gr[4 * q + 2]) * rf * f.z,
                                                   __uint_as_float(gr[4 * q + 3]) * rf * f.w);
                     }
-                    ptx::tmem_st16(lane_addr + kTmM + 16 * r, pk);
+                    ptx::tmem_st16(gm + 16 * r, pk);
                 }
-                // 1-SS diagonal block rb: running sums from the diagonal
+                // 1-SS diagonal block rb (running sums from the diagonal), plus D on the diagonal
                 {
                     uint32_t gr[32];
-                    ptx::tmem_ld32(lane_addr + kTmG + 32 * rb, gr);
-                    const float4* dv = reinterpret_cast<const float4*>(sh.dtv + 32 * rb);
+                    ptx::tmem_ld32(gm + 32 * rb, gr);
+                    const float4* dv = reinterpret_cast<const float4*>(ms.dtv + 32 * rb);
                     ptx::tmem_ld_wait();
                     uint32_t pk[16];
 #pragma unroll
                     for (int q = 0; q < 8; ++q) {
                         const float4 f = dv[q];
-                        // every term computed, then masked: no divergent branches
+                        const float fv[4] = {f.x, f.y, f.z, f.w};
                         float mm[4];
 #pragma unroll
                         for (int e = 0; e < 4; ++e) {
-                            const float v = __uint_as_float(gr[4 * q + e]) * ex2_approx(row.d[4 * q + e]);
-                            mm[e] = (4 * q + e <= lane) ? v : 0.f;
+                            // every term computed, then masked: no divergent branches
+                            const int col = 4 * q + e;
+                            const float v = __uint_as_float(gr[col]) * ex2_approx(row.d[col]);
+                            mm[e] = ((col <= lane) ? v : 0.f) * fv[e] + ((col == lane) ? Dh : 0.f);
                         }
-                        const float m0 = mm[0] * f.x, m1 = mm[1] * f.y, m2 = mm[2] * f.z, m3 = mm[3] * f.w;
-                        pk[2 * q] = pack_bf16(m0, m1);
-                        pk[2 * q + 1] = pack_bf16(m2, m3);
+                        pk[2 * q] = pack_bf16(mm[0], mm[1]);
+                        pk[2 * q + 1] = pack_bf16(mm[2], mm[3]);
                     }
-                    ptx::tmem_st16(lane_addr + kTmM + 16 * rb, pk);
+                    ptx::tmem_st16(gm + 16 * rb, pk);
+                }
+                // above the diagonal blocks: zero (those columns held G)
+                {
+                    uint32_t z[16];
+#pragma unroll
+                    for (int q = 0; q < 16; ++q) z[q] = 0u;
+#pragma unroll 1
+                    for (int r = rb + 1; r < 4; ++r) ptx::tmem_st16(gm + 16 * r, z);
                 }
                 ptx::tmem_st_wait();
             }
             ptx::tc_fence_before();
             __syncwarp();
-            if (lane == 0) ptx::mbar_arrive(&sh.barM);
-            if (ptx::named_bar_any(kBarMask, 128, *(volatile int*)&sh.abort != 0)) break;
+            if (lane == 0) ptx::mbar_arrive(&sh.barM[X]);
+            if (full_mode) {
+                // ---- epilogue of chunk c: y = Ydiag + 2^{p_i} Yoff  (D x is in Ydiag)
+                wait_or_fail(sh, a, &sh.barYd[X], j & 1, kWhereBarYd);
+                wait_or_fail(sh, a, &sh.barY[X], j & 1, kWhereBarY);
+                ptx::tc_fence_after();
+                const uint32_t yd_addr = lane_addr + kTmGM + 128 * X + 64;
+                const uint32_t yo_addr = lane_addr + kTmYo + 64 * X;
+                __nv_bfloat16* yrow = yg + (((size_t)b * a.L + t + i) * a.H + h) * P;
+#pragma unroll
+                for (int q4 = 0; q4 < 4; ++q4) {
+                    uint32_t yd[16], yo[16];
+                    ptx::tmem_ld16(yd_addr + 16 * q4, yd);
+                    ptx::tmem_ld16(yo_addr + 16 * q4, yo);
+                    ptx::tmem_ld_wait();
+                    uint32_t ow[8];
+#pragma unroll
+                    for (int e = 0; e < 8; ++e)
+                        ow[e] = pack_bf16(fmaf(pe, __uint_as_float(yo[2 * e]), __uint_as_float(yd[2 * e])),
+                                          fmaf(pe, __uint_as_float(yo[2 * e + 1]), __uint_as_float(yd[2 * e + 1])));
+                    if (i < nv) {
+                        uint4* dst = reinterpret_cast<uint4*>(yrow + 16 * q4);
+                        dst[0] = make_uint4(ow[0], ow[1], ow[2], ow[3]);
+                        dst[1] = make_uint4(ow[4], ow[5], ow[6], ow[7]);
+                    }
+                }
+                ptx::tc_fence_before();
+                __syncwarp();
+                if (lane == 0) ptx::mbar_arrive(&sh.yFree[X]);
+            }
+            if (ptx::named_bar_any(nb, 128, *(volatile int*)&sh.abort != 0)) break;
         }
     } else {
         // ================================================================ state group
-        const int mt = threadIdx.x - 192;         // 0..127
+        ptx::regs_inc<kRegsMath>();
+        const int mt = threadIdx.x - 384;         // 0..127
         const int rb = warp & 3;
-        const int i = 32 * rb + lane;             // chunk row = TMEM lane = state column n
+        const int i = 32 * rb + lane;             // TMEM lane = state column n
         const uint32_t lane_addr = tb + ((uint32_t)(32 * rb) << 16);
-        const float Dh = a.D ? a.D[h] : 0.f;
         const size_t PN = (size_t)P * N;
         float S[P];
         if (full_mode && a.nsplit > 1 && s > 0) {
@@ -474,6 +511,7 @@ __global__ void __launch_bounds__(kThreads, 1) ssd_chunk_tc(const __grid_constan
 #pragma unroll
             for (int p = 0; p < P; ++p) S[p] = 0.f;
         }
+        // incoming state as the bf16 operand of Yoff; then one thread issues Yoff(k)
         auto write_sin = [&]() {
             uint8_t* sin = sm + kSin;
 #pragma unroll
@@ -486,29 +524,47 @@ __global__ void __launch_bounds__(kThreads, 1) ssd_chunk_tc(const __grid_constan
                 *reinterpret_cast<uint4*>(sin + sw128_off(i, 8 * q)) = sv;
             }
             ptx::fence_proxy_async();
-            __syncwarp();
-            if (lane == 0) ptx::mbar_arrive(&sh.barS);
         };
-        if (full_mode && nch > 0) write_sin();
+        auto issue_yoff = [&](int k) -> bool {
+            constexpr uint32_t idYo = ptx::idesc_bf16(128, 64, 0, 1);
+            const int Y = k & 1, jj = k >> 1;
+            if (!wait_or_fail(sh, a, &sh.full[Y], jj & 1, kWhereFull)) return false;
+            // Yoff buffer Y is free once the epilogue of chunk k-2 has read it
+            if (jj >= 1 && !wait_or_fail(sh, a, &sh.yFree[Y], (jj - 1) & 1, kWhereYFree)) return false;
+            ptx::tc_fence_after();
+            const uint32_t stg = ptx::smem_u32(sm + Y * kStageBytes);
+            const uint32_t sin = ptx::smem_u32(sm + kSin);
+#pragma unroll
+            for (int kk = 0; kk < 8; ++kk)
+                ptx::mma_ss(tb + kTmYo + 64 * Y, desc_k(stg + kTileC, kk), desc_mn1(sin, kk), idYo, kk > 0);
+            ptx::mma_commit(&sh.barY[Y]);
+            ptx::mma_commit(&sh.empty[Y]);
+            return true;
+        };
+        if (full_mode && nch > 0) {
+            write_sin();
+            ptx::named_bar(kBarState, 128);
+            if (mt == 0) issue_yoff(0);
+        }
         float tau_split = 0.f;
         for (int c = 0; c < nch; ++c) {
-            const int st = c % NS, k = c / NS, mb = c & 1;
-            uint8_t* stg = sm + st * kStageBytes;
+            const int X = c & 1, j = c >> 1, mb = c % NMETA;
+            uint8_t* stg = sm + X * kStageBytes;
             const int64_t t = t0 + (int64_t)c * Q;
             const int nv = (int)((t + Q < t1) ? Q : t1 - t);
-            wait_or_fail(sh, a, &sh.metaFull[mb], (c >> 1) & 1, kWhereMetaFull);
+            wait_or_fail(sh, a, &sh.metaFull[mb], (c / NMETA) & 1, kWhereMetaFull);
             const ChunkMeta& m = sh.meta[mb];
             // ---- packed documents that end inside this chunk: their final states
             if (full_mode && a.fin && a.cu) {
                 bool any = false;
                 for (int e = 0; e < nv - 1; ++e) any |= (m.rowflag[e] & 2) != 0;
                 if (any) {
-                    wait_or_fail(sh, a, &sh.full[st], k & 1, kWhereFull);
+                    wait_or_fail(sh, a, &sh.full[X], j & 1, kWhereFull);
                     doc_end_states(sh, m, stg, sm + kSin, a.fin, a.H, h, nv, i);
                 }
             }
             // ---- state update: S = 2^tau S + dS (TMEM lane = state column n)
-            wait_or_fail(sh, a, &sh.barDS, c & 1, kWhereBarDS);
+            wait_or_fail(sh, a, &sh.barDS[X], j & 1, kWhereBarDS);
             ptx::tc_fence_after();
             {
                 uint32_t ds0[32], ds1[32];
@@ -531,60 +587,17 @@ __global__ void __launch_bounds__(kThreads, 1) ssd_chunk_tc(const __grid_constan
 #pragma unroll
                 for (int p = 0; p < P; ++p) fo[(size_t)p * N] = S[p];
             }
-            if (full_mode) {
-                // Yoff(c) has read the incoming-state tile: stage the next one, then the outputs of c
-                wait_or_fail(sh, a, &sh.barY, c & 1, kWhereBarY);
-                ptx::tc_fence_after();
-                if (c + 1 < nch) write_sin();
-                wait_or_fail(sh, a, &sh.full[st], k & 1, kWhereFull);
-                if (mt == 0) ptx::bulk_wait_read0();   // the previous y store has read the staging tile
-                ptx::named_bar(kBarState, 128);
-                const uint8_t* xrow = stg + kTileX;
-                uint8_t* ys = sm + kYs;
-                const float pe = m.pexp[i];
-                const uint32_t yd_addr = lane_addr + kTmYd + 64 * (c & 1);
-                const uint32_t yo_addr = lane_addr + kTmYo + 64 * (c & 1);
-#pragma unroll
-                for (int half = 0; half < 2; ++half) {
-                    uint32_t yd[32], yo[32];
-                    ptx::tmem_ld32(yd_addr + 32 * half, yd);
-                    ptx::tmem_ld32(yo_addr + 32 * half, yo);
-                    ptx::tmem_ld_wait();
-                    if (half == 1) {
-                        ptx::tc_fence_before();
-                        __syncwarp();
-                        if (lane == 0) ptx::mbar_arrive(&sh.yFree[c & 1]);
-                    }
-#pragma unroll
-                    for (int q = 0; q < 4; ++q) {
-                        const int e0 = 32 * half + 8 * q;
-                        const uint4 v = *reinterpret_cast<const uint4*>(xrow + sw128_off(i, e0));
-                        const uint32_t xw[4] = {v.x, v.y, v.z, v.w};
-                        uint32_t ow[4];
-#pragma unroll
-                        for (int w2 = 0; w2 < 4; ++w2) {
-                            const int e = 8 * q + 2 * w2;
-                            float y0 = fmaf(pe, __uint_as_float(yo[e]), __uint_as_float(yd[e]));
-                            float y1 = fmaf(pe, __uint_as_float(yo[e + 1]), __uint_as_float(yd[e + 1]));
-                            y0 = fmaf(Dh, bf16lo(xw[w2]), y0);
-                            y1 = fmaf(Dh, bf16hi(xw[w2]), y1);
-                            ow[w2] = pack_bf16(y0, y1);
-                        }
-                        *reinterpret_cast<uint4*>(ys + sw128_off(i, e0)) = make_uint4(ow[0], ow[1], ow[2], ow[3]);
-                    }
-                }
-                ptx::fence_proxy_async();
-                ptx::named_bar(kBarState, 128);
-                if (mt == 0) {
-                    ptx::tma_store_4d(&prm.tm_y, ys, 0, h, (int)t, (int)b);
-                    ptx::bulk_commit();
-                }
-            }
-            // release the chunk's meta and input stage
-            ptx::named_bar(kBarState, 128);
+            ptx::named_bar(kBarState, 128);       // meta and stage reads of chunk c are done
             if (mt == 0) {
                 ptx::mbar_arrive(&sh.metaFree[mb]);
-                ptx::mbar_arrive(&sh.empty[st]);
+                ptx::mbar_arrive(&sh.empty[X]);
+            }
+            if (full_mode && c + 1 < nch) {
+                // Yoff(c) has read the incoming-state tile: stage S_in(c+1), issue Yoff(c+1)
+                wait_or_fail(sh, a, &sh.barY[X], j & 1, kWhereBarY);
+                write_sin();
+                ptx::named_bar(kBarState, 128);
+                if (mt == 0) issue_yoff(c + 1);
             }
             if (ptx::named_bar_any(kBarState, 128, *(volatile int*)&sh.abort != 0)) break;
         }
@@ -593,7 +606,10 @@ __global__ void __launch_bounds__(kThreads, 1) ssd_chunk_tc(const __grid_constan
             for (int p = 0; p < P; ++p) a.ws_state[uw * PN + (size_t)p * N + i] = S[p];
             if (mt == 0) a.ws_tau[uw] = tau_split * kLn2;
         }
-        if (mt == 0) ptx::bulk_wait0();
+        if (mt == 0 && full_mode) {
+            ptx::mma_commit(&sh.drain[2]);
+            if (!ptx::mbar_wait(&sh.drain[2], 0, &sh.never, kWaitNs)) fail(sh, a, kWhereDrain);
+        }
     }
     ptx::tc_fence_before();
     __syncthreads();
@@ -632,7 +648,7 @@ bool encode_4d(CUtensorMap* tm, const void* base, int64_t inner, int64_t mid, in
 
 }  // namespace
 
-size_t tc_smem_bytes() { return 1024 + kTiles + sizeof(TcSmall); }
+size_t tc_smem_bytes() { return kSmemBytes; }
 
 bool tc_supported(int P_, int N_, int Q_, int dtype) {
     return P_ == P && N_ == N && Q_ == Q && dtype == SSD_BF16;
@@ -642,8 +658,8 @@ cudaError_t launch_tc(const FwdArgs& a, cudaStream_t st) {
     TcParams prm;
     memset(&prm, 0, sizeof(prm));
     prm.a = a;
-    if (!encode_4d(&prm.tm_x, a.x, P, a.H, a.L, a.batch) || !encode_4d(&prm.tm_y, a.y, P, a.H, a.L, a.batch) ||
-        !encode_4d(&prm.tm_B, a.B, N, a.G, a.L, a.batch) || !encode_4d(&prm.tm_C, a.C, N, a.G, a.L, a.batch))
+    if (!encode_4d(&prm.tm_x, a.x, P, a.H, a.L, a.batch) || !encode_4d(&prm.tm_B, a.B, N, a.G, a.L, a.batch) ||
+        !encode_4d(&prm.tm_C, a.C, N, a.G, a.L, a.batch))
         return cudaErrorInvalidValue;
     const size_t smem = tc_smem_bytes();
     cudaError_t e = cudaFuncSetAttribute(ssd_chunk_tc, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
