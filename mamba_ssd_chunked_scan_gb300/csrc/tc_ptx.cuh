@@ -52,6 +52,7 @@ __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, const 
     if (mbar_try_wait(bar, parity)) return true;
     const uint64_t t0 = globaltimer();
     for (uint32_t it = 1;; ++it) {
+        __nanosleep(32);   // back off: a waiting warp must not take issue slots from working warps
         if (mbar_try_wait(bar, parity)) return true;
         if ((it & 63) == 0) {
             if (*abort) return false;
