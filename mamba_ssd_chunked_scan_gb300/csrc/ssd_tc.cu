@@ -45,6 +45,7 @@ namespace {
 
 constexpr int Q = 128, P = 64, N = 128;
 constexpr int NMETA = 3;                     // per-chunk value buffers between the math groups
+constexpr int kPrefetch = 4;                 // chunks of L2 prefetch beyond the shared-memory stages
 constexpr int kThreads = 512;
 constexpr int kRegsIssue = 56, kRegsMath = 152;   // 128 * (56 + 3 * 152) = 65536 = 512 * 128
 static_assert(128 * (kRegsIssue + 3 * kRegsMath) == kThreads * 128, "register split must equal the launch total");
@@ -54,7 +55,7 @@ constexpr uint32_t kSin = kXt + 2 * 16384;   // incoming state, bf16, (n rows, p
 constexpr uint32_t kTiles = kSin + 16384;
 // TMEM columns: G/M/Ydiag [2] (G, then M in cols 0-63 and Ydiag in 64-127) | Yoff [2] | dS
 constexpr uint32_t kTmGM = 0, kTmYo = 256, kTmDS = 384, kTmCols = 512;
-constexpr uint64_t kWaitNs = 2000000000ull;  // 2 s: far beyond any legitimate wait
+constexpr uint32_t kWaitIters = 1u << 26;   // >= 2 s of 32 ns back-offs: far beyond any legitimate wait
 constexpr float kLn2 = 0.6931471805599453f;
 constexpr int kBarMask0 = 1, kBarState = 3;  // named barriers: mask groups 1 and 2, state group 3
 
@@ -136,7 +137,7 @@ __device__ __noinline__ void fail(TcSmall& sh, const FwdArgs& a, uint32_t where)
 // bounded wait; the first role that gives up records why and raises abort
 __device__ __forceinline__ bool wait_or_fail(TcSmall& sh, const FwdArgs& a, uint64_t* bar, uint32_t parity,
                                              uint32_t where) {
-    if (ptx::mbar_wait(bar, parity, &sh.abort, kWaitNs)) return true;
+    if (ptx::mbar_wait(bar, parity, &sh.abort, kWaitIters)) return true;
     if (!*(volatile int*)&sh.abort) fail(sh, a, where);
     return false;
 }
@@ -252,8 +253,23 @@ __global__ void __launch_bounds__(kThreads, 1) ssd_chunk_tc(const __grid_constan
         if (warp == 0 && lane == 0) {
             // ============================================================ TMA producer
             int issued = 0;
+            // L2 prefetch runs kPrefetch chunks ahead of the two-stage shared-memory ring,
+            // so a stage refill finds its tiles in L2 instead of waiting on HBM
+            auto prefetch = [&](int c) {
+                if (c >= nch) return;
+                const int t = (int)(t0 + (int64_t)c * Q);
+                ptx::tma_prefetch_4d(&prm.tm_x, 0, h, t, (int)b);
+                ptx::tma_prefetch_4d(&prm.tm_B, 0, g, t, (int)b);
+                ptx::tma_prefetch_4d(&prm.tm_B, 64, g, t, (int)b);
+                if (full_mode) {
+                    ptx::tma_prefetch_4d(&prm.tm_C, 0, g, t, (int)b);
+                    ptx::tma_prefetch_4d(&prm.tm_C, 64, g, t, (int)b);
+                }
+            };
+            for (int c = 2; c < 2 + kPrefetch; ++c) prefetch(c);
             for (int c = 0; c < nch; ++c) {
                 const int st = c & 1;
+                prefetch(c + 2 + kPrefetch);
                 if (c >= 2 && !wait_or_fail(sh, a, &sh.empty[st], ((c >> 1) - 1) & 1, kWhereEmpty)) break;
                 const int t = (int)(t0 + (int64_t)c * Q);
                 uint8_t* stg = sm + st * kStageBytes;
@@ -270,7 +286,7 @@ __global__ void __launch_bounds__(kThreads, 1) ssd_chunk_tc(const __grid_constan
             // drain: the last load issued into each stage has landed
             for (int st = 0; st < 2 && st < issued; ++st) {
                 const int last = ((issued - 1 - st) >> 1) * 2 + st;
-                if (!ptx::mbar_wait(&sh.full[st], (last >> 1) & 1, &sh.never, kWaitNs)) fail(sh, a, kWhereDrain);
+                if (!ptx::mbar_wait(&sh.full[st], (last >> 1) & 1, &sh.never, kWaitIters)) fail(sh, a, kWhereDrain);
             }
         } else if (warp == 1 && lane == 0) {
             // ============================================================ Ydiag / dS issuer
@@ -283,7 +299,7 @@ __global__ void __launch_bounds__(kThreads, 1) ssd_chunk_tc(const __grid_constan
                 ptx::tc_fence_after();
                 if (full_mode) {
                     const uint32_t gm = tb + kTmGM + 128 * X;
-#pragma unroll
+#pragma unroll 1
                     for (int kk = 0; kk < 8; ++kk)
                         ptx::mma_ts(gm + 64, gm + 8 * kk, desc_mn1(stg + kTileX, kk), idYd, kk > 0);
                     ptx::mma_commit(&sh.barYd[X]);
@@ -291,14 +307,14 @@ __global__ void __launch_bounds__(kThreads, 1) ssd_chunk_tc(const __grid_constan
                 if (c >= 1 && !wait_or_fail(sh, a, &sh.dsFree, (c - 1) & 1, kWhereDsFree)) break;
                 ptx::tc_fence_after();
                 const uint32_t xt = ptx::smem_u32(sm + kXt + 16384 * X);
-#pragma unroll
+#pragma unroll 1
                 for (int kk = 0; kk < 8; ++kk)
                     ptx::mma_ss(tb + kTmDS, desc_mn2(stg + kTileB, kk), desc_mn1(xt, kk), idDS, kk > 0);
                 ptx::mma_commit(&sh.barDS[X]);
                 ptx::mma_commit(&sh.empty[X]);
             }
             ptx::mma_commit(&sh.drain[0]);
-            if (!ptx::mbar_wait(&sh.drain[0], 0, &sh.never, kWaitNs)) fail(sh, a, kWhereDrain);
+            if (!ptx::mbar_wait(&sh.drain[0], 0, &sh.never, kWaitIters)) fail(sh, a, kWhereDrain);
         } else if (warp == 2 && lane == 0 && full_mode) {
             // ============================================================ G issuer
             constexpr uint32_t idG = ptx::idesc_bf16(128, 128, 0, 0);
@@ -310,13 +326,13 @@ __global__ void __launch_bounds__(kThreads, 1) ssd_chunk_tc(const __grid_constan
                 if (j >= 1 && !wait_or_fail(sh, a, &sh.yFree[X], (j - 1) & 1, kWhereYFree)) break;
                 ptx::tc_fence_after();
                 const uint32_t d = tb + kTmGM + 128 * X;
-#pragma unroll
+#pragma unroll 1
                 for (int kk = 0; kk < 8; ++kk)
                     ptx::mma_ss(d, desc_k(stg + kTileC, kk), desc_k(stg + kTileB, kk), idG, kk > 0);
                 ptx::mma_commit(&sh.barG[X]);
             }
             ptx::mma_commit(&sh.drain[1]);
-            if (!ptx::mbar_wait(&sh.drain[1], 0, &sh.never, kWaitNs)) fail(sh, a, kWhereDrain);
+            if (!ptx::mbar_wait(&sh.drain[1], 0, &sh.never, kWaitIters)) fail(sh, a, kWhereDrain);
         }
     } else if (wg <= 2) {
         // ================================================================ mask groups
@@ -385,7 +401,7 @@ __global__ void __launch_bounds__(kThreads, 1) ssd_chunk_tc(const __grid_constan
             {
                 const uint8_t* xrow = stg + kTileX;
                 uint8_t* xt = sm + kXt + 16384 * X;
-#pragma unroll
+#pragma unroll 2
                 for (int q = 0; q < 8; ++q) {
                     const uint4 v = *reinterpret_cast<const uint4*>(xrow + sw128_off(i, 8 * q));
                     uint4 o;
@@ -408,11 +424,10 @@ __global__ void __launch_bounds__(kThreads, 1) ssd_chunk_tc(const __grid_constan
 #pragma unroll 1
                 for (int r = 0; r < rb; ++r) {
                     uint32_t gr[32];
-                    ptx::tmem_ld32(gm + 32 * r, gr);
+                    ptx::tmem_load32(gm + 32 * r, gr);
                     const float Rr = (r == 0) ? row.R[0] : (r == 1) ? row.R[1] : row.R[2];
                     const float rf = ex2_approx(Rr);
                     const float4* cf = reinterpret_cast<const float4*>(ms.colfac + 32 * r);
-                    ptx::tmem_ld_wait();
                     uint32_t pk[16];
 #pragma unroll
                     for (int q = 0; q < 8; ++q) {
@@ -427,9 +442,8 @@ __global__ void __launch_bounds__(kThreads, 1) ssd_chunk_tc(const __grid_constan
                 // 1-SS diagonal block rb (running sums from the diagonal), plus D on the diagonal
                 {
                     uint32_t gr[32];
-                    ptx::tmem_ld32(gm + 32 * rb, gr);
+                    ptx::tmem_load32(gm + 32 * rb, gr);
                     const float4* dv = reinterpret_cast<const float4*>(ms.dtv + 32 * rb);
-                    ptx::tmem_ld_wait();
                     uint32_t pk[16];
 #pragma unroll
                     for (int q = 0; q < 8; ++q) {
@@ -469,21 +483,21 @@ __global__ void __launch_bounds__(kThreads, 1) ssd_chunk_tc(const __grid_constan
                 const uint32_t yd_addr = lane_addr + kTmGM + 128 * X + 64;
                 const uint32_t yo_addr = lane_addr + kTmYo + 64 * X;
                 __nv_bfloat16* yrow = yg + (((size_t)b * a.L + t + i) * a.H + h) * P;
+#pragma unroll 1
+                for (int q8 = 0; q8 < 2; ++q8) {
+                    uint32_t yd[32], yo[32];
+                    ptx::tmem_load32x2(yd_addr + 32 * q8, yd, yo_addr + 32 * q8, yo);
+                    uint32_t ow[16];
 #pragma unroll
-                for (int q4 = 0; q4 < 4; ++q4) {
-                    uint32_t yd[16], yo[16];
-                    ptx::tmem_ld16(yd_addr + 16 * q4, yd);
-                    ptx::tmem_ld16(yo_addr + 16 * q4, yo);
-                    ptx::tmem_ld_wait();
-                    uint32_t ow[8];
-#pragma unroll
-                    for (int e = 0; e < 8; ++e)
+                    for (int e = 0; e < 16; ++e)
                         ow[e] = pack_bf16(fmaf(pe, __uint_as_float(yo[2 * e]), __uint_as_float(yd[2 * e])),
                                           fmaf(pe, __uint_as_float(yo[2 * e + 1]), __uint_as_float(yd[2 * e + 1])));
                     if (i < nv) {
-                        uint4* dst = reinterpret_cast<uint4*>(yrow + 16 * q4);
+                        uint4* dst = reinterpret_cast<uint4*>(yrow + 32 * q8);
                         dst[0] = make_uint4(ow[0], ow[1], ow[2], ow[3]);
                         dst[1] = make_uint4(ow[4], ow[5], ow[6], ow[7]);
+                        dst[2] = make_uint4(ow[8], ow[9], ow[10], ow[11]);
+                        dst[3] = make_uint4(ow[12], ow[13], ow[14], ow[15]);
                     }
                 }
                 ptx::tc_fence_before();
@@ -534,7 +548,7 @@ __global__ void __launch_bounds__(kThreads, 1) ssd_chunk_tc(const __grid_constan
             ptx::tc_fence_after();
             const uint32_t stg = ptx::smem_u32(sm + Y * kStageBytes);
             const uint32_t sin = ptx::smem_u32(sm + kSin);
-#pragma unroll
+#pragma unroll 1
             for (int kk = 0; kk < 8; ++kk)
                 ptx::mma_ss(tb + kTmYo + 64 * Y, desc_k(stg + kTileC, kk), desc_mn1(sin, kk), idYo, kk > 0);
             ptx::mma_commit(&sh.barY[Y]);
@@ -568,9 +582,7 @@ __global__ void __launch_bounds__(kThreads, 1) ssd_chunk_tc(const __grid_constan
             ptx::tc_fence_after();
             {
                 uint32_t ds0[32], ds1[32];
-                ptx::tmem_ld32(lane_addr + kTmDS, ds0);
-                ptx::tmem_ld32(lane_addr + kTmDS + 32, ds1);
-                ptx::tmem_ld_wait();
+                ptx::tmem_load32x2(lane_addr + kTmDS, ds0, lane_addr + kTmDS + 32, ds1);
                 ptx::tc_fence_before();
                 __syncwarp();
                 if (lane == 0) ptx::mbar_arrive(&sh.dsFree);
@@ -608,7 +620,7 @@ __global__ void __launch_bounds__(kThreads, 1) ssd_chunk_tc(const __grid_constan
         }
         if (mt == 0 && full_mode) {
             ptx::mma_commit(&sh.drain[2]);
-            if (!ptx::mbar_wait(&sh.drain[2], 0, &sh.never, kWaitNs)) fail(sh, a, kWhereDrain);
+            if (!ptx::mbar_wait(&sh.drain[2], 0, &sh.never, kWaitIters)) fail(sh, a, kWhereDrain);
         }
     }
     ptx::tc_fence_before();

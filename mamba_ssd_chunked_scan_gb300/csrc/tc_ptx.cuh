@@ -45,20 +45,17 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
 }
 
 // Wait for the phase with the given parity to complete.  Gives up (returns
-// false) after `limit_ns` of wall time or as soon as *abort is set, so that
-// no wait can hang the GPU.
+// false) after `max_iters` back-off rounds (each sleeps ~32 ns or more), or
+// as soon as *abort is set, so that no wait can hang the GPU.
 __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, const volatile int* abort,
-                                          uint64_t limit_ns) {
+                                          uint32_t max_iters) {
     if (mbar_try_wait(bar, parity)) return true;
-    const uint64_t t0 = globaltimer();
-    for (uint32_t it = 1;; ++it) {
+    for (uint32_t it = 1; it < max_iters; ++it) {
         __nanosleep(32);   // back off: a waiting warp must not take issue slots from working warps
         if (mbar_try_wait(bar, parity)) return true;
-        if ((it & 63) == 0) {
-            if (*abort) return false;
-            if (globaltimer() - t0 > limit_ns) return false;
-        }
+        if ((it & 255) == 0 && *abort) return false;
     }
+    return false;
 }
 
 // ---------------------------------------------------------------- TMA
@@ -69,6 +66,12 @@ __device__ __forceinline__ void tma_load_4d(void* smem_dst, const CUtensorMap* t
         "%6}], [%2];" ::"r"(smem_u32(smem_dst)),
         "l"(tm), "r"(smem_u32(bar)), "r"(c0), "r"(c1), "r"(c2), "r"(c3)
         : "memory");
+}
+// bring a tile into L2 ahead of its load (no shared memory, no completion)
+__device__ __forceinline__ void tma_prefetch_4d(const CUtensorMap* tm, int c0, int c1, int c2, int c3) {
+    asm volatile("cp.async.bulk.prefetch.tensor.4d.L2.global [%0, {%1, %2, %3, %4}];" ::"l"(tm), "r"(c0), "r"(c1),
+                 "r"(c2), "r"(c3)
+                 : "memory");
 }
 __device__ __forceinline__ void tma_store_4d(const CUtensorMap* tm, const void* smem_src, int c0, int c1,
                                              int c2, int c3) {
@@ -158,6 +161,35 @@ __device__ __forceinline__ void tmem_ld32(uint32_t taddr, uint32_t (&r)[32]) {
           "=r"(r[30]), "=r"(r[31])
         : "r"(taddr));
 }
+// Loads fused with their wait: the destination registers are defined only
+// after the data has landed, so the compiler can never read, move or spill
+// them while the asynchronous load is still filling them.
+#define SSD_R32(r) "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]), \
+    "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15]),          \
+    "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]), "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]),        \
+    "=r"(r[24]), "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
+__device__ __forceinline__ void tmem_load32(uint32_t taddr, uint32_t (&r)[32]) {
+    asm volatile(
+        "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,"
+        "%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%32];\n\t"
+        "tcgen05.wait::ld.sync.aligned;"
+        : SSD_R32(r)
+        : "r"(taddr)
+        : "memory");
+}
+__device__ __forceinline__ void tmem_load32x2(uint32_t ta, uint32_t (&ra)[32], uint32_t tb, uint32_t (&rb)[32]) {
+    asm volatile(
+        "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,"
+        "%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%64];\n\t"
+        "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%32,%33,%34,%35,%36,%37,%38,%39,%40,%41,%42,%43,%44,%45,%46,%47,"
+        "%48,%49,%50,%51,%52,%53,%54,%55,%56,%57,%58,%59,%60,%61,%62,%63}, [%65];\n\t"
+        "tcgen05.wait::ld.sync.aligned;"
+        : SSD_R32(ra), SSD_R32(rb)
+        : "r"(ta), "r"(tb)
+        : "memory");
+}
+#undef SSD_R32
+
 // 32 lanes x 16 consecutive 32-bit columns
 __device__ __forceinline__ void tmem_ld16(uint32_t taddr, uint32_t (&r)[16]) {
     asm volatile(
