@@ -106,6 +106,30 @@ SSD_API int ssd_fwd(const ssd_params_t* p,
             void* y, float* final_states,
             void* workspace, size_t workspace_bytes, void* stream);
 
+/* ssd_fwd() for callers that cannot allocate device memory (for example a
+ * plugin inside a host application that owns every device allocation, or a
+ * C caller that only holds the input and output pointers it was given).
+ * The paper has no counterpart of this entry point.
+ *
+ * Same operation, arguments and layouts as ssd_fwd(), without a workspace:
+ * the workspace is a library-owned device array of 8 MiB that every GPU
+ * loading the library reserves until process exit.  Problems whose
+ * ssd_fwd_workspace_size() exceeds 8 MiB are rejected with
+ * SSD_ERR_WORKSPACE before anything is launched; single-split problems only
+ * need 256 bytes.  The caller still passes all inputs and outputs.
+ * The first call on a device looks up the array's device address with that
+ * device current (cudaGetSymbolAddress); make that first call before any
+ * stream capture.  Every call uses the same array: calls whose GPU work
+ * overlaps (other streams or other host threads) race on it.  The call
+ * clears the status word, enqueues the work on `stream`, then synchronises
+ * the stream and returns the device status (SSD_OK or the first device
+ * error).  It calls no allocating routine. */
+SSD_API int ssd_fwd_static_scratch(const ssd_params_t* p,
+            const void* x, const float* dt, const float* A,
+            const void* B, const void* C, const float* D,
+            const float* initial_states, const int32_t* cu_seqlens,
+            void* y, float* final_states, void* stream);
+
 /* Synchronise `stream`, read the device status word of `workspace`, clear it,
  * and return it (SSD_OK when no device error was recorded). */
 SSD_API int ssd_check_status(void* workspace, void* stream);

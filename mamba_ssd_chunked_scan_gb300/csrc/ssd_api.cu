@@ -4,6 +4,8 @@
 #include <stdio.h>
 #include <string.h>
 
+#include <mutex>
+
 #include "ssd_common.cuh"
 #include "ssd_kernels.h"
 
@@ -74,6 +76,40 @@ bool use_tc(const ssd_params_t* p, bool has_init) {
     return true;
 }
 
+}  // namespace
+
+// ---------------------------------------------------------------------------
+// Library-owned scratch for callers that cannot allocate device memory.
+//
+// Some callers of this library have no way to allocate device memory: a
+// plugin running inside a host application that owns and budgets every
+// device allocation, or a thin C caller that only holds pointers handed to it.
+// ssd_fwd_static_scratch() serves them with a workspace that lives in this
+// file-scope device array instead of caller memory.  Every GPU that loads the
+// library keeps these bytes reserved until the process exits.
+// ---------------------------------------------------------------------------
+static constexpr size_t kStaticScratchBytes = (size_t)8 << 20;   // 8 MiB
+static __device__ __align__(256) unsigned char g_static_scratch[kStaticScratchBytes];
+
+namespace {
+std::mutex g_static_mu;
+void* g_static_ptr[256];   // device address of g_static_scratch, per device ordinal
+
+// Device address of the scratch array on the current device.  In host code the
+// array's name is only a host-side stand-in, so the address is looked up with
+// cudaGetSymbolAddress once per device (with that device current) and cached.
+int static_scratch_ptr(void** out) {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 256) return SSD_ERR_CUDA;
+    std::lock_guard<std::mutex> lk(g_static_mu);
+    if (!g_static_ptr[dev]) {
+        void* ptr = nullptr;
+        if (cudaGetSymbolAddress(&ptr, g_static_scratch) != cudaSuccess || !ptr) return SSD_ERR_CUDA;
+        g_static_ptr[dev] = ptr;
+    }
+    *out = g_static_ptr[dev];
+    return SSD_OK;
+}
 }  // namespace
 
 extern "C" {
@@ -171,6 +207,24 @@ int ssd_fwd(const ssd_params_t* p, const void* x, const float* dt, const float* 
     a.mode = kModeFull;
     if (launch(a) != cudaSuccess) return SSD_ERR_CUDA;
     return SSD_OK;
+}
+
+int ssd_fwd_static_scratch(const ssd_params_t* p, const void* x, const float* dt, const float* A,
+                           const void* B, const void* C, const float* D, const float* init,
+                           const int32_t* cu, void* y, float* fin, void* stream) {
+    int rc = check_params(p);
+    if (rc != SSD_OK) return rc;
+    const size_t need = ssd_fwd_workspace_size(p);
+    if (need > kStaticScratchBytes) return SSD_ERR_WORKSPACE;   // problem too large for the static scratch
+    void* ws = nullptr;
+    if ((rc = static_scratch_ptr(&ws)) != SSD_OK) return rc;
+    cudaStream_t st = (cudaStream_t)stream;
+    // the array keeps the previous call's contents: the status word must start at zero
+    if (cudaMemsetAsync(ws, 0, sizeof(WsHeader), st) != cudaSuccess) return SSD_ERR_CUDA;
+    rc = ssd_fwd(p, x, dt, A, B, C, D, init, cu, y, fin, ws, kStaticScratchBytes, stream);
+    if (rc != SSD_OK) return rc;
+    // synchronous: wait for the work and report what the device recorded
+    return ssd_check_status(ws, stream);
 }
 
 int ssd_segsum_dump(const float* l2, int64_t nrows, int32_t chunk, float* seg, float* L, void* stream) {
