@@ -129,6 +129,18 @@ class ClockSampler:
                 "reasons": reasons, "samples": len(self.rows)}
 
 
+def kernel_sources_sha() -> str:
+    """Fingerprint of every CUDA source of the library (to tell whether a
+    recorded counter still belongs to the kernels being timed)."""
+    csrc = os.path.join(ROOT, "mamba_ssd_chunked_scan_gb300", "csrc")
+    h = hashlib.sha256()
+    for name in sorted(os.listdir(csrc)):
+        if name.endswith((".cu", ".cuh", ".h")):
+            h.update(name.encode())
+            h.update(open(os.path.join(csrc, name), "rb").read())
+    return h.hexdigest()[:16]
+
+
 def kernel_traffic(family: int):
     """DRAM bytes per launch of the dominant kernel from the committed ncu
     summary, used only while the kernel source is unchanged since capture."""
@@ -140,9 +152,7 @@ def kernel_traffic(family: int):
         ent = d.get(str(family))
         if not ent:
             return None
-        src = os.path.join(ROOT, "mamba_ssd_chunked_scan_gb300", "csrc", ent["source"])
-        sha = hashlib.sha256(open(src, "rb").read()).hexdigest()[:16]
-        return ent["dram_bytes_per_launch"] if sha == ent["source_sha"] else None
+        return ent["dram_bytes_per_launch"] if kernel_sources_sha() == ent["source_sha"] else None
     except Exception:
         return None
 
