@@ -16,7 +16,7 @@
 //   dS    = B^T (exp(s_j) dt_j x_j)      (UMMA, chunk state summary)
 //   Yoff  = C S_in^T                     (UMMA; the row decay exp(p_i) is applied in the epilogue)
 //   S     = exp(tau) S + dS              (state carried in registers)
-//   y     = Ydiag + exp(p_i) Yoff        (epilogue, stored from registers)
+//   y     = Ydiag + exp(p_i) Yoff        (epilogue, TMA store)
 //
 // Warpgroups (512 threads; register budgets rebalanced with setmaxnreg):
 //   WG0  warp 0: TMA producer; warp 1: issues Ydiag and dS; warp 2: issues G
@@ -109,7 +109,7 @@ constexpr size_t kSmemBytes = 1024 + kTiles + sizeof(TcSmall);
 static_assert(kSmemBytes <= 227 * 1024, "shared memory per CTA");
 
 struct TcParams {
-    CUtensorMap tm_x, tm_B, tm_C;
+    CUtensorMap tm_x, tm_B, tm_C, tm_y;
     FwdArgs a;
 };
 
@@ -241,6 +241,7 @@ __global__ void __launch_bounds__(kThreads, 1) ssd_chunk_tc(const __grid_constan
         ptx::prefetch_tmap(&prm.tm_x);
         ptx::prefetch_tmap(&prm.tm_B);
         ptx::prefetch_tmap(&prm.tm_C);
+        ptx::prefetch_tmap(&prm.tm_y);
     }
     if (warp == 1) ptx::tmem_alloc(&sh.tmem_base, kTmCols);
     ptx::tc_fence_before();
@@ -346,7 +347,6 @@ __global__ void __launch_bounds__(kThreads, 1) ssd_chunk_tc(const __grid_constan
         const uint32_t lane_addr = tb + ((uint32_t)(32 * rb) << 16);
         const float A2 = a.A[h] * kLog2e;
         const float Dh = a.D ? a.D[h] : 0.f;
-        __nv_bfloat16* yg = (__nv_bfloat16*)a.y;
         auto load_dt = [&](int c) -> float {
             const int64_t t = t0 + (int64_t)c * Q;
             return (c < nch && t + i < t1) ? __ldg(a.dt + ((size_t)b * a.L + t + i) * a.H + h) : 0.f;
@@ -381,6 +381,8 @@ __global__ void __launch_bounds__(kThreads, 1) ssd_chunk_tc(const __grid_constan
             m.dtv[i] = dti;
             m.rowflag[i] = flag;
             m.rowdoc[i] = doc;
+            // the y store of chunk c-2 (staged in this group's scaled-X buffer) has read it
+            if (mt == 0 && j >= 1) ptx::bulk_wait_read0();
             ptx::named_bar(nb, 128);
             if (mt == Q - 1 && a.cu) ms.doc_cursor = doc;   // later chunks start in (or after) this document
             SegsumRow<4> row;
@@ -476,36 +478,45 @@ __global__ void __launch_bounds__(kThreads, 1) ssd_chunk_tc(const __grid_constan
             __syncwarp();
             if (lane == 0) ptx::mbar_arrive(&sh.barM[X]);
             if (full_mode) {
-                // ---- epilogue of chunk c: y = Ydiag + 2^{p_i} Yoff  (D x is in Ydiag)
+                // ---- epilogue of chunk c: y = Ydiag + 2^{p_i} Yoff  (D x is in Ydiag).
+                // The rows are staged in this group's scaled-X buffer (free once dS(c)
+                // is done) and written by one TMA store (rows past L are clipped).
                 wait_or_fail(sh, a, &sh.barYd[X], j & 1, kWhereBarYd);
                 wait_or_fail(sh, a, &sh.barY[X], j & 1, kWhereBarY);
+                wait_or_fail(sh, a, &sh.barDS[X], j & 1, kWhereBarDS);
                 ptx::tc_fence_after();
                 const uint32_t yd_addr = lane_addr + kTmGM + 128 * X + 64;
                 const uint32_t yo_addr = lane_addr + kTmYo + 64 * X;
-                __nv_bfloat16* yrow = yg + (((size_t)b * a.L + t + i) * a.H + h) * P;
+                uint8_t* ys = sm + kXt + 16384 * X;
 #pragma unroll 1
                 for (int q8 = 0; q8 < 2; ++q8) {
                     uint32_t yd[32], yo[32];
                     ptx::tmem_load32x2(yd_addr + 32 * q8, yd, yo_addr + 32 * q8, yo);
+                    if (q8 == 1) {
+                        ptx::tc_fence_before();
+                        __syncwarp();
+                        if (lane == 0) ptx::mbar_arrive(&sh.yFree[X]);
+                    }
                     uint32_t ow[16];
 #pragma unroll
                     for (int e = 0; e < 16; ++e)
                         ow[e] = pack_bf16(fmaf(pe, __uint_as_float(yo[2 * e]), __uint_as_float(yd[2 * e])),
                                           fmaf(pe, __uint_as_float(yo[2 * e + 1]), __uint_as_float(yd[2 * e + 1])));
-                    if (i < nv) {
-                        uint4* dst = reinterpret_cast<uint4*>(yrow + 32 * q8);
-                        dst[0] = make_uint4(ow[0], ow[1], ow[2], ow[3]);
-                        dst[1] = make_uint4(ow[4], ow[5], ow[6], ow[7]);
-                        dst[2] = make_uint4(ow[8], ow[9], ow[10], ow[11]);
-                        dst[3] = make_uint4(ow[12], ow[13], ow[14], ow[15]);
-                    }
+#pragma unroll
+                    for (int q = 0; q < 4; ++q)
+                        *reinterpret_cast<uint4*>(ys + sw128_off(i, 32 * q8 + 8 * q)) =
+                            make_uint4(ow[4 * q], ow[4 * q + 1], ow[4 * q + 2], ow[4 * q + 3]);
                 }
-                ptx::tc_fence_before();
-                __syncwarp();
-                if (lane == 0) ptx::mbar_arrive(&sh.yFree[X]);
+                ptx::fence_proxy_async();
+                ptx::named_bar(nb, 128);
+                if (mt == 0) {
+                    ptx::tma_store_4d(&prm.tm_y, ys, 0, h, (int)t, (int)b);
+                    ptx::bulk_commit();
+                }
             }
             if (ptx::named_bar_any(nb, 128, *(volatile int*)&sh.abort != 0)) break;
         }
+        if (mt == 0) ptx::bulk_wait0();
     } else {
         // ================================================================ state group
         ptx::regs_inc<kRegsMath>();
@@ -671,7 +682,7 @@ cudaError_t launch_tc(const FwdArgs& a, cudaStream_t st) {
     memset(&prm, 0, sizeof(prm));
     prm.a = a;
     if (!encode_4d(&prm.tm_x, a.x, P, a.H, a.L, a.batch) || !encode_4d(&prm.tm_B, a.B, N, a.G, a.L, a.batch) ||
-        !encode_4d(&prm.tm_C, a.C, N, a.G, a.L, a.batch))
+        !encode_4d(&prm.tm_C, a.C, N, a.G, a.L, a.batch) || !encode_4d(&prm.tm_y, a.y, P, a.H, a.L, a.batch))
         return cudaErrorInvalidValue;
     const size_t smem = tc_smem_bytes();
     cudaError_t e = cudaFuncSetAttribute(ssd_chunk_tc, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
