@@ -19,7 +19,7 @@
 //   y     = Ydiag + exp(p_i) Yoff        (epilogue, TMA store)
 //
 // Warpgroups (512 threads; register budgets rebalanced with setmaxnreg):
-//   WG0  warp 0: TMA producer; warp 1: issues Ydiag and dS; warp 2: issues G
+//   WG0  warp 0: TMA producer; warp 1: issues dS; warp 2: issues G; warp 3: issues Ydiag
 //   WG1  mask group for even chunks, WG2 mask group for odd chunks:
 //        log-decays, segsum, scaled X tile, mask M, and the chunk's epilogue
 //   WG3  state group: state update, incoming-state tile, issues Yoff
@@ -89,10 +89,10 @@ struct TcSmall {
     ChunkMeta meta[NMETA];
     alignas(16) float wv[Q];
     uint64_t full[2], empty[2];
-    uint64_t barG[2], barM[2], barYd[2], barDS[2], barY[2], yFree[2];
+    uint64_t barG[2], barM[2], barXt[2], barYd[2], barDS[2], barY[2], yFree[2];
     uint64_t dsFree;
     uint64_t metaFull[NMETA], metaFree[NMETA];
-    uint64_t drain[3];
+    uint64_t drain[4];
     uint32_t tmem_base;
     int abort;
     int never;                     // stays 0: lets drain waits ignore the abort flag
@@ -215,10 +215,11 @@ __global__ void __launch_bounds__(kThreads, 1) ssd_chunk_tc(const __grid_constan
     if (threadIdx.x == 0) {
         for (int i = 0; i < 2; ++i) {
             ptx::mbar_init(&sh.full[i], 1);
-            // stage readers: dS issuer, mask group, state group (+ Yoff issuer)
-            ptx::mbar_init(&sh.empty[i], full_mode ? 4 : 3);
+            // stage readers: dS issuer, mask group, state group (+ Ydiag and Yoff issuers)
+            ptx::mbar_init(&sh.empty[i], full_mode ? 5 : 3);
             ptx::mbar_init(&sh.barG[i], 1);
             ptx::mbar_init(&sh.barM[i], 4);
+            ptx::mbar_init(&sh.barXt[i], 4);
             ptx::mbar_init(&sh.barYd[i], 1);
             ptx::mbar_init(&sh.barDS[i], 1);
             ptx::mbar_init(&sh.barY[i], 1);
@@ -229,7 +230,7 @@ __global__ void __launch_bounds__(kThreads, 1) ssd_chunk_tc(const __grid_constan
             ptx::mbar_init(&sh.metaFull[i], 4);
             ptx::mbar_init(&sh.metaFree[i], 1);
         }
-        for (int i = 0; i < 3; ++i) ptx::mbar_init(&sh.drain[i], 1);
+        for (int i = 0; i < 4; ++i) ptx::mbar_init(&sh.drain[i], 1);
         sh.abort = 0;
         sh.never = 0;
         const int dc = a.cu ? find_doc_tc(a.cu, a.ndocs, t0) : 0;
@@ -290,21 +291,14 @@ __global__ void __launch_bounds__(kThreads, 1) ssd_chunk_tc(const __grid_constan
                 if (!ptx::mbar_wait(&sh.full[st], (last >> 1) & 1, &sh.never, kWaitIters)) fail(sh, a, kWhereDrain);
             }
         } else if (warp == 1 && lane == 0) {
-            // ============================================================ Ydiag / dS issuer
-            constexpr uint32_t idYd = ptx::idesc_bf16(128, 64, 0, 1);
+            // ============================================================ dS issuer
+            // the chunk state summary needs only the scaled X tile, so it runs as soon
+            // as that is written (ahead of the mask), which keeps the state recurrence short
             constexpr uint32_t idDS = ptx::idesc_bf16(128, 64, 1, 1);
             for (int c = 0; c < nch; ++c) {
                 const int X = c & 1, j = c >> 1;
                 const uint32_t stg = ptx::smem_u32(sm + X * kStageBytes);
-                if (!wait_or_fail(sh, a, &sh.barM[X], j & 1, kWhereBarM)) break;
-                ptx::tc_fence_after();
-                if (full_mode) {
-                    const uint32_t gm = tb + kTmGM + 128 * X;
-#pragma unroll 1
-                    for (int kk = 0; kk < 8; ++kk)
-                        ptx::mma_ts(gm + 64, gm + 8 * kk, desc_mn1(stg + kTileX, kk), idYd, kk > 0);
-                    ptx::mma_commit(&sh.barYd[X]);
-                }
+                if (!wait_or_fail(sh, a, &sh.barXt[X], j & 1, kWhereBarM)) break;
                 if (c >= 1 && !wait_or_fail(sh, a, &sh.dsFree, (c - 1) & 1, kWhereDsFree)) break;
                 ptx::tc_fence_after();
                 const uint32_t xt = ptx::smem_u32(sm + kXt + 16384 * X);
@@ -316,6 +310,23 @@ __global__ void __launch_bounds__(kThreads, 1) ssd_chunk_tc(const __grid_constan
             }
             ptx::mma_commit(&sh.drain[0]);
             if (!ptx::mbar_wait(&sh.drain[0], 0, &sh.never, kWaitIters)) fail(sh, a, kWhereDrain);
+        } else if (warp == 3 && lane == 0 && full_mode) {
+            // ============================================================ Ydiag issuer
+            constexpr uint32_t idYd = ptx::idesc_bf16(128, 64, 0, 1);
+            for (int c = 0; c < nch; ++c) {
+                const int X = c & 1, j = c >> 1;
+                const uint32_t stg = ptx::smem_u32(sm + X * kStageBytes);
+                if (!wait_or_fail(sh, a, &sh.barM[X], j & 1, kWhereBarM)) break;
+                ptx::tc_fence_after();
+                const uint32_t gm = tb + kTmGM + 128 * X;
+#pragma unroll 1
+                for (int kk = 0; kk < 8; ++kk)
+                    ptx::mma_ts(gm + 64, gm + 8 * kk, desc_mn1(stg + kTileX, kk), idYd, kk > 0);
+                ptx::mma_commit(&sh.barYd[X]);
+                ptx::mma_commit(&sh.empty[X]);
+            }
+            ptx::mma_commit(&sh.drain[3]);
+            if (!ptx::mbar_wait(&sh.drain[3], 0, &sh.never, kWaitIters)) fail(sh, a, kWhereDrain);
         } else if (warp == 2 && lane == 0 && full_mode) {
             // ============================================================ G issuer
             constexpr uint32_t idG = ptx::idesc_bf16(128, 128, 0, 0);
@@ -415,6 +426,8 @@ __global__ void __launch_bounds__(kThreads, 1) ssd_chunk_tc(const __grid_constan
                 }
                 ptx::fence_proxy_async();
             }
+            __syncwarp();
+            if (lane == 0) ptx::mbar_arrive(&sh.barXt[X]);   // the state summary can start
             ptx::named_bar(nb, 128);              // colfac complete; X tile reads done
             if (mt == 0) ptx::mbar_arrive(&sh.empty[X]);
             if (full_mode) {
