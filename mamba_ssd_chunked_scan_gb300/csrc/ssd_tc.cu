@@ -192,6 +192,12 @@ __device__ __noinline__ void doc_end_states(TcSmall& sh, const ChunkMeta& m, con
     }
 }
 
+// kFull: full pass (else the aggregate pass of a split plan); kDocs: packed
+// documents (cu_seqlens).  Each combination is its own kernel, so the hot
+// loops carry no run-time mode branches: the compiler would otherwise keep a
+// copy of a loop body per branch, and instruction fetch is a scarce resource
+// for this kernel (its warps run several different loops at once).
+template <bool kFull, bool kDocs>
 __global__ void __launch_bounds__(kThreads, 1) ssd_chunk_tc(const __grid_constant__ TcParams prm) {
     extern __shared__ uint8_t smem_raw[];
     uint8_t* sm = (uint8_t*)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
@@ -199,7 +205,7 @@ __global__ void __launch_bounds__(kThreads, 1) ssd_chunk_tc(const __grid_constan
     const FwdArgs& a = prm.a;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int wg = warp >> 2;
-    const bool full_mode = (a.mode == kModeFull);
+    constexpr bool full_mode = kFull;
 
     // unit: heads of one (row, split) are adjacent so they share B / C in L2
     const int64_t u = blockIdx.x;
@@ -233,7 +239,7 @@ __global__ void __launch_bounds__(kThreads, 1) ssd_chunk_tc(const __grid_constan
         for (int i = 0; i < 4; ++i) ptx::mbar_init(&sh.drain[i], 1);
         sh.abort = 0;
         sh.never = 0;
-        const int dc = a.cu ? find_doc_tc(a.cu, a.ndocs, t0) : 0;
+        const int dc = kDocs ? find_doc_tc(a.cu, a.ndocs, t0) : 0;
         sh.mask[0].doc_cursor = dc;
         sh.mask[1].doc_cursor = dc;
         ptx::mbar_fence_init();
@@ -374,7 +380,7 @@ __global__ void __launch_bounds__(kThreads, 1) ssd_chunk_tc(const __grid_constan
             // document boundaries: walk forward from this group's cursor
             int flag = 0, doc = (int)b;
             if (i < nv) {
-                if (a.cu) {
+                if (kDocs) {
                     int d = ms.doc_cursor;
                     while (d + 1 < a.ndocs && __ldg(a.cu + d + 1) <= t + i) ++d;
                     doc = d;
@@ -395,7 +401,7 @@ __global__ void __launch_bounds__(kThreads, 1) ssd_chunk_tc(const __grid_constan
             // the y store of chunk c-2 (staged in this group's scaled-X buffer) has read it
             if (mt == 0 && j >= 1) ptx::bulk_wait_read0();
             ptx::named_bar(nb, 128);
-            if (mt == Q - 1 && a.cu) ms.doc_cursor = doc;   // later chunks start in (or after) this document
+            if (kDocs && mt == Q - 1) ms.doc_cursor = doc;   // later chunks start in (or after) this document
             SegsumRow<4> row;
             segsum_phase1<4>(ms.seg, row, rb, lane);
             ptx::named_bar(nb, 128);
@@ -542,7 +548,7 @@ __global__ void __launch_bounds__(kThreads, 1) ssd_chunk_tc(const __grid_constan
         if (full_mode && a.nsplit > 1 && s > 0) {
 #pragma unroll
             for (int p = 0; p < P; ++p) S[p] = a.ws_state[uw * PN + (size_t)p * N + i];
-        } else if (s == 0 && a.init && !a.cu) {
+        } else if (!kDocs && s == 0 && a.init) {
 #pragma unroll
             for (int p = 0; p < P; ++p) S[p] = a.init[((size_t)b * a.H + h) * PN + (size_t)p * N + i];
         } else {
@@ -593,7 +599,7 @@ __global__ void __launch_bounds__(kThreads, 1) ssd_chunk_tc(const __grid_constan
             wait_or_fail(sh, a, &sh.metaFull[mb], (c / NMETA) & 1, kWhereMetaFull);
             const ChunkMeta& m = sh.meta[mb];
             // ---- packed documents that end inside this chunk: their final states
-            if (full_mode && a.fin && a.cu) {
+            if (full_mode && kDocs && a.fin) {
                 bool any = false;
                 for (int e = 0; e < nv - 1; ++e) any |= (m.rowflag[e] & 2) != 0;
                 if (any) {
@@ -698,10 +704,13 @@ cudaError_t launch_tc(const FwdArgs& a, cudaStream_t st) {
         !encode_4d(&prm.tm_C, a.C, N, a.G, a.L, a.batch) || !encode_4d(&prm.tm_y, a.y, P, a.H, a.L, a.batch))
         return cudaErrorInvalidValue;
     const size_t smem = tc_smem_bytes();
-    cudaError_t e = cudaFuncSetAttribute(ssd_chunk_tc, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    const bool full = a.mode == kModeFull, docs = a.cu != nullptr;
+    void (*kern)(TcParams) = full ? (docs ? ssd_chunk_tc<true, true> : ssd_chunk_tc<true, false>)
+                                  : (docs ? ssd_chunk_tc<false, true> : ssd_chunk_tc<false, false>);
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
     const int64_t grid = a.batch * a.H * a.nsplit;
-    ssd_chunk_tc<<<(unsigned)grid, kThreads, smem, st>>>(prm);
+    kern<<<(unsigned)grid, kThreads, smem, st>>>(prm);
     return cudaGetLastError();
 }
 
