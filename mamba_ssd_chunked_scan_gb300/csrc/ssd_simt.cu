@@ -210,18 +210,57 @@ __global__ void __launch_bounds__(256) ssd_chunk_simt(FwdArgs a) {
 // Composition of split aggregates, left to right per (row, head):
 // (tau_1, S_1) then (tau_2, S_2) -> (tau_1 + tau_2, exp(tau_2) S_1 + S_2).
 // In place: slot s receives the state entering split s.
+// Exclusive scan over the splits of one (row, head): the incoming state of
+// split s is the composition of the aggregates of splits 0..s-1 (affine steps
+// S -> exp(tau_s) S + agg_s).  One thread owns 4 consecutive state elements;
+// the loads of the next kDepth splits are issued before the current ones are
+// combined, so the sequential chain waits on arithmetic, not on memory.
+constexpr int kScanDepth = 8;
+
 __global__ void ssd_split_scan(const float* __restrict__ tau, float* __restrict__ state,
                                int64_t units_bh, int nsplit, int PN) {
+    const int PN4 = PN >> 2;
     const int64_t k = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
-    if (k >= units_bh * PN) return;
-    const int64_t bh = k / PN;
-    const int e = (int)(k % PN);
-    float run = 0.f;
-    for (int s = 0; s < nsplit; ++s) {
-        const int64_t uu = bh * nsplit + s;
-        const float agg = state[uu * PN + e];
-        state[uu * PN + e] = run;
-        run = fmaf(expf(tau[uu]), run, agg);
+    if (k >= units_bh * PN4) return;
+    const int64_t bh = k / PN4;
+    const int e4 = (int)(k % PN4);
+    float4* st = reinterpret_cast<float4*>(state) + bh * nsplit * (int64_t)PN4 + e4;
+    const float* tu = tau + bh * nsplit;
+    float4 cur[kScanDepth];
+    float ct[kScanDepth];
+#pragma unroll
+    for (int d = 0; d < kScanDepth; ++d) {
+        if (d < nsplit) {
+            cur[d] = st[(int64_t)d * PN4];
+            ct[d] = tu[d];
+        }
+    }
+    float4 run = make_float4(0.f, 0.f, 0.f, 0.f);
+    for (int s0 = 0; s0 < nsplit; s0 += kScanDepth) {
+        float4 nxt[kScanDepth];
+        float nt[kScanDepth];
+#pragma unroll
+        for (int d = 0; d < kScanDepth; ++d) {
+            const int sn = s0 + kScanDepth + d;
+            if (sn < nsplit) {
+                nxt[d] = st[(int64_t)sn * PN4];
+                nt[d] = tu[sn];
+            }
+        }
+#pragma unroll
+        for (int d = 0; d < kScanDepth; ++d) {
+            if (s0 + d < nsplit) {
+                st[(int64_t)(s0 + d) * PN4] = run;
+                const float e = expf(ct[d]);
+                run = make_float4(fmaf(e, run.x, cur[d].x), fmaf(e, run.y, cur[d].y), fmaf(e, run.z, cur[d].z),
+                                  fmaf(e, run.w, cur[d].w));
+            }
+        }
+#pragma unroll
+        for (int d = 0; d < kScanDepth; ++d) {
+            cur[d] = nxt[d];
+            ct[d] = nt[d];
+        }
     }
 }
 
@@ -282,8 +321,8 @@ cudaError_t launch_simt(const FwdArgs& a, cudaStream_t st) {
 }
 
 cudaError_t launch_split_scan(const FwdArgs& a, cudaStream_t st) {
-    const int PN = a.P * a.N;
-    const int64_t total = a.batch * a.H * (int64_t)PN;
+    const int PN = a.P * a.N;   // a multiple of 4: P * 4 bytes is a multiple of 16
+    const int64_t total = a.batch * a.H * (int64_t)(PN / 4);
     const int threads = 256;
     ssd_split_scan<<<(unsigned)((total + threads - 1) / threads), threads, 0, st>>>(
         a.ws_tau, a.ws_state, a.batch * a.H, a.nsplit, PN);
