@@ -72,6 +72,7 @@ int simt_chunk(const ssd_params_t* p) {
 // with their own initial states go to the SIMT kernel.
 bool use_tc(const ssd_params_t* p, bool has_init) {
     if (!tc_supported(p->headdim, p->dstate, p->chunk, p->dtype)) return false;
+    if (p->seqlen >= ((int64_t)1 << 31) - 256) return false;   // token indices are 32-bit TMA coordinates
     if (p->ndocs > 0 && has_init) return false;
     return true;
 }
@@ -179,6 +180,7 @@ int ssd_fwd(const ssd_params_t* p, const void* x, const float* dt, const float* 
     if (!workspace || workspace_bytes < need || !aligned(workspace, 256)) return SSD_ERR_WORKSPACE;
 
     const int ns = plan_nsplit(p);
+    if (p->batch * p->nheads * ns >= ((int64_t)1 << 31)) return SSD_ERR_UNSUPPORTED;   // units are 32-bit
     const WsLayout wl = ws_layout(p->batch, p->nheads, p->headdim, p->dstate, ns);
     FwdArgs a;
     memset(&a, 0, sizeof(a));
@@ -195,6 +197,9 @@ int ssd_fwd(const ssd_params_t* p, const void* x, const float* dt, const float* 
     a.ws_state = (float*)((char*)workspace + wl.state_off);
     cudaStream_t st = (cudaStream_t)stream;
 
+    fastdiv_consts((uint32_t)p->nheads, &a.divH_m, &a.divH_l);
+    fastdiv_consts((uint32_t)ns, &a.divS_m, &a.divS_l);
+    fastdiv_consts((uint32_t)(p->nheads / p->ngroups), &a.divHG_m, &a.divHG_l);
     const bool tc = use_tc(p, init != nullptr);
     a.Q = tc ? p->chunk : simt_chunk(p);
     if (a.Q == 0) return SSD_ERR_UNSUPPORTED;

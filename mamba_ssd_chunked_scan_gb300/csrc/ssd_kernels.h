@@ -33,7 +33,21 @@ struct FwdArgs {
     float* ws_tau;         // [batch * H * nsplit] natural-log split decays
     float* ws_state;       // [batch * H * nsplit * P * N] split states
     WsHeader* ws;
+    // n / H, n / nsplit and n / (H / G) for 0 <= n < 2^31 as (mulhi(m, n) + n) >> l
+    uint32_t divH_m, divH_l, divS_m, divS_l, divHG_m, divHG_l;
 };
+
+// Constants of division by an invariant divisor d >= 1 through one high
+// multiply and a shift (Granlund and Montgomery, "Division by Invariant
+// Integers using Multiplication", 1994): l = ceil(log2 d),
+// m = floor(2^32 (2^l - d) / d) + 1; then n / d = (mulhi(m, n) + n) >> l,
+// exact for 0 <= n < 2^31 (the sum cannot wrap).
+inline void fastdiv_consts(uint32_t d, uint32_t* m, uint32_t* l) {
+    uint32_t k = 0;
+    while ((1ull << k) < d) ++k;
+    *l = k;
+    *m = (uint32_t)((((1ull << k) - d) << 32) / d + 1);
+}
 
 size_t simt_smem_bytes(int Q, int P, int N);
 cudaError_t launch_simt(const FwdArgs& a, cudaStream_t st);

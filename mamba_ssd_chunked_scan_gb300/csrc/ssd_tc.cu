@@ -46,6 +46,7 @@ namespace {
 constexpr int Q = 128, P = 64, N = 128;
 constexpr int NMETA = 3;                     // per-chunk value buffers between the math groups
 constexpr int kPrefetch = 4;                 // chunks of L2 prefetch beyond the shared-memory stages
+constexpr int kPersistChunks = 4;            // units of at most this many chunks run on a persistent grid
 constexpr int kThreads = 512;
 constexpr int kRegsIssue = 56, kRegsMath = 152;   // 128 * (56 + 3 * 152) = 65536 = 512 * 128
 static_assert(128 * (kRegsIssue + 3 * kRegsMath) == kThreads * 128, "register split must equal the launch total");
@@ -192,13 +193,84 @@ __device__ __noinline__ void doc_end_states(TcSmall& sh, const ChunkMeta& m, con
     }
 }
 
+// A unit: batch row b, split s, head h (heads of one (row, split) are adjacent
+// in unit order, so CTAs that run at the same time share B and C in L2).
+struct Unit {
+    int b, h, g, s;
+    int t0, t1, nch;   // token range of the split (tokens < 2^31, as TMA coordinates are), its chunks
+};
+
+__device__ __forceinline__ uint32_t fdiv(uint32_t n, uint32_t m, uint32_t l) { return (__umulhi(m, n) + n) >> l; }
+
+__device__ __forceinline__ Unit unit_at(const FwdArgs& a, int64_t u64) {
+    // unit u = (b * nsplit + s) * H + h, below 2^31 (checked by the caller of the kernel)
+    const uint32_t u = (uint32_t)u64;
+    const uint32_t bs = fdiv(u, a.divH_m, a.divH_l);
+    const uint32_t bb = fdiv(bs, a.divS_m, a.divS_l);
+    Unit r;
+    r.h = (int)(u - bs * (uint32_t)a.H);
+    r.s = (int)(bs - bb * (uint32_t)a.nsplit);
+    r.b = (int)bb;
+    r.g = (int)fdiv((uint32_t)r.h, a.divHG_m, a.divHG_l);
+    r.t0 = r.s * (int)a.split_len;
+    r.t1 = (r.t0 + a.split_len < a.L) ? r.t0 + (int)a.split_len : (int)a.L;
+    r.nch = (r.t1 - r.t0 + Q - 1) / Q;
+    return r;
+}
+
+// Walks this CTA's items (unit, chunk) in order.  CTA k runs the units k,
+// k + gridDim.x, ...: with more units than SMs the grid is persistent (one CTA
+// per SM) and the pipeline runs on across unit boundaries, instead of paying a
+// CTA start and a pipeline ramp per unit.
+// (U = the number of units: a.batch * a.H * a.nsplit < 2^31.)  kPersist = false:
+// one unit per CTA, and the cursor never moves to another unit.
+template <bool kPersist>
+struct Cursor {
+    int u, c;
+    Unit un;
+    __device__ void init(const FwdArgs& a) {
+        u = (int)blockIdx.x;
+        c = 0;
+        un = unit_at(a, u);
+    }
+    __device__ __forceinline__ bool valid(int U) const { return u < U; }
+    __device__ __forceinline__ int t() const { return un.t0 + c * Q; }
+    __device__ void next(const FwdArgs& a, int U) {
+        if (++c >= un.nch) {
+            c = 0;
+            if (kPersist) {
+                u += (int)gridDim.x;
+                if (u < U) un = unit_at(a, u);
+            } else {
+                u = U;
+            }
+        }
+    }
+    // two items on (a unit may be a single chunk)
+    __device__ void next2(const FwdArgs& a, int U) {
+        c += 2;
+        if (!kPersist) {
+            if (c >= un.nch) u = U;
+            return;
+        }
+        while (c >= un.nch && u < U) {
+            c -= un.nch;
+            u += (int)gridDim.x;
+            if (u < U) un = unit_at(a, u);
+        }
+    }
+};
+
 // kFull: full pass (else the aggregate pass of a split plan); kDocs: packed
 // documents (cu_seqlens).  Each combination is its own kernel, so the hot
 // loops carry no run-time mode branches: the compiler would otherwise keep a
 // copy of a loop body per branch, and instruction fetch is a scarce resource
 // for this kernel (its warps run several different loops at once).
-template <bool kFull, bool kDocs>
+// kPersist: a persistent grid (one CTA per SM, each running several units),
+// used for short units, whose per-CTA start and pipeline ramp would dominate.
+template <bool kFull, bool kDocs, bool kPersist>
 __global__ void __launch_bounds__(kThreads, 1) ssd_chunk_tc(const __grid_constant__ TcParams prm) {
+    using Cursor = ssd::Cursor<kPersist>;
     extern __shared__ uint8_t smem_raw[];
     uint8_t* sm = (uint8_t*)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
     TcSmall& sh = *reinterpret_cast<TcSmall*>(sm + kTiles);
@@ -207,16 +279,14 @@ __global__ void __launch_bounds__(kThreads, 1) ssd_chunk_tc(const __grid_constan
     const int wg = warp >> 2;
     constexpr bool full_mode = kFull;
 
-    // unit: heads of one (row, split) are adjacent so they share B / C in L2
-    const int64_t u = blockIdx.x;
-    const int h = (int)(u % a.H);
-    const int s = (int)((u / a.H) % a.nsplit);
-    const int64_t b = u / ((int64_t)a.H * a.nsplit);
-    const int64_t uw = ((b * a.H) + h) * a.nsplit + s;   // workspace slot
-    const int g = h / (a.H / a.G);
-    const int64_t t0 = (int64_t)s * a.split_len;
-    const int64_t t1 = (t0 + a.split_len < a.L) ? t0 + a.split_len : a.L;
-    const int nch = (int)((t1 - t0 + Q - 1) / Q);
+    // items of this CTA: the chunks of units blockIdx.x, blockIdx.x + gridDim.x, ...
+    const int nunits = (int)(a.batch * a.H * a.nsplit);
+    int nch = 0;
+    if (kPersist) {
+        for (int u = (int)blockIdx.x; u < nunits; u += (int)gridDim.x) nch += unit_at(a, u).nch;
+    } else {
+        nch = unit_at(a, (int)blockIdx.x).nch;
+    }
 
     if (threadIdx.x == 0) {
         for (int i = 0; i < 2; ++i) {
@@ -239,9 +309,6 @@ __global__ void __launch_bounds__(kThreads, 1) ssd_chunk_tc(const __grid_constan
         for (int i = 0; i < 4; ++i) ptx::mbar_init(&sh.drain[i], 1);
         sh.abort = 0;
         sh.never = 0;
-        const int dc = kDocs ? find_doc_tc(a.cu, a.ndocs, t0) : 0;
-        sh.mask[0].doc_cursor = dc;
-        sh.mask[1].doc_cursor = dc;
         ptx::mbar_fence_init();
     }
     if (warp == 0 && lane == 0) {
@@ -261,25 +328,34 @@ __global__ void __launch_bounds__(kThreads, 1) ssd_chunk_tc(const __grid_constan
         if (warp == 0 && lane == 0) {
             // ============================================================ TMA producer
             int issued = 0;
-            // L2 prefetch runs kPrefetch chunks ahead of the two-stage shared-memory ring,
+            // L2 prefetch runs kPrefetch items ahead of the two-stage shared-memory ring,
             // so a stage refill finds its tiles in L2 instead of waiting on HBM
-            auto prefetch = [&](int c) {
-                if (c >= nch) return;
-                const int t = (int)(t0 + (int64_t)c * Q);
-                ptx::tma_prefetch_4d(&prm.tm_x, 0, h, t, (int)b);
-                ptx::tma_prefetch_4d(&prm.tm_B, 0, g, t, (int)b);
-                ptx::tma_prefetch_4d(&prm.tm_B, 64, g, t, (int)b);
+            auto prefetch = [&](const Cursor& k) {
+                if (!k.valid(nunits)) return;
+                const int t = k.t(), hh = k.un.h, gg = k.un.g, bb = k.un.b;
+                ptx::tma_prefetch_4d(&prm.tm_x, 0, hh, t, bb);
+                ptx::tma_prefetch_4d(&prm.tm_B, 0, gg, t, bb);
+                ptx::tma_prefetch_4d(&prm.tm_B, 64, gg, t, bb);
                 if (full_mode) {
-                    ptx::tma_prefetch_4d(&prm.tm_C, 0, g, t, (int)b);
-                    ptx::tma_prefetch_4d(&prm.tm_C, 64, g, t, (int)b);
+                    ptx::tma_prefetch_4d(&prm.tm_C, 0, gg, t, bb);
+                    ptx::tma_prefetch_4d(&prm.tm_C, 64, gg, t, bb);
                 }
             };
-            for (int c = 2; c < 2 + kPrefetch; ++c) prefetch(c);
-            for (int c = 0; c < nch; ++c) {
+            Cursor cl, cp;                         // the item loaded, the item prefetched
+            cl.init(a);
+            cp.init(a);
+            cp.next2(a, nunits);
+#pragma unroll 1
+            for (int k = 0; k < kPrefetch; ++k) {
+                prefetch(cp);
+                cp.next(a, nunits);
+            }
+            for (int c = 0; c < nch; ++c, cl.next(a, nunits)) {
                 const int st = c & 1;
-                prefetch(c + 2 + kPrefetch);
+                prefetch(cp);
+                cp.next(a, nunits);
                 if (c >= 2 && !wait_or_fail(sh, a, &sh.empty[st], ((c >> 1) - 1) & 1, kWhereEmpty)) break;
-                const int t = (int)(t0 + (int64_t)c * Q);
+                const int t = cl.t(), h = cl.un.h, g = cl.un.g, b = cl.un.b;
                 uint8_t* stg = sm + st * kStageBytes;
                 ptx::mbar_expect_tx(&sh.full[st], full_mode ? 81920u : 49152u);
                 if (full_mode) {
@@ -362,26 +438,36 @@ __global__ void __launch_bounds__(kThreads, 1) ssd_chunk_tc(const __grid_constan
         const int rb = warp & 3;                  // TMEM lane quarter = row block
         const int i = 32 * rb + lane;             // chunk row = TMEM lane
         const uint32_t lane_addr = tb + ((uint32_t)(32 * rb) << 16);
-        const float A2 = a.A[h] * kLog2e;
-        const float Dh = a.D ? a.D[h] : 0.f;
-        auto load_dt = [&](int c) -> float {
-            const int64_t t = t0 + (int64_t)c * Q;
-            return (c < nch && t + i < t1) ? __ldg(a.dt + ((size_t)b * a.L + t + i) * a.H + h) : 0.f;
+        auto load_dt = [&](const Cursor& k) -> float {
+            if (!k.valid(nunits)) return 0.f;
+            const int t = k.t();
+            return (t + i < k.un.t1) ? __ldg(a.dt + ((size_t)k.un.b * a.L + t + i) * a.H + k.un.h) : 0.f;
         };
-        float dt_next = load_dt(X);
+        Cursor cur;                               // this group's item
+        cur.init(a);
+        if (X) cur.next(a, nunits);
+        float dt_next = load_dt(cur);
+        int unit_prev = -1;
+        float A2 = 0.f, Dh = 0.f;
         for (int c = X; c < nch; c += 2) {
             const int j = c >> 1, mb = c % NMETA;
             uint8_t* stg = sm + X * kStageBytes;
-            const int64_t t = t0 + (int64_t)c * Q;
+            const int t = cur.t(), t1 = cur.un.t1, b = cur.un.b, h = cur.un.h;
             const int nv = (int)((t + Q < t1) ? Q : t1 - t);
+            const bool new_unit = cur.u != unit_prev;
+            if (new_unit) {
+                unit_prev = cur.u;
+                A2 = a.A[h] * kLog2e;
+                Dh = a.D ? a.D[h] : 0.f;
+            }
             const float dti = dt_next;
-            dt_next = load_dt(c + 2);
             if (c >= NMETA) wait_or_fail(sh, a, &sh.metaFree[mb], ((c / NMETA) - 1) & 1, kWhereMetaFree);
             // document boundaries: walk forward from this group's cursor
             int flag = 0, doc = (int)b;
             if (i < nv) {
                 if (kDocs) {
-                    int d = ms.doc_cursor;
+                    // (the cursor restarts with every unit this group enters)
+                    int d = new_unit ? find_doc_tc(a.cu, a.ndocs, t) : ms.doc_cursor;
                     while (d + 1 < a.ndocs && __ldg(a.cu + d + 1) <= t + i) ++d;
                     doc = d;
                     if (d > 0 && __ldg(a.cu + d) == t + i) flag |= 1;
@@ -533,6 +619,8 @@ __global__ void __launch_bounds__(kThreads, 1) ssd_chunk_tc(const __grid_constan
                     ptx::bulk_commit();
                 }
             }
+            cur.next2(a, nunits);                 // this group's next item, and its dt
+            dt_next = load_dt(cur);
             if (ptx::named_bar_any(nb, 128, *(volatile int*)&sh.abort != 0)) break;
         }
         if (mt == 0) ptx::bulk_wait0();
@@ -545,16 +633,19 @@ __global__ void __launch_bounds__(kThreads, 1) ssd_chunk_tc(const __grid_constan
         const uint32_t lane_addr = tb + ((uint32_t)(32 * rb) << 16);
         const size_t PN = (size_t)P * N;
         float S[P];
-        if (full_mode && a.nsplit > 1 && s > 0) {
+        // the state entering a unit: the composed state of the earlier splits, the
+        // caller's initial state, or zero
+        auto enter_state = [&](const Unit& un) {
+            const float* src = nullptr;
+            if (full_mode && a.nsplit > 1 && un.s > 0)
+                src = a.ws_state + (((size_t)un.b * a.H + un.h) * a.nsplit + un.s) * PN;
+            else if (!kDocs && un.s == 0 && a.init) src = a.init + ((size_t)un.b * a.H + un.h) * PN;
 #pragma unroll
-            for (int p = 0; p < P; ++p) S[p] = a.ws_state[uw * PN + (size_t)p * N + i];
-        } else if (!kDocs && s == 0 && a.init) {
-#pragma unroll
-            for (int p = 0; p < P; ++p) S[p] = a.init[((size_t)b * a.H + h) * PN + (size_t)p * N + i];
-        } else {
-#pragma unroll
-            for (int p = 0; p < P; ++p) S[p] = 0.f;
-        }
+            for (int p = 0; p < P; ++p) S[p] = src ? src[(size_t)p * N + i] : 0.f;
+        };
+        Cursor cs;
+        cs.init(a);
+        enter_state(cs.un);
         // incoming state as the bf16 operand of Yoff; then one thread issues Yoff(k)
         auto write_sin = [&]() {
             uint8_t* sin = sm + kSin;
@@ -594,8 +685,10 @@ __global__ void __launch_bounds__(kThreads, 1) ssd_chunk_tc(const __grid_constan
         for (int c = 0; c < nch; ++c) {
             const int X = c & 1, j = c >> 1, mb = c % NMETA;
             uint8_t* stg = sm + X * kStageBytes;
-            const int64_t t = t0 + (int64_t)c * Q;
+            const int t = cs.t(), t1 = cs.un.t1, h = cs.un.h;
+            const size_t uw = ((size_t)cs.un.b * a.H + h) * a.nsplit + cs.un.s;
             const int nv = (int)((t + Q < t1) ? Q : t1 - t);
+            const bool unit_end = cs.c == cs.un.nch - 1;
             wait_or_fail(sh, a, &sh.metaFull[mb], (c / NMETA) & 1, kWhereMetaFull);
             const ChunkMeta& m = sh.meta[mb];
             // ---- packed documents that end inside this chunk: their final states
@@ -634,6 +727,15 @@ __global__ void __launch_bounds__(kThreads, 1) ssd_chunk_tc(const __grid_constan
                 ptx::mbar_arrive(&sh.metaFree[mb]);
                 ptx::mbar_arrive(&sh.empty[X]);
             }
+            if (!full_mode && unit_end && !*(volatile int*)&sh.abort) {
+                // aggregate pass: the split's state summary and total decay
+#pragma unroll
+                for (int p = 0; p < P; ++p) a.ws_state[uw * PN + (size_t)p * N + i] = S[p];
+                if (mt == 0) a.ws_tau[uw] = tau_split * kLn2;
+                tau_split = 0.f;
+            }
+            cs.next(a, nunits);
+            if (unit_end && c + 1 < nch) enter_state(cs.un);   // the next unit starts
             if (full_mode && c + 1 < nch) {
                 // Yoff(c) has read the incoming-state tile: stage S_in(c+1), issue Yoff(c+1)
                 wait_or_fail(sh, a, &sh.barY[X], j & 1, kWhereBarY);
@@ -642,11 +744,6 @@ __global__ void __launch_bounds__(kThreads, 1) ssd_chunk_tc(const __grid_constan
                 if (mt == 0) issue_yoff(c + 1);
             }
             if (ptx::named_bar_any(kBarState, 128, *(volatile int*)&sh.abort != 0)) break;
-        }
-        if (!full_mode && !*(volatile int*)&sh.abort) {
-#pragma unroll
-            for (int p = 0; p < P; ++p) a.ws_state[uw * PN + (size_t)p * N + i] = S[p];
-            if (mt == 0) a.ws_tau[uw] = tau_split * kLn2;
         }
         if (mt == 0 && full_mode) {
             ptx::mma_commit(&sh.drain[2]);
@@ -705,11 +802,23 @@ cudaError_t launch_tc(const FwdArgs& a, cudaStream_t st) {
         return cudaErrorInvalidValue;
     const size_t smem = tc_smem_bytes();
     const bool full = a.mode == kModeFull, docs = a.cu != nullptr;
-    void (*kern)(TcParams) = full ? (docs ? ssd_chunk_tc<true, true> : ssd_chunk_tc<true, false>)
-                                  : (docs ? ssd_chunk_tc<false, true> : ssd_chunk_tc<false, false>);
+    // one CTA per unit; units of at most kPersistChunks chunks run on a persistent
+    // grid of at most one CTA per SM instead
+    int64_t grid = a.batch * a.H * a.nsplit;
+    int dev = 0, nsm = 0;
+    const bool persist = (a.split_len + Q - 1) / Q <= kPersistChunks && cudaGetDevice(&dev) == cudaSuccess &&
+                         cudaDeviceGetAttribute(&nsm, cudaDevAttrMultiProcessorCount, dev) == cudaSuccess &&
+                         nsm > 0 && grid > nsm;
+    if (persist) grid = nsm;
+    void (*kern)(TcParams);
+    if (persist)
+        kern = full ? (docs ? ssd_chunk_tc<true, true, true> : ssd_chunk_tc<true, false, true>)
+                    : (docs ? ssd_chunk_tc<false, true, true> : ssd_chunk_tc<false, false, true>);
+    else
+        kern = full ? (docs ? ssd_chunk_tc<true, true, false> : ssd_chunk_tc<true, false, false>)
+                    : (docs ? ssd_chunk_tc<false, true, false> : ssd_chunk_tc<false, false, false>);
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
-    const int64_t grid = a.batch * a.H * a.nsplit;
     kern<<<(unsigned)grid, kThreads, smem, st>>>(prm);
     return cudaGetLastError();
 }
