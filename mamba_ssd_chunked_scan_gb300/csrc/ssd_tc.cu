@@ -74,15 +74,36 @@ struct ChunkMeta {
     alignas(16) float dtv[Q];
     int rowflag[Q];              // bit0: a document starts at this token, bit1: one ends here
     int rowdoc[Q];               // state index (document, or batch row)
-    float tau;                   // whole-chunk log2-decay
+    float tau;                   // whole-chunk log2-decay (aggregate pass)
+    float tauexp;                // 2^tau
 };
 
 // Scratch of one mask group.
+// Segsum scratch of one mask group, in the linear domain: a_k = 2^{l_k}
+// (exactly 0 at a document start).  The hierarchy is that of "GPU Hierarchy
+// Meets Structured Matrices" (1-SS diagonal blocks of 32 rows grown from the
+// diagonal, rank-one off-diagonal blocks, no prefix subtraction) with every
+// sum of log-decays replaced by the product of the factors in the same order.
+// Products of factors in [0, 1] are monotone under rounding exactly as the
+// sums are, and the mask needs one exp2 per token instead of one per entry.
 struct MaskScratch {
-    SegsumShared<4> seg;
+    alignas(16) float alin[Q];     // a_k, read as float4
+    alignas(16) float colL[Q];     // 2^{seg(end of j's block, j)}, written as float4
     alignas(16) float dtv[Q];      // read as float4
-    alignas(16) float colfac[Q];   // read as float4
+    alignas(16) float colfac[Q];   // colL[j] dt_j, read as float4
+    float totL[4];                 // 2^{block total}
+    float rlastL[4];               // 2^{R[r]} of the chunk's last row
+    float totLog[4];               // block sums of the log2-decays (aggregate pass)
+    float tauL;                    // 2^{chunk total}
     int doc_cursor;
+};
+
+// Row values of one chunk that a mask-group thread carries from the segsum
+// to the scaled X tile, the mask and the epilogue (row i = 32 w + lane).
+struct MaskRow {
+    float wl[32];   // 2^{seg(i, 32 w + c)} for c <= lane, 0 above the diagonal
+    float rf[3];    // 2^{seg(i, end of block r)}, r < w
+    float pe;       // 2^{p_i}, the decay of the incoming state at row i
 };
 
 struct TcSmall {
@@ -99,9 +120,10 @@ struct TcSmall {
     int never;                     // stays 0: lets drain waits ignore the abort flag
 };
 
-static_assert(offsetof(MaskScratch, seg) == 0 && sizeof(MaskScratch) % 16 == 0, "segsum inputs are read as float4");
-static_assert(offsetof(MaskScratch, dtv) % 16 == 0 && offsetof(MaskScratch, colfac) % 16 == 0,
-              "vector-loaded arrays must be 16-byte aligned");
+static_assert(sizeof(MaskScratch) % 16 == 0, "mask scratch keeps 16-byte alignment");
+static_assert(offsetof(MaskScratch, alin) % 16 == 0 && offsetof(MaskScratch, colL) % 16 == 0 &&
+                  offsetof(MaskScratch, dtv) % 16 == 0 && offsetof(MaskScratch, colfac) % 16 == 0,
+              "vector-accessed arrays must be 16-byte aligned");
 static_assert(offsetof(TcSmall, meta) % 16 == 0 && sizeof(ChunkMeta) % 16 == 0, "meta alignment");
 static_assert(offsetof(TcSmall, full) % 8 == 0, "mbarriers are 8-byte aligned");
 static_assert(kTiles % 1024 == 0, "swizzled tiles start on 1024-byte boundaries");
@@ -478,26 +500,79 @@ __global__ void __launch_bounds__(kThreads, 1) ssd_chunk_tc(const __grid_constan
             }
             const float l2 = (flag & 1) ? -INFINITY : dti * A2;
             ChunkMeta& m = sh.meta[mb];
-            ms.seg.ell[i] = l2;
+            ms.alin[i] = ex2_approx(l2);          // 0 at a document start
             ms.dtv[i] = dti;
             m.ell[i] = l2;
             m.dtv[i] = dti;
             m.rowflag[i] = flag;
             m.rowdoc[i] = doc;
+            if (!full_mode) {
+                float ls = l2;                     // block sum of the log-decays (the split's tau)
+#pragma unroll
+                for (int o = 16; o > 0; o >>= 1) ls += __shfl_xor_sync(0xffffffffu, ls, o);
+                if (lane == 0) ms.totLog[rb] = ls;
+            }
+            ptx::named_bar(nb, 128);
+            if (kDocs && mt == Q - 1) ms.doc_cursor = doc;   // later chunks start in (or after) this document
+            MaskRow row;
+            // segsum phase 1: the diagonal 1-SS block, products grown leftwards from the diagonal
+            {
+                float e[32];
+                const float4* src = reinterpret_cast<const float4*>(ms.alin + 32 * rb);
+#pragma unroll
+                for (int q = 0; q < 8; ++q) {
+                    const float4 v = src[q];
+                    e[4 * q] = v.x;
+                    e[4 * q + 1] = v.y;
+                    e[4 * q + 2] = v.z;
+                    e[4 * q + 3] = v.w;
+                }
+                float r = 1.f;
+#pragma unroll
+                for (int c2 = 31; c2 >= 0; --c2) {
+                    if (c2 < lane) r *= e[c2 + 1];
+                    row.wl[c2] = (c2 <= lane) ? r : 0.f;
+                }
+                if (lane == 31) {
+                    float4* dst = reinterpret_cast<float4*>(ms.colL + 32 * rb);
+#pragma unroll
+                    for (int q = 0; q < 8; ++q)
+                        dst[q] = make_float4(row.wl[4 * q], row.wl[4 * q + 1], row.wl[4 * q + 2], row.wl[4 * q + 3]);
+                    ms.totL[rb] = row.wl[0] * e[0];
+                }
+            }
+            ptx::named_bar(nb, 128);
+            // segsum phase 2: row offsets into the earlier blocks and the chunk prefix
+            {
+                float acc = row.wl[0] * ms.alin[32 * rb];   // 2^{sum_{k=32w..i} l_k}
+#pragma unroll
+                for (int r = 2; r >= 0; --r) {
+                    if (r < rb) {
+                        row.rf[r] = acc;
+                        acc *= ms.totL[r];
+                    } else {
+                        row.rf[r] = 0.f;
+                    }
+                }
+                row.pe = acc;
+                if (rb == 3 && lane == 31) {
+#pragma unroll
+                    for (int r = 0; r < 3; ++r) ms.rlastL[r] = row.rf[r];
+                    ms.tauL = acc;
+                }
+            }
             // the y store of chunk c-2 (staged in this group's scaled-X buffer) has read it
             if (mt == 0 && j >= 1) ptx::bulk_wait_read0();
             ptx::named_bar(nb, 128);
-            if (kDocs && mt == Q - 1) ms.doc_cursor = doc;   // later chunks start in (or after) this document
-            SegsumRow<4> row;
-            segsum_phase1<4>(ms.seg, row, rb, lane);
-            ptx::named_bar(nb, 128);
-            segsum_phase2<4>(ms.seg, row, rb, lane);
-            ptx::named_bar(nb, 128);
-            ms.colfac[i] = ex2_approx(ms.seg.colS[i]) * dti;
-            const float xf = ex2_approx(segsum_chunk_suffix<4>(ms.seg, i)) * dti;
-            const float pe = ex2_approx(row.p);
+            const float cl = ms.colL[i];
+            ms.colfac[i] = cl * dti;
+            const float xf = ((rb == 3) ? cl : ms.rlastL[rb] * cl) * dti;   // 2^{s_i} dt_i
+            const float pe = row.pe;
             m.pexp[i] = pe;
-            if (mt == 0) m.tau = ms.seg.tau;
+            if (mt == 0) {
+                m.tauexp = ms.tauL;
+                if (!full_mode) m.tau = (ms.totLog[0] + ms.totLog[1]) + (ms.totLog[2] + ms.totLog[3]);
+            }
             __syncwarp();
             if (lane == 0) ptx::mbar_arrive(&sh.metaFull[mb]);
             // scaled X (state-summary operand): buffer X is free once dS(c-2) is done
@@ -532,8 +607,7 @@ __global__ void __launch_bounds__(kThreads, 1) ssd_chunk_tc(const __grid_constan
                 for (int r = 0; r < rb; ++r) {
                     uint32_t gr[32];
                     ptx::tmem_load32(gm + 32 * r, gr);
-                    const float Rr = (r == 0) ? row.R[0] : (r == 1) ? row.R[1] : row.R[2];
-                    const float rf = ex2_approx(Rr);
+                    const float rf = (r == 0) ? row.rf[0] : (r == 1) ? row.rf[1] : row.rf[2];
                     const float4* cf = reinterpret_cast<const float4*>(ms.colfac + 32 * r);
                     uint32_t pk[16];
 #pragma unroll
@@ -546,7 +620,8 @@ __global__ void __launch_bounds__(kThreads, 1) ssd_chunk_tc(const __grid_constan
                     }
                     ptx::tmem_st16(gm + 16 * r, pk);
                 }
-                // 1-SS diagonal block rb (running sums from the diagonal), plus D on the diagonal
+                // 1-SS diagonal block rb (products grown from the diagonal, 0 above it), plus D
+                // on the diagonal
                 {
                     uint32_t gr[32];
                     ptx::tmem_load32(gm + 32 * rb, gr);
@@ -559,10 +634,8 @@ __global__ void __launch_bounds__(kThreads, 1) ssd_chunk_tc(const __grid_constan
                         float mm[4];
 #pragma unroll
                         for (int e = 0; e < 4; ++e) {
-                            // every term computed, then masked: no divergent branches
                             const int col = 4 * q + e;
-                            const float v = __uint_as_float(gr[col]) * ex2_approx(row.d[col]);
-                            mm[e] = ((col <= lane) ? v : 0.f) * fv[e] + ((col == lane) ? Dh : 0.f);
+                            mm[e] = fmaf(__uint_as_float(gr[col]) * row.wl[col], fv[e], (col == lane) ? Dh : 0.f);
                         }
                         pk[2 * q] = pack_bf16(mm[0], mm[1]);
                         pk[2 * q + 1] = pack_bf16(mm[2], mm[3]);
@@ -709,9 +782,8 @@ __global__ void __launch_bounds__(kThreads, 1) ssd_chunk_tc(const __grid_constan
                 ptx::tc_fence_before();
                 __syncwarp();
                 if (lane == 0) ptx::mbar_arrive(&sh.dsFree);
-                const float tau2 = m.tau;
-                const float ed = ex2_approx(tau2);
-                tau_split += tau2;
+                const float ed = m.tauexp;
+                if (!full_mode) tau_split += m.tau;
 #pragma unroll
                 for (int q = 0; q < 32; ++q) S[q] = fmaf(ed, S[q], __uint_as_float(ds0[q]));
 #pragma unroll
