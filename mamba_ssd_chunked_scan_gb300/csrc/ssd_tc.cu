@@ -149,6 +149,11 @@ __device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
     __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
     return *reinterpret_cast<uint32_t*>(&v);
 }
+__device__ __forceinline__ uint32_t pack_bf16_2(uint64_t v) {
+    float lo, hi;
+    ptx::f2_unpack(v, lo, hi);
+    return pack_bf16(lo, hi);
+}
 __device__ __forceinline__ float bf16lo(uint32_t w) { return __uint_as_float(w << 16); }
 __device__ __forceinline__ float bf16hi(uint32_t w) { return __uint_as_float(w & 0xFFFF0000u); }
 
@@ -581,14 +586,15 @@ __global__ void __launch_bounds__(kThreads, 1) ssd_chunk_tc(const __grid_constan
             {
                 const uint8_t* xrow = stg + kTileX;
                 uint8_t* xt = sm + kXt + 16384 * X;
+                const uint64_t xf2 = ptx::f2_pack(xf, xf);
 #pragma unroll 2
                 for (int q = 0; q < 8; ++q) {
                     const uint4 v = *reinterpret_cast<const uint4*>(xrow + sw128_off(i, 8 * q));
                     uint4 o;
-                    o.x = pack_bf16(bf16lo(v.x) * xf, bf16hi(v.x) * xf);
-                    o.y = pack_bf16(bf16lo(v.y) * xf, bf16hi(v.y) * xf);
-                    o.z = pack_bf16(bf16lo(v.z) * xf, bf16hi(v.z) * xf);
-                    o.w = pack_bf16(bf16lo(v.w) * xf, bf16hi(v.w) * xf);
+                    o.x = pack_bf16_2(ptx::f2_mul(ptx::f2_pack(bf16lo(v.x), bf16hi(v.x)), xf2));
+                    o.y = pack_bf16_2(ptx::f2_mul(ptx::f2_pack(bf16lo(v.y), bf16hi(v.y)), xf2));
+                    o.z = pack_bf16_2(ptx::f2_mul(ptx::f2_pack(bf16lo(v.z), bf16hi(v.z)), xf2));
+                    o.w = pack_bf16_2(ptx::f2_mul(ptx::f2_pack(bf16lo(v.w), bf16hi(v.w)), xf2));
                     *reinterpret_cast<uint4*>(xt + sw128_off(i, 8 * q)) = o;
                 }
                 ptx::fence_proxy_async();
@@ -608,15 +614,17 @@ __global__ void __launch_bounds__(kThreads, 1) ssd_chunk_tc(const __grid_constan
                     uint32_t gr[32];
                     ptx::tmem_load32(gm + 32 * r, gr);
                     const float rf = (r == 0) ? row.rf[0] : (r == 1) ? row.rf[1] : row.rf[2];
+                    const uint64_t rf2 = ptx::f2_pack(rf, rf);
                     const float4* cf = reinterpret_cast<const float4*>(ms.colfac + 32 * r);
                     uint32_t pk[16];
 #pragma unroll
                     for (int q = 0; q < 8; ++q) {
                         const float4 f = cf[q];
-                        pk[2 * q] = pack_bf16(__uint_as_float(gr[4 * q]) * rf * f.x,
-                                              __uint_as_float(gr[4 * q + 1]) * rf * f.y);
-                        pk[2 * q + 1] = pack_bf16(__uint_as_float(gr[4 * q + 2]) * rf * f.z,
-                                                  __uint_as_float(gr[4 * q + 3]) * rf * f.w);
+                        const uint64_t g01 = ptx::f2_pack(__uint_as_float(gr[4 * q]), __uint_as_float(gr[4 * q + 1]));
+                        const uint64_t g23 =
+                            ptx::f2_pack(__uint_as_float(gr[4 * q + 2]), __uint_as_float(gr[4 * q + 3]));
+                        pk[2 * q] = pack_bf16_2(ptx::f2_mul(ptx::f2_mul(g01, rf2), ptx::f2_pack(f.x, f.y)));
+                        pk[2 * q + 1] = pack_bf16_2(ptx::f2_mul(ptx::f2_mul(g23, rf2), ptx::f2_pack(f.z, f.w)));
                     }
                     ptx::tmem_st16(gm + 16 * r, pk);
                 }
@@ -631,14 +639,15 @@ __global__ void __launch_bounds__(kThreads, 1) ssd_chunk_tc(const __grid_constan
                     for (int q = 0; q < 8; ++q) {
                         const float4 f = dv[q];
                         const float fv[4] = {f.x, f.y, f.z, f.w};
-                        float mm[4];
 #pragma unroll
-                        for (int e = 0; e < 4; ++e) {
+                        for (int e = 0; e < 4; e += 2) {
                             const int col = 4 * q + e;
-                            mm[e] = fmaf(__uint_as_float(gr[col]) * row.wl[col], fv[e], (col == lane) ? Dh : 0.f);
+                            const uint64_t gw = ptx::f2_mul(
+                                ptx::f2_pack(__uint_as_float(gr[col]), __uint_as_float(gr[col + 1])),
+                                ptx::f2_pack(row.wl[col], row.wl[col + 1]));
+                            const uint64_t dd = ptx::f2_pack((col == lane) ? Dh : 0.f, (col + 1 == lane) ? Dh : 0.f);
+                            pk[2 * q + e / 2] = pack_bf16_2(ptx::f2_fma(gw, ptx::f2_pack(fv[e], fv[e + 1]), dd));
                         }
-                        pk[2 * q] = pack_bf16(mm[0], mm[1]);
-                        pk[2 * q + 1] = pack_bf16(mm[2], mm[3]);
                     }
                     ptx::tmem_st16(gm + 16 * rb, pk);
                 }
@@ -676,10 +685,12 @@ __global__ void __launch_bounds__(kThreads, 1) ssd_chunk_tc(const __grid_constan
                         if (lane == 0) ptx::mbar_arrive(&sh.yFree[X]);
                     }
                     uint32_t ow[16];
+                    const uint64_t pe2 = ptx::f2_pack(pe, pe);
 #pragma unroll
                     for (int e = 0; e < 16; ++e)
-                        ow[e] = pack_bf16(fmaf(pe, __uint_as_float(yo[2 * e]), __uint_as_float(yd[2 * e])),
-                                          fmaf(pe, __uint_as_float(yo[2 * e + 1]), __uint_as_float(yd[2 * e + 1])));
+                        ow[e] = pack_bf16_2(ptx::f2_fma(
+                            pe2, ptx::f2_pack(__uint_as_float(yo[2 * e]), __uint_as_float(yo[2 * e + 1])),
+                            ptx::f2_pack(__uint_as_float(yd[2 * e]), __uint_as_float(yd[2 * e + 1]))));
 #pragma unroll
                     for (int q = 0; q < 4; ++q)
                         *reinterpret_cast<uint4*>(ys + sw128_off(i, 32 * q8 + 8 * q)) =
@@ -784,10 +795,17 @@ __global__ void __launch_bounds__(kThreads, 1) ssd_chunk_tc(const __grid_constan
                 if (lane == 0) ptx::mbar_arrive(&sh.dsFree);
                 const float ed = m.tauexp;
                 if (!full_mode) tau_split += m.tau;
+                const uint64_t ed2 = ptx::f2_pack(ed, ed);
 #pragma unroll
-                for (int q = 0; q < 32; ++q) S[q] = fmaf(ed, S[q], __uint_as_float(ds0[q]));
-#pragma unroll
-                for (int q = 0; q < 32; ++q) S[32 + q] = fmaf(ed, S[32 + q], __uint_as_float(ds1[q]));
+                for (int q = 0; q < 32; q += 2) {
+                    const uint64_t r0 = ptx::f2_fma(ed2, ptx::f2_pack(S[q], S[q + 1]),
+                                                    ptx::f2_pack(__uint_as_float(ds0[q]), __uint_as_float(ds0[q + 1])));
+                    ptx::f2_unpack(r0, S[q], S[q + 1]);
+                    const uint64_t r1 = ptx::f2_fma(
+                        ed2, ptx::f2_pack(S[32 + q], S[33 + q]),
+                        ptx::f2_pack(__uint_as_float(ds1[q]), __uint_as_float(ds1[q + 1])));
+                    ptx::f2_unpack(r1, S[32 + q], S[33 + q]);
+                }
             }
             if (full_mode && a.fin && (m.rowflag[nv - 1] & 2)) {
                 float* fo = a.fin + ((size_t)m.rowdoc[nv - 1] * a.H + h) * PN + i;
