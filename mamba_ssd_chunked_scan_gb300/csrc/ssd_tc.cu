@@ -157,7 +157,7 @@ __device__ __forceinline__ uint32_t pack_bf16_2(uint64_t v) {
 __device__ __forceinline__ float bf16lo(uint32_t w) { return __uint_as_float(w << 16); }
 __device__ __forceinline__ float bf16hi(uint32_t w) { return __uint_as_float(w & 0xFFFF0000u); }
 
-__device__ __noinline__ void fail(TcSmall& sh, const FwdArgs& a, uint32_t where) {
+__device__ __forceinline__ void fail(TcSmall& sh, const FwdArgs& a, uint32_t where) {
     record_error(a.ws, SSD_ERR_TIMEOUT, where);
     *(volatile int*)&sh.abort = 1;
 }
