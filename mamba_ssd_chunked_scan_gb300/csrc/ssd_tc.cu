@@ -48,8 +48,12 @@ constexpr int NMETA = 3;                     // per-chunk value buffers between 
 constexpr int kPrefetch = 4;                 // chunks of L2 prefetch beyond the shared-memory stages
 constexpr int kPersistChunks = 4;            // units of at most this many chunks run on a persistent grid
 constexpr int kThreads = 512;
+// setmaxnreg budgets (issue warpgroup, each math warpgroup); the persistent grid's
+// unit bookkeeping needs more registers in the issue warpgroup
 constexpr int kRegsIssue = 56, kRegsMath = 152;   // 128 * (56 + 3 * 152) = 65536 = 512 * 128
+constexpr int kRegsIssueP = 72, kRegsMathP = 144;   // 128 * (72 + 3 * 144) = 64512 <= 65536
 static_assert(128 * (kRegsIssue + 3 * kRegsMath) == kThreads * 128, "register split must equal the launch total");
+static_assert(128 * (kRegsIssueP + 3 * kRegsMathP) <= kThreads * 128, "register split must fit the launch total");
 constexpr uint32_t kTileC = 0, kTileB = 32768, kTileX = 65536, kStageBytes = 81920;
 constexpr uint32_t kXt = 2 * kStageBytes;    // scaled X for the state summary, two buffers
 constexpr uint32_t kSin = kXt + 2 * 16384;   // incoming state, bf16, (n rows, p)
@@ -351,7 +355,7 @@ __global__ void __launch_bounds__(kThreads, 1) ssd_chunk_tc(const __grid_constan
     const uint32_t tb = sh.tmem_base;
 
     if (wg == 0) {
-        ptx::regs_dec<kRegsIssue>();
+        ptx::regs_dec<(kPersist ? kRegsIssueP : kRegsIssue)>();
         if (warp == 0 && lane == 0) {
             // ============================================================ TMA producer
             int issued = 0;
@@ -457,7 +461,7 @@ __global__ void __launch_bounds__(kThreads, 1) ssd_chunk_tc(const __grid_constan
         }
     } else if (wg <= 2) {
         // ================================================================ mask groups
-        ptx::regs_inc<kRegsMath>();
+        ptx::regs_inc<(kPersist ? kRegsMathP : kRegsMath)>();
         const int X = wg - 1;                     // this group takes chunks c with c & 1 == X
         const int nb = kBarMask0 + X;
         MaskScratch& ms = sh.mask[X];
@@ -710,7 +714,7 @@ __global__ void __launch_bounds__(kThreads, 1) ssd_chunk_tc(const __grid_constan
         if (mt == 0) ptx::bulk_wait0();
     } else {
         // ================================================================ state group
-        ptx::regs_inc<kRegsMath>();
+        ptx::regs_inc<(kPersist ? kRegsMathP : kRegsMath)>();
         const int mt = threadIdx.x - 384;         // 0..127
         const int rb = warp & 3;
         const int i = 32 * rb + lane;             // TMEM lane = state column n
@@ -909,6 +913,12 @@ cudaError_t launch_tc(const FwdArgs& a, cudaStream_t st) {
                     : (docs ? ssd_chunk_tc<false, true, false> : ssd_chunk_tc<false, false, false>);
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
+    // setmaxnreg.inc draws on the registers the CTA was launched with: the warpgroup
+    // budgets must fit that pool, or the increase would wait forever
+    cudaFuncAttributes fa;
+    if ((e = cudaFuncGetAttributes(&fa, kern)) != cudaSuccess) return e;
+    const int need = persist ? kRegsIssueP + 3 * kRegsMathP : kRegsIssue + 3 * kRegsMath;
+    if (fa.numRegs * 4 < need) return cudaErrorInvalidConfiguration;
     kern<<<(unsigned)grid, kThreads, smem, st>>>(prm);
     return cudaGetLastError();
 }
