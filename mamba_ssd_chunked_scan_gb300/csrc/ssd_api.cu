@@ -77,6 +77,47 @@ bool use_tc(const ssd_params_t* p, bool has_init) {
     return true;
 }
 
+// Leftover-unit plan for the tensor-core kernel with one split.  One CTA runs
+// one (row, head) unit, so U units on S SMs run in ceil(U / S) waves, and when
+// U % S is small the last wave keeps most SMs idle for a whole unit (640 units
+// on 152 SMs: the fifth wave holds 32).  Instead the T = U % S leftover units
+// are cut into m pieces each ("GPU Hierarchy Meets Structured Matrices": the
+// split-sequence algorithm): their split aggregates, the composition, then one
+// full launch of the whole units followed by the pieces, so the last wave is
+// about 1 / m of a unit long.
+struct TailPlan {
+    int T = 0, m = 0;
+    int64_t split_len = 0;
+};
+
+bool plan_tail(const ssd_params_t* p, TailPlan* tp) {
+    if (!tc_supported(p->headdim, p->dstate, p->chunk, p->dtype)) return false;
+    if (plan_nsplit(p) != 1) return false;
+    int dev = 0, nsm = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&nsm, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || nsm < 2) {
+        cudaGetLastError();   // no device here: no plan
+        return false;
+    }
+    const int64_t units = p->batch * p->nheads;
+    const int64_t T = units % nsm;
+    const int64_t nch = (p->seqlen + p->chunk - 1) / p->chunk;
+    if (units < nsm || T == 0 || nch < 4) return false;
+    int64_t m = nsm / T;
+    if (m > 8) m = 8;
+    if (m > nch / 2) m = nch / 2;   // pieces of at least 2 chunks
+    if (m < 2) return false;
+    tp->split_len = (nch + m - 1) / m * p->chunk;
+    tp->m = (int)((p->seqlen + tp->split_len - 1) / tp->split_len);
+    tp->T = (int)T;
+    return tp->m >= 2;
+}
+
+WsLayout layout_for(const ssd_params_t* p, int ns, const TailPlan& tp) {
+    if (tp.T > 0) return ws_layout(1, tp.T, p->headdim, p->dstate, tp.m);   // T * m pieces
+    return ws_layout(p->batch, p->nheads, p->headdim, p->dstate, ns);
+}
+
 }  // namespace
 
 // ---------------------------------------------------------------------------
@@ -131,14 +172,18 @@ const char* ssd_status_string(int s) {
 size_t ssd_fwd_workspace_size(const ssd_params_t* p) {
     if (check_params(p) != SSD_OK) return 0;
     const int ns = plan_nsplit(p);
-    return ws_layout(p->batch, p->nheads, p->headdim, p->dstate, ns).total;
+    TailPlan tp;
+    plan_tail(p, &tp);
+    return layout_for(p, ns, tp).total;
 }
 
 int ssd_fwd_plan(const ssd_params_t* p, int has_init, int has_final, int* launches, int* nsplits) {
     (void)has_final;
     if (check_params(p) != SSD_OK) return -1;
     const int ns = plan_nsplit(p);
-    if (launches) *launches = (ns > 1) ? 3 : 1;
+    TailPlan tp;
+    const bool tail = use_tc(p, has_init != 0) && plan_tail(p, &tp);
+    if (launches) *launches = (ns > 1 || tail) ? 3 : 1;
     if (nsplits) *nsplits = ns;
     return use_tc(p, has_init != 0) ? 1 : 0;
 }
@@ -181,7 +226,9 @@ int ssd_fwd(const ssd_params_t* p, const void* x, const float* dt, const float* 
 
     const int ns = plan_nsplit(p);
     if (p->batch * p->nheads * ns >= ((int64_t)1 << 31)) return SSD_ERR_UNSUPPORTED;   // units are 32-bit
-    const WsLayout wl = ws_layout(p->batch, p->nheads, p->headdim, p->dstate, ns);
+    TailPlan tp;
+    plan_tail(p, &tp);
+    const WsLayout wl = layout_for(p, ns, tp);
     FwdArgs a;
     memset(&a, 0, sizeof(a));
     a.batch = p->batch; a.L = p->seqlen;
@@ -204,6 +251,27 @@ int ssd_fwd(const ssd_params_t* p, const void* x, const float* dt, const float* 
     a.Q = tc ? p->chunk : simt_chunk(p);
     if (a.Q == 0) return SSD_ERR_UNSUPPORTED;
     auto launch = [&](const FwdArgs& aa) { return tc ? launch_tc(aa, st) : launch_simt(aa, st); };
+    if (tc && tp.T > 0) {
+        // leftover-unit plan: aggregates of the pieces, their composition, then the
+        // whole units and the pieces in one launch
+        const int64_t units = p->batch * p->nheads;
+        a.nsplit = tp.m;
+        a.split_len = tp.split_len;
+        a.tail_units = tp.T;
+        a.tail_first = units - tp.T;
+        fastdiv_consts((uint32_t)tp.m, &a.divS_m, &a.divS_l);
+        a.mode = kModeAggregate;
+        a.grid_units = (int64_t)tp.T * tp.m;
+        if (launch(a) != cudaSuccess) return SSD_ERR_CUDA;
+        FwdArgs sa = a;   // the scan runs over T "rows" of m splits
+        sa.batch = 1;
+        sa.H = tp.T;
+        if (launch_split_scan(sa, st) != cudaSuccess) return SSD_ERR_CUDA;
+        a.mode = kModeFull;
+        a.grid_units = a.tail_first + (int64_t)tp.T * tp.m;
+        if (launch(a) != cudaSuccess) return SSD_ERR_CUDA;
+        return SSD_OK;
+    }
     if (ns > 1) {
         a.mode = kModeAggregate;
         if (launch(a) != cudaSuccess) return SSD_ERR_CUDA;

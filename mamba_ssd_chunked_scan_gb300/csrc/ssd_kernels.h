@@ -35,6 +35,12 @@ struct FwdArgs {
     WsHeader* ws;
     // n / H, n / nsplit and n / (H / G) for 0 <= n < 2^31 as (mulhi(m, n) + n) >> l
     uint32_t divH_m, divH_l, divS_m, divS_l, divHG_m, divHG_l;
+    // leftover-unit plan (tail_units > 0, one split otherwise): the (row, head) units
+    // [0, tail_first) run whole, the last tail_units are cut into nsplit pieces of
+    // split_len tokens; grid_units = CTAs of this launch (0: batch * H * nsplit)
+    int tail_units;
+    int64_t tail_first;
+    int64_t grid_units;
 };
 
 // Constants of division by an invariant divisor d >= 1 through one high

@@ -48,12 +48,10 @@ constexpr int NMETA = 3;                     // per-chunk value buffers between 
 constexpr int kPrefetch = 4;                 // chunks of L2 prefetch beyond the shared-memory stages
 constexpr int kPersistChunks = 4;            // units of at most this many chunks run on a persistent grid
 constexpr int kThreads = 512;
-// setmaxnreg budgets (issue warpgroup, each math warpgroup); the persistent grid's
-// unit bookkeeping needs more registers in the issue warpgroup
-constexpr int kRegsIssue = 56, kRegsMath = 152;   // 128 * (56 + 3 * 152) = 65536 = 512 * 128
-constexpr int kRegsIssueP = 72, kRegsMathP = 144;   // 128 * (72 + 3 * 144) = 64512 <= 65536
-static_assert(128 * (kRegsIssue + 3 * kRegsMath) == kThreads * 128, "register split must equal the launch total");
-static_assert(128 * (kRegsIssueP + 3 * kRegsMathP) <= kThreads * 128, "register split must fit the launch total");
+// setmaxnreg budgets: issue warpgroup (unit bookkeeping of the producer, MMA
+// issue) and each math warpgroup
+constexpr int kRegsIssue = 72, kRegsMath = 144;   // 128 * (72 + 3 * 144) = 64512 <= 65536 = 512 * 128
+static_assert(128 * (kRegsIssue + 3 * kRegsMath) <= kThreads * 128, "register split must fit the launch total");
 constexpr uint32_t kTileC = 0, kTileB = 32768, kTileX = 65536, kStageBytes = 81920;
 constexpr uint32_t kXt = 2 * kStageBytes;    // scaled X for the state summary, two buffers
 constexpr uint32_t kSin = kXt + 2 * 16384;   // incoming state, bf16, (n rows, p)
@@ -229,22 +227,50 @@ __device__ __noinline__ void doc_end_states(TcSmall& sh, const ChunkMeta& m, con
 struct Unit {
     int b, h, g, s;
     int t0, t1, nch;   // token range of the split (tokens < 2^31, as TMA coordinates are), its chunks
+    int ws;            // workspace slot of a split (a whole unit has none)
 };
 
 __device__ __forceinline__ uint32_t fdiv(uint32_t n, uint32_t m, uint32_t l) { return (__umulhi(m, n) + n) >> l; }
 
+template <bool kFull>
 __device__ __forceinline__ Unit unit_at(const FwdArgs& a, int64_t u64) {
-    // unit u = (b * nsplit + s) * H + h, below 2^31 (checked by the caller of the kernel)
     const uint32_t u = (uint32_t)u64;
-    const uint32_t bs = fdiv(u, a.divH_m, a.divH_l);
-    const uint32_t bb = fdiv(bs, a.divS_m, a.divS_l);
     Unit r;
-    r.h = (int)(u - bs * (uint32_t)a.H);
-    r.s = (int)(bs - bb * (uint32_t)a.nsplit);
-    r.b = (int)bb;
+    if (a.tail_units > 0) {
+        // leftover-unit plan: whole (row, head) units first (full pass only), then the
+        // pieces: leftover unit t, split s at index tail_first + t * nsplit + s
+        if (kFull && u < (uint32_t)a.tail_first) {
+            const uint32_t bb = fdiv(u, a.divH_m, a.divH_l);
+            r.h = (int)(u - bb * (uint32_t)a.H);
+            r.b = (int)bb;
+            r.s = 0;
+            r.ws = -1;
+            r.t0 = 0;
+            r.t1 = (int)a.L;
+        } else {
+            const uint32_t v = kFull ? u - (uint32_t)a.tail_first : u;
+            const uint32_t t = fdiv(v, a.divS_m, a.divS_l);
+            const uint32_t unit = (uint32_t)a.tail_first + t;
+            const uint32_t bb = fdiv(unit, a.divH_m, a.divH_l);
+            r.h = (int)(unit - bb * (uint32_t)a.H);
+            r.b = (int)bb;
+            r.s = (int)(v - t * (uint32_t)a.nsplit);
+            r.ws = (int)v;
+            r.t0 = r.s * (int)a.split_len;
+            r.t1 = (r.t0 + a.split_len < a.L) ? r.t0 + (int)a.split_len : (int)a.L;
+        }
+    } else {
+        // unit u = (b * nsplit + s) * H + h, below 2^31 (checked by the caller of the kernel)
+        const uint32_t bs = fdiv(u, a.divH_m, a.divH_l);
+        const uint32_t bb = fdiv(bs, a.divS_m, a.divS_l);
+        r.h = (int)(u - bs * (uint32_t)a.H);
+        r.s = (int)(bs - bb * (uint32_t)a.nsplit);
+        r.b = (int)bb;
+        r.ws = (int)(((uint32_t)r.b * (uint32_t)a.H + (uint32_t)r.h) * (uint32_t)a.nsplit + (uint32_t)r.s);
+        r.t0 = r.s * (int)a.split_len;
+        r.t1 = (r.t0 + a.split_len < a.L) ? r.t0 + (int)a.split_len : (int)a.L;
+    }
     r.g = (int)fdiv((uint32_t)r.h, a.divHG_m, a.divHG_l);
-    r.t0 = r.s * (int)a.split_len;
-    r.t1 = (r.t0 + a.split_len < a.L) ? r.t0 + (int)a.split_len : (int)a.L;
     r.nch = (r.t1 - r.t0 + Q - 1) / Q;
     return r;
 }
@@ -255,14 +281,14 @@ __device__ __forceinline__ Unit unit_at(const FwdArgs& a, int64_t u64) {
 // CTA start and a pipeline ramp per unit.
 // (U = the number of units: a.batch * a.H * a.nsplit < 2^31.)  kPersist = false:
 // one unit per CTA, and the cursor never moves to another unit.
-template <bool kPersist>
+template <bool kFull, bool kPersist>
 struct Cursor {
     int u, c;
     Unit un;
     __device__ void init(const FwdArgs& a) {
         u = (int)blockIdx.x;
         c = 0;
-        un = unit_at(a, u);
+        un = unit_at<kFull>(a, u);
     }
     __device__ __forceinline__ bool valid(int U) const { return u < U; }
     __device__ __forceinline__ int t() const { return un.t0 + c * Q; }
@@ -271,7 +297,7 @@ struct Cursor {
             c = 0;
             if (kPersist) {
                 u += (int)gridDim.x;
-                if (u < U) un = unit_at(a, u);
+                if (u < U) un = unit_at<kFull>(a, u);
             } else {
                 u = U;
             }
@@ -287,7 +313,7 @@ struct Cursor {
         while (c >= un.nch && u < U) {
             c -= un.nch;
             u += (int)gridDim.x;
-            if (u < U) un = unit_at(a, u);
+            if (u < U) un = unit_at<kFull>(a, u);
         }
     }
 };
@@ -301,7 +327,7 @@ struct Cursor {
 // used for short units, whose per-CTA start and pipeline ramp would dominate.
 template <bool kFull, bool kDocs, bool kPersist>
 __global__ void __launch_bounds__(kThreads, 1) ssd_chunk_tc(const __grid_constant__ TcParams prm) {
-    using Cursor = ssd::Cursor<kPersist>;
+    using Cursor = ssd::Cursor<kFull, kPersist>;
     extern __shared__ uint8_t smem_raw[];
     uint8_t* sm = (uint8_t*)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
     TcSmall& sh = *reinterpret_cast<TcSmall*>(sm + kTiles);
@@ -314,9 +340,9 @@ __global__ void __launch_bounds__(kThreads, 1) ssd_chunk_tc(const __grid_constan
     const int nunits = (int)(a.batch * a.H * a.nsplit);
     int nch = 0;
     if (kPersist) {
-        for (int u = (int)blockIdx.x; u < nunits; u += (int)gridDim.x) nch += unit_at(a, u).nch;
+        for (int u = (int)blockIdx.x; u < nunits; u += (int)gridDim.x) nch += unit_at<kFull>(a, u).nch;
     } else {
-        nch = unit_at(a, (int)blockIdx.x).nch;
+        nch = unit_at<kFull>(a, (int)blockIdx.x).nch;
     }
 
     if (threadIdx.x == 0) {
@@ -355,7 +381,7 @@ __global__ void __launch_bounds__(kThreads, 1) ssd_chunk_tc(const __grid_constan
     const uint32_t tb = sh.tmem_base;
 
     if (wg == 0) {
-        ptx::regs_dec<(kPersist ? kRegsIssueP : kRegsIssue)>();
+        ptx::regs_dec<kRegsIssue>();
         if (warp == 0 && lane == 0) {
             // ============================================================ TMA producer
             int issued = 0;
@@ -461,7 +487,7 @@ __global__ void __launch_bounds__(kThreads, 1) ssd_chunk_tc(const __grid_constan
         }
     } else if (wg <= 2) {
         // ================================================================ mask groups
-        ptx::regs_inc<(kPersist ? kRegsMathP : kRegsMath)>();
+        ptx::regs_inc<kRegsMath>();
         const int X = wg - 1;                     // this group takes chunks c with c & 1 == X
         const int nb = kBarMask0 + X;
         MaskScratch& ms = sh.mask[X];
@@ -714,7 +740,7 @@ __global__ void __launch_bounds__(kThreads, 1) ssd_chunk_tc(const __grid_constan
         if (mt == 0) ptx::bulk_wait0();
     } else {
         // ================================================================ state group
-        ptx::regs_inc<(kPersist ? kRegsMathP : kRegsMath)>();
+        ptx::regs_inc<kRegsMath>();
         const int mt = threadIdx.x - 384;         // 0..127
         const int rb = warp & 3;
         const int i = 32 * rb + lane;             // TMEM lane = state column n
@@ -725,8 +751,7 @@ __global__ void __launch_bounds__(kThreads, 1) ssd_chunk_tc(const __grid_constan
         // caller's initial state, or zero
         auto enter_state = [&](const Unit& un) {
             const float* src = nullptr;
-            if (full_mode && a.nsplit > 1 && un.s > 0)
-                src = a.ws_state + (((size_t)un.b * a.H + un.h) * a.nsplit + un.s) * PN;
+            if (full_mode && a.nsplit > 1 && un.s > 0) src = a.ws_state + (size_t)un.ws * PN;
             else if (!kDocs && un.s == 0 && a.init) src = a.init + ((size_t)un.b * a.H + un.h) * PN;
 #pragma unroll
             for (int p = 0; p < P; ++p) S[p] = src ? src[(size_t)p * N + i] : 0.f;
@@ -774,7 +799,7 @@ __global__ void __launch_bounds__(kThreads, 1) ssd_chunk_tc(const __grid_constan
             const int X = c & 1, j = c >> 1, mb = c % NMETA;
             uint8_t* stg = sm + X * kStageBytes;
             const int t = cs.t(), t1 = cs.un.t1, h = cs.un.h;
-            const size_t uw = ((size_t)cs.un.b * a.H + h) * a.nsplit + cs.un.s;
+            const size_t uw = (size_t)cs.un.ws;
             const int nv = (int)((t + Q < t1) ? Q : t1 - t);
             const bool unit_end = cs.c == cs.un.nch - 1;
             wait_or_fail(sh, a, &sh.metaFull[mb], (c / NMETA) & 1, kWhereMetaFull);
@@ -898,9 +923,10 @@ cudaError_t launch_tc(const FwdArgs& a, cudaStream_t st) {
     const bool full = a.mode == kModeFull, docs = a.cu != nullptr;
     // one CTA per unit; units of at most kPersistChunks chunks run on a persistent
     // grid of at most one CTA per SM instead
-    int64_t grid = a.batch * a.H * a.nsplit;
+    int64_t grid = a.grid_units > 0 ? a.grid_units : a.batch * a.H * a.nsplit;
     int dev = 0, nsm = 0;
-    const bool persist = (a.split_len + Q - 1) / Q <= kPersistChunks && cudaGetDevice(&dev) == cudaSuccess &&
+    const bool persist = a.tail_units == 0 && (a.split_len + Q - 1) / Q <= kPersistChunks &&
+                         cudaGetDevice(&dev) == cudaSuccess &&
                          cudaDeviceGetAttribute(&nsm, cudaDevAttrMultiProcessorCount, dev) == cudaSuccess &&
                          nsm > 0 && grid > nsm;
     if (persist) grid = nsm;
@@ -917,7 +943,7 @@ cudaError_t launch_tc(const FwdArgs& a, cudaStream_t st) {
     // budgets must fit that pool, or the increase would wait forever
     cudaFuncAttributes fa;
     if ((e = cudaFuncGetAttributes(&fa, kern)) != cudaSuccess) return e;
-    const int need = persist ? kRegsIssueP + 3 * kRegsMathP : kRegsIssue + 3 * kRegsMath;
+    const int need = kRegsIssue + 3 * kRegsMath;
     if (fa.numRegs * 4 < need) return cudaErrorInvalidConfiguration;
     kern<<<(unsigned)grid, kThreads, smem, st>>>(prm);
     return cudaGetLastError();
