@@ -115,8 +115,9 @@ SSD_API int ssd_fwd(const ssd_params_t* p,
  * the workspace is a library-owned device array of 8 MiB that every GPU
  * loading the library reserves until process exit.  Problems whose
  * ssd_fwd_workspace_size() exceeds 8 MiB are rejected with
- * SSD_ERR_WORKSPACE before anything is launched; single-split problems only
- * need 256 bytes.  The caller still passes all inputs and outputs.
+ * SSD_ERR_WORKSPACE before anything is launched; single-split problems need
+ * at most 256 bytes plus 4 MiB (the states of the pieces the leftover-unit
+ * plan cuts the last wave's units into).  The caller still passes all inputs and outputs.
  * The first call on a device looks up the array's device address with that
  * device current (cudaGetSymbolAddress); make that first call before any
  * stream capture.  Every call uses the same array: calls whose GPU work

@@ -85,6 +85,8 @@ bool use_tc(const ssd_params_t* p, bool has_init) {
 // split-sequence algorithm): their split aggregates, the composition, then one
 // full launch of the whole units followed by the pieces, so the last wave is
 // about 1 / m of a unit long.
+constexpr int64_t kTailStateBytes = (int64_t)4 << 20;
+
 struct TailPlan {
     int T = 0, m = 0;
     int64_t split_len = 0;
@@ -106,6 +108,10 @@ bool plan_tail(const ssd_params_t* p, TailPlan* tp) {
     int64_t m = nsm / T;
     if (m > 8) m = 8;
     if (m > nch / 2) m = nch / 2;   // pieces of at least 2 chunks
+    // keep the pieces' states within 4 MiB of workspace (so the library-owned
+    // scratch of ssd_fwd_static_scratch covers every one-split problem)
+    const int64_t state_bytes = (int64_t)p->headdim * p->dstate * 4;
+    while (m >= 2 && T * m * state_bytes > kTailStateBytes) --m;
     if (m < 2) return false;
     tp->split_len = (nch + m - 1) / m * p->chunk;
     tp->m = (int)((p->seqlen + tp->split_len - 1) / tp->split_len);
