@@ -14,7 +14,7 @@ using namespace ssd;
 namespace {
 
 constexpr int kSmemLimit = 227 * 1024;
-constexpr int64_t kAutoTargetUnits = 2 * 152;   // independent (row, head, split) units wanted
+constexpr int64_t kAutoSMs = 152;   // SMs the automatic split plan fills (GB300)
 
 bool aligned(const void* p, size_t a) { return ((uintptr_t)p % a) == 0; }
 
@@ -37,19 +37,40 @@ int check_params(const ssd_params_t* p) {
     return SSD_OK;
 }
 
+// Automatic split plan (split_len = 0).  With at least as many (row, head)
+// units as SMs there is one split (the leftover-unit plan evens out the last
+// wave).  Otherwise each sequence is cut into n splits of at least 4 chunks:
+// the smallest n in [ceil(S / units), 4 S / units] whose units fill their waves
+// to at least 95 %, else the n with the best fill.  (Fewer splits means less
+// boundary-state traffic; a part-empty last wave idles SMs for a whole split.)
 int64_t plan_split_len(const ssd_params_t* p) {
     const int64_t L = p->seqlen;
     int64_t sl = p->split_len;
     if (sl == 0) {
         const int64_t bh = p->batch * p->nheads;
-        if (bh >= kAutoTargetUnits) {
-            sl = L;
-        } else {
-            const int64_t want = (kAutoTargetUnits + bh - 1) / bh;
-            sl = (L + want - 1) / want;
-            sl = (sl + p->chunk - 1) / p->chunk * p->chunk;
-            if (sl < 4 * p->chunk) sl = 4 * p->chunk;   // keep boundary-state traffic small
+        const int64_t nchunks = (L + p->chunk - 1) / p->chunk;
+        int64_t n = 1;
+        if (bh < kAutoSMs) {
+            const int64_t n_min = (kAutoSMs + bh - 1) / bh;
+            int64_t n_max = (4 * kAutoSMs + bh - 1) / bh;
+            if (n_max > nchunks / 4) n_max = nchunks / 4;
+            if (n_max < 1) n_max = 1;
+            if (n_min >= n_max) {
+                n = n_max;
+            } else {
+                double best = -1.0;
+                for (int64_t k = n_min; k <= n_max; ++k) {
+                    const int64_t units = bh * k;
+                    const double fill = (double)units / (double)(((units + kAutoSMs - 1) / kAutoSMs) * kAutoSMs);
+                    if (fill > best + 1e-12) {
+                        best = fill;
+                        n = k;
+                    }
+                    if (fill >= 0.95) break;
+                }
+            }
         }
+        sl = (nchunks + n - 1) / n * p->chunk;
     }
     if (sl >= L) sl = (L + p->chunk - 1) / p->chunk * p->chunk;
     return sl;
