@@ -343,7 +343,8 @@ def run_ours(args):
                        "compulsory_bytes": nbytes, "achieved_GBps": achieved,
                        "pct_of_8TBps_spec": 100.0 * achieved / 8000.0},
             "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
-                         "frac": achieved / peak, "peak_source": peak_kind, "traffic": traffic},
+                         "frac": achieved / peak, "peak_source": peak_kind, "traffic": traffic,
+                         "scope": f"compulsory bytes over the whole ssd_fwd call ({launches} launches)"},
             "e2e": {"value": e2e_value, "unit": "tokens/s", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
             "gpu_launches": launches * args.steps,
             "clocks": clk.summary(),
