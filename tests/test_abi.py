@@ -89,3 +89,32 @@ def test_status_strings(L):
     assert L.lib.ssd_status_string(0) == b"SSD_OK"
     assert L.lib.ssd_status_string(5) == b"SSD_ERR_TIMEOUT"
     assert L.lib.ssd_status_string(99) == b"SSD_ERR_UNKNOWN"
+
+
+def wave_fill(units, sms=152):
+    return units / (-(-units // sms) * sms)
+
+
+@pytest.mark.parametrize("batch,seqlen,nheads,want", [
+    (1, 32768, 48, 6),     # packed varlen config: 7 splits would run 3 waves, 6 fill 2 to 95 %
+    (1, 16384, 64, 7),     # 448 units, 98 % of 3 waves
+    (2, 256, 4, 1),        # too short to split (splits keep at least 4 chunks)
+    (2, 1000, 3, 2),       # as many 4-chunk splits as the length allows
+    (8, 2048, 80, 1),      # at least as many units as SMs: one split
+    (2, 2048, 80, 1),      # 160 units: one split (the leftover-unit plan evens the waves)
+])
+def test_automatic_split_plan(L, batch, seqlen, nheads, want):
+    p = params(L, batch=batch, seqlen=seqlen, nheads=nheads, ngroups=1)
+    fam, launches, ns = L.plan(p)
+    assert ns == want
+    nchunks = -(-seqlen // 128)
+    if ns > 1:
+        # the chosen count is the smallest in its range whose units fill their waves to 95 %,
+        # or the best fill when none does; splits keep at least 4 chunks
+        assert -(-nchunks // ns) >= 4 or ns == nchunks // 4
+        lo = -(-152 // (batch * nheads))
+        if wave_fill(batch * nheads * ns) < 0.95:
+            hi = min(-(-4 * 152 // (batch * nheads)), nchunks // 4)
+            assert all(wave_fill(batch * nheads * k) <= wave_fill(batch * nheads * ns) for k in range(lo, hi + 1))
+        else:
+            assert all(wave_fill(batch * nheads * k) < 0.95 for k in range(lo, ns))
