@@ -2,7 +2,7 @@
 """Benchmark of the SSD forward pass (one JSON line on rank 0).
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
-                    [--workload 27b|sweep:B:L:S|long|varlen|tiny]
+                    [--workload 27b|sweep:B:L:S|long|varlen|tiny|decode[:B]]
 
 A step is one ssd_fwd call over one batch of the workload (default: the
 Mamba-2 2.7B-like layer, batch 8 x 2048 tokens, 80 heads, P 64, N 128, bf16).
@@ -13,6 +13,9 @@ reports the aggregate over ranks with the slowest rank's time.
 
 --impl reference times the fp64 CPU oracle recurrence on the host cores on a
 bounded sample of the same workload (one batch row per step).
+
+--workload decode[:B] times the single-token decode step (ssd_step) of the
+same layer shape over a batch of B rows (default 256) from a resident state.
 """
 from __future__ import annotations
 
@@ -37,7 +40,13 @@ METRIC = "SSD fwd tokens/s and achieved HBM GB/s (% of GB300 roofline) vs L, 1 G
 FALLBACK_HBM_GBS = 6800.0
 
 
+DECODE_METRIC = "SSD decode step tokens/s and achieved HBM GB/s on the resident state, 1 GPU"
+
+
 def workload(name: str):
+    if name.startswith("decode"):
+        parts = name.split(":")
+        return synth.config_decode(int(parts[1]) if len(parts) > 1 else 256)
     if name == "27b":
         return synth.config_27b()
     if name == "tiny":
@@ -57,6 +66,13 @@ def compulsory_bytes(p) -> int:
     e = 2 if p.dtype == "bf16" else 4
     T = p.batch * p.seqlen
     return T * (2 * p.nheads * p.headdim * e + p.nheads * 4 + 2 * p.ngroups * p.dstate * e)
+
+
+def decode_bytes(p) -> int:
+    """State read and write, x, y, dt, B and C of one decode step."""
+    e = 2 if p.dtype == "bf16" else 4
+    bh = p.batch * p.nheads
+    return bh * (2 * p.headdim * p.dstate * 4 + 2 * p.headdim * e + 4) + p.batch * p.ngroups * 2 * p.dstate * e
 
 
 def peaks():
@@ -157,12 +173,40 @@ def kernel_traffic(family: int):
         return None
 
 
+def oracle_decode(p, rows):
+    import oracle
+    return oracle.ssd_step(p.initial_states[:rows], p.x[:rows, 0], p.dt[:rows, 0], p.A, p.B[:rows, 0],
+                           p.C[:rows, 0], p.D)
+
+
 def run_reference(args):
     import oracle
     rank, _, world = dist_env()
     if rank != 0:
         return
     p = workload(args.workload)
+    if p.seqlen == 1:
+        rows = min(p.batch, 64)
+        for _ in range(args.warmup):
+            oracle_decode(p, rows)
+        times = []
+        for _ in range(args.steps):
+            t0 = time.perf_counter()
+            oracle_decode(p, rows)
+            times.append(time.perf_counter() - t0)
+        ms = 1e3 * sum(times) / len(times)
+        value = rows / (ms / 1e3)
+        sample = f"fp64 decode step of batch rows 0..{rows - 1} of {p.name} per step"
+        print(json.dumps({
+            "impl": "reference", "metric": DECODE_METRIC, "value": value, "unit": "tokens/s", "n_gpus": world,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": {"workload": p.name, "sample": f"{rows} of {p.batch} batch rows per step"},
+            "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": oracle.max_threads(), "kind": "oracle",
+                             "sample": sample},
+            "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}),
+            flush=True)
+        return
     # bounded sample: one batch row of the workload per step
     q = synth.SSDProblem(1, p.seqlen, p.nheads, p.headdim, p.dstate, p.ngroups, p.chunk, p.split_len,
                          p.dtype, p.x[:1].copy(), p.dt[:1].copy(), p.A, p.B[:1].copy(), p.C[:1].copy(), p.D,
@@ -206,6 +250,115 @@ def cpu_baseline(p):
             "sample": f"fp64 recurrence on batch row 0 of {p.name}, {reps} passes, {t_all:.1f} s wall"}
 
 
+def run_decode(args, p, dev, rank, local_rank, world):
+    """Decode workload: a step is one ssd_step over the whole batch (one new
+    token per row), the state resident in HBM and updated in place."""
+    import torch
+    import torch.distributed as dist
+    import mamba_ssd_chunked_scan_gb300 as ssd
+
+    def io(name):
+        return torch.from_numpy(p.storage(name)[:, 0].view(np.int16).copy()).to(dev).view(torch.bfloat16)
+
+    x, B, C = io("x"), io("B"), io("C")
+    dt = torch.from_numpy(p.dt[:, 0].copy()).to(dev)
+    A = torch.from_numpy(p.A).to(dev)
+    D = torch.from_numpy(p.D).to(dev)
+    state = torch.from_numpy(p.initial_states).to(dev)
+    y = torch.empty_like(x)
+    flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
+    stream = torch.cuda.current_stream()
+
+    def step(xx=x, dd=dt, bb=B, cc=C, yy=y):
+        ssd.ssd_step(state, xx, dd, A, bb, cc, D, y=yy, stream=stream)
+
+    for _ in range(args.warmup):
+        flush.zero_()
+        step()
+    torch.cuda.synchronize()
+    if world > 1:
+        dist.barrier()
+    torch.cuda.synchronize()
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
+    with ClockSampler(local_rank) as clk:
+        for i in range(args.steps):
+            flush.zero_()
+            ev[i][0].record(stream)
+            step()
+            ev[i][1].record(stream)
+        torch.cuda.synchronize()
+    ms = sum(a.elapsed_time(b) for a, b in ev) / args.steps
+
+    # end to end: each step's token inputs come from pinned host memory and its
+    # y goes back; the state stays resident on the device between steps
+    hx, hB, hC, hdt = (t.cpu().pin_memory() for t in (x, B, C, dt))
+    hy = torch.empty(y.shape, dtype=y.dtype).pin_memory()
+    h2d = sum(t.numel() * t.element_size() for t in (hx, hB, hC, hdt))
+    d2h = hy.numel() * hy.element_size()
+    dx, dB, dC, ddt = (torch.empty_like(t) for t in (x, B, C, dt))
+
+    def e2e_step():
+        dx.copy_(hx, non_blocking=True)
+        dB.copy_(hB, non_blocking=True)
+        dC.copy_(hC, non_blocking=True)
+        ddt.copy_(hdt, non_blocking=True)
+        step(dx, ddt, dB, dC, y)
+        hy.copy_(y, non_blocking=True)
+
+    for _ in range(args.warmup):
+        e2e_step()
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(args.steps):
+        e2e_step()
+    e1.record(stream)
+    torch.cuda.synchronize()
+    e2e_ms = e0.elapsed_time(e1) / args.steps
+
+    t_tensor = torch.tensor([ms, e2e_ms], dtype=torch.float64, device=dev)
+    if world > 1:
+        dist.all_reduce(t_tensor, op=dist.ReduceOp.MAX)
+        dist.barrier()
+    ms_max, e2e_max = float(t_tensor[0]), float(t_tensor[1])
+    if rank == 0:
+        nbytes = decode_bytes(p)
+        peak, peak_kind = peaks()
+        achieved = nbytes / (ms / 1e3) / 1e9
+        line = {
+            "metric": DECODE_METRIC, "value": world * p.batch / (ms_max / 1e3), "unit": "tokens/s",
+            "n_gpus": world, "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_max,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32",
+            "data": "synthetic",
+            "config": {"workload": p.name, "batch": p.batch, "nheads": p.nheads, "headdim": p.headdim,
+                       "dstate": p.dstate, "ngroups": p.ngroups, "storage": p.dtype, "kernel": "ssd_step",
+                       "l2": "256 MiB write before every timed step; the state is larger than L2",
+                       "bytes_per_step": nbytes, "achieved_GBps": achieved},
+            "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
+                         "frac": achieved / peak, "peak_source": peak_kind, "traffic": None,
+                         "scope": "state read + write, x, y, dt, B, C of one ssd_step launch"},
+            "e2e": {"value": world * p.batch / (e2e_max / 1e3), "unit": "tokens/s", "h2d_bytes_per_step": h2d,
+                    "d2h_bytes_per_step": d2h},
+            "gpu_launches": args.steps,
+            "clocks": clk.summary(),
+        }
+        if world == 1 and not args.no_cpu_baseline:
+            rows = min(p.batch, 64)
+            reps, t_all = 0, 0.0
+            while t_all < 5.0 and reps < 200:
+                t0 = time.perf_counter()
+                oracle_decode(p, rows)
+                t_all += time.perf_counter() - t0
+                reps += 1
+            import oracle
+            line["cpu_baseline"] = {"value": rows * reps / t_all, "unit": "tokens/s", "cores": oracle.max_threads(),
+                                    "kind": "oracle",
+                                    "sample": f"fp64 decode step of {rows} batch rows of {p.name}, {reps} passes"}
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        dist.destroy_process_group()
+
+
 def run_ours(args):
     import torch
     import torch.distributed as dist
@@ -217,6 +370,8 @@ def run_ours(args):
     if world > 1:
         dist.init_process_group("nccl", device_id=dev)
     p = workload(args.workload)
+    if p.seqlen == 1:
+        return run_decode(args, p, dev, rank, local_rank, world)
     dtype = torch.bfloat16 if p.dtype == "bf16" else torch.float32
 
     def dev_io(name):

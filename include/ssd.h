@@ -131,6 +131,39 @@ SSD_API int ssd_fwd_static_scratch(const ssd_params_t* p,
             const float* initial_states, const int32_t* cu_seqlens,
             void* y, float* final_states, void* stream);
 
+/* One autoregressive (decode) step: a single new token per batch row from a
+ * resident state.  "State Space Duality and Mamba-2", section "Performance and
+ * Serving Economics": generation keeps a fixed-size recurrent state and costs
+ * constant time and memory per token.  The step is the recurrence above taken
+ * once per (b, h), g = h / (H / G):
+ *
+ *     state'[b,h] = exp(dt[b,h] A_h) state[b,h] + dt[b,h] x[b,h] B[b,g]^T
+ *     y[b,h]      = state'[b,h] C[b,g] + D_h x[b,h]
+ *
+ * so a prefill by ssd_fwd() (final_states) followed by steps gives the same
+ * outputs, up to rounding, as one ssd_fwd() over the whole sequence.
+ *
+ * Layouts (row-major, contiguous, device memory): the forward's layouts with
+ * one token per row (seqlen = 1):
+ *   state_in, state_out (batch, nheads, headdim, dstate)  fp32, 16-byte aligned
+ *   x, y                (batch, nheads, headdim)          dtype
+ *   dt                  (batch, nheads)                   fp32, >= 0
+ *   A, D                (nheads)                          fp32 (D optional)
+ *   B, C                (batch, ngroups, dstate)          dtype
+ * state_out may equal state_in (an in-place update) or be a disjoint buffer;
+ * any other overlap is an argument error, as is y equal to an input.
+ * dtype is an ssd_dtype_t.  dstate must be a multiple of 4 and at most 512,
+ * headdim at most 2048 (else SSD_ERR_UNSUPPORTED).
+ *
+ * No workspace and no device-side waits: the call enqueues one kernel on
+ * `stream` and returns (SSD_OK, an argument error before any launch, or
+ * SSD_ERR_CUDA for a failed launch).  It can be captured in a CUDA graph.
+ * Bitwise deterministic. */
+SSD_API int ssd_step(int64_t batch, int32_t nheads, int32_t headdim, int32_t dstate, int32_t ngroups,
+             int32_t dtype, const float* state_in, float* state_out,
+             const void* x, const float* dt, const float* A, const void* B, const void* C,
+             const float* D, void* y, void* stream);
+
 /* Synchronise `stream`, read the device status word of `workspace`, clear it,
  * and return it (SSD_OK when no device error was recorded). */
 SSD_API int ssd_check_status(void* workspace, void* stream);

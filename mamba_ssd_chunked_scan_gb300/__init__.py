@@ -33,7 +33,7 @@ def __getattr__(name):
         return _lib.SSDError
     raise AttributeError(name)
 
-__all__ = ["ssd_fwd", "SSDForward", "segsum_dump", "check_status", "SSDError", "plan"]
+__all__ = ["ssd_fwd", "SSDForward", "ssd_step", "segsum_dump", "check_status", "SSDError", "plan"]
 
 
 def _ptr(t: Optional[torch.Tensor]):
@@ -132,6 +132,37 @@ def ssd_fwd(x, dt, A, B, C, D=None, initial_states=None, cu_seqlens=None, *, chu
     if st != 0:
         raise _lib.SSDError(st, "ssd_fwd device status")
     return (y, fin) if return_final_states else y
+
+
+def ssd_step(state, x, dt, A, B, C, D=None, *, state_out=None, y=None, stream=None):
+    """One decode step: a new token per batch row from the resident state.
+
+    state (batch, H, P, N) fp32 is updated in place unless ``state_out`` (same
+    shape, disjoint) is given; x (batch, H, P), dt (batch, H), A (H),
+    B/C (batch, G, N), D (H) or None.  Returns y (batch, H, P) in x's dtype.
+    """
+    batch, nheads, headdim = x.shape
+    ngroups, dstate = B.shape[1], B.shape[2]
+    dev = x.device
+    if state_out is None:
+        state_out = state
+    for name, t, shp, dt_ in (("state", state, (batch, nheads, headdim, dstate), torch.float32),
+                              ("state_out", state_out, (batch, nheads, headdim, dstate), torch.float32),
+                              ("x", x, (batch, nheads, headdim), x.dtype),
+                              ("dt", dt, (batch, nheads), torch.float32), ("A", A, (nheads,), torch.float32),
+                              ("B", B, (batch, ngroups, dstate), x.dtype), ("C", C, (batch, ngroups, dstate), x.dtype),
+                              ("D", D, (nheads,), torch.float32), ("y", y, (batch, nheads, headdim), x.dtype)):
+        if t is None:
+            continue
+        if tuple(t.shape) != shp or t.dtype != dt_ or not t.is_contiguous() or t.device != dev:
+            raise ValueError(f"{name}: expected contiguous {dt_} {shp} on {dev}, got "
+                             f"{t.dtype} {tuple(t.shape)} on {t.device}")
+    if y is None:
+        y = torch.empty((batch, nheads, headdim), dtype=x.dtype, device=dev)
+    rc = _lib.lib.ssd_step(batch, nheads, headdim, dstate, ngroups, _dtype_code(x), _ptr(state), _ptr(state_out),
+                           _ptr(x), _ptr(dt), _ptr(A), _ptr(B), _ptr(C), _ptr(D), _ptr(y), _stream_handle(stream))
+    _lib.check(rc, "ssd_step")
+    return y
 
 
 def check_status(workspace: torch.Tensor, stream=None) -> int:

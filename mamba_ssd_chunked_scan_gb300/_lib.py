@@ -18,7 +18,7 @@ STATUS = {0: "SSD_OK", 1: "SSD_ERR_INVALID_ARG", 2: "SSD_ERR_UNSUPPORTED", 3: "S
 
 # every symbol include/ssd.h declares
 EXPORTS = ("ssd_fwd_workspace_size", "ssd_workspace_init", "ssd_fwd", "ssd_check_status",
-           "ssd_status_string", "ssd_fwd_plan", "ssd_segsum_dump", "ssd_fwd_static_scratch")
+           "ssd_status_string", "ssd_fwd_plan", "ssd_segsum_dump", "ssd_fwd_static_scratch", "ssd_step")
 
 
 class SSDParams(ctypes.Structure):
@@ -55,6 +55,8 @@ def _load():
     lib.ssd_fwd_plan.restype = ctypes.c_int
     lib.ssd_fwd_static_scratch.argtypes = [P, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp]
     lib.ssd_fwd_static_scratch.restype = ctypes.c_int
+    lib.ssd_step.argtypes = [i64, i32, i32, i32, i32, i32, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp]
+    lib.ssd_step.restype = ctypes.c_int
     lib.ssd_segsum_dump.argtypes = [vp, i64, i32, vp, vp, vp]
     lib.ssd_segsum_dump.restype = ctypes.c_int
     return lib

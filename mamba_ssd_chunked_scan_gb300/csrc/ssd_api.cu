@@ -16,6 +16,9 @@ namespace {
 constexpr int kSmemLimit = 227 * 1024;
 constexpr int64_t kAutoSMs = 152;   // SMs the automatic split plan fills (GB300)
 
+constexpr int kStepMaxN = 512;    // dstate limit of the decode step (float4 vectors per lane)
+constexpr int kStepMaxP = 2048;   // headdim limit of the decode step (shared-memory rows)
+
 bool aligned(const void* p, size_t a) { return ((uintptr_t)p % a) == 0; }
 
 int check_params(const ssd_params_t* p) {
@@ -325,6 +328,33 @@ int ssd_fwd_static_scratch(const ssd_params_t* p, const void* x, const float* dt
     if (rc != SSD_OK) return rc;
     // synchronous: wait for the work and report what the device recorded
     return ssd_check_status(ws, stream);
+}
+
+int ssd_step(int64_t batch, int32_t nheads, int32_t headdim, int32_t dstate, int32_t ngroups, int32_t dtype,
+             const float* state_in, float* state_out, const void* x, const float* dt, const float* A,
+             const void* B, const void* C, const float* D, void* y, void* stream) {
+    if (batch < 1 || nheads < 1 || headdim < 1 || dstate < 1 || ngroups < 1 || nheads % ngroups != 0)
+        return SSD_ERR_INVALID_ARG;
+    if (dtype != SSD_F32 && dtype != SSD_BF16) return SSD_ERR_INVALID_ARG;
+    if (dstate % 4 != 0 || dstate > kStepMaxN || headdim > kStepMaxP) return SSD_ERR_UNSUPPORTED;
+    if (batch * nheads >= ((int64_t)1 << 31)) return SSD_ERR_UNSUPPORTED;   // one CTA per (row, head)
+    if (!state_in || !state_out || !x || !dt || !A || !B || !C || !y) return SSD_ERR_INVALID_ARG;
+    const size_t esz = dtype == SSD_BF16 ? 2 : 4;
+    if (!aligned(state_in, 16) || !aligned(state_out, 16) || !aligned(dt, 4) || !aligned(A, 4) ||
+        (D && !aligned(D, 4)) || !aligned(x, esz) || !aligned(B, esz) || !aligned(C, esz) || !aligned(y, esz))
+        return SSD_ERR_INVALID_ARG;
+    // the state is updated in place or written to a disjoint buffer
+    const size_t sbytes = (size_t)batch * nheads * headdim * dstate * sizeof(float);
+    const uintptr_t si = (uintptr_t)state_in, so = (uintptr_t)state_out;
+    if (si != so && si < so + sbytes && so < si + sbytes) return SSD_ERR_INVALID_ARG;
+    if (y == x || y == B || y == C || y == (const void*)state_in || y == (void*)state_out)
+        return SSD_ERR_INVALID_ARG;
+    StepArgs a;
+    a.batch = batch; a.H = nheads; a.P = headdim; a.N = dstate; a.G = ngroups; a.dtype = dtype;
+    a.state_in = state_in; a.state_out = state_out;
+    a.x = x; a.dt = dt; a.A = A; a.B = B; a.C = C; a.D = D; a.y = y;
+    if (launch_step(a, (cudaStream_t)stream) != cudaSuccess) return SSD_ERR_CUDA;
+    return SSD_OK;
 }
 
 int ssd_segsum_dump(const float* l2, int64_t nrows, int32_t chunk, float* seg, float* L, void* stream) {

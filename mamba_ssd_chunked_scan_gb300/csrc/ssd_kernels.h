@@ -43,6 +43,22 @@ struct FwdArgs {
     int64_t grid_units;
 };
 
+// One decode step (ssd_step): everything the launch needs.
+struct StepArgs {
+    int64_t batch;
+    int H, P, N, G;
+    int dtype;             // ssd_dtype_t of x, B, C and y
+    const float* state_in;
+    float* state_out;      // == state_in for an in-place step
+    const void* x;
+    const float* dt;
+    const float* A;
+    const void* B;
+    const void* C;
+    const float* D;
+    void* y;
+};
+
 // Constants of division by an invariant divisor d >= 1 through one high
 // multiply and a shift (Granlund and Montgomery, "Division by Invariant
 // Integers using Multiplication", 1994): l = ceil(log2 d),
@@ -61,6 +77,8 @@ cudaError_t launch_split_scan(const FwdArgs& a, cudaStream_t st);
 size_t tc_smem_bytes();
 bool tc_supported(int P, int N, int Q, int dtype);
 cudaError_t launch_tc(const FwdArgs& a, cudaStream_t st);
+size_t step_smem_bytes(int P, int N);
+cudaError_t launch_step(const StepArgs& a, cudaStream_t st);
 cudaError_t launch_segsum_dump(const float* l2, int64_t nrows, int chunk, float* seg, float* L,
                                cudaStream_t st);
 

@@ -236,3 +236,10 @@ def varlen_logdecay_rows(nrows: int, length: int, seed: int = 101) -> np.ndarray
     dt = _softplus(g.normal(2.0, 2.0, size=(nrows, length))).astype(np.float32)
     A = (-g.uniform(1.0, 16.0, size=(nrows, 1))).astype(np.float32)
     return (dt * A).astype(np.float32)
+
+
+def config_decode(batch: int = 256) -> SSDProblem:
+    """One decode step of the 2.7B-like layer: one token per batch row from a
+    resident state (seqlen 1 with initial states)."""
+    return make_problem(batch=batch, seqlen=1, nheads=80, headdim=64, dstate=128, ngroups=1, chunk=128,
+                        dtype="bf16", seed=5, init_std=0.1, name=f"decode_b{batch}_H80_P64_N128_G1")

@@ -105,6 +105,33 @@ def ssd_recurrence(p, want_final: bool = True, nthreads: int = 0):
     return y, fin
 
 
+class _StepProblem:
+    """A one-token problem: the arrays of a decode step seen as seqlen = 1."""
+
+    def __init__(self, state, x, dt, A, B, C, D):
+        self.batch, self.nheads, self.headdim = x.shape
+        self.ngroups, self.dstate = B.shape[1], B.shape[2]
+        self.seqlen, self.ndocs, self.nstates, self.cu_seqlens = 1, 0, self.batch, None
+        self.x = x.reshape(self.batch, 1, self.nheads, self.headdim)
+        self.dt = dt.reshape(self.batch, 1, self.nheads)
+        self.B = B.reshape(self.batch, 1, self.ngroups, self.dstate)
+        self.C = C.reshape(self.batch, 1, self.ngroups, self.dstate)
+        self.A, self.D, self.initial_states = A, D, state
+
+
+def ssd_step(state, x, dt, A, B, C, D=None):
+    """One decode step, fp64: the recurrence taken once from ``state``
+    ("State Space Duality and Mamba-2", "Performance and Serving Economics":
+    a fixed-size state updated once per generated token).
+
+    state (batch, H, P, N), x (batch, H, P), dt (batch, H), A (H),
+    B, C (batch, G, N), D (H) or None.  Returns (y (batch, H, P), state')."""
+    q = _StepProblem(np.asarray(state), np.asarray(x), np.asarray(dt), np.asarray(A), np.asarray(B),
+                     np.asarray(C), None if D is None else np.asarray(D))
+    y, fin = ssd_recurrence(q, want_final=True)
+    return y.reshape(q.batch, q.nheads, q.headdim), fin
+
+
 def ssd_quadratic(p):
     """(C B^T) o L form plus the initial-state term, fp64, O(L^2)."""
     _check(p)

@@ -118,3 +118,34 @@ def test_automatic_split_plan(L, batch, seqlen, nheads, want):
             assert all(wave_fill(batch * nheads * k) <= wave_fill(batch * nheads * ns) for k in range(lo, hi + 1))
         else:
             assert all(wave_fill(batch * nheads * k) < 0.95 for k in range(lo, ns))
+
+
+def step_args(L, **kw):
+    """ssd_step arguments with distinct, 256-byte aligned fake device addresses
+    (every case below is rejected before anything touches the device)."""
+    base = 1 << 40
+    d = dict(batch=4, nheads=8, headdim=64, dstate=128, ngroups=2, dtype=1,
+             state_in=base, state_out=base, x=base + (1 << 30), dt=base + (2 << 30), A=base + (3 << 30),
+             B=base + (4 << 30), C=base + (5 << 30), D=base + (6 << 30), y=base + (7 << 30), stream=None)
+    d.update(kw)
+    return d
+
+
+def call_step(L, d):
+    vp = ctypes.c_void_p
+    return L.lib.ssd_step(d["batch"], d["nheads"], d["headdim"], d["dstate"], d["ngroups"], d["dtype"],
+                          *(vp(d[k]) if d[k] is not None else None
+                            for k in ("state_in", "state_out", "x", "dt", "A", "B", "C", "D", "y", "stream")))
+
+
+@pytest.mark.parametrize("kw,code", [
+    (dict(batch=0), 1), (dict(nheads=0), 1), (dict(ngroups=3), 1), (dict(dtype=5), 1),
+    (dict(dstate=6), 2), (dict(dstate=1024), 2), (dict(headdim=4096), 2), (dict(batch=1 << 28, nheads=8), 2),
+    (dict(x=None), 1), (dict(state_in=None), 1), (dict(y=None), 1),
+    (dict(state_out=(1 << 40) + 8), 1),                    # misaligned state
+    (dict(state_out=(1 << 40) + 4096), 1),                 # partial overlap with state_in
+    (dict(y=(1 << 40) + (1 << 30)), 1),                    # y == x
+    (dict(dt=(1 << 40) + (2 << 30) + 2), 1),               # misaligned dt
+])
+def test_step_invalid_args(L, kw, code):
+    assert call_step(L, step_args(L, **kw)) == code
