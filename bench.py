@@ -145,15 +145,19 @@ class ClockSampler:
                 "reasons": reasons, "samples": len(self.rows)}
 
 
-def kernel_sources_sha() -> str:
-    """Fingerprint of every CUDA source of the library (to tell whether a
-    recorded counter still belongs to the kernels being timed)."""
+# the sources that define each kernel family's device code and launch
+FAMILY_SOURCES = {1: ("ssd_tc.cu", "tc_ptx.cuh", "ssd_common.cuh"),
+                  0: ("ssd_simt.cu", "segsum.cuh", "ssd_common.cuh")}
+
+
+def kernel_sources_sha(family: int) -> str:
+    """Fingerprint of the CUDA sources of one kernel family (to tell whether a
+    recorded counter still belongs to the kernel being timed)."""
     csrc = os.path.join(ROOT, "mamba_ssd_chunked_scan_gb300", "csrc")
     h = hashlib.sha256()
-    for name in sorted(os.listdir(csrc)):
-        if name.endswith((".cu", ".cuh", ".h")):
-            h.update(name.encode())
-            h.update(open(os.path.join(csrc, name), "rb").read())
+    for name in FAMILY_SOURCES[family]:
+        h.update(name.encode())
+        h.update(open(os.path.join(csrc, name), "rb").read())
     return h.hexdigest()[:16]
 
 
@@ -168,7 +172,7 @@ def kernel_traffic(family: int):
         ent = d.get(str(family))
         if not ent:
             return None
-        return ent["dram_bytes_per_launch"] if kernel_sources_sha() == ent["source_sha"] else None
+        return ent["dram_bytes_per_launch"] if kernel_sources_sha(family) == ent["source_sha"] else None
     except Exception:
         return None
 
