@@ -48,11 +48,13 @@ def _load():
             lib.oracle_ssd_recurrence.argtypes = common + [d, d, ci]
             lib.oracle_ssd_quadratic.argtypes = common + [d]
             lib.oracle_ssd_chunked.argtypes = common + [ci, i64, d, d]
+            lib.oracle_ssd_backward.argtypes = [i64, i64, ci, ci, ci, ci, d, d, d, d, d, d, d, d, d,
+                                                d, d, d, d, d, d, d, ci]
             lib.oracle_segsum.argtypes = [d, i64, ci, d]
             lib.oracle_diff_segsum_f32.argtypes = [f, i64, ci, f]
             lib.oracle_max_threads.restype = ci
             for fn in (lib.oracle_ssd_recurrence, lib.oracle_ssd_quadratic, lib.oracle_ssd_chunked,
-                       lib.oracle_segsum, lib.oracle_diff_segsum_f32):
+                       lib.oracle_ssd_backward, lib.oracle_segsum, lib.oracle_diff_segsum_f32):
                 fn.restype = None
             _lib = lib
     return _lib
@@ -130,6 +132,32 @@ def ssd_step(state, x, dt, A, B, C, D=None):
                      np.asarray(C), None if D is None else np.asarray(D))
     y, fin = ssd_recurrence(q, want_final=True)
     return y.reshape(q.batch, q.nheads, q.headdim), fin
+
+
+def ssd_backward(p, dy, dfinal=None, nthreads: int = 0):
+    """Gradients of <dy, y> + <dfinal, final_states> with respect to every input
+    of the forward pass, fp64 (batch rows only, no packed documents).
+
+    Returns a dict of arrays: dx, ddt, dA, dB, dC, dD (None without D) and
+    dinit (the initial states' gradient, also when the forward had none)."""
+    _check(p)
+    if p.cu_seqlens is not None:
+        raise ValueError("the backward oracle takes batch rows only")
+    lib = _load()
+    arrs, _ = _args(p)
+    dy64 = _f64(dy)
+    df64 = _f64(dfinal)
+    out = dict(dx=np.zeros((p.batch, p.seqlen, p.nheads, p.headdim)), ddt=np.zeros((p.batch, p.seqlen, p.nheads)),
+               dA=np.zeros(p.nheads), dB=np.zeros((p.batch, p.seqlen, p.ngroups, p.dstate)),
+               dC=np.zeros((p.batch, p.seqlen, p.ngroups, p.dstate)),
+               dD=None if p.D is None else np.zeros(p.nheads),
+               dinit=np.zeros((p.batch, p.nheads, p.headdim, p.dstate)))
+    lib.oracle_ssd_backward(p.batch, p.seqlen, p.nheads, p.headdim, p.dstate, p.ngroups,
+                            _dp(arrs["x"]), _dp(arrs["dt"]), _dp(arrs["A"]), _dp(arrs["B"]), _dp(arrs["C"]),
+                            _dp(arrs["D"]), _dp(arrs["init"]), _dp(dy64), _dp(df64),
+                            _dp(out["dx"]), _dp(out["ddt"]), _dp(out["dA"]), _dp(out["dB"]), _dp(out["dC"]),
+                            _dp(out["dD"]), _dp(out["dinit"]), int(nthreads))
+    return out
 
 
 def ssd_quadratic(p):
