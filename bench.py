@@ -2,7 +2,7 @@
 """Benchmark of the SSD forward pass (one JSON line on rank 0).
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
-                    [--workload 27b|sweep:B:L:S|long|varlen|tiny|decode[:B]]
+                    [--workload 27b|sweep:B:L:S|long|varlen|tiny|decode[:B]|bwd]
 
 A step is one ssd_fwd call over one batch of the workload (default: the
 Mamba-2 2.7B-like layer, batch 8 x 2048 tokens, 80 heads, P 64, N 128, bf16).
@@ -15,7 +15,8 @@ reports the aggregate over ranks with the slowest rank's time.
 bounded sample of the same workload (one batch row per step).
 
 --workload decode[:B] times the single-token decode step (ssd_step) of the
-same layer shape over a batch of B rows (default 256) from a resident state.
+same layer shape over a batch of B rows (default 256) from a resident state;
+--workload bwd times the backward pass (ssd_bwd) of the 2.7B-like layer.
 """
 from __future__ import annotations
 
@@ -41,13 +42,26 @@ FALLBACK_HBM_GBS = 6800.0
 
 
 DECODE_METRIC = "SSD decode step tokens/s and achieved HBM GB/s on the resident state, 1 GPU"
+BWD_METRIC = "SSD bwd tokens/s and achieved fp32 TFLOP/s (% of the CUDA-core fp32 peak), 1 GPU"
+# fp32 CUDA-core peak: 152 SMs x 128 fp32 lanes x 2 flop (FMA) x 2.07 GHz (maximum SM clock)
+FP32_PEAK_TFLOPS = 152 * 128 * 2 * 2.07e9 / 1e12
+
+
+def bwd_flops(p, Qb=32) -> float:
+    """Algorithmic flops of ssd_bwd (2 per multiply-add): per token and head,
+    2PN (chunk-entry states and the adjoint carry) + Qb (N + P) / 2 (C B^T and
+    dy x^T, lower triangle) + P (2N + Qb / 2) (dx: Lam B, S_in C, the masked
+    sum) + N (2P + Qb) (dB and dC)."""
+    P, N = p.headdim, p.dstate
+    mac = 2 * P * N + Qb * (N + P) / 2 + P * (2 * N + Qb / 2) + N * (2 * P + Qb)
+    return 2.0 * mac * p.batch * p.seqlen * p.nheads
 
 
 def workload(name: str):
     if name.startswith("decode"):
         parts = name.split(":")
         return synth.config_decode(int(parts[1]) if len(parts) > 1 else 256)
-    if name == "27b":
+    if name in ("27b", "bwd"):
         return synth.config_27b()
     if name == "tiny":
         return synth.config_tiny_f32()
@@ -189,6 +203,28 @@ def run_reference(args):
     if rank != 0:
         return
     p = workload(args.workload)
+    if args.workload == "bwd":
+        dy_h = np.random.default_rng(11).standard_normal((p.batch, p.seqlen, p.nheads, p.headdim)).astype(np.float32)
+        q, dyq = bwd_sample(p, dy_h)
+        for _ in range(args.warmup):
+            oracle.ssd_backward(q, dyq)
+        times = []
+        for _ in range(args.steps):
+            t0 = time.perf_counter()
+            oracle.ssd_backward(q, dyq)
+            times.append(time.perf_counter() - t0)
+        ms = 1e3 * sum(times) / len(times)
+        value = q.seqlen / (ms / 1e3)
+        print(json.dumps({
+            "impl": "reference", "metric": BWD_METRIC, "value": value, "unit": "tokens/s", "n_gpus": world,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": {"workload": "bwd_" + p.name, "sample": f"batch row 0, {q.seqlen} tokens per step"},
+            "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": oracle.max_threads(), "kind": "oracle",
+                             "sample": f"fp64 reverse-mode recurrence on batch row 0, {q.seqlen} tokens"},
+            "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}),
+            flush=True)
+        return
     if p.seqlen == 1:
         rows = min(p.batch, 64)
         for _ in range(args.warmup):
@@ -363,6 +399,127 @@ def run_decode(args, p, dev, rank, local_rank, world):
         dist.destroy_process_group()
 
 
+def run_bwd(args, p, dev, rank, local_rank, world):
+    """Backward workload: a step is one ssd_bwd call over the 2.7B-like layer
+    (the forward's inputs, random dy and dfinal_states)."""
+    import torch
+    import torch.distributed as dist
+    import mamba_ssd_chunked_scan_gb300 as ssd
+
+    def io(a):
+        return torch.from_numpy(synth.bf16_bits(a).view(np.int16).copy()).to(dev).view(torch.bfloat16)
+
+    rng = np.random.default_rng(11)
+    dy_h = rng.standard_normal((p.batch, p.seqlen, p.nheads, p.headdim)).astype(np.float32)
+    x, B, C, dy = io(p.x), io(p.B), io(p.C), io(dy_h)
+    dt = torch.from_numpy(p.dt).to(dev)
+    A = torch.from_numpy(p.A).to(dev)
+    D = torch.from_numpy(p.D).to(dev)
+    dfin = torch.from_numpy(rng.standard_normal((p.batch, p.nheads, p.headdim, p.dstate)).astype(np.float32)).to(dev)
+    flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
+    stream = torch.cuda.current_stream()
+
+    def step(xx=x, dd=dt, bb=B, cc=C, yy=dy):
+        return ssd.ssd_bwd(xx, dd, A, bb, cc, yy, D, None, dfin, want_dinit=False, stream=stream)
+
+    for _ in range(args.warmup):
+        flush.zero_()
+        step()
+    torch.cuda.synchronize()
+    if world > 1:
+        dist.barrier()
+    torch.cuda.synchronize()
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
+    with ClockSampler(local_rank) as clk:
+        for i in range(args.steps):
+            flush.zero_()
+            ev[i][0].record(stream)
+            step()
+            ev[i][1].record(stream)
+        torch.cuda.synchronize()
+    ms = sum(a.elapsed_time(b) for a, b in ev) / args.steps
+
+    # end to end: inputs from pinned host memory, the gradients back to pinned host memory
+    hin = [t.cpu().pin_memory() for t in (x, dt, B, C, dy)]
+    h2d = sum(t.numel() * t.element_size() for t in hin)
+    din = [torch.empty_like(t) for t in (x, dt, B, C, dy)]
+    g0 = step()
+    hout = {k: torch.empty(v.shape, dtype=v.dtype).pin_memory() for k, v in g0.items() if v is not None}
+    d2h = sum(t.numel() * t.element_size() for t in hout.values())
+
+    def e2e_step():
+        for dst, src in zip(din, hin):
+            dst.copy_(src, non_blocking=True)
+        g = step(*din)
+        for k, t in hout.items():
+            t.copy_(g[k], non_blocking=True)
+
+    for _ in range(args.warmup):
+        e2e_step()
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(args.steps):
+        e2e_step()
+    e1.record(stream)
+    torch.cuda.synchronize()
+    e2e_ms = e0.elapsed_time(e1) / args.steps
+
+    t_tensor = torch.tensor([ms, e2e_ms], dtype=torch.float64, device=dev)
+    if world > 1:
+        dist.all_reduce(t_tensor, op=dist.ReduceOp.MAX)
+        dist.barrier()
+    ms_max, e2e_max = float(t_tensor[0]), float(t_tensor[1])
+    tokens = p.batch * p.seqlen
+    if rank == 0:
+        fl = bwd_flops(p)
+        achieved = fl / (ms / 1e3) / 1e12
+        line = {
+            "metric": BWD_METRIC, "value": world * tokens / (ms_max / 1e3), "unit": "tokens/s", "n_gpus": world,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_max, "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "f32", "data": "synthetic",
+            "config": {"workload": "bwd_" + p.name, "batch": p.batch, "seq_len": p.seqlen, "nheads": p.nheads,
+                       "headdim": p.headdim, "dstate": p.dstate, "ngroups": p.ngroups, "storage": p.dtype,
+                       "kernel": "ssd_bwd_chunk + ssd_bwd_reduce (CUDA cores, fp32)",
+                       "l2": "256 MiB write before every timed step; inputs larger than L2",
+                       "algorithmic_flops": fl},
+            "roofline": {"bound": "alu", "achieved": achieved, "peak": FP32_PEAK_TFLOPS, "unit": "TFLOP/s",
+                         "frac": achieved / FP32_PEAK_TFLOPS,
+                         "peak_source": "derived: 152 SMs x 128 fp32 lanes x 2 x 2.07 GHz", "traffic": None,
+                         "scope": "algorithmic fp32 flops of the whole ssd_bwd call (2 launches)"},
+            "e2e": {"value": world * tokens / (e2e_max / 1e3), "unit": "tokens/s", "h2d_bytes_per_step": h2d,
+                    "d2h_bytes_per_step": d2h},
+            "gpu_launches": 2 * args.steps,
+            "clocks": clk.summary(),
+        }
+        if world == 1 and not args.no_cpu_baseline:
+            line["cpu_baseline"] = bwd_cpu_baseline(p, dy_h)
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        dist.destroy_process_group()
+
+
+def bwd_sample(p, dy_h, tokens=512):
+    """One batch row, the first `tokens` tokens: the oracle backward's sample."""
+    q = synth.SSDProblem(1, tokens, p.nheads, p.headdim, p.dstate, p.ngroups, p.chunk, 0, p.dtype,
+                         p.x[:1, :tokens].copy(), p.dt[:1, :tokens].copy(), p.A, p.B[:1, :tokens].copy(),
+                         p.C[:1, :tokens].copy(), p.D, None, None, p.name)
+    return q, dy_h[:1, :tokens].copy()
+
+
+def bwd_cpu_baseline(p, dy_h):
+    import oracle
+    q, dyq = bwd_sample(p, dy_h)
+    reps, t_all = 0, 0.0
+    while t_all < 10.0 and reps < 8:
+        t0 = time.perf_counter()
+        oracle.ssd_backward(q, dyq)
+        t_all += time.perf_counter() - t0
+        reps += 1
+    return {"value": q.seqlen * reps / t_all, "unit": "tokens/s", "cores": oracle.max_threads(), "kind": "oracle",
+            "sample": f"fp64 reverse-mode recurrence, batch row 0, tokens 0..{q.seqlen - 1} of {p.name}, {reps} passes"}
+
+
 def run_ours(args):
     import torch
     import torch.distributed as dist
@@ -376,6 +533,8 @@ def run_ours(args):
     p = workload(args.workload)
     if p.seqlen == 1:
         return run_decode(args, p, dev, rank, local_rank, world)
+    if args.workload == "bwd":
+        return run_bwd(args, p, dev, rank, local_rank, world)
     dtype = torch.bfloat16 if p.dtype == "bf16" else torch.float32
 
     def dev_io(name):

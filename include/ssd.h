@@ -131,6 +131,46 @@ SSD_API int ssd_fwd_static_scratch(const ssd_params_t* p,
             const float* initial_states, const int32_t* cu_seqlens,
             void* y, float* final_states, void* stream);
 
+/* Bytes of device workspace ssd_bwd() needs for these parameters; 0 when the
+ * parameters are invalid or the backward pass does not support them. */
+SSD_API size_t ssd_bwd_workspace_size(const ssd_params_t* p);
+
+/* Backward pass of ssd_fwd(): the gradients of the scalar
+ *     <dy, y> + <dfinal_states, final_states>
+ * with respect to every input, where y and final_states are ssd_fwd()'s outputs
+ * for the same inputs.  The states are recomputed from the inputs, as "Parallel
+ * Scan and Hardware-Aware SSM Kernels" ("Why the kernel matters more than the
+ * algorithm") describes: only the state entering each backward chunk is kept, in
+ * the workspace.  Arithmetic is fp32 on CUDA cores (bf16 inputs are widened,
+ * bf16 gradients rounded once at the end).
+ *
+ * Inputs: x, dt, A, B, C, D (optional), initial_states (optional: zeros) exactly
+ * as for ssd_fwd(); dy (batch, seqlen, nheads, headdim) dtype;
+ * dfinal_states (batch, nheads, headdim, dstate) fp32 or NULL (zeros).
+ * Outputs (written, not accumulated into):
+ *   dx               (batch, seqlen, nheads, headdim)   dtype
+ *   ddt              (batch, seqlen, nheads)            fp32
+ *   dA               (nheads)                           fp32
+ *   dB, dC           (batch, seqlen, ngroups, dstate)   dtype (summed over each group's heads)
+ *   dD               (nheads) fp32, or NULL; written only when D is given
+ *   dinitial_states  (batch, nheads, headdim, dstate)   fp32, or NULL
+ * All pointers are device memory with 16-byte aligned bases; no output may equal
+ * an input.  Packed documents (cu_seqlens) are not supported by the backward
+ * pass: cu_seqlens != NULL or ndocs != 0 returns SSD_ERR_UNSUPPORTED, as do
+ * headdim * dstate > 8192 and shapes whose tiles do not fit in shared memory.
+ * `chunk` and `split_len` in p are validated but do not change the result.
+ * `workspace`: at least ssd_bwd_workspace_size(p) bytes, 256-byte aligned
+ * (else SSD_ERR_WORKSPACE).  Asynchronous on `stream`; two launches; no
+ * device-side waits.  Bitwise deterministic (fixed summation orders). */
+SSD_API int ssd_bwd(const ssd_params_t* p,
+            const void* x, const float* dt, const float* A,
+            const void* B, const void* C, const float* D,
+            const float* initial_states, const int32_t* cu_seqlens,
+            const void* dy, const float* dfinal_states,
+            void* dx, float* ddt, float* dA, void* dB, void* dC, float* dD,
+            float* dinitial_states,
+            void* workspace, size_t workspace_bytes, void* stream);
+
 /* One autoregressive (decode) step: a single new token per batch row from a
  * resident state.  "State Space Duality and Mamba-2", section "Performance and
  * Serving Economics": generation keeps a fixed-size recurrent state and costs

@@ -33,7 +33,7 @@ def __getattr__(name):
         return _lib.SSDError
     raise AttributeError(name)
 
-__all__ = ["ssd_fwd", "SSDForward", "ssd_step", "segsum_dump", "check_status", "SSDError", "plan"]
+__all__ = ["ssd_fwd", "SSDForward", "ssd_bwd", "ssd_step", "segsum_dump", "check_status", "SSDError", "plan"]
 
 
 def _ptr(t: Optional[torch.Tensor]):
@@ -132,6 +132,43 @@ def ssd_fwd(x, dt, A, B, C, D=None, initial_states=None, cu_seqlens=None, *, chu
     if st != 0:
         raise _lib.SSDError(st, "ssd_fwd device status")
     return (y, fin) if return_final_states else y
+
+
+def ssd_bwd(x, dt, A, B, C, dy, D=None, initial_states=None, dfinal_states=None, *, chunk=128,
+            want_dinit=True, stream=None):
+    """Gradients of <dy, y> + <dfinal_states, final_states> for one ssd_fwd
+    call's inputs (batch rows, no packed documents).  Returns a dict with dx,
+    ddt, dA, dB, dC, dD (None without D) and dinit (None unless asked)."""
+    batch, seqlen, nheads, headdim = x.shape
+    ngroups, dstate = B.shape[2], B.shape[3]
+    dev = x.device
+    params = _lib.make_params(batch, seqlen, nheads, headdim, dstate, ngroups, chunk, 0, 0, _dtype_code(x))
+    shp_x, shp_bc = (batch, seqlen, nheads, headdim), (batch, seqlen, ngroups, dstate)
+    shp_s = (batch, nheads, headdim, dstate)
+    for name, t, shp, dt_ in (("x", x, shp_x, x.dtype), ("dt", dt, shp_x[:3], torch.float32),
+                              ("A", A, (nheads,), torch.float32), ("B", B, shp_bc, x.dtype),
+                              ("C", C, shp_bc, x.dtype), ("dy", dy, shp_x, x.dtype),
+                              ("D", D, (nheads,), torch.float32),
+                              ("initial_states", initial_states, shp_s, torch.float32),
+                              ("dfinal_states", dfinal_states, shp_s, torch.float32)):
+        if t is None:
+            continue
+        if tuple(t.shape) != shp or t.dtype != dt_ or not t.is_contiguous() or t.device != dev:
+            raise ValueError(f"{name}: expected contiguous {dt_} {shp} on {dev}, got "
+                             f"{t.dtype} {tuple(t.shape)} on {t.device}")
+    nbytes = int(_lib.lib.ssd_bwd_workspace_size(ctypes.byref(params)))
+    if nbytes == 0:
+        raise _lib.SSDError(2, "ssd_bwd: unsupported parameters")
+    ws = torch.empty(nbytes, dtype=torch.uint8, device=dev)
+    g = dict(dx=torch.empty_like(x), ddt=torch.empty_like(dt), dA=torch.empty_like(A),
+             dB=torch.empty_like(B), dC=torch.empty_like(C), dD=None if D is None else torch.empty_like(D),
+             dinit=torch.empty(shp_s, dtype=torch.float32, device=dev) if want_dinit else None)
+    rc = _lib.lib.ssd_bwd(ctypes.byref(params), _ptr(x), _ptr(dt), _ptr(A), _ptr(B), _ptr(C), _ptr(D),
+                          _ptr(initial_states), None, _ptr(dy), _ptr(dfinal_states), _ptr(g["dx"]),
+                          _ptr(g["ddt"]), _ptr(g["dA"]), _ptr(g["dB"]), _ptr(g["dC"]), _ptr(g["dD"]),
+                          _ptr(g["dinit"]), _ptr(ws), nbytes, _stream_handle(stream))
+    _lib.check(rc, "ssd_bwd")
+    return g
 
 
 def ssd_step(state, x, dt, A, B, C, D=None, *, state_out=None, y=None, stream=None):

@@ -148,6 +148,31 @@ WsLayout layout_for(const ssd_params_t* p, int ns, const TailPlan& tp) {
     return ws_layout(p->batch, p->nheads, p->headdim, p->dstate, ns);
 }
 
+// Backward workspace: status header, the state entering every backward chunk,
+// the per-head shares of dB and dC, and the per-row shares of dA and dD.
+struct BwdLayout {
+    int Qb = 0;
+    size_t ckpt = 0, dB = 0, dC = 0, dA = 0, dD = 0, total = 0;
+};
+
+bool bwd_layout(const ssd_params_t* p, BwdLayout* l) {
+    if (check_params(p) != SSD_OK || p->ndocs != 0) return false;
+    l->Qb = bwd_chunk(p->headdim, p->dstate, kSmemLimit);
+    if (l->Qb == 0) return false;
+    const size_t bh = (size_t)p->batch * p->nheads;
+    const size_t nch = (size_t)((p->seqlen + l->Qb - 1) / l->Qb);
+    const size_t PN = (size_t)p->headdim * p->dstate;
+    const size_t share = (size_t)p->batch * p->seqlen * p->nheads * p->dstate;
+    size_t o = sizeof(WsHeader);
+    l->ckpt = o;  o = align_up(o + bh * nch * PN * sizeof(float), 256);
+    l->dB = o;    o = align_up(o + share * sizeof(float), 256);
+    l->dC = o;    o = align_up(o + share * sizeof(float), 256);
+    l->dA = o;    o = align_up(o + bh * sizeof(float), 256);
+    l->dD = o;    o = align_up(o + bh * sizeof(float), 256);
+    l->total = o;
+    return true;
+}
+
 }  // namespace
 
 // ---------------------------------------------------------------------------
@@ -328,6 +353,51 @@ int ssd_fwd_static_scratch(const ssd_params_t* p, const void* x, const float* dt
     if (rc != SSD_OK) return rc;
     // synchronous: wait for the work and report what the device recorded
     return ssd_check_status(ws, stream);
+}
+
+size_t ssd_bwd_workspace_size(const ssd_params_t* p) {
+    BwdLayout l;
+    return bwd_layout(p, &l) ? l.total : 0;
+}
+
+int ssd_bwd(const ssd_params_t* p, const void* x, const float* dt, const float* A, const void* B,
+            const void* C, const float* D, const float* init, const int32_t* cu, const void* dy,
+            const float* dfin, void* dx, float* ddt, float* dA, void* dB, void* dC, float* dD,
+            float* dinit, void* workspace, size_t workspace_bytes, void* stream) {
+    int rc = check_params(p);
+    if (rc != SSD_OK) return rc;
+    if (cu || p->ndocs != 0) return SSD_ERR_UNSUPPORTED;   // packed documents: forward only
+    if (bwd_chunk(p->headdim, p->dstate, kSmemLimit) == 0) return SSD_ERR_UNSUPPORTED;
+    if (p->batch * p->nheads >= ((int64_t)1 << 31)) return SSD_ERR_UNSUPPORTED;
+    if (!x || !dt || !A || !B || !C || !dy || !dx || !ddt || !dA || !dB || !dC) return SSD_ERR_INVALID_ARG;
+    const void* in[] = {x, dt, A, B, C, D, init, dy, dfin};
+    const void* out[] = {dx, ddt, dA, dB, dC, dD, dinit};
+    for (const void* q : in)
+        if (q && !aligned(q, 16)) return SSD_ERR_INVALID_ARG;
+    for (const void* q : out) {
+        if (q && !aligned(q, 16)) return SSD_ERR_INVALID_ARG;
+        for (const void* r : in)
+            if (q && q == r) return SSD_ERR_INVALID_ARG;   // outputs never alias inputs
+    }
+    BwdLayout l;
+    if (!bwd_layout(p, &l)) return SSD_ERR_UNSUPPORTED;
+    if (!workspace || workspace_bytes < l.total || !aligned(workspace, 256)) return SSD_ERR_WORKSPACE;
+    BwdArgs a;
+    memset(&a, 0, sizeof(a));
+    a.batch = p->batch; a.L = p->seqlen;
+    a.H = p->nheads; a.P = p->headdim; a.N = p->dstate; a.G = p->ngroups;
+    a.Qb = l.Qb;
+    a.dtype = p->dtype;
+    a.x = x; a.dt = dt; a.A = A; a.B = B; a.C = C; a.D = D; a.init = init; a.dy = dy; a.dfin = dfin;
+    a.dx = dx; a.ddt = ddt; a.dA = dA; a.dB = dB; a.dC = dC; a.dD = D ? dD : nullptr; a.dinit = dinit;
+    char* ws = static_cast<char*>(workspace);
+    a.ws_ckpt = (float*)(ws + l.ckpt);
+    a.ws_dB = (float*)(ws + l.dB);
+    a.ws_dC = (float*)(ws + l.dC);
+    a.ws_dA = (float*)(ws + l.dA);
+    a.ws_dD = (float*)(ws + l.dD);
+    if (launch_bwd(a, (cudaStream_t)stream) != cudaSuccess) return SSD_ERR_CUDA;
+    return SSD_OK;
 }
 
 int ssd_step(int64_t batch, int32_t nheads, int32_t headdim, int32_t dstate, int32_t ngroups, int32_t dtype,

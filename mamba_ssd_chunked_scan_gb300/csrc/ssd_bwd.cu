@@ -1,0 +1,436 @@
+// Backward pass of the SSD forward by recomputation (CUDA cores, fp32):
+//   ssd_bwd_chunk       per (batch row, head): recompute the state entering
+//                       every backward chunk, then walk the chunks backwards
+//                       carrying the state's adjoint, and form every gradient
+//                       of the chunk in the chunked (matrix) form
+//   ssd_bwd_reduce      sums the per-head dB, dC shares over each group's
+//                       heads and the per-row dA, dD shares over the batch
+//
+// "Parallel Scan and Hardware-Aware SSM Kernels", "Why the kernel matters more
+// than the algorithm": the backward pass recomputes the states from the saved
+// inputs instead of storing one per token.  Here only the state entering each
+// chunk of Qb tokens is kept (P x N fp32 per chunk, in the workspace).
+//
+// Within a chunk (tokens i, j, t; l_t = dt_t A_h; p_i = sum_{k<=i} l_k and
+// s_j = sum_{k>j} l_k within the chunk, tau = the chunk total; L_ij =
+// exp(sum_{k=j+1..i} l_k) for j <= i; S_in the state entering the chunk and
+// Lam the adjoint of the state leaving it), with G_ij = C_i . B_j and
+// X_ij = dy_i . x_j, the reverse-mode derivatives of the recurrence are
+//   v_j   = sum_{i>=j} L_ij G_ij dy_i + e^{s_j} Lam B_j       (= Lam_j B_j)
+//   dx_j  = dt_j v_j + D dy_j
+//   dB_j  = dt_j (sum_{i>=j} L_ij X_ij C_i + e^{s_j} Lam^T x_j)
+//   dC_i  = sum_{j<=i} L_ij dt_j X_ij B_j + e^{p_i} S_in^T dy_i
+//   dl_t  = <Lam_t, S_t> - dt_t x_t . v_t, where
+//   <Lam_t, S_t> = sum_{j<=t<=i} L_ij dt_j X_ij G_ij + sum_{i>=t} e^{p_i} dy_i . S_in C_i
+//                + sum_{j<=t} e^{s_j} dt_j x_j . Lam B_j + e^{tau} <Lam, S_in>
+//   ddt_t = x_t . v_t + A dl_t,  dA += dt_t dl_t,  dD += dy_t . x_t
+//   Lam  <- e^{tau} Lam + sum_i e^{p_i} dy_i C_i^T            (adjoint of S_in)
+// Every sum of log-decays is a direct sum (no prefix subtraction).
+#include "ssd_common.cuh"
+#include "ssd_kernels.h"
+
+namespace ssd {
+namespace {
+
+constexpr int kBwdThreads = 256;
+constexpr int kBwdOwn = 32;   // state elements each thread keeps in registers (P * N <= 8192)
+
+struct BwdSmem {
+    int Qb, P, N, sx, sb;      // chunk, sizes, padded row strides of x/dy and B/S_in/Lam
+    size_t x, dy, B, C, Sin, Lam, A1, A2, W, vx, lbx, scdy, dts, ell, ep, es, ddta, wv, uv, rv, red, total;
+};
+
+__host__ __device__ inline BwdSmem bwd_smem(int Qb, int P, int N) {
+    BwdSmem s;
+    s.Qb = Qb; s.P = P; s.N = N;
+    s.sx = P + 1;              // odd strides: column walks hit distinct banks
+    s.sb = N + 1;
+    size_t o = 0;
+    s.x = o;    o += (size_t)Qb * s.sx;
+    s.dy = o;   o += (size_t)Qb * s.sx;
+    s.B = o;    o += (size_t)Qb * s.sb;
+    s.C = o;    o += (size_t)Qb * N;
+    s.Sin = o;  o += (size_t)P * s.sb;
+    s.Lam = o;  o += (size_t)P * s.sb;
+    s.A1 = o;   o += (size_t)Qb * Qb;      // L_ij G_ij
+    s.A2 = o;   o += (size_t)Qb * Qb;      // L_ij X_ij
+    s.W = o;    o += (size_t)Qb * Qb;      // L_ij dt_j X_ij G_ij
+    s.vx = o;   o += (size_t)Qb * P;       // v_j[p] x_j[p]
+    s.lbx = o;  o += (size_t)Qb * P;       // (Lam B_j)[p] x_j[p]
+    s.scdy = o; o += (size_t)Qb * P;       // (S_in C_i)[p] dy_i[p]
+    s.dts = o;  o += Qb;
+    s.ell = o;  o += Qb;
+    s.ep = o;   o += Qb;
+    s.es = o;   o += Qb;
+    s.ddta = o; o += Qb;
+    s.wv = o;   o += Qb;
+    s.uv = o;   o += Qb;
+    s.rv = o;   o += Qb;
+    s.red = o;  o += 2 * (kBwdThreads / 32);
+    s.total = o * sizeof(float);
+    return s;
+}
+
+__device__ __forceinline__ float warp_sum(float v) {
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+    return v;
+}
+
+// Block-wide sum (every thread gets the result); `red` holds 8 floats.
+__device__ __forceinline__ float block_sum(float v, float* red) {
+    v = warp_sum(v);
+    const int w = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    __syncthreads();
+    if (lane == 0) red[w] = v;
+    __syncthreads();
+    float s = 0.f;
+#pragma unroll
+    for (int k = 0; k < kBwdThreads / 32; ++k) s += red[k];
+    return s;
+}
+
+template <typename T>
+__global__ void __launch_bounds__(kBwdThreads) ssd_bwd_chunk(BwdArgs a) {
+    extern __shared__ float sm[];
+    const BwdSmem L = bwd_smem(a.Qb, a.P, a.N);
+    const int Qb = a.Qb, P = a.P, N = a.N, H = a.H, G = a.G;
+    const int PN = P * N;
+    float* xs = sm + L.x;
+    float* dys = sm + L.dy;
+    float* Bs = sm + L.B;
+    float* Cs = sm + L.C;
+    float* Sin = sm + L.Sin;
+    float* Lam = sm + L.Lam;
+    float* A1 = sm + L.A1;
+    float* A2 = sm + L.A2;
+    float* Wm = sm + L.W;
+    float* vx = sm + L.vx;
+    float* lbx = sm + L.lbx;
+    float* scdy = sm + L.scdy;
+    float* dts = sm + L.dts;
+    float* ell = sm + L.ell;
+    float* ep = sm + L.ep;
+    float* es = sm + L.es;
+    float* ddta = sm + L.ddta;
+    float* wv = sm + L.wv;
+    float* uv = sm + L.uv;
+    float* rv = sm + L.rv;
+    float* red = sm + L.red;
+
+    const int tid = threadIdx.x;
+    const int64_t unit = blockIdx.x;               // b * H + h
+    const int h = (int)(unit % H);
+    const int64_t b = unit / H;
+    const int g = h / (H / G);
+    const float Ah = a.A[h];
+    const float Dh = a.D ? a.D[h] : 0.f;
+    const int64_t Lseq = a.L;
+    const int nch = (int)((Lseq + Qb - 1) / Qb);
+    const T* x = static_cast<const T*>(a.x);
+    const T* Bg = static_cast<const T*>(a.B);
+    const T* Cg = static_cast<const T*>(a.C);
+    const T* dy = static_cast<const T*>(a.dy);
+    float* ckpt = a.ws_ckpt + (size_t)unit * nch * PN;
+
+    // token row k of this chunk: x / dy row, B / C row (zeros past the end)
+    auto xrow = [&](int64_t t) { return x + ((size_t)(b * Lseq + t) * H + h) * P; };
+    auto dyrow = [&](int64_t t) { return dy + ((size_t)(b * Lseq + t) * H + h) * P; };
+    auto bcoff = [&](int64_t t) { return ((size_t)(b * Lseq + t) * G + g) * N; };
+
+    // ------------------------------------------------------------ phase 1
+    // forward over the chunks: the state entering each chunk, kept in the workspace
+    float S[kBwdOwn];
+#pragma unroll
+    for (int r = 0; r < kBwdOwn; ++r) {
+        const int e = tid + kBwdThreads * r;
+        S[r] = (e < PN && a.init) ? a.init[(size_t)unit * PN + e] : 0.f;
+    }
+    for (int c = 0; c < nch; ++c) {
+        const int64_t t0 = (int64_t)c * Qb;
+#pragma unroll
+        for (int r = 0; r < kBwdOwn; ++r) {
+            const int e = tid + kBwdThreads * r;
+            if (e < PN) ckpt[(size_t)c * PN + e] = S[r];
+        }
+        __syncthreads();   // the previous chunk's tile reads are done
+        for (int k = tid; k < Qb * P; k += kBwdThreads) {
+            const int i = k / P, p = k - i * P;
+            xs[i * L.sx + p] = (t0 + i < Lseq) ? Elem<T>::load(xrow(t0 + i) + p) : 0.f;
+        }
+        for (int k = tid; k < Qb * N; k += kBwdThreads) {
+            const int i = k / N, n = k - i * N;
+            Bs[i * L.sb + n] = (t0 + i < Lseq) ? Elem<T>::load(Bg + bcoff(t0 + i) + n) : 0.f;
+        }
+        if (tid < Qb) {
+            const float d = (t0 + tid < Lseq) ? a.dt[(size_t)(b * Lseq + t0 + tid) * H + h] : 0.f;
+            dts[tid] = d;
+            ell[tid] = d * Ah;
+        }
+        __syncthreads();
+        if (tid < Qb) {
+            float s = 0.f;                          // s_t: the log-decays after t in the chunk
+            for (int k = tid + 1; k < Qb; ++k) s += ell[k];
+            es[tid] = expf(s) * dts[tid];           // the weight of token t's input in the chunk's end state
+        }
+        if (tid == 0) {
+            float tau = 0.f;
+            for (int k = 0; k < Qb; ++k) tau += ell[k];
+            red[0] = expf(tau);
+        }
+        __syncthreads();
+        const float etau = red[0];
+#pragma unroll
+        for (int r = 0; r < kBwdOwn; ++r) {
+            const int e = tid + kBwdThreads * r;
+            if (e < PN) {
+                const int p = e / N, n = e - p * N;
+                float acc = etau * S[r];
+                for (int j = 0; j < Qb; ++j) acc = fmaf(es[j] * xs[j * L.sx + p], Bs[j * L.sb + n], acc);
+                S[r] = acc;
+            }
+        }
+    }
+
+    // ------------------------------------------------------------ phase 2
+    // backward over the chunks, carrying Lam (the adjoint of the state leaving the chunk)
+    float Lr[kBwdOwn];
+#pragma unroll
+    for (int r = 0; r < kBwdOwn; ++r) {
+        const int e = tid + kBwdThreads * r;
+        Lr[r] = (e < PN && a.dfin) ? a.dfin[(size_t)unit * PN + e] : 0.f;
+    }
+    float dA_acc = 0.f, dD_acc = 0.f;    // thread 0's running sums
+    for (int c = nch - 1; c >= 0; --c) {
+        const int64_t t0 = (int64_t)c * Qb;
+        __syncthreads();   // the previous chunk's shared-memory reads are done
+        for (int k = tid; k < Qb * P; k += kBwdThreads) {
+            const int i = k / P, p = k - i * P;
+            const bool ok = t0 + i < Lseq;
+            xs[i * L.sx + p] = ok ? Elem<T>::load(xrow(t0 + i) + p) : 0.f;
+            dys[i * L.sx + p] = ok ? Elem<T>::load(dyrow(t0 + i) + p) : 0.f;
+        }
+        for (int k = tid; k < Qb * N; k += kBwdThreads) {
+            const int i = k / N, n = k - i * N;
+            const bool ok = t0 + i < Lseq;
+            Bs[i * L.sb + n] = ok ? Elem<T>::load(Bg + bcoff(t0 + i) + n) : 0.f;
+            Cs[i * N + n] = ok ? Elem<T>::load(Cg + bcoff(t0 + i) + n) : 0.f;
+        }
+        float kdot = 0.f;   // this thread's share of <Lam, S_in>
+#pragma unroll
+        for (int r = 0; r < kBwdOwn; ++r) {
+            const int e = tid + kBwdThreads * r;
+            if (e < PN) {
+                const int p = e / N, n = e - p * N;
+                const float sv = ckpt[(size_t)c * PN + e];
+                Sin[p * L.sb + n] = sv;
+                Lam[p * L.sb + n] = Lr[r];
+                kdot = fmaf(Lr[r], sv, kdot);
+            }
+        }
+        if (tid < Qb) {
+            const float d = (t0 + tid < Lseq) ? a.dt[(size_t)(b * Lseq + t0 + tid) * H + h] : 0.f;
+            dts[tid] = d;
+            ell[tid] = d * Ah;
+        }
+        const float K = block_sum(kdot, red);   // (contains a barrier: the tiles are visible)
+        if (tid < Qb) {
+            float pfx = 0.f, sfx = 0.f;
+            for (int k = 0; k <= tid; ++k) pfx += ell[k];
+            for (int k = tid + 1; k < Qb; ++k) sfx += ell[k];
+            ep[tid] = expf(pfx);
+            es[tid] = expf(sfx);
+        }
+        float tau = 0.f;
+        for (int k = 0; k < Qb; ++k) tau += ell[k];
+        const float etau = expf(tau);
+        // pair quantities (i, j): L_ij by a direct sum, G_ij, X_ij
+        for (int q = tid; q < Qb * Qb; q += kBwdThreads) {
+            const int i = q / Qb, j = q - i * Qb;
+            float a1 = 0.f, a2 = 0.f, w = 0.f;
+            if (j <= i) {
+                float seg = 0.f;
+                for (int k = j + 1; k <= i; ++k) seg += ell[k];
+                const float Lij = expf(seg);
+                float gij = 0.f, xij = 0.f;
+                for (int n = 0; n < N; ++n) gij = fmaf(Cs[i * N + n], Bs[j * L.sb + n], gij);
+                for (int p = 0; p < P; ++p) xij = fmaf(dys[i * L.sx + p], xs[j * L.sx + p], xij);
+                a1 = Lij * gij;
+                a2 = Lij * xij;
+                w = a1 * dts[j] * xij;
+            }
+            A1[q] = a1;
+            A2[q] = a2;
+            Wm[q] = w;
+        }
+        __syncthreads();
+        // dx, and the per-token dot products of ddt
+        for (int q = tid; q < Qb * P; q += kBwdThreads) {
+            const int j = q / P, p = q - j * P;
+            float lb = 0.f;
+            for (int n = 0; n < N; ++n) lb = fmaf(Lam[p * L.sb + n], Bs[j * L.sb + n], lb);
+            float v = es[j] * lb;
+            for (int i = j; i < Qb; ++i) v = fmaf(A1[i * Qb + j], dys[i * L.sx + p], v);
+            const float xv = xs[j * L.sx + p];
+            vx[q] = v * xv;
+            lbx[q] = lb * xv;
+            float sc = 0.f;   // (S_in C_j)[p], for the row j as an output row
+            for (int n = 0; n < N; ++n) sc = fmaf(Sin[p * L.sb + n], Cs[j * N + n], sc);
+            scdy[q] = sc * dys[j * L.sx + p];
+            if (t0 + j < Lseq)
+                Elem<T>::store(static_cast<T*>(a.dx) + ((size_t)(b * Lseq + t0 + j) * H + h) * P + p,
+                               fmaf(dts[j], v, Dh * dys[j * L.sx + p]));
+        }
+        // this head's shares of dB and dC
+        for (int q = tid; q < Qb * N; q += kBwdThreads) {
+            const int j = q / N, n = q - j * N;
+            if (t0 + j >= Lseq) continue;
+            float lx = 0.f, sd = 0.f;
+            for (int p = 0; p < P; ++p) {
+                lx = fmaf(Lam[p * L.sb + n], xs[j * L.sx + p], lx);
+                sd = fmaf(Sin[p * L.sb + n], dys[j * L.sx + p], sd);
+            }
+            float db = es[j] * lx;
+            for (int i = j; i < Qb; ++i) db = fmaf(A2[i * Qb + j], Cs[i * N + n], db);
+            float dc = ep[j] * sd;
+            for (int k = 0; k <= j; ++k) dc = fmaf(A2[j * Qb + k] * dts[k], Bs[k * L.sb + n], dc);
+            const size_t o = ((size_t)(b * Lseq + t0 + j) * H + h) * N + n;
+            a.ws_dB[o] = dts[j] * db;
+            a.ws_dC[o] = dc;
+        }
+        __syncthreads();
+        // per-token reductions (warp w takes tokens w, w + 8, ...)
+        {
+            const int w = tid >> 5, lane = tid & 31;
+            for (int t = w; t < Qb; t += kBwdThreads / 32) {
+                float s1 = 0.f, s2 = 0.f, s3 = 0.f, s4 = 0.f;
+                for (int p = lane; p < P; p += 32) {
+                    s1 += vx[t * P + p];
+                    s2 += lbx[t * P + p];
+                    s3 += scdy[t * P + p];
+                }
+                for (int i = t + lane; i < Qb; i += 32)
+                    for (int j = 0; j <= t; ++j) s4 += Wm[i * Qb + j];
+                s1 = warp_sum(s1);
+                s2 = warp_sum(s2);
+                s3 = warp_sum(s3);
+                s4 = warp_sum(s4);
+                if (lane == 0) {
+                    ddta[t] = s1;
+                    wv[t] = es[t] * dts[t] * s2;
+                    uv[t] = ep[t] * s3;
+                    rv[t] = s4;
+                }
+            }
+        }
+        __syncthreads();
+        if (tid < Qb) {
+            const int t = tid;
+            float U = 0.f, V = 0.f;
+            for (int i = t; i < Qb; ++i) U += uv[i];
+            for (int j = 0; j <= t; ++j) V += wv[j];
+            const float dl = rv[t] + U + V + etau * K - dts[t] * ddta[t];
+            if (t0 + t < Lseq) a.ddt[(size_t)(b * Lseq + t0 + t) * H + h] = fmaf(Ah, dl, ddta[t]);
+            float da = dts[t] * dl;
+            float dd = 0.f;
+            for (int p = 0; p < P; ++p) dd = fmaf(dys[t * L.sx + p], xs[t * L.sx + p], dd);
+            // lanes 0..Qb-1 of warps 0-1: fixed-order reduction through shared memory
+            ddta[t] = da;
+            wv[t] = dd;
+        }
+        __syncthreads();
+        if (tid == 0) {
+            for (int t = 0; t < Qb; ++t) {
+                dA_acc += ddta[t];
+                dD_acc += wv[t];
+            }
+        }
+        // Lam becomes the adjoint of the state entering this chunk
+#pragma unroll
+        for (int r = 0; r < kBwdOwn; ++r) {
+            const int e = tid + kBwdThreads * r;
+            if (e < PN) {
+                const int p = e / N, n = e - p * N;
+                float acc = etau * Lr[r];
+                for (int i = 0; i < Qb; ++i) acc = fmaf(ep[i] * dys[i * L.sx + p], Cs[i * N + n], acc);
+                Lr[r] = acc;
+            }
+        }
+    }
+    if (a.dinit) {
+#pragma unroll
+        for (int r = 0; r < kBwdOwn; ++r) {
+            const int e = tid + kBwdThreads * r;
+            if (e < PN) a.dinit[(size_t)unit * PN + e] = Lr[r];
+        }
+    }
+    if (tid == 0) {
+        a.ws_dA[unit] = dA_acc;
+        a.ws_dD[unit] = dD_acc;
+    }
+}
+
+// dB, dC (batch, L, G, N) = sums over each group's heads of the per-head shares;
+// dA, dD (H) = sums over the batch rows.  Fixed summation order.
+template <typename T>
+__global__ void __launch_bounds__(256) ssd_bwd_reduce(BwdArgs a) {
+    const int64_t total = a.batch * a.L * a.G * a.N;
+    const int hpg = a.H / a.G;
+    for (int64_t k = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; k < total; k += (int64_t)gridDim.x * blockDim.x) {
+        const int n = (int)(k % a.N);
+        const int64_t rest = k / a.N;
+        const int g = (int)(rest % a.G);
+        const int64_t bt = rest / a.G;   // b * L + t
+        float sb = 0.f, sc = 0.f;
+        for (int hh = 0; hh < hpg; ++hh) {
+            const size_t o = ((size_t)bt * a.H + g * hpg + hh) * a.N + n;
+            sb += a.ws_dB[o];
+            sc += a.ws_dC[o];
+        }
+        Elem<T>::store(static_cast<T*>(a.dB) + k, sb);
+        Elem<T>::store(static_cast<T*>(a.dC) + k, sc);
+    }
+    if (blockIdx.x == 0) {
+        for (int h = threadIdx.x; h < a.H; h += blockDim.x) {
+            float sa = 0.f, sd = 0.f;
+            for (int64_t b = 0; b < a.batch; ++b) {
+                sa += a.ws_dA[b * a.H + h];
+                sd += a.ws_dD[b * a.H + h];
+            }
+            a.dA[h] = sa;
+            if (a.dD) a.dD[h] = sd;
+        }
+    }
+}
+
+}  // namespace
+
+size_t bwd_smem_bytes(int Qb, int P, int N) { return bwd_smem(Qb, P, N).total; }
+
+int bwd_chunk(int P, int N, size_t smem_limit) {
+    if (P * N > kBwdThreads * kBwdOwn) return 0;
+    for (int Qb = 64; Qb >= 8; Qb >>= 1)
+        if (bwd_smem_bytes(Qb, P, N) <= smem_limit) return Qb;
+    return 0;
+}
+
+cudaError_t launch_bwd(const BwdArgs& a, cudaStream_t st) {
+    const size_t smem = bwd_smem_bytes(a.Qb, a.P, a.N);
+    auto k1 = a.dtype == SSD_BF16 ? ssd_bwd_chunk<__nv_bfloat16> : ssd_bwd_chunk<float>;
+    cudaError_t e = cudaFuncSetAttribute(k1, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (e != cudaSuccess) return e;
+    k1<<<(unsigned)(a.batch * a.H), kBwdThreads, smem, st>>>(a);
+    if ((e = cudaGetLastError()) != cudaSuccess) return e;
+    int dev = 0, nsm = 0;
+    cudaGetDevice(&dev);
+    cudaDeviceGetAttribute(&nsm, cudaDevAttrMultiProcessorCount, dev);
+    const int64_t total = a.batch * a.L * a.G * a.N;
+    int64_t blocks = (total + 255) / 256;
+    if (blocks > (int64_t)nsm * 8) blocks = (int64_t)nsm * 8;
+    if (blocks < 1) blocks = 1;
+    auto k2 = a.dtype == SSD_BF16 ? ssd_bwd_reduce<__nv_bfloat16> : ssd_bwd_reduce<float>;
+    k2<<<(unsigned)blocks, 256, 0, st>>>(a);
+    return cudaGetLastError();
+}
+
+}  // namespace ssd

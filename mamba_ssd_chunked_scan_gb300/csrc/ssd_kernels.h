@@ -59,6 +59,35 @@ struct StepArgs {
     void* y;
 };
 
+// Backward pass (ssd_bwd): everything its two launches need.
+struct BwdArgs {
+    int64_t batch, L;
+    int H, P, N, G;
+    int Qb;                // backward chunk (tokens)
+    int dtype;             // ssd_dtype_t of x, B, C, dy, dx, dB, dC
+    const void* x;
+    const float* dt;
+    const float* A;
+    const void* B;
+    const void* C;
+    const float* D;
+    const float* init;
+    const void* dy;
+    const float* dfin;
+    void* dx;
+    float* ddt;
+    float* dA;
+    void* dB;
+    void* dC;
+    float* dD;
+    float* dinit;
+    float* ws_ckpt;        // [batch * H * nchunks * P * N] state entering each chunk
+    float* ws_dB;          // [batch * L * H * N] per-head shares of dB
+    float* ws_dC;          // [batch * L * H * N] per-head shares of dC
+    float* ws_dA;          // [batch * H]
+    float* ws_dD;          // [batch * H]
+};
+
 // Constants of division by an invariant divisor d >= 1 through one high
 // multiply and a shift (Granlund and Montgomery, "Division by Invariant
 // Integers using Multiplication", 1994): l = ceil(log2 d),
@@ -77,6 +106,9 @@ cudaError_t launch_split_scan(const FwdArgs& a, cudaStream_t st);
 size_t tc_smem_bytes();
 bool tc_supported(int P, int N, int Q, int dtype);
 cudaError_t launch_tc(const FwdArgs& a, cudaStream_t st);
+size_t bwd_smem_bytes(int Qb, int P, int N);
+int bwd_chunk(int P, int N, size_t smem_limit);
+cudaError_t launch_bwd(const BwdArgs& a, cudaStream_t st);
 size_t step_smem_bytes(int P, int N);
 cudaError_t launch_step(const StepArgs& a, cudaStream_t st);
 cudaError_t launch_segsum_dump(const float* l2, int64_t nrows, int chunk, float* seg, float* L,

@@ -149,3 +149,40 @@ def call_step(L, d):
 ])
 def test_step_invalid_args(L, kw, code):
     assert call_step(L, step_args(L, **kw)) == code
+
+
+def test_bwd_workspace_size(L):
+    p = params(L, batch=2, seqlen=1000, nheads=4)
+    n = L.lib.ssd_bwd_workspace_size(ctypes.byref(p))
+    # status header + chunk-entry states (32-token chunks) + dB, dC shares + dA, dD shares
+    assert n >= 256 + 2 * 4 * 32 * 64 * 128 * 4 + 2 * 2 * 1000 * 4 * 128 * 4 + 2 * 8 * 4
+    assert L.lib.ssd_bwd_workspace_size(ctypes.byref(params(L, ndocs=3, batch=1))) == 0   # packed documents
+    assert L.lib.ssd_bwd_workspace_size(ctypes.byref(params(L, headdim=128, dstate=128))) == 0   # P * N > 8192
+
+
+@pytest.mark.parametrize("case,code", [("docs", 2), ("null_dx", 1), ("alias", 1), ("misaligned", 1),
+                                       ("no_ws", 3)])
+def test_bwd_invalid_args(L, case, code):
+    base = 1 << 40
+    ptr = {k: base + (i << 30) for i, k in enumerate(
+        ("x", "dt", "A", "B", "C", "D", "dy", "dx", "ddt", "dA", "dB", "dC", "ws"))}
+    p = params(L, batch=2, seqlen=256, nheads=4)
+    cu = None
+    if case == "docs":
+        p = params(L, batch=1, seqlen=256, nheads=4, ndocs=2)
+        cu = base + (40 << 30)
+    if case == "null_dx":
+        ptr["dx"] = None
+    if case == "alias":
+        ptr["dB"] = ptr["B"]
+    if case == "misaligned":
+        ptr["ddt"] += 4
+    nbytes = L.lib.ssd_bwd_workspace_size(ctypes.byref(p))
+    if case == "no_ws":
+        ptr["ws"], nbytes = None, 0
+    vp = ctypes.c_void_p
+    v = lambda k: None if ptr[k] is None else vp(ptr[k])
+    rc = L.lib.ssd_bwd(ctypes.byref(p), v("x"), v("dt"), v("A"), v("B"), v("C"), v("D"), None,
+                       None if cu is None else vp(cu), v("dy"), None, v("dx"), v("ddt"), v("dA"), v("dB"),
+                       v("dC"), None, None, v("ws"), nbytes, None)
+    assert rc == code
