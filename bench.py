@@ -2,7 +2,7 @@
 """Benchmark of the SSD forward pass (one JSON line on rank 0).
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
-                    [--workload 27b|sweep:B:L:S|long|varlen|tiny|decode[:B]|bwd]
+                    [--workload 27b|sweep:B:L:S|long|varlen|tiny|decode[:B]|bwd[:B]]
 
 A step is one ssd_fwd call over one batch of the workload (default: the
 Mamba-2 2.7B-like layer, batch 8 x 2048 tokens, 80 heads, P 64, N 128, bf16).
@@ -16,7 +16,8 @@ bounded sample of the same workload (one batch row per step).
 
 --workload decode[:B] times the single-token decode step (ssd_step) of the
 same layer shape over a batch of B rows (default 256) from a resident state;
---workload bwd times the backward pass (ssd_bwd) of the 2.7B-like layer.
+--workload bwd[:B] times the backward pass (ssd_bwd) of the 2.7B-like layer
+(batch B, default 8).
 """
 from __future__ import annotations
 
@@ -61,7 +62,10 @@ def workload(name: str):
     if name.startswith("decode"):
         parts = name.split(":")
         return synth.config_decode(int(parts[1]) if len(parts) > 1 else 256)
-    if name in ("27b", "bwd"):
+    if name.startswith("bwd"):
+        parts = name.split(":")
+        return synth.config_27b(batch=int(parts[1]) if len(parts) > 1 else 8)
+    if name == "27b":
         return synth.config_27b()
     if name == "tiny":
         return synth.config_tiny_f32()
@@ -203,7 +207,7 @@ def run_reference(args):
     if rank != 0:
         return
     p = workload(args.workload)
-    if args.workload == "bwd":
+    if args.workload.startswith("bwd"):
         dy_h = np.random.default_rng(11).standard_normal((p.batch, p.seqlen, p.nheads, p.headdim)).astype(np.float32)
         q, dyq = bwd_sample(p, dy_h)
         for _ in range(args.warmup):
@@ -533,7 +537,7 @@ def run_ours(args):
     p = workload(args.workload)
     if p.seqlen == 1:
         return run_decode(args, p, dev, rank, local_rank, world)
-    if args.workload == "bwd":
+    if args.workload.startswith("bwd"):
         return run_bwd(args, p, dev, rank, local_rank, world)
     dtype = torch.bfloat16 if p.dtype == "bf16" else torch.float32
 

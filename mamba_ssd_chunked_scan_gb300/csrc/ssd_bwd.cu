@@ -32,41 +32,55 @@
 namespace ssd {
 namespace {
 
-constexpr int kBwdThreads = 256;
-constexpr int kBwdOwn = 32;   // state elements each thread keeps in registers (P * N <= 8192)
+constexpr int kBwdThreads = 1024;
+constexpr int kBwdOwn = 8;    // state elements each thread keeps in registers (P * N <= 8192)
 
 struct BwdSmem {
-    int Qb, P, N, sx, sb;      // chunk, sizes, padded row strides of x/dy and B/S_in/Lam
-    size_t x, dy, B, C, Sin, Lam, A1, A2, W, vx, lbx, scdy, dts, ell, ep, es, ddta, wv, uv, rv, red, total;
+    int Qb, P, N, sx, sb, st;  // chunk, sizes, padded row strides of x, of B/S_in/Lam, of the transposes
+    size_t x, dy, B, C, Sin, Lam, A1, A2, W, vx, lbx, scdy, dts, ell, ep, es, ddta, wv, uv, rv, red;
+    size_t xT, dyT, BT, CT, A2dtT, total;
 };
 
-__host__ __device__ inline BwdSmem bwd_smem(int Qb, int P, int N) {
+// Shared-memory layout of one CTA (offsets in floats, each 16-byte aligned).
+// `tiled` adds the transposed copies the register-tiled loops of the common
+// head shape read as 8- and 16-byte vectors.
+__host__ __device__ inline BwdSmem bwd_smem(int Qb, int P, int N, bool tiled) {
     BwdSmem s;
     s.Qb = Qb; s.P = P; s.N = N;
     s.sx = P + 1;              // odd strides: column walks hit distinct banks
     s.sb = N + 1;
+    s.st = Qb + 4;
     size_t o = 0;
-    s.x = o;    o += (size_t)Qb * s.sx;
-    s.dy = o;   o += (size_t)Qb * s.sx;
-    s.B = o;    o += (size_t)Qb * s.sb;
-    s.C = o;    o += (size_t)Qb * N;
-    s.Sin = o;  o += (size_t)P * s.sb;
-    s.Lam = o;  o += (size_t)P * s.sb;
-    s.A1 = o;   o += (size_t)Qb * Qb;      // L_ij G_ij
-    s.A2 = o;   o += (size_t)Qb * Qb;      // L_ij X_ij
-    s.W = o;    o += (size_t)Qb * Qb;      // L_ij dt_j X_ij G_ij
-    s.vx = o;   o += (size_t)Qb * P;       // v_j[p] x_j[p]
-    s.lbx = o;  o += (size_t)Qb * P;       // (Lam B_j)[p] x_j[p]
-    s.scdy = o; o += (size_t)Qb * P;       // (S_in C_i)[p] dy_i[p]
-    s.dts = o;  o += Qb;
-    s.ell = o;  o += Qb;
-    s.ep = o;   o += Qb;
-    s.es = o;   o += Qb;
-    s.ddta = o; o += Qb;
-    s.wv = o;   o += Qb;
-    s.uv = o;   o += Qb;
-    s.rv = o;   o += Qb;
-    s.red = o;  o += 2 * (kBwdThreads / 32);
+    auto take = [&](size_t n) { const size_t at = o; o = (o + n + 3) & ~(size_t)3; return at; };
+    s.x = take((size_t)Qb * s.sx);
+    s.dy = take((size_t)Qb * P);
+    s.B = take((size_t)Qb * s.sb);
+    s.C = take((size_t)Qb * N);
+    s.Sin = take((size_t)P * s.sb);
+    s.Lam = take((size_t)P * s.sb);
+    s.A1 = take((size_t)Qb * Qb);       // L_ij G_ij
+    s.A2 = take((size_t)Qb * Qb);       // L_ij X_ij
+    s.W = take((size_t)Qb * Qb);        // L_ij dt_j X_ij G_ij
+    s.vx = take((size_t)Qb * P);        // v_j[p] x_j[p]
+    s.lbx = take((size_t)Qb * P);       // (Lam B_j)[p] x_j[p]
+    s.scdy = take((size_t)Qb * P);      // (S_in C_i)[p] dy_i[p]
+    s.dts = take(Qb);
+    s.ell = take(Qb);
+    s.ep = take(Qb);
+    s.es = take(Qb);
+    s.ddta = take(Qb);
+    s.wv = take(Qb);
+    s.uv = take(Qb);
+    s.rv = take(Qb);
+    s.red = take(2 * (kBwdThreads / 32));
+    s.xT = s.dyT = s.BT = s.CT = s.A2dtT = 0;
+    if (tiled) {
+        s.xT = take((size_t)P * s.st);     // x[j][p] at [p][j]
+        s.dyT = take((size_t)P * s.st);    // dy[j][p] at [p][j]
+        s.BT = take((size_t)N * s.st);     // B[j][n] at [n][j]
+        s.CT = take((size_t)N * s.st);     // C[j][n] at [n][j]
+        s.A2dtT = take((size_t)Qb * s.st); // L_jk X_jk dt_k at [k][j]
+    }
     s.total = o * sizeof(float);
     return s;
 }
@@ -77,7 +91,7 @@ __device__ __forceinline__ float warp_sum(float v) {
     return v;
 }
 
-// Block-wide sum (every thread gets the result); `red` holds 8 floats.
+// Block-wide sum (every thread gets the result); `red` holds one float per warp.
 __device__ __forceinline__ float block_sum(float v, float* red) {
     v = warp_sum(v);
     const int w = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -90,11 +104,16 @@ __device__ __forceinline__ float block_sum(float v, float* red) {
     return s;
 }
 
-template <typename T>
+// kP, kN, kQ: compile-time P, N and chunk (0: run-time values).  The common head
+// shape (64, 128, 32) runs register-tiled loops: each thread owns 8 state rows of
+// one column, and the matrix products read their operands as vectors, so a shared-
+// memory load feeds 2 to 4 multiply-adds instead of half of one.
+template <typename T, int kP, int kN, int kQ>
 __global__ void __launch_bounds__(kBwdThreads) ssd_bwd_chunk(BwdArgs a) {
-    extern __shared__ float sm[];
-    const BwdSmem L = bwd_smem(a.Qb, a.P, a.N);
-    const int Qb = a.Qb, P = a.P, N = a.N, H = a.H, G = a.G;
+    extern __shared__ __align__(16) float sm[];
+    constexpr bool kT = kP == 64 && kN == 128 && kQ == 32;
+    const int Qb = kQ ? kQ : a.Qb, P = kP ? kP : a.P, N = kN ? kN : a.N, H = a.H, G = a.G;
+    const BwdSmem L = bwd_smem(Qb, P, N, kT);
     const int PN = P * N;
     float* xs = sm + L.x;
     float* dys = sm + L.dy;
@@ -117,6 +136,11 @@ __global__ void __launch_bounds__(kBwdThreads) ssd_bwd_chunk(BwdArgs a) {
     float* uv = sm + L.uv;
     float* rv = sm + L.rv;
     float* red = sm + L.red;
+    float* xT = sm + L.xT;
+    float* dyT = sm + L.dyT;
+    float* BT = sm + L.BT;
+    float* CT = sm + L.CT;
+    float* A2dtT = sm + L.A2dtT;
 
     const int tid = threadIdx.x;
     const int64_t unit = blockIdx.x;               // b * H + h
@@ -137,26 +161,31 @@ __global__ void __launch_bounds__(kBwdThreads) ssd_bwd_chunk(BwdArgs a) {
     auto xrow = [&](int64_t t) { return x + ((size_t)(b * Lseq + t) * H + h) * P; };
     auto dyrow = [&](int64_t t) { return dy + ((size_t)(b * Lseq + t) * H + h) * P; };
     auto bcoff = [&](int64_t t) { return ((size_t)(b * Lseq + t) * G + g) * N; };
+    // the state elements this thread owns: (p, n) of its r-th element
+    const int own_n = kT ? (tid & 127) : 0, own_p0 = kT ? (tid >> 7) * 8 : 0;
+    auto own = [&](int r) -> int { return kT ? (own_p0 + r) * N + own_n : tid + kBwdThreads * r; };
 
     // ------------------------------------------------------------ phase 1
     // forward over the chunks: the state entering each chunk, kept in the workspace
     float S[kBwdOwn];
 #pragma unroll
     for (int r = 0; r < kBwdOwn; ++r) {
-        const int e = tid + kBwdThreads * r;
+        const int e = own(r);
         S[r] = (e < PN && a.init) ? a.init[(size_t)unit * PN + e] : 0.f;
     }
     for (int c = 0; c < nch; ++c) {
         const int64_t t0 = (int64_t)c * Qb;
 #pragma unroll
         for (int r = 0; r < kBwdOwn; ++r) {
-            const int e = tid + kBwdThreads * r;
+            const int e = own(r);
             if (e < PN) ckpt[(size_t)c * PN + e] = S[r];
         }
         __syncthreads();   // the previous chunk's tile reads are done
         for (int k = tid; k < Qb * P; k += kBwdThreads) {
             const int i = k / P, p = k - i * P;
-            xs[i * L.sx + p] = (t0 + i < Lseq) ? Elem<T>::load(xrow(t0 + i) + p) : 0.f;
+            const float v = (t0 + i < Lseq) ? Elem<T>::load(xrow(t0 + i) + p) : 0.f;
+            if (kT) dys[i * P + p] = v;    // x rows, 16-byte aligned (the dy buffer is free here)
+            else xs[i * L.sx + p] = v;
         }
         for (int k = tid; k < Qb * N; k += kBwdThreads) {
             const int i = k / N, n = k - i * N;
@@ -180,14 +209,34 @@ __global__ void __launch_bounds__(kBwdThreads) ssd_bwd_chunk(BwdArgs a) {
         }
         __syncthreads();
         const float etau = red[0];
+        if constexpr (kT) {
 #pragma unroll
-        for (int r = 0; r < kBwdOwn; ++r) {
-            const int e = tid + kBwdThreads * r;
-            if (e < PN) {
-                const int p = e / N, n = e - p * N;
-                float acc = etau * S[r];
-                for (int j = 0; j < Qb; ++j) acc = fmaf(es[j] * xs[j * L.sx + p], Bs[j * L.sb + n], acc);
-                S[r] = acc;
+            for (int r = 0; r < kBwdOwn; ++r) S[r] *= etau;
+#pragma unroll 4
+            for (int j = 0; j < Qb; ++j) {
+                const float w = es[j], bv = Bs[j * L.sb + own_n];
+                const float4 x0 = *reinterpret_cast<const float4*>(dys + j * P + own_p0);
+                const float4 x1 = *reinterpret_cast<const float4*>(dys + j * P + own_p0 + 4);
+                S[0] = fmaf(w * x0.x, bv, S[0]);
+                S[1] = fmaf(w * x0.y, bv, S[1]);
+                S[2] = fmaf(w * x0.z, bv, S[2]);
+                S[3] = fmaf(w * x0.w, bv, S[3]);
+                S[4] = fmaf(w * x1.x, bv, S[4]);
+                S[5] = fmaf(w * x1.y, bv, S[5]);
+                S[6] = fmaf(w * x1.z, bv, S[6]);
+                S[7] = fmaf(w * x1.w, bv, S[7]);
+            }
+        } else {
+#pragma unroll
+            for (int r = 0; r < kBwdOwn; ++r) {
+                const int e = own(r);
+                if (e < PN) {
+                    const int p = e / N, n = e - p * N;
+                    float acc = etau * S[r];
+#pragma unroll 8
+                    for (int j = 0; j < Qb; ++j) acc = fmaf(es[j] * xs[j * L.sx + p], Bs[j * L.sb + n], acc);
+                    S[r] = acc;
+                }
             }
         }
     }
@@ -197,7 +246,7 @@ __global__ void __launch_bounds__(kBwdThreads) ssd_bwd_chunk(BwdArgs a) {
     float Lr[kBwdOwn];
 #pragma unroll
     for (int r = 0; r < kBwdOwn; ++r) {
-        const int e = tid + kBwdThreads * r;
+        const int e = own(r);
         Lr[r] = (e < PN && a.dfin) ? a.dfin[(size_t)unit * PN + e] : 0.f;
     }
     float dA_acc = 0.f, dD_acc = 0.f;    // thread 0's running sums
@@ -207,19 +256,31 @@ __global__ void __launch_bounds__(kBwdThreads) ssd_bwd_chunk(BwdArgs a) {
         for (int k = tid; k < Qb * P; k += kBwdThreads) {
             const int i = k / P, p = k - i * P;
             const bool ok = t0 + i < Lseq;
-            xs[i * L.sx + p] = ok ? Elem<T>::load(xrow(t0 + i) + p) : 0.f;
-            dys[i * L.sx + p] = ok ? Elem<T>::load(dyrow(t0 + i) + p) : 0.f;
+            const float xv = ok ? Elem<T>::load(xrow(t0 + i) + p) : 0.f;
+            const float dv = ok ? Elem<T>::load(dyrow(t0 + i) + p) : 0.f;
+            xs[i * L.sx + p] = xv;
+            dys[i * P + p] = dv;
+            if (kT) {
+                xT[p * L.st + i] = xv;
+                dyT[p * L.st + i] = dv;
+            }
         }
         for (int k = tid; k < Qb * N; k += kBwdThreads) {
             const int i = k / N, n = k - i * N;
             const bool ok = t0 + i < Lseq;
-            Bs[i * L.sb + n] = ok ? Elem<T>::load(Bg + bcoff(t0 + i) + n) : 0.f;
-            Cs[i * N + n] = ok ? Elem<T>::load(Cg + bcoff(t0 + i) + n) : 0.f;
+            const float bv = ok ? Elem<T>::load(Bg + bcoff(t0 + i) + n) : 0.f;
+            const float cv = ok ? Elem<T>::load(Cg + bcoff(t0 + i) + n) : 0.f;
+            Bs[i * L.sb + n] = bv;
+            Cs[i * N + n] = cv;
+            if (kT) {
+                BT[n * L.st + i] = bv;
+                CT[n * L.st + i] = cv;
+            }
         }
         float kdot = 0.f;   // this thread's share of <Lam, S_in>
 #pragma unroll
         for (int r = 0; r < kBwdOwn; ++r) {
-            const int e = tid + kBwdThreads * r;
+            const int e = own(r);
             if (e < PN) {
                 const int p = e / N, n = e - p * N;
                 const float sv = ckpt[(size_t)c * PN + e];
@@ -253,8 +314,10 @@ __global__ void __launch_bounds__(kBwdThreads) ssd_bwd_chunk(BwdArgs a) {
                 for (int k = j + 1; k <= i; ++k) seg += ell[k];
                 const float Lij = expf(seg);
                 float gij = 0.f, xij = 0.f;
+#pragma unroll 8
                 for (int n = 0; n < N; ++n) gij = fmaf(Cs[i * N + n], Bs[j * L.sb + n], gij);
-                for (int p = 0; p < P; ++p) xij = fmaf(dys[i * L.sx + p], xs[j * L.sx + p], xij);
+#pragma unroll 8
+                for (int p = 0; p < P; ++p) xij = fmaf(dys[i * P + p], xs[j * L.sx + p], xij);
                 a1 = Lij * gij;
                 a2 = Lij * xij;
                 w = a1 * dts[j] * xij;
@@ -262,44 +325,141 @@ __global__ void __launch_bounds__(kBwdThreads) ssd_bwd_chunk(BwdArgs a) {
             A1[q] = a1;
             A2[q] = a2;
             Wm[q] = w;
+            if (kT) A2dtT[j * L.st + i] = a2 * dts[j];
         }
         __syncthreads();
-        // dx, and the per-token dot products of ddt
-        for (int q = tid; q < Qb * P; q += kBwdThreads) {
-            const int j = q / P, p = q - j * P;
-            float lb = 0.f;
-            for (int n = 0; n < N; ++n) lb = fmaf(Lam[p * L.sb + n], Bs[j * L.sb + n], lb);
-            float v = es[j] * lb;
-            for (int i = j; i < Qb; ++i) v = fmaf(A1[i * Qb + j], dys[i * L.sx + p], v);
-            const float xv = xs[j * L.sx + p];
-            vx[q] = v * xv;
-            lbx[q] = lb * xv;
-            float sc = 0.f;   // (S_in C_j)[p], for the row j as an output row
-            for (int n = 0; n < N; ++n) sc = fmaf(Sin[p * L.sb + n], Cs[j * N + n], sc);
-            scdy[q] = sc * dys[j * L.sx + p];
-            if (t0 + j < Lseq)
-                Elem<T>::store(static_cast<T*>(a.dx) + ((size_t)(b * Lseq + t0 + j) * H + h) * P + p,
-                               fmaf(dts[j], v, Dh * dys[j * L.sx + p]));
-        }
-        // this head's shares of dB and dC
-        for (int q = tid; q < Qb * N; q += kBwdThreads) {
-            const int j = q / N, n = q - j * N;
-            if (t0 + j >= Lseq) continue;
-            float lx = 0.f, sd = 0.f;
-            for (int p = 0; p < P; ++p) {
-                lx = fmaf(Lam[p * L.sb + n], xs[j * L.sx + p], lx);
-                sd = fmaf(Sin[p * L.sb + n], dys[j * L.sx + p], sd);
+        if constexpr (kT) {
+            // dx and the per-token dot products of ddt: thread = (p, two rows j0, j0 + 1)
+            {
+                const int p = tid & 63, j0 = (tid >> 6) * 2;
+                float lb0 = 0.f, lb1 = 0.f, sc0 = 0.f, sc1 = 0.f;
+#pragma unroll 8
+                for (int n = 0; n < 128; ++n) {
+                    const float lam = Lam[p * L.sb + n], sin = Sin[p * L.sb + n];
+                    const float2 bb = *reinterpret_cast<const float2*>(BT + n * L.st + j0);
+                    const float2 cc = *reinterpret_cast<const float2*>(CT + n * L.st + j0);
+                    lb0 = fmaf(lam, bb.x, lb0);
+                    lb1 = fmaf(lam, bb.y, lb1);
+                    sc0 = fmaf(sin, cc.x, sc0);
+                    sc1 = fmaf(sin, cc.y, sc1);
+                }
+                float v0 = es[j0] * lb0, v1 = es[j0 + 1] * lb1;
+#pragma unroll 4
+                for (int i = j0; i < 32; ++i) {
+                    const float2 aa = *reinterpret_cast<const float2*>(A1 + i * 32 + j0);   // 0 where j > i
+                    const float d = dys[i * 64 + p];
+                    v0 = fmaf(aa.x, d, v0);
+                    v1 = fmaf(aa.y, d, v1);
+                }
+                const float lbs[2] = {lb0, lb1}, vs[2] = {v0, v1}, scs[2] = {sc0, sc1};
+#pragma unroll
+                for (int u = 0; u < 2; ++u) {
+                    const int j = j0 + u, q = j * 64 + p;
+                    const float xv = xs[j * L.sx + p], dv = dys[j * 64 + p];
+                    vx[q] = vs[u] * xv;
+                    lbx[q] = lbs[u] * xv;
+                    scdy[q] = scs[u] * dv;
+                    if (t0 + j < Lseq)
+                        Elem<T>::store(static_cast<T*>(a.dx) + ((size_t)(b * Lseq + t0 + j) * H + h) * 64 + p,
+                                       fmaf(dts[j], vs[u], Dh * dv));
+                }
             }
-            float db = es[j] * lx;
-            for (int i = j; i < Qb; ++i) db = fmaf(A2[i * Qb + j], Cs[i * N + n], db);
-            float dc = ep[j] * sd;
-            for (int k = 0; k <= j; ++k) dc = fmaf(A2[j * Qb + k] * dts[k], Bs[k * L.sb + n], dc);
-            const size_t o = ((size_t)(b * Lseq + t0 + j) * H + h) * N + n;
-            a.ws_dB[o] = dts[j] * db;
-            a.ws_dC[o] = dc;
+            // this head's shares of dB and dC: thread = (n, four rows j0 .. j0 + 3)
+            {
+                const int n = tid & 127, j0 = (tid >> 7) * 4;
+                float lx[4] = {0.f, 0.f, 0.f, 0.f}, sd[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll 4
+                for (int p = 0; p < 64; ++p) {
+                    const float lam = Lam[p * L.sb + n], sin = Sin[p * L.sb + n];
+                    const float4 xx = *reinterpret_cast<const float4*>(xT + p * L.st + j0);
+                    const float4 dd = *reinterpret_cast<const float4*>(dyT + p * L.st + j0);
+                    lx[0] = fmaf(lam, xx.x, lx[0]);
+                    lx[1] = fmaf(lam, xx.y, lx[1]);
+                    lx[2] = fmaf(lam, xx.z, lx[2]);
+                    lx[3] = fmaf(lam, xx.w, lx[3]);
+                    sd[0] = fmaf(sin, dd.x, sd[0]);
+                    sd[1] = fmaf(sin, dd.y, sd[1]);
+                    sd[2] = fmaf(sin, dd.z, sd[2]);
+                    sd[3] = fmaf(sin, dd.w, sd[3]);
+                }
+                float db[4], dc[4];
+#pragma unroll
+                for (int u = 0; u < 4; ++u) {
+                    db[u] = es[j0 + u] * lx[u];
+                    dc[u] = ep[j0 + u] * sd[u];
+                }
+#pragma unroll 4
+                for (int i = j0; i < 32; ++i) {   // A2[i][j] = 0 where j > i
+                    const float4 aa = *reinterpret_cast<const float4*>(A2 + i * 32 + j0);
+                    const float cv = Cs[i * 128 + n];
+                    db[0] = fmaf(aa.x, cv, db[0]);
+                    db[1] = fmaf(aa.y, cv, db[1]);
+                    db[2] = fmaf(aa.z, cv, db[2]);
+                    db[3] = fmaf(aa.w, cv, db[3]);
+                }
+#pragma unroll 4
+                for (int k = 0; k < j0 + 4; ++k) {   // A2[j][k] = 0 where k > j
+                    const float4 aa = *reinterpret_cast<const float4*>(A2dtT + k * L.st + j0);
+                    const float bv = Bs[k * L.sb + n];
+                    dc[0] = fmaf(aa.x, bv, dc[0]);
+                    dc[1] = fmaf(aa.y, bv, dc[1]);
+                    dc[2] = fmaf(aa.z, bv, dc[2]);
+                    dc[3] = fmaf(aa.w, bv, dc[3]);
+                }
+#pragma unroll
+                for (int u = 0; u < 4; ++u) {
+                    const int j = j0 + u;
+                    if (t0 + j < Lseq) {
+                        const size_t o = ((size_t)(b * Lseq + t0 + j) * H + h) * 128 + n;
+                        a.ws_dB[o] = dts[j] * db[u];
+                        a.ws_dC[o] = dc[u];
+                    }
+                }
+            }
+        } else {
+            // dx, and the per-token dot products of ddt
+            for (int q = tid; q < Qb * P; q += kBwdThreads) {
+                const int j = q / P, p = q - j * P;
+                float lb = 0.f;
+#pragma unroll 8
+                for (int n = 0; n < N; ++n) lb = fmaf(Lam[p * L.sb + n], Bs[j * L.sb + n], lb);
+                float v = es[j] * lb;
+#pragma unroll 8
+                for (int i = j; i < Qb; ++i) v = fmaf(A1[i * Qb + j], dys[i * P + p], v);
+                const float xv = xs[j * L.sx + p];
+                vx[q] = v * xv;
+                lbx[q] = lb * xv;
+                float sc = 0.f;   // (S_in C_j)[p], for the row j as an output row
+#pragma unroll 8
+                for (int n = 0; n < N; ++n) sc = fmaf(Sin[p * L.sb + n], Cs[j * N + n], sc);
+                scdy[q] = sc * dys[j * P + p];
+                if (t0 + j < Lseq)
+                    Elem<T>::store(static_cast<T*>(a.dx) + ((size_t)(b * Lseq + t0 + j) * H + h) * P + p,
+                                   fmaf(dts[j], v, Dh * dys[j * P + p]));
+            }
+            // this head's shares of dB and dC
+            for (int q = tid; q < Qb * N; q += kBwdThreads) {
+                const int j = q / N, n = q - j * N;
+                if (t0 + j >= Lseq) continue;
+                float lx = 0.f, sd = 0.f;
+#pragma unroll 8
+                for (int p = 0; p < P; ++p) {
+                    lx = fmaf(Lam[p * L.sb + n], xs[j * L.sx + p], lx);
+                    sd = fmaf(Sin[p * L.sb + n], dys[j * P + p], sd);
+                }
+                float db = es[j] * lx;
+#pragma unroll 8
+                for (int i = j; i < Qb; ++i) db = fmaf(A2[i * Qb + j], Cs[i * N + n], db);
+                float dc = ep[j] * sd;
+#pragma unroll 8
+                for (int k = 0; k <= j; ++k) dc = fmaf(A2[j * Qb + k] * dts[k], Bs[k * L.sb + n], dc);
+                const size_t o = ((size_t)(b * Lseq + t0 + j) * H + h) * N + n;
+                a.ws_dB[o] = dts[j] * db;
+                a.ws_dC[o] = dc;
+            }
         }
         __syncthreads();
-        // per-token reductions (warp w takes tokens w, w + 8, ...)
+        // per-token reductions (warp w takes tokens w, w + 32, ...)
         {
             const int w = tid >> 5, lane = tid & 31;
             for (int t = w; t < Qb; t += kBwdThreads / 32) {
@@ -331,10 +491,10 @@ __global__ void __launch_bounds__(kBwdThreads) ssd_bwd_chunk(BwdArgs a) {
             for (int j = 0; j <= t; ++j) V += wv[j];
             const float dl = rv[t] + U + V + etau * K - dts[t] * ddta[t];
             if (t0 + t < Lseq) a.ddt[(size_t)(b * Lseq + t0 + t) * H + h] = fmaf(Ah, dl, ddta[t]);
-            float da = dts[t] * dl;
+            const float da = dts[t] * dl;
             float dd = 0.f;
-            for (int p = 0; p < P; ++p) dd = fmaf(dys[t * L.sx + p], xs[t * L.sx + p], dd);
-            // lanes 0..Qb-1 of warps 0-1: fixed-order reduction through shared memory
+            for (int p = 0; p < P; ++p) dd = fmaf(dys[t * P + p], xs[t * L.sx + p], dd);
+            // thread 0 sums these in token order below
             ddta[t] = da;
             wv[t] = dd;
         }
@@ -346,21 +506,41 @@ __global__ void __launch_bounds__(kBwdThreads) ssd_bwd_chunk(BwdArgs a) {
             }
         }
         // Lam becomes the adjoint of the state entering this chunk
+        if constexpr (kT) {
 #pragma unroll
-        for (int r = 0; r < kBwdOwn; ++r) {
-            const int e = tid + kBwdThreads * r;
-            if (e < PN) {
-                const int p = e / N, n = e - p * N;
-                float acc = etau * Lr[r];
-                for (int i = 0; i < Qb; ++i) acc = fmaf(ep[i] * dys[i * L.sx + p], Cs[i * N + n], acc);
-                Lr[r] = acc;
+            for (int r = 0; r < kBwdOwn; ++r) Lr[r] *= etau;
+#pragma unroll 4
+            for (int i = 0; i < 32; ++i) {
+                const float w = ep[i], cv = Cs[i * 128 + own_n];
+                const float4 d0 = *reinterpret_cast<const float4*>(dys + i * 64 + own_p0);
+                const float4 d1 = *reinterpret_cast<const float4*>(dys + i * 64 + own_p0 + 4);
+                Lr[0] = fmaf(w * d0.x, cv, Lr[0]);
+                Lr[1] = fmaf(w * d0.y, cv, Lr[1]);
+                Lr[2] = fmaf(w * d0.z, cv, Lr[2]);
+                Lr[3] = fmaf(w * d0.w, cv, Lr[3]);
+                Lr[4] = fmaf(w * d1.x, cv, Lr[4]);
+                Lr[5] = fmaf(w * d1.y, cv, Lr[5]);
+                Lr[6] = fmaf(w * d1.z, cv, Lr[6]);
+                Lr[7] = fmaf(w * d1.w, cv, Lr[7]);
+            }
+        } else {
+#pragma unroll
+            for (int r = 0; r < kBwdOwn; ++r) {
+                const int e = own(r);
+                if (e < PN) {
+                    const int p = e / N, n = e - p * N;
+                    float acc = etau * Lr[r];
+#pragma unroll 8
+                    for (int i = 0; i < Qb; ++i) acc = fmaf(ep[i] * dys[i * P + p], Cs[i * N + n], acc);
+                    Lr[r] = acc;
+                }
             }
         }
     }
     if (a.dinit) {
 #pragma unroll
         for (int r = 0; r < kBwdOwn; ++r) {
-            const int e = tid + kBwdThreads * r;
+            const int e = own(r);
             if (e < PN) a.dinit[(size_t)unit * PN + e] = Lr[r];
         }
     }
@@ -405,10 +585,13 @@ __global__ void __launch_bounds__(256) ssd_bwd_reduce(BwdArgs a) {
 
 }  // namespace
 
-size_t bwd_smem_bytes(int Qb, int P, int N) { return bwd_smem(Qb, P, N).total; }
+static bool bwd_tiled(int Qb, int P, int N) { return P == 64 && N == 128 && Qb == 32; }
+
+size_t bwd_smem_bytes(int Qb, int P, int N) { return bwd_smem(Qb, P, N, bwd_tiled(Qb, P, N)).total; }
 
 int bwd_chunk(int P, int N, size_t smem_limit) {
     if (P * N > kBwdThreads * kBwdOwn) return 0;
+    if (P == 64 && N == 128 && bwd_smem_bytes(32, P, N) <= smem_limit) return 32;   // the tiled loops
     for (int Qb = 64; Qb >= 8; Qb >>= 1)
         if (bwd_smem_bytes(Qb, P, N) <= smem_limit) return Qb;
     return 0;
@@ -416,7 +599,10 @@ int bwd_chunk(int P, int N, size_t smem_limit) {
 
 cudaError_t launch_bwd(const BwdArgs& a, cudaStream_t st) {
     const size_t smem = bwd_smem_bytes(a.Qb, a.P, a.N);
-    auto k1 = a.dtype == SSD_BF16 ? ssd_bwd_chunk<__nv_bfloat16> : ssd_bwd_chunk<float>;
+    const bool mamba_shape = bwd_tiled(a.Qb, a.P, a.N);
+    auto k1 = a.dtype == SSD_BF16 ? (mamba_shape ? ssd_bwd_chunk<__nv_bfloat16, 64, 128, 32>
+                                                 : ssd_bwd_chunk<__nv_bfloat16, 0, 0, 0>)
+                                  : (mamba_shape ? ssd_bwd_chunk<float, 64, 128, 32> : ssd_bwd_chunk<float, 0, 0, 0>);
     cudaError_t e = cudaFuncSetAttribute(k1, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
     k1<<<(unsigned)(a.batch * a.H), kBwdThreads, smem, st>>>(a);
