@@ -37,7 +37,7 @@ constexpr int kBwdOwn = 8;    // state elements each thread keeps in registers (
 
 struct BwdSmem {
     int Qb, P, N, sx, sb, st;  // chunk, sizes, padded row strides of x, of B/S_in/Lam, of the transposes
-    size_t x, dy, B, C, Sin, Lam, A1, A2, W, vx, lbx, scdy, dts, ell, ep, es, ddta, wv, uv, rv, red;
+    size_t x, dy, B, C, Sin, Lam, A1, A2, W, vx, lbx, scdy, dts, ell, ep, es, ddta, wv, uv, rv, ddv, misc, red;
     size_t xT, dyT, BT, CT, A2dtT, total;
 };
 
@@ -72,6 +72,8 @@ __host__ __device__ inline BwdSmem bwd_smem(int Qb, int P, int N, bool tiled) {
     s.wv = take(Qb);
     s.uv = take(Qb);
     s.rv = take(Qb);
+    s.ddv = take(Qb);                   // dy_t . x_t
+    s.misc = take(4);                   // [0]: e^{tau} of the chunk
     s.red = take(2 * (kBwdThreads / 32));
     s.xT = s.dyT = s.BT = s.CT = s.A2dtT = 0;
     if (tiled) {
@@ -88,6 +90,27 @@ __host__ __device__ inline BwdSmem bwd_smem(int Qb, int P, int N, bool tiled) {
 __device__ __forceinline__ float warp_sum(float v) {
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+    return v;
+}
+
+// Inclusive prefix sum over lanes 0..lane, and inclusive suffix sum over lanes
+// lane..31 (direct sums in a fixed order: no subtraction).
+__device__ __forceinline__ float warp_prefix(float v) {
+    const int lane = threadIdx.x & 31;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+        const float t = __shfl_up_sync(0xffffffffu, v, o);
+        if (lane >= o) v += t;
+    }
+    return v;
+}
+__device__ __forceinline__ float warp_suffix(float v) {
+    const int lane = threadIdx.x & 31;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+        const float t = __shfl_down_sync(0xffffffffu, v, o);
+        if (lane + o < 32) v += t;
+    }
     return v;
 }
 
@@ -135,6 +158,8 @@ __global__ void __launch_bounds__(kBwdThreads) ssd_bwd_chunk(BwdArgs a) {
     float* wv = sm + L.wv;
     float* uv = sm + L.uv;
     float* rv = sm + L.rv;
+    float* ddv = sm + L.ddv;
+    float* misc = sm + L.misc;
     float* red = sm + L.red;
     float* xT = sm + L.xT;
     float* dyT = sm + L.dyT;
@@ -191,21 +216,33 @@ __global__ void __launch_bounds__(kBwdThreads) ssd_bwd_chunk(BwdArgs a) {
             const int i = k / N, n = k - i * N;
             Bs[i * L.sb + n] = (t0 + i < Lseq) ? Elem<T>::load(Bg + bcoff(t0 + i) + n) : 0.f;
         }
-        if (tid < Qb) {
-            const float d = (t0 + tid < Lseq) ? a.dt[(size_t)(b * Lseq + t0 + tid) * H + h] : 0.f;
-            dts[tid] = d;
-            ell[tid] = d * Ah;
-        }
-        __syncthreads();
-        if (tid < Qb) {
-            float s = 0.f;                          // s_t: the log-decays after t in the chunk
-            for (int k = tid + 1; k < Qb; ++k) s += ell[k];
-            es[tid] = expf(s) * dts[tid];           // the weight of token t's input in the chunk's end state
-        }
-        if (tid == 0) {
-            float tau = 0.f;
-            for (int k = 0; k < Qb; ++k) tau += ell[k];
-            red[0] = expf(tau);
+        if constexpr (kT) {
+            if (tid < 32) {   // warp 0, lane = token: suffix sums by shuffles
+                const float d = (t0 + tid < Lseq) ? a.dt[(size_t)(b * Lseq + t0 + tid) * H + h] : 0.f;
+                const float l = d * Ah;
+                const float nxt = __shfl_down_sync(0xffffffffu, l, 1);
+                const float sfx = warp_suffix(tid < 31 ? nxt : 0.f);   // s_t: the log-decays after t
+                es[tid] = expf(sfx) * d;          // the weight of token t's input in the chunk's end state
+                const float tau = __shfl_sync(0xffffffffu, l + sfx, 0);
+                if (tid == 0) red[0] = expf(tau);
+            }
+        } else {
+            if (tid < Qb) {
+                const float d = (t0 + tid < Lseq) ? a.dt[(size_t)(b * Lseq + t0 + tid) * H + h] : 0.f;
+                dts[tid] = d;
+                ell[tid] = d * Ah;
+            }
+            __syncthreads();
+            if (tid < Qb) {
+                float s = 0.f;                          // s_t: the log-decays after t in the chunk
+                for (int k = tid + 1; k < Qb; ++k) s += ell[k];
+                es[tid] = expf(s) * dts[tid];           // the weight of token t's input in the chunk's end state
+            }
+            if (tid == 0) {
+                float tau = 0.f;
+                for (int k = 0; k < Qb; ++k) tau += ell[k];
+                red[0] = expf(tau);
+            }
         }
         __syncthreads();
         const float etau = red[0];
@@ -295,23 +332,42 @@ __global__ void __launch_bounds__(kBwdThreads) ssd_bwd_chunk(BwdArgs a) {
             ell[tid] = d * Ah;
         }
         const float K = block_sum(kdot, red);   // (contains a barrier: the tiles are visible)
-        if (tid < Qb) {
-            float pfx = 0.f, sfx = 0.f;
-            for (int k = 0; k <= tid; ++k) pfx += ell[k];
-            for (int k = tid + 1; k < Qb; ++k) sfx += ell[k];
-            ep[tid] = expf(pfx);
-            es[tid] = expf(sfx);
+        if constexpr (kT) {
+            if (tid < 32) {   // warp 0, lane = token: prefix and suffix sums by shuffles
+                const float l = ell[tid];
+                const float pfx = warp_prefix(l);                                  // p_t
+                const float nxt = __shfl_down_sync(0xffffffffu, l, 1);
+                const float sfx = warp_suffix(tid < 31 ? nxt : 0.f);               // s_t
+                ep[tid] = expf(pfx);
+                es[tid] = expf(sfx);
+                const float tau = __shfl_sync(0xffffffffu, l + sfx, 0);
+                if (tid == 0) misc[0] = expf(tau);
+            }
+        } else {
+            if (tid < Qb) {
+                float pfx = 0.f, sfx = 0.f;
+                for (int k = 0; k <= tid; ++k) pfx += ell[k];
+                for (int k = tid + 1; k < Qb; ++k) sfx += ell[k];
+                ep[tid] = expf(pfx);
+                es[tid] = expf(sfx);
+            }
+            if (tid == 0) {
+                float tau = 0.f;
+                for (int k = 0; k < Qb; ++k) tau += ell[k];
+                misc[0] = expf(tau);
+            }
         }
-        float tau = 0.f;
-        for (int k = 0; k < Qb; ++k) tau += ell[k];
-        const float etau = expf(tau);
         // pair quantities (i, j): L_ij by a direct sum, G_ij, X_ij
         for (int q = tid; q < Qb * Qb; q += kBwdThreads) {
             const int i = q / Qb, j = q - i * Qb;
             float a1 = 0.f, a2 = 0.f, w = 0.f;
-            if (j <= i) {
-                float seg = 0.f;
+            float seg = 0.f;
+            if constexpr (kT) {   // a warp holds row i, lane = j: seg = sum_{k=j+1..i} l_k by shuffles
+                seg = warp_suffix((j + 1 <= i) ? ell[j + 1] : 0.f);
+            } else {
                 for (int k = j + 1; k <= i; ++k) seg += ell[k];
+            }
+            if (j <= i) {
                 const float Lij = expf(seg);
                 float gij = 0.f, xij = 0.f;
 #pragma unroll 8
@@ -328,6 +384,7 @@ __global__ void __launch_bounds__(kBwdThreads) ssd_bwd_chunk(BwdArgs a) {
             if (kT) A2dtT[j * L.st + i] = a2 * dts[j];
         }
         __syncthreads();
+        const float etau = misc[0];
         if constexpr (kT) {
             // dx and the per-token dot products of ddt: thread = (p, two rows j0, j0 + 1)
             {
@@ -463,11 +520,12 @@ __global__ void __launch_bounds__(kBwdThreads) ssd_bwd_chunk(BwdArgs a) {
         {
             const int w = tid >> 5, lane = tid & 31;
             for (int t = w; t < Qb; t += kBwdThreads / 32) {
-                float s1 = 0.f, s2 = 0.f, s3 = 0.f, s4 = 0.f;
+                float s1 = 0.f, s2 = 0.f, s3 = 0.f, s4 = 0.f, s5 = 0.f;
                 for (int p = lane; p < P; p += 32) {
                     s1 += vx[t * P + p];
                     s2 += lbx[t * P + p];
                     s3 += scdy[t * P + p];
+                    s5 = fmaf(dys[t * P + p], xs[t * L.sx + p], s5);
                 }
                 for (int i = t + lane; i < Qb; i += 32)
                     for (int j = 0; j <= t; ++j) s4 += Wm[i * Qb + j];
@@ -475,7 +533,9 @@ __global__ void __launch_bounds__(kBwdThreads) ssd_bwd_chunk(BwdArgs a) {
                 s2 = warp_sum(s2);
                 s3 = warp_sum(s3);
                 s4 = warp_sum(s4);
+                s5 = warp_sum(s5);
                 if (lane == 0) {
+                    ddv[t] = s5;
                     ddta[t] = s1;
                     wv[t] = es[t] * dts[t] * s2;
                     uv[t] = ep[t] * s3;
@@ -484,25 +544,33 @@ __global__ void __launch_bounds__(kBwdThreads) ssd_bwd_chunk(BwdArgs a) {
             }
         }
         __syncthreads();
-        if (tid < Qb) {
-            const int t = tid;
-            float U = 0.f, V = 0.f;
-            for (int i = t; i < Qb; ++i) U += uv[i];
-            for (int j = 0; j <= t; ++j) V += wv[j];
-            const float dl = rv[t] + U + V + etau * K - dts[t] * ddta[t];
-            if (t0 + t < Lseq) a.ddt[(size_t)(b * Lseq + t0 + t) * H + h] = fmaf(Ah, dl, ddta[t]);
-            const float da = dts[t] * dl;
-            float dd = 0.f;
-            for (int p = 0; p < P; ++p) dd = fmaf(dys[t * P + p], xs[t * L.sx + p], dd);
-            // thread 0 sums these in token order below
-            ddta[t] = da;
-            wv[t] = dd;
-        }
-        __syncthreads();
-        if (tid == 0) {
-            for (int t = 0; t < Qb; ++t) {
-                dA_acc += ddta[t];
-                dD_acc += wv[t];
+        if constexpr (kT) {
+            if (tid < 32) {   // warp 0, lane = token
+                const int t = tid;
+                const float U = warp_suffix(uv[t]), V = warp_prefix(wv[t]);
+                const float dl = rv[t] + U + V + etau * K - dts[t] * ddta[t];
+                if (t0 + t < Lseq) a.ddt[(size_t)(b * Lseq + t0 + t) * H + h] = fmaf(Ah, dl, ddta[t]);
+                const float da = warp_sum(dts[t] * dl), dd = warp_sum(ddv[t]);
+                dA_acc += da;
+                dD_acc += dd;
+            }
+        } else {
+            if (tid < Qb) {
+                const int t = tid;
+                float U = 0.f, V = 0.f;
+                for (int i = t; i < Qb; ++i) U += uv[i];
+                for (int j = 0; j <= t; ++j) V += wv[j];
+                const float dl = rv[t] + U + V + etau * K - dts[t] * ddta[t];
+                if (t0 + t < Lseq) a.ddt[(size_t)(b * Lseq + t0 + t) * H + h] = fmaf(Ah, dl, ddta[t]);
+                // thread 0 sums these in token order below
+                ddta[t] = dts[t] * dl;
+            }
+            __syncthreads();
+            if (tid == 0) {
+                for (int t = 0; t < Qb; ++t) {
+                    dA_acc += ddta[t];
+                    dD_acc += ddv[t];
+                }
             }
         }
         // Lam becomes the adjoint of the state entering this chunk
