@@ -106,6 +106,24 @@ def peaks():
     return FALLBACK_HBM_GBS, "fallback"
 
 
+def slowest_rank(times, device):
+    """Each timing's maximum over the ranks of the process group (the job is as
+    fast as its slowest rank); the local values when there is no group."""
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor(list(times), dtype=torch.float64, device=device)
+    if dist.is_initialized() and dist.get_world_size() > 1:
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        dist.barrier()
+    return [float(v) for v in t]
+
+
+def job_rate(units_per_rank, world, ms):
+    """Whole-job throughput: the units every rank processed over the slowest
+    rank's time per step (weak scaling: each rank runs its own copy)."""
+    return world * units_per_rank / (ms / 1e3)
+
+
 def dist_env():
     return int(os.environ.get("RANK", 0)), int(os.environ.get("LOCAL_RANK", 0)), int(os.environ.get("WORLD_SIZE", 1))
 
@@ -360,17 +378,13 @@ def run_decode(args, p, dev, rank, local_rank, world):
     torch.cuda.synchronize()
     e2e_ms = e0.elapsed_time(e1) / args.steps
 
-    t_tensor = torch.tensor([ms, e2e_ms], dtype=torch.float64, device=dev)
-    if world > 1:
-        dist.all_reduce(t_tensor, op=dist.ReduceOp.MAX)
-        dist.barrier()
-    ms_max, e2e_max = float(t_tensor[0]), float(t_tensor[1])
+    ms_max, e2e_max = slowest_rank([ms, e2e_ms], dev)
     if rank == 0:
         nbytes = decode_bytes(p)
         peak, peak_kind = peaks()
         achieved = nbytes / (ms / 1e3) / 1e9
         line = {
-            "metric": DECODE_METRIC, "value": world * p.batch / (ms_max / 1e3), "unit": "tokens/s",
+            "metric": DECODE_METRIC, "value": job_rate(p.batch, world, ms_max), "unit": "tokens/s",
             "n_gpus": world, "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_max,
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32",
             "data": "synthetic",
@@ -381,7 +395,7 @@ def run_decode(args, p, dev, rank, local_rank, world):
             "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
                          "frac": achieved / peak, "peak_source": peak_kind, "traffic": None,
                          "scope": "state read + write, x, y, dt, B, C of one ssd_step launch"},
-            "e2e": {"value": world * p.batch / (e2e_max / 1e3), "unit": "tokens/s", "h2d_bytes_per_step": h2d,
+            "e2e": {"value": job_rate(p.batch, world, e2e_max), "unit": "tokens/s", "h2d_bytes_per_step": h2d,
                     "d2h_bytes_per_step": d2h},
             "gpu_launches": args.steps,
             "clocks": clk.summary(),
@@ -469,17 +483,13 @@ def run_bwd(args, p, dev, rank, local_rank, world):
     torch.cuda.synchronize()
     e2e_ms = e0.elapsed_time(e1) / args.steps
 
-    t_tensor = torch.tensor([ms, e2e_ms], dtype=torch.float64, device=dev)
-    if world > 1:
-        dist.all_reduce(t_tensor, op=dist.ReduceOp.MAX)
-        dist.barrier()
-    ms_max, e2e_max = float(t_tensor[0]), float(t_tensor[1])
+    ms_max, e2e_max = slowest_rank([ms, e2e_ms], dev)
     tokens = p.batch * p.seqlen
     if rank == 0:
         fl = bwd_flops(p)
         achieved = fl / (ms / 1e3) / 1e12
         line = {
-            "metric": BWD_METRIC, "value": world * tokens / (ms_max / 1e3), "unit": "tokens/s", "n_gpus": world,
+            "metric": BWD_METRIC, "value": job_rate(tokens, world, ms_max), "unit": "tokens/s", "n_gpus": world,
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_max, "higher_is_better": True,
             "scaling": "weak", "vs_baseline": None, "dtype": "f32", "data": "synthetic",
             "config": {"workload": "bwd_" + p.name, "batch": p.batch, "seq_len": p.seqlen, "nheads": p.nheads,
@@ -491,7 +501,7 @@ def run_bwd(args, p, dev, rank, local_rank, world):
                          "frac": achieved / FP32_PEAK_TFLOPS,
                          "peak_source": "derived: 152 SMs x 128 fp32 lanes x 2 x 2.07 GHz", "traffic": None,
                          "scope": "algorithmic fp32 flops of the whole ssd_bwd call (2 launches)"},
-            "e2e": {"value": world * tokens / (e2e_max / 1e3), "unit": "tokens/s", "h2d_bytes_per_step": h2d,
+            "e2e": {"value": job_rate(tokens, world, e2e_max), "unit": "tokens/s", "h2d_bytes_per_step": h2d,
                     "d2h_bytes_per_step": d2h},
             "gpu_launches": 2 * args.steps,
             "clocks": clk.summary(),
@@ -640,14 +650,10 @@ def run_ours(args):
     assert f.check_status() == 0
     e2e_ms = e0.elapsed_time(e1) / args.steps
 
-    t_tensor = torch.tensor([ms, e2e_ms], dtype=torch.float64, device=dev)
-    if world > 1:
-        dist.all_reduce(t_tensor, op=dist.ReduceOp.MAX)
-        dist.barrier()
-    ms_max, e2e_max = float(t_tensor[0]), float(t_tensor[1])
+    ms_max, e2e_max = slowest_rank([ms, e2e_ms], dev)
     tokens = p.batch * p.seqlen
-    value = world * tokens / (ms_max / 1e3)
-    e2e_value = world * tokens / (e2e_max / 1e3)
+    value = job_rate(tokens, world, ms_max)
+    e2e_value = job_rate(tokens, world, e2e_max)
     if rank == 0:
         nbytes = compulsory_bytes(p)
         peak, peak_kind = peaks()
