@@ -308,8 +308,13 @@ def cpu_baseline(p):
         t_all += time.perf_counter() - t0
         reps += 1
     tok = q.batch * q.seqlen * reps
+    # the same sample on one thread, once
+    t0 = time.perf_counter()
+    oracle.ssd_recurrence(q, want_final=False, nthreads=1)
+    t1 = time.perf_counter() - t0
     return {"value": tok / t_all, "unit": "tokens/s", "cores": oracle.max_threads(), "kind": "oracle",
-            "sample": f"fp64 recurrence on batch row 0 of {p.name}, {reps} passes, {t_all:.1f} s wall"}
+            "sample": f"fp64 recurrence on batch row 0 of {p.name}, {reps} passes, {t_all:.1f} s wall",
+            "single_thread_value": q.batch * q.seqlen / t1}
 
 
 def run_decode(args, p, dev, rank, local_rank, world):
