@@ -370,10 +370,29 @@ __global__ void __launch_bounds__(kBwdThreads) ssd_bwd_chunk(BwdArgs a) {
             if (j <= i) {
                 const float Lij = expf(seg);
                 float gij = 0.f, xij = 0.f;
+                if constexpr (kT) {   // row i as broadcast vectors, column j from the transposes
+#pragma unroll 4
+                    for (int n = 0; n < 128; n += 4) {
+                        const float4 cc = *reinterpret_cast<const float4*>(Cs + i * 128 + n);
+                        gij = fmaf(cc.x, BT[(n + 0) * L.st + j], gij);
+                        gij = fmaf(cc.y, BT[(n + 1) * L.st + j], gij);
+                        gij = fmaf(cc.z, BT[(n + 2) * L.st + j], gij);
+                        gij = fmaf(cc.w, BT[(n + 3) * L.st + j], gij);
+                    }
+#pragma unroll 4
+                    for (int p = 0; p < 64; p += 4) {
+                        const float4 dd = *reinterpret_cast<const float4*>(dys + i * 64 + p);
+                        xij = fmaf(dd.x, xT[(p + 0) * L.st + j], xij);
+                        xij = fmaf(dd.y, xT[(p + 1) * L.st + j], xij);
+                        xij = fmaf(dd.z, xT[(p + 2) * L.st + j], xij);
+                        xij = fmaf(dd.w, xT[(p + 3) * L.st + j], xij);
+                    }
+                } else {
 #pragma unroll 8
-                for (int n = 0; n < N; ++n) gij = fmaf(Cs[i * N + n], Bs[j * L.sb + n], gij);
+                    for (int n = 0; n < N; ++n) gij = fmaf(Cs[i * N + n], Bs[j * L.sb + n], gij);
 #pragma unroll 8
-                for (int p = 0; p < P; ++p) xij = fmaf(dys[i * P + p], xs[j * L.sx + p], xij);
+                    for (int p = 0; p < P; ++p) xij = fmaf(dys[i * P + p], xs[j * L.sx + p], xij);
+                }
                 a1 = Lij * gij;
                 a2 = Lij * xij;
                 w = a1 * dts[j] * xij;
@@ -386,39 +405,52 @@ __global__ void __launch_bounds__(kBwdThreads) ssd_bwd_chunk(BwdArgs a) {
         __syncthreads();
         const float etau = misc[0];
         if constexpr (kT) {
-            // dx and the per-token dot products of ddt: thread = (p, two rows j0, j0 + 1)
+            // dx and the per-token dot products of ddt.  Threads 0-511: Lam B_j and v_j for
+            // (p, rows j0 .. j0 + 3); threads 512-1023: S_in C_j for the same tiles.
             {
-                const int p = tid & 63, j0 = (tid >> 6) * 2;
-                float lb0 = 0.f, lb1 = 0.f, sc0 = 0.f, sc1 = 0.f;
+                const int half = tid >> 9, tt = tid & 511;
+                const int p = tt & 63, j0 = (tt >> 6) * 4;
+                const float* M = half ? Sin : Lam;
+                const float* V = half ? CT : BT;
+                float acc[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll 8
                 for (int n = 0; n < 128; ++n) {
-                    const float lam = Lam[p * L.sb + n], sin = Sin[p * L.sb + n];
-                    const float2 bb = *reinterpret_cast<const float2*>(BT + n * L.st + j0);
-                    const float2 cc = *reinterpret_cast<const float2*>(CT + n * L.st + j0);
-                    lb0 = fmaf(lam, bb.x, lb0);
-                    lb1 = fmaf(lam, bb.y, lb1);
-                    sc0 = fmaf(sin, cc.x, sc0);
-                    sc1 = fmaf(sin, cc.y, sc1);
+                    const float m = M[p * L.sb + n];
+                    const float4 vv = *reinterpret_cast<const float4*>(V + n * L.st + j0);
+                    acc[0] = fmaf(m, vv.x, acc[0]);
+                    acc[1] = fmaf(m, vv.y, acc[1]);
+                    acc[2] = fmaf(m, vv.z, acc[2]);
+                    acc[3] = fmaf(m, vv.w, acc[3]);
                 }
-                float v0 = es[j0] * lb0, v1 = es[j0 + 1] * lb1;
-#pragma unroll 4
-                for (int i = j0; i < 32; ++i) {
-                    const float2 aa = *reinterpret_cast<const float2*>(A1 + i * 32 + j0);   // 0 where j > i
-                    const float d = dys[i * 64 + p];
-                    v0 = fmaf(aa.x, d, v0);
-                    v1 = fmaf(aa.y, d, v1);
-                }
-                const float lbs[2] = {lb0, lb1}, vs[2] = {v0, v1}, scs[2] = {sc0, sc1};
+                if (half == 0) {
+                    float v[4];
 #pragma unroll
-                for (int u = 0; u < 2; ++u) {
-                    const int j = j0 + u, q = j * 64 + p;
-                    const float xv = xs[j * L.sx + p], dv = dys[j * 64 + p];
-                    vx[q] = vs[u] * xv;
-                    lbx[q] = lbs[u] * xv;
-                    scdy[q] = scs[u] * dv;
-                    if (t0 + j < Lseq)
-                        Elem<T>::store(static_cast<T*>(a.dx) + ((size_t)(b * Lseq + t0 + j) * H + h) * 64 + p,
-                                       fmaf(dts[j], vs[u], Dh * dv));
+                    for (int u = 0; u < 4; ++u) v[u] = es[j0 + u] * acc[u];
+#pragma unroll 4
+                    for (int i = j0; i < 32; ++i) {
+                        const float4 aa = *reinterpret_cast<const float4*>(A1 + i * 32 + j0);   // 0 where j > i
+                        const float d = dys[i * 64 + p];
+                        v[0] = fmaf(aa.x, d, v[0]);
+                        v[1] = fmaf(aa.y, d, v[1]);
+                        v[2] = fmaf(aa.z, d, v[2]);
+                        v[3] = fmaf(aa.w, d, v[3]);
+                    }
+#pragma unroll
+                    for (int u = 0; u < 4; ++u) {
+                        const int j = j0 + u, q = j * 64 + p;
+                        const float xv = xs[j * L.sx + p], dv = dys[j * 64 + p];
+                        vx[q] = v[u] * xv;
+                        lbx[q] = acc[u] * xv;
+                        if (t0 + j < Lseq)
+                            Elem<T>::store(static_cast<T*>(a.dx) + ((size_t)(b * Lseq + t0 + j) * H + h) * 64 + p,
+                                           fmaf(dts[j], v[u], Dh * dv));
+                    }
+                } else {
+#pragma unroll
+                    for (int u = 0; u < 4; ++u) {
+                        const int j = j0 + u;
+                        scdy[j * 64 + p] = acc[u] * dys[j * 64 + p];
+                    }
                 }
             }
             // this head's shares of dB and dC: thread = (n, four rows j0 .. j0 + 3)
