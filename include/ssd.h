@@ -106,6 +106,22 @@ SSD_API int ssd_fwd(const ssd_params_t* p,
             void* y, float* final_states,
             void* workspace, size_t workspace_bytes, void* stream);
 
+/* ssd_fwd() for measurement: the same call, with a CUDA event recorded on
+ * `stream` before and after each of its kernel launches.  Synchronises on the
+ * last event, writes the first min(launches, max_launches) launch durations in
+ * milliseconds to ms_per_launch (in launch order: for split plans the
+ * aggregate pass, the composition, then the full pass) and the launch count
+ * to *nlaunches.  Creates and destroys its events on every call: meant for
+ * benchmarks, not for the hot path.  Errors as ssd_fwd(); SSD_ERR_INVALID_ARG
+ * when ms_per_launch or nlaunches is NULL or max_launches < 1. */
+SSD_API int ssd_fwd_timed(const ssd_params_t* p,
+            const void* x, const float* dt, const float* A,
+            const void* B, const void* C, const float* D,
+            const float* initial_states, const int32_t* cu_seqlens,
+            void* y, float* final_states,
+            void* workspace, size_t workspace_bytes, void* stream,
+            float* ms_per_launch, int max_launches, int* nlaunches);
+
 /* ssd_fwd() for callers that cannot allocate device memory (for example a
  * plugin inside a host application that owns every device allocation, or a
  * C caller that only holds the input and output pointers it was given).

@@ -84,6 +84,21 @@ class SSDForward:
 
     def __call__(self, x, dt, A, B, C, D=None, initial_states=None, cu_seqlens=None, y=None,
                  final_states=None, stream=None):
+        args, y = self._args(x, dt, A, B, C, D, initial_states, cu_seqlens, y, final_states, stream)
+        _lib.check(_lib.lib.ssd_fwd(*args), "ssd_fwd")
+        return y
+
+    def launch_times(self, x, dt, A, B, C, D=None, initial_states=None, cu_seqlens=None, y=None,
+                     final_states=None, stream=None):
+        """The same call through ssd_fwd_timed: returns the duration (ms) of each
+        kernel launch, in launch order (synchronises the stream)."""
+        args, _ = self._args(x, dt, A, B, C, D, initial_states, cu_seqlens, y, final_states, stream)
+        ms = (ctypes.c_float * 4)()
+        n = ctypes.c_int(0)
+        _lib.check(_lib.lib.ssd_fwd_timed(*args, ms, 4, ctypes.byref(n)), "ssd_fwd_timed")
+        return [float(ms[k]) for k in range(min(n.value, 4))]
+
+    def _args(self, x, dt, A, B, C, D, initial_states, cu_seqlens, y, final_states, stream):
         p = self.params
         shp_x = (p.batch, p.seqlen, p.nheads, p.headdim)
         shp_bc = (p.batch, p.seqlen, p.ngroups, p.dstate)
@@ -106,11 +121,10 @@ class SSDForward:
             raise ValueError("cu_seqlens: expected int32 (ndocs + 1) on the device")
         if y is None:
             y = torch.empty(shp_x, dtype=self.dtype, device=self.device)
-        rc = _lib.lib.ssd_fwd(ctypes.byref(p), _ptr(x), _ptr(dt), _ptr(A), _ptr(B), _ptr(C), _ptr(D),
-                              _ptr(initial_states), _ptr(cu_seqlens), _ptr(y), _ptr(final_states),
-                              _ptr(self.workspace), self.workspace.numel(), _stream_handle(stream))
-        _lib.check(rc, "ssd_fwd")
-        return y
+        args = (ctypes.byref(p), _ptr(x), _ptr(dt), _ptr(A), _ptr(B), _ptr(C), _ptr(D), _ptr(initial_states),
+                _ptr(cu_seqlens), _ptr(y), _ptr(final_states), _ptr(self.workspace), self.workspace.numel(),
+                _stream_handle(stream))
+        return args, y
 
     def check_status(self, stream=None) -> int:
         return check_status(self.workspace, stream)

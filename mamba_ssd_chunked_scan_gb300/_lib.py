@@ -19,7 +19,7 @@ STATUS = {0: "SSD_OK", 1: "SSD_ERR_INVALID_ARG", 2: "SSD_ERR_UNSUPPORTED", 3: "S
 # every symbol include/ssd.h declares
 EXPORTS = ("ssd_fwd_workspace_size", "ssd_workspace_init", "ssd_fwd", "ssd_check_status",
            "ssd_status_string", "ssd_fwd_plan", "ssd_segsum_dump", "ssd_fwd_static_scratch", "ssd_step",
-           "ssd_bwd_workspace_size", "ssd_bwd")
+           "ssd_bwd_workspace_size", "ssd_bwd", "ssd_fwd_timed")
 
 
 class SSDParams(ctypes.Structure):
@@ -54,6 +54,9 @@ def _load():
     lib.ssd_fwd_plan.argtypes = [P, ctypes.c_int, ctypes.c_int, ctypes.POINTER(ctypes.c_int),
                                  ctypes.POINTER(ctypes.c_int)]
     lib.ssd_fwd_plan.restype = ctypes.c_int
+    lib.ssd_fwd_timed.argtypes = [P, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, sz, vp,
+                                  ctypes.POINTER(ctypes.c_float), ctypes.c_int, ctypes.POINTER(ctypes.c_int)]
+    lib.ssd_fwd_timed.restype = ctypes.c_int
     lib.ssd_fwd_static_scratch.argtypes = [P, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp]
     lib.ssd_fwd_static_scratch.restype = ctypes.c_int
     lib.ssd_bwd_workspace_size.argtypes = [P]

@@ -263,9 +263,21 @@ int ssd_check_status(void* workspace, void* stream) {
     return (int)h.status;
 }
 
-int ssd_fwd(const ssd_params_t* p, const void* x, const float* dt, const float* A, const void* B,
-            const void* C, const float* D, const float* init, const int32_t* cu, void* y,
-            float* fin, void* workspace, size_t workspace_bytes, void* stream) {
+}  // extern "C"
+
+namespace {
+
+// Events recorded around each launch of one forward call (the measurement entry
+// point ssd_fwd_timed only).
+constexpr int kMaxTimedLaunches = 4;
+struct LaunchTimer {
+    cudaEvent_t ev[2 * kMaxTimedLaunches];
+    int n = 0;
+};
+
+int fwd_impl(const ssd_params_t* p, const void* x, const float* dt, const float* A, const void* B,
+             const void* C, const float* D, const float* init, const int32_t* cu, void* y,
+             float* fin, void* workspace, size_t workspace_bytes, void* stream, LaunchTimer* tm) {
     int rc = check_params(p);
     if (rc != SSD_OK) return rc;
     if (!x || !dt || !A || !B || !C || !y) return SSD_ERR_INVALID_ARG;
@@ -305,7 +317,14 @@ int ssd_fwd(const ssd_params_t* p, const void* x, const float* dt, const float* 
     const bool tc = use_tc(p, init != nullptr);
     a.Q = tc ? p->chunk : simt_chunk(p);
     if (a.Q == 0) return SSD_ERR_UNSUPPORTED;
-    auto launch = [&](const FwdArgs& aa) { return tc ? launch_tc(aa, st) : launch_simt(aa, st); };
+    auto timed = [&](cudaError_t (*fn)(const FwdArgs&, cudaStream_t), const FwdArgs& aa) {
+        const bool rec = tm && tm->n < kMaxTimedLaunches;
+        if (rec) cudaEventRecord(tm->ev[2 * tm->n], st);
+        const cudaError_t e = fn(aa, st);
+        if (rec) cudaEventRecord(tm->ev[2 * tm->n++ + 1], st);
+        return e;
+    };
+    auto launch = [&](const FwdArgs& aa) { return timed(tc ? launch_tc : launch_simt, aa); };
     if (tc && tp.T > 0) {
         // leftover-unit plan: aggregates of the pieces, their composition, then the
         // whole units and the pieces in one launch
@@ -321,7 +340,7 @@ int ssd_fwd(const ssd_params_t* p, const void* x, const float* dt, const float* 
         FwdArgs sa = a;   // the scan runs over T "rows" of m splits
         sa.batch = 1;
         sa.H = tp.T;
-        if (launch_split_scan(sa, st) != cudaSuccess) return SSD_ERR_CUDA;
+        if (timed(launch_split_scan, sa) != cudaSuccess) return SSD_ERR_CUDA;
         a.mode = kModeFull;
         a.grid_units = a.tail_first + (int64_t)tp.T * tp.m;
         if (launch(a) != cudaSuccess) return SSD_ERR_CUDA;
@@ -330,11 +349,43 @@ int ssd_fwd(const ssd_params_t* p, const void* x, const float* dt, const float* 
     if (ns > 1) {
         a.mode = kModeAggregate;
         if (launch(a) != cudaSuccess) return SSD_ERR_CUDA;
-        if (launch_split_scan(a, st) != cudaSuccess) return SSD_ERR_CUDA;
+        if (timed(launch_split_scan, a) != cudaSuccess) return SSD_ERR_CUDA;
     }
     a.mode = kModeFull;
     if (launch(a) != cudaSuccess) return SSD_ERR_CUDA;
     return SSD_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+int ssd_fwd(const ssd_params_t* p, const void* x, const float* dt, const float* A, const void* B,
+            const void* C, const float* D, const float* init, const int32_t* cu, void* y,
+            float* fin, void* workspace, size_t workspace_bytes, void* stream) {
+    return fwd_impl(p, x, dt, A, B, C, D, init, cu, y, fin, workspace, workspace_bytes, stream, nullptr);
+}
+
+int ssd_fwd_timed(const ssd_params_t* p, const void* x, const float* dt, const float* A, const void* B,
+                  const void* C, const float* D, const float* init, const int32_t* cu, void* y,
+                  float* fin, void* workspace, size_t workspace_bytes, void* stream,
+                  float* ms_per_launch, int max_launches, int* nlaunches) {
+    if (!ms_per_launch || max_launches < 1 || !nlaunches) return SSD_ERR_INVALID_ARG;
+    LaunchTimer tm;
+    int made = 0;
+    for (; made < 2 * kMaxTimedLaunches; ++made)
+        if (cudaEventCreate(&tm.ev[made]) != cudaSuccess) break;
+    int rc = made == 2 * kMaxTimedLaunches ? SSD_OK : SSD_ERR_CUDA;
+    if (rc == SSD_OK) rc = fwd_impl(p, x, dt, A, B, C, D, init, cu, y, fin, workspace, workspace_bytes, stream, &tm);
+    *nlaunches = 0;
+    if (rc == SSD_OK && tm.n > 0 && cudaEventSynchronize(tm.ev[2 * tm.n - 1]) != cudaSuccess) rc = SSD_ERR_CUDA;
+    if (rc == SSD_OK) {
+        for (int k = 0; k < tm.n && k < max_launches; ++k)
+            if (cudaEventElapsedTime(&ms_per_launch[k], tm.ev[2 * k], tm.ev[2 * k + 1]) != cudaSuccess) rc = SSD_ERR_CUDA;
+        *nlaunches = tm.n;
+    }
+    for (int k = 0; k < made; ++k) cudaEventDestroy(tm.ev[k]);
+    return rc;
 }
 
 int ssd_fwd_static_scratch(const ssd_params_t* p, const void* x, const float* dt, const float* A,

@@ -186,3 +186,14 @@ def test_bwd_invalid_args(L, case, code):
                        None if cu is None else vp(cu), v("dy"), None, v("dx"), v("ddt"), v("dA"), v("dB"),
                        v("dC"), None, None, v("ws"), nbytes, None)
     assert rc == code
+
+
+def test_fwd_timed_rejects_missing_outputs(L):
+    p = params(L)
+    n = ctypes.c_int(0)
+    ms = (ctypes.c_float * 4)()
+    vp = ctypes.c_void_p
+    args = [ctypes.byref(p)] + [vp(1 << 40)] * 10 + [vp(1 << 41), 256, None]
+    assert L.lib.ssd_fwd_timed(*args, None, 4, ctypes.byref(n)) == 1
+    assert L.lib.ssd_fwd_timed(*args, ms, 0, ctypes.byref(n)) == 1
+    assert L.lib.ssd_fwd_timed(*args, ms, 4, None) == 1
