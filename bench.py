@@ -124,6 +124,25 @@ def job_rate(units_per_rank, world, ms):
     return world * units_per_rank / (ms / 1e3)
 
 
+def device_copy_gbps(dev, stream, nbytes=1 << 30, reps=5):
+    """Context only: a 1 GiB device-to-device copy (read + write bytes over its
+    CUDA-event time, best of `reps`), the copy bandwidth of this GPU now."""
+    import torch
+    src = torch.empty(nbytes, dtype=torch.uint8, device=dev)
+    dst = torch.empty_like(src)
+    dst.copy_(src)
+    best = 0.0
+    for _ in range(reps):
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        dst.copy_(src)
+        b.record(stream)
+        b.synchronize()
+        best = max(best, 2 * nbytes / (a.elapsed_time(b) / 1e3) / 1e9)
+    del src, dst
+    return best
+
+
 def tail_pieces(p, nsm=152):
     """Pieces with an incoming state under the leftover-unit plan (one split):
     the last U % S units are cut into m pieces, all but the first of each
@@ -629,6 +648,7 @@ def run_ours(args):
         flush.zero_()
         per_launch.append(f.launch_times(x, dt, A, B, C, D, init, cu, y=y, final_states=fin, stream=stream))
     launch_ms = [sum(r[k] for r in per_launch) / len(per_launch) for k in range(len(per_launch[0]))]
+    copy_bw = device_copy_gbps(dev, stream)
 
     # End to end through the public API, as a job that streams batches runs it: every
     # step copies its inputs from pinned host memory to the device and its result back
@@ -714,10 +734,10 @@ def run_ours(args):
                        "compulsory_bytes": nbytes, "achieved_GBps_call": achieved_call,
                        "frac_call": achieved_call / peak,
                        "pct_of_8TBps_spec_call": 100.0 * achieved_call / 8000.0,
-                       "launch_ms": launch_ms},
+                       "launch_ms": launch_ms, "copy_GBps_here": copy_bw},
             "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
                          "frac": achieved / peak, "peak_source": peak_kind, "traffic": traffic,
-                         "algorithmic_bytes": kernel_bytes,
+                         "algorithmic_bytes": kernel_bytes, "frac_of_8TBps_spec": achieved / 8000.0,
                          "scope": ("the full-pass launch of ssd_chunk_tc: compulsory bytes plus incoming "
                                    "states, over its own CUDA-event duration; config.frac_call is the "
                                    f"whole call ({launches} launches)") if family == 1 else
