@@ -48,7 +48,7 @@ def _load():
             lib.oracle_ssd_recurrence.argtypes = common + [d, d, ci]
             lib.oracle_ssd_quadratic.argtypes = common + [d]
             lib.oracle_ssd_chunked.argtypes = common + [ci, i64, d, d]
-            lib.oracle_ssd_backward.argtypes = [i64, i64, ci, ci, ci, ci, d, d, d, d, d, d, d, d, d,
+            lib.oracle_ssd_backward.argtypes = [i64, i64, ci, ci, ci, ci, d, d, d, d, d, d, d, i32, ci, d, d,
                                                 d, d, d, d, d, d, d, ci]
             lib.oracle_segsum.argtypes = [d, i64, ci, d]
             lib.oracle_diff_segsum_f32.argtypes = [f, i64, ci, f]
@@ -136,25 +136,25 @@ def ssd_step(state, x, dt, A, B, C, D=None):
 
 def ssd_backward(p, dy, dfinal=None, nthreads: int = 0):
     """Gradients of <dy, y> + <dfinal, final_states> with respect to every input
-    of the forward pass, fp64 (batch rows only, no packed documents).
+    of the forward pass, fp64 (batch rows, or packed documents each with its own
+    initial and final state).
 
     Returns a dict of arrays: dx, ddt, dA, dB, dC, dD (None without D) and
     dinit (the initial states' gradient, also when the forward had none)."""
     _check(p)
-    if p.cu_seqlens is not None:
-        raise ValueError("the backward oracle takes batch rows only")
     lib = _load()
-    arrs, _ = _args(p)
+    arrs, cu = _args(p)
+    cup = None if cu is None else cu.ctypes.data_as(ctypes.POINTER(ctypes.c_int32))
     dy64 = _f64(dy)
     df64 = _f64(dfinal)
     out = dict(dx=np.zeros((p.batch, p.seqlen, p.nheads, p.headdim)), ddt=np.zeros((p.batch, p.seqlen, p.nheads)),
                dA=np.zeros(p.nheads), dB=np.zeros((p.batch, p.seqlen, p.ngroups, p.dstate)),
                dC=np.zeros((p.batch, p.seqlen, p.ngroups, p.dstate)),
                dD=None if p.D is None else np.zeros(p.nheads),
-               dinit=np.zeros((p.batch, p.nheads, p.headdim, p.dstate)))
+               dinit=np.zeros((p.nstates, p.nheads, p.headdim, p.dstate)))
     lib.oracle_ssd_backward(p.batch, p.seqlen, p.nheads, p.headdim, p.dstate, p.ngroups,
                             _dp(arrs["x"]), _dp(arrs["dt"]), _dp(arrs["A"]), _dp(arrs["B"]), _dp(arrs["C"]),
-                            _dp(arrs["D"]), _dp(arrs["init"]), _dp(dy64), _dp(df64),
+                            _dp(arrs["D"]), _dp(arrs["init"]), cup, p.ndocs, _dp(dy64), _dp(df64),
                             _dp(out["dx"]), _dp(out["ddt"]), _dp(out["dA"]), _dp(out["dB"]), _dp(out["dC"]),
                             _dp(out["dD"]), _dp(out["dinit"]), int(nthreads))
     return out

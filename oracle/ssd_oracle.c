@@ -33,8 +33,8 @@
  *                          backwards in time from the stored per-token states
  *                          (the states the backward pass needs, "Parallel Scan and
  *                          Hardware-Aware SSM Kernels", "Why the kernel matters
- *                          more than the algorithm").  Batch rows only (no packed
- *                          documents).
+ *                          more than the algorithm"), batch rows or packed
+ *                          documents.
  *   oracle_segsum          seg(i, j) = sum_{k=j+1..i} l_k for j <= i, -inf
  *                          above the diagonal, accumulated from the diagonal
  *                          leftwards (no prefix subtraction).
@@ -143,7 +143,7 @@ void oracle_ssd_recurrence(int64_t batch, int64_t L, int H, int P, int N, int G,
 /* With S_t = a_t S_{t-1} + dt_t x_t B_t^T, a_t = exp(dt_t A_h), and
  * y_t = S_t C_t + D_h x_t, the adjoint Lam_t of S_t (the gradient of the loss
  * <dy, y> + <dfin, S_final> with respect to S_t, all later uses included) obeys
- *   Lam_t = dy_t C_t^T + a_{t+1} Lam_{t+1},  Lam_{L-1} = dfin + dy_{L-1} C_{L-1}^T
+ *   Lam_t = dy_t C_t^T + a_{t+1} Lam_{t+1},  Lam_e = dfin + dy_e C_e^T at an end e
  * and each token's inputs collect
  *   dx_t  = dt_t Lam_t B_t + D_h dy_t
  *   dB_t += dt_t Lam_t^T x_t              (summed over the heads of the group)
@@ -151,14 +151,19 @@ void oracle_ssd_recurrence(int64_t batch, int64_t L, int H, int P, int N, int G,
  *   dl_t  = a_t <Lam_t, S_{t-1}>          (the log-decay l_t = dt_t A_h)
  *   ddt_t = x_t . (Lam_t B_t) + A_h dl_t
  *   dA_h += dt_t dl_t,  dD_h += dy_t . x_t
- * and the initial state's gradient is a_0 Lam_0.
+ * and a start's initial state gets a_s Lam_s.  With packed documents
+ * (cu != NULL, batch 1) every document is its own sequence: its state starts
+ * from init[d] (or zero), its final state is dfin[d]'s, and no adjoint crosses
+ * a document boundary.
  * Outputs are written (not accumulated into): dx (batch, L, H, P),
  * ddt (batch, L, H), dA (H), dB, dC (batch, L, G, N), dD (H) or NULL,
- * dinit (batch, H, P, N) or NULL.  dfin may be NULL (zero). */
+ * dinit (nst, H, P, N) or NULL; nst = ndocs with cu, else batch.  dfin may be
+ * NULL (zero). */
 void oracle_ssd_backward(int64_t batch, int64_t L, int H, int P, int N, int G,
                          const double* x, const double* dt, const double* A,
                          const double* B, const double* C, const double* D,
-                         const double* init, const double* dy, const double* dfin,
+                         const double* init, const int32_t* cu, int ndocs,
+                         const double* dy, const double* dfin,
                          double* dx, double* ddt, double* dA, double* dB, double* dC,
                          double* dD, double* dinit, int nthreads) {
     const int hpg = H / G;
@@ -173,32 +178,38 @@ void oracle_ssd_backward(int64_t batch, int64_t L, int H, int P, int N, int G,
     for (int64_t b = 0; b < batch; ++b) {
         for (int g = 0; g < G; ++g) {
             const size_t PN = (size_t)P * N;
-            /* states S_{-1} (the initial state) .. S_{L-1} of one head */
-            double* St = (double*)malloc(sizeof(double) * PN * (size_t)(L + 1));
+            /* Sb[t]: the state token t starts from (the initial state at a start) */
+            double* Sb = (double*)malloc(sizeof(double) * PN * (size_t)L);
+            double* S = (double*)malloc(sizeof(double) * PN);
             double* Lam = (double*)malloc(sizeof(double) * PN);
-            double* v = (double*)malloc(sizeof(double) * P);
             /* the heads of group g, in order: each adds its share of dB and dC */
             for (int h = g * hpg; h < (g + 1) * hpg; ++h) {
-                for (int p = 0; p < P; ++p)
-                    for (int n = 0; n < N; ++n)
-                        St[p * N + n] = init ? init[IDX_S(b, h, p, n)] : 0.0;
+                int doc = 0;
                 for (int64_t t = 0; t < L; ++t) {
+                    int start = (t == 0);
+                    if (cu && t > 0 && doc + 1 < ndocs && t == cu[doc + 1]) { ++doc; start = 1; }
+                    if (start) {
+                        const int st = cu ? doc : (int)b;
+                        for (size_t k = 0; k < PN; ++k) S[k] = init ? init[IDX_S(st, h, 0, 0) + (int64_t)k] : 0.0;
+                    }
+                    memcpy(Sb + PN * (size_t)t, S, sizeof(double) * PN);
                     const double d = dt[IDX_DT(b, t, h)];
                     const double a = exp(d * A[h]);
-                    const double* Sp = St + PN * (size_t)t;
-                    double* Sn = St + PN * (size_t)(t + 1);
                     for (int p = 0; p < P; ++p) {
                         const double u = d * x[IDX_X(b, t, h, p)];
-                        for (int n = 0; n < N; ++n)
-                            Sn[p * N + n] = a * Sp[p * N + n] + u * B[IDX_BC(b, t, g, n)];
+                        for (int n = 0; n < N; ++n) S[p * N + n] = a * S[p * N + n] + u * B[IDX_BC(b, t, g, n)];
                     }
                 }
-                for (size_t k = 0; k < PN; ++k) Lam[k] = dfin ? dfin[IDX_S(b, h, 0, 0) + (int64_t)k] : 0.0;
+                /* backwards in time; doc = the document of token t */
                 for (int64_t t = L - 1; t >= 0; --t) {
+                    while (cu && doc > 0 && t < cu[doc]) --doc;
+                    const int st = cu ? doc : (int)b;
+                    const int end = (t == L - 1) || (cu && doc + 1 <= ndocs && t + 1 == cu[doc + 1]);
+                    if (end)   /* the final state of this sequence or document */
+                        for (size_t k = 0; k < PN; ++k) Lam[k] = dfin ? dfin[IDX_S(st, h, 0, 0) + (int64_t)k] : 0.0;
                     const double d = dt[IDX_DT(b, t, h)];
                     const double a = exp(d * A[h]);
-                    const double* Sprev = St + PN * (size_t)t;        /* S_{t-1} */
-                    const double* Scur = St + PN * (size_t)(t + 1);   /* S_t */
+                    const double* Sprev = Sb + PN * (size_t)t;   /* S_{t-1} (or the initial state) */
                     /* Lam becomes Lam_t: add the output's use of S_t */
                     for (int p = 0; p < P; ++p)
                         for (int n = 0; n < N; ++n)
@@ -206,7 +217,8 @@ void oracle_ssd_backward(int64_t batch, int64_t L, int H, int P, int N, int G,
                     for (int n = 0; n < N; ++n) {
                         double sc = 0.0, sb = 0.0;
                         for (int p = 0; p < P; ++p) {
-                            sc += Scur[p * N + n] * dy[IDX_X(b, t, h, p)];
+                            const double scur = a * Sprev[p * N + n] + d * x[IDX_X(b, t, h, p)] * B[IDX_BC(b, t, g, n)];
+                            sc += scur * dy[IDX_X(b, t, h, p)];
                             sb += Lam[p * N + n] * x[IDX_X(b, t, h, p)];
                         }
                         dC[IDX_BC(b, t, g, n)] += sc;
@@ -216,7 +228,6 @@ void oracle_ssd_backward(int64_t batch, int64_t L, int H, int P, int N, int G,
                     for (int p = 0; p < P; ++p) {
                         double acc = 0.0;
                         for (int n = 0; n < N; ++n) acc += Lam[p * N + n] * B[IDX_BC(b, t, g, n)];
-                        v[p] = acc;
                         dx[IDX_X(b, t, h, p)] = d * acc + (D ? D[h] * dy[IDX_X(b, t, h, p)] : 0.0);
                         xv += x[IDX_X(b, t, h, p)] * acc;
                         dyx += dy[IDX_X(b, t, h, p)] * x[IDX_X(b, t, h, p)];
@@ -227,15 +238,16 @@ void oracle_ssd_backward(int64_t batch, int64_t L, int H, int P, int N, int G,
                     ddt[IDX_DT(b, t, h)] = xv + A[h] * dl;
                     dA_part[b * H + h] += d * dl;
                     dD_part[b * H + h] += dyx;
-                    /* Lam becomes the adjoint of S_{t-1} */
+                    /* Lam becomes the adjoint of S_{t-1} (the initial state at a start) */
                     for (size_t k = 0; k < PN; ++k) Lam[k] *= a;
+                    const int start = (t == 0) || (cu && t == cu[doc]);
+                    if (start && dinit)
+                        for (size_t k = 0; k < PN; ++k) dinit[IDX_S(st, h, 0, 0) + (int64_t)k] = Lam[k];
                 }
-                if (dinit)
-                    for (size_t k = 0; k < PN; ++k) dinit[IDX_S(b, h, 0, 0) + (int64_t)k] = Lam[k];
             }
-            free(v);
             free(Lam);
-            free(St);
+            free(S);
+            free(Sb);
         }
     }
     for (int h = 0; h < H; ++h) {
