@@ -171,9 +171,11 @@ SSD_API size_t ssd_bwd_workspace_size(const ssd_params_t* p);
  *   dD               (nheads) fp32, or NULL; written only when D is given
  *   dinitial_states  (batch, nheads, headdim, dstate)   fp32, or NULL
  * All pointers are device memory with 16-byte aligned bases; no output may equal
- * an input.  Packed documents (cu_seqlens) are not supported by the backward
- * pass: cu_seqlens != NULL or ndocs != 0 returns SSD_ERR_UNSUPPORTED, as do
- * headdim * dstate > 8192 and shapes whose tiles do not fit in shared memory.
+ * an input.  Packed documents (cu_seqlens with ndocs, batch 1) are supported
+ * when every document starts from a zero state and carries no final-state
+ * gradient: with cu_seqlens, a non-NULL initial_states, dfinal_states or
+ * dinitial_states returns SSD_ERR_UNSUPPORTED.  So do headdim * dstate > 8192
+ * and shapes whose tiles do not fit in shared memory.
  * `chunk` and `split_len` in p are validated but do not change the result.
  * `workspace`: at least ssd_bwd_workspace_size(p) bytes, 256-byte aligned
  * (else SSD_ERR_WORKSPACE).  Asynchronous on `stream`; two launches; no

@@ -148,15 +148,21 @@ def ssd_fwd(x, dt, A, B, C, D=None, initial_states=None, cu_seqlens=None, *, chu
     return (y, fin) if return_final_states else y
 
 
-def ssd_bwd(x, dt, A, B, C, dy, D=None, initial_states=None, dfinal_states=None, *, chunk=128,
-            want_dinit=True, stream=None):
+def ssd_bwd(x, dt, A, B, C, dy, D=None, initial_states=None, dfinal_states=None, cu_seqlens=None, *,
+            chunk=128, want_dinit=None, stream=None):
     """Gradients of <dy, y> + <dfinal_states, final_states> for one ssd_fwd
-    call's inputs (batch rows, no packed documents).  Returns a dict with dx,
-    ddt, dA, dB, dC, dD (None without D) and dinit (None unless asked)."""
+    call's inputs.  Packed documents (cu_seqlens, batch 1) start from zero
+    states and take no dfinal_states.  Returns a dict with dx, ddt, dA, dB, dC,
+    dD (None without D) and dinit (by default for batch rows only)."""
     batch, seqlen, nheads, headdim = x.shape
     ngroups, dstate = B.shape[2], B.shape[3]
     dev = x.device
-    params = _lib.make_params(batch, seqlen, nheads, headdim, dstate, ngroups, chunk, 0, 0, _dtype_code(x))
+    ndocs = 0 if cu_seqlens is None else cu_seqlens.numel() - 1
+    if want_dinit is None:
+        want_dinit = cu_seqlens is None
+    if cu_seqlens is not None and (cu_seqlens.dtype != torch.int32 or cu_seqlens.device != dev):
+        raise ValueError("cu_seqlens: expected int32 (ndocs + 1) on the device")
+    params = _lib.make_params(batch, seqlen, nheads, headdim, dstate, ngroups, chunk, 0, ndocs, _dtype_code(x))
     shp_x, shp_bc = (batch, seqlen, nheads, headdim), (batch, seqlen, ngroups, dstate)
     shp_s = (batch, nheads, headdim, dstate)
     for name, t, shp, dt_ in (("x", x, shp_x, x.dtype), ("dt", dt, shp_x[:3], torch.float32),
@@ -178,7 +184,7 @@ def ssd_bwd(x, dt, A, B, C, dy, D=None, initial_states=None, dfinal_states=None,
              dB=torch.empty_like(B), dC=torch.empty_like(C), dD=None if D is None else torch.empty_like(D),
              dinit=torch.empty(shp_s, dtype=torch.float32, device=dev) if want_dinit else None)
     rc = _lib.lib.ssd_bwd(ctypes.byref(params), _ptr(x), _ptr(dt), _ptr(A), _ptr(B), _ptr(C), _ptr(D),
-                          _ptr(initial_states), None, _ptr(dy), _ptr(dfinal_states), _ptr(g["dx"]),
+                          _ptr(initial_states), _ptr(cu_seqlens), _ptr(dy), _ptr(dfinal_states), _ptr(g["dx"]),
                           _ptr(g["ddt"]), _ptr(g["dA"]), _ptr(g["dB"]), _ptr(g["dC"]), _ptr(g["dD"]),
                           _ptr(g["dinit"]), _ptr(ws), nbytes, _stream_handle(stream))
     _lib.check(rc, "ssd_bwd")

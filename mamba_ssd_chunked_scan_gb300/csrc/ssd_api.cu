@@ -156,7 +156,7 @@ struct BwdLayout {
 };
 
 bool bwd_layout(const ssd_params_t* p, BwdLayout* l) {
-    if (check_params(p) != SSD_OK || p->ndocs != 0) return false;
+    if (check_params(p) != SSD_OK) return false;
     l->Qb = bwd_chunk(p->headdim, p->dstate, kSmemLimit);
     if (l->Qb == 0) return false;
     const size_t bh = (size_t)p->batch * p->nheads;
@@ -417,7 +417,10 @@ int ssd_bwd(const ssd_params_t* p, const void* x, const float* dt, const float* 
             float* dinit, void* workspace, size_t workspace_bytes, void* stream) {
     int rc = check_params(p);
     if (rc != SSD_OK) return rc;
-    if (cu || p->ndocs != 0) return SSD_ERR_UNSUPPORTED;   // packed documents: forward only
+    if ((cu == nullptr) != (p->ndocs == 0)) return SSD_ERR_INVALID_ARG;
+    // packed documents: each starts from a zero state and has no final-state gradient
+    if (cu && (init || dfin || dinit)) return SSD_ERR_UNSUPPORTED;
+    if (cu && !aligned(cu, 4)) return SSD_ERR_INVALID_ARG;
     if (bwd_chunk(p->headdim, p->dstate, kSmemLimit) == 0) return SSD_ERR_UNSUPPORTED;
     if (p->batch * p->nheads >= ((int64_t)1 << 31)) return SSD_ERR_UNSUPPORTED;
     if (!x || !dt || !A || !B || !C || !dy || !dx || !ddt || !dA || !dB || !dC) return SSD_ERR_INVALID_ARG;
@@ -440,6 +443,7 @@ int ssd_bwd(const ssd_params_t* p, const void* x, const float* dt, const float* 
     a.Qb = l.Qb;
     a.dtype = p->dtype;
     a.x = x; a.dt = dt; a.A = A; a.B = B; a.C = C; a.D = D; a.init = init; a.dy = dy; a.dfin = dfin;
+    a.cu = cu; a.ndocs = p->ndocs;
     a.dx = dx; a.ddt = ddt; a.dA = dA; a.dB = dB; a.dC = dC; a.dD = D ? dD : nullptr; a.dinit = dinit;
     char* ws = static_cast<char*>(workspace);
     a.ws_ckpt = (float*)(ws + l.ckpt);

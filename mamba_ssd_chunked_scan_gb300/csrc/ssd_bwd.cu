@@ -114,6 +114,21 @@ __device__ __forceinline__ float warp_suffix(float v) {
     return v;
 }
 
+// Packed documents: token t starts document d >= 1 (t == cu[d]).  Its log-decay
+// is taken as -inf, so no state and no adjoint cross the boundary (documents
+// start from a zero state and carry no final-state gradient here).
+__device__ __forceinline__ bool doc_start(const BwdArgs& a, int64_t t) {
+    if (!a.cu) return false;
+    int lo = 1, hi = a.ndocs - 1;
+    while (lo <= hi) {
+        const int mid = (lo + hi) >> 1;
+        const int64_t v = __ldg(a.cu + mid);
+        if (v == t) return true;
+        if (v < t) lo = mid + 1; else hi = mid - 1;
+    }
+    return false;
+}
+
 // Block-wide sum (every thread gets the result); `red` holds one float per warp.
 __device__ __forceinline__ float block_sum(float v, float* red) {
     v = warp_sum(v);
@@ -219,7 +234,7 @@ __global__ void __launch_bounds__(kBwdThreads) ssd_bwd_chunk(BwdArgs a) {
         if constexpr (kT) {
             if (tid < 32) {   // warp 0, lane = token: suffix sums by shuffles
                 const float d = (t0 + tid < Lseq) ? a.dt[(size_t)(b * Lseq + t0 + tid) * H + h] : 0.f;
-                const float l = d * Ah;
+                const float l = doc_start(a, t0 + tid) ? -INFINITY : d * Ah;
                 const float nxt = __shfl_down_sync(0xffffffffu, l, 1);
                 const float sfx = warp_suffix(tid < 31 ? nxt : 0.f);   // s_t: the log-decays after t
                 es[tid] = expf(sfx) * d;          // the weight of token t's input in the chunk's end state
@@ -230,7 +245,7 @@ __global__ void __launch_bounds__(kBwdThreads) ssd_bwd_chunk(BwdArgs a) {
             if (tid < Qb) {
                 const float d = (t0 + tid < Lseq) ? a.dt[(size_t)(b * Lseq + t0 + tid) * H + h] : 0.f;
                 dts[tid] = d;
-                ell[tid] = d * Ah;
+                ell[tid] = doc_start(a, t0 + tid) ? -INFINITY : d * Ah;
             }
             __syncthreads();
             if (tid < Qb) {
@@ -329,7 +344,7 @@ __global__ void __launch_bounds__(kBwdThreads) ssd_bwd_chunk(BwdArgs a) {
         if (tid < Qb) {
             const float d = (t0 + tid < Lseq) ? a.dt[(size_t)(b * Lseq + t0 + tid) * H + h] : 0.f;
             dts[tid] = d;
-            ell[tid] = d * Ah;
+            ell[tid] = doc_start(a, t0 + tid) ? -INFINITY : d * Ah;
         }
         const float K = block_sum(kdot, red);   // (contains a barrier: the tiles are visible)
         if constexpr (kT) {

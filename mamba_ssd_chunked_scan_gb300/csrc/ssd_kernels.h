@@ -74,6 +74,8 @@ struct BwdArgs {
     const float* init;
     const void* dy;
     const float* dfin;
+    const int32_t* cu;     // packed documents (batch 1), or NULL
+    int ndocs;
     void* dx;
     float* ddt;
     float* dA;

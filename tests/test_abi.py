@@ -156,21 +156,23 @@ def test_bwd_workspace_size(L):
     n = L.lib.ssd_bwd_workspace_size(ctypes.byref(p))
     # status header + chunk-entry states (32-token chunks) + dB, dC shares + dA, dD shares
     assert n >= 256 + 2 * 4 * 32 * 64 * 128 * 4 + 2 * 2 * 1000 * 4 * 128 * 4 + 2 * 8 * 4
-    assert L.lib.ssd_bwd_workspace_size(ctypes.byref(params(L, ndocs=3, batch=1))) == 0   # packed documents
+    assert L.lib.ssd_bwd_workspace_size(ctypes.byref(params(L, ndocs=3, batch=1))) > 0    # packed documents
     assert L.lib.ssd_bwd_workspace_size(ctypes.byref(params(L, headdim=128, dstate=128))) == 0   # P * N > 8192
 
 
-@pytest.mark.parametrize("case,code", [("docs", 2), ("null_dx", 1), ("alias", 1), ("misaligned", 1),
-                                       ("no_ws", 3)])
+@pytest.mark.parametrize("case,code", [("docs_dinit", 2), ("docs_no_cu", 1), ("null_dx", 1), ("alias", 1),
+                                       ("misaligned", 1), ("no_ws", 3)])
 def test_bwd_invalid_args(L, case, code):
     base = 1 << 40
     ptr = {k: base + (i << 30) for i, k in enumerate(
         ("x", "dt", "A", "B", "C", "D", "dy", "dx", "ddt", "dA", "dB", "dC", "ws"))}
     p = params(L, batch=2, seqlen=256, nheads=4)
-    cu = None
-    if case == "docs":
+    cu, dinit = None, None
+    if case == "docs_dinit":     # packed documents take no initial-state gradient
         p = params(L, batch=1, seqlen=256, nheads=4, ndocs=2)
-        cu = base + (40 << 30)
+        cu, dinit = base + (40 << 30), base + (41 << 30)
+    if case == "docs_no_cu":     # ndocs without cu_seqlens
+        p = params(L, batch=1, seqlen=256, nheads=4, ndocs=2)
     if case == "null_dx":
         ptr["dx"] = None
     if case == "alias":
@@ -184,7 +186,7 @@ def test_bwd_invalid_args(L, case, code):
     v = lambda k: None if ptr[k] is None else vp(ptr[k])
     rc = L.lib.ssd_bwd(ctypes.byref(p), v("x"), v("dt"), v("A"), v("B"), v("C"), v("D"), None,
                        None if cu is None else vp(cu), v("dy"), None, v("dx"), v("ddt"), v("dA"), v("dB"),
-                       v("dC"), None, None, v("ws"), nbytes, None)
+                       v("dC"), None, None if dinit is None else vp(dinit), v("ws"), nbytes, None)
     assert rc == code
 
 

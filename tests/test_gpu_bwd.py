@@ -38,7 +38,7 @@ def run_bwd(p, dy, dfin):
     else:
         dyt = torch.from_numpy(dy).cuda()
     dft = None if dfin is None else torch.from_numpy(dfin).cuda()
-    g = ssd.ssd_bwd(d["x"], d["dt"], d["A"], d["B"], d["C"], dyt, d["D"], d["init"], dft)
+    g = ssd.ssd_bwd(d["x"], d["dt"], d["A"], d["B"], d["C"], dyt, d["D"], d["init"], dft, d["cu"])
     torch.cuda.synchronize()
     return {k: (None if v is None else v.float().cpu().numpy().astype(np.float64)) for k, v in g.items()}
 
@@ -49,8 +49,8 @@ def check(p, seed=1, with_dfin=True):
     got = run_bwd(p, dy, dfin)
     tol = BWD_TOL[p.dtype]
     for k in ("dx", "ddt", "dA", "dB", "dC", "dD", "dinit"):
-        if want[k] is None:
-            assert got[k] is None
+        if want[k] is None or got[k] is None:
+            assert got[k] is None and (want[k] is None or p.cu_seqlens is not None), k
             continue
         assert np.isfinite(got[k]).all(), k
         e = rel_err(got[k], want[k])
@@ -99,3 +99,15 @@ def test_bwd_long_sequence():
     p = synth.make_problem(batch=1, seqlen=2048, nheads=4, headdim=64, dstate=128, ngroups=1, chunk=128,
                            dtype="bf16", seed=309, init_std=0.1)
     check(p)
+
+
+@pytest.mark.parametrize("lens,kw", [
+    ([3, 300, 128, 1, 257, 90, 500], dict(headdim=64, dstate=128, dtype="bf16")),    # tiled instance
+    ([32, 1, 31, 64, 33, 2], dict(headdim=64, dstate=128, dtype="f32")),             # ends on chunk edges
+    ([10, 1, 50, 39], dict(headdim=16, dstate=32, dtype="f32")),                    # generic instance
+])
+def test_bwd_packed_documents(lens, kw):
+    """Packed documents from zero states: no gradient crosses a boundary."""
+    p = synth.make_problem(batch=1, seqlen=sum(lens), nheads=4, ngroups=2, chunk=128, seed=311,
+                           doc_lengths=lens, dt_dist="softplus_n22", **kw)
+    check(p, with_dfin=False)
