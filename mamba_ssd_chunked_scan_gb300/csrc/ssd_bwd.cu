@@ -468,56 +468,70 @@ __global__ void __launch_bounds__(kBwdThreads) ssd_bwd_chunk(BwdArgs a) {
                     }
                 }
             }
-            // this head's shares of dB and dC: thread = (n, four rows j0 .. j0 + 3)
+            // this head's shares of dB (threads 0-511) and dC (threads 512-1023):
+            // thread = (n, eight rows j0 .. j0 + 7)
             {
-                const int n = tid & 127, j0 = (tid >> 7) * 4;
-                float lx[4] = {0.f, 0.f, 0.f, 0.f}, sd[4] = {0.f, 0.f, 0.f, 0.f};
+                const int half = tid >> 9, tt = tid & 511;
+                const int n = tt & 127, j0 = (tt >> 7) * 8;
+                const float* M = half ? Sin : Lam;
+                const float* V = half ? dyT : xT;
+                float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
 #pragma unroll 4
                 for (int p = 0; p < 64; ++p) {
-                    const float lam = Lam[p * L.sb + n], sin = Sin[p * L.sb + n];
-                    const float4 xx = *reinterpret_cast<const float4*>(xT + p * L.st + j0);
-                    const float4 dd = *reinterpret_cast<const float4*>(dyT + p * L.st + j0);
-                    lx[0] = fmaf(lam, xx.x, lx[0]);
-                    lx[1] = fmaf(lam, xx.y, lx[1]);
-                    lx[2] = fmaf(lam, xx.z, lx[2]);
-                    lx[3] = fmaf(lam, xx.w, lx[3]);
-                    sd[0] = fmaf(sin, dd.x, sd[0]);
-                    sd[1] = fmaf(sin, dd.y, sd[1]);
-                    sd[2] = fmaf(sin, dd.z, sd[2]);
-                    sd[3] = fmaf(sin, dd.w, sd[3]);
+                    const float m = M[p * L.sb + n];
+                    const float4 v0 = *reinterpret_cast<const float4*>(V + p * L.st + j0);
+                    const float4 v1 = *reinterpret_cast<const float4*>(V + p * L.st + j0 + 4);
+                    acc[0] = fmaf(m, v0.x, acc[0]);
+                    acc[1] = fmaf(m, v0.y, acc[1]);
+                    acc[2] = fmaf(m, v0.z, acc[2]);
+                    acc[3] = fmaf(m, v0.w, acc[3]);
+                    acc[4] = fmaf(m, v1.x, acc[4]);
+                    acc[5] = fmaf(m, v1.y, acc[5]);
+                    acc[6] = fmaf(m, v1.z, acc[6]);
+                    acc[7] = fmaf(m, v1.w, acc[7]);
                 }
-                float db[4], dc[4];
+                float r[8];
+                if (half == 0) {   // dB_j = dt_j (e^{s_j} Lam^T x_j + sum_{i>=j} L_ij X_ij C_i)
 #pragma unroll
-                for (int u = 0; u < 4; ++u) {
-                    db[u] = es[j0 + u] * lx[u];
-                    dc[u] = ep[j0 + u] * sd[u];
-                }
+                    for (int u = 0; u < 8; ++u) r[u] = es[j0 + u] * acc[u];
 #pragma unroll 4
-                for (int i = j0; i < 32; ++i) {   // A2[i][j] = 0 where j > i
-                    const float4 aa = *reinterpret_cast<const float4*>(A2 + i * 32 + j0);
-                    const float cv = Cs[i * 128 + n];
-                    db[0] = fmaf(aa.x, cv, db[0]);
-                    db[1] = fmaf(aa.y, cv, db[1]);
-                    db[2] = fmaf(aa.z, cv, db[2]);
-                    db[3] = fmaf(aa.w, cv, db[3]);
-                }
-#pragma unroll 4
-                for (int k = 0; k < j0 + 4; ++k) {   // A2[j][k] = 0 where k > j
-                    const float4 aa = *reinterpret_cast<const float4*>(A2dtT + k * L.st + j0);
-                    const float bv = Bs[k * L.sb + n];
-                    dc[0] = fmaf(aa.x, bv, dc[0]);
-                    dc[1] = fmaf(aa.y, bv, dc[1]);
-                    dc[2] = fmaf(aa.z, bv, dc[2]);
-                    dc[3] = fmaf(aa.w, bv, dc[3]);
-                }
-#pragma unroll
-                for (int u = 0; u < 4; ++u) {
-                    const int j = j0 + u;
-                    if (t0 + j < Lseq) {
-                        const size_t o = ((size_t)(b * Lseq + t0 + j) * H + h) * 128 + n;
-                        a.ws_dB[o] = dts[j] * db[u];
-                        a.ws_dC[o] = dc[u];
+                    for (int i = j0; i < 32; ++i) {   // A2[i][j] = 0 where j > i
+                        const float4 a0 = *reinterpret_cast<const float4*>(A2 + i * 32 + j0);
+                        const float4 a1 = *reinterpret_cast<const float4*>(A2 + i * 32 + j0 + 4);
+                        const float cv = Cs[i * 128 + n];
+                        r[0] = fmaf(a0.x, cv, r[0]);
+                        r[1] = fmaf(a0.y, cv, r[1]);
+                        r[2] = fmaf(a0.z, cv, r[2]);
+                        r[3] = fmaf(a0.w, cv, r[3]);
+                        r[4] = fmaf(a1.x, cv, r[4]);
+                        r[5] = fmaf(a1.y, cv, r[5]);
+                        r[6] = fmaf(a1.z, cv, r[6]);
+                        r[7] = fmaf(a1.w, cv, r[7]);
                     }
+                } else {           // dC_j = e^{p_j} S_in^T dy_j + sum_{k<=j} L_jk dt_k X_jk B_k
+#pragma unroll
+                    for (int u = 0; u < 8; ++u) r[u] = ep[j0 + u] * acc[u];
+#pragma unroll 4
+                    for (int k = 0; k < j0 + 8; ++k) {   // A2[j][k] = 0 where k > j
+                        const float4 a0 = *reinterpret_cast<const float4*>(A2dtT + k * L.st + j0);
+                        const float4 a1 = *reinterpret_cast<const float4*>(A2dtT + k * L.st + j0 + 4);
+                        const float bv = Bs[k * L.sb + n];
+                        r[0] = fmaf(a0.x, bv, r[0]);
+                        r[1] = fmaf(a0.y, bv, r[1]);
+                        r[2] = fmaf(a0.z, bv, r[2]);
+                        r[3] = fmaf(a0.w, bv, r[3]);
+                        r[4] = fmaf(a1.x, bv, r[4]);
+                        r[5] = fmaf(a1.y, bv, r[5]);
+                        r[6] = fmaf(a1.z, bv, r[6]);
+                        r[7] = fmaf(a1.w, bv, r[7]);
+                    }
+                }
+                float* out = half ? a.ws_dC : a.ws_dB;
+#pragma unroll
+                for (int u = 0; u < 8; ++u) {
+                    const int j = j0 + u;
+                    if (t0 + j < Lseq)
+                        out[((size_t)(b * Lseq + t0 + j) * H + h) * 128 + n] = half ? r[u] : dts[j] * r[u];
                 }
             }
         } else {
