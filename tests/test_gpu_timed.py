@@ -1,0 +1,30 @@
+"""ssd_fwd_timed: the same results as ssd_fwd, bit for bit, with one positive
+duration per kernel launch of the plan."""
+import numpy as np
+import pytest
+import torch
+
+import mamba_ssd_chunked_scan_gb300 as ssd
+from mamba_ssd_chunked_scan_gb300 import synth
+
+from gpu_helpers import to_device
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.mark.parametrize("batch,seqlen,split_len", [(2, 300, 0), (1, 1000, 256), (3, 512, 1 << 16)])
+def test_timed_matches_plain(batch, seqlen, split_len):
+    p = synth.make_problem(batch=batch, seqlen=seqlen, nheads=8, headdim=64, dstate=128, ngroups=2, chunk=128,
+                           dtype="bf16", seed=401, init_std=0.1)
+    d = to_device(p)
+    f = ssd.SSDForward(p.batch, p.seqlen, p.nheads, p.headdim, p.dstate, p.ngroups, 128, split_len, 0,
+                       torch.bfloat16)
+    fin1 = torch.empty((p.batch, p.nheads, p.headdim, p.dstate), dtype=torch.float32, device="cuda")
+    fin2 = torch.empty_like(fin1)
+    y1 = f(d["x"], d["dt"], d["A"], d["B"], d["C"], d["D"], d["init"], None, final_states=fin1)
+    y2 = torch.empty_like(y1)
+    ms = f.launch_times(d["x"], d["dt"], d["A"], d["B"], d["C"], d["D"], d["init"], None, y=y2, final_states=fin2)
+    assert f.check_status() == 0
+    _, launches, _ = f.plan(True, True)
+    assert len(ms) == launches and all(t > 0 for t in ms)
+    assert torch.equal(y1, y2) and torch.equal(fin1, fin2)
