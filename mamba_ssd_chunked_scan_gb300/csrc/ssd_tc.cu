@@ -45,7 +45,6 @@ namespace {
 
 constexpr int Q = 128, P = 64, N = 128;
 constexpr int NMETA = 3;                     // per-chunk value buffers between the math groups
-constexpr int kPrefetch = 4;                 // chunks of L2 prefetch beyond the shared-memory stages
 constexpr int kPersistChunks = 4;            // units of at most this many chunks run on a persistent grid
 constexpr int kThreads = 512;
 // setmaxnreg budgets: issue warpgroup (unit bookkeeping of the producer, MMA
@@ -385,8 +384,10 @@ __global__ void __launch_bounds__(kThreads, 1) ssd_chunk_tc(const __grid_constan
         if (warp == 0 && lane == 0) {
             // ============================================================ TMA producer
             int issued = 0;
-            // L2 prefetch runs kPrefetch items ahead of the two-stage shared-memory ring,
-            // so a stage refill finds its tiles in L2 instead of waiting on HBM
+            // L2 prefetch of the item two ahead of the one being loaded (the tiles of this
+            // stage's next refill), so a refill finds them in L2 instead of waiting on
+            // HBM.  Longer distances (4 and 8 items) measured slower: the prefetched
+            // tiles of all CTAs then compete in L2 with tiles still in use.
             auto prefetch = [&](const Cursor& k) {
                 if (!k.valid(nunits)) return;
                 const int t = k.t(), hh = k.un.h, gg = k.un.g, bb = k.un.b;
@@ -402,11 +403,6 @@ __global__ void __launch_bounds__(kThreads, 1) ssd_chunk_tc(const __grid_constan
             cl.init(a);
             cp.init(a);
             cp.next2(a, nunits);
-#pragma unroll 1
-            for (int k = 0; k < kPrefetch; ++k) {
-                prefetch(cp);
-                cp.next(a, nunits);
-            }
             for (int c = 0; c < nch; ++c, cl.next(a, nunits)) {
                 const int st = c & 1;
                 prefetch(cp);
