@@ -386,7 +386,7 @@ __global__ void __launch_bounds__(kThreads, 1) ssd_chunk_tc(const __grid_constan
             int issued = 0;
             // L2 prefetch of the item two ahead of the one being loaded (the tiles of this
             // stage's next refill), so a refill finds them in L2 instead of waiting on
-            // HBM.  Longer distances (4 and 8 items) measured slower: the prefetched
+            // HBM.  Longer distances (4, 6 and 10 items) measured slower: the prefetched
             // tiles of all CTAs then compete in L2 with tiles still in use.
             auto prefetch = [&](const Cursor& k) {
                 if (!k.valid(nunits)) return;
