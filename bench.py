@@ -2,7 +2,7 @@
 """Benchmark of the SSD forward pass (one JSON line on rank 0).
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
-                    [--workload 27b|sweep:B:L:S|long|varlen|tiny|decode[:B]|bwd[:B]]
+                    [--workload 27b|sweep:B:L:S|long|varlen|tiny|decode[:B]|bwd[:B]|gatenorm]
 
 A step is one ssd_fwd call over one batch of the workload (default: the
 Mamba-2 2.7B-like layer, batch 8 x 2048 tokens, 80 heads, P 64, N 128, bf16).
@@ -17,7 +17,7 @@ bounded sample of the same workload (one batch row per step).
 --workload decode[:B] times the single-token decode step (ssd_step) of the
 same layer shape over a batch of B rows (default 256) from a resident state;
 --workload bwd[:B] times the backward pass (ssd_bwd) of the 2.7B-like layer
-(batch B, default 8).
+(batch B, default 8); --workload gatenorm the gated RMS norm of its output.
 """
 from __future__ import annotations
 
@@ -43,6 +43,7 @@ FALLBACK_HBM_GBS = 6800.0
 
 
 DECODE_METRIC = "SSD decode step tokens/s and achieved HBM GB/s on the resident state, 1 GPU"
+GATE_NORM_METRIC = "gated RMS norm of the scan output, tokens/s and achieved HBM GB/s, 1 GPU"
 BWD_METRIC = "SSD bwd tokens/s and achieved fp32 TFLOP/s (% of the CUDA-core fp32 peak), 1 GPU"
 # fp32 CUDA-core peak: 152 SMs x 128 fp32 lanes x 2 flop (FMA) x 2.07 GHz (maximum SM clock)
 FP32_PEAK_TFLOPS = 152 * 128 * 2 * 2.07e9 / 1e12
@@ -65,7 +66,7 @@ def workload(name: str):
     if name.startswith("bwd"):
         parts = name.split(":")
         return synth.config_27b(batch=int(parts[1]) if len(parts) > 1 else 8)
-    if name == "27b":
+    if name in ("27b", "gatenorm"):
         return synth.config_27b()
     if name == "tiny":
         return synth.config_tiny_f32()
@@ -263,6 +264,31 @@ def run_reference(args):
     if rank != 0:
         return
     p = workload(args.workload)
+    if args.workload == "gatenorm":
+        rows, width = 1024, p.nheads * p.headdim
+        rng = np.random.default_rng(13)
+        y = synth.bf16_to_f32(synth.bf16_bits(rng.standard_normal((rows, width)).astype(np.float32)))
+        z = synth.bf16_to_f32(synth.bf16_bits(rng.standard_normal((rows, width)).astype(np.float32)))
+        w = rng.uniform(0.5, 1.5, width)
+        for _ in range(args.warmup):
+            oracle.gate_norm(y, z, w, width, 1e-5)
+        times = []
+        for _ in range(args.steps):
+            t0 = time.perf_counter()
+            oracle.gate_norm(y, z, w, width, 1e-5)
+            times.append(time.perf_counter() - t0)
+        ms = 1e3 * sum(times) / len(times)
+        value = rows / (ms / 1e3)
+        print(json.dumps({
+            "impl": "reference", "metric": GATE_NORM_METRIC, "value": value, "unit": "tokens/s", "n_gpus": world,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": {"workload": f"gate_norm_width{width}", "sample": f"{rows} rows per step"},
+            "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": 1, "kind": "oracle",
+                             "sample": f"fp64 numpy gate and norm of {rows} rows of {width} channels"},
+            "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}),
+            flush=True)
+        return
     if args.workload.startswith("bwd"):
         dy_h = np.random.default_rng(11).standard_normal((p.batch, p.seqlen, p.nheads, p.headdim)).astype(np.float32)
         q, dyq = bwd_sample(p, dy_h)
@@ -460,6 +486,71 @@ def run_decode(args, p, dev, rank, local_rank, world):
         dist.destroy_process_group()
 
 
+def run_gate_norm(args, p, dev, rank, local_rank, world):
+    """Gate/norm workload: a step is one ssd_gate_norm over the 2.7B-like layer's
+    scan output (batch x L tokens, 5120 channels normalised as one group)."""
+    import torch
+    import mamba_ssd_chunked_scan_gb300 as ssd
+
+    rows, width = p.batch * p.seqlen, p.nheads * p.headdim
+    rng = np.random.default_rng(13)
+
+    def io(a):
+        return torch.from_numpy(synth.bf16_bits(a).view(np.int16).copy()).to(dev).view(torch.bfloat16)
+
+    y = io(rng.standard_normal((rows, width)).astype(np.float32))
+    z = io(rng.standard_normal((rows, width)).astype(np.float32))
+    w = torch.from_numpy(rng.uniform(0.5, 1.5, width).astype(np.float32)).to(dev)
+    out = torch.empty_like(y)
+    flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
+    stream = torch.cuda.current_stream()
+    for _ in range(args.warmup):
+        flush.zero_()
+        ssd.gate_norm(y, z, w, width, out=out, stream=stream)
+    torch.cuda.synchronize()
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
+    with ClockSampler(local_rank) as clk:
+        for i in range(args.steps):
+            flush.zero_()
+            ev[i][0].record(stream)
+            ssd.gate_norm(y, z, w, width, out=out, stream=stream)
+            ev[i][1].record(stream)
+        torch.cuda.synchronize()
+    ms = sum(a.elapsed_time(b) for a, b in ev) / args.steps
+    # end to end: y and z from pinned host memory, out back to it
+    hy, hz = y.cpu().pin_memory(), z.cpu().pin_memory()
+    ho = torch.empty(out.shape, dtype=out.dtype).pin_memory()
+    dy_, dz_ = torch.empty_like(y), torch.empty_like(z)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(args.steps):
+        dy_.copy_(hy, non_blocking=True)
+        dz_.copy_(hz, non_blocking=True)
+        ssd.gate_norm(dy_, dz_, w, width, out=out, stream=stream)
+        ho.copy_(out, non_blocking=True)
+    e1.record(stream)
+    torch.cuda.synchronize()
+    e2e_ms = e0.elapsed_time(e1) / args.steps
+    ms_max, e2e_max = slowest_rank([ms, e2e_ms], dev)
+    if rank == 0:
+        nbytes = 3 * rows * width * 2 + width * 4
+        peak, peak_kind = peaks()
+        achieved = nbytes / (ms / 1e3) / 1e9
+        print(json.dumps({
+            "metric": GATE_NORM_METRIC, "value": job_rate(rows, world, ms_max), "unit": "tokens/s", "n_gpus": world,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_max, "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "f32", "data": "synthetic",
+            "config": {"workload": f"gate_norm_rows{rows}_width{width}_group{width}", "storage": "bf16",
+                       "kernel": "ssd_gate_norm_kernel", "l2": "256 MiB write before every timed step",
+                       "bytes_per_step": nbytes},
+            "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s", "frac": achieved / peak,
+                         "peak_source": peak_kind, "traffic": None,
+                         "scope": "y and z read, out written, weight read: one ssd_gate_norm launch"},
+            "e2e": {"value": job_rate(rows, world, e2e_max), "unit": "tokens/s",
+                    "h2d_bytes_per_step": 2 * rows * width * 2, "d2h_bytes_per_step": rows * width * 2},
+            "gpu_launches": args.steps, "clocks": clk.summary()}), flush=True)
+
+
 def run_bwd(args, p, dev, rank, local_rank, world):
     """Backward workload: a step is one ssd_bwd call over the 2.7B-like layer
     (the forward's inputs, random dy and dfinal_states)."""
@@ -592,6 +683,8 @@ def run_ours(args):
         return run_decode(args, p, dev, rank, local_rank, world)
     if args.workload.startswith("bwd"):
         return run_bwd(args, p, dev, rank, local_rank, world)
+    if args.workload == "gatenorm":
+        return run_gate_norm(args, p, dev, rank, local_rank, world)
     dtype = torch.bfloat16 if p.dtype == "bf16" else torch.float32
 
     def dev_io(name):

@@ -189,6 +189,24 @@ SSD_API int ssd_bwd(const ssd_params_t* p,
             float* dinitial_states,
             void* workspace, size_t workspace_bytes, void* stream);
 
+/* Gated RMS normalisation of the scan's output in one pass ("NVIDIA Accelerates
+ * Mamba-2 Forward Kernel with CUDA Tile", operator fusion: the scan is followed
+ * by gating and normalisation, fused so the gated values never leave the chip).
+ * For each row r and each group of group_size consecutive channels:
+ *
+ *     g[r,k]   = y[r,k] * silu(z[r,k]),   silu(v) = v / (1 + exp(-v))
+ *     out[r,k] = g[r,k] / sqrt(mean_{k' in group} g[r,k']^2 + eps) * weight[k]
+ *
+ * (the Mamba-2 block's output gate and its grouped RMS norm, gate applied before
+ * the norm).  Layouts: y, z, out (rows, width) dtype, row-major, contiguous,
+ * 16-byte aligned; weight (width) fp32.  rows = batch * seqlen and width =
+ * nheads * headdim for ssd_fwd's y.  width must be a multiple of group_size;
+ * group_size a multiple of 8 (bf16) or 4 (fp32) and at most 8192 (else
+ * SSD_ERR_UNSUPPORTED); eps >= 0 and finite.  out may be y itself (in place).
+ * One launch on `stream`, no workspace; bitwise deterministic. */
+SSD_API int ssd_gate_norm(int64_t rows, int32_t width, int32_t group_size, int32_t dtype,
+             const void* y, const void* z, const float* weight, float eps, void* out, void* stream);
+
 /* One autoregressive (decode) step: a single new token per batch row from a
  * resident state.  "State Space Duality and Mamba-2", section "Performance and
  * Serving Economics": generation keeps a fixed-size recurrent state and costs

@@ -33,7 +33,7 @@ def __getattr__(name):
         return _lib.SSDError
     raise AttributeError(name)
 
-__all__ = ["ssd_fwd", "SSDForward", "ssd_bwd", "ssd_step", "segsum_dump", "check_status", "SSDError", "plan"]
+__all__ = ["ssd_fwd", "SSDForward", "ssd_bwd", "ssd_step", "gate_norm", "segsum_dump", "check_status", "SSDError", "plan"]
 
 
 def _ptr(t: Optional[torch.Tensor]):
@@ -189,6 +189,24 @@ def ssd_bwd(x, dt, A, B, C, dy, D=None, initial_states=None, dfinal_states=None,
                           _ptr(g["dinit"]), _ptr(ws), nbytes, _stream_handle(stream))
     _lib.check(rc, "ssd_bwd")
     return g
+
+
+def gate_norm(y, z, weight, group_size, eps=1e-5, *, out=None, stream=None):
+    """out = rmsnorm_groups(y * silu(z)) * weight over the last dimension, in one
+    pass (groups of `group_size` channels).  y, z: (..., width) bf16 or fp32,
+    contiguous; weight: (width,) fp32.  `out` may be y (in place)."""
+    width = y.shape[-1]
+    rows = y.numel() // width if width else 0
+    if tuple(z.shape) != tuple(y.shape) or z.dtype != y.dtype or not (y.is_contiguous() and z.is_contiguous()):
+        raise ValueError("z: expected the shape, dtype and layout of y")
+    if weight.dtype != torch.float32 or tuple(weight.shape) != (width,) or weight.device != y.device:
+        raise ValueError("weight: expected fp32 (width,) on y's device")
+    if out is None:
+        out = torch.empty_like(y)
+    rc = _lib.lib.ssd_gate_norm(rows, width, int(group_size), _dtype_code(y), _ptr(y), _ptr(z), _ptr(weight),
+                                float(eps), _ptr(out), _stream_handle(stream))
+    _lib.check(rc, "ssd_gate_norm")
+    return out
 
 
 def ssd_step(state, x, dt, A, B, C, D=None, *, state_out=None, y=None, stream=None):

@@ -19,7 +19,8 @@ STATUS = {0: "SSD_OK", 1: "SSD_ERR_INVALID_ARG", 2: "SSD_ERR_UNSUPPORTED", 3: "S
 # every symbol include/ssd.h declares
 EXPORTS = ("ssd_fwd_workspace_size", "ssd_workspace_init", "ssd_fwd", "ssd_check_status",
            "ssd_status_string", "ssd_fwd_plan", "ssd_segsum_dump", "ssd_fwd_static_scratch", "ssd_step",
-           "ssd_bwd_workspace_size", "ssd_bwd", "ssd_fwd_timed")
+           "ssd_bwd_workspace_size", "ssd_bwd", "ssd_fwd_timed",
+           "ssd_gate_norm")
 
 
 class SSDParams(ctypes.Structure):
@@ -63,6 +64,8 @@ def _load():
     lib.ssd_bwd_workspace_size.restype = sz
     lib.ssd_bwd.argtypes = [P] + [vp] * 18 + [sz, vp]
     lib.ssd_bwd.restype = ctypes.c_int
+    lib.ssd_gate_norm.argtypes = [i64, i32, i32, i32, vp, vp, vp, ctypes.c_float, vp, vp]
+    lib.ssd_gate_norm.restype = ctypes.c_int
     lib.ssd_step.argtypes = [i64, i32, i32, i32, i32, i32, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp]
     lib.ssd_step.restype = ctypes.c_int
     lib.ssd_segsum_dump.argtypes = [vp, i64, i32, vp, vp, vp]

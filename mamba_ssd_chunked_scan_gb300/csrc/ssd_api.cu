@@ -455,6 +455,23 @@ int ssd_bwd(const ssd_params_t* p, const void* x, const float* dt, const float* 
     return SSD_OK;
 }
 
+int ssd_gate_norm(int64_t rows, int32_t width, int32_t group_size, int32_t dtype, const void* y,
+                  const void* z, const float* weight, float eps, void* out, void* stream) {
+    if (rows < 1 || width < 1 || group_size < 1 || width % group_size != 0) return SSD_ERR_INVALID_ARG;
+    if (dtype != SSD_F32 && dtype != SSD_BF16) return SSD_ERR_INVALID_ARG;
+    if (!(eps >= 0.f) || eps > 3.0e38f) return SSD_ERR_INVALID_ARG;   // rejects NaN and inf
+    const int vec = dtype == SSD_BF16 ? 8 : 4;                          // elements per 16-byte vector
+    if (group_size % vec != 0 || group_size > 8192) return SSD_ERR_UNSUPPORTED;
+    if (rows * (width / group_size) >= ((int64_t)1 << 31)) return SSD_ERR_UNSUPPORTED;
+    if (!y || !z || !weight || !out) return SSD_ERR_INVALID_ARG;
+    if (!aligned(y, 16) || !aligned(z, 16) || !aligned(out, 16) || !aligned(weight, 4)) return SSD_ERR_INVALID_ARG;
+    GateNormArgs a;
+    a.rows = rows; a.width = width; a.group_size = group_size; a.dtype = dtype; a.eps = eps;
+    a.y = y; a.z = z; a.weight = weight; a.out = out;
+    if (launch_gate_norm(a, (cudaStream_t)stream) != cudaSuccess) return SSD_ERR_CUDA;
+    return SSD_OK;
+}
+
 int ssd_step(int64_t batch, int32_t nheads, int32_t headdim, int32_t dstate, int32_t ngroups, int32_t dtype,
              const float* state_in, float* state_out, const void* x, const float* dt, const float* A,
              const void* B, const void* C, const float* D, void* y, void* stream) {

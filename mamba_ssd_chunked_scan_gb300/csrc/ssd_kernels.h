@@ -90,6 +90,18 @@ struct BwdArgs {
     float* ws_dD;          // [batch * H]
 };
 
+// Gated RMS normalisation (ssd_gate_norm): everything its launch needs.
+struct GateNormArgs {
+    int64_t rows;
+    int width, group_size;
+    int dtype;             // ssd_dtype_t of y, z and out
+    float eps;
+    const void* y;
+    const void* z;
+    const float* weight;
+    void* out;
+};
+
 // Constants of division by an invariant divisor d >= 1 through one high
 // multiply and a shift (Granlund and Montgomery, "Division by Invariant
 // Integers using Multiplication", 1994): l = ceil(log2 d),
@@ -108,6 +120,7 @@ cudaError_t launch_split_scan(const FwdArgs& a, cudaStream_t st);
 size_t tc_smem_bytes();
 bool tc_supported(int P, int N, int Q, int dtype);
 cudaError_t launch_tc(const FwdArgs& a, cudaStream_t st);
+cudaError_t launch_gate_norm(const GateNormArgs& a, cudaStream_t st);
 size_t bwd_smem_bytes(int Qb, int P, int N);
 int bwd_chunk(int P, int N, size_t smem_limit);
 cudaError_t launch_bwd(const BwdArgs& a, cudaStream_t st);

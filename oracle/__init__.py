@@ -160,6 +160,22 @@ def ssd_backward(p, dy, dfinal=None, nthreads: int = 0):
     return out
 
 
+def gate_norm(y, z, weight, group_size, eps):
+    """Gated RMS normalisation, fp64 numpy: g = y * silu(z), then over each group
+    of `group_size` consecutive channels out = g / sqrt(mean(g^2) + eps) * weight
+    (the gating and normalisation that follow the scan in the Mamba-2 forward
+    pass, "NVIDIA Accelerates Mamba-2 Forward Kernel with CUDA Tile", operator
+    fusion; the gate is applied before the norm).  y, z: (rows, width)."""
+    y = np.asarray(y, dtype=np.float64)
+    z = np.asarray(z, dtype=np.float64)
+    w = np.asarray(weight, dtype=np.float64)
+    rows, width = y.shape
+    g = y * (z / (1.0 + np.exp(-z)))
+    gg = g.reshape(rows, width // group_size, group_size)
+    ms = np.mean(gg * gg, axis=2, keepdims=True)
+    return (gg / np.sqrt(ms + eps)).reshape(rows, width) * w
+
+
 def ssd_quadratic(p):
     """(C B^T) o L form plus the initial-state term, fp64, O(L^2)."""
     _check(p)

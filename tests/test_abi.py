@@ -199,3 +199,19 @@ def test_fwd_timed_rejects_missing_outputs(L):
     assert L.lib.ssd_fwd_timed(*args, None, 4, ctypes.byref(n)) == 1
     assert L.lib.ssd_fwd_timed(*args, ms, 0, ctypes.byref(n)) == 1
     assert L.lib.ssd_fwd_timed(*args, ms, 4, None) == 1
+
+
+@pytest.mark.parametrize("kw,code", [
+    (dict(rows=0), 1), (dict(width=50), 1), (dict(dtype=3), 1), (dict(eps=-1.0), 1), (dict(eps=float("nan")), 1),
+    (dict(group_size=12, width=48), 2), (dict(group_size=16384, width=16384), 2), (dict(y=None), 1),
+    (dict(out=(1 << 40) + 8), 1),
+])
+def test_gate_norm_invalid_args(L, kw, code):
+    d = dict(rows=4, width=64, group_size=16, dtype=1, y=1 << 40, z=(1 << 40) + (1 << 30),
+             weight=(1 << 40) + (2 << 30), eps=1e-5, out=(1 << 40) + (3 << 30))
+    d.update(kw)
+    vp = ctypes.c_void_p
+    ptr = lambda k: None if d[k] is None else vp(d[k])
+    rc = L.lib.ssd_gate_norm(d["rows"], d["width"], d["group_size"], d["dtype"], ptr("y"), ptr("z"), ptr("weight"),
+                             d["eps"], ptr("out"), None)
+    assert rc == code
