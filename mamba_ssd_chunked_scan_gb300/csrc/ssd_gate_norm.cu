@@ -19,6 +19,7 @@ namespace ssd {
 namespace {
 
 constexpr int kNormThreads = 256;
+constexpr int kNormVecs = 4;   // 16-byte vectors per thread loaded before any is used
 
 __device__ __forceinline__ float silu_gate(float y, float z) { return y * (z / (1.f + expf(-z))); }
 
@@ -71,16 +72,36 @@ __global__ void __launch_bounds__(kNormThreads) ssd_gate_norm_kernel(GateNormArg
     const T* y = static_cast<const T*>(a.y) + base;
     const T* z = static_cast<const T*>(a.z) + base;
     float ss = 0.f;
-    for (int k = threadIdx.x; k < nvec; k += kNormThreads) {
+    auto gate = [&](int k, const uint4& yr, const uint4& zr) {
         float yv[V], zv[V];
-        Vec<T>::load(y + k * V, yv);
-        Vec<T>::load(z + k * V, zv);
+        Vec<T>::load(reinterpret_cast<const T*>(&yr), yv);
+        Vec<T>::load(reinterpret_cast<const T*>(&zr), zv);
 #pragma unroll
         for (int e = 0; e < V; ++e) {
             const float gv = silu_gate(yv[e], zv[e]);
             g[k * V + e] = gv;
             ss = fmaf(gv, gv, ss);
         }
+    };
+    if (nvec <= kNormVecs * kNormThreads) {
+        // all of this thread's vectors in flight at once: one HBM round trip
+        uint4 yr[kNormVecs], zr[kNormVecs];
+#pragma unroll
+        for (int r = 0; r < kNormVecs; ++r) {
+            const int k = threadIdx.x + r * kNormThreads;
+            if (k < nvec) {
+                yr[r] = *reinterpret_cast<const uint4*>(y + k * V);
+                zr[r] = *reinterpret_cast<const uint4*>(z + k * V);
+            }
+        }
+#pragma unroll
+        for (int r = 0; r < kNormVecs; ++r) {
+            const int k = threadIdx.x + r * kNormThreads;
+            if (k < nvec) gate(k, yr[r], zr[r]);
+        }
+    } else {
+        for (int k = threadIdx.x; k < nvec; k += kNormThreads)
+            gate(k, *reinterpret_cast<const uint4*>(y + k * V), *reinterpret_cast<const uint4*>(z + k * V));
     }
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, o);
