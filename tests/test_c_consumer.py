@@ -36,4 +36,5 @@ def test_c99_program_uses_the_abi(tmp_path):
     subprocess.check_call(["gcc", "-std=c99", "-Wall", "-Werror", "-I", os.path.join(ROOT, "include"), str(c),
                            "-L", PKG, "-lssd", f"-Wl,-rpath,{PKG}", "-o", str(exe)])
     out = subprocess.check_output([str(exe)], text=True).split()
-    assert out == ["SSD_OK", "256", "0", "SSD_ERR_UNSUPPORTED"]
+    # 256 bytes (the status header) without a GPU; with one, the leftover-unit plan's piece states too
+    assert out[0] == "SSD_OK" and int(out[1]) >= 256 and out[2:] == ["0", "SSD_ERR_UNSUPPORTED"]
