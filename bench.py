@@ -144,7 +144,7 @@ def device_copy_gbps(dev, stream, nbytes=1 << 30, reps=5):
     return best
 
 
-def tail_pieces(p, nsm=152):
+def tail_pieces(p, nsm):
     """Pieces with an incoming state under the leftover-unit plan (one split):
     the last U % S units are cut into m pieces, all but the first of each
     continue a sequence."""
@@ -221,8 +221,8 @@ class ClockSampler:
 
 
 # the sources that define each kernel family's device code and launch
-FAMILY_SOURCES = {1: ("ssd_tc.cu", "tc_ptx.cuh", "ssd_common.cuh"),
-                  0: ("ssd_simt.cu", "segsum.cuh", "ssd_common.cuh")}
+FAMILY_SOURCES = {1: ("ssd_tc.cu", "tc_ptx.cuh", "ssd_common.cuh", "segsum.cuh", "ssd_kernels.h"),
+                  0: ("ssd_simt.cu", "segsum.cuh", "ssd_common.cuh", "ssd_kernels.h")}
 
 
 def kernel_sources_sha(family: int) -> str:

@@ -132,11 +132,15 @@ SSD_API int ssd_fwd_timed(const ssd_params_t* p,
  * loading the library reserves until process exit.  Problems whose
  * ssd_fwd_workspace_size() exceeds 8 MiB are rejected with
  * SSD_ERR_WORKSPACE before anything is launched; single-split problems need
- * at most 256 bytes plus 4 MiB (the states of the pieces the leftover-unit
- * plan cuts the last wave's units into).  The caller still passes all inputs and outputs.
+ * less than 4.01 MiB: the 256-byte status header, the pieces' log-decays
+ * (4 bytes each, rounded up to 256 bytes) and their states (at most 4 MiB),
+ * for the pieces the leftover-unit plan cuts the last wave's units into.  The
+ * caller still passes all inputs and outputs.
  * The first call on a device looks up the array's device address with that
- * device current (cudaGetSymbolAddress); make that first call before any
- * stream capture.  Every call uses the same array: calls whose GPU work
+ * device current (cudaGetSymbolAddress) and keeps it for the life of the
+ * process; make that first call before any stream capture, and make no call
+ * after resetting the device (cudaDeviceReset), which invalidates the kept
+ * address.  Every call uses the same array: calls whose GPU work
  * overlaps (other streams or other host threads) race on it.  The call
  * clears the status word, enqueues the work on `stream`, then synchronises
  * the stream and returns the device status (SSD_OK or the first device
@@ -253,19 +257,31 @@ SSD_API const char* ssd_status_string(int status);
 SSD_API int ssd_fwd_plan(const ssd_params_t* p, int has_initial_states, int has_final_states,
                  int* launches, int* nsplits);
 
-/* The hierarchy-aware segsum device routine on its own (test aid).
+/* The hierarchy-aware segsum device routines on their own (test aid).  Both
+ * forms of csrc/segsum.cuh run here with the inputs the forward kernels give
+ * them: the log-domain form, whose seg the SIMT kernel exponentiates, and the
+ * linear-domain form, whose factors the tensor-core kernel multiplies in.
  * log2decay: (nrows, chunk) fp32 log2-domain log-decays (<= 0, may be -inf),
- * chunk 64 or 128.  For each row, writes seg (chunk x chunk, fp32):
- * seg[i][j] = sum_{k=j+1..i} log2decay[k] for j <= i as the kernels compute
- * it (no prefix subtraction), -inf above the diagonal; and L (chunk x chunk):
- * the decay-mask values 2^seg the tensor-core kernel multiplies in (on
- * off-diagonal 32 x 32 blocks as the rank-one product of a row and a column
- * factor), 0 above the diagonal.  Either output may be NULL.
- * Device pointers; async on `stream`.
+ * chunk 64 or 128.  Per row (each output may be NULL):
+ *   seg_out  (chunk x chunk) seg[i][j] = sum_{k=j+1..i} log2decay[k] for j <= i,
+ *            as the log-domain routine forms it (no prefix subtraction),
+ *            -inf above the diagonal;
+ *   L_out    (chunk x chunk) the decay mask prod_{k=j+1..i} a_k of the
+ *            linear-domain routine, with a_k = ex2.approx(log2decay[k]) (the
+ *            tensor-core kernel's factors): products grown from the diagonal
+ *            on the 32 x 32 diagonal blocks, the rank-one product of the row
+ *            factor and the column factor on the blocks left of them, 0 above
+ *            the diagonal;
+ *   pexp_out (chunk) the row prefixes prod_{k=0..i} a_k (decay of the state
+ *            entering the chunk, at row i);
+ *   sfx_out  (chunk) the column suffixes prod_{k=j+1..chunk-1} a_k (decay of
+ *            token j's contribution to the state leaving the chunk).
+ * Device pointers; async on `stream`.  Returns SSD_ERR_INVALID_ARG for a NULL
+ * input or an unsupported chunk, SSD_ERR_CUDA for a failed launch.
  * Source: "GPU Hierarchy Meets Structured Matrices" (abstract): the 1-SS mask
  * as 1-SS diagonal blocks plus rank-one off-diagonal blocks. */
 SSD_API int ssd_segsum_dump(const float* log2decay, int64_t nrows, int32_t chunk,
-                    float* seg_out, float* L_out, void* stream);
+                    float* seg_out, float* L_out, float* pexp_out, float* sfx_out, void* stream);
 
 #ifdef __cplusplus
 }

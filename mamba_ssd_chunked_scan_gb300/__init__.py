@@ -248,14 +248,23 @@ def plan(params) -> tuple:
     return _lib.plan(params)
 
 
-def segsum_dump(log2decay: torch.Tensor, want_seg=True, want_L=True, stream=None):
-    """Run the hierarchy-aware segsum device routine on rows of log2-decays
-    (nrows, chunk) fp32; returns (seg, L), each (nrows, chunk, chunk) or None."""
+def segsum_dump(log2decay: torch.Tensor, want_seg=True, want_L=True, want_factors=False, stream=None):
+    """Run the hierarchy-aware segsum device routines on rows of log2-decays
+    (nrows, chunk) fp32.  Returns (seg, L) — the log-domain routine's seg and
+    the linear-domain routine's mask, each (nrows, chunk, chunk) or None — and,
+    with want_factors, also the linear-domain row prefixes and column suffixes
+    (nrows, chunk) as (seg, L, pexp, sfx)."""
     if log2decay.dtype != torch.float32 or log2decay.dim() != 2 or not log2decay.is_contiguous():
         raise ValueError("log2decay: contiguous fp32 (nrows, chunk)")
     nrows, q = log2decay.shape
-    seg = torch.empty((nrows, q, q), dtype=torch.float32, device=log2decay.device) if want_seg else None
-    L = torch.empty((nrows, q, q), dtype=torch.float32, device=log2decay.device) if want_L else None
-    rc = _lib.lib.ssd_segsum_dump(_ptr(log2decay), nrows, q, _ptr(seg), _ptr(L), _stream_handle(stream))
+    dev = log2decay.device
+    seg = torch.empty((nrows, q, q), dtype=torch.float32, device=dev) if want_seg else None
+    L = torch.empty((nrows, q, q), dtype=torch.float32, device=dev) if want_L else None
+    pexp = torch.empty((nrows, q), dtype=torch.float32, device=dev) if want_factors else None
+    sfx = torch.empty((nrows, q), dtype=torch.float32, device=dev) if want_factors else None
+    rc = _lib.lib.ssd_segsum_dump(_ptr(log2decay), nrows, q, _ptr(seg), _ptr(L), _ptr(pexp), _ptr(sfx),
+                                  _stream_handle(stream))
     _lib.check(rc, "ssd_segsum_dump")
+    if want_factors:
+        return seg, L, pexp, sfx
     return seg, L

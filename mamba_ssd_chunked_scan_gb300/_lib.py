@@ -68,7 +68,7 @@ def _load():
     lib.ssd_gate_norm.restype = ctypes.c_int
     lib.ssd_step.argtypes = [i64, i32, i32, i32, i32, i32, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp]
     lib.ssd_step.restype = ctypes.c_int
-    lib.ssd_segsum_dump.argtypes = [vp, i64, i32, vp, vp, vp]
+    lib.ssd_segsum_dump.argtypes = [vp, i64, i32, vp, vp, vp, vp, vp]
     lib.ssd_segsum_dump.restype = ctypes.c_int
     return lib
 

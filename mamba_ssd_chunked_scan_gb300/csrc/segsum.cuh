@@ -1,40 +1,57 @@
-// Hierarchy-aware segsum for one chunk of Q = 32 * NW tokens.
+// Hierarchy-aware segsum for one chunk of Q = 32 * NW tokens, in two forms
+// that share one hierarchy:
+//
+//   log domain     seg(i, j) = sum_{k=j+1..i} l_k          (SIMT kernel: exp2 of seg)
+//   linear domain  L(i, j)   = prod_{k=j+1..i} a_k, a_k = 2^{l_k}
+//                                                            (tensor-core kernel: L itself)
 //
 // "GPU Hierarchy Meets Structured Matrices" (abstract): the 1-semiseparable
-// decay mask L_ij = exp(seg(i, j)), seg(i, j) = sum_{k=j+1..i} l_k, is split
-// into 1-SS diagonal blocks (one per warp) and rank-one off-diagonal blocks,
-// built from warp-level scans and cross-warp aggregation, with no prefix
-// subtraction.
+// decay mask is split into 1-SS diagonal blocks (one per warp) and rank-one
+// off-diagonal blocks, built from per-warp scans and cross-warp aggregation,
+// with no prefix subtraction.  l is already scaled by log2 e, so the mask is
+// 2^seg.  One thread owns one row i = 32 w + lane of the chunk (warp w of the
+// row group).  In the log domain "+" combines ranges; in the linear domain
+// "*" does, and each a_k costs one exp2 per token instead of one per entry.
 //
-// One thread owns one row i = 32 w + lane of the chunk (warp w of the row
-// group).  All sums are in the log2 domain (l already scaled by log2 e), so
-// the mask is 2^seg.
+//   diagonal block w:   d[c] = range (32w + c, i], c <= lane, a running
+//                       combination grown leftwards from the diagonal
+//                       (d[lane] = identity).
+//   block suffix:       col[j] = range (j, end_r] for j in block r: the running
+//                       values of block r's last row (lane 31 of warp r).
+//   block total:        tot[r] = col[32 r] (+) l_{32 r}.
+//   row offsets:        R[w-1] = d[0] (+) l_{32 w};  R[r-1] = R[r] (+) tot[r];
+//                       R[r] = range (end_r, i].
+//   off-diagonal:       entry (i, j) = R[r] (+) col[j] for j in block r < w:
+//                       in the linear domain the block is the rank-one product
+//                       of a row factor and a column factor.
+//   chunk prefix:       p_i = R[0] (+) tot[0] = range [0, i].
+//   chunk suffix:       s_j = range (j, Q-1] = rlast[r] (+) col[j].
 //
-//   diagonal block w:   d[c] = seg(i, 32w + c), c <= lane, a running sum
-//                       grown leftwards from the diagonal (d[lane] = 0).
-//   block suffix:       colS[j] = seg(end_r, j) for j in block r: the running
-//                       sums of block r's last row (lane 31 of warp r).
-//   block total:        tot[r] = colS[32 r] + l_{32 r}.
-//   row offsets:        R[w-1] = d[0] + l_{32 w};  R[r-1] = R[r] + tot[r];
-//                       R[r] = seg(i, end_r).
-//   off-diagonal:       seg(i, j) = R[r] + colS[j] (j in block r < w); in the
-//                       linear domain the block is the rank-one product
-//                       2^R[r] * 2^colS[j].
-//   chunk prefix:       p_i = R[0] + tot[0] = sum_{k=0..i} l_k.
-//   chunk suffix:       s_j = seg(Q-1, j).
-//
-// Monotone by construction: every longer range is formed from a shorter
-// range's computed value plus further terms <= 0, along one path, and fp
-// rounding is monotone, so in fp32 exactly seg(i, j) <= seg(i, j+1),
-// seg(i+1, j) <= seg(i, j) and seg <= 0.  (Two rows that meet at column c
-// add the same terms in the same order from there on; rows of adjacent warps
-// meet through tot, which is the earlier block's last-row value plus one more
-// term.)  A -inf log-decay (document start) propagates as -inf, never NaN:
-// nothing is subtracted.
+// Monotone by construction, in either domain.  Every operand combined into a
+// range is <= 0 (log) or in [0, 1] (linear), and rounding is monotone, so a
+// combination never moves a value up.  Row order, seg(i, j) <= seg(i, j+1):
+// each longer range is formed from the shorter one's computed value (within a
+// block, across a block edge through R, and across rank-one blocks because
+// R[r-1] = R[r] (+) tot[r] with tot[r] <= identity).  Column order,
+// seg(i+1, j) <= seg(i, j): rows i and i+1 start one step apart and then
+// combine the same terms in the same order, and combining the same term with
+// two ordered values keeps them ordered; rows of adjacent warps meet through
+// tot, which is bit for bit the earlier block's last-row value combined with
+// one more term, exactly what the later row's offset is built from.  A -inf
+// log-decay (document start) gives -inf (log) or an exact 0 (linear), never
+// NaN: nothing is subtracted.
 #pragma once
 #include <cuda_runtime.h>
 
 namespace ssd {
+
+__device__ __forceinline__ float ex2_approx(float v) {
+    float r;
+    asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(r) : "f"(v));
+    return r;
+}
+
+// ============================================================== log domain
 
 template <int NW>
 struct SegsumShared {
@@ -51,12 +68,6 @@ struct SegsumRow {
     float R[NW];   // row offsets into earlier blocks, valid for r < w
     float p;       // chunk prefix through row i
 };
-
-__device__ __forceinline__ float ex2_approx(float v) {
-    float r;
-    asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(r) : "f"(v));
-    return r;
-}
 
 // Phase 1: the diagonal 1-SS block of row i; the block's last row publishes
 // its column suffixes and the block total.  Needs sh.ell complete (barrier
@@ -118,6 +129,107 @@ template <int NW>
 __device__ __forceinline__ float segsum_chunk_suffix(const SegsumShared<NW>& sh, int j) {
     const int r = j >> 5;
     return (r == NW - 1) ? sh.colS[j] : sh.rlast[r] + sh.colS[j];
+}
+
+// seg(i, j) of the calling thread's row i = 32 w + lane, any column j
+// (compile-time block index r and column c within it; -inf above the diagonal).
+template <int NW>
+__device__ __forceinline__ float segsum_entry(const SegsumShared<NW>& sh, const SegsumRow<NW>& row, int w,
+                                              int lane, int r, int c) {
+    if (r < w) return row.R[r] + sh.colS[32 * r + c];
+    if (r == w) return (c <= lane) ? row.d[c] : -INFINITY;
+    return -INFINITY;
+}
+
+// =========================================================== linear domain
+
+template <int NW>
+struct alignas(16) SegsumLinShared {
+    alignas(16) float a[32 * NW];      // input: a_k = 2^{l_k} (exactly 0 at a document start)
+    alignas(16) float colL[32 * NW];   // L(end of j's block, j)
+    float totL[NW];                    // block totals L(end_r, start_r - 1) = prod over block r
+    float rlastL[NW];                  // row factors of the chunk's last row, r < NW - 1
+    float tauL;                        // 2^{whole-chunk total}
+};
+
+template <int NW>
+struct SegsumLinRow {
+    float wl[32];                      // L(i, 32 w + c) for c <= lane, 0 above the diagonal
+    float rf[NW > 1 ? NW - 1 : 1];     // L(i, end of block r) for r < w: the rank-one row factors
+    float pe;                          // 2^{p_i}: prod_{k=0..i} a_k
+};
+
+// Phase 1: the diagonal 1-SS block, products grown leftwards from the
+// diagonal; the block's last row publishes its column factors and the block
+// total.  Needs sh.a complete (barrier before), a barrier after.
+template <int NW>
+__device__ __forceinline__ void segsum_lin_phase1(SegsumLinShared<NW>& sh, SegsumLinRow<NW>& row, int w,
+                                                  int lane) {
+    float e[32];
+    const float4* src = reinterpret_cast<const float4*>(sh.a + 32 * w);
+#pragma unroll
+    for (int q = 0; q < 8; ++q) {
+        const float4 v = src[q];
+        e[4 * q] = v.x;
+        e[4 * q + 1] = v.y;
+        e[4 * q + 2] = v.z;
+        e[4 * q + 3] = v.w;
+    }
+    float r = 1.f;
+#pragma unroll
+    for (int c = 31; c >= 0; --c) {
+        if (c < lane) r *= e[c + 1];
+        row.wl[c] = (c <= lane) ? r : 0.f;
+    }
+    if (lane == 31) {
+        float4* dst = reinterpret_cast<float4*>(sh.colL + 32 * w);
+#pragma unroll
+        for (int q = 0; q < 8; ++q)
+            dst[q] = make_float4(row.wl[4 * q], row.wl[4 * q + 1], row.wl[4 * q + 2], row.wl[4 * q + 3]);
+        sh.totL[w] = row.wl[0] * e[0];
+    }
+}
+
+// Phase 2: the rank-one row factors and the chunk prefix; the chunk's last
+// row publishes its factors (for the chunk suffixes) and the chunk total.
+// Needs the phase-1 barrier; a barrier after before segsum_lin_suffix().
+template <int NW>
+__device__ __forceinline__ void segsum_lin_phase2(SegsumLinShared<NW>& sh, SegsumLinRow<NW>& row, int w,
+                                                  int lane) {
+    float acc = row.wl[0] * sh.a[32 * w];   // prod_{k=32w..i} a_k
+#pragma unroll
+    for (int r = NW - 2; r >= 0; --r) {
+        if (r < w) {
+            row.rf[r] = acc;
+            acc *= sh.totL[r];
+        } else {
+            row.rf[r] = 0.f;
+        }
+    }
+    row.pe = acc;
+    if (w == NW - 1 && lane == 31) {
+#pragma unroll
+        for (int r = 0; r < NW - 1; ++r) sh.rlastL[r] = row.rf[r];
+        sh.tauL = acc;
+    }
+}
+
+// 2^{s_j} = L(Q-1, j) for column j (after the phase-2 barrier).
+template <int NW>
+__device__ __forceinline__ float segsum_lin_suffix(const SegsumLinShared<NW>& sh, int j) {
+    const int r = j >> 5;
+    return (r == NW - 1) ? sh.colL[j] : sh.rlastL[r] * sh.colL[j];
+}
+
+// L(i, j) of the calling thread's row: block r, column c within it.  The
+// kernels apply the same factors to G (row factor) and dt (column factor)
+// instead of forming L; this is the mask those factors make.
+template <int NW>
+__device__ __forceinline__ float segsum_lin_entry(const SegsumLinShared<NW>& sh, const SegsumLinRow<NW>& row,
+                                                  int w, int r, int c) {
+    if (r < w) return row.rf[r] * sh.colL[32 * r + c];
+    if (r == w) return row.wl[c];
+    return 0.f;
 }
 
 }  // namespace ssd

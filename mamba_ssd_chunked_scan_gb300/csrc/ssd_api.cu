@@ -4,6 +4,7 @@
 #include <stdio.h>
 #include <string.h>
 
+#include <atomic>
 #include <mutex>
 
 #include "ssd_common.cuh"
@@ -11,10 +12,32 @@
 
 using namespace ssd;
 
+namespace ssd {
+
+// SM count of the current device, looked up once per device and cached.
+int device_sms() {
+    static std::atomic<int> cache[kMaxDevices];
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) {
+        cudaGetLastError();   // no device visible: clear the error it left
+        return 0;
+    }
+    int v = cache[dev].load(std::memory_order_relaxed);
+    if (v > 0) return v;
+    if (cudaDeviceGetAttribute(&v, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || v <= 0) {
+        cudaGetLastError();
+        return 0;
+    }
+    cache[dev].store(v, std::memory_order_relaxed);
+    return v;
+}
+
+}  // namespace ssd
+
 namespace {
 
 constexpr int kSmemLimit = 227 * 1024;
-constexpr int64_t kAutoSMs = 152;   // SMs the automatic split plan fills (GB300)
+constexpr int64_t kFallbackSMs = 152;   // SMs the automatic split plan assumes when no device is visible
 
 constexpr int kStepMaxN = 512;    // dstate limit of the decode step (float4 vectors per lane)
 constexpr int kStepMaxP = 2048;   // headdim limit of the decode step (shared-memory rows)
@@ -40,9 +63,10 @@ int check_params(const ssd_params_t* p) {
     return SSD_OK;
 }
 
-// Automatic split plan (split_len = 0).  With at least as many (row, head)
-// units as SMs there is one split (the leftover-unit plan evens out the last
-// wave).  Otherwise each sequence is cut into n splits of at least 4 chunks:
+// Automatic split plan (split_len = 0), for the current device's SM count S
+// (152 when no device is visible).  With at least as many (row, head) units as
+// SMs there is one split (the leftover-unit plan evens out the last wave).
+// Otherwise each sequence is cut into n splits of at least 4 chunks:
 // the smallest n in [ceil(S / units), 4 S / units] whose units fill their waves
 // to at least 95 %, else the n with the best fill.  (Fewer splits means less
 // boundary-state traffic; a part-empty last wave idles SMs for a whole split.)
@@ -50,12 +74,14 @@ int64_t plan_split_len(const ssd_params_t* p) {
     const int64_t L = p->seqlen;
     int64_t sl = p->split_len;
     if (sl == 0) {
+        const int nsm = device_sms();
+        const int64_t sms = nsm > 0 ? nsm : kFallbackSMs;   // this device's SMs
         const int64_t bh = p->batch * p->nheads;
         const int64_t nchunks = (L + p->chunk - 1) / p->chunk;
         int64_t n = 1;
-        if (bh < kAutoSMs) {
-            const int64_t n_min = (kAutoSMs + bh - 1) / bh;
-            int64_t n_max = (4 * kAutoSMs + bh - 1) / bh;
+        if (bh < sms) {
+            const int64_t n_min = (sms + bh - 1) / bh;
+            int64_t n_max = (4 * sms + bh - 1) / bh;
             if (n_max > nchunks / 4) n_max = nchunks / 4;
             if (n_max < 1) n_max = 1;
             if (n_min >= n_max) {
@@ -64,7 +90,7 @@ int64_t plan_split_len(const ssd_params_t* p) {
                 double best = -1.0;
                 for (int64_t k = n_min; k <= n_max; ++k) {
                     const int64_t units = bh * k;
-                    const double fill = (double)units / (double)(((units + kAutoSMs - 1) / kAutoSMs) * kAutoSMs);
+                    const double fill = (double)units / (double)(((units + sms - 1) / sms) * sms);
                     if (fill > best + 1e-12) {
                         best = fill;
                         n = k;
@@ -119,12 +145,8 @@ struct TailPlan {
 bool plan_tail(const ssd_params_t* p, TailPlan* tp) {
     if (!tc_supported(p->headdim, p->dstate, p->chunk, p->dtype)) return false;
     if (plan_nsplit(p) != 1) return false;
-    int dev = 0, nsm = 0;
-    if (cudaGetDevice(&dev) != cudaSuccess ||
-        cudaDeviceGetAttribute(&nsm, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || nsm < 2) {
-        cudaGetLastError();   // no device here: no plan
-        return false;
-    }
+    const int nsm = device_sms();
+    if (nsm < 2) return false;   // no device here: no plan
     const int64_t units = p->batch * p->nheads;
     const int64_t T = units % nsm;
     const int64_t nch = (p->seqlen + p->chunk - 1) / p->chunk;
@@ -499,10 +521,12 @@ int ssd_step(int64_t batch, int32_t nheads, int32_t headdim, int32_t dstate, int
     return SSD_OK;
 }
 
-int ssd_segsum_dump(const float* l2, int64_t nrows, int32_t chunk, float* seg, float* L, void* stream) {
+int ssd_segsum_dump(const float* l2, int64_t nrows, int32_t chunk, float* seg, float* L, float* pexp,
+                    float* sfx, void* stream) {
     if (!l2 || nrows < 0 || (chunk != 64 && chunk != 128)) return SSD_ERR_INVALID_ARG;
     if (nrows == 0) return SSD_OK;
-    if (launch_segsum_dump(l2, nrows, chunk, seg, L, (cudaStream_t)stream) != cudaSuccess) return SSD_ERR_CUDA;
+    if (launch_segsum_dump(l2, nrows, chunk, seg, L, pexp, sfx, (cudaStream_t)stream) != cudaSuccess)
+        return SSD_ERR_CUDA;
     return SSD_OK;
 }
 

@@ -114,6 +114,11 @@ inline void fastdiv_consts(uint32_t d, uint32_t* m, uint32_t* l) {
     *m = (uint32_t)((((1ull << k) - d) << 32) / d + 1);
 }
 
+constexpr int kMaxDevices = 256;   // device ordinals the per-device caches cover
+
+// SM count of the current device (cached per device); 0 when no device is visible.
+int device_sms();
+
 size_t simt_smem_bytes(int Q, int P, int N);
 cudaError_t launch_simt(const FwdArgs& a, cudaStream_t st);
 cudaError_t launch_split_scan(const FwdArgs& a, cudaStream_t st);
@@ -126,7 +131,7 @@ int bwd_chunk(int P, int N, size_t smem_limit);
 cudaError_t launch_bwd(const BwdArgs& a, cudaStream_t st);
 size_t step_smem_bytes(int P, int N);
 cudaError_t launch_step(const StepArgs& a, cudaStream_t st);
-cudaError_t launch_segsum_dump(const float* l2, int64_t nrows, int chunk, float* seg, float* L,
-                               cudaStream_t st);
+cudaError_t launch_segsum_dump(const float* l2, int64_t nrows, int chunk, float* seg, float* L, float* pexp,
+                               float* sfx, cudaStream_t st);
 
 }  // namespace ssd

@@ -2,7 +2,9 @@
 //   ssd_chunk_simt      the chunked SSD forward for any supported shape and
 //                       dtype, fp32 arithmetic throughout (the fp32 path)
 //   ssd_split_scan      composes split aggregates into incoming states
-//   ssd_segsum_dump_k   the hierarchy-aware segsum routine on its own
+//   ssd_segsum_dump_k   both forms of the hierarchy-aware segsum routine on
+//                       their own (the log-domain form this file's forward
+//                       kernel uses, the linear-domain form of ssd_tc.cu)
 //
 // The chunked form follows "State Space Duality and Mamba-2", "The SSD Block
 // Decomposition Algorithm": per chunk the diagonal block ((C B^T) o L) X, the
@@ -28,25 +30,38 @@ __device__ __forceinline__ int find_doc(const int32_t* cu, int ndocs, int64_t t)
     return lo;
 }
 
+// The segsum scratch (SegsumShared<4> at most) sits at the start of the
+// dynamic shared memory, ahead of the tiles.
+constexpr size_t kSegsumBytes = (sizeof(SegsumShared<4>) + 15) / 16 * 16;
+
 size_t simt_smem_bytes(int Q, int P, int N) {
     size_t floats = (size_t)Q * P + 2 * (size_t)Q * N + (size_t)Q * Q + (size_t)P * N + 6 * (size_t)Q;
     size_t ints = 3 * (size_t)Q;
-    return floats * 4 + ints * 4 + 64;
+    return kSegsumBytes + floats * 4 + ints * 4 + 64;
 }
 
-template <typename T>
+// Chunk Q = 32 NW.  The decay mask comes from the hierarchy-aware segsum in
+// the log domain (segsum.cuh): one thread per chunk row, exp2 of each entry.
+// A document that starts at row st > 0 of the chunk gets a -inf log-decay
+// there, which zeroes every mask entry that would cross into it; the decay of
+// its own initial state (which the document's first token does apply) is
+// 2^{seg(i, st) + l_st}.
+template <typename T, int NW>
 __global__ void __launch_bounds__(256) ssd_chunk_simt(FwdArgs a) {
-    extern __shared__ float smem[];
-    const int Q = a.Q, P = a.P, N = a.N, H = a.H, G = a.G;
+    constexpr int Q = 32 * NW;
+    extern __shared__ float4 smem4[];
+    SegsumShared<NW>& sg = *reinterpret_cast<SegsumShared<NW>*>(smem4);
+    float* smem = reinterpret_cast<float*>(reinterpret_cast<char*>(smem4) + kSegsumBytes);
+    const int P = a.P, N = a.N, H = a.H, G = a.G;
     const int64_t L = a.L;
     float* xs = smem;                       // [Q][P]
     float* Bs = xs + Q * P;                 // [Q][N]
     float* Cs = Bs + Q * N;                 // [Q][N]
     float* M = Cs + Q * N;                  // [Q][Q]
     float* S = M + Q * Q;                   // [P][N] carried state
-    float* ell = S + P * N;                 // [Q] natural-log decays
-    float* dtv = ell + Q;                   // [Q]
-    float* pexp = dtv + Q;                  // [Q] exp(sum_{k=segstart..i} l_k)
+    float* lreal = S + P * N;               // [Q] log2-decays (no document-start -inf)
+    float* dtv = lreal + Q;                 // [Q]
+    float* pexp = dtv + Q;                  // [Q] decay of row i's segment-entry state
     float* wv = pexp + Q;                   // [Q] state weights of one segment end
     float* misc = wv + Q;                   // [2Q]: misc[0] = segment total
     int* segstart = (int*)(misc + 2 * Q);   // [Q] first row of row i's segment
@@ -54,6 +69,7 @@ __global__ void __launch_bounds__(256) ssd_chunk_simt(FwdArgs a) {
     int* flags = docid + Q;                 // [Q] bit0: segment starts a document; bit1: row ends a document
 
     const int tid = threadIdx.x, nt = blockDim.x;
+    const int w = tid >> 5, lane = tid & 31;   // segsum row tid (threads < Q)
     const int64_t u = blockIdx.x;
     const int s = (int)(u % a.nsplit);
     const int h = (int)((u / a.nsplit) % H);
@@ -61,7 +77,7 @@ __global__ void __launch_bounds__(256) ssd_chunk_simt(FwdArgs a) {
     const int g = h / (H / G);
     const int64_t t0 = (int64_t)s * a.split_len;
     const int64_t t1 = (t0 + a.split_len < L) ? t0 + a.split_len : L;
-    const float Ah = a.A[h];
+    const float A2 = a.A[h] * kLog2e;
     const float Dh = a.D ? a.D[h] : 0.f;
     const T* x = (const T*)a.x;
     const T* Bg = (const T*)a.B;
@@ -91,7 +107,7 @@ __global__ void __launch_bounds__(256) ssd_chunk_simt(FwdArgs a) {
         for (int i = tid; i < Q; i += nt) {
             float d = (i < n) ? a.dt[(b * L + c0 + i) * H + h] : 0.f;
             dtv[i] = d;
-            ell[i] = d * Ah;
+            const float l2 = d * A2;   // 0 past the chunk's last token
             int st = 0, doc = (int)b, fl = 0;
             if (i < n) {
                 const int64_t t = c0 + i;
@@ -106,24 +122,35 @@ __global__ void __launch_bounds__(256) ssd_chunk_simt(FwdArgs a) {
                     if (t == L - 1) fl |= 2;
                 }
             }
+            lreal[i] = l2;
+            sg.ell[i] = (st == i && i > 0) ? -INFINITY : l2;   // a document starts inside the chunk
             segstart[i] = st;
             docid[i] = doc;
             flags[i] = fl;
         }
         __syncthreads();
-        // (a) decay mask rows: M[i][j] = exp(seg(i, j)) dt_j on the segment,
-        //     seg grown leftwards from the diagonal; pexp_i for the state term
-        for (int i = tid; i < Q; i += nt) {
+        SegsumRow<NW> R;
+        if (tid < Q) segsum_phase1<NW>(sg, R, w, lane);
+        __syncthreads();
+        if (tid < Q) segsum_phase2<NW>(sg, R, w, lane);
+        // (a) decay mask rows: M[i][j] = 2^{seg(i, j)} dt_j (0 before the row's
+        //     segment start and above the diagonal); pexp_i for the state term
+        if (tid < Q) {
+            const int i = tid;
             float* Mi = M + (size_t)i * Q;
-            for (int j = 0; j < Q; ++j) Mi[j] = 0.f;
-            if (i < n) {
-                float r = 0.f;
-                for (int j = i; j >= segstart[i]; --j) {
-                    Mi[j] = expf(r) * dtv[j];
-                    r += ell[j];
+            const int st = segstart[i];
+            float sst = 0.f;   // seg(i, st)
+#pragma unroll
+            for (int r = 0; r < NW; ++r) {
+#pragma unroll
+                for (int c = 0; c < 32; ++c) {
+                    const int j = 32 * r + c;
+                    const float sv = segsum_entry<NW>(sg, R, w, lane, r, c);
+                    if (j == st) sst = sv;
+                    Mi[j] = (i < n && j <= i) ? exp2f(sv) * dtv[j] : 0.f;
                 }
-                pexp[i] = expf(r);
             }
+            pexp[i] = (st > 0) ? exp2f(sst + lreal[st]) : exp2f(R.p);
         }
         __syncthreads();
         // (b) times C_i . B_j
@@ -168,13 +195,17 @@ __global__ void __launch_bounds__(256) ssd_chunk_simt(FwdArgs a) {
             if (!chunk_end && !write_fin) continue;
             const int st = segstart[e];
             __syncthreads();
-            if (tid == 0) {
-                float r = 0.f;
-                for (int j = e; j >= st; --j) {
-                    wv[j] = expf(r) * dtv[j];
-                    r += ell[j];
+            if (tid == e) {
+                // row e of the segsum: weights 2^{seg(e, j)} dt_j (0 before the segment)
+#pragma unroll
+                for (int r = 0; r < NW; ++r) {
+#pragma unroll
+                    for (int c = 0; c < 32; ++c) {
+                        const int j = 32 * r + c;
+                        if (j <= e) wv[j] = exp2f(segsum_entry<NW>(sg, R, w, lane, r, c)) * dtv[j];
+                    }
                 }
-                misc[0] = expf(r);
+                misc[0] = pexp[e];
             }
             __syncthreads();
             const bool starts_doc = (flags[st] & 1) != 0;
@@ -189,15 +220,13 @@ __global__ void __launch_bounds__(256) ssd_chunk_simt(FwdArgs a) {
                 if (chunk_end) S[k] = v;   // each element read and written by one thread only
             }
         }
-        // the split's total decay: -inf once a document starts inside it
+        // the split's total decay: -inf once a document starts inside it (the
+        // chunk total is the segsum's, in log2, -inf past a document start)
         if (tid == 0) {
             bool restart = false;
-            float csum = 0.f;
-            for (int i = 0; i < n; ++i) {
+            for (int i = 0; i < n; ++i)
                 if (i == segstart[i] && (flags[i] & 1)) restart = true;
-                csum += ell[i];
-            }
-            tau = restart ? -INFINITY : tau + csum;
+            tau = restart ? -INFINITY : tau + sg.tau * 0.6931471805599453f;
         }
     }
     if (a.mode == kModeAggregate) {
@@ -264,60 +293,65 @@ __global__ void ssd_split_scan(const float* __restrict__ tau, float* __restrict_
     }
 }
 
+// Both forms of the segsum routine on rows of log2-decays: the log-domain
+// seg the SIMT kernel exponentiates, and the linear-domain mask, row prefix
+// and column suffix factors the tensor-core kernel multiplies in (the same
+// device functions, with the same inputs a_k = ex2(l_k)).
 template <int NW>
 __global__ void __launch_bounds__(32 * NW) ssd_segsum_dump_k(const float* __restrict__ l2, int64_t nrows,
                                                              float* __restrict__ seg_out,
-                                                             float* __restrict__ L_out) {
+                                                             float* __restrict__ L_out,
+                                                             float* __restrict__ pexp_out,
+                                                             float* __restrict__ sfx_out) {
     constexpr int Q = 32 * NW;
     __shared__ SegsumShared<NW> sh;
+    __shared__ SegsumLinShared<NW> shl;
     const int i = threadIdx.x, w = i >> 5, lane = i & 31;
     for (int64_t row = blockIdx.x; row < nrows; row += gridDim.x) {
         __syncthreads();
-        sh.ell[i] = l2[row * Q + i];
+        const float l = l2[row * Q + i];
+        sh.ell[i] = l;
+        shl.a[i] = ex2_approx(l);
         __syncthreads();
         SegsumRow<NW> R;
+        SegsumLinRow<NW> RL;
         segsum_phase1<NW>(sh, R, w, lane);
+        segsum_lin_phase1<NW>(shl, RL, w, lane);
         __syncthreads();
         segsum_phase2<NW>(sh, R, w, lane);
+        segsum_lin_phase2<NW>(shl, RL, w, lane);
+        __syncthreads();
+        if (pexp_out) pexp_out[row * Q + i] = RL.pe;
+        if (sfx_out) sfx_out[row * Q + i] = segsum_lin_suffix<NW>(shl, i);
         float* so = seg_out ? seg_out + (row * Q + i) * Q : nullptr;
         float* lo = L_out ? L_out + (row * Q + i) * Q : nullptr;
 #pragma unroll
         for (int r = 0; r < NW; ++r) {
-            if (r < w) {
-                const float rf = ex2_approx(R.R[r]);
-#pragma unroll 8
-                for (int c = 0; c < 32; ++c) {
-                    const float cs = sh.colS[32 * r + c];
-                    if (so) so[32 * r + c] = R.R[r] + cs;
-                    if (lo) lo[32 * r + c] = rf * ex2_approx(cs);
-                }
-            } else if (r == w) {
 #pragma unroll
-                for (int c = 0; c < 32; ++c) {
-                    if (so) so[32 * r + c] = (c <= lane) ? R.d[c] : -INFINITY;
-                    if (lo) lo[32 * r + c] = (c <= lane) ? ex2_approx(R.d[c]) : 0.f;
-                }
-            } else {
-                for (int c = 0; c < 32; ++c) {
-                    if (so) so[32 * r + c] = -INFINITY;
-                    if (lo) lo[32 * r + c] = 0.f;
-                }
+            for (int c = 0; c < 32; ++c) {
+                if (so) so[32 * r + c] = segsum_entry<NW>(sh, R, w, lane, r, c);
+                if (lo) lo[32 * r + c] = segsum_lin_entry<NW>(shl, RL, w, r, c);
             }
         }
     }
 }
 
+template <typename T, int NW>
+cudaError_t launch_simt_q(const FwdArgs& a, size_t smem, int64_t grid, cudaStream_t st) {
+    cudaError_t e = cudaFuncSetAttribute(ssd_chunk_simt<T, NW>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (e != cudaSuccess) return e;
+    ssd_chunk_simt<T, NW><<<(unsigned)grid, 256, smem, st>>>(a);
+    return cudaGetLastError();
+}
+
 cudaError_t launch_simt(const FwdArgs& a, cudaStream_t st) {
     const size_t smem = simt_smem_bytes(a.Q, a.P, a.N);
     const int64_t grid = a.batch * a.H * a.nsplit;
-    if (a.dtype == SSD_BF16) {
-        cudaFuncSetAttribute(ssd_chunk_simt<__nv_bfloat16>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-        ssd_chunk_simt<__nv_bfloat16><<<(unsigned)grid, 256, smem, st>>>(a);
-    } else {
-        cudaFuncSetAttribute(ssd_chunk_simt<float>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-        ssd_chunk_simt<float><<<(unsigned)grid, 256, smem, st>>>(a);
-    }
-    return cudaGetLastError();
+    if (a.Q != 64 && a.Q != 128) return cudaErrorInvalidValue;
+    if (a.dtype == SSD_BF16)
+        return a.Q == 128 ? launch_simt_q<__nv_bfloat16, 4>(a, smem, grid, st)
+                          : launch_simt_q<__nv_bfloat16, 2>(a, smem, grid, st);
+    return a.Q == 128 ? launch_simt_q<float, 4>(a, smem, grid, st) : launch_simt_q<float, 2>(a, smem, grid, st);
 }
 
 cudaError_t launch_split_scan(const FwdArgs& a, cudaStream_t st) {
@@ -329,11 +363,11 @@ cudaError_t launch_split_scan(const FwdArgs& a, cudaStream_t st) {
     return cudaGetLastError();
 }
 
-cudaError_t launch_segsum_dump(const float* l2, int64_t nrows, int chunk, float* seg, float* L,
-                               cudaStream_t st) {
+cudaError_t launch_segsum_dump(const float* l2, int64_t nrows, int chunk, float* seg, float* L, float* pexp,
+                               float* sfx, cudaStream_t st) {
     const unsigned grid = (unsigned)(nrows < 4096 ? nrows : 4096);
-    if (chunk == 128) ssd_segsum_dump_k<4><<<grid, 128, 0, st>>>(l2, nrows, seg, L);
-    else ssd_segsum_dump_k<2><<<grid, 64, 0, st>>>(l2, nrows, seg, L);
+    if (chunk == 128) ssd_segsum_dump_k<4><<<grid, 128, 0, st>>>(l2, nrows, seg, L, pexp, sfx);
+    else ssd_segsum_dump_k<2><<<grid, 64, 0, st>>>(l2, nrows, seg, L, pexp, sfx);
     return cudaGetLastError();
 }
 

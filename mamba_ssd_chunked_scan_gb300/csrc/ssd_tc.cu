@@ -35,6 +35,8 @@
 #include <cuda_bf16.h>
 #include <stddef.h>
 
+#include <atomic>
+
 #include "ssd_common.cuh"
 #include "segsum.cuh"
 #include "ssd_kernels.h"
@@ -79,32 +81,16 @@ struct ChunkMeta {
     float tauexp;                // 2^tau
 };
 
-// Scratch of one mask group.
-// Segsum scratch of one mask group, in the linear domain: a_k = 2^{l_k}
-// (exactly 0 at a document start).  The hierarchy is that of "GPU Hierarchy
-// Meets Structured Matrices" (1-SS diagonal blocks of 32 rows grown from the
-// diagonal, rank-one off-diagonal blocks, no prefix subtraction) with every
-// sum of log-decays replaced by the product of the factors in the same order.
-// Products of factors in [0, 1] are monotone under rounding exactly as the
-// sums are, and the mask needs one exp2 per token instead of one per entry.
+// Scratch of one mask group.  The segsum runs in the linear domain (the
+// hierarchy-aware routine segsum_lin_* of segsum.cuh): a_k = 2^{l_k}, exactly
+// 0 at a document start, and the mask needs one exp2 per token instead of
+// one per entry.
 struct MaskScratch {
-    alignas(16) float alin[Q];     // a_k, read as float4
-    alignas(16) float colL[Q];     // 2^{seg(end of j's block, j)}, written as float4
+    SegsumLinShared<4> seg;        // a_k in, column factors, block totals, last-row factors out
     alignas(16) float dtv[Q];      // read as float4
     alignas(16) float colfac[Q];   // colL[j] dt_j, read as float4
-    float totL[4];                 // 2^{block total}
-    float rlastL[4];               // 2^{R[r]} of the chunk's last row
     float totLog[4];               // block sums of the log2-decays (aggregate pass)
-    float tauL;                    // 2^{chunk total}
     int doc_cursor;
-};
-
-// Row values of one chunk that a mask-group thread carries from the segsum
-// to the scaled X tile, the mask and the epilogue (row i = 32 w + lane).
-struct MaskRow {
-    float wl[32];   // 2^{seg(i, 32 w + c)} for c <= lane, 0 above the diagonal
-    float rf[3];    // 2^{seg(i, end of block r)}, r < w
-    float pe;       // 2^{p_i}, the decay of the incoming state at row i
 };
 
 struct TcSmall {
@@ -122,8 +108,8 @@ struct TcSmall {
 };
 
 static_assert(sizeof(MaskScratch) % 16 == 0, "mask scratch keeps 16-byte alignment");
-static_assert(offsetof(MaskScratch, alin) % 16 == 0 && offsetof(MaskScratch, colL) % 16 == 0 &&
-                  offsetof(MaskScratch, dtv) % 16 == 0 && offsetof(MaskScratch, colfac) % 16 == 0,
+static_assert(offsetof(MaskScratch, seg) % 16 == 0 && offsetof(MaskScratch, dtv) % 16 == 0 &&
+                  offsetof(MaskScratch, colfac) % 16 == 0,
               "vector-accessed arrays must be 16-byte aligned");
 static_assert(offsetof(TcSmall, meta) % 16 == 0 && sizeof(ChunkMeta) % 16 == 0, "meta alignment");
 static_assert(offsetof(TcSmall, full) % 8 == 0, "mbarriers are 8-byte aligned");
@@ -531,7 +517,7 @@ __global__ void __launch_bounds__(kThreads, 1) ssd_chunk_tc(const __grid_constan
             }
             const float l2 = (flag & 1) ? -INFINITY : dti * A2;
             ChunkMeta& m = sh.meta[mb];
-            ms.alin[i] = ex2_approx(l2);          // 0 at a document start
+            ms.seg.a[i] = ex2_approx(l2);         // 0 at a document start
             ms.dtv[i] = dti;
             m.ell[i] = l2;
             m.dtv[i] = dti;
@@ -545,63 +531,19 @@ __global__ void __launch_bounds__(kThreads, 1) ssd_chunk_tc(const __grid_constan
             }
             ptx::named_bar(nb, 128);
             if (kDocs && mt == Q - 1) ms.doc_cursor = doc;   // later chunks start in (or after) this document
-            MaskRow row;
-            // segsum phase 1: the diagonal 1-SS block, products grown leftwards from the diagonal
-            {
-                float e[32];
-                const float4* src = reinterpret_cast<const float4*>(ms.alin + 32 * rb);
-#pragma unroll
-                for (int q = 0; q < 8; ++q) {
-                    const float4 v = src[q];
-                    e[4 * q] = v.x;
-                    e[4 * q + 1] = v.y;
-                    e[4 * q + 2] = v.z;
-                    e[4 * q + 3] = v.w;
-                }
-                float r = 1.f;
-#pragma unroll
-                for (int c2 = 31; c2 >= 0; --c2) {
-                    if (c2 < lane) r *= e[c2 + 1];
-                    row.wl[c2] = (c2 <= lane) ? r : 0.f;
-                }
-                if (lane == 31) {
-                    float4* dst = reinterpret_cast<float4*>(ms.colL + 32 * rb);
-#pragma unroll
-                    for (int q = 0; q < 8; ++q)
-                        dst[q] = make_float4(row.wl[4 * q], row.wl[4 * q + 1], row.wl[4 * q + 2], row.wl[4 * q + 3]);
-                    ms.totL[rb] = row.wl[0] * e[0];
-                }
-            }
+            SegsumLinRow<4> row;
+            segsum_lin_phase1<4>(ms.seg, row, rb, lane);   // the diagonal 1-SS block
             ptx::named_bar(nb, 128);
-            // segsum phase 2: row offsets into the earlier blocks and the chunk prefix
-            {
-                float acc = row.wl[0] * ms.alin[32 * rb];   // 2^{sum_{k=32w..i} l_k}
-#pragma unroll
-                for (int r = 2; r >= 0; --r) {
-                    if (r < rb) {
-                        row.rf[r] = acc;
-                        acc *= ms.totL[r];
-                    } else {
-                        row.rf[r] = 0.f;
-                    }
-                }
-                row.pe = acc;
-                if (rb == 3 && lane == 31) {
-#pragma unroll
-                    for (int r = 0; r < 3; ++r) ms.rlastL[r] = row.rf[r];
-                    ms.tauL = acc;
-                }
-            }
+            segsum_lin_phase2<4>(ms.seg, row, rb, lane);   // rank-one row factors, chunk prefix
             // the y store of chunk c-2 (staged in this group's scaled-X buffer) has read it
             if (mt == 0 && j >= 1) ptx::bulk_wait_read0();
             ptx::named_bar(nb, 128);
-            const float cl = ms.colL[i];
-            ms.colfac[i] = cl * dti;
-            const float xf = ((rb == 3) ? cl : ms.rlastL[rb] * cl) * dti;   // 2^{s_i} dt_i
+            ms.colfac[i] = ms.seg.colL[i] * dti;
+            const float xf = segsum_lin_suffix<4>(ms.seg, i) * dti;   // 2^{s_i} dt_i
             const float pe = row.pe;
             m.pexp[i] = pe;
             if (mt == 0) {
-                m.tauexp = ms.tauL;
+                m.tauexp = ms.seg.tauL;
                 if (!full_mode) m.tau = (ms.totLog[0] + ms.totLog[1]) + (ms.totLog[2] + ms.totLog[3]);
             }
             __syncwarp();
@@ -920,11 +862,8 @@ cudaError_t launch_tc(const FwdArgs& a, cudaStream_t st) {
     // one CTA per unit; units of at most kPersistChunks chunks run on a persistent
     // grid of at most one CTA per SM instead
     int64_t grid = a.grid_units > 0 ? a.grid_units : a.batch * a.H * a.nsplit;
-    int dev = 0, nsm = 0;
-    const bool persist = a.tail_units == 0 && (a.split_len + Q - 1) / Q <= kPersistChunks &&
-                         cudaGetDevice(&dev) == cudaSuccess &&
-                         cudaDeviceGetAttribute(&nsm, cudaDevAttrMultiProcessorCount, dev) == cudaSuccess &&
-                         nsm > 0 && grid > nsm;
+    const int nsm = device_sms();
+    const bool persist = a.tail_units == 0 && (a.split_len + Q - 1) / Q <= kPersistChunks && nsm > 0 && grid > nsm;
     if (persist) grid = nsm;
     void (*kern)(TcParams);
     if (persist)
@@ -933,14 +872,24 @@ cudaError_t launch_tc(const FwdArgs& a, cudaStream_t st) {
     else
         kern = full ? (docs ? ssd_chunk_tc<true, true, false> : ssd_chunk_tc<true, false, false>)
                     : (docs ? ssd_chunk_tc<false, true, false> : ssd_chunk_tc<false, false, false>);
-    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    // once per device and variant: the shared-memory opt-in, and the check that the
+    // warpgroup register budgets fit the registers the CTA is launched with
+    // (setmaxnreg.inc draws on that pool; a budget beyond it would wait forever)
+    static std::atomic<uint8_t> ready[kMaxDevices][8];
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess) return e;
-    // setmaxnreg.inc draws on the registers the CTA was launched with: the warpgroup
-    // budgets must fit that pool, or the increase would wait forever
-    cudaFuncAttributes fa;
-    if ((e = cudaFuncGetAttributes(&fa, kern)) != cudaSuccess) return e;
-    const int need = kRegsIssue + 3 * kRegsMath;
-    if (fa.numRegs * 4 < need) return cudaErrorInvalidConfiguration;
+    if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
+    std::atomic<uint8_t>& rd = ready[dev][(full ? 4 : 0) | (docs ? 2 : 0) | (persist ? 1 : 0)];
+    if (!rd.load(std::memory_order_acquire)) {
+        if ((e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem)) != cudaSuccess)
+            return e;
+        cudaFuncAttributes fa;
+        if ((e = cudaFuncGetAttributes(&fa, kern)) != cudaSuccess) return e;
+        const int need = kRegsIssue + 3 * kRegsMath;
+        if (fa.numRegs * 4 < need) return cudaErrorInvalidConfiguration;
+        rd.store(1, std::memory_order_release);
+    }
     kern<<<(unsigned)grid, kThreads, smem, st>>>(prm);
     return cudaGetLastError();
 }

@@ -40,8 +40,12 @@ def params(L, **kw):
 
 def test_workspace_size_and_plan(L):
     p = params(L)
-    # one split: the status header only (with a GPU present, also the leftover-unit plan's piece states)
-    assert L.workspace_size(p) == 256 or 256 < L.workspace_size(p) <= 256 + 512 + (4 << 20)
+    # one split: the status header only (with a GPU present, also the leftover-unit plan's
+    # piece log-decays and states), always inside the 8 MiB allocation-free scratch
+    for q in (p, params(L, batch=2), params(L, batch=4, nheads=48), params(L, batch=16, seqlen=1024, nheads=64,
+                                                                           ngroups=8)):
+        assert L.workspace_size(q) == 256 or 256 < L.workspace_size(q) < int(4.01 * (1 << 20))
+        assert L.workspace_size(q) <= 8 << 20
     fam, launches, ns = L.plan(p)
     assert ns == 1 and launches >= 1
     p = params(L, batch=1, seqlen=65536, nheads=32, split_len=2048)
@@ -82,8 +86,8 @@ def test_invalid_pointers_rejected_before_launch(L):
     assert call(bad) == 1
     assert call(args, wsb=100) == 3                       # workspace too small
     assert call(args, w=None) == 3                        # workspace missing
-    assert L.lib.ssd_segsum_dump(None, 10, 128, None, None, None) == 1
-    assert L.lib.ssd_segsum_dump(ok, 10, 96, None, None, None) == 1
+    assert L.lib.ssd_segsum_dump(None, 10, 128, None, None, None, None, None) == 1
+    assert L.lib.ssd_segsum_dump(ok, 10, 96, None, None, None, None, None) == 1
 
 
 def test_status_strings(L):
