@@ -4,15 +4,20 @@
     python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
                     [--workload 27b|sweep:B:L:S|long|varlen|tiny|decode[:B]|bwd[:B]|gatenorm]
 
-A step is one ssd_fwd call over one batch of the workload (default: the
-Mamba-2 2.7B-like layer, batch 8 x 2048 tokens, 80 heads, P 64, N 128, bf16).
-Inputs are synthetic (seeded), resident in HBM before timing; L2 is flushed
-(a 256 MiB write) before every timed step.  Under torchrun each rank runs its
+A step is one ssd_fwd call over one batch of the workload.  The default is
+the largest single-GPU configuration, one 65,536-token sequence with 32 heads
+(P 64, N 128, bf16, split length 2048, initial and final states); the same
+run then measures the other points of the tokens/s-vs-L curve (the 2.7B-like
+layer, the 16,384-token sweep at every (batch, L) and split length, the
+packed-document case) and reports them under "vs_L" in the same JSON line
+(--no-sweep skips them).  Inputs are synthetic (seeded), resident in HBM
+before timing; L2 is flushed (a 256 MiB write) before every timed step.  Under torchrun each rank runs its
 own copy of the workload (independent batch rows: weak scaling) and rank 0
 reports the aggregate over ranks with the slowest rank's time.
 
 --impl reference times the fp64 CPU oracle recurrence on the host cores on a
-bounded sample of the same workload (one batch row per step).
+bounded sample of the same workload (one batch row, at most 16,384 tokens of
+it, per step).
 
 --workload decode[:B] times the single-token decode step (ssd_step) of the
 same layer shape over a batch of B rows (default 256) from a resident state;
@@ -39,6 +44,9 @@ import numpy as np  # noqa: E402
 from mamba_ssd_chunked_scan_gb300 import synth  # noqa: E402
 
 METRIC = "SSD fwd tokens/s and achieved HBM GB/s (% of GB300 roofline) vs L, 1 GPU"
+# the headline: the largest single-GPU forward configuration (65,536 tokens of
+# one sequence, 32 heads, split length 2048, initial and final states)
+DEFAULT_WORKLOAD = "long"
 FALLBACK_HBM_GBS = 6800.0
 
 
@@ -333,9 +341,11 @@ def run_reference(args):
             "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}),
             flush=True)
         return
-    # bounded sample: one batch row of the workload per step
-    q = synth.SSDProblem(1, p.seqlen, p.nheads, p.headdim, p.dstate, p.ngroups, p.chunk, p.split_len,
-                         p.dtype, p.x[:1].copy(), p.dt[:1].copy(), p.A, p.B[:1].copy(), p.C[:1].copy(), p.D,
+    # bounded sample: one batch row of the workload per step, at most 16,384 tokens of it
+    T = p.seqlen if p.cu_seqlens is not None else min(p.seqlen, 16384)
+    q = synth.SSDProblem(1, T, p.nheads, p.headdim, p.dstate, p.ngroups, p.chunk, 0,
+                         p.dtype, p.x[:1, :T].copy(), p.dt[:1, :T].copy(), p.A, p.B[:1, :T].copy(),
+                         p.C[:1, :T].copy(), p.D,
                          None if p.initial_states is None else p.initial_states[:1].copy(), p.cu_seqlens,
                          p.name)
     for _ in range(args.warmup):
@@ -352,33 +362,28 @@ def run_reference(args):
     line = {"impl": "reference", "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world,
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True,
             "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-            "config": {"workload": p.name, "sample": f"1 of {p.batch} batch rows per step"},
+            "config": {"workload": p.name, "sample": f"batch row 0 of {p.batch}, tokens 0..{T - 1}, per step"},
             "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": cores, "kind": "oracle",
-                             "sample": f"fp64 sequential recurrence, batch row 0 of {p.name} per step"},
+                             "sample": f"fp64 sequential recurrence, batch row 0 (tokens 0..{T - 1}) of "
+                                       f"{p.name} per step"},
             "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
     print(json.dumps(line), flush=True)
 
 
 def cpu_baseline(p):
+    """The oracle beside the GPU number: all cores on a bounded sample (batch
+    row 0, at most 16,384 tokens), and one thread on its first 2,048 tokens."""
     import oracle
-    q = synth.SSDProblem(1, p.seqlen, p.nheads, p.headdim, p.dstate, p.ngroups, p.chunk, p.split_len,
-                         p.dtype, p.x[:1].copy(), p.dt[:1].copy(), p.A, p.B[:1].copy(), p.C[:1].copy(), p.D,
-                         None if p.initial_states is None else p.initial_states[:1].copy(), p.cu_seqlens,
-                         p.name)
-    reps, t_all = 0, 0.0
-    while t_all < 10.0 and reps < 16:
-        t0 = time.perf_counter()
-        oracle.ssd_recurrence(q, want_final=False)
-        t_all += time.perf_counter() - t0
-        reps += 1
-    tok = q.batch * q.seqlen * reps
-    # the same sample on one thread, once
+    r = oracle_rate(p, seconds=10.0)
+    T = min(p.seqlen, 2048) if p.cu_seqlens is None else p.seqlen
+    q = synth.SSDProblem(1, T, p.nheads, p.headdim, p.dstate, p.ngroups, p.chunk, 0,
+                         p.dtype, p.x[:1, :T].copy(), p.dt[:1, :T].copy(), p.A, p.B[:1, :T].copy(),
+                         p.C[:1, :T].copy(), p.D, None, p.cu_seqlens, p.name)
     t0 = time.perf_counter()
     oracle.ssd_recurrence(q, want_final=False, nthreads=1)
-    t1 = time.perf_counter() - t0
-    return {"value": tok / t_all, "unit": "tokens/s", "cores": oracle.max_threads(), "kind": "oracle",
-            "sample": f"fp64 recurrence on batch row 0 of {p.name}, {reps} passes, {t_all:.1f} s wall",
-            "single_thread_value": q.batch * q.seqlen / t1}
+    r["single_thread_value"] = T / (time.perf_counter() - t0)
+    r["single_thread_sample"] = f"batch row 0, tokens 0..{T - 1}, one thread"
+    return r
 
 
 def run_decode(args, p, dev, rank, local_rank, world):
@@ -668,10 +673,155 @@ def bwd_cpu_baseline(p, dy_h):
             "sample": f"fp64 reverse-mode recurrence, batch row 0, tokens 0..{q.seqlen - 1} of {p.name}, {reps} passes"}
 
 
+def forward_inputs(p, dev):
+    """Device tensors of one forward workload (the bytes the oracle reads)."""
+    import torch
+
+    def dev_io(name):
+        if p.dtype == "bf16":
+            return torch.from_numpy(p.storage(name).view(np.int16).copy()).to(dev).view(torch.bfloat16)
+        return torch.from_numpy(getattr(p, name)).to(dev)
+
+    d = dict(x=dev_io("x"), B=dev_io("B"), C=dev_io("C"), dt=torch.from_numpy(p.dt).to(dev),
+             A=torch.from_numpy(p.A).to(dev))
+    d["D"] = None if p.D is None else torch.from_numpy(p.D).to(dev)
+    d["init"] = None if p.initial_states is None else torch.from_numpy(p.initial_states).to(dev)
+    d["cu"] = None if p.cu_seqlens is None else torch.from_numpy(p.cu_seqlens).to(dev)
+    return d
+
+
+def time_forward(p, d, dev, stream, flush, warmup, steps, clk_index=None):
+    """Device time of one ssd_fwd call (CUDA events on the launching stream, L2
+    flushed before every call), and each launch's own duration (ssd_fwd_timed).
+    Returns (call object, plan, y, final_states, mean call ms, mean ms per launch, clocks)."""
+    import torch
+    import mamba_ssd_chunked_scan_gb300 as ssd
+
+    dtype = torch.bfloat16 if p.dtype == "bf16" else torch.float32
+    f = ssd.SSDForward(p.batch, p.seqlen, p.nheads, p.headdim, p.dstate, p.ngroups, p.chunk, p.split_len,
+                       p.ndocs, dtype, dev)
+    want_final = d["init"] is not None
+    plan = f.plan(want_final, want_final)
+    y = torch.empty_like(d["x"])
+    fin = torch.empty((f.nstates, p.nheads, p.headdim, p.dstate), dtype=torch.float32, device=dev) \
+        if want_final else None
+
+    def step():
+        f(d["x"], d["dt"], d["A"], d["B"], d["C"], d["D"], d["init"], d["cu"], y=y, final_states=fin, stream=stream)
+
+    for _ in range(warmup):
+        flush.zero_()
+        step()
+    assert f.check_status() == 0
+    torch.cuda.synchronize()
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(steps)]
+    clk = ClockSampler(clk_index) if clk_index is not None else None
+    if clk:
+        clk.__enter__()
+    try:
+        for i in range(steps):
+            flush.zero_()
+            ev[i][0].record(stream)
+            step()
+            ev[i][1].record(stream)
+        torch.cuda.synchronize()
+    finally:
+        if clk:
+            clk.__exit__()
+    st = f.check_status()
+    assert st == 0, f"device status {st}"
+    ms = sum(a.elapsed_time(b) for a, b in ev) / steps
+    per_launch = []
+    for _ in range(steps):
+        flush.zero_()
+        per_launch.append(f.launch_times(d["x"], d["dt"], d["A"], d["B"], d["C"], d["D"], d["init"], d["cu"],
+                                         y=y, final_states=fin, stream=stream))
+    launch_ms = [sum(r[k] for r in per_launch) / len(per_launch) for k in range(len(per_launch[0]))]
+    return f, plan, y, fin, ms, launch_ms, (clk.summary() if clk else None)
+
+
+def forward_roofline(p, plan, ms, launch_ms, nsm):
+    """The call's compulsory-byte rate and the full-pass launch's roofline: the
+    full pass (the call's last launch) reads all of x, dt, B, C, writes all of
+    y, and reads the incoming state of every unit that continues a sequence."""
+    family, launches, nsplit = plan
+    nbytes = compulsory_bytes(p)
+    peak, peak_kind = peaks()
+    achieved_call = nbytes / (ms / 1e3) / 1e9
+    state_bytes = 0
+    if launches > 1:
+        cont = p.batch * p.nheads * (nsplit - 1) if nsplit > 1 else tail_pieces(p, nsm)
+        state_bytes = cont * p.headdim * p.dstate * 4
+    kernel_bytes = nbytes + state_bytes
+    achieved = kernel_bytes / (launch_ms[-1] / 1e3) / 1e9
+    traffic = kernel_traffic(family) if nsplit == 1 else None
+    roof = {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s", "frac": achieved / peak,
+            "peak_source": peak_kind, "traffic": traffic, "algorithmic_bytes": kernel_bytes,
+            "frac_of_8TBps_spec": achieved / 8000.0,
+            "scope": ("the full-pass launch of ssd_chunk_tc: compulsory bytes plus incoming states, over its "
+                      f"own CUDA-event duration; frac_call is the whole call ({launches} launches)")
+            if family == 1 else f"the full-pass launch of ssd_chunk_simt ({launches} launches per call)"}
+    return nbytes, achieved_call, achieved_call / peak, roof
+
+
+def sweep_points():
+    """The other forward configurations, each a point of the tokens/s-vs-L
+    curve: the 2.7B-like layer, the fixed-16,384-token sweep at every (batch,
+    L) and split length, and the packed-document stress case."""
+    pts = [("27b", synth.config_27b)]
+    for b, L in ((16, 1024), (8, 2048), (4, 4096), (2, 8192), (1, 16384)):
+        for sc in (1, 4, 16):
+            pts.append((f"sweep:{b}:{L}:{sc}", lambda b=b, L=L, sc=sc: synth.config_sweep(b, L, sc)))
+    pts.append(("varlen", synth.config_varlen))
+    return pts
+
+
+def oracle_rate(p, seconds=2.0, max_tokens=16384):
+    """The fp64 oracle recurrence on a bounded sample (batch row 0, at most
+    max_tokens tokens; packed documents: the whole row), tokens/s on all cores."""
+    import oracle
+    T = p.seqlen if p.cu_seqlens is not None else min(p.seqlen, max_tokens)
+    q = synth.SSDProblem(1, T, p.nheads, p.headdim, p.dstate, p.ngroups, p.chunk, 0,
+                         p.dtype, p.x[:1, :T].copy(), p.dt[:1, :T].copy(), p.A, p.B[:1, :T].copy(),
+                         p.C[:1, :T].copy(), p.D,
+                         None if p.initial_states is None else p.initial_states[:1].copy(), p.cu_seqlens, p.name)
+    reps, t_all = 0, 0.0
+    while t_all < seconds and reps < 16:
+        t0 = time.perf_counter()
+        oracle.ssd_recurrence(q, want_final=False)
+        t_all += time.perf_counter() - t0
+        reps += 1
+    return {"value": T * reps / t_all, "unit": "tokens/s", "cores": oracle.max_threads(), "kind": "oracle",
+            "sample": f"fp64 recurrence on batch row 0 (tokens 0..{T - 1}) of {p.name}, {reps} passes, "
+                      f"{t_all:.1f} s wall"}
+
+
+def run_sweep(args, dev, stream, flush, nsm):
+    """One line per point of the vs-L curve (device time per call, the
+    full-pass roofline, the oracle on the host beside it)."""
+    import torch
+    out, rates = [], {}
+    for name, make in sweep_points():
+        p = make()
+        d = forward_inputs(p, dev)
+        f, plan, y, fin, ms, launch_ms, _ = time_forward(p, d, dev, stream, flush, 3, min(args.steps, 10))
+        nbytes, ach_call, frac_call, roof = forward_roofline(p, plan, ms, launch_ms, nsm)
+        key = (p.nheads, p.headdim, p.dstate, p.ngroups, p.cu_seqlens is not None)
+        if not args.no_cpu_baseline and key not in rates:
+            rates[key] = oracle_rate(p)
+        out.append({"workload": p.name, "batch": p.batch, "seq_len": p.seqlen, "nheads": p.nheads,
+                    "split_len": p.split_len, "nsplits": plan[2], "launches": plan[1],
+                    "ms_per_step": ms, "tokens_per_s": p.batch * p.seqlen / (ms / 1e3),
+                    "achieved_GBps_call": ach_call, "frac_call": frac_call, "launch_ms": launch_ms,
+                    "roofline": roof, "cpu_baseline": rates.get(key)})
+        del d, f, y, fin
+        torch.cuda.empty_cache()
+    return out
+
+
 def run_ours(args):
     import torch
     import torch.distributed as dist
-    import mamba_ssd_chunked_scan_gb300 as ssd
 
     rank, local_rank, world = dist_env()
     torch.cuda.set_device(local_rank)
@@ -685,62 +835,19 @@ def run_ours(args):
         return run_bwd(args, p, dev, rank, local_rank, world)
     if args.workload == "gatenorm":
         return run_gate_norm(args, p, dev, rank, local_rank, world)
-    dtype = torch.bfloat16 if p.dtype == "bf16" else torch.float32
 
-    def dev_io(name):
-        if p.dtype == "bf16":
-            return torch.from_numpy(p.storage(name).view(np.int16).copy()).to(dev).view(torch.bfloat16)
-        return torch.from_numpy(getattr(p, name)).to(dev)
-
-    x, B, C = dev_io("x"), dev_io("B"), dev_io("C")
-    dt = torch.from_numpy(p.dt).to(dev)
-    A = torch.from_numpy(p.A).to(dev)
-    D = None if p.D is None else torch.from_numpy(p.D).to(dev)
-    init = None if p.initial_states is None else torch.from_numpy(p.initial_states).to(dev)
-    cu = None if p.cu_seqlens is None else torch.from_numpy(p.cu_seqlens).to(dev)
-    want_final = init is not None
-    f = ssd.SSDForward(p.batch, p.seqlen, p.nheads, p.headdim, p.dstate, p.ngroups, p.chunk, p.split_len,
-                       p.ndocs, dtype, dev)
-    family, launches, nsplit = f.plan(init is not None, want_final)
-    y = torch.empty_like(x)
-    fin = torch.empty((f.nstates, p.nheads, p.headdim, p.dstate), dtype=torch.float32, device=dev) \
-        if want_final else None
+    d = forward_inputs(p, dev)
+    x, B, C, dt, A, D, init, cu = (d[k] for k in ("x", "B", "C", "dt", "A", "D", "init", "cu"))
     flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
     stream = torch.cuda.current_stream()
-
-    def step():
-        f(x, dt, A, B, C, D, init, cu, y=y, final_states=fin, stream=stream)
-
-    for _ in range(args.warmup):
-        flush.zero_()
-        step()
-    assert f.check_status() == 0
-    torch.cuda.synchronize()
     if world > 1:
         dist.barrier()
     torch.cuda.synchronize()
-    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
-    with ClockSampler(local_rank) as clk:
-        for i in range(args.steps):
-            flush.zero_()
-            ev[i][0].record(stream)
-            step()
-            ev[i][1].record(stream)
-        torch.cuda.synchronize()
+    f, plan, y, fin, ms, launch_ms, clocks = time_forward(p, d, dev, stream, flush, args.warmup, args.steps,
+                                                          clk_index=local_rank)
+    family, launches, nsplit = plan
     if world > 1:
         dist.barrier()
-    st = f.check_status()
-    assert st == 0, f"device status {st}"
-    kt = [a.elapsed_time(b) for a, b in ev]
-    ms = sum(kt) / len(kt)
-
-    # each launch of the call on its own (CUDA events around every launch, on the
-    # launching stream, L2 flushed before each call): the roofline's kernel figure
-    per_launch = []
-    for _ in range(args.steps):
-        flush.zero_()
-        per_launch.append(f.launch_times(x, dt, A, B, C, D, init, cu, y=y, final_states=fin, stream=stream))
-    launch_ms = [sum(r[k] for r in per_launch) / len(per_launch) for k in range(len(per_launch[0]))]
     copy_bw = device_copy_gbps(dev, stream)
 
     # End to end through the public API, as a job that streams batches runs it: every
@@ -762,25 +869,25 @@ def run_ours(args):
 
     def e2e_step(i):
         k = i % 2
-        d = dbufs[k]
+        b = dbufs[k]
         with torch.cuda.stream(s_in):
             if i >= 2:
                 s_in.wait_event(ev_comp[k])       # step i-2 has read this buffer set's inputs
-            d["x"].copy_(hx, non_blocking=True)
-            d["B"].copy_(hB, non_blocking=True)
-            d["C"].copy_(hC, non_blocking=True)
-            d["dt"].copy_(hdt, non_blocking=True)
+            b["x"].copy_(hx, non_blocking=True)
+            b["B"].copy_(hB, non_blocking=True)
+            b["C"].copy_(hC, non_blocking=True)
+            b["dt"].copy_(hdt, non_blocking=True)
             ev_in[k].record(s_in)
         stream.wait_event(ev_in[k])
         if i >= 2:
             stream.wait_event(ev_out[k])          # step i-2's result has left this buffer set
-        f(d["x"], d["dt"], A, d["B"], d["C"], D, init, cu, y=d["y"], final_states=d["fin"], stream=stream)
+        f(b["x"], b["dt"], A, b["B"], b["C"], D, init, cu, y=b["y"], final_states=b["fin"], stream=stream)
         ev_comp[k].record(stream)
         with torch.cuda.stream(s_out):
             s_out.wait_event(ev_comp[k])
-            hy[k].copy_(d["y"], non_blocking=True)
+            hy[k].copy_(b["y"], non_blocking=True)
             if hfin is not None:
-                hfin[k].copy_(d["fin"], non_blocking=True)
+                hfin[k].copy_(b["fin"], non_blocking=True)
             ev_out[k].record(s_out)
 
     for i in range(args.warmup):
@@ -794,27 +901,15 @@ def run_ours(args):
     torch.cuda.synchronize()
     assert f.check_status() == 0
     e2e_ms = e0.elapsed_time(e1) / args.steps
+    del dbufs, hy, hfin
 
     ms_max, e2e_max = slowest_rank([ms, e2e_ms], dev)
     tokens = p.batch * p.seqlen
     value = job_rate(tokens, world, ms_max)
     e2e_value = job_rate(tokens, world, e2e_max)
     if rank == 0:
-        nbytes = compulsory_bytes(p)
-        peak, peak_kind = peaks()
-        achieved_call = nbytes / (ms / 1e3) / 1e9
-        # the dominant kernel is the full pass (the call's last launch): it reads all of
-        # x, dt, B, C, writes all of y, and reads the incoming state of every unit that
-        # continues a sequence (split plans and the leftover-unit pieces)
-        full_ms = launch_ms[-1]
-        state_bytes = 0
-        if launches > 1:
-            nsm = torch.cuda.get_device_properties(dev).multi_processor_count
-            cont = p.batch * p.nheads * (nsplit - 1) if nsplit > 1 else tail_pieces(p, nsm)
-            state_bytes = cont * p.headdim * p.dstate * 4
-        kernel_bytes = nbytes + state_bytes
-        achieved = kernel_bytes / (full_ms / 1e3) / 1e9
-        traffic = kernel_traffic(family) if nsplit == 1 else None
+        nsm = torch.cuda.get_device_properties(dev).multi_processor_count
+        nbytes, achieved_call, frac_call, roof = forward_roofline(p, plan, ms, launch_ms, nsm)
         line = {
             "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world, "steps": args.steps,
             "warmup": args.warmup, "ms_per_step": ms_max, "higher_is_better": True, "scaling": "weak",
@@ -825,22 +920,19 @@ def run_ours(args):
                        "kernel": "tcgen05" if family == 1 else "simt",
                        "l2": "256 MiB write before every timed step; inputs larger than L2",
                        "compulsory_bytes": nbytes, "achieved_GBps_call": achieved_call,
-                       "frac_call": achieved_call / peak,
-                       "pct_of_8TBps_spec_call": 100.0 * achieved_call / 8000.0,
+                       "frac_call": frac_call, "pct_of_8TBps_spec_call": 100.0 * achieved_call / 8000.0,
                        "launch_ms": launch_ms, "copy_GBps_here": copy_bw},
-            "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
-                         "frac": achieved / peak, "peak_source": peak_kind, "traffic": traffic,
-                         "algorithmic_bytes": kernel_bytes, "frac_of_8TBps_spec": achieved / 8000.0,
-                         "scope": ("the full-pass launch of ssd_chunk_tc: compulsory bytes plus incoming "
-                                   "states, over its own CUDA-event duration; config.frac_call is the "
-                                   f"whole call ({launches} launches)") if family == 1 else
-                                  f"the full-pass launch of ssd_chunk_simt ({launches} launches per call)"},
+            "roofline": roof,
             "e2e": {"value": e2e_value, "unit": "tokens/s", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
             "gpu_launches": launches * args.steps,
-            "clocks": clk.summary(),
+            "clocks": clocks,
         }
         if world == 1 and not args.no_cpu_baseline:
             line["cpu_baseline"] = cpu_baseline(p)
+        if world == 1 and not args.no_sweep and args.workload == DEFAULT_WORKLOAD:
+            del d, x, B, C, dt, y, fin, hx, hB, hC, hdt, f
+            torch.cuda.empty_cache()
+            line["vs_L"] = run_sweep(args, dev, stream, flush, nsm)
         print(json.dumps(line), flush=True)
     if world > 1:
         dist.destroy_process_group()
@@ -852,8 +944,9 @@ def main():
     ap.add_argument("--steps", type=int, default=20)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
-    ap.add_argument("--workload", default="27b")
+    ap.add_argument("--workload", default=DEFAULT_WORKLOAD)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-sweep", action="store_true", help="skip the vs-L points of the default run")
     args = ap.parse_args()
     if args.warmup < 3 and args.impl == "ours":
         args.warmup = 3

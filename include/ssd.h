@@ -248,6 +248,33 @@ SSD_API int ssd_step(int64_t batch, int32_t nheads, int32_t headdim, int32_t dst
  * and return it (SSD_OK when no device error was recorded). */
 SSD_API int ssd_check_status(void* workspace, void* stream);
 
+/* ssd_check_status(), also returning in *where (if not NULL) which device wait
+ * recorded the error: 0 with SSD_OK, else a code of the tensor-core kernel
+ * (1 stage free, 2 stage loaded, 3 mask ready, 4 output buffer free, 5 state
+ * summary buffer free, 6 scaled-X tile ready, 7 chunk values free, 8 state
+ * summary done, 9 C B^T done, 10 chunk values ready, 11 off-diagonal output
+ * done, 12 drain of copies or MMAs in flight, 13 diagonal output done). */
+SSD_API int ssd_check_status_where(void* workspace, void* stream, uint32_t* where);
+
+/* Test aid for the device-side failure path: ssd_fwd() with an injected stall.
+ * The tensor-core kernel's TMA producer issues no loads, and every bounded
+ * wait gives up after max_wait_rounds back-off rounds (each 32 ns or more;
+ * ordinary calls allow 2^26).  The waits that depend on the loads run out;
+ * the first records SSD_ERR_TIMEOUT and its code in the status word, and
+ * every CTA stops waiting, lets its copies and MMAs finish, frees its tensor
+ * memory and exits.  y and final_states are undefined afterwards;
+ * ssd_check_status_where() reports the error and clears it, and the
+ * workspace serves ordinary calls again.  Arguments as ssd_fwd(); returns
+ * SSD_ERR_INVALID_ARG when max_wait_rounds < 4096 (the drain waits share the
+ * cap) and SSD_ERR_UNSUPPORTED for problems the tensor-core kernel does not
+ * run (the SIMT kernel has no device waits).  Not for production use. */
+SSD_API int ssd_fwd_fault_inject(const ssd_params_t* p,
+            const void* x, const float* dt, const float* A,
+            const void* B, const void* C, const float* D,
+            const float* initial_states, const int32_t* cu_seqlens,
+            void* y, float* final_states,
+            void* workspace, size_t workspace_bytes, uint32_t max_wait_rounds, void* stream);
+
 /* Human-readable name of a status code (static storage). */
 SSD_API const char* ssd_status_string(int status);
 

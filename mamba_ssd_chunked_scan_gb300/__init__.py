@@ -129,6 +129,21 @@ class SSDForward:
     def check_status(self, stream=None) -> int:
         return check_status(self.workspace, stream)
 
+    def check_status_where(self, stream=None):
+        """(status, code of the device wait that recorded it); clears the status."""
+        where = ctypes.c_uint32(0)
+        st = _lib.lib.ssd_check_status_where(_ptr(self.workspace), _stream_handle(stream), ctypes.byref(where))
+        return int(st), int(where.value)
+
+    def fault_inject(self, x, dt, A, B, C, D=None, initial_states=None, cu_seqlens=None, y=None,
+                     final_states=None, max_wait_rounds=1 << 14, stream=None):
+        """Test aid: the call with an injected stall (ssd_fwd_fault_inject): the
+        kernel's loads are never issued and its waits give up after
+        max_wait_rounds back-off rounds.  Read the outcome with check_status_where()."""
+        args, y = self._args(x, dt, A, B, C, D, initial_states, cu_seqlens, y, final_states, stream)
+        _lib.check(_lib.lib.ssd_fwd_fault_inject(*args[:-1], int(max_wait_rounds), args[-1]), "ssd_fwd_fault_inject")
+        return y
+
 
 def ssd_fwd(x, dt, A, B, C, D=None, initial_states=None, cu_seqlens=None, *, chunk=128, split_len=0,
             return_final_states=False, stream=None):

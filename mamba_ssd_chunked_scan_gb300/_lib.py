@@ -20,7 +20,7 @@ STATUS = {0: "SSD_OK", 1: "SSD_ERR_INVALID_ARG", 2: "SSD_ERR_UNSUPPORTED", 3: "S
 EXPORTS = ("ssd_fwd_workspace_size", "ssd_workspace_init", "ssd_fwd", "ssd_check_status",
            "ssd_status_string", "ssd_fwd_plan", "ssd_segsum_dump", "ssd_fwd_static_scratch", "ssd_step",
            "ssd_bwd_workspace_size", "ssd_bwd", "ssd_fwd_timed",
-           "ssd_gate_norm")
+           "ssd_gate_norm", "ssd_check_status_where", "ssd_fwd_fault_inject")
 
 
 class SSDParams(ctypes.Structure):
@@ -50,6 +50,10 @@ def _load():
     lib.ssd_fwd.restype = ctypes.c_int
     lib.ssd_check_status.argtypes = [vp, vp]
     lib.ssd_check_status.restype = ctypes.c_int
+    lib.ssd_check_status_where.argtypes = [vp, vp, ctypes.POINTER(ctypes.c_uint32)]
+    lib.ssd_check_status_where.restype = ctypes.c_int
+    lib.ssd_fwd_fault_inject.argtypes = [P, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, sz, ctypes.c_uint32, vp]
+    lib.ssd_fwd_fault_inject.restype = ctypes.c_int
     lib.ssd_status_string.argtypes = [ctypes.c_int]
     lib.ssd_status_string.restype = ctypes.c_char_p
     lib.ssd_fwd_plan.argtypes = [P, ctypes.c_int, ctypes.c_int, ctypes.POINTER(ctypes.c_int),

@@ -272,7 +272,8 @@ int ssd_workspace_init(void* workspace, size_t bytes, void* stream) {
     return SSD_OK;
 }
 
-int ssd_check_status(void* workspace, void* stream) {
+int ssd_check_status_where(void* workspace, void* stream, uint32_t* where) {
+    if (where) *where = 0;
     if (!workspace) return SSD_ERR_WORKSPACE;
     cudaStream_t st = (cudaStream_t)stream;
     WsHeader h;
@@ -281,13 +282,20 @@ int ssd_check_status(void* workspace, void* stream) {
     if (h.status != 0) {
         if (cudaMemsetAsync(workspace, 0, sizeof(WsHeader), st) != cudaSuccess) return SSD_ERR_CUDA;
         if (cudaStreamSynchronize(st) != cudaSuccess) return SSD_ERR_CUDA;
+        if (where) *where = h.where;
     }
     return (int)h.status;
 }
 
+int ssd_check_status(void* workspace, void* stream) { return ssd_check_status_where(workspace, stream, nullptr); }
+
 }  // extern "C"
 
 namespace {
+
+// Smallest wait cap the fault-injection entry point accepts: the drain waits
+// share the cap and must outlast the MMAs and copies still in flight.
+constexpr uint32_t kMinInjectWaitRounds = 4096;
 
 // Events recorded around each launch of one forward call (the measurement entry
 // point ssd_fwd_timed only).
@@ -297,9 +305,17 @@ struct LaunchTimer {
     int n = 0;
 };
 
+// Fault injection for the time-out test (test aid): a wait cap and a producer
+// that issues no loads.
+struct FaultInject {
+    uint32_t wait_iters;
+    int stall_loads;
+};
+
 int fwd_impl(const ssd_params_t* p, const void* x, const float* dt, const float* A, const void* B,
              const void* C, const float* D, const float* init, const int32_t* cu, void* y,
-             float* fin, void* workspace, size_t workspace_bytes, void* stream, LaunchTimer* tm) {
+             float* fin, void* workspace, size_t workspace_bytes, void* stream, LaunchTimer* tm,
+             const FaultInject* fi = nullptr) {
     int rc = check_params(p);
     if (rc != SSD_OK) return rc;
     if (!x || !dt || !A || !B || !C || !y) return SSD_ERR_INVALID_ARG;
@@ -331,12 +347,15 @@ int fwd_impl(const ssd_params_t* p, const void* x, const float* dt, const float*
     a.ws = (WsHeader*)workspace;
     a.ws_tau = (float*)((char*)workspace + wl.tau_off);
     a.ws_state = (float*)((char*)workspace + wl.state_off);
+    a.wait_iters = fi ? fi->wait_iters : kDefaultWaitIters;
+    a.stall_loads = fi ? fi->stall_loads : 0;
     cudaStream_t st = (cudaStream_t)stream;
 
     fastdiv_consts((uint32_t)p->nheads, &a.divH_m, &a.divH_l);
     fastdiv_consts((uint32_t)ns, &a.divS_m, &a.divS_l);
     fastdiv_consts((uint32_t)(p->nheads / p->ngroups), &a.divHG_m, &a.divHG_l);
     const bool tc = use_tc(p, init != nullptr);
+    if (fi && !tc) return SSD_ERR_UNSUPPORTED;   // only the tensor-core kernel has device waits
     a.Q = tc ? p->chunk : simt_chunk(p);
     if (a.Q == 0) return SSD_ERR_UNSUPPORTED;
     auto timed = [&](cudaError_t (*fn)(const FwdArgs&, cudaStream_t), const FwdArgs& aa) {
@@ -408,6 +427,15 @@ int ssd_fwd_timed(const ssd_params_t* p, const void* x, const float* dt, const f
     }
     for (int k = 0; k < made; ++k) cudaEventDestroy(tm.ev[k]);
     return rc;
+}
+
+int ssd_fwd_fault_inject(const ssd_params_t* p, const void* x, const float* dt, const float* A, const void* B,
+                         const void* C, const float* D, const float* init, const int32_t* cu, void* y,
+                         float* fin, void* workspace, size_t workspace_bytes, uint32_t max_wait_rounds,
+                         void* stream) {
+    if (max_wait_rounds < kMinInjectWaitRounds) return SSD_ERR_INVALID_ARG;
+    const FaultInject fi{max_wait_rounds, 1};
+    return fwd_impl(p, x, dt, A, B, C, D, init, cu, y, fin, workspace, workspace_bytes, stream, nullptr, &fi);
 }
 
 int ssd_fwd_static_scratch(const ssd_params_t* p, const void* x, const float* dt, const float* A,

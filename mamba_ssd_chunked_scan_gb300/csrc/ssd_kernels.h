@@ -10,6 +10,10 @@ struct WsHeader;
 
 enum { kModeFull = 0, kModeAggregate = 1 };
 
+// Back-off rounds (each >= 32 ns) a device-side wait of the tensor-core kernel
+// makes before it gives up: >= 2 s, far beyond any legitimate wait.
+constexpr uint32_t kDefaultWaitIters = 1u << 26;
+
 // Everything one launch of a chunk kernel needs (passed by value).
 struct FwdArgs {
     int64_t batch, L;
@@ -41,6 +45,11 @@ struct FwdArgs {
     int tail_units;
     int64_t tail_first;
     int64_t grid_units;
+    // bounded waits give up after this many back-off rounds (kDefaultWaitIters)
+    uint32_t wait_iters;
+    // fault injection (test aid, 0 otherwise): the TMA producer issues no loads,
+    // so every wait that depends on them runs out
+    int stall_loads;
 };
 
 // One decode step (ssd_step): everything the launch needs.

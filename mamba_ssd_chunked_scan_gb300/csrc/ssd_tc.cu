@@ -28,8 +28,9 @@
 // dependency, the state recurrence, is a short loop through the state group.
 // One thread of each math group owns one chunk row (= TMEM lane).
 //
-// Every wait is bounded; a wait that runs out records SSD_ERR_TIMEOUT in the
-// workspace status word, and the CTA drains its copies, frees TMEM and exits.
+// Every wait is bounded (FwdArgs::wait_iters back-off rounds); a wait that
+// runs out records SSD_ERR_TIMEOUT in the workspace status word, and the CTA
+// drains its copies, frees TMEM and exits.
 #include <cuda.h>
 #include <cudaTypedefs.h>
 #include <cuda_bf16.h>
@@ -59,13 +60,12 @@ constexpr uint32_t kSin = kXt + 2 * 16384;   // incoming state, bf16, (n rows, p
 constexpr uint32_t kTiles = kSin + 16384;
 // TMEM columns: G/M/Ydiag [2] (G, then M in cols 0-63 and Ydiag in 64-127) | Yoff [2] | dS
 constexpr uint32_t kTmGM = 0, kTmYo = 256, kTmDS = 384, kTmCols = 512;
-constexpr uint32_t kWaitIters = 1u << 26;   // >= 2 s of 32 ns back-offs: far beyond any legitimate wait
 constexpr float kLn2 = 0.6931471805599453f;
 constexpr int kBarMask0 = 1, kBarState = 3;  // named barriers: mask groups 1 and 2, state group 3
 
 // codes of the wait that gave up (WsHeader::where)
 enum : uint32_t {
-    kWhereEmpty = 1, kWhereFull = 2, kWhereBarM = 3, kWhereYFree = 4, kWhereDsFree = 5,
+    kWhereEmpty = 1, kWhereFull = 2, kWhereBarM = 3, kWhereYFree = 4, kWhereDsFree = 5, kWhereBarXt = 6,
     kWhereMetaFree = 7, kWhereBarDS = 8, kWhereBarG = 9, kWhereMetaFull = 10, kWhereBarY = 11,
     kWhereDrain = 12, kWhereBarYd = 13
 };
@@ -152,7 +152,7 @@ __device__ __forceinline__ void fail(TcSmall& sh, const FwdArgs& a, uint32_t whe
 // bounded wait; the first role that gives up records why and raises abort
 __device__ __forceinline__ bool wait_or_fail(TcSmall& sh, const FwdArgs& a, uint64_t* bar, uint32_t parity,
                                              uint32_t where) {
-    if (ptx::mbar_wait(bar, parity, &sh.abort, kWaitIters)) return true;
+    if (ptx::mbar_wait(bar, parity, &sh.abort, a.wait_iters)) return true;
     if (!*(volatile int*)&sh.abort) fail(sh, a, where);
     return false;
 }
@@ -389,7 +389,8 @@ __global__ void __launch_bounds__(kThreads, 1) ssd_chunk_tc(const __grid_constan
             cl.init(a);
             cp.init(a);
             cp.next2(a, nunits);
-            for (int c = 0; c < nch; ++c, cl.next(a, nunits)) {
+            // (fault injection: no load is issued, so the waits on them run out)
+            for (int c = 0; c < (a.stall_loads ? 0 : nch); ++c, cl.next(a, nunits)) {
                 const int st = c & 1;
                 prefetch(cp);
                 cp.next(a, nunits);
@@ -409,7 +410,7 @@ __global__ void __launch_bounds__(kThreads, 1) ssd_chunk_tc(const __grid_constan
             // drain: the last load issued into each stage has landed
             for (int st = 0; st < 2 && st < issued; ++st) {
                 const int last = ((issued - 1 - st) >> 1) * 2 + st;
-                if (!ptx::mbar_wait(&sh.full[st], (last >> 1) & 1, &sh.never, kWaitIters)) fail(sh, a, kWhereDrain);
+                if (!ptx::mbar_wait(&sh.full[st], (last >> 1) & 1, &sh.never, a.wait_iters)) fail(sh, a, kWhereDrain);
             }
         } else if (warp == 1 && lane == 0) {
             // ============================================================ dS issuer
@@ -419,7 +420,7 @@ __global__ void __launch_bounds__(kThreads, 1) ssd_chunk_tc(const __grid_constan
             for (int c = 0; c < nch; ++c) {
                 const int X = c & 1, j = c >> 1;
                 const uint32_t stg = ptx::smem_u32(sm + X * kStageBytes);
-                if (!wait_or_fail(sh, a, &sh.barXt[X], j & 1, kWhereBarM)) break;
+                if (!wait_or_fail(sh, a, &sh.barXt[X], j & 1, kWhereBarXt)) break;
                 if (c >= 1 && !wait_or_fail(sh, a, &sh.dsFree, (c - 1) & 1, kWhereDsFree)) break;
                 ptx::tc_fence_after();
                 const uint32_t xt = ptx::smem_u32(sm + kXt + 16384 * X);
@@ -430,7 +431,7 @@ __global__ void __launch_bounds__(kThreads, 1) ssd_chunk_tc(const __grid_constan
                 ptx::mma_commit(&sh.empty[X]);
             }
             ptx::mma_commit(&sh.drain[0]);
-            if (!ptx::mbar_wait(&sh.drain[0], 0, &sh.never, kWaitIters)) fail(sh, a, kWhereDrain);
+            if (!ptx::mbar_wait(&sh.drain[0], 0, &sh.never, a.wait_iters)) fail(sh, a, kWhereDrain);
         } else if (warp == 3 && lane == 0 && full_mode) {
             // ============================================================ Ydiag issuer
             constexpr uint32_t idYd = ptx::idesc_bf16(128, 64, 0, 1);
@@ -447,7 +448,7 @@ __global__ void __launch_bounds__(kThreads, 1) ssd_chunk_tc(const __grid_constan
                 ptx::mma_commit(&sh.empty[X]);
             }
             ptx::mma_commit(&sh.drain[3]);
-            if (!ptx::mbar_wait(&sh.drain[3], 0, &sh.never, kWaitIters)) fail(sh, a, kWhereDrain);
+            if (!ptx::mbar_wait(&sh.drain[3], 0, &sh.never, a.wait_iters)) fail(sh, a, kWhereDrain);
         } else if (warp == 2 && lane == 0 && full_mode) {
             // ============================================================ G issuer
             constexpr uint32_t idG = ptx::idesc_bf16(128, 128, 0, 0);
@@ -465,7 +466,7 @@ __global__ void __launch_bounds__(kThreads, 1) ssd_chunk_tc(const __grid_constan
                 ptx::mma_commit(&sh.barG[X]);
             }
             ptx::mma_commit(&sh.drain[1]);
-            if (!ptx::mbar_wait(&sh.drain[1], 0, &sh.never, kWaitIters)) fail(sh, a, kWhereDrain);
+            if (!ptx::mbar_wait(&sh.drain[1], 0, &sh.never, a.wait_iters)) fail(sh, a, kWhereDrain);
         }
     } else if (wg <= 2) {
         // ================================================================ mask groups
@@ -740,12 +741,17 @@ __global__ void __launch_bounds__(kThreads, 1) ssd_chunk_tc(const __grid_constan
             const size_t uw = (size_t)cs.un.ws;
             const int nv = (int)((t + Q < t1) ? Q : t1 - t);
             const bool unit_end = cs.c == cs.un.nch - 1;
-            wait_or_fail(sh, a, &sh.metaFull[mb], (c / NMETA) & 1, kWhereMetaFull);
+            const bool meta_ok = wait_or_fail(sh, a, &sh.metaFull[mb], (c / NMETA) & 1, kWhereMetaFull);
             const ChunkMeta& m = sh.meta[mb];
             // ---- packed documents that end inside this chunk: their final states
             if (full_mode && kDocs && a.fin) {
                 bool any = false;
                 for (int e = 0; e < nv - 1; ++e) any |= (m.rowflag[e] & 2) != 0;
+                // agreed by the whole group, and only on chunk values that are
+                // complete: the branch holds barriers, and after a wait that ran
+                // out the values may still be changing
+                const bool stale = ptx::named_bar_any(kBarState, 128, !meta_ok);
+                any = ptx::named_bar_any(kBarState, 128, any) && !stale;
                 if (any) {
                     wait_or_fail(sh, a, &sh.full[X], j & 1, kWhereFull);
                     doc_end_states(sh, m, stg, sm + kSin, a.fin, a.H, h, nv, i);
@@ -804,7 +810,7 @@ __global__ void __launch_bounds__(kThreads, 1) ssd_chunk_tc(const __grid_constan
         }
         if (mt == 0 && full_mode) {
             ptx::mma_commit(&sh.drain[2]);
-            if (!ptx::mbar_wait(&sh.drain[2], 0, &sh.never, kWaitIters)) fail(sh, a, kWhereDrain);
+            if (!ptx::mbar_wait(&sh.drain[2], 0, &sh.never, a.wait_iters)) fail(sh, a, kWhereDrain);
         }
     }
     ptx::tc_fence_before();
@@ -854,6 +860,7 @@ cudaError_t launch_tc(const FwdArgs& a, cudaStream_t st) {
     TcParams prm;
     memset(&prm, 0, sizeof(prm));
     prm.a = a;
+    if (prm.a.wait_iters == 0) prm.a.wait_iters = kDefaultWaitIters;
     if (!encode_4d(&prm.tm_x, a.x, P, a.H, a.L, a.batch) || !encode_4d(&prm.tm_B, a.B, N, a.G, a.L, a.batch) ||
         !encode_4d(&prm.tm_C, a.C, N, a.G, a.L, a.batch) || !encode_4d(&prm.tm_y, a.y, P, a.H, a.L, a.batch))
         return cudaErrorInvalidValue;

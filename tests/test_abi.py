@@ -220,3 +220,20 @@ def test_gate_norm_invalid_args(L, kw, code):
     rc = L.lib.ssd_gate_norm(d["rows"], d["width"], d["group_size"], d["dtype"], ptr("y"), ptr("z"), ptr("weight"),
                              d["eps"], ptr("out"), None)
     assert rc == code
+
+
+def test_fault_inject_argument_checks(L):
+    """The fault-injection test aid rejects a wait cap below 4096 rounds and
+    problems without device waits (the fp32 SIMT kernel) before any launch."""
+    ok = ctypes.c_void_p(0x1000)
+    p = params(L)
+    assert L.lib.ssd_fwd_fault_inject(ctypes.byref(p), *([ok] * 10), ok, 1 << 20, 100, None) == 1
+    p32 = params(L, batch=1, seqlen=256, nheads=2, headdim=16, dstate=16, chunk=64, dtype=0)
+    ptrs = [ctypes.c_void_p(0x100000 * (k + 1)) for k in range(10)]   # distinct, aligned, never dereferenced
+    ptrs[7] = None                                                     # no cu_seqlens
+    assert L.lib.ssd_fwd_fault_inject(ctypes.byref(p32), *ptrs, ok, 1 << 20, 1 << 14, None) == 2
+
+
+def test_check_status_where_without_workspace(L):
+    where = ctypes.c_uint32(7)
+    assert L.lib.ssd_check_status_where(None, None, ctypes.byref(where)) == 3 and where.value == 0
