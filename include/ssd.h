@@ -203,7 +203,7 @@ SSD_API int ssd_bwd(const ssd_params_t* p,
  *
  * (the Mamba-2 block's output gate and its grouped RMS norm, gate applied before
  * the norm).  Layouts: y, z, out (rows, width) dtype, row-major, contiguous,
- * 16-byte aligned; weight (width) fp32.  rows = batch * seqlen and width =
+ * 16-byte aligned; weight (width) fp32, 16-byte aligned.  rows = batch * seqlen and width =
  * nheads * headdim for ssd_fwd's y.  width must be a multiple of group_size;
  * group_size a multiple of 8 (bf16) or 4 (fp32) and at most 8192 (else
  * SSD_ERR_UNSUPPORTED); eps >= 0 and finite.  out may be y itself (in place).
@@ -249,11 +249,13 @@ SSD_API int ssd_step(int64_t batch, int32_t nheads, int32_t headdim, int32_t dst
 SSD_API int ssd_check_status(void* workspace, void* stream);
 
 /* ssd_check_status(), also returning in *where (if not NULL) which device wait
- * recorded the error: 0 with SSD_OK, else a code of the tensor-core kernel
- * (1 stage free, 2 stage loaded, 3 mask ready, 4 output buffer free, 5 state
- * summary buffer free, 6 scaled-X tile ready, 7 chunk values free, 8 state
- * summary done, 9 C B^T done, 10 chunk values ready, 11 off-diagonal output
- * done, 12 drain of copies or MMAs in flight, 13 diagonal output done). */
+ * recorded the error: 0 with SSD_OK, else a code of the tensor-core full-pass
+ * kernel (1 stage free, 2 stage loaded, 3 mask ready, 4 output buffer free,
+ * 5 state summary buffer free, 6 scaled-X tile ready, 7 chunk values free,
+ * 8 state summary done, 9 C B^T done, 10 chunk values ready, 11 off-diagonal
+ * output done, 12 drain of copies or MMAs in flight, 13 diagonal output done)
+ * or of the split-aggregate kernel (21 stage free, 22 stage loaded, 23 scaled
+ * tile ready, 24 split contraction done, 25 drain of copies in flight). */
 SSD_API int ssd_check_status_where(void* workspace, void* stream, uint32_t* where);
 
 /* Test aid for the device-side failure path: ssd_fwd() with an injected stall.

@@ -293,6 +293,9 @@ int ssd_check_status(void* workspace, void* stream) { return ssd_check_status_wh
 
 namespace {
 
+// Splits of at least this many chunks take the tensor-core aggregate kernel.
+constexpr int kAggMinChunks = 4;
+
 // Smallest wait cap the fault-injection entry point accepts: the drain waits
 // share the cap and must outlast the MMAs and copies still in flight.
 constexpr uint32_t kMinInjectWaitRounds = 4096;
@@ -388,8 +391,14 @@ int fwd_impl(const ssd_params_t* p, const void* x, const float* dt, const float*
         return SSD_OK;
     }
     if (ns > 1) {
+        // split plan: the splits' aggregates, their composition, then the full pass.
+        // Splits of several chunks take the tensor-core aggregate kernel (one
+        // contraction per split and pair of heads); splits of one to three chunks
+        // the full kernel's aggregate mode, whose persistent grid carries its
+        // pipeline across such short units.
         a.mode = kModeAggregate;
-        if (launch(a) != cudaSuccess) return SSD_ERR_CUDA;
+        const bool agg_tc = tc && a.split_len >= (int64_t)kAggMinChunks * p->chunk;
+        if ((agg_tc ? timed(launch_agg_tc, a) : launch(a)) != cudaSuccess) return SSD_ERR_CUDA;
         if (timed(launch_split_scan, a) != cudaSuccess) return SSD_ERR_CUDA;
     }
     a.mode = kModeFull;
@@ -514,7 +523,7 @@ int ssd_gate_norm(int64_t rows, int32_t width, int32_t group_size, int32_t dtype
     if (group_size % vec != 0 || group_size > 8192) return SSD_ERR_UNSUPPORTED;
     if (rows * (width / group_size) >= ((int64_t)1 << 31)) return SSD_ERR_UNSUPPORTED;
     if (!y || !z || !weight || !out) return SSD_ERR_INVALID_ARG;
-    if (!aligned(y, 16) || !aligned(z, 16) || !aligned(out, 16) || !aligned(weight, 4)) return SSD_ERR_INVALID_ARG;
+    if (!aligned(y, 16) || !aligned(z, 16) || !aligned(out, 16) || !aligned(weight, 16)) return SSD_ERR_INVALID_ARG;
     GateNormArgs a;
     a.rows = rows; a.width = width; a.group_size = group_size; a.dtype = dtype; a.eps = eps;
     a.y = y; a.z = z; a.weight = weight; a.out = out;

@@ -9,17 +9,22 @@
 // (silu of the gate branch z) and the normalisation is a root-mean-square norm
 // over groups of `group_size` consecutive channels with a per-channel weight.
 //
-// One CTA takes one (row, group): it reads y and z once as 16-byte vectors,
-// keeps g in shared memory while the sum of squares is reduced (warp shuffles,
-// then the warps' partials in a fixed order), and writes out once.
+// One CTA takes one (row, group) with just enough threads that each holds
+// kNormVecs 16-byte vectors of y and z: every load is issued before any value
+// is used (one HBM round trip per CTA), the gated values stay in registers
+// while the sum of squares is reduced (warp shuffles, then the warps'
+// partials in a fixed order), and each output vector is written once.
 #include "ssd_common.cuh"
 #include "ssd_kernels.h"
 
 namespace ssd {
 namespace {
 
-constexpr int kNormThreads = 256;
-constexpr int kNormVecs = 4;   // 16-byte vectors per thread loaded before any is used
+constexpr int kNormVecs = 4;   // 16-byte vectors of y (and of z) per thread
+// group_size <= 8192: at most 1024 bf16 or 2048 fp32 vectors, so at most
+// 256 (bf16) or 512 (fp32) threads
+template <typename T>
+constexpr int kNormMaxThreads = sizeof(T) == 2 ? 256 : 512;
 
 __device__ __forceinline__ float silu_gate(float y, float z) { return y * (z / (1.f + expf(-z))); }
 
@@ -60,9 +65,8 @@ struct Vec<__nv_bfloat16> {
 };
 
 template <typename T>
-__global__ void __launch_bounds__(kNormThreads) ssd_gate_norm_kernel(GateNormArgs a) {
-    extern __shared__ __align__(16) float g[];   // [group_size] gated values
-    __shared__ float part[kNormThreads / 32];
+__global__ void __launch_bounds__(kNormMaxThreads<T>) ssd_gate_norm_kernel(GateNormArgs a) {
+    __shared__ float part[kNormMaxThreads<T> / 32];
     constexpr int V = Vec<T>::n;
     const int gs = a.group_size, nvec = gs / V;
     const int ngroup = a.width / gs;
@@ -71,65 +75,74 @@ __global__ void __launch_bounds__(kNormThreads) ssd_gate_norm_kernel(GateNormArg
     const size_t base = (size_t)row * a.width + (size_t)grp * gs;
     const T* y = static_cast<const T*>(a.y) + base;
     const T* z = static_cast<const T*>(a.z) + base;
-    float ss = 0.f;
-    auto gate = [&](int k, const uint4& yr, const uint4& zr) {
-        float yv[V], zv[V];
-        Vec<T>::load(reinterpret_cast<const T*>(&yr), yv);
-        Vec<T>::load(reinterpret_cast<const T*>(&zr), zv);
+    const int nt = blockDim.x;
+    uint4 yr[kNormVecs], zr[kNormVecs];
 #pragma unroll
-        for (int e = 0; e < V; ++e) {
-            const float gv = silu_gate(yv[e], zv[e]);
-            g[k * V + e] = gv;
-            ss = fmaf(gv, gv, ss);
+    for (int r = 0; r < kNormVecs; ++r) {
+        const int k = threadIdx.x + r * nt;
+        if (k < nvec) {
+            yr[r] = __ldcs(reinterpret_cast<const uint4*>(y + k * V));
+            zr[r] = __ldcs(reinterpret_cast<const uint4*>(z + k * V));
         }
-    };
-    if (nvec <= kNormVecs * kNormThreads) {
-        // all of this thread's vectors in flight at once: one HBM round trip
-        uint4 yr[kNormVecs], zr[kNormVecs];
+    }
+    float gv[kNormVecs][V];
+    float ss = 0.f;
 #pragma unroll
-        for (int r = 0; r < kNormVecs; ++r) {
-            const int k = threadIdx.x + r * kNormThreads;
-            if (k < nvec) {
-                yr[r] = *reinterpret_cast<const uint4*>(y + k * V);
-                zr[r] = *reinterpret_cast<const uint4*>(z + k * V);
+    for (int r = 0; r < kNormVecs; ++r) {
+        const int k = threadIdx.x + r * nt;
+        if (k < nvec) {
+            float yv[V], zv[V];
+            Vec<T>::load(reinterpret_cast<const T*>(&yr[r]), yv);
+            Vec<T>::load(reinterpret_cast<const T*>(&zr[r]), zv);
+#pragma unroll
+            for (int e = 0; e < V; ++e) {
+                gv[r][e] = silu_gate(yv[e], zv[e]);
+                ss = fmaf(gv[r][e], gv[r][e], ss);
             }
         }
-#pragma unroll
-        for (int r = 0; r < kNormVecs; ++r) {
-            const int k = threadIdx.x + r * kNormThreads;
-            if (k < nvec) gate(k, yr[r], zr[r]);
-        }
-    } else {
-        for (int k = threadIdx.x; k < nvec; k += kNormThreads)
-            gate(k, *reinterpret_cast<const uint4*>(y + k * V), *reinterpret_cast<const uint4*>(z + k * V));
     }
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, o);
     if ((threadIdx.x & 31) == 0) part[threadIdx.x >> 5] = ss;
     __syncthreads();
     float tot = 0.f;
-#pragma unroll
-    for (int w = 0; w < kNormThreads / 32; ++w) tot += part[w];
+    for (int w = 0; w < nt / 32; ++w) tot += part[w];
     const float rstd = rsqrtf(tot / (float)gs + a.eps);
     const float* wt = a.weight + (size_t)grp * gs;
     T* out = static_cast<T*>(a.out) + base;
-    for (int k = threadIdx.x; k < nvec; k += kNormThreads) {
-        float ov[V];
 #pragma unroll
-        for (int e = 0; e < V; ++e) ov[e] = g[k * V + e] * rstd * wt[k * V + e];
-        Vec<T>::store(out + k * V, ov);
+    for (int r = 0; r < kNormVecs; ++r) {
+        const int k = threadIdx.x + r * nt;
+        if (k < nvec) {
+            float wv[V];
+#pragma unroll
+            for (int e = 0; e < V; e += 4) {
+                const float4 w4 = __ldg(reinterpret_cast<const float4*>(wt + k * V + e));
+                wv[e] = w4.x; wv[e + 1] = w4.y; wv[e + 2] = w4.z; wv[e + 3] = w4.w;
+            }
+            float ov[V];
+#pragma unroll
+            for (int e = 0; e < V; ++e) ov[e] = gv[r][e] * rstd * wv[e];
+            Vec<T>::store(out + k * V, ov);
+        }
     }
 }
 
 }  // namespace
 
 cudaError_t launch_gate_norm(const GateNormArgs& a, cudaStream_t st) {
-    const size_t smem = (size_t)a.group_size * sizeof(float);
+    const int V = a.dtype == SSD_BF16 ? 8 : 4;
+    const int nvec = a.group_size / V;
+    // threads: enough warps that each thread holds at most kNormVecs vectors
+    int threads = (nvec + kNormVecs - 1) / kNormVecs;
+    threads = (threads + 31) / 32 * 32;
+    if (threads > (a.dtype == SSD_BF16 ? kNormMaxThreads<__nv_bfloat16> : kNormMaxThreads<float>))
+        return cudaErrorInvalidValue;
     const int64_t ctas = a.rows * (a.width / a.group_size);
     if (a.dtype == SSD_BF16)
-        ssd_gate_norm_kernel<__nv_bfloat16><<<(unsigned)ctas, kNormThreads, smem, st>>>(a);
+        ssd_gate_norm_kernel<__nv_bfloat16><<<(unsigned)ctas, threads, 0, st>>>(a);
     else
-        ssd_gate_norm_kernel<float><<<(unsigned)ctas, kNormThreads, smem, st>>>(a);
+        ssd_gate_norm_kernel<float><<<(unsigned)ctas, threads, 0, st>>>(a);
     return cudaGetLastError();
 }
 

@@ -1,5 +1,6 @@
 // Host-side declarations shared by the libssd CUDA sources.
 #pragma once
+#include <cuda.h>
 #include <cuda_runtime.h>
 #include <stddef.h>
 #include <stdint.h>
@@ -131,9 +132,14 @@ int device_sms();
 size_t simt_smem_bytes(int Q, int P, int N);
 cudaError_t launch_simt(const FwdArgs& a, cudaStream_t st);
 cudaError_t launch_split_scan(const FwdArgs& a, cudaStream_t st);
+// 4-D TMA map over a (batch, L, heads_or_groups, inner) bf16 tensor; box = one
+// 64-element x 128-row tile of one head (group), 128-byte swizzle.
+bool encode_4d(CUtensorMap* tm, const void* base, int64_t inner, int64_t mid, int64_t L, int64_t batch);
 size_t tc_smem_bytes();
 bool tc_supported(int P, int N, int Q, int dtype);
 cudaError_t launch_tc(const FwdArgs& a, cudaStream_t st);
+int agg_heads_per_cta(int H, int G);
+cudaError_t launch_agg_tc(const FwdArgs& a, cudaStream_t st);
 cudaError_t launch_gate_norm(const GateNormArgs& a, cudaStream_t st);
 size_t bwd_smem_bytes(int Qb, int P, int N);
 int bwd_chunk(int P, int N, size_t smem_limit);

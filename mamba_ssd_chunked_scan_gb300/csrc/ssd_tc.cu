@@ -501,6 +501,11 @@ __global__ void __launch_bounds__(kThreads, 1) ssd_chunk_tc(const __grid_constan
                 Dh = a.D ? a.D[h] : 0.f;
             }
             const float dti = dt_next;
+            {
+                Cursor cn = cur;                  // this group's next item: its dt is loaded now,
+                cn.next2(a, nunits);              // a whole iteration before it is used
+                dt_next = load_dt(cn);
+            }
             if (c >= NMETA) wait_or_fail(sh, a, &sh.metaFree[mb], ((c / NMETA) - 1) & 1, kWhereMetaFree);
             // document boundaries: walk forward from this group's cursor
             int flag = 0, doc = (int)b;
@@ -672,8 +677,7 @@ __global__ void __launch_bounds__(kThreads, 1) ssd_chunk_tc(const __grid_constan
                     ptx::bulk_commit();
                 }
             }
-            cur.next2(a, nunits);                 // this group's next item, and its dt
-            dt_next = load_dt(cur);
+            cur.next2(a, nunits);                 // this group's next item
             if (ptx::named_bar_any(nb, 128, *(volatile int*)&sh.abort != 0)) break;
         }
         if (mt == 0) ptx::bulk_wait0();
@@ -819,7 +823,9 @@ __global__ void __launch_bounds__(kThreads, 1) ssd_chunk_tc(const __grid_constan
     if (warp == 1) ptx::tmem_dealloc(tb, kTmCols);
 }
 
-PFN_cuTensorMapEncodeTiled_v12000 get_encode() {
+}  // namespace
+
+static PFN_cuTensorMapEncodeTiled_v12000 get_encode() {
     static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
     if (!fn) {
         cudaDriverEntryPointQueryResult q;
@@ -847,8 +853,6 @@ bool encode_4d(CUtensorMap* tm, const void* base, int64_t inner, int64_t mid, in
                      CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     return r == CUDA_SUCCESS;
 }
-
-}  // namespace
 
 size_t tc_smem_bytes() { return kSmemBytes; }
 

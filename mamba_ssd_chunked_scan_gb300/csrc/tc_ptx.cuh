@@ -210,6 +210,27 @@ __device__ __forceinline__ void tmem_load32x2(uint32_t ta, uint32_t (&ra)[32], u
         : "r"(ta), "r"(tb)
         : "memory");
 }
+#define SSD_R16(r) "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]), \
+    "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15])
+__device__ __forceinline__ void tmem_load16(uint32_t ta, uint32_t (&r)[16]) {
+    asm volatile(
+        "tcgen05.ld.sync.aligned.32x32b.x16.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15}, [%16];\n\t"
+        "tcgen05.wait::ld.sync.aligned;"
+        : SSD_R16(r)
+        : "r"(ta)
+        : "memory");
+}
+__device__ __forceinline__ void tmem_load16x2(uint32_t ta, uint32_t (&ra)[16], uint32_t tb, uint32_t (&rb)[16]) {
+    asm volatile(
+        "tcgen05.ld.sync.aligned.32x32b.x16.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15}, [%32];\n\t"
+        "tcgen05.ld.sync.aligned.32x32b.x16.b32 {%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, "
+        "[%33];\n\t"
+        "tcgen05.wait::ld.sync.aligned;"
+        : SSD_R16(ra), SSD_R16(rb)
+        : "r"(ta), "r"(tb)
+        : "memory");
+}
+#undef SSD_R16
 #undef SSD_R32
 
 // 32 lanes x 16 consecutive 32-bit columns

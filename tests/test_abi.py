@@ -209,7 +209,7 @@ def test_fwd_timed_rejects_missing_outputs(L):
 @pytest.mark.parametrize("kw,code", [
     (dict(rows=0), 1), (dict(width=50), 1), (dict(dtype=3), 1), (dict(eps=-1.0), 1), (dict(eps=float("nan")), 1),
     (dict(group_size=12, width=48), 2), (dict(group_size=16384, width=16384), 2), (dict(y=None), 1),
-    (dict(out=(1 << 40) + 8), 1),
+    (dict(out=(1 << 40) + 8), 1), (dict(weight=(1 << 40) + (2 << 30) + 4), 1),
 ])
 def test_gate_norm_invalid_args(L, kw, code):
     d = dict(rows=4, width=64, group_size=16, dtype=1, y=1 << 40, z=(1 << 40) + (1 << 30),
