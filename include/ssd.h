@@ -260,8 +260,8 @@ SSD_API int ssd_check_status_where(void* workspace, void* stream, uint32_t* wher
 
 /* Test aid for the device-side failure path: ssd_fwd() with an injected stall.
  * The tensor-core kernel's TMA producer issues no loads, and every bounded
- * wait gives up after max_wait_rounds back-off rounds (each 32 ns or more;
- * ordinary calls allow 2^26).  The waits that depend on the loads run out;
+ * wait gives up after max_wait_rounds polls of its barrier (ordinary calls
+ * allow 2^26 polls, and every wait gives up after 2 s).  The waits that depend on the loads run out;
  * the first records SSD_ERR_TIMEOUT and its code in the status word, and
  * every CTA stops waiting, lets its copies and MMAs finish, frees its tensor
  * memory and exits.  y and final_states are undefined afterwards;

@@ -139,7 +139,7 @@ class SSDForward:
                      final_states=None, max_wait_rounds=1 << 14, stream=None):
         """Test aid: the call with an injected stall (ssd_fwd_fault_inject): the
         kernel's loads are never issued and its waits give up after
-        max_wait_rounds back-off rounds.  Read the outcome with check_status_where()."""
+        max_wait_rounds polls.  Read the outcome with check_status_where()."""
         args, y = self._args(x, dt, A, B, C, D, initial_states, cu_seqlens, y, final_states, stream)
         _lib.check(_lib.lib.ssd_fwd_fault_inject(*args[:-1], int(max_wait_rounds), args[-1]), "ssd_fwd_fault_inject")
         return y

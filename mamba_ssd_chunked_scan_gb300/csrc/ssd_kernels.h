@@ -11,8 +11,9 @@ struct WsHeader;
 
 enum { kModeFull = 0, kModeAggregate = 1 };
 
-// Back-off rounds (each >= 32 ns) a device-side wait of the tensor-core kernel
-// makes before it gives up: >= 2 s, far beyond any legitimate wait.
+// Polls a device-side wait of the tensor-core kernels makes before it gives up
+// (each poll is an mbarrier try_wait, which may suspend the thread for a while;
+// every wait also gives up after 2 s).
 constexpr uint32_t kDefaultWaitIters = 1u << 26;
 
 // Everything one launch of a chunk kernel needs (passed by value).
@@ -46,7 +47,7 @@ struct FwdArgs {
     int tail_units;
     int64_t tail_first;
     int64_t grid_units;
-    // bounded waits give up after this many back-off rounds (kDefaultWaitIters)
+    // bounded waits give up after this many polls (kDefaultWaitIters) or 2 s
     uint32_t wait_iters;
     // fault injection (test aid, 0 otherwise): the TMA producer issues no loads,
     // so every wait that depends on them runs out

@@ -28,7 +28,7 @@
 // dependency, the state recurrence, is a short loop through the state group.
 // One thread of each math group owns one chunk row (= TMEM lane).
 //
-// Every wait is bounded (FwdArgs::wait_iters back-off rounds); a wait that
+// Every wait is bounded (FwdArgs::wait_iters polls, and 2 s); a wait that
 // runs out records SSD_ERR_TIMEOUT in the workspace status word, and the CTA
 // drains its copies, frees TMEM and exits.
 #include <cuda.h>

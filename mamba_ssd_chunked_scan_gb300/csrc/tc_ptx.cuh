@@ -44,16 +44,20 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
     return ok != 0;
 }
 
-// Wait for the phase with the given parity to complete.  Gives up (returns
-// false) after `max_iters` back-off rounds (each sleeps ~32 ns or more), or
-// as soon as *abort is set, so that no wait can hang the GPU.
+// Wait for the phase with the given parity to complete.  try_wait suspends
+// the thread in hardware for a while when the phase is not yet complete, so
+// the loop polls without sleeping (a sleep between polls only delays the
+// waiter's reaction).  Gives up (returns false) after `max_iters` polls, after
+// kWaitLimitNs of %globaltimer, or as soon as *abort is set (both checked
+// every 64 polls), so that no wait can hang the GPU.
+constexpr uint64_t kWaitLimitNs = 2000000000ull;   // 2 s: far beyond any legitimate wait
 __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, const volatile int* abort,
                                           uint32_t max_iters) {
     if (mbar_try_wait(bar, parity)) return true;
+    const uint64_t t0 = globaltimer();
     for (uint32_t it = 1; it < max_iters; ++it) {
-        __nanosleep(32);   // back off: a waiting warp must not take issue slots from working warps
         if (mbar_try_wait(bar, parity)) return true;
-        if ((it & 255) == 0 && *abort) return false;
+        if ((it & 63) == 0 && (*abort || globaltimer() - t0 > kWaitLimitNs)) return false;
     }
     return false;
 }

@@ -63,6 +63,27 @@ def test_bf16_splits(split):
     check(p, split_len=split)
 
 
+@pytest.mark.parametrize("nheads", [3, 4])
+@pytest.mark.parametrize("split", [512, 1024])
+def test_bf16_split_aggregates_with_states(nheads, split):
+    # splits of 4 or more chunks take the tensor-core aggregate kernel: one or two
+    # heads per CTA (odd / even heads per group), two batch rows, initial states,
+    # a ragged last split
+    p = synth.make_problem(batch=2, seqlen=4 * 512 + 300, nheads=nheads, headdim=64, dstate=128, ngroups=1,
+                           chunk=128, dtype="bf16", seed=44, init_std=0.1)
+    check(p, split_len=split)
+
+
+@pytest.mark.parametrize("nheads", [3, 4])
+def test_bf16_split_aggregates_packed_documents(nheads):
+    # documents that start on a split start, on a chunk start and inside chunks, of
+    # length 1 up to a whole split, with splits of 4 chunks
+    lens = [1, 511, 512, 3, 509, 130, 1024, 77, 300]
+    p = synth.make_problem(batch=1, seqlen=sum(lens), nheads=nheads, headdim=64, dstate=128, ngroups=1,
+                           chunk=128, dtype="bf16", seed=46, dt_dist="softplus_n22", doc_lengths=lens)
+    check(p, split_len=512)
+
+
 @pytest.mark.parametrize("split", [0, 256])
 @pytest.mark.parametrize("init", [0.0, 0.2])
 def test_bf16_varlen_edges(split, init):

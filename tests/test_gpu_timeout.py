@@ -1,7 +1,7 @@
 """The device-side failure path of the tensor-core kernel, made to run on
 purpose without faulting or hanging the GPU: ssd_fwd_fault_inject() stops the
 kernel's TMA producer from issuing loads and caps every bounded wait at a
-short count of back-off rounds.  The waits that depend on the loads run out,
+short count of polls.  The waits that depend on the loads run out,
 the kernel records SSD_ERR_TIMEOUT with the code of the wait, every CTA drains
 and frees its tensor memory and exits; the status is read and cleared on the
 host, and the next ordinary call on the same workspace is correct."""
