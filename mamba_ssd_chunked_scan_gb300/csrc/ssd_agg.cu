@@ -261,11 +261,23 @@ __global__ void __launch_bounds__(kThreads, 1) ssd_split_agg_tc(const __grid_con
                 segsum_lin_phase2<4>(sh.seg[X][h], row, rb, lane);
             }
             ptx::named_bar(nb, 128);
-            // the product of the later chunks' totals (from the other group)
+            // the product of the later chunks' totals (from the other group); as soon
+            // as every thread has read it (and the chunk's sums), the product that
+            // includes this chunk's total goes on to the earlier chunk's group, so the
+            // two groups' scaling work overlaps
             agg_wait(sh, a, &sh.rdy[r & 1], j & 1, kWhereAggRdy);
             float R[K];
 #pragma unroll
-            for (int h = 0; h < K; ++h) R[h] = sh.rin[r & 1][h];
+            for (int h = 0; h < K; ++h) {
+                R[h] = sh.rin[r & 1][h];
+                Ls[h] += (sh.lsum[X][h][0] + sh.lsum[X][h][1]) + (sh.lsum[X][h][2] + sh.lsum[X][h][3]);
+            }
+            const bool stop = ptx::named_bar_any(nb, 128, *(volatile int*)&sh.abort != 0);
+            if (mt == 0 && r + 1 < nch) {
+#pragma unroll
+                for (int h = 0; h < K; ++h) sh.rin[(r + 1) & 1][h] = R[h] * sh.seg[X][h].tauL;
+                ptx::mbar_arrive(&sh.rdy[(r + 1) & 1]);
+            }
             // x~ = 2^{seg(split end, t)} dt_t x_t, written over the x rows in place
             const int st = r % Cfg::kStages;
             agg_wait(sh, a, &sh.full[st], (r / Cfg::kStages) & 1, kWhereAggFull);
@@ -274,31 +286,21 @@ __global__ void __launch_bounds__(kThreads, 1) ssd_split_agg_tc(const __grid_con
             for (int h = 0; h < K; ++h) {
                 const float wgt = segsum_lin_suffix<4>(sh.seg[X][h], i) * R[h] * dtv[h];
                 uint8_t* row = xs + h * kTileX;
+                uint4 v[8];   // the whole row's loads in flight before the first multiply
+#pragma unroll
+                for (int q = 0; q < 8; ++q) v[q] = *reinterpret_cast<const uint4*>(row + sw128_off(i, 8 * q));
 #pragma unroll
                 for (int q = 0; q < 8; ++q) {
-                    uint4* p4 = reinterpret_cast<uint4*>(row + sw128_off(i, 8 * q));
-                    uint4 v = *p4;
-                    v.x = scale_pair(v.x, wgt);
-                    v.y = scale_pair(v.y, wgt);
-                    v.z = scale_pair(v.z, wgt);
-                    v.w = scale_pair(v.w, wgt);
-                    *p4 = v;
+                    v[q].x = scale_pair(v[q].x, wgt);
+                    v[q].y = scale_pair(v[q].y, wgt);
+                    v[q].z = scale_pair(v[q].z, wgt);
+                    v[q].w = scale_pair(v[q].w, wgt);
+                    *reinterpret_cast<uint4*>(row + sw128_off(i, 8 * q)) = v[q];
                 }
             }
             ptx::fence_proxy_async();
             __syncwarp();
             if (lane == 0) ptx::mbar_arrive(&sh.ready[st]);
-#pragma unroll
-            for (int h = 0; h < K; ++h)
-                Ls[h] += (sh.lsum[X][h][0] + sh.lsum[X][h][1]) + (sh.lsum[X][h][2] + sh.lsum[X][h][3]);
-            // every thread of the group has read rin and the chunk's values: hand the
-            // earlier chunk the product that now includes this chunk's total
-            const bool stop = ptx::named_bar_any(nb, 128, *(volatile int*)&sh.abort != 0);
-            if (mt == 0 && r + 1 < nch) {
-#pragma unroll
-                for (int h = 0; h < K; ++h) sh.rin[(r + 1) & 1][h] = R[h] * sh.seg[X][h].tauL;
-                ptx::mbar_arrive(&sh.rdy[(r + 1) & 1]);
-            }
             if (stop) break;
         }
         if (mt == 0) {
