@@ -244,15 +244,15 @@ def kernel_sources_sha(family: int) -> str:
     return h.hexdigest()[:16]
 
 
-def kernel_traffic(family: int):
-    """DRAM bytes per launch of the dominant kernel from the committed ncu
-    summary, used only while the kernel source is unchanged since capture."""
+def kernel_traffic(family: int, workload: str):
+    """DRAM bytes per launch of the dominant kernel (the full pass) on this
+    workload, from the committed ncu summary, used only while the kernel
+    source is unchanged since the capture."""
     path = os.path.join(ROOT, "profiles", "traffic.json")
     if not os.path.exists(path):
         return None
     try:
-        d = json.load(open(path))
-        ent = d.get(str(family))
+        ent = json.load(open(path)).get(f"{family}:{workload}")
         if not ent:
             return None
         return ent["dram_bytes_per_launch"] if kernel_sources_sha(family) == ent["source_sha"] else None
@@ -754,7 +754,7 @@ def forward_roofline(p, plan, ms, launch_ms, nsm):
         state_bytes = cont * p.headdim * p.dstate * 4
     kernel_bytes = nbytes + state_bytes
     achieved = kernel_bytes / (launch_ms[-1] / 1e3) / 1e9
-    traffic = kernel_traffic(family) if nsplit == 1 else None
+    traffic = kernel_traffic(family, p.name)
     roof = {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s", "frac": achieved / peak,
             "peak_source": peak_kind, "traffic": traffic, "algorithmic_bytes": kernel_bytes,
             "frac_of_8TBps_spec": achieved / 8000.0,

@@ -26,7 +26,17 @@ constexpr int kNormVecs = 4;   // 16-byte vectors of y (and of z) per thread
 template <typename T>
 constexpr int kNormMaxThreads = sizeof(T) == 2 ? 256 : 512;
 
-__device__ __forceinline__ float silu_gate(float y, float z) { return y * (z / (1.f + expf(-z))); }
+// y silu(z) = y z / (1 + e^{-z}), with e^{-z} = 2^{-z log2 e} and the reciprocal
+// taken by the special-function unit (ex2.approx, rcp.approx: relative errors of a
+// few units in the last place, far inside the fp32 and bf16 tolerances).  The
+// gate is issue-bound with an IEEE exp and divide per element.  Large negative z
+// gives 1 / inf = 0 (the limit), large positive z gives 1.
+__device__ __forceinline__ float silu_gate(float y, float z) {
+    float e, r;
+    asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(e) : "f"(-z * 1.4426950408889634f));
+    asm("rcp.approx.ftz.f32 %0, %1;" : "=f"(r) : "f"(1.f + e));
+    return y * z * r;
+}
 
 template <typename T>
 struct Vec;   // 16 bytes of T
