@@ -86,11 +86,13 @@ __device__ __forceinline__ void segsum_phase1(SegsumShared<NW>& sh, SegsumRow<NW
         e[4 * q + 2] = v.z;
         e[4 * q + 3] = v.w;
     }
+    // the running sum takes -0 (an exact no-op) instead of a term past the
+    // diagonal, so its dependent chain is one add per column
     float r = 0.f;
     row.d[31] = 0.f;
 #pragma unroll
     for (int c = 30; c >= 0; --c) {
-        if (c < lane) r += e[c + 1];
+        r += (c < lane) ? e[c + 1] : -0.f;
         row.d[c] = r;
     }
     if (lane == 31) {
@@ -161,33 +163,55 @@ struct SegsumLinRow {
 
 // Phase 1: the diagonal 1-SS block, products grown leftwards from the
 // diagonal; the block's last row publishes its column factors and the block
-// total.  Needs sh.a complete (barrier before), a barrier after.
+// total.  Needs sh.a complete (barrier before), a barrier after.  K
+// independent chunks (of different heads) at once: their product chains
+// interleave, each one multiply per column.
+template <int NW, int K>
+__device__ __forceinline__ void segsum_lin_phase1_k(SegsumLinShared<NW>* sh, SegsumLinRow<NW>* row, int w,
+                                                    int lane) {
+    float e[K][32];
+#pragma unroll
+    for (int h = 0; h < K; ++h) {
+        const float4* src = reinterpret_cast<const float4*>(sh[h].a + 32 * w);
+#pragma unroll
+        for (int q = 0; q < 8; ++q) {
+            const float4 v = src[q];
+            e[h][4 * q] = v.x;
+            e[h][4 * q + 1] = v.y;
+            e[h][4 * q + 2] = v.z;
+            e[h][4 * q + 3] = v.w;
+        }
+    }
+    // the running product takes 1 (an exact no-op) instead of a factor past the
+    // diagonal, so its dependent chain is one multiply per column
+    float r[K];
+#pragma unroll
+    for (int h = 0; h < K; ++h) r[h] = 1.f;
+#pragma unroll
+    for (int c = 31; c >= 0; --c) {
+#pragma unroll
+        for (int h = 0; h < K; ++h) {
+            r[h] *= (c < lane) ? e[h][c + 1] : 1.f;
+            row[h].wl[c] = (c <= lane) ? r[h] : 0.f;
+        }
+    }
+    if (lane == 31) {
+#pragma unroll
+        for (int h = 0; h < K; ++h) {
+            float4* dst = reinterpret_cast<float4*>(sh[h].colL + 32 * w);
+#pragma unroll
+            for (int q = 0; q < 8; ++q)
+                dst[q] = make_float4(row[h].wl[4 * q], row[h].wl[4 * q + 1], row[h].wl[4 * q + 2],
+                                     row[h].wl[4 * q + 3]);
+            sh[h].totL[w] = row[h].wl[0] * e[h][0];
+        }
+    }
+}
+
 template <int NW>
 __device__ __forceinline__ void segsum_lin_phase1(SegsumLinShared<NW>& sh, SegsumLinRow<NW>& row, int w,
                                                   int lane) {
-    float e[32];
-    const float4* src = reinterpret_cast<const float4*>(sh.a + 32 * w);
-#pragma unroll
-    for (int q = 0; q < 8; ++q) {
-        const float4 v = src[q];
-        e[4 * q] = v.x;
-        e[4 * q + 1] = v.y;
-        e[4 * q + 2] = v.z;
-        e[4 * q + 3] = v.w;
-    }
-    float r = 1.f;
-#pragma unroll
-    for (int c = 31; c >= 0; --c) {
-        if (c < lane) r *= e[c + 1];
-        row.wl[c] = (c <= lane) ? r : 0.f;
-    }
-    if (lane == 31) {
-        float4* dst = reinterpret_cast<float4*>(sh.colL + 32 * w);
-#pragma unroll
-        for (int q = 0; q < 8; ++q)
-            dst[q] = make_float4(row.wl[4 * q], row.wl[4 * q + 1], row.wl[4 * q + 2], row.wl[4 * q + 3]);
-        sh.totL[w] = row.wl[0] * e[0];
-    }
+    segsum_lin_phase1_k<NW, 1>(&sh, &row, w, lane);
 }
 
 // Phase 2: the rank-one row factors and the chunk prefix; the chunk's last
@@ -199,12 +223,8 @@ __device__ __forceinline__ void segsum_lin_phase2(SegsumLinShared<NW>& sh, Segsu
     float acc = row.wl[0] * sh.a[32 * w];   // prod_{k=32w..i} a_k
 #pragma unroll
     for (int r = NW - 2; r >= 0; --r) {
-        if (r < w) {
-            row.rf[r] = acc;
-            acc *= sh.totL[r];
-        } else {
-            row.rf[r] = 0.f;
-        }
+        row.rf[r] = (r < w) ? acc : 0.f;
+        acc *= (r < w) ? sh.totL[r] : 1.f;   // 1: an exact no-op past the row's own block
     }
     row.pe = acc;
     if (w == NW - 1 && lane == 31) {

@@ -247,11 +247,11 @@ __global__ void __launch_bounds__(kThreads, 1) ssd_split_agg_tc(const __grid_con
             // segsum: the diagonal blocks, then the rank-one row factors (the
             // column suffixes need both; the rows themselves are not used)
             float w0[K];
+            {
+                SegsumLinRow<4> rows[K];
+                segsum_lin_phase1_k<4, K>(sh.seg[X], rows, rb, lane);
 #pragma unroll
-            for (int h = 0; h < K; ++h) {
-                SegsumLinRow<4> row;
-                segsum_lin_phase1<4>(sh.seg[X][h], row, rb, lane);
-                w0[h] = row.wl[0];
+                for (int h = 0; h < K; ++h) w0[h] = rows[h].wl[0];
             }
             ptx::named_bar(nb, 128);
 #pragma unroll
