@@ -57,8 +57,7 @@ struct AggCfg {
 
 struct AggSmall {
     SegsumLinShared<4> seg[2][4];   // per scaling group and head
-    float lsum[2][4][4];            // per group, head and warp: sums of the log2-decays
-    float lsgrp[2][4];              // per group and head: the group's sum over its chunks
+    float lsum[2][4][4];            // per group, head and warp: sums of the log2-decays over the split
     float rin[2][4];                // running product of the later chunks' totals, by chunk parity
     uint64_t full[4], empty[4], ready[4], rdy[2], done;
     uint32_t tmem_base;
@@ -91,8 +90,11 @@ __device__ __forceinline__ int find_doc_agg(const int32_t* cu, int ndocs, int64_
     return lo;
 }
 
-__device__ __forceinline__ uint32_t scale_pair(uint32_t w, float f) {
-    float lo = __uint_as_float(w << 16) * f, hi = __uint_as_float(w & 0xFFFF0000u) * f;
+// Two bf16 values (one 32-bit word) times f2 = (f, f), rounded back to bf16;
+// the two products in one packed fp32 multiply (each lane rounds as mul.rn.f32).
+__device__ __forceinline__ uint32_t scale_pair(uint32_t w, uint64_t f2) {
+    float lo, hi;
+    ptx::f2_unpack(ptx::f2_mul(ptx::f2_pack(__uint_as_float(w << 16), __uint_as_float(w & 0xFFFF0000u)), f2), lo, hi);
     __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
     return *reinterpret_cast<uint32_t*>(&v);
 }
@@ -238,10 +240,7 @@ __global__ void __launch_bounds__(kThreads, 1) ssd_split_agg_tc(const __grid_con
             for (int h = 0; h < K; ++h) {
                 const float l2 = start ? -INFINITY : dtv[h] * A2[h];
                 sh.seg[X][h].a[i] = ex2_approx(l2);   // 0 at a document start
-                float ls = l2;
-#pragma unroll
-                for (int o = 16; o > 0; o >>= 1) ls += __shfl_xor_sync(0xffffffffu, ls, o);
-                if (lane == 0) sh.lsum[X][h][rb] = ls;
+                Ls[h] += l2;                          // this row's share of the split's total
             }
             ptx::named_bar(nb, 128);
             // segsum: the diagonal blocks, then the rank-one row factors (the
@@ -262,16 +261,13 @@ __global__ void __launch_bounds__(kThreads, 1) ssd_split_agg_tc(const __grid_con
             }
             ptx::named_bar(nb, 128);
             // the product of the later chunks' totals (from the other group); as soon
-            // as every thread has read it (and the chunk's sums), the product that
-            // includes this chunk's total goes on to the earlier chunk's group, so the
-            // two groups' scaling work overlaps
+            // as every thread has read it, the product that includes this chunk's
+            // total goes on to the earlier chunk's group, so the two groups' scaling
+            // work overlaps
             agg_wait(sh, a, &sh.rdy[r & 1], j & 1, kWhereAggRdy);
             float R[K];
 #pragma unroll
-            for (int h = 0; h < K; ++h) {
-                R[h] = sh.rin[r & 1][h];
-                Ls[h] += (sh.lsum[X][h][0] + sh.lsum[X][h][1]) + (sh.lsum[X][h][2] + sh.lsum[X][h][3]);
-            }
+            for (int h = 0; h < K; ++h) R[h] = sh.rin[r & 1][h];
             const bool stop = ptx::named_bar_any(nb, 128, *(volatile int*)&sh.abort != 0);
             if (mt == 0 && r + 1 < nch) {
 #pragma unroll
@@ -285,16 +281,17 @@ __global__ void __launch_bounds__(kThreads, 1) ssd_split_agg_tc(const __grid_con
 #pragma unroll
             for (int h = 0; h < K; ++h) {
                 const float wgt = segsum_lin_suffix<4>(sh.seg[X][h], i) * R[h] * dtv[h];
+                const uint64_t wgt2 = ptx::f2_pack(wgt, wgt);
                 uint8_t* row = xs + h * kTileX;
                 uint4 v[8];   // the whole row's loads in flight before the first multiply
 #pragma unroll
                 for (int q = 0; q < 8; ++q) v[q] = *reinterpret_cast<const uint4*>(row + sw128_off(i, 8 * q));
 #pragma unroll
                 for (int q = 0; q < 8; ++q) {
-                    v[q].x = scale_pair(v[q].x, wgt);
-                    v[q].y = scale_pair(v[q].y, wgt);
-                    v[q].z = scale_pair(v[q].z, wgt);
-                    v[q].w = scale_pair(v[q].w, wgt);
+                    v[q].x = scale_pair(v[q].x, wgt2);
+                    v[q].y = scale_pair(v[q].y, wgt2);
+                    v[q].z = scale_pair(v[q].z, wgt2);
+                    v[q].w = scale_pair(v[q].w, wgt2);
                     *reinterpret_cast<uint4*>(row + sw128_off(i, 8 * q)) = v[q];
                 }
             }
@@ -303,9 +300,13 @@ __global__ void __launch_bounds__(kThreads, 1) ssd_split_agg_tc(const __grid_con
             if (lane == 0) ptx::mbar_arrive(&sh.ready[st]);
             if (stop) break;
         }
-        if (mt == 0) {
+        // the split's total log-decay: each thread's rows, then the warps' sums
 #pragma unroll
-            for (int h = 0; h < K; ++h) sh.lsgrp[X][h] = Ls[h];
+        for (int h = 0; h < K; ++h) {
+            float ls = Ls[h];
+#pragma unroll
+            for (int o = 16; o > 0; o >>= 1) ls += __shfl_xor_sync(0xffffffffu, ls, o);
+            if (lane == 0) sh.lsum[X][h][rb] = ls;
         }
         ptx::named_bar(kBarBoth, 256);
         if (X == 0) {
@@ -324,7 +325,8 @@ __global__ void __launch_bounds__(kThreads, 1) ssd_split_agg_tc(const __grid_con
                     uint32_t d0[32], d1[32];
                     ptx::tmem_load32x2(lane_addr + h * P, d0, lane_addr + h * P + 32, d1);
                     const size_t ws = ((size_t)b * a.H + h0 + h) * a.nsplit + s;
-                    const float lsum = sh.lsgrp[0][h] + sh.lsgrp[1][h];
+                    const float lsum = ((sh.lsum[0][h][0] + sh.lsum[0][h][1]) + (sh.lsum[0][h][2] + sh.lsum[0][h][3])) +
+                                       ((sh.lsum[1][h][0] + sh.lsum[1][h][1]) + (sh.lsum[1][h][2] + sh.lsum[1][h][3]));
                     float* out = a.ws_state + ws * PN + i;
                     // the first split starts from the caller's initial state
                     const float* init =
