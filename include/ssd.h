@@ -20,7 +20,9 @@
  * ("GPU Hierarchy Meets Structured Matrices", abstract: the split-sequence
  * algorithm; "Parallel Scan and Hardware-Aware SSM Kernels", "The scan": the
  * affine-step composition).  Packed documents (cu_seqlens) restart the state
- * at every document start (same page, "When it breaks").
+ * at every document start (same page, "When it breaks"): document d starts
+ * from initial_states[d] (or zero), which its first token decays like any
+ * carried state.
  *
  * Layouts (all row-major, contiguous, device memory, 16-byte aligned bases):
  *   x, y            (batch, seqlen, nheads, headdim)      dtype
@@ -29,7 +31,8 @@
  *   B, C            (batch, seqlen, ngroups, dstate)      dtype
  *   initial_states  (nstates, nheads, headdim, dstate)    fp32, optional (zeros)
  *   final_states    (nstates, nheads, headdim, dstate)    fp32, optional
- *   cu_seqlens      (ndocs + 1) int32, cu[0] = 0, cu[ndocs] = seqlen, optional
+ *   cu_seqlens      (ndocs + 1) int32, cu[0] = 0 < cu[1] < ... < cu[ndocs] = seqlen
+ *                   (no empty document), optional
  *   nstates = ndocs when cu_seqlens is given (then batch must be 1), else batch.
  *
  * Ownership: the caller owns every buffer; the library keeps no pointer past
@@ -253,9 +256,11 @@ SSD_API int ssd_check_status(void* workspace, void* stream);
  * kernel (1 stage free, 2 stage loaded, 3 mask ready, 4 output buffer free,
  * 5 state summary buffer free, 6 scaled-X tile ready, 7 chunk values free,
  * 8 state summary done, 9 C B^T done, 10 chunk values ready, 11 off-diagonal
- * output done, 12 drain of copies or MMAs in flight, 13 diagonal output done)
+ * output done, 12 drain of copies or MMAs in flight, 13 diagonal output done,
+ * 14 C init_d^T done, 15 state terms of a chunk with document starts ready)
  * or of the split-aggregate kernel (21 stage free, 22 stage loaded, 23 scaled
- * tile ready, 24 split contraction done, 25 drain of copies in flight). */
+ * tile ready, 24 split contraction done, 25 drain of copies in flight, 26 the
+ * other scaling group's decay product ready). */
 SSD_API int ssd_check_status_where(void* workspace, void* stream, uint32_t* where);
 
 /* Test aid for the device-side failure path: ssd_fwd() with an injected stall.

@@ -328,19 +328,25 @@ __global__ void __launch_bounds__(kThreads, 1) ssd_split_agg_tc(const __grid_con
                     const float lsum = ((sh.lsum[0][h][0] + sh.lsum[0][h][1]) + (sh.lsum[0][h][2] + sh.lsum[0][h][3])) +
                                        ((sh.lsum[1][h][0] + sh.lsum[1][h][1]) + (sh.lsum[1][h][2] + sh.lsum[1][h][3]));
                     float* out = a.ws_state + ws * PN + i;
-                    // the first split starts from the caller's initial state
+                    // the first split starts from the caller's initial state (packed
+                    // documents: the first document's, d = 0 = b; a later start in the
+                    // split makes its decay 2^{-inf} = 0)
                     const float* init =
-                        (!kDocs && s == 0 && a.init) ? a.init + ((size_t)b * a.H + h0 + h) * PN + i : nullptr;
-                    const float dec = init ? ex2_approx(lsum) : 0.f;
+                        (s == 0 && a.init) ? a.init + ((size_t)b * a.H + h0 + h) * PN + i : nullptr;
+                    if (init) {
+                        // (read-only loads, so that all of them are issued before the stores)
+                        const float dec = ex2_approx(lsum);
+#pragma unroll
+                        for (int p = 0; p < 32; ++p) {
+                            d0[p] = __float_as_uint(fmaf(dec, __ldg(init + (size_t)p * N), __uint_as_float(d0[p])));
+                            d1[p] = __float_as_uint(
+                                fmaf(dec, __ldg(init + (size_t)(p + 32) * N), __uint_as_float(d1[p])));
+                        }
+                    }
 #pragma unroll
                     for (int p = 0; p < 32; ++p) {
-                        float v0 = __uint_as_float(d0[p]), v1 = __uint_as_float(d1[p]);
-                        if (init) {
-                            v0 = fmaf(dec, init[(size_t)p * N], v0);
-                            v1 = fmaf(dec, init[(size_t)(p + 32) * N], v1);
-                        }
-                        out[(size_t)p * N] = v0;
-                        out[(size_t)(p + 32) * N] = v1;
+                        out[(size_t)p * N] = __uint_as_float(d0[p]);
+                        out[(size_t)(p + 32) * N] = __uint_as_float(d1[p]);
                     }
                     if (mt == 0) a.ws_tau[ws] = lsum * kLn2;
                 }

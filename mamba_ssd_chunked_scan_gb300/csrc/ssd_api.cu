@@ -118,12 +118,11 @@ int simt_chunk(const ssd_params_t* p) {
     return 0;
 }
 
-// The tcgen05 kernel covers the Mamba-2 head shape in bf16; packed documents
-// with their own initial states go to the SIMT kernel.
-bool use_tc(const ssd_params_t* p, bool has_init) {
+// The tcgen05 kernel covers the Mamba-2 head shape in bf16 (with or without
+// packed documents and initial states).
+bool use_tc(const ssd_params_t* p) {
     if (!tc_supported(p->headdim, p->dstate, p->chunk, p->dtype)) return false;
     if (p->seqlen >= ((int64_t)1 << 31) - 256) return false;   // token indices are 32-bit TMA coordinates
-    if (p->ndocs > 0 && has_init) return false;
     return true;
 }
 
@@ -259,10 +258,13 @@ int ssd_fwd_plan(const ssd_params_t* p, int has_init, int has_final, int* launch
     if (check_params(p) != SSD_OK) return -1;
     const int ns = plan_nsplit(p);
     TailPlan tp;
-    const bool tail = use_tc(p, has_init != 0) && plan_tail(p, &tp);
-    if (launches) *launches = (ns > 1 || tail) ? 3 : 1;
+    const bool tc = use_tc(p);
+    const bool tail = tc && plan_tail(p, &tp);
+    // aggregates (+ initial states of packed documents starting inside splits), composition, full pass
+    const bool doc_init = tc && p->ndocs > 0 && has_init;
+    if (launches) *launches = (ns > 1 || tail) ? (doc_init ? 4 : 3) : 1;
     if (nsplits) *nsplits = ns;
-    return use_tc(p, has_init != 0) ? 1 : 0;
+    return tc ? 1 : 0;
 }
 
 int ssd_workspace_init(void* workspace, size_t bytes, void* stream) {
@@ -357,7 +359,8 @@ int fwd_impl(const ssd_params_t* p, const void* x, const float* dt, const float*
     fastdiv_consts((uint32_t)p->nheads, &a.divH_m, &a.divH_l);
     fastdiv_consts((uint32_t)ns, &a.divS_m, &a.divS_l);
     fastdiv_consts((uint32_t)(p->nheads / p->ngroups), &a.divHG_m, &a.divHG_l);
-    const bool tc = use_tc(p, init != nullptr);
+    const bool tc = use_tc(p);
+    const bool doc_init = tc && cu && init;   // packed documents with initial states
     if (fi && !tc) return SSD_ERR_UNSUPPORTED;   // only the tensor-core kernel has device waits
     a.Q = tc ? p->chunk : simt_chunk(p);
     if (a.Q == 0) return SSD_ERR_UNSUPPORTED;
@@ -381,6 +384,7 @@ int fwd_impl(const ssd_params_t* p, const void* x, const float* dt, const float*
         a.mode = kModeAggregate;
         a.grid_units = (int64_t)tp.T * tp.m;
         if (launch(a) != cudaSuccess) return SSD_ERR_CUDA;
+        if (doc_init && timed(launch_doc_init_agg, a) != cudaSuccess) return SSD_ERR_CUDA;
         FwdArgs sa = a;   // the scan runs over T "rows" of m splits
         sa.batch = 1;
         sa.H = tp.T;
@@ -399,6 +403,7 @@ int fwd_impl(const ssd_params_t* p, const void* x, const float* dt, const float*
         a.mode = kModeAggregate;
         const bool agg_tc = tc && a.split_len >= (int64_t)kAggMinChunks * p->chunk;
         if ((agg_tc ? timed(launch_agg_tc, a) : launch(a)) != cudaSuccess) return SSD_ERR_CUDA;
+        if (doc_init && timed(launch_doc_init_agg, a) != cudaSuccess) return SSD_ERR_CUDA;
         if (timed(launch_split_scan, a) != cudaSuccess) return SSD_ERR_CUDA;
     }
     a.mode = kModeFull;

@@ -139,6 +139,9 @@ bool encode_4d(CUtensorMap* tm, const void* base, int64_t inner, int64_t mid, in
 size_t tc_smem_bytes();
 bool tc_supported(int P, int N, int Q, int dtype);
 cudaError_t launch_tc(const FwdArgs& a, cudaStream_t st);
+// adds the initial states of packed documents that start inside a split to the
+// split aggregates (after the aggregate pass, before their composition)
+cudaError_t launch_doc_init_agg(const FwdArgs& a, cudaStream_t st);
 int agg_heads_per_cta(int H, int G);
 cudaError_t launch_agg_tc(const FwdArgs& a, cudaStream_t st);
 cudaError_t launch_gate_norm(const GateNormArgs& a, cudaStream_t st);

@@ -58,8 +58,9 @@ constexpr uint32_t kTileC = 0, kTileB = 32768, kTileX = 65536, kStageBytes = 819
 constexpr uint32_t kXt = 2 * kStageBytes;    // scaled X for the state summary, two buffers
 constexpr uint32_t kSin = kXt + 2 * 16384;   // incoming state, bf16, (n rows, p)
 constexpr uint32_t kTiles = kSin + 16384;
-// TMEM columns: G/M/Ydiag [2] (G, then M in cols 0-63 and Ydiag in 64-127) | Yoff [2] | dS
-constexpr uint32_t kTmGM = 0, kTmYo = 256, kTmDS = 384, kTmCols = 512;
+// TMEM columns: G/M/Ydiag [2] (G, then M in cols 0-63 and Ydiag in 64-127) | Yoff [2] | dS |
+// C init_d^T (packed documents with initial states)
+constexpr uint32_t kTmGM = 0, kTmYo = 256, kTmDS = 384, kTmInit = 448, kTmCols = 512;
 constexpr float kLn2 = 0.6931471805599453f;
 constexpr int kBarMask0 = 1, kBarState = 3;  // named barriers: mask groups 1 and 2, state group 3
 
@@ -67,7 +68,7 @@ constexpr int kBarMask0 = 1, kBarState = 3;  // named barriers: mask groups 1 an
 enum : uint32_t {
     kWhereEmpty = 1, kWhereFull = 2, kWhereBarM = 3, kWhereYFree = 4, kWhereDsFree = 5, kWhereBarXt = 6,
     kWhereMetaFree = 7, kWhereBarDS = 8, kWhereBarG = 9, kWhereMetaFull = 10, kWhereBarY = 11,
-    kWhereDrain = 12, kWhereBarYd = 13
+    kWhereDrain = 12, kWhereBarYd = 13, kWhereBarInit = 14, kWhereBarFix = 15
 };
 
 // Per-chunk values handed from a mask group to the state group.
@@ -102,6 +103,13 @@ struct TcSmall {
     uint64_t dsFree;
     uint64_t metaFull[NMETA], metaFree[NMETA];
     uint64_t drain[4];
+    uint64_t barInit;              // C init_d^T of one document start is in TMEM
+    uint64_t barFix[2];            // the state group has rewritten the Yoff rows of a chunk
+    uint32_t startmask[4];         // per warp: rows where a document starts (state group)
+    uint32_t endmask[4];           // per warp: rows e < nv - 1 where a document ends (state group)
+    float segtot[4];               // per warp: log2-decay sum of the warp's last document segment
+    float qlast, qend;             // initial-state decay at the chunk's last row / at a document end
+    int dlast;                     // the document open at the chunk's last row, if it started in the chunk
     uint32_t tmem_base;
     int abort;
     int never;                     // stays 0: lets drain waits ignore the abort flag
@@ -170,41 +178,199 @@ __device__ __forceinline__ uint64_t desc_mn2(uint32_t base, int kk) {
     return ptx::sdesc_sw128(base + kk * 2048, 16384, 1024);
 }
 
-// Final states of packed documents that end at row e < nv - 1 of a chunk:
-//   S_e[p][n] = 2^{p_e} S_in[p][n] + sum_{j <= e} 2^{seg(e, j)} dt_j x_j[p] B_j[n]
-// (seg grown leftwards from the diagonal; -inf log-decays at document starts
-// zero the terms of earlier documents).  S_in is read from the bf16
-// incoming-state tile.  Rare path, kept out of line: one thread per state
-// column n = i, all 128 threads of the state group call it together.
-__device__ __noinline__ void doc_end_states(TcSmall& sh, const ChunkMeta& m, const uint8_t* stg,
-                                            const uint8_t* sin_tile, float* fin, int H, int h, int nv, int i) {
-    const uint8_t* xt = stg + kTileX;
-    const uint8_t* bt = stg + kTileB + (i >> 6) * 16384;
-    for (int e = 0; e < nv - 1; ++e) {
-        if (!(m.rowflag[e] & 2)) continue;
-        ptx::named_bar(kBarState, 128);
-        if (i == e) {
-            float r = 0.f;
-            for (int j = e; j >= 0; --j) {
-                sh.wv[j] = ex2_approx(r) * m.dtv[j];
-                r += m.ell[j];
-            }
+// Final state of a packed document that ends at row e < nv - 1 of a chunk:
+//   S_e = 2^{p_e} S_in + q_e init_d + D_e,   D_e^T = B^T X~,
+//   X~_j = w_j x_j,  w_j = 2^{seg(e, j)} dt_j for j <= e, else 0
+// (the chunk state summary's contraction with row e's decays in place of the
+// chunk end's; -inf log-decays at document starts zero the terms of earlier
+// documents, and 2^{p_e} = 0 once one started in the chunk).  This computes
+// D_e on the tensor cores: seg(e, j) = sum_{k=j+1..e} l_k from a reverse scan
+// over the rows (no prefix subtraction), X~ staged as bf16 in the
+// incoming-state tile (which Yoff has finished reading), one UMMA into the
+// spare TMEM columns (lane n, column p).  It also leaves in sh.qend the decay
+// q_e = 2^{seg(e, st) + l_st} of d's initial state when d started in this
+// chunk at row st and the call has initial states, else 0; the caller adds
+// 2^{p_e} S_in (its fp32 registers) and q_e init_d.  Rare path, kept out of
+// line: all 128 threads of the state group call it together (thread i = row i).
+__device__ __noinline__ void doc_end_mma(TcSmall& sh, const FwdArgs& a, const ChunkMeta& m, const uint8_t* stg,
+                                         uint8_t* sin_tile, uint32_t tb, int e, float A2, int i, int& init_cnt) {
+    constexpr uint32_t idDS = ptx::idesc_bf16(128, 64, 1, 1);
+    const int lane = i & 31, rb = i >> 5;
+    // reverse inclusive scan of v_j = l_{j+1} (j < e): s_j = sum_{k=j+1..e} l_k
+    float v = (i < e) ? m.ell[i + 1] : 0.f;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+        const float t = __shfl_down_sync(0xffffffffu, v, o);
+        if (lane + o < 32) v = v + t;
+    }
+    if (lane == 0) sh.segtot[rb] = v;
+    if (i == 0) sh.qend = 0.f;
+    ptx::named_bar(kBarState, 128);
+    for (int r = rb + 1; r < 4; ++r) v = v + sh.segtot[r];
+    if (a.init && i <= e && (m.rowflag[i] & 1) && m.rowdoc[i] == m.rowdoc[e])
+        sh.qend = ex2_approx(v + m.dtv[i] * A2);
+    const float w = (i <= e) ? ex2_approx(v) * m.dtv[i] : 0.f;
+    {
+        // X~ row i = w_i x_i, in the layout of the scaled-X operand
+        const uint8_t* xrow = stg + kTileX;
+        const uint64_t w2 = ptx::f2_pack(w, w);
+#pragma unroll
+        for (int q = 0; q < 8; ++q) {
+            const uint4 xv = *reinterpret_cast<const uint4*>(xrow + sw128_off(i, 8 * q));
+            uint4 o;
+            o.x = pack_bf16_2(ptx::f2_mul(ptx::f2_pack(bf16lo(xv.x), bf16hi(xv.x)), w2));
+            o.y = pack_bf16_2(ptx::f2_mul(ptx::f2_pack(bf16lo(xv.y), bf16hi(xv.y)), w2));
+            o.z = pack_bf16_2(ptx::f2_mul(ptx::f2_pack(bf16lo(xv.z), bf16hi(xv.z)), w2));
+            o.w = pack_bf16_2(ptx::f2_mul(ptx::f2_pack(bf16lo(xv.w), bf16hi(xv.w)), w2));
+            *reinterpret_cast<uint4*>(sin_tile + sw128_off(i, 8 * q)) = o;
         }
-        ptx::named_bar(kBarState, 128);
-        const float pe = m.pexp[e];
-        float* fo = fin + ((size_t)m.rowdoc[e] * H + h) * (size_t)(P * N) + i;
+        ptx::fence_proxy_async();
+    }
+    ptx::named_bar(kBarState, 128);
+    if (i == 0) {
+        ptx::tc_fence_after();
+        const uint32_t bt = ptx::smem_u32(stg + kTileB), xt = ptx::smem_u32(sin_tile);
 #pragma unroll 1
-        for (int p = 0; p < P; ++p) {
-            float acc = pe * __bfloat162float(*reinterpret_cast<const __nv_bfloat16*>(sin_tile + sw128_off(i, p)));
-#pragma unroll 4
-            for (int j = 0; j <= e; ++j) {
-                const float xv = __bfloat162float(*reinterpret_cast<const __nv_bfloat16*>(xt + sw128_off(j, p)));
-                const float bv = __bfloat162float(*reinterpret_cast<const __nv_bfloat16*>(bt + sw128_off(j, i & 63)));
-                acc = fmaf(sh.wv[j] * xv, bv, acc);
-            }
-            fo[(size_t)p * N] = acc;
+        for (int kk = 0; kk < 8; ++kk) ptx::mma_ss(tb + kTmInit, desc_mn2(bt, kk), desc_mn1(xt, kk), idDS, kk > 0);
+        ptx::mma_commit(&sh.barInit);
+    }
+    wait_or_fail(sh, a, &sh.barInit, (uint32_t)(init_cnt & 1), kWhereBarInit);
+    ++init_cnt;
+    ptx::tc_fence_after();
+}
+
+// Rows of a chunk in which documents with initial states start.  Row i of
+// document d, which started at row st of this chunk, takes its state term
+// from d's initial state, decayed from the start:
+//   q_i C_i init_d^T,   q_i = 2^{sum_{k=st..i} l_k}
+// (the start token applies its own decay l_st: h_st = a_st init_d + dt_st
+// x_st B_st^T), where the carried state's term 2^{p_i} C_i S_in^T is 0 (the
+// -inf log-decay at st is in p_i).  The state group rewrites the chunk's Yoff
+// accumulator rows in TMEM to the finished state terms: 2^{p_i} Yoff_i for
+// the rows before the first start, q_i C_i init_d^T after it (one UMMA per
+// start into the spare TMEM columns, with init_d staged as the bf16 operand
+// in the incoming-state tile, which Yoff has finished reading); the
+// epilogue then adds them unscaled.  q_i comes from a segmented scan of the
+// log2-decays that restarts at each start (no prefix subtraction).  Also
+// leaves in sh.qlast / sh.dlast the decay and document of the initial state
+// that reaches the chunk's end (dlast = -1: none).  Rare path, kept out of
+// line: all 128 threads of the state group call it together (thread i =
+// chunk row i = TMEM lane i).
+__device__ __noinline__ void doc_start_rows(TcSmall& sh, const FwdArgs& a, const ChunkMeta& m, uint32_t ctile,
+                                            uint8_t* sin_tile, uint32_t tb, int X, float A2, int h, int nv, int i,
+                                            int& init_cnt) {
+    constexpr uint32_t idYo = ptx::idesc_bf16(128, 64, 0, 1);
+    const int lane = i & 31, rb = i >> 5;
+    const uint32_t lane_off = (uint32_t)(32 * rb) << 16;
+    const uint32_t yo = tb + lane_off + kTmYo + 64 * X, scr = tb + lane_off + kTmInit;
+    // (the caller has waited for this chunk's Yoff, which has read the incoming-state tile)
+    // segmented inclusive scan of l within the warp, restarting at starts
+    const bool st_i = i < nv && (m.rowflag[i] & 1);
+    float v = (i < nv) ? (st_i ? m.dtv[i] * A2 : m.ell[i]) : 0.f;
+    bool f = st_i;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+        const float vu = __shfl_up_sync(0xffffffffu, v, o);
+        const int fu = __shfl_up_sync(0xffffffffu, (int)f, o);
+        if (lane >= o && !f) {
+            v = vu + v;
+            f = fu != 0;
         }
     }
+    const uint32_t smask = __ballot_sync(0xffffffffu, st_i);
+    if (lane == 31) sh.segtot[rb] = v;
+    if (lane == 0) sh.startmask[rb] = smask;
+    ptx::named_bar(kBarState, 128);
+    // rows whose segment began in an earlier warp carry the later warps' sums
+    bool has = f;
+    if (!f) {
+        for (int r = rb - 1; r >= 0; --r) {
+            v = sh.segtot[r] + v;
+            if (sh.startmask[r]) {
+                has = true;
+                break;
+            }
+        }
+    }
+    const float q = has ? ex2_approx(v) : 0.f;
+    // rows before the first start: 2^{p_i} Yoff_i (rows after it are rewritten below)
+    {
+        const float pe = m.pexp[i];
+#pragma unroll 1
+        for (int hf = 0; hf < 2; ++hf) {
+            uint32_t r[32], lo[16], hi[16];
+            ptx::tmem_load32(yo + 32 * hf, r);
+#pragma unroll
+            for (int k = 0; k < 16; ++k) {
+                lo[k] = __float_as_uint(__uint_as_float(r[k]) * pe);
+                hi[k] = __float_as_uint(__uint_as_float(r[16 + k]) * pe);
+            }
+            ptx::tmem_st16(yo + 32 * hf, lo);
+            ptx::tmem_st16(yo + 32 * hf + 16, hi);
+        }
+        ptx::tmem_st_wait();
+    }
+    // one UMMA C init_d^T per document start, its rows merged into Yoff
+#pragma unroll 1
+    for (int w = 0; w < 4; ++w) {
+        uint32_t mk = sh.startmask[w];
+        while (mk) {
+            const int st = 32 * w + __ffs(mk) - 1;
+            mk &= mk - 1;
+            const int d = m.rowdoc[st];
+            // init_d as the (n, p) bf16 operand; thread i writes state column n = i
+            // (all 64 loads in flight at once)
+            const float* src = a.init + ((size_t)d * a.H + h) * (size_t)(P * N) + i;
+            float iv[P];
+#pragma unroll
+            for (int p = 0; p < P; ++p) iv[p] = __ldg(src + (size_t)p * N);
+#pragma unroll
+            for (int q8 = 0; q8 < 8; ++q8)
+                *reinterpret_cast<uint4*>(sin_tile + sw128_off(i, 8 * q8)) =
+                    make_uint4(pack_bf16(iv[8 * q8], iv[8 * q8 + 1]), pack_bf16(iv[8 * q8 + 2], iv[8 * q8 + 3]),
+                               pack_bf16(iv[8 * q8 + 4], iv[8 * q8 + 5]), pack_bf16(iv[8 * q8 + 6], iv[8 * q8 + 7]));
+            ptx::fence_proxy_async();
+            ptx::named_bar(kBarState, 128);
+            if (i == 0) {
+                ptx::tc_fence_after();
+                const uint32_t sin = ptx::smem_u32(sin_tile);
+#pragma unroll 1
+                for (int kk = 0; kk < 8; ++kk)
+                    ptx::mma_ss(tb + kTmInit, desc_k(ctile, kk), desc_mn1(sin, kk), idYo, kk > 0);
+                ptx::mma_commit(&sh.barInit);
+            }
+            wait_or_fail(sh, a, &sh.barInit, (uint32_t)(init_cnt & 1), kWhereBarInit);
+            ++init_cnt;
+            ptx::tc_fence_after();
+            const bool mine = has && i < nv && m.rowdoc[i] == d;
+            if (__any_sync(0xffffffffu, mine)) {
+#pragma unroll 1
+                for (int hf = 0; hf < 2; ++hf) {
+                    uint32_t sr[32], yr[32], lo[16], hi[16];
+                    ptx::tmem_load32x2(scr + 32 * hf, sr, yo + 32 * hf, yr);
+#pragma unroll
+                    for (int k = 0; k < 16; ++k) {
+                        lo[k] = mine ? __float_as_uint(q * __uint_as_float(sr[k])) : yr[k];
+                        hi[k] = mine ? __float_as_uint(q * __uint_as_float(sr[16 + k])) : yr[16 + k];
+                    }
+                    ptx::tmem_st16(yo + 32 * hf, lo);
+                    ptx::tmem_st16(yo + 32 * hf + 16, hi);
+                }
+                ptx::tmem_st_wait();
+            }
+            // the spare columns and the operand tile are free for the next start
+            ptx::tc_fence_before();
+            ptx::named_bar(kBarState, 128);
+        }
+    }
+    if (i == nv - 1) {
+        sh.dlast = has ? m.rowdoc[i] : -1;
+        sh.qlast = q;
+    }
+    ptx::tc_fence_before();
+    __syncwarp();
+    if (lane == 0) ptx::mbar_arrive(&sh.barFix[X]);
+    ptx::named_bar(kBarState, 128);   // dlast / qlast visible to the group
 }
 
 // A unit: batch row b, split s, head h (heads of one (row, split) are adjacent
@@ -349,6 +515,9 @@ __global__ void __launch_bounds__(kThreads, 1) ssd_chunk_tc(const __grid_constan
             ptx::mbar_init(&sh.metaFree[i], 1);
         }
         for (int i = 0; i < 4; ++i) ptx::mbar_init(&sh.drain[i], 1);
+        ptx::mbar_init(&sh.barInit, 1);
+        ptx::mbar_init(&sh.barFix[0], 4);
+        ptx::mbar_init(&sh.barFix[1], 4);
         sh.abort = 0;
         sh.never = 0;
         ptx::mbar_fence_init();
@@ -488,6 +657,7 @@ __global__ void __launch_bounds__(kThreads, 1) ssd_chunk_tc(const __grid_constan
         if (X) cur.next(a, nunits);
         float dt_next = load_dt(cur);
         int unit_prev = -1;
+        int nfix = 0;                             // chunks of this group whose Yoff rows the state group rewrote
         float A2 = 0.f, Dh = 0.f;
         for (int c = X; c < nch; c += 2) {
             const int j = c >> 1, mb = c % NMETA;
@@ -517,6 +687,10 @@ __global__ void __launch_bounds__(kThreads, 1) ssd_chunk_tc(const __grid_constan
                     doc = d;
                     if (d > 0 && __ldg(a.cu + d) == t + i) flag |= 1;
                     if (t + i + 1 == __ldg(a.cu + d + 1)) flag |= 2;
+                    // the document's initial state, which the state group reads for this
+                    // chunk, on its way to L2 a chunk ahead
+                    if (full_mode && (flag & 1) && a.init)
+                        ptx::bulk_prefetch_l2(a.init + ((size_t)d * a.H + h) * (P * N), P * N * 4);
                 } else if (t + i == a.L - 1) {
                     flag |= 2;
                 }
@@ -535,7 +709,13 @@ __global__ void __launch_bounds__(kThreads, 1) ssd_chunk_tc(const __grid_constan
                 for (int o = 16; o > 0; o >>= 1) ls += __shfl_xor_sync(0xffffffffu, ls, o);
                 if (lane == 0) ms.totLog[rb] = ls;
             }
-            ptx::named_bar(nb, 128);
+            // packed documents with initial states: when one starts in this chunk, the
+            // state group rewrites the chunk's Yoff rows, which the epilogue adds unscaled
+            bool fix = false;
+            if (kDocs && full_mode)
+                fix = ptx::named_bar_any(nb, 128, (flag & 1) != 0) && a.init != nullptr;
+            else
+                ptx::named_bar(nb, 128);
             if (kDocs && mt == Q - 1) ms.doc_cursor = doc;   // later chunks start in (or after) this document
             SegsumLinRow<4> row;
             segsum_lin_phase1<4>(ms.seg, row, rb, lane);   // the diagonal 1-SS block
@@ -644,6 +824,10 @@ __global__ void __launch_bounds__(kThreads, 1) ssd_chunk_tc(const __grid_constan
                 // is done) and written by one TMA store (rows past L are clipped).
                 wait_or_fail(sh, a, &sh.barYd[X], j & 1, kWhereBarYd);
                 wait_or_fail(sh, a, &sh.barY[X], j & 1, kWhereBarY);
+                if (fix) {
+                    wait_or_fail(sh, a, &sh.barFix[X], nfix & 1, kWhereBarFix);
+                    ++nfix;
+                }
                 wait_or_fail(sh, a, &sh.barDS[X], j & 1, kWhereBarDS);
                 ptx::tc_fence_after();
                 const uint32_t yd_addr = lane_addr + kTmGM + 128 * X + 64;
@@ -659,7 +843,8 @@ __global__ void __launch_bounds__(kThreads, 1) ssd_chunk_tc(const __grid_constan
                         if (lane == 0) ptx::mbar_arrive(&sh.yFree[X]);
                     }
                     uint32_t ow[16];
-                    const uint64_t pe2 = ptx::f2_pack(pe, pe);
+                    const float ps = fix ? 1.f : pe;
+                    const uint64_t pe2 = ptx::f2_pack(ps, ps);
 #pragma unroll
                     for (int e = 0; e < 16; ++e)
                         ow[e] = pack_bf16_2(ptx::f2_fma(
@@ -695,7 +880,7 @@ __global__ void __launch_bounds__(kThreads, 1) ssd_chunk_tc(const __grid_constan
         auto enter_state = [&](const Unit& un) {
             const float* src = nullptr;
             if (full_mode && a.nsplit > 1 && un.s > 0) src = a.ws_state + (size_t)un.ws * PN;
-            else if (!kDocs && un.s == 0 && a.init) src = a.init + ((size_t)un.b * a.H + un.h) * PN;
+            else if (un.s == 0 && a.init) src = a.init + ((size_t)un.b * a.H + un.h) * PN;   // (documents: d = 0 = b)
 #pragma unroll
             for (int p = 0; p < P; ++p) S[p] = src ? src[(size_t)p * N + i] : 0.f;
         };
@@ -738,6 +923,7 @@ __global__ void __launch_bounds__(kThreads, 1) ssd_chunk_tc(const __grid_constan
             if (mt == 0) issue_yoff(0);
         }
         float tau_split = 0.f;
+        int init_cnt = 0;                         // UMMAs C init_d^T issued (packed documents with initial states)
         for (int c = 0; c < nch; ++c) {
             const int X = c & 1, j = c >> 1, mb = c % NMETA;
             uint8_t* stg = sm + X * kStageBytes;
@@ -747,19 +933,66 @@ __global__ void __launch_bounds__(kThreads, 1) ssd_chunk_tc(const __grid_constan
             const bool unit_end = cs.c == cs.un.nch - 1;
             const bool meta_ok = wait_or_fail(sh, a, &sh.metaFull[mb], (c / NMETA) & 1, kWhereMetaFull);
             const ChunkMeta& m = sh.meta[mb];
-            // ---- packed documents that end inside this chunk: their final states
-            if (full_mode && kDocs && a.fin) {
-                bool any = false;
-                for (int e = 0; e < nv - 1; ++e) any |= (m.rowflag[e] & 2) != 0;
+            // ---- packed documents: final states of those that end inside this chunk,
+            // and the state terms of the rows of those that start in it
+            bool fix = false;
+            if (full_mode && kDocs && (a.fin || a.init)) {
+                const int fl = m.rowflag[i];       // 0 past the chunk's last row
+                const float A2 = a.A[h] * kLog2e;
+                const bool end_row = i < nv - 1 && (fl & 2);
                 // agreed by the whole group, and only on chunk values that are
-                // complete: the branch holds barriers, and after a wait that ran
+                // complete: the branches hold barriers, and after a wait that ran
                 // out the values may still be changing
                 const bool stale = ptx::named_bar_any(kBarState, 128, !meta_ok);
-                any = ptx::named_bar_any(kBarState, 128, any) && !stale;
-                if (any) {
-                    wait_or_fail(sh, a, &sh.full[X], j & 1, kWhereFull);
-                    doc_end_states(sh, m, stg, sm + kSin, a.fin, a.H, h, nv, i);
+                const bool any_end = ptx::named_bar_any(kBarState, 128, end_row) && !stale && a.fin != nullptr;
+                fix = ptx::named_bar_any(kBarState, 128, (fl & 1) != 0) && !stale && a.init != nullptr;
+                if (any_end || fix) {
+                    // Yoff(c) is complete: the incoming-state tile and the spare TMEM
+                    // columns are free for the rare paths below
+                    wait_or_fail(sh, a, &sh.barY[X], j & 1, kWhereBarY);
+                    ptx::tc_fence_after();
                 }
+                if (any_end) {
+                    wait_or_fail(sh, a, &sh.full[X], j & 1, kWhereFull);   // the chunk's x and B
+                    const uint32_t emask = __ballot_sync(0xffffffffu, end_row);
+                    if (lane == 0) sh.endmask[rb] = emask;
+                    ptx::named_bar(kBarState, 128);
+#pragma unroll 1
+                    for (int w = 0; w < 4; ++w) {
+                        uint32_t mk = sh.endmask[w];
+                        while (mk) {
+                            const int e = 32 * w + __ffs(mk) - 1;
+                            mk &= mk - 1;
+                            doc_end_mma(sh, a, m, stg, sm + kSin, tb, e, A2, i, init_cnt);
+                            uint32_t d0[32], d1[32];
+                            ptx::tmem_load32x2(lane_addr + kTmInit, d0, lane_addr + kTmInit + 32, d1);
+                            const float pe = m.pexp[e], qe = sh.qend;
+                            const size_t so = ((size_t)m.rowdoc[e] * a.H + h) * PN + i;
+                            float* fo = a.fin + so;
+                            if (qe != 0.f) {
+                                const float* src = a.init + so;
+#pragma unroll
+                                for (int p = 0; p < 32; ++p) {
+                                    fo[(size_t)p * N] = fmaf(qe, __ldg(src + (size_t)p * N),
+                                                             fmaf(pe, S[p], __uint_as_float(d0[p])));
+                                    fo[(size_t)(p + 32) * N] = fmaf(qe, __ldg(src + (size_t)(p + 32) * N),
+                                                                    fmaf(pe, S[p + 32], __uint_as_float(d1[p])));
+                                }
+                            } else {
+#pragma unroll
+                                for (int p = 0; p < 32; ++p) {
+                                    fo[(size_t)p * N] = fmaf(pe, S[p], __uint_as_float(d0[p]));
+                                    fo[(size_t)(p + 32) * N] = fmaf(pe, S[p + 32], __uint_as_float(d1[p]));
+                                }
+                            }
+                            // the spare TMEM columns and the operand tile are free again
+                            ptx::tc_fence_before();
+                            ptx::named_bar(kBarState, 128);
+                        }
+                    }
+                }
+                if (fix)
+                    doc_start_rows(sh, a, m, ptx::smem_u32(stg + kTileC), sm + kSin, tb, X, A2, h, nv, i, init_cnt);
             }
             // ---- state update: S = 2^tau S + dS (TMEM lane = state column n)
             wait_or_fail(sh, a, &sh.barDS[X], j & 1, kWhereBarDS);
@@ -783,6 +1016,13 @@ __global__ void __launch_bounds__(kThreads, 1) ssd_chunk_tc(const __grid_constan
                         ptx::f2_pack(__uint_as_float(ds1[q]), __uint_as_float(ds1[q + 1])));
                     ptx::f2_unpack(r1, S[32 + q], S[33 + q]);
                 }
+            }
+            if (fix && sh.dlast >= 0) {
+                // the initial state of the document open at the chunk's end, which started in it
+                const float ql = sh.qlast;
+                const float* src = a.init + ((size_t)sh.dlast * a.H + h) * PN + i;
+#pragma unroll
+                for (int p = 0; p < P; ++p) S[p] = fmaf(ql, __ldg(src + (size_t)p * N), S[p]);
             }
             if (full_mode && a.fin && (m.rowflag[nv - 1] & 2)) {
                 float* fo = a.fin + ((size_t)m.rowdoc[nv - 1] * a.H + h) * PN + i;
@@ -823,7 +1063,60 @@ __global__ void __launch_bounds__(kThreads, 1) ssd_chunk_tc(const __grid_constan
     if (warp == 1) ptx::tmem_dealloc(tb, kTmCols);
 }
 
+// Split aggregates of packed documents with initial states.  The aggregate
+// passes start each split from zero (the first split from the first
+// document's initial state), so the initial state of a document d > 0 that
+// starts inside split s, at token st, and is still open at the split's end t1
+// is added here:
+//   S_s += exp(A_h sum_{t=st..t1-1} dt_t) init_d
+// (the start token applies its own decay).  The split's total decay is
+// already -inf there (the start resets the state).  One CTA per aggregate
+// unit; dt is read with the heads' stride (neighbouring heads' CTAs share
+// its sectors in L2).
+constexpr int kDocInitThreads = 128;
+
+__global__ void __launch_bounds__(kDocInitThreads) ssd_doc_init_agg(const FwdArgs a) {
+    __shared__ float part[kDocInitThreads / 32];
+    const Unit un = unit_at<false>(a, blockIdx.x);
+    if (un.s == (int)a.nsplit - 1) return;   // the last split's aggregate is never composed
+    const int d = find_doc_tc(a.cu, a.ndocs, un.t1 - 1);
+    const int st = __ldg(a.cu + d);
+    if (d == 0 || st < un.t0) return;       // no document starts inside the split
+    float sum = 0.f;
+#pragma unroll 8
+    for (int t = st + (int)threadIdx.x; t < un.t1; t += kDocInitThreads)
+        sum += __ldg(a.dt + (size_t)t * a.H + un.h);   // packed documents: batch 1
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) sum += __shfl_xor_sync(0xffffffffu, sum, o);
+    if ((threadIdx.x & 31) == 0) part[threadIdx.x >> 5] = sum;
+    __syncthreads();
+    const float tot = (part[0] + part[1]) + (part[2] + part[3]);
+    const float dec = expf(__ldg(a.A + un.h) * tot);
+    constexpr int PN4 = P * N / 4, kPer = PN4 / kDocInitThreads;
+    float4* S = reinterpret_cast<float4*>(a.ws_state) + (size_t)un.ws * PN4 + threadIdx.x;
+    const float4* I = reinterpret_cast<const float4*>(a.init) + ((size_t)d * a.H + un.h) * PN4 + threadIdx.x;
+    float4 v[kPer], w[kPer];
+#pragma unroll
+    for (int k = 0; k < kPer; ++k) {   // every load in flight before the first store
+        v[k] = S[k * kDocInitThreads];
+        w[k] = __ldg(I + k * kDocInitThreads);
+    }
+#pragma unroll
+    for (int k = 0; k < kPer; ++k)
+        S[k * kDocInitThreads] = make_float4(fmaf(dec, w[k].x, v[k].x), fmaf(dec, w[k].y, v[k].y),
+                                             fmaf(dec, w[k].z, v[k].z), fmaf(dec, w[k].w, v[k].w));
+}
+static_assert(P * N / 4 % kDocInitThreads == 0, "whole float4 vectors per thread");
+static_assert(kDocInitThreads == 128, "the reduction above sums four warps");
+
 }  // namespace
+
+cudaError_t launch_doc_init_agg(const FwdArgs& a, cudaStream_t st) {
+    const int64_t grid = a.grid_units > 0 ? a.grid_units : a.batch * a.H * a.nsplit;
+    if (grid <= 0 || !a.cu || !a.init) return cudaSuccess;
+    ssd_doc_init_agg<<<(unsigned)grid, kDocInitThreads, 0, st>>>(a);
+    return cudaGetLastError();
+}
 
 static PFN_cuTensorMapEncodeTiled_v12000 get_encode() {
     static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;

@@ -100,6 +100,18 @@ def wave_fill(units, sms=152):
     return units / (-(-units // sms) * sms)
 
 
+def test_plan_packed_documents_with_init_states(L):
+    # the bf16 Mamba-2 head shape runs packed documents with initial states on the
+    # tensor-core kernel; a split plan adds one launch (the documents' initial states
+    # in the split aggregates, before their composition)
+    p = params(L, batch=1, seqlen=4096, nheads=8, split_len=1024, ndocs=5)
+    assert L.plan(p, True, True) == (1, 4, 4)
+    assert L.plan(p, False, True) == (1, 3, 4)
+    assert L.plan(params(L, batch=1, seqlen=4096, nheads=8, split_len=4096, ndocs=5), True, True) == (1, 1, 1)
+    # fp32 stays on the SIMT kernel
+    assert L.plan(params(L, batch=1, seqlen=4096, nheads=8, split_len=1024, ndocs=5, dtype=0), True, True)[0] == 0
+
+
 @pytest.mark.parametrize("batch,seqlen,nheads,want", [
     (1, 32768, 48, 6),     # packed varlen config: 7 splits would run 3 waves, 6 fill 2 to 95 %
     (1, 16384, 64, 7),     # 448 units, 98 % of 3 waves

@@ -95,6 +95,46 @@ def test_bf16_varlen_edges(split, init):
     check(p, split_len=split)
 
 
+@pytest.mark.parametrize("decay", ["slow", "fast"])
+@pytest.mark.parametrize("nheads", [3, 4])
+@pytest.mark.parametrize("split", [0, 256, 512])
+def test_bf16_packed_documents_with_init_states(nheads, split, decay):
+    # every document brings its own initial state, on the tensor-core kernel: several
+    # documents start inside one chunk (lengths 1 to 5), others on a chunk start, on a
+    # split start (splits of 2 chunks take the full kernel's aggregate mode, of 4 chunks
+    # the split-aggregate kernel), or run over several splits.  "slow": per-token decay
+    # near 0.98, so the initial states' decayed terms carry most of y over tens of
+    # tokens and reach the final states; "fast": the packed-varlen stress decays
+    lens = [5, 1, 2, 40, 3, 77, 128, 300, 17, 129, 256, 1, 600, 4, 130]
+    dist = dict(dt_dist="loguniform", A_dist="exp") if decay == "slow" else dict(dt_dist="softplus_n22")
+    p = synth.make_problem(batch=1, seqlen=sum(lens), nheads=nheads, headdim=64, dstate=128, ngroups=1,
+                           chunk=128, dtype="bf16", seed=48, doc_lengths=lens, init_std=1.0, **dist)
+    check(p, split_len=split)
+    import mamba_ssd_chunked_scan_gb300 as ssd
+    f = ssd.SSDForward(1, p.seqlen, nheads, 64, 128, 1, 128, split, p.ndocs)
+    fam, launches, ns = f.plan(True, True)
+    assert fam == 1 and launches == (4 if ns > 1 else 1)
+
+
+def test_varlen_init_no_leakage():
+    """Changing the initial states of the other documents leaves a target
+    document's y and final state bit-identical."""
+    lens = [70, 200, 77, 300]
+    p = synth.make_problem(batch=1, seqlen=sum(lens), nheads=2, headdim=64, dstate=128, ngroups=1,
+                           chunk=128, dtype="bf16", seed=62, doc_lengths=lens, init_std=0.5, A_dist="exp")
+    y1, f1, _ = run(p, split_len=128)
+    q = synth.SSDProblem(**{k: (v.copy() if isinstance(v, np.ndarray) else v) for k, v in vars(p).items()})
+    q.initial_states[[0, 2, 3]] *= -3.0
+    y2, f2, _ = run(q, split_len=128)
+    a, b, c = int(p.cu_seqlens[1]), int(p.cu_seqlens[2]), int(p.cu_seqlens[3])
+    assert np.array_equal(y1[:, a:b], y2[:, a:b])
+    assert np.array_equal(f1[1], f2[1])
+    # the changed initial states do reach their own documents
+    assert not np.array_equal(y1[:, :a], y2[:, :a])
+    assert not np.array_equal(y1[:, c], y2[:, c])
+    assert not np.array_equal(f1[3], f2[3])
+
+
 def test_fp32_varlen_with_init():
     lens = [3, 60, 64, 65, 1, 40]
     p = synth.make_problem(batch=1, seqlen=sum(lens), nheads=2, headdim=16, dstate=16, ngroups=1,

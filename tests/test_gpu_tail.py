@@ -26,7 +26,7 @@ def sm_count():
 ONE_SPLIT = 1 << 16   # split_len >= seqlen: one split (the automatic plan would split these sizes)
 
 
-def check(p):
+def check(p, launches_expected=3):
     y_o, f_o = oracle.ssd_recurrence(p, want_final=True)
     for _ in range(2):
         y_g, f_g, f = run(p, want_final=True, split_len=ONE_SPLIT)
@@ -35,7 +35,7 @@ def check(p):
         assert ey <= TOL["bf16"], f"y err {ey:.3e}"
         assert ef <= TOL["bf16"], f"final state err {ef:.3e}"
     fam, launches, ns = f.plan(p.initial_states is not None, True)
-    assert fam == 1 and ns == 1 and launches == 3   # the plan is in use
+    assert fam == 1 and ns == 1 and launches == launches_expected   # the plan is in use
 
 
 @pytest.mark.parametrize("seqlen", [1024, 1000 + 37])
@@ -54,3 +54,13 @@ def test_tail_units_packed_documents():
     p = synth.make_problem(batch=1, seqlen=sum(lens), nheads=H, headdim=64, dstate=128, ngroups=1,
                            chunk=128, dtype="bf16", seed=103, doc_lengths=lens)
     check(p)
+
+
+def test_tail_units_packed_documents_with_init_states():
+    # documents with their own initial states, starting inside and at the edges of
+    # the cut units' pieces (their aggregates then take the initial states too)
+    lens = [3, 300, 128, 1, 257, 90, 500]
+    H = sm_count() + 5
+    p = synth.make_problem(batch=1, seqlen=sum(lens), nheads=H, headdim=64, dstate=128, ngroups=1,
+                           chunk=128, dtype="bf16", seed=104, doc_lengths=lens, init_std=1.0)
+    check(p, launches_expected=4)
