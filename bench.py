@@ -2,7 +2,7 @@
 """Benchmark of the SSD forward pass (one JSON line on rank 0).
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
-                    [--workload 27b|sweep:B:L:S|long|varlen|tiny|decode[:B]|bwd[:B]|gatenorm]
+                    [--workload 27b|sweep:B:L:S|long|varlen|varlen_states|tiny|decode[:B]|bwd[:B]|gatenorm]
 
 A step is one ssd_fwd call over one batch of the workload.  The default is
 the largest single-GPU configuration, one 65,536-token sequence with 32 heads
@@ -82,6 +82,8 @@ def workload(name: str):
         return synth.config_long()
     if name == "varlen":
         return synth.config_varlen()
+    if name == "varlen_states":
+        return synth.config_varlen(init_std=0.2)
     if name.startswith("sweep"):
         _, b, L, s = name.split(":")
         return synth.config_sweep(int(b), int(L), int(s))
@@ -89,10 +91,15 @@ def workload(name: str):
 
 
 def compulsory_bytes(p) -> int:
-    """x + dt + B + C + y: the bytes the operator must move at least once."""
+    """x + dt + B + C + y, and with initial states also those and the final
+    states (which the bench then asks for): the bytes the operator must move
+    at least once."""
     e = 2 if p.dtype == "bf16" else 4
     T = p.batch * p.seqlen
-    return T * (2 * p.nheads * p.headdim * e + p.nheads * 4 + 2 * p.ngroups * p.dstate * e)
+    nb = T * (2 * p.nheads * p.headdim * e + p.nheads * 4 + 2 * p.ngroups * p.dstate * e)
+    if p.initial_states is not None:
+        nb += 2 * p.nstates * p.nheads * p.headdim * p.dstate * 4
+    return nb
 
 
 def decode_bytes(p) -> int:
@@ -773,6 +780,7 @@ def sweep_points():
         for sc in (1, 4, 16):
             pts.append((f"sweep:{b}:{L}:{sc}", lambda b=b, L=L, sc=sc: synth.config_sweep(b, L, sc)))
     pts.append(("varlen", synth.config_varlen))
+    pts.append(("varlen_states", lambda: synth.config_varlen(init_std=0.2)))
     return pts
 
 
@@ -784,7 +792,9 @@ def oracle_rate(p, seconds=2.0, max_tokens=16384):
     q = synth.SSDProblem(1, T, p.nheads, p.headdim, p.dstate, p.ngroups, p.chunk, 0,
                          p.dtype, p.x[:1, :T].copy(), p.dt[:1, :T].copy(), p.A, p.B[:1, :T].copy(),
                          p.C[:1, :T].copy(), p.D,
-                         None if p.initial_states is None else p.initial_states[:1].copy(), p.cu_seqlens, p.name)
+                         None if p.initial_states is None else
+                         (p.initial_states if p.cu_seqlens is not None else p.initial_states[:1].copy()),
+                         p.cu_seqlens, p.name)
     reps, t_all = 0, 0.0
     while t_all < seconds and reps < 16:
         t0 = time.perf_counter()
@@ -806,7 +816,7 @@ def run_sweep(args, dev, stream, flush, nsm):
         d = forward_inputs(p, dev)
         f, plan, y, fin, ms, launch_ms, _ = time_forward(p, d, dev, stream, flush, 3, min(args.steps, 10))
         nbytes, ach_call, frac_call, roof = forward_roofline(p, plan, ms, launch_ms, nsm)
-        key = (p.nheads, p.headdim, p.dstate, p.ngroups, p.cu_seqlens is not None)
+        key = (p.nheads, p.headdim, p.dstate, p.ngroups, p.cu_seqlens is not None, p.initial_states is not None)
         if not args.no_cpu_baseline and key not in rates:
             rates[key] = oracle_rate(p)
         out.append({"workload": p.name, "batch": p.batch, "seq_len": p.seqlen, "nheads": p.nheads,

@@ -207,11 +207,14 @@ def config_long(seqlen: int = 65536, split_len: int = 2048) -> SSDProblem:
                         name=f"long_b1_L{seqlen}_H32_split{split_len}")
 
 
-def config_varlen(total: int = 32768, ndocs: int = 37, nheads: int = 48) -> SSDProblem:
+def config_varlen(total: int = 32768, ndocs: int = 37, nheads: int = 48, init_std: float = 0.0) -> SSDProblem:
+    """Packed documents; with init_std > 0 every document also has its own
+    initial state (and the bench then asks for every final state)."""
     lens = geometric_doc_lengths(4, total, ndocs, 900.0)
     return make_problem(batch=1, seqlen=total, nheads=nheads, headdim=64, dstate=128, ngroups=1,
-                        chunk=128, dtype="bf16", seed=4, dt_dist="softplus_n22",
-                        doc_lengths=lens, name=f"varlen_T{total}_docs{ndocs}_H{nheads}")
+                        chunk=128, dtype="bf16", seed=4, dt_dist="softplus_n22", doc_lengths=lens,
+                        init_std=init_std,
+                        name=f"varlen_T{total}_docs{ndocs}_H{nheads}" + ("_states" if init_std > 0 else ""))
 
 
 def stress_logdecay_rows(nrows: int, length: int, seed: int = 100) -> np.ndarray:

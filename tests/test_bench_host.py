@@ -9,12 +9,19 @@ import bench
 def layer(batch=8, seqlen=2048, nheads=80):
     """Shape of the 2.7B-like layer (the accounting reads only the sizes)."""
     return SimpleNamespace(batch=batch, seqlen=seqlen, nheads=nheads, headdim=64, dstate=128, ngroups=1,
-                           chunk=128, dtype="bf16")
+                           chunk=128, dtype="bf16", initial_states=None, nstates=batch)
 
 
 def test_compulsory_bytes_of_the_27b_layer():
     # per token: x + y (80 heads x 64 x 2 B each), dt (80 x 4 B), B + C (128 x 2 B each)
     assert bench.compulsory_bytes(layer()) == 16384 * (2 * 80 * 64 * 2 + 80 * 4 + 2 * 128 * 2) == 349175808
+
+
+def test_compulsory_bytes_with_states():
+    # initial states read and final states written: 2 x (nstates, H, P, N) fp32
+    p = layer()
+    p.initial_states = object()
+    assert bench.compulsory_bytes(p) == 349175808 + 2 * 8 * 80 * 64 * 128 * 4
 
 
 def test_decode_bytes():
