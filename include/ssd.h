@@ -164,8 +164,13 @@ SSD_API size_t ssd_bwd_workspace_size(const ssd_params_t* p);
  * for the same inputs.  The states are recomputed from the inputs, as "Parallel
  * Scan and Hardware-Aware SSM Kernels" ("Why the kernel matters more than the
  * algorithm") describes: only the state entering each backward chunk is kept, in
- * the workspace.  Arithmetic is fp32 on CUDA cores (bf16 inputs are widened,
- * bf16 gradients rounded once at the end).
+ * the workspace.  bf16 with headdim 64 and dstate 128 (the Mamba-2 head
+ * shape) runs on the tensor cores: chunks of 128 tokens, every contraction a
+ * bf16 x bf16 -> fp32 MMA (the decay-masked Q x Q products, the adjoint and
+ * the incoming state are rounded to bf16 as MMA operands; sums, scans and
+ * the adjoint recurrence stay fp32).  Every other shape, and fp32, runs on
+ * CUDA cores in fp32 (bf16 inputs widened, bf16 gradients rounded once at the
+ * end).
  *
  * Inputs: x, dt, A, B, C, D (optional), initial_states (optional: zeros) exactly
  * as for ssd_fwd(); dy (batch, seqlen, nheads, headdim) dtype;
@@ -185,8 +190,11 @@ SSD_API size_t ssd_bwd_workspace_size(const ssd_params_t* p);
  * and shapes whose tiles do not fit in shared memory.
  * `chunk` and `split_len` in p are validated but do not change the result.
  * `workspace`: at least ssd_bwd_workspace_size(p) bytes, 256-byte aligned
- * (else SSD_ERR_WORKSPACE).  Asynchronous on `stream`; two launches; no
- * device-side waits.  Bitwise deterministic (fixed summation orders). */
+ * (else SSD_ERR_WORKSPACE).  Asynchronous on `stream`; a status-word reset
+ * and two launches.  The tensor-core path's device waits are bounded: one that
+ * runs out records SSD_ERR_TIMEOUT (where codes 31-37) in the status word at
+ * the start of `workspace`, read by ssd_check_status(); the CUDA-core path has
+ * no device waits.  Bitwise deterministic (fixed summation orders). */
 SSD_API int ssd_bwd(const ssd_params_t* p,
             const void* x, const float* dt, const float* A,
             const void* B, const void* C, const float* D,

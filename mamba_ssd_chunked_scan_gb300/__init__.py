@@ -164,11 +164,13 @@ def ssd_fwd(x, dt, A, B, C, D=None, initial_states=None, cu_seqlens=None, *, chu
 
 
 def ssd_bwd(x, dt, A, B, C, dy, D=None, initial_states=None, dfinal_states=None, cu_seqlens=None, *,
-            chunk=128, want_dinit=None, stream=None):
+            chunk=128, want_dinit=None, stream=None, check_status=False):
     """Gradients of <dy, y> + <dfinal_states, final_states> for one ssd_fwd
     call's inputs.  Packed documents (cu_seqlens, batch 1) start from zero
     states and take no dfinal_states.  Returns a dict with dx, ddt, dA, dB, dC,
-    dD (None without D) and dinit (by default for batch rows only)."""
+    dD (None without D) and dinit (by default for batch rows only).  With
+    check_status, also synchronises the stream and raises if a device-side
+    wait ran out (the workspace's status word)."""
     batch, seqlen, nheads, headdim = x.shape
     ngroups, dstate = B.shape[2], B.shape[3]
     dev = x.device
@@ -203,6 +205,8 @@ def ssd_bwd(x, dt, A, B, C, dy, D=None, initial_states=None, dfinal_states=None,
                           _ptr(g["ddt"]), _ptr(g["dA"]), _ptr(g["dB"]), _ptr(g["dC"]), _ptr(g["dD"]),
                           _ptr(g["dinit"]), _ptr(ws), nbytes, _stream_handle(stream))
     _lib.check(rc, "ssd_bwd")
+    if check_status:
+        _lib.check(_lib.lib.ssd_check_status(_ptr(ws), _stream_handle(stream)), "ssd_bwd device status")
     return g
 
 

@@ -15,7 +15,7 @@ ROOT = os.path.dirname(HERE)
 CSRC = os.path.join(HERE, "csrc")
 OUT_DIR = os.path.join(HERE, "_build")
 LIB = os.path.join(HERE, "libssd.so")
-SOURCES = ["ssd_api.cu", "ssd_simt.cu", "ssd_tc.cu", "ssd_agg.cu", "ssd_step.cu", "ssd_bwd.cu", "ssd_gate_norm.cu"]
+SOURCES = ["ssd_api.cu", "ssd_simt.cu", "ssd_tc.cu", "ssd_agg.cu", "ssd_step.cu", "ssd_bwd.cu", "ssd_bwd_tc.cu", "ssd_gate_norm.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC", "-Xcompiler", "-fvisibility=hidden",
          "--expt-relaxed-constexpr", "-I", os.path.join(ROOT, "include")]

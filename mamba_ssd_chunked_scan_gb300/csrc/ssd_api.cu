@@ -176,9 +176,14 @@ struct BwdLayout {
     size_t ckpt = 0, dB = 0, dC = 0, dA = 0, dD = 0, total = 0;
 };
 
+// The backward runs on the tensor cores for the bf16 Mamba-2 head shape.
+bool bwd_use_tc(const ssd_params_t* p) {
+    return bwd_tc_supported(p->headdim, p->dstate, p->dtype) && p->seqlen < ((int64_t)1 << 31) - 256;
+}
+
 bool bwd_layout(const ssd_params_t* p, BwdLayout* l) {
     if (check_params(p) != SSD_OK) return false;
-    l->Qb = bwd_chunk(p->headdim, p->dstate, kSmemLimit);
+    l->Qb = bwd_use_tc(p) ? kBwdTcChunk : bwd_chunk(p->headdim, p->dstate, kSmemLimit);
     if (l->Qb == 0) return false;
     const size_t bh = (size_t)p->batch * p->nheads;
     const size_t nch = (size_t)((p->seqlen + l->Qb - 1) / l->Qb);
@@ -515,7 +520,12 @@ int ssd_bwd(const ssd_params_t* p, const void* x, const float* dt, const float* 
     a.ws_dC = (float*)(ws + l.dC);
     a.ws_dA = (float*)(ws + l.dA);
     a.ws_dD = (float*)(ws + l.dD);
-    if (launch_bwd(a, (cudaStream_t)stream) != cudaSuccess) return SSD_ERR_CUDA;
+    a.ws = (WsHeader*)ws;
+    a.wait_iters = kDefaultWaitIters;
+    // a fresh status word for this call's bounded device waits
+    if (cudaMemsetAsync(ws, 0, sizeof(WsHeader), (cudaStream_t)stream) != cudaSuccess) return SSD_ERR_CUDA;
+    if ((bwd_use_tc(p) ? launch_bwd_tc(a, (cudaStream_t)stream) : launch_bwd(a, (cudaStream_t)stream)) != cudaSuccess)
+        return SSD_ERR_CUDA;
     return SSD_OK;
 }
 

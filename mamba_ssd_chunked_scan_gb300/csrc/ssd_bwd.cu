@@ -736,6 +736,10 @@ cudaError_t launch_bwd(const BwdArgs& a, cudaStream_t st) {
     if (e != cudaSuccess) return e;
     k1<<<(unsigned)(a.batch * a.H), kBwdThreads, smem, st>>>(a);
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
+    return launch_bwd_reduce(a, st);
+}
+
+cudaError_t launch_bwd_reduce(const BwdArgs& a, cudaStream_t st) {
     int dev = 0, nsm = 0;
     cudaGetDevice(&dev);
     cudaDeviceGetAttribute(&nsm, cudaDevAttrMultiProcessorCount, dev);

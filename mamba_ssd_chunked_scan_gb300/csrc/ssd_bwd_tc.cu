@@ -1,0 +1,667 @@
+// Backward pass on the tensor cores (tcgen05 / TMEM / TMA) for the Mamba-2
+// head shape: chunk Q = 128, P = 64, N = 128, bf16 x / B / C / dy / dx, fp32
+// dt / A / D / states and fp32 accumulation.  The reverse-mode formulas are
+// those of ssd_bwd_chunk (ssd_bwd.cu, which states them), by recomputation
+// ("Parallel Scan and Hardware-Aware SSM Kernels", "Why the kernel matters
+// more than the algorithm"), with every contraction one UMMA chain:
+//
+//   phase 1, chunks forwards:  S^T <- 2^tau S^T + B^T (w o x),  w_j = 2^{s_j} dt_j
+//                              (the state entering each chunk is kept)
+//   phase 2, chunks backwards (L = the decay mask of the hierarchy-aware
+//   segsum, Lam = the adjoint of the state leaving the chunk):
+//     G = C B^T, X = dy x^T              A1 = L o G, A2 = L o X (bf16 tiles)
+//     V1 = A1^T dy, V2 = B Lam^T         v_j = V1_j + 2^{s_j} V2_j
+//     SC = C S_in^T                      dx_j = dt_j v_j + D dy_j
+//     dB_j = dt_j [A2^T C + (2^s o x) Lam^T]_j        (one accumulator)
+//     dC_i = [(A2 o dt) B + (2^p o dy) S_in^T]_i       (one accumulator)
+//     Lam^T <- 2^tau Lam^T + C^T (2^p o dy)
+//   and the per-token terms of ddt from row sums of those products and of
+//   W = A1 o dt o X (its corner sums by a warp transpose-reduction).
+//
+// One CTA of 128 threads per (batch row, head): thread r owns chunk row r,
+// and state column n = r of S, Lam and the contractions whose rows are state
+// columns.  Thread 0 issues the TMA loads and the MMAs; every wait is bounded
+// and a wait that runs out records SSD_ERR_TIMEOUT in the workspace status
+// word, after which the CTA drains its MMAs, frees its TMEM and exits.
+#include <cuda.h>
+#include <cuda_bf16.h>
+#include <stddef.h>
+
+#include <atomic>
+
+#include "ssd_common.cuh"
+#include "segsum.cuh"
+#include "ssd_kernels.h"
+#include "tc_ptx.cuh"
+
+namespace ssd {
+namespace {
+
+constexpr int Q = 128, P = 64, N = 128;
+constexpr int kThreads = 128;
+// shared tiles (each 1024-byte aligned for the 128-byte swizzle)
+constexpr uint32_t kTX = 0;           // x (row j, p); then 2^{s_j} x_j (phase 1: w_j x_j)
+constexpr uint32_t kTDY = 16384;      // dy (row i, p); then 2^{p_i} dy_i
+constexpr uint32_t kTB = 32768;       // B (row j, n in two 64-column slabs)
+constexpr uint32_t kTC = 65536;       // C
+constexpr uint32_t kTLam = 98304;     // Lam as (row n, p) bf16
+constexpr uint32_t kTSin = 114688;    // S_in as (row n, p) bf16
+constexpr uint32_t kT1 = 131072;      // A1 (row i, column j); then A2 o dt
+constexpr uint32_t kT2 = 163840;      // A2
+constexpr uint32_t kTiles = 196608;
+// TMEM columns
+constexpr uint32_t kTmG = 0, kTmX = 128, kTmV2 = 256, kTmSC = 320, kTmV1 = 384, kTmLU = 448, kTmCols = 512;
+
+// codes of the wait that gave up (WsHeader::where)
+enum : uint32_t { kWhereLoad = 31, kWhereMma1 = 32, kWhereV1 = 33, kWhereDB = 34, kWhereDC = 35,
+                  kWhereF = 36, kWhereDrain = 37 };
+
+struct BwdTcSmall {
+    SegsumLinShared<4> seg;
+    alignas(16) float dts[Q];
+    float part[4][Q];       // per-warp partial corner sums of W
+    float red[8];
+    float carry[2][4];      // warp totals of the token scans
+    uint64_t full, mma1, mmaV1, mmaDB, mmaDC, mmaF, drain;
+    uint32_t tmem_base;
+    int abort;
+    int never;
+};
+static_assert(offsetof(BwdTcSmall, full) % 8 == 0, "mbarriers are 8-byte aligned");
+constexpr size_t kSmemBytes = 1024 + kTiles + sizeof(BwdTcSmall);
+static_assert(kSmemBytes <= 227 * 1024, "shared memory per CTA");
+
+struct BwdTcParams {
+    CUtensorMap tm_x, tm_dy, tm_B, tm_C;
+    BwdArgs a;
+};
+
+// K-major operand of 128 rows with K = 128 (two 64-column slabs), k-step kk of 16
+__device__ __forceinline__ uint64_t desc_k2(uint32_t base, int kk) {
+    return ptx::sdesc_sw128(base + (kk >> 2) * 16384 + (kk & 3) * 32, 16, 1024);
+}
+// K-major operand of 128 rows with K = 64 (one slab), k-step kk < 4
+__device__ __forceinline__ uint64_t desc_k1(uint32_t base, int kk) {
+    return ptx::sdesc_sw128(base + kk * 32, 16, 1024);
+}
+// MN-major operand, MN extent 64 (one block), k-step kk (16 rows of the tile)
+__device__ __forceinline__ uint64_t desc_mn1(uint32_t base, int kk) {
+    return ptx::sdesc_sw128(base + kk * 2048, 8192, 1024);
+}
+// MN-major operand, MN extent 128 (two 64-wide blocks, 16 KB apart), k-step kk
+__device__ __forceinline__ uint64_t desc_mn2(uint32_t base, int kk) {
+    return ptx::sdesc_sw128(base + kk * 2048, 16384, 1024);
+}
+
+__device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
+    __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
+    return *reinterpret_cast<uint32_t*>(&v);
+}
+__device__ __forceinline__ float bf16lo(uint32_t w) { return __uint_as_float(w << 16); }
+__device__ __forceinline__ float bf16hi(uint32_t w) { return __uint_as_float(w & 0xFFFF0000u); }
+
+// offset of element (row r, column j < 128) in a two-slab tile
+__device__ __forceinline__ uint32_t off2(int r, int j) { return (uint32_t)(j >> 6) * 16384u + sw128_off(r, j & 63); }
+
+__device__ __forceinline__ bool wait_bar(BwdTcSmall& sh, const BwdArgs& a, uint64_t* bar, uint32_t parity,
+                                         uint32_t where) {
+    if (ptx::mbar_wait(bar, parity, &sh.abort, a.wait_iters)) return true;
+    if (!*(volatile int*)&sh.abort) {
+        record_error(a.ws, SSD_ERR_TIMEOUT, where);
+        *(volatile int*)&sh.abort = 1;
+    }
+    return false;
+}
+
+__device__ __forceinline__ float warp_sum(float v) {
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+    return v;
+}
+
+// Sum over the warp's 32 lanes of element (lane & 15) of each lane's
+// 16-vector (a reduction and a transpose in 16 shuffles: each step hands half
+// of the remaining elements to the partner lane, the last adds the two
+// half-warps).
+__device__ __forceinline__ float warp_transpose_sum16(float (&v)[16], int lane) {
+#pragma unroll
+    for (int h = 8; h >= 1; h >>= 1) {
+        const bool up = (lane & h) != 0;
+#pragma unroll
+        for (int k = 0; k < h; ++k) {
+            const float send = up ? v[k] : v[k + h];
+            const float keep = up ? v[k + h] : v[k];
+            v[k] = keep + __shfl_xor_sync(0xffffffffu, send, h);
+        }
+    }
+    return v[0] + __shfl_xor_sync(0xffffffffu, v[0], 16);
+}
+
+// Document start (d >= 1) at token t of a packed row: its log-decay is -inf.
+__device__ __forceinline__ bool doc_start_tc(const BwdArgs& a, int64_t t) {
+    if (!a.cu) return false;
+    int lo = 1, hi = a.ndocs - 1;
+    while (lo <= hi) {
+        const int mid = (lo + hi) >> 1;
+        const int64_t v = __ldg(a.cu + mid);
+        if (v == t) return true;
+        if (v < t) lo = mid + 1; else hi = mid - 1;
+    }
+    return false;
+}
+
+__global__ void __launch_bounds__(kThreads, 1) ssd_bwd_tc(const __grid_constant__ BwdTcParams prm) {
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t* sm = (uint8_t*)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
+    BwdTcSmall& sh = *reinterpret_cast<BwdTcSmall*>(sm + kTiles);
+    const BwdArgs& a = prm.a;
+    const int r = threadIdx.x, warp = r >> 5, lane = r & 31;
+    const uint32_t s0 = ptx::smem_u32(sm);
+    const int64_t unit = blockIdx.x;   // b * H + h
+    const int h = (int)(unit % a.H);
+    const int b = (int)(unit / a.H);
+    const int g = h / (a.H / a.G);
+    const int64_t L = a.L;
+    const int nch = (int)((L + Q - 1) / Q);
+    const size_t PN = (size_t)P * N;
+    const float A2 = a.A[h] * kLog2e;
+    const float Ah = a.A[h];
+    const float Dh = a.D ? a.D[h] : 0.f;
+    float* ckpt = a.ws_ckpt + (size_t)unit * nch * PN;
+
+    if (r == 0) {
+        ptx::mbar_init(&sh.full, 1);
+        ptx::mbar_init(&sh.mma1, 1);
+        ptx::mbar_init(&sh.mmaV1, 1);
+        ptx::mbar_init(&sh.mmaDB, 1);
+        ptx::mbar_init(&sh.mmaDC, 1);
+        ptx::mbar_init(&sh.mmaF, 1);
+        ptx::mbar_init(&sh.drain, 1);
+        sh.abort = 0;
+        sh.never = 0;
+        ptx::mbar_fence_init();
+        ptx::prefetch_tmap(&prm.tm_x);
+        ptx::prefetch_tmap(&prm.tm_dy);
+        ptx::prefetch_tmap(&prm.tm_B);
+        ptx::prefetch_tmap(&prm.tm_C);
+    }
+    if (warp == 0) ptx::tmem_alloc(&sh.tmem_base, kTmCols);
+    ptx::tc_fence_before();
+    __syncthreads();
+    ptx::tc_fence_after();
+    const uint32_t tb = sh.tmem_base;
+    const uint32_t lane_addr = tb + ((uint32_t)(32 * warp) << 16);
+    uint32_t nfull = 0, nF = 0, n1 = 0;   // completed phases of the reused barriers
+    uint32_t nissue = 0;                  // loads issued (thread 0)
+
+    // log-decays of the chunk at t0 into the segsum input; dt into sh.dts
+    bool start = false;   // a document starts at this thread's token
+    auto chunk_decays = [&](int64_t t0) -> float {
+        const bool ok = t0 + r < L;
+        const float d = ok ? __ldg(a.dt + ((size_t)b * L + t0 + r) * a.H + h) : 0.f;
+        start = ok && doc_start_tc(a, t0 + r);
+        const float l2 = start ? -INFINITY : d * A2;
+        sh.seg.a[r] = ex2_approx(l2);   // 0 at a document start, 1 past the end
+        sh.dts[r] = d;
+        return d;
+    };
+
+    // ------------------------------------------------------------ phase 1
+    float S[P];
+#pragma unroll
+    for (int p = 0; p < P; ++p) S[p] = a.init ? a.init[unit * PN + (size_t)p * N + r] : 0.f;
+    for (int c = 0; c < nch && !*(volatile int*)&sh.abort; ++c) {
+        const int64_t t0 = (int64_t)c * Q;
+        if (r == 0) {
+            ++nissue;
+            ptx::mbar_expect_tx(&sh.full, 16384u + 32768u);
+            ptx::tma_load_4d(sm + kTX, &prm.tm_x, &sh.full, 0, h, (int)t0, b);
+            ptx::tma_load_4d(sm + kTB, &prm.tm_B, &sh.full, 0, g, (int)t0, b);
+            ptx::tma_load_4d(sm + kTB + 16384, &prm.tm_B, &sh.full, 64, g, (int)t0, b);
+        }
+        const float d = chunk_decays(t0);
+#pragma unroll
+        for (int p = 0; p < P; ++p) ckpt[(size_t)c * PN + (size_t)p * N + r] = S[p];
+        __syncthreads();
+        SegsumLinRow<4> row;
+        segsum_lin_phase1<4>(sh.seg, row, warp, lane);
+        __syncthreads();
+        segsum_lin_phase2<4>(sh.seg, row, warp, lane);
+        __syncthreads();
+        const float w = segsum_lin_suffix<4>(sh.seg, r) * d;
+        const float etau = sh.seg.tauL;
+        wait_bar(sh, a, &sh.full, nfull & 1, kWhereLoad);
+        ++nfull;
+        {   // w_j x_j in place (row j = r)
+            uint8_t* xr = sm + kTX;
+#pragma unroll
+            for (int q = 0; q < 8; ++q) {
+                uint4 v = *reinterpret_cast<const uint4*>(xr + sw128_off(r, 8 * q));
+                v.x = pack_bf16(bf16lo(v.x) * w, bf16hi(v.x) * w);
+                v.y = pack_bf16(bf16lo(v.y) * w, bf16hi(v.y) * w);
+                v.z = pack_bf16(bf16lo(v.z) * w, bf16hi(v.z) * w);
+                v.w = pack_bf16(bf16lo(v.w) * w, bf16hi(v.w) * w);
+                *reinterpret_cast<uint4*>(xr + sw128_off(r, 8 * q)) = v;
+            }
+            ptx::fence_proxy_async();
+        }
+        __syncthreads();
+        if (r == 0) {
+            ptx::tc_fence_after();
+            constexpr uint32_t id = ptx::idesc_bf16(128, 64, 1, 1);
+#pragma unroll 1
+            for (int kk = 0; kk < 8; ++kk)
+                ptx::mma_ss(tb + kTmG, desc_mn2(s0 + kTB, kk), desc_mn1(s0 + kTX, kk), id, kk > 0);
+            ptx::mma_commit(&sh.mmaF);
+        }
+        wait_bar(sh, a, &sh.mmaF, nF & 1, kWhereF);
+        ++nF;
+        ptx::tc_fence_after();
+        {
+            uint32_t d0[32], d1[32];
+            ptx::tmem_load32x2(lane_addr + kTmG, d0, lane_addr + kTmG + 32, d1);
+#pragma unroll
+            for (int p = 0; p < 32; ++p) {
+                S[p] = fmaf(etau, S[p], __uint_as_float(d0[p]));
+                S[p + 32] = fmaf(etau, S[p + 32], __uint_as_float(d1[p]));
+            }
+        }
+        ptx::tc_fence_before();
+        __syncthreads();   // tiles and TMEM free for the next chunk
+    }
+
+    // ------------------------------------------------------------ phase 2
+    float Lm[P];   // Lam[p][n = r]
+#pragma unroll
+    for (int p = 0; p < P; ++p) Lm[p] = a.dfin ? a.dfin[unit * PN + (size_t)p * N + r] : 0.f;
+    float dA_acc = 0.f, dD_acc = 0.f;
+    for (int c = nch - 1; c >= 0 && !*(volatile int*)&sh.abort; --c) {
+        const int64_t t0 = (int64_t)c * Q;
+        const bool valid = t0 + r < L;
+        if (r == 0) {
+            ++nissue;
+            ptx::mbar_expect_tx(&sh.full, 16384u * 2u + 32768u * 2u);
+            ptx::tma_load_4d(sm + kTX, &prm.tm_x, &sh.full, 0, h, (int)t0, b);
+            ptx::tma_load_4d(sm + kTDY, &prm.tm_dy, &sh.full, 0, h, (int)t0, b);
+            ptx::tma_load_4d(sm + kTB, &prm.tm_B, &sh.full, 0, g, (int)t0, b);
+            ptx::tma_load_4d(sm + kTB + 16384, &prm.tm_B, &sh.full, 64, g, (int)t0, b);
+            ptx::tma_load_4d(sm + kTC, &prm.tm_C, &sh.full, 0, g, (int)t0, b);
+            ptx::tma_load_4d(sm + kTC + 16384, &prm.tm_C, &sh.full, 64, g, (int)t0, b);
+            if (c > 0) {   // the next chunk's tiles on their way to L2
+                const int tp = (int)(t0 - Q);
+                ptx::tma_prefetch_4d(&prm.tm_x, 0, h, tp, b);
+                ptx::tma_prefetch_4d(&prm.tm_dy, 0, h, tp, b);
+                ptx::tma_prefetch_4d(&prm.tm_B, 0, g, tp, b);
+                ptx::tma_prefetch_4d(&prm.tm_B, 64, g, tp, b);
+                ptx::tma_prefetch_4d(&prm.tm_C, 0, g, tp, b);
+                ptx::tma_prefetch_4d(&prm.tm_C, 64, g, tp, b);
+            }
+        }
+        const float d = chunk_decays(t0);
+        // S_in and Lam as bf16 (row n = r, p) operands; <Lam, S_in>
+        float kdot = 0.f;
+        {
+            const float* src = ckpt + (size_t)c * PN + r;
+#pragma unroll
+            for (int q = 0; q < 8; ++q) {
+                float sv[8];
+#pragma unroll
+                for (int e = 0; e < 8; ++e) {
+                    sv[e] = src[(size_t)(8 * q + e) * N];
+                    kdot = fmaf(Lm[8 * q + e], sv[e], kdot);
+                }
+                *reinterpret_cast<uint4*>(sm + kTSin + sw128_off(r, 8 * q)) =
+                    make_uint4(pack_bf16(sv[0], sv[1]), pack_bf16(sv[2], sv[3]), pack_bf16(sv[4], sv[5]),
+                               pack_bf16(sv[6], sv[7]));
+                *reinterpret_cast<uint4*>(sm + kTLam + sw128_off(r, 8 * q)) =
+                    make_uint4(pack_bf16(Lm[8 * q], Lm[8 * q + 1]), pack_bf16(Lm[8 * q + 2], Lm[8 * q + 3]),
+                               pack_bf16(Lm[8 * q + 4], Lm[8 * q + 5]), pack_bf16(Lm[8 * q + 6], Lm[8 * q + 7]));
+            }
+            ptx::fence_proxy_async();
+        }
+        kdot = warp_sum(kdot);
+        if (lane == 0) sh.red[warp] = kdot;
+        __syncthreads();
+        const float K = (sh.red[0] + sh.red[1]) + (sh.red[2] + sh.red[3]);
+        SegsumLinRow<4> row;
+        segsum_lin_phase1<4>(sh.seg, row, warp, lane);
+        __syncthreads();
+        segsum_lin_phase2<4>(sh.seg, row, warp, lane);
+        __syncthreads();
+        const float es_r = segsum_lin_suffix<4>(sh.seg, r);
+        const float ep_r = row.pe;
+        const float etau = sh.seg.tauL;
+        // ---- G, X, V2, SC
+        wait_bar(sh, a, &sh.full, nfull & 1, kWhereLoad);
+        ++nfull;
+        if (r == 0) {
+            ptx::tc_fence_after();
+            constexpr uint32_t idQQ = ptx::idesc_bf16(128, 128, 0, 0);
+            constexpr uint32_t idQP = ptx::idesc_bf16(128, 64, 0, 1);
+#pragma unroll 1
+            for (int kk = 0; kk < 8; ++kk)
+                ptx::mma_ss(tb + kTmG, desc_k2(s0 + kTC, kk), desc_k2(s0 + kTB, kk), idQQ, kk > 0);
+#pragma unroll 1
+            for (int kk = 0; kk < 4; ++kk)
+                ptx::mma_ss(tb + kTmX, desc_k1(s0 + kTDY, kk), desc_k1(s0 + kTX, kk), idQQ, kk > 0);
+#pragma unroll 1
+            for (int kk = 0; kk < 8; ++kk)
+                ptx::mma_ss(tb + kTmV2, desc_k2(s0 + kTB, kk), desc_mn1(s0 + kTLam, kk), idQP, kk > 0);
+#pragma unroll 1
+            for (int kk = 0; kk < 8; ++kk)
+                ptx::mma_ss(tb + kTmSC, desc_k2(s0 + kTC, kk), desc_mn1(s0 + kTSin, kk), idQP, kk > 0);
+            ptx::mma_commit(&sh.mma1);
+        }
+        wait_bar(sh, a, &sh.mma1, n1 & 1, kWhereMma1);
+        ptx::tc_fence_after();
+        // ---- rows of A1 = L o G and A2 = L o X (bf16 tiles); corner sums of W.
+        // Column block cb of 32: L_rj = rf[cb] colL[j] below the diagonal block
+        // (rank-one), wl[j - 32 cb] in it, 0 above it.
+        {
+            float zrun = 0.f;   // sum of W_rj over the columns done
+#pragma unroll 1
+            for (int cb = 0; cb < 4; ++cb) {
+                const float rfc = (cb == 0) ? row.rf[0] : (cb == 1) ? row.rf[1] : row.rf[2];
+                const bool below = cb < warp, diag = cb == warp;
+#pragma unroll
+                for (int hf = 0; hf < 2; ++hf) {
+                    const int j0 = 32 * cb + 16 * hf;
+                    uint32_t gr[16], xr[16];
+                    ptx::tmem_load16x2(lane_addr + kTmG + j0, gr, lane_addr + kTmX + j0, xr);
+                    float z[16];
+                    uint32_t p1[8], p2[8];
+#pragma unroll
+                    for (int cc = 0; cc < 16; cc += 2) {
+                        const float l0 = below ? rfc * sh.seg.colL[j0 + cc] : diag ? row.wl[16 * hf + cc] : 0.f;
+                        const float l1 = below ? rfc * sh.seg.colL[j0 + cc + 1] : diag ? row.wl[16 * hf + cc + 1] : 0.f;
+                        const float a1_0 = l0 * __uint_as_float(gr[cc]), a1_1 = l1 * __uint_as_float(gr[cc + 1]);
+                        const float x0 = __uint_as_float(xr[cc]), x1 = __uint_as_float(xr[cc + 1]);
+                        p1[cc / 2] = pack_bf16(a1_0, a1_1);
+                        p2[cc / 2] = pack_bf16(l0 * x0, l1 * x1);
+                        // W from the bf16 A1 that V1 contracts: the token's own term of
+                        // <Lam_t, S_t> and of dt_t x_t . v_t then cancel in dl_t
+                        zrun += bf16lo(p1[cc / 2]) * sh.dts[j0 + cc] * x0;
+                        z[cc] = (j0 + cc <= r) ? zrun : 0.f;
+                        zrun += bf16hi(p1[cc / 2]) * sh.dts[j0 + cc + 1] * x1;
+                        z[cc + 1] = (j0 + cc + 1 <= r) ? zrun : 0.f;
+                    }
+#pragma unroll
+                    for (int q = 0; q < 2; ++q) {
+                        *reinterpret_cast<uint4*>(sm + kT1 + off2(r, j0 + 8 * q)) =
+                            make_uint4(p1[4 * q], p1[4 * q + 1], p1[4 * q + 2], p1[4 * q + 3]);
+                        *reinterpret_cast<uint4*>(sm + kT2 + off2(r, j0 + 8 * q)) =
+                            make_uint4(p2[4 * q], p2[4 * q + 1], p2[4 * q + 2], p2[4 * q + 3]);
+                    }
+                    const float zs = warp_transpose_sum16(z, lane);
+                    if (lane < 16) sh.part[warp][j0 + lane] = zs;
+                }
+            }
+        }
+        {   // x row j = r becomes 2^{s_j} x_j (the X contraction is done)
+            uint8_t* xr = sm + kTX;
+#pragma unroll
+            for (int q = 0; q < 8; ++q) {
+                uint4 v = *reinterpret_cast<const uint4*>(xr + sw128_off(r, 8 * q));
+                v.x = pack_bf16(bf16lo(v.x) * es_r, bf16hi(v.x) * es_r);
+                v.y = pack_bf16(bf16lo(v.y) * es_r, bf16hi(v.y) * es_r);
+                v.z = pack_bf16(bf16lo(v.z) * es_r, bf16hi(v.z) * es_r);
+                v.w = pack_bf16(bf16lo(v.w) * es_r, bf16hi(v.w) * es_r);
+                *reinterpret_cast<uint4*>(xr + sw128_off(r, 8 * q)) = v;
+            }
+        }
+        ptx::fence_proxy_async();
+        ptx::tc_fence_before();
+        __syncthreads();
+        // ---- V1 = A1^T dy; dB~ = A2^T C + (2^s o x) Lam^T
+        if (r == 0) {
+            ptx::tc_fence_after();
+            constexpr uint32_t idV = ptx::idesc_bf16(128, 64, 1, 1);
+            constexpr uint32_t idB1 = ptx::idesc_bf16(128, 128, 1, 1);
+            constexpr uint32_t idB2 = ptx::idesc_bf16(128, 128, 0, 0);
+#pragma unroll 1
+            for (int kk = 0; kk < 8; ++kk)
+                ptx::mma_ss(tb + kTmV1, desc_mn2(s0 + kT1, kk), desc_mn1(s0 + kTDY, kk), idV, kk > 0);
+            ptx::mma_commit(&sh.mmaV1);
+#pragma unroll 1
+            for (int kk = 0; kk < 8; ++kk)
+                ptx::mma_ss(tb + kTmG, desc_mn2(s0 + kT2, kk), desc_mn2(s0 + kTC, kk), idB1, kk > 0);
+#pragma unroll 1
+            for (int kk = 0; kk < 4; ++kk)
+                ptx::mma_ss(tb + kTmG, desc_k1(s0 + kTX, kk), desc_k1(s0 + kTLam, kk), idB2, 1);
+            ptx::mma_commit(&sh.mmaDB);
+        }
+        wait_bar(sh, a, &sh.mmaV1, n1 & 1, kWhereV1);
+        ptx::tc_fence_after();
+        // ---- rows of A2 o dt (from X, still in TMEM) over A1; dy row i = r becomes 2^{p_i} dy_i
+#pragma unroll 1
+        for (int cb = 0; cb < 4; ++cb) {
+            const float rfc = (cb == 0) ? row.rf[0] : (cb == 1) ? row.rf[1] : row.rf[2];
+            const bool below = cb < warp, diag = cb == warp;
+#pragma unroll
+            for (int hf = 0; hf < 2; ++hf) {
+                const int j0 = 32 * cb + 16 * hf;
+                uint32_t xr[16];
+                ptx::tmem_load16(lane_addr + kTmX + j0, xr);
+                uint32_t p1[8];
+#pragma unroll
+                for (int cc = 0; cc < 16; cc += 2) {
+                    const float l0 = below ? rfc * sh.seg.colL[j0 + cc] : diag ? row.wl[16 * hf + cc] : 0.f;
+                    const float l1 = below ? rfc * sh.seg.colL[j0 + cc + 1] : diag ? row.wl[16 * hf + cc + 1] : 0.f;
+                    p1[cc / 2] = pack_bf16(l0 * __uint_as_float(xr[cc]) * sh.dts[j0 + cc],
+                                           l1 * __uint_as_float(xr[cc + 1]) * sh.dts[j0 + cc + 1]);
+                }
+#pragma unroll
+                for (int q = 0; q < 2; ++q)
+                    *reinterpret_cast<uint4*>(sm + kT1 + off2(r, j0 + 8 * q)) =
+                        make_uint4(p1[4 * q], p1[4 * q + 1], p1[4 * q + 2], p1[4 * q + 3]);
+            }
+        }
+        {
+            uint8_t* dr = sm + kTDY;
+#pragma unroll
+            for (int q = 0; q < 8; ++q) {
+                uint4 v = *reinterpret_cast<const uint4*>(dr + sw128_off(r, 8 * q));
+                v.x = pack_bf16(bf16lo(v.x) * ep_r, bf16hi(v.x) * ep_r);
+                v.y = pack_bf16(bf16lo(v.y) * ep_r, bf16hi(v.y) * ep_r);
+                v.z = pack_bf16(bf16lo(v.z) * ep_r, bf16hi(v.z) * ep_r);
+                v.w = pack_bf16(bf16lo(v.w) * ep_r, bf16hi(v.w) * ep_r);
+                *reinterpret_cast<uint4*>(dr + sw128_off(r, 8 * q)) = v;
+            }
+        }
+        ptx::fence_proxy_async();
+        ptx::tc_fence_before();
+        __syncthreads();
+        // ---- dC = (A2 o dt) B + (2^p o dy) S_in^T; Lam^T update C^T (2^p o dy)
+        if (r == 0) {
+            ptx::tc_fence_after();
+            constexpr uint32_t idC1 = ptx::idesc_bf16(128, 128, 0, 1);
+            constexpr uint32_t idC2 = ptx::idesc_bf16(128, 128, 0, 0);
+            constexpr uint32_t idL = ptx::idesc_bf16(128, 64, 1, 1);
+#pragma unroll 1
+            for (int kk = 0; kk < 8; ++kk)
+                ptx::mma_ss(tb + kTmX, desc_k2(s0 + kT1, kk), desc_mn2(s0 + kTB, kk), idC1, kk > 0);
+#pragma unroll 1
+            for (int kk = 0; kk < 4; ++kk)
+                ptx::mma_ss(tb + kTmX, desc_k1(s0 + kTDY, kk), desc_k1(s0 + kTSin, kk), idC2, 1);
+#pragma unroll 1
+            for (int kk = 0; kk < 8; ++kk)
+                ptx::mma_ss(tb + kTmLU, desc_mn2(s0 + kTC, kk), desc_mn1(s0 + kTDY, kk), idL, kk > 0);
+            ptx::mma_commit(&sh.mmaDC);
+        }
+        // ---- dx and the per-token products (row j = r)
+        const size_t row_io = ((size_t)b * L + t0 + r) * a.H + h;
+        float vx = 0.f, lbx = 0.f, scdy = 0.f, ddv = 0.f;
+        {
+            uint4 xv[8], dv[8];
+            const uint4* xg = reinterpret_cast<const uint4*>(static_cast<const __nv_bfloat16*>(a.x) + row_io * P);
+            const uint4* dg = reinterpret_cast<const uint4*>(static_cast<const __nv_bfloat16*>(a.dy) + row_io * P);
+#pragma unroll
+            for (int q = 0; q < 8; ++q) {
+                xv[q] = valid ? __ldg(xg + q) : make_uint4(0u, 0u, 0u, 0u);
+                dv[q] = valid ? __ldg(dg + q) : make_uint4(0u, 0u, 0u, 0u);
+            }
+            uint32_t dxo[16];
+#pragma unroll
+            for (int hf = 0; hf < 2; ++hf) {
+                uint32_t v1[32], v2[32], sc[32];
+                ptx::tmem_load32x2(lane_addr + kTmV1 + 32 * hf, v1, lane_addr + kTmV2 + 32 * hf, v2);
+                ptx::tmem_load32(lane_addr + kTmSC + 32 * hf, sc);
+#pragma unroll
+                for (int k = 0; k < 32; k += 2) {
+                    const int q = (32 * hf + k) >> 3, e = (32 * hf + k) & 7;
+                    const uint32_t xw = e == 0 ? xv[q].x : e == 2 ? xv[q].y : e == 4 ? xv[q].z : xv[q].w;
+                    const uint32_t dw = e == 0 ? dv[q].x : e == 2 ? dv[q].y : e == 4 ? dv[q].z : dv[q].w;
+                    const float x0 = bf16lo(xw), x1 = bf16hi(xw), y0 = bf16lo(dw), y1 = bf16hi(dw);
+                    const float w0 = __uint_as_float(v2[k]), w1 = __uint_as_float(v2[k + 1]);
+                    const float v0 = fmaf(es_r, w0, __uint_as_float(v1[k]));
+                    const float v1v = fmaf(es_r, w1, __uint_as_float(v1[k + 1]));
+                    vx = fmaf(v0, x0, fmaf(v1v, x1, vx));
+                    lbx = fmaf(w0, x0, fmaf(w1, x1, lbx));
+                    scdy = fmaf(__uint_as_float(sc[k]), y0, fmaf(__uint_as_float(sc[k + 1]), y1, scdy));
+                    ddv = fmaf(y0, x0, fmaf(y1, x1, ddv));
+                    dxo[(32 * hf + k) / 2 - 16 * hf] = pack_bf16(fmaf(d, v0, Dh * y0), fmaf(d, v1v, Dh * y1));
+                }
+                if (valid) {
+                    uint4* dxg = reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(a.dx) + row_io * P) + 4 * hf;
+#pragma unroll
+                    for (int q = 0; q < 4; ++q)
+                        dxg[q] = make_uint4(dxo[4 * q], dxo[4 * q + 1], dxo[4 * q + 2], dxo[4 * q + 3]);
+                }
+            }
+        }
+        // ---- this head's share of dB (row j = r), then of dC, then the Lam update
+        wait_bar(sh, a, &sh.mmaDB, n1 & 1, kWhereDB);
+        ptx::tc_fence_after();
+        {
+            // (the TMEM loads are warp-wide: every lane takes part, valid rows store)
+            float4* out = reinterpret_cast<float4*>(a.ws_dB + row_io * N);
+#pragma unroll 1
+            for (int hf = 0; hf < 2; ++hf) {
+                uint32_t d0[32], d1[32];
+                ptx::tmem_load32x2(lane_addr + kTmG + 64 * hf, d0, lane_addr + kTmG + 64 * hf + 32, d1);
+                if (valid) {
+#pragma unroll
+                    for (int q = 0; q < 8; ++q) {
+                        out[16 * hf + q] =
+                            make_float4(d * __uint_as_float(d0[4 * q]), d * __uint_as_float(d0[4 * q + 1]),
+                                        d * __uint_as_float(d0[4 * q + 2]), d * __uint_as_float(d0[4 * q + 3]));
+                        out[16 * hf + 8 + q] =
+                            make_float4(d * __uint_as_float(d1[4 * q]), d * __uint_as_float(d1[4 * q + 1]),
+                                        d * __uint_as_float(d1[4 * q + 2]), d * __uint_as_float(d1[4 * q + 3]));
+                    }
+                }
+            }
+        }
+        wait_bar(sh, a, &sh.mmaDC, n1 & 1, kWhereDC);
+        ++n1;
+        ptx::tc_fence_after();
+        {
+            float4* out = reinterpret_cast<float4*>(a.ws_dC + row_io * N);
+#pragma unroll 1
+            for (int hf = 0; hf < 2; ++hf) {
+                uint32_t d0[32], d1[32];
+                ptx::tmem_load32x2(lane_addr + kTmX + 64 * hf, d0, lane_addr + kTmX + 64 * hf + 32, d1);
+                if (valid) {
+#pragma unroll
+                    for (int q = 0; q < 8; ++q) {
+                        out[16 * hf + q] = make_float4(__uint_as_float(d0[4 * q]), __uint_as_float(d0[4 * q + 1]),
+                                                       __uint_as_float(d0[4 * q + 2]), __uint_as_float(d0[4 * q + 3]));
+                        out[16 * hf + 8 + q] =
+                            make_float4(__uint_as_float(d1[4 * q]), __uint_as_float(d1[4 * q + 1]),
+                                        __uint_as_float(d1[4 * q + 2]), __uint_as_float(d1[4 * q + 3]));
+                    }
+                }
+            }
+            uint32_t l0[32], l1[32];
+            ptx::tmem_load32x2(lane_addr + kTmLU, l0, lane_addr + kTmLU + 32, l1);
+#pragma unroll
+            for (int p = 0; p < 32; ++p) {
+                Lm[p] = fmaf(etau, Lm[p], __uint_as_float(l0[p]));
+                Lm[p + 32] = fmaf(etau, Lm[p + 32], __uint_as_float(l1[p]));
+            }
+        }
+        ptx::tc_fence_before();
+        __syncthreads();   // sh.part complete
+        // ---- ddt of token t = r, dA and dD
+        {
+            const float rv = (sh.part[0][r] + sh.part[1][r]) + (sh.part[2][r] + sh.part[3][r]);
+            // U_t = sum_{i >= t} 2^{p_i} scdy_i, V_t = sum_{j <= t} 2^{s_j} dt_j lbx_j
+            float u = ep_r * scdy, v = es_r * d * lbx;
+#pragma unroll
+            for (int o = 1; o < 32; o <<= 1) {
+                const float tu = __shfl_down_sync(0xffffffffu, u, o);
+                const float tv = __shfl_up_sync(0xffffffffu, v, o);
+                if (lane + o < 32) u += tu;
+                if (lane >= o) v += tv;
+            }
+            if (lane == 0) sh.carry[0][warp] = u;    // the warp's total of u
+            if (lane == 31) sh.carry[1][warp] = v;   // the warp's total of v
+            __syncthreads();
+            for (int w = warp + 1; w < 4; ++w) u += sh.carry[0][w];
+            for (int w = warp - 1; w >= 0; --w) v += sh.carry[1][w];
+            // (a document start's decay is not dt A: it is 0, and so is its gradient)
+            const float dl = start ? 0.f : rv + u + v + etau * K - d * vx;
+            if (valid) a.ddt[row_io] = fmaf(Ah, dl, vx);
+            dA_acc = fmaf(d, dl, dA_acc);
+            dD_acc += ddv;
+        }
+        __syncthreads();   // the token scans' shared values are read; tiles and TMEM free
+    }
+    // ---- the adjoint of the initial state; this unit's dA and dD shares
+    if (a.dinit && !*(volatile int*)&sh.abort) {
+#pragma unroll
+        for (int p = 0; p < P; ++p) a.dinit[unit * PN + (size_t)p * N + r] = Lm[p];
+    }
+    dA_acc = warp_sum(dA_acc);
+    dD_acc = warp_sum(dD_acc);
+    __syncthreads();
+    if (lane == 0) {
+        sh.red[warp] = dA_acc;
+        sh.red[4 + warp] = dD_acc;
+    }
+    __syncthreads();
+    if (r == 0) {
+        a.ws_dA[unit] = (sh.red[0] + sh.red[1]) + (sh.red[2] + sh.red[3]);
+        a.ws_dD[unit] = (sh.red[4] + sh.red[5]) + (sh.red[6] + sh.red[7]);
+        // every MMA issued has completed before the tensor memory is freed, and (after
+        // a wait that ran out) the last load issued has landed before the CTA exits
+        ptx::mma_commit(&sh.drain);
+        if (!ptx::mbar_wait(&sh.drain, 0, &sh.never, a.wait_iters)) record_error(a.ws, SSD_ERR_TIMEOUT, kWhereDrain);
+        if (nissue > nfull && !ptx::mbar_wait(&sh.full, (nissue - 1) & 1, &sh.never, a.wait_iters))
+            record_error(a.ws, SSD_ERR_TIMEOUT, kWhereDrain);
+    }
+    ptx::tc_fence_before();
+    __syncthreads();
+    ptx::tc_fence_after();
+    if (warp == 0) ptx::tmem_dealloc(tb, kTmCols);
+}
+
+}  // namespace
+
+bool bwd_tc_supported(int P_, int N_, int dtype) { return P_ == P && N_ == N && dtype == SSD_BF16; }
+
+cudaError_t launch_bwd_tc(const BwdArgs& a, cudaStream_t st) {
+    BwdTcParams prm;
+    memset(&prm, 0, sizeof(prm));
+    prm.a = a;
+    if (prm.a.wait_iters == 0) prm.a.wait_iters = kDefaultWaitIters;
+    if (!encode_4d(&prm.tm_x, a.x, P, a.H, a.L, a.batch) || !encode_4d(&prm.tm_dy, a.dy, P, a.H, a.L, a.batch) ||
+        !encode_4d(&prm.tm_B, a.B, N, a.G, a.L, a.batch) || !encode_4d(&prm.tm_C, a.C, N, a.G, a.L, a.batch))
+        return cudaErrorInvalidValue;
+    static std::atomic<uint8_t> ready[kMaxDevices];
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
+    if (!ready[dev].load(std::memory_order_acquire)) {
+        if ((e = cudaFuncSetAttribute(ssd_bwd_tc, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmemBytes)) !=
+            cudaSuccess)
+            return e;
+        ready[dev].store(1, std::memory_order_release);
+    }
+    ssd_bwd_tc<<<(unsigned)(a.batch * a.H), kThreads, kSmemBytes, st>>>(prm);
+    if ((e = cudaGetLastError()) != cudaSuccess) return e;
+    return launch_bwd_reduce(a, st);
+}
+
+}  // namespace ssd

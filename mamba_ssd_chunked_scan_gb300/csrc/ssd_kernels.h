@@ -99,6 +99,8 @@ struct BwdArgs {
     float* ws_dC;          // [batch * L * H * N] per-head shares of dC
     float* ws_dA;          // [batch * H]
     float* ws_dD;          // [batch * H]
+    WsHeader* ws;          // status word (the tensor-core kernel's bounded waits)
+    uint32_t wait_iters;   // poll cap of each bounded wait (0: the default)
 };
 
 // Gated RMS normalisation (ssd_gate_norm): everything its launch needs.
@@ -148,6 +150,12 @@ cudaError_t launch_gate_norm(const GateNormArgs& a, cudaStream_t st);
 size_t bwd_smem_bytes(int Qb, int P, int N);
 int bwd_chunk(int P, int N, size_t smem_limit);
 cudaError_t launch_bwd(const BwdArgs& a, cudaStream_t st);
+// sums the per-head dB, dC shares over each group and the per-row dA, dD shares
+cudaError_t launch_bwd_reduce(const BwdArgs& a, cudaStream_t st);
+// the backward on the tensor cores: bf16, P = 64, N = 128, chunks of 128 tokens
+bool bwd_tc_supported(int P, int N, int dtype);
+constexpr int kBwdTcChunk = 128;
+cudaError_t launch_bwd_tc(const BwdArgs& a, cudaStream_t st);
 size_t step_smem_bytes(int P, int N);
 cudaError_t launch_step(const StepArgs& a, cudaStream_t st);
 cudaError_t launch_segsum_dump(const float* l2, int64_t nrows, int chunk, float* seg, float* L, float* pexp,

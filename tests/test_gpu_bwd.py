@@ -38,7 +38,8 @@ def run_bwd(p, dy, dfin):
     else:
         dyt = torch.from_numpy(dy).cuda()
     dft = None if dfin is None else torch.from_numpy(dfin).cuda()
-    g = ssd.ssd_bwd(d["x"], d["dt"], d["A"], d["B"], d["C"], dyt, d["D"], d["init"], dft, d["cu"])
+    g = ssd.ssd_bwd(d["x"], d["dt"], d["A"], d["B"], d["C"], dyt, d["D"], d["init"], dft, d["cu"],
+                    check_status=True)
     torch.cuda.synchronize()
     return {k: (None if v is None else v.float().cpu().numpy().astype(np.float64)) for k, v in g.items()}
 
@@ -111,3 +112,16 @@ def test_bwd_packed_documents(lens, kw):
     p = synth.make_problem(batch=1, seqlen=sum(lens), nheads=4, ngroups=2, chunk=128, seed=311,
                            doc_lengths=lens, dt_dist="softplus_n22", **kw)
     check(p, with_dfin=False)
+
+
+@pytest.mark.parametrize("kw", [
+    dict(batch=1, seqlen=37, nheads=2, ngroups=1),                          # shorter than a chunk
+    dict(batch=2, seqlen=128 * 3 + 5, nheads=6, ngroups=2),                 # ragged, 3 heads per group
+    dict(batch=1, seqlen=512, nheads=4, ngroups=4, dt_dist="softplus_n22"),  # strong decay, one head per group
+])
+def test_bwd_tensor_core_shapes(kw):
+    """The tensor-core backward (bf16, P 64, N 128, 128-token chunks) with
+    initial and final states."""
+    p = synth.make_problem(headdim=64, dstate=128, chunk=128, dtype="bf16", seed=313, init_std=0.3, **kw)
+    got = check(p)
+    assert got["dinit"] is not None
