@@ -62,7 +62,7 @@ struct BwdTcSmall {
     float part[4][Q];       // per-warp partial corner sums of W
     float red[8];
     float carry[2][4];      // warp totals of the token scans
-    uint64_t full, mma1, mmaV1, mmaDB, mmaDC, mmaF, drain;
+    uint64_t full, mma1, mma2, mmaV1, mmaDB, mmaDC, mmaF, drain;
     uint32_t tmem_base;
     int abort;
     int never;
@@ -72,7 +72,9 @@ constexpr size_t kSmemBytes = 1024 + kTiles + sizeof(BwdTcSmall);
 static_assert(kSmemBytes <= 227 * 1024, "shared memory per CTA");
 
 struct BwdTcParams {
-    CUtensorMap tm_x, tm_dy, tm_B, tm_C;
+    CUtensorMap tm_x, tm_dy, tm_B, tm_C;   // loads (bf16)
+    CUtensorMap tm_dx;                     // store (bf16)
+    CUtensorMap tm_dB, tm_dC;              // stores of this head's shares (fp32)
     BwdArgs a;
 };
 
@@ -102,6 +104,9 @@ __device__ __forceinline__ float bf16hi(uint32_t w) { return __uint_as_float(w &
 
 // offset of element (row r, column j < 128) in a two-slab tile
 __device__ __forceinline__ uint32_t off2(int r, int j) { return (uint32_t)(j >> 6) * 16384u + sw128_off(r, j & 63); }
+// offset of the 16-byte chunk q < 8 (fp32 columns 4q .. 4q + 3) of row r in a
+// 128-row x 32-column fp32 box with the 128-byte swizzle
+__device__ __forceinline__ uint32_t offf(int r, int q) { return (uint32_t)(r * 128 + ((q ^ (r & 7)) << 4)); }
 
 __device__ __forceinline__ bool wait_bar(BwdTcSmall& sh, const BwdArgs& a, uint64_t* bar, uint32_t parity,
                                          uint32_t where) {
@@ -172,6 +177,7 @@ __global__ void __launch_bounds__(kThreads, 1) ssd_bwd_tc(const __grid_constant_
     if (r == 0) {
         ptx::mbar_init(&sh.full, 1);
         ptx::mbar_init(&sh.mma1, 1);
+        ptx::mbar_init(&sh.mma2, 1);
         ptx::mbar_init(&sh.mmaV1, 1);
         ptx::mbar_init(&sh.mmaDB, 1);
         ptx::mbar_init(&sh.mmaDC, 1);
@@ -184,6 +190,9 @@ __global__ void __launch_bounds__(kThreads, 1) ssd_bwd_tc(const __grid_constant_
         ptx::prefetch_tmap(&prm.tm_dy);
         ptx::prefetch_tmap(&prm.tm_B);
         ptx::prefetch_tmap(&prm.tm_C);
+        ptx::prefetch_tmap(&prm.tm_dx);
+        ptx::prefetch_tmap(&prm.tm_dB);
+        ptx::prefetch_tmap(&prm.tm_dC);
     }
     if (warp == 0) ptx::tmem_alloc(&sh.tmem_base, kTmCols);
     ptx::tc_fence_before();
@@ -271,10 +280,22 @@ __global__ void __launch_bounds__(kThreads, 1) ssd_bwd_tc(const __grid_constant_
     }
 
     // ------------------------------------------------------------ phase 2
-    float Lm[P];   // Lam[p][n = r]
+    // Lam^T (lane n, column p) lives in TMEM: each chunk scales it by 2^tau in
+    // place and the update contraction accumulates onto it
+    {
+#pragma unroll 1
+        for (int q = 0; q < 4; ++q) {
+            uint32_t v[16];
 #pragma unroll
-    for (int p = 0; p < P; ++p) Lm[p] = a.dfin ? a.dfin[unit * PN + (size_t)p * N + r] : 0.f;
+            for (int e = 0; e < 16; ++e)
+                v[e] = __float_as_uint(a.dfin ? a.dfin[unit * PN + (size_t)(16 * q + e) * N + r] : 0.f);
+            ptx::tmem_st16(lane_addr + kTmLU + 16 * q, v);
+        }
+        ptx::tmem_st_wait();
+    }
     float dA_acc = 0.f, dD_acc = 0.f;
+    float d_next = (nch > 0 && (int64_t)(nch - 1) * Q + r < L)
+                       ? __ldg(a.dt + ((size_t)b * L + (int64_t)(nch - 1) * Q + r) * a.H + h) : 0.f;
     for (int c = nch - 1; c >= 0 && !*(volatile int*)&sh.abort; --c) {
         const int64_t t0 = (int64_t)c * Q;
         const bool valid = t0 + r < L;
@@ -287,7 +308,8 @@ __global__ void __launch_bounds__(kThreads, 1) ssd_bwd_tc(const __grid_constant_
             ptx::tma_load_4d(sm + kTB + 16384, &prm.tm_B, &sh.full, 64, g, (int)t0, b);
             ptx::tma_load_4d(sm + kTC, &prm.tm_C, &sh.full, 0, g, (int)t0, b);
             ptx::tma_load_4d(sm + kTC + 16384, &prm.tm_C, &sh.full, 64, g, (int)t0, b);
-            if (c > 0) {   // the next chunk's tiles on their way to L2
+            if (c > 0) {   // the next chunk's tiles and incoming state on their way to L2
+                ptx::bulk_prefetch_l2(ckpt + (size_t)(c - 1) * PN, (uint32_t)(PN * 4));
                 const int tp = (int)(t0 - Q);
                 ptx::tma_prefetch_4d(&prm.tm_x, 0, h, tp, b);
                 ptx::tma_prefetch_4d(&prm.tm_dy, 0, h, tp, b);
@@ -297,32 +319,13 @@ __global__ void __launch_bounds__(kThreads, 1) ssd_bwd_tc(const __grid_constant_
                 ptx::tma_prefetch_4d(&prm.tm_C, 64, g, tp, b);
             }
         }
-        const float d = chunk_decays(t0);
-        // S_in and Lam as bf16 (row n = r, p) operands; <Lam, S_in>
-        float kdot = 0.f;
-        {
-            const float* src = ckpt + (size_t)c * PN + r;
-#pragma unroll
-            for (int q = 0; q < 8; ++q) {
-                float sv[8];
-#pragma unroll
-                for (int e = 0; e < 8; ++e) {
-                    sv[e] = src[(size_t)(8 * q + e) * N];
-                    kdot = fmaf(Lm[8 * q + e], sv[e], kdot);
-                }
-                *reinterpret_cast<uint4*>(sm + kTSin + sw128_off(r, 8 * q)) =
-                    make_uint4(pack_bf16(sv[0], sv[1]), pack_bf16(sv[2], sv[3]), pack_bf16(sv[4], sv[5]),
-                               pack_bf16(sv[6], sv[7]));
-                *reinterpret_cast<uint4*>(sm + kTLam + sw128_off(r, 8 * q)) =
-                    make_uint4(pack_bf16(Lm[8 * q], Lm[8 * q + 1]), pack_bf16(Lm[8 * q + 2], Lm[8 * q + 3]),
-                               pack_bf16(Lm[8 * q + 4], Lm[8 * q + 5]), pack_bf16(Lm[8 * q + 6], Lm[8 * q + 7]));
-            }
-            ptx::fence_proxy_async();
-        }
-        kdot = warp_sum(kdot);
-        if (lane == 0) sh.red[warp] = kdot;
+        // log-decays (dt was loaded a chunk earlier); the next chunk's dt
+        const float d = d_next;
+        start = valid && doc_start_tc(a, t0 + r);
+        sh.seg.a[r] = ex2_approx(start ? -INFINITY : d * A2);   // 0 at a document start, 1 past the end
+        sh.dts[r] = d;
+        d_next = (c > 0) ? __ldg(a.dt + ((size_t)b * L + t0 - Q + r) * a.H + h) : 0.f;
         __syncthreads();
-        const float K = (sh.red[0] + sh.red[1]) + (sh.red[2] + sh.red[3]);
         SegsumLinRow<4> row;
         segsum_lin_phase1<4>(sh.seg, row, warp, lane);
         __syncthreads();
@@ -331,9 +334,52 @@ __global__ void __launch_bounds__(kThreads, 1) ssd_bwd_tc(const __grid_constant_
         const float es_r = segsum_lin_suffix<4>(sh.seg, r);
         const float ep_r = row.pe;
         const float etau = sh.seg.tauL;
-        // ---- G, X, V2, SC
+        // S_in and Lam as bf16 (row n = r, p) operands; <Lam, S_in>; Lam^T <- 2^tau Lam^T in TMEM
+        float kdot = 0.f;
+        {
+            const float* src = ckpt + (size_t)c * PN + r;
+#pragma unroll 1
+            for (int hf = 0; hf < 2; ++hf) {
+                float sv[32];
+#pragma unroll
+                for (int p = 0; p < 32; ++p) sv[p] = src[(size_t)(32 * hf + p) * N];
+                uint32_t lv[32];
+                ptx::tmem_load32(lane_addr + kTmLU + 32 * hf, lv);
+#pragma unroll
+                for (int q = 0; q < 4; ++q) {
+                    float lf[8];
+#pragma unroll
+                    for (int e = 0; e < 8; ++e) {
+                        lf[e] = __uint_as_float(lv[8 * q + e]);
+                        kdot = fmaf(lf[e], sv[8 * q + e], kdot);
+                    }
+                    *reinterpret_cast<uint4*>(sm + kTSin + sw128_off(r, 32 * hf + 8 * q)) =
+                        make_uint4(pack_bf16(sv[8 * q], sv[8 * q + 1]), pack_bf16(sv[8 * q + 2], sv[8 * q + 3]),
+                                   pack_bf16(sv[8 * q + 4], sv[8 * q + 5]), pack_bf16(sv[8 * q + 6], sv[8 * q + 7]));
+                    *reinterpret_cast<uint4*>(sm + kTLam + sw128_off(r, 32 * hf + 8 * q)) =
+                        make_uint4(pack_bf16(lf[0], lf[1]), pack_bf16(lf[2], lf[3]), pack_bf16(lf[4], lf[5]),
+                                   pack_bf16(lf[6], lf[7]));
+                }
+                uint32_t lo[16], hi[16];
+#pragma unroll
+                for (int e = 0; e < 16; ++e) {
+                    lo[e] = __float_as_uint(etau * __uint_as_float(lv[e]));
+                    hi[e] = __float_as_uint(etau * __uint_as_float(lv[16 + e]));
+                }
+                ptx::tmem_st16(lane_addr + kTmLU + 32 * hf, lo);
+                ptx::tmem_st16(lane_addr + kTmLU + 32 * hf + 16, hi);
+            }
+            ptx::tmem_st_wait();
+            ptx::fence_proxy_async();
+        }
+        kdot = warp_sum(kdot);
+        if (lane == 0) sh.red[warp] = kdot;
+        // ---- G, X (needed first), then V2, SC
         wait_bar(sh, a, &sh.full, nfull & 1, kWhereLoad);
         ++nfull;
+        ptx::tc_fence_before();
+        __syncthreads();
+        const float K = (sh.red[0] + sh.red[1]) + (sh.red[2] + sh.red[3]);
         if (r == 0) {
             ptx::tc_fence_after();
             constexpr uint32_t idQQ = ptx::idesc_bf16(128, 128, 0, 0);
@@ -344,13 +390,21 @@ __global__ void __launch_bounds__(kThreads, 1) ssd_bwd_tc(const __grid_constant_
 #pragma unroll 1
             for (int kk = 0; kk < 4; ++kk)
                 ptx::mma_ss(tb + kTmX, desc_k1(s0 + kTDY, kk), desc_k1(s0 + kTX, kk), idQQ, kk > 0);
+            ptx::mma_commit(&sh.mma1);
 #pragma unroll 1
             for (int kk = 0; kk < 8; ++kk)
                 ptx::mma_ss(tb + kTmV2, desc_k2(s0 + kTB, kk), desc_mn1(s0 + kTLam, kk), idQP, kk > 0);
 #pragma unroll 1
             for (int kk = 0; kk < 8; ++kk)
                 ptx::mma_ss(tb + kTmSC, desc_k2(s0 + kTC, kk), desc_mn1(s0 + kTSin, kk), idQP, kk > 0);
-            ptx::mma_commit(&sh.mma1);
+            ptx::mma_commit(&sh.mma2);
+        }
+        // this row's x and dy (bf16 pairs), kept for the epilogue before the tiles are rescaled
+        uint4 xv[8], dv[8];
+#pragma unroll
+        for (int q = 0; q < 8; ++q) {
+            xv[q] = *reinterpret_cast<const uint4*>(sm + kTX + sw128_off(r, 8 * q));
+            dv[q] = *reinterpret_cast<const uint4*>(sm + kTDY + sw128_off(r, 8 * q));
         }
         wait_bar(sh, a, &sh.mma1, n1 & 1, kWhereMma1);
         ptx::tc_fence_after();
@@ -363,20 +417,20 @@ __global__ void __launch_bounds__(kThreads, 1) ssd_bwd_tc(const __grid_constant_
             for (int cb = 0; cb < 4; ++cb) {
                 const float rfc = (cb == 0) ? row.rf[0] : (cb == 1) ? row.rf[1] : row.rf[2];
                 const bool below = cb < warp, diag = cb == warp;
+                uint32_t gr[32], xr[32];
+                ptx::tmem_load32x2(lane_addr + kTmG + 32 * cb, gr, lane_addr + kTmX + 32 * cb, xr);
 #pragma unroll
                 for (int hf = 0; hf < 2; ++hf) {
                     const int j0 = 32 * cb + 16 * hf;
-                    uint32_t gr[16], xr[16];
-                    ptx::tmem_load16x2(lane_addr + kTmG + j0, gr, lane_addr + kTmX + j0, xr);
                     float z[16];
                     uint32_t p1[8], p2[8];
 #pragma unroll
                     for (int cc = 0; cc < 16; cc += 2) {
-                        const float l0 = below ? rfc * sh.seg.colL[j0 + cc] : diag ? row.wl[16 * hf + cc] : 0.f;
-                        const float l1 = below ? rfc * sh.seg.colL[j0 + cc + 1] : diag ? row.wl[16 * hf + cc + 1] : 0.f;
-                        const float a1_0 = l0 * __uint_as_float(gr[cc]), a1_1 = l1 * __uint_as_float(gr[cc + 1]);
-                        const float x0 = __uint_as_float(xr[cc]), x1 = __uint_as_float(xr[cc + 1]);
-                        p1[cc / 2] = pack_bf16(a1_0, a1_1);
+                        const int k = 16 * hf + cc;
+                        const float l0 = below ? rfc * sh.seg.colL[j0 + cc] : diag ? row.wl[k] : 0.f;
+                        const float l1 = below ? rfc * sh.seg.colL[j0 + cc + 1] : diag ? row.wl[k + 1] : 0.f;
+                        const float x0 = __uint_as_float(xr[k]), x1 = __uint_as_float(xr[k + 1]);
+                        p1[cc / 2] = pack_bf16(l0 * __uint_as_float(gr[k]), l1 * __uint_as_float(gr[k + 1]));
                         p2[cc / 2] = pack_bf16(l0 * x0, l1 * x1);
                         // W from the bf16 A1 that V1 contracts: the token's own term of
                         // <Lam_t, S_t> and of dt_t x_t . v_t then cancel in dl_t
@@ -397,17 +451,15 @@ __global__ void __launch_bounds__(kThreads, 1) ssd_bwd_tc(const __grid_constant_
                 }
             }
         }
-        {   // x row j = r becomes 2^{s_j} x_j (the X contraction is done)
-            uint8_t* xr = sm + kTX;
+        // x row j = r becomes 2^{s_j} x_j (the X contraction is done)
 #pragma unroll
-            for (int q = 0; q < 8; ++q) {
-                uint4 v = *reinterpret_cast<const uint4*>(xr + sw128_off(r, 8 * q));
-                v.x = pack_bf16(bf16lo(v.x) * es_r, bf16hi(v.x) * es_r);
-                v.y = pack_bf16(bf16lo(v.y) * es_r, bf16hi(v.y) * es_r);
-                v.z = pack_bf16(bf16lo(v.z) * es_r, bf16hi(v.z) * es_r);
-                v.w = pack_bf16(bf16lo(v.w) * es_r, bf16hi(v.w) * es_r);
-                *reinterpret_cast<uint4*>(xr + sw128_off(r, 8 * q)) = v;
-            }
+        for (int q = 0; q < 8; ++q) {
+            const uint4 v = xv[q];
+            *reinterpret_cast<uint4*>(sm + kTX + sw128_off(r, 8 * q)) =
+                make_uint4(pack_bf16(bf16lo(v.x) * es_r, bf16hi(v.x) * es_r),
+                           pack_bf16(bf16lo(v.y) * es_r, bf16hi(v.y) * es_r),
+                           pack_bf16(bf16lo(v.z) * es_r, bf16hi(v.z) * es_r),
+                           pack_bf16(bf16lo(v.w) * es_r, bf16hi(v.w) * es_r));
         }
         ptx::fence_proxy_async();
         ptx::tc_fence_before();
@@ -437,18 +489,19 @@ __global__ void __launch_bounds__(kThreads, 1) ssd_bwd_tc(const __grid_constant_
         for (int cb = 0; cb < 4; ++cb) {
             const float rfc = (cb == 0) ? row.rf[0] : (cb == 1) ? row.rf[1] : row.rf[2];
             const bool below = cb < warp, diag = cb == warp;
+            uint32_t xr[32];
+            ptx::tmem_load32(lane_addr + kTmX + 32 * cb, xr);
 #pragma unroll
             for (int hf = 0; hf < 2; ++hf) {
                 const int j0 = 32 * cb + 16 * hf;
-                uint32_t xr[16];
-                ptx::tmem_load16(lane_addr + kTmX + j0, xr);
                 uint32_t p1[8];
 #pragma unroll
                 for (int cc = 0; cc < 16; cc += 2) {
-                    const float l0 = below ? rfc * sh.seg.colL[j0 + cc] : diag ? row.wl[16 * hf + cc] : 0.f;
-                    const float l1 = below ? rfc * sh.seg.colL[j0 + cc + 1] : diag ? row.wl[16 * hf + cc + 1] : 0.f;
-                    p1[cc / 2] = pack_bf16(l0 * __uint_as_float(xr[cc]) * sh.dts[j0 + cc],
-                                           l1 * __uint_as_float(xr[cc + 1]) * sh.dts[j0 + cc + 1]);
+                    const int k = 16 * hf + cc;
+                    const float l0 = below ? rfc * sh.seg.colL[j0 + cc] : diag ? row.wl[k] : 0.f;
+                    const float l1 = below ? rfc * sh.seg.colL[j0 + cc + 1] : diag ? row.wl[k + 1] : 0.f;
+                    p1[cc / 2] = pack_bf16(l0 * __uint_as_float(xr[k]) * sh.dts[j0 + cc],
+                                           l1 * __uint_as_float(xr[k + 1]) * sh.dts[j0 + cc + 1]);
                 }
 #pragma unroll
                 for (int q = 0; q < 2; ++q)
@@ -456,22 +509,19 @@ __global__ void __launch_bounds__(kThreads, 1) ssd_bwd_tc(const __grid_constant_
                         make_uint4(p1[4 * q], p1[4 * q + 1], p1[4 * q + 2], p1[4 * q + 3]);
             }
         }
-        {
-            uint8_t* dr = sm + kTDY;
 #pragma unroll
-            for (int q = 0; q < 8; ++q) {
-                uint4 v = *reinterpret_cast<const uint4*>(dr + sw128_off(r, 8 * q));
-                v.x = pack_bf16(bf16lo(v.x) * ep_r, bf16hi(v.x) * ep_r);
-                v.y = pack_bf16(bf16lo(v.y) * ep_r, bf16hi(v.y) * ep_r);
-                v.z = pack_bf16(bf16lo(v.z) * ep_r, bf16hi(v.z) * ep_r);
-                v.w = pack_bf16(bf16lo(v.w) * ep_r, bf16hi(v.w) * ep_r);
-                *reinterpret_cast<uint4*>(dr + sw128_off(r, 8 * q)) = v;
-            }
+        for (int q = 0; q < 8; ++q) {
+            const uint4 v = dv[q];
+            *reinterpret_cast<uint4*>(sm + kTDY + sw128_off(r, 8 * q)) =
+                make_uint4(pack_bf16(bf16lo(v.x) * ep_r, bf16hi(v.x) * ep_r),
+                           pack_bf16(bf16lo(v.y) * ep_r, bf16hi(v.y) * ep_r),
+                           pack_bf16(bf16lo(v.z) * ep_r, bf16hi(v.z) * ep_r),
+                           pack_bf16(bf16lo(v.w) * ep_r, bf16hi(v.w) * ep_r));
         }
         ptx::fence_proxy_async();
         ptx::tc_fence_before();
         __syncthreads();
-        // ---- dC = (A2 o dt) B + (2^p o dy) S_in^T; Lam^T update C^T (2^p o dy)
+        // ---- dC = (A2 o dt) B + (2^p o dy) S_in^T; Lam^T += C^T (2^p o dy)
         if (r == 0) {
             ptx::tc_fence_after();
             constexpr uint32_t idC1 = ptx::idesc_bf16(128, 128, 0, 1);
@@ -485,103 +535,90 @@ __global__ void __launch_bounds__(kThreads, 1) ssd_bwd_tc(const __grid_constant_
                 ptx::mma_ss(tb + kTmX, desc_k1(s0 + kTDY, kk), desc_k1(s0 + kTSin, kk), idC2, 1);
 #pragma unroll 1
             for (int kk = 0; kk < 8; ++kk)
-                ptx::mma_ss(tb + kTmLU, desc_mn2(s0 + kTC, kk), desc_mn1(s0 + kTDY, kk), idL, kk > 0);
+                ptx::mma_ss(tb + kTmLU, desc_mn2(s0 + kTC, kk), desc_mn1(s0 + kTDY, kk), idL, 1);
             ptx::mma_commit(&sh.mmaDC);
         }
         // ---- dx and the per-token products (row j = r)
-        const size_t row_io = ((size_t)b * L + t0 + r) * a.H + h;
         float vx = 0.f, lbx = 0.f, scdy = 0.f, ddv = 0.f;
-        {
-            uint4 xv[8], dv[8];
-            const uint4* xg = reinterpret_cast<const uint4*>(static_cast<const __nv_bfloat16*>(a.x) + row_io * P);
-            const uint4* dg = reinterpret_cast<const uint4*>(static_cast<const __nv_bfloat16*>(a.dy) + row_io * P);
+        uint32_t dxo[32];   // dx row, bf16 pairs
+        wait_bar(sh, a, &sh.mma2, n1 & 1, kWhereMma1);
+        ptx::tc_fence_after();
 #pragma unroll
-            for (int q = 0; q < 8; ++q) {
-                xv[q] = valid ? __ldg(xg + q) : make_uint4(0u, 0u, 0u, 0u);
-                dv[q] = valid ? __ldg(dg + q) : make_uint4(0u, 0u, 0u, 0u);
-            }
-            uint32_t dxo[16];
+        for (int hf = 0; hf < 2; ++hf) {
+            uint32_t v1[32], v2[32], sc[32];
+            ptx::tmem_load32x2(lane_addr + kTmV1 + 32 * hf, v1, lane_addr + kTmV2 + 32 * hf, v2);
+            ptx::tmem_load32(lane_addr + kTmSC + 32 * hf, sc);
 #pragma unroll
-            for (int hf = 0; hf < 2; ++hf) {
-                uint32_t v1[32], v2[32], sc[32];
-                ptx::tmem_load32x2(lane_addr + kTmV1 + 32 * hf, v1, lane_addr + kTmV2 + 32 * hf, v2);
-                ptx::tmem_load32(lane_addr + kTmSC + 32 * hf, sc);
-#pragma unroll
-                for (int k = 0; k < 32; k += 2) {
-                    const int q = (32 * hf + k) >> 3, e = (32 * hf + k) & 7;
-                    const uint32_t xw = e == 0 ? xv[q].x : e == 2 ? xv[q].y : e == 4 ? xv[q].z : xv[q].w;
-                    const uint32_t dw = e == 0 ? dv[q].x : e == 2 ? dv[q].y : e == 4 ? dv[q].z : dv[q].w;
-                    const float x0 = bf16lo(xw), x1 = bf16hi(xw), y0 = bf16lo(dw), y1 = bf16hi(dw);
-                    const float w0 = __uint_as_float(v2[k]), w1 = __uint_as_float(v2[k + 1]);
-                    const float v0 = fmaf(es_r, w0, __uint_as_float(v1[k]));
-                    const float v1v = fmaf(es_r, w1, __uint_as_float(v1[k + 1]));
-                    vx = fmaf(v0, x0, fmaf(v1v, x1, vx));
-                    lbx = fmaf(w0, x0, fmaf(w1, x1, lbx));
-                    scdy = fmaf(__uint_as_float(sc[k]), y0, fmaf(__uint_as_float(sc[k + 1]), y1, scdy));
-                    ddv = fmaf(y0, x0, fmaf(y1, x1, ddv));
-                    dxo[(32 * hf + k) / 2 - 16 * hf] = pack_bf16(fmaf(d, v0, Dh * y0), fmaf(d, v1v, Dh * y1));
-                }
-                if (valid) {
-                    uint4* dxg = reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(a.dx) + row_io * P) + 4 * hf;
-#pragma unroll
-                    for (int q = 0; q < 4; ++q)
-                        dxg[q] = make_uint4(dxo[4 * q], dxo[4 * q + 1], dxo[4 * q + 2], dxo[4 * q + 3]);
-                }
+            for (int k = 0; k < 32; k += 2) {
+                const int q = (32 * hf + k) >> 3, e = (32 * hf + k) & 7;
+                const uint32_t xw = e == 0 ? xv[q].x : e == 2 ? xv[q].y : e == 4 ? xv[q].z : xv[q].w;
+                const uint32_t dw = e == 0 ? dv[q].x : e == 2 ? dv[q].y : e == 4 ? dv[q].z : dv[q].w;
+                const float x0 = bf16lo(xw), x1 = bf16hi(xw), y0 = bf16lo(dw), y1 = bf16hi(dw);
+                const float w0 = __uint_as_float(v2[k]), w1 = __uint_as_float(v2[k + 1]);
+                const float v0 = fmaf(es_r, w0, __uint_as_float(v1[k]));
+                const float v1v = fmaf(es_r, w1, __uint_as_float(v1[k + 1]));
+                vx = fmaf(v0, x0, fmaf(v1v, x1, vx));
+                lbx = fmaf(w0, x0, fmaf(w1, x1, lbx));
+                scdy = fmaf(__uint_as_float(sc[k]), y0, fmaf(__uint_as_float(sc[k + 1]), y1, scdy));
+                ddv = fmaf(y0, x0, fmaf(y1, x1, ddv));
+                dxo[(32 * hf + k) / 2] = pack_bf16(fmaf(d, v0, Dh * y0), fmaf(d, v1v, Dh * y1));
             }
         }
-        // ---- this head's share of dB (row j = r), then of dC, then the Lam update
+        // ---- this head's share of dB (row j = r), staged for TMA stores in tiles the
+        // dB contraction has finished reading: 2^s x (box 0), Lam (box 1), A2 (boxes 2, 3)
         wait_bar(sh, a, &sh.mmaDB, n1 & 1, kWhereDB);
         ptx::tc_fence_after();
         {
-            // (the TMEM loads are warp-wide: every lane takes part, valid rows store)
-            float4* out = reinterpret_cast<float4*>(a.ws_dB + row_io * N);
-#pragma unroll 1
-            for (int hf = 0; hf < 2; ++hf) {
-                uint32_t d0[32], d1[32];
-                ptx::tmem_load32x2(lane_addr + kTmG + 64 * hf, d0, lane_addr + kTmG + 64 * hf + 32, d1);
-                if (valid) {
+            uint8_t* box[4] = {sm + kTX, sm + kTLam, sm + kT2, sm + kT2 + 16384};
 #pragma unroll
-                    for (int q = 0; q < 8; ++q) {
-                        out[16 * hf + q] =
-                            make_float4(d * __uint_as_float(d0[4 * q]), d * __uint_as_float(d0[4 * q + 1]),
-                                        d * __uint_as_float(d0[4 * q + 2]), d * __uint_as_float(d0[4 * q + 3]));
-                        out[16 * hf + 8 + q] =
-                            make_float4(d * __uint_as_float(d1[4 * q]), d * __uint_as_float(d1[4 * q + 1]),
-                                        d * __uint_as_float(d1[4 * q + 2]), d * __uint_as_float(d1[4 * q + 3]));
-                    }
-                }
+            for (int k = 0; k < 4; ++k) {
+                uint32_t v[32];
+                ptx::tmem_load32(lane_addr + kTmG + 32 * k, v);
+#pragma unroll
+                for (int q = 0; q < 8; ++q)
+                    *reinterpret_cast<float4*>(box[k] + offf(r, q)) =
+                        make_float4(d * __uint_as_float(v[4 * q]), d * __uint_as_float(v[4 * q + 1]),
+                                    d * __uint_as_float(v[4 * q + 2]), d * __uint_as_float(v[4 * q + 3]));
             }
         }
+        // ---- dC (row i = r) over A2 o dt (boxes 0, 1) and B (boxes 2, 3), dx over
+        // S_in, once the dC and Lam contractions are done
         wait_bar(sh, a, &sh.mmaDC, n1 & 1, kWhereDC);
         ++n1;
         ptx::tc_fence_after();
         {
-            float4* out = reinterpret_cast<float4*>(a.ws_dC + row_io * N);
-#pragma unroll 1
-            for (int hf = 0; hf < 2; ++hf) {
-                uint32_t d0[32], d1[32];
-                ptx::tmem_load32x2(lane_addr + kTmX + 64 * hf, d0, lane_addr + kTmX + 64 * hf + 32, d1);
-                if (valid) {
+            uint8_t* box[4] = {sm + kT1, sm + kT1 + 16384, sm + kTB, sm + kTB + 16384};
 #pragma unroll
-                    for (int q = 0; q < 8; ++q) {
-                        out[16 * hf + q] = make_float4(__uint_as_float(d0[4 * q]), __uint_as_float(d0[4 * q + 1]),
-                                                       __uint_as_float(d0[4 * q + 2]), __uint_as_float(d0[4 * q + 3]));
-                        out[16 * hf + 8 + q] =
-                            make_float4(__uint_as_float(d1[4 * q]), __uint_as_float(d1[4 * q + 1]),
-                                        __uint_as_float(d1[4 * q + 2]), __uint_as_float(d1[4 * q + 3]));
-                    }
-                }
-            }
-            uint32_t l0[32], l1[32];
-            ptx::tmem_load32x2(lane_addr + kTmLU, l0, lane_addr + kTmLU + 32, l1);
+            for (int k = 0; k < 4; ++k) {
+                uint32_t v[32];
+                ptx::tmem_load32(lane_addr + kTmX + 32 * k, v);
 #pragma unroll
-            for (int p = 0; p < 32; ++p) {
-                Lm[p] = fmaf(etau, Lm[p], __uint_as_float(l0[p]));
-                Lm[p + 32] = fmaf(etau, Lm[p + 32], __uint_as_float(l1[p]));
+                for (int q = 0; q < 8; ++q)
+                    *reinterpret_cast<float4*>(box[k] + offf(r, q)) =
+                        make_float4(__uint_as_float(v[4 * q]), __uint_as_float(v[4 * q + 1]),
+                                    __uint_as_float(v[4 * q + 2]), __uint_as_float(v[4 * q + 3]));
             }
+#pragma unroll
+            for (int q = 0; q < 8; ++q)
+                *reinterpret_cast<uint4*>(sm + kTSin + sw128_off(r, 8 * q)) =
+                    make_uint4(dxo[4 * q], dxo[4 * q + 1], dxo[4 * q + 2], dxo[4 * q + 3]);
         }
+        ptx::fence_proxy_async();
         ptx::tc_fence_before();
-        __syncthreads();   // sh.part complete
+        __syncthreads();   // staged rows complete; sh.part complete
+        if (r == 0) {
+            // rows past the sequence's end are clipped by the tensor maps
+            ptx::tma_store_4d(&prm.tm_dB, sm + kTX, 0, h, (int)t0, b);
+            ptx::tma_store_4d(&prm.tm_dB, sm + kTLam, 32, h, (int)t0, b);
+            ptx::tma_store_4d(&prm.tm_dB, sm + kT2, 64, h, (int)t0, b);
+            ptx::tma_store_4d(&prm.tm_dB, sm + kT2 + 16384, 96, h, (int)t0, b);
+            ptx::tma_store_4d(&prm.tm_dC, sm + kT1, 0, h, (int)t0, b);
+            ptx::tma_store_4d(&prm.tm_dC, sm + kT1 + 16384, 32, h, (int)t0, b);
+            ptx::tma_store_4d(&prm.tm_dC, sm + kTB, 64, h, (int)t0, b);
+            ptx::tma_store_4d(&prm.tm_dC, sm + kTB + 16384, 96, h, (int)t0, b);
+            ptx::tma_store_4d(&prm.tm_dx, sm + kTSin, 0, h, (int)t0, b);
+            ptx::bulk_commit();
+        }
         // ---- ddt of token t = r, dA and dD
         {
             const float rv = (sh.part[0][r] + sh.part[1][r]) + (sh.part[2][r] + sh.part[3][r]);
@@ -601,16 +638,23 @@ __global__ void __launch_bounds__(kThreads, 1) ssd_bwd_tc(const __grid_constant_
             for (int w = warp - 1; w >= 0; --w) v += sh.carry[1][w];
             // (a document start's decay is not dt A: it is 0, and so is its gradient)
             const float dl = start ? 0.f : rv + u + v + etau * K - d * vx;
-            if (valid) a.ddt[row_io] = fmaf(Ah, dl, vx);
+            if (valid) a.ddt[((size_t)b * L + t0 + r) * a.H + h] = fmaf(Ah, dl, vx);
             dA_acc = fmaf(d, dl, dA_acc);
             dD_acc += ddv;
         }
+        if (r == 0) ptx::bulk_wait_read0();   // the stores have read their staged tiles
         __syncthreads();   // the token scans' shared values are read; tiles and TMEM free
     }
     // ---- the adjoint of the initial state; this unit's dA and dD shares
     if (a.dinit && !*(volatile int*)&sh.abort) {
+        ptx::tc_fence_after();
+        uint32_t l0[32], l1[32];
+        ptx::tmem_load32x2(lane_addr + kTmLU, l0, lane_addr + kTmLU + 32, l1);
 #pragma unroll
-        for (int p = 0; p < P; ++p) a.dinit[unit * PN + (size_t)p * N + r] = Lm[p];
+        for (int p = 0; p < 32; ++p) {
+            a.dinit[unit * PN + (size_t)p * N + r] = __uint_as_float(l0[p]);
+            a.dinit[unit * PN + (size_t)(p + 32) * N + r] = __uint_as_float(l1[p]);
+        }
     }
     dA_acc = warp_sum(dA_acc);
     dD_acc = warp_sum(dD_acc);
@@ -621,6 +665,7 @@ __global__ void __launch_bounds__(kThreads, 1) ssd_bwd_tc(const __grid_constant_
     }
     __syncthreads();
     if (r == 0) {
+        ptx::bulk_wait0();   // this CTA's stores are complete
         a.ws_dA[unit] = (sh.red[0] + sh.red[1]) + (sh.red[2] + sh.red[3]);
         a.ws_dD[unit] = (sh.red[4] + sh.red[5]) + (sh.red[6] + sh.red[7]);
         // every MMA issued has completed before the tensor memory is freed, and (after
@@ -646,7 +691,10 @@ cudaError_t launch_bwd_tc(const BwdArgs& a, cudaStream_t st) {
     prm.a = a;
     if (prm.a.wait_iters == 0) prm.a.wait_iters = kDefaultWaitIters;
     if (!encode_4d(&prm.tm_x, a.x, P, a.H, a.L, a.batch) || !encode_4d(&prm.tm_dy, a.dy, P, a.H, a.L, a.batch) ||
-        !encode_4d(&prm.tm_B, a.B, N, a.G, a.L, a.batch) || !encode_4d(&prm.tm_C, a.C, N, a.G, a.L, a.batch))
+        !encode_4d(&prm.tm_B, a.B, N, a.G, a.L, a.batch) || !encode_4d(&prm.tm_C, a.C, N, a.G, a.L, a.batch) ||
+        !encode_4d(&prm.tm_dx, a.dx, P, a.H, a.L, a.batch) ||
+        !encode_4d_f32(&prm.tm_dB, a.ws_dB, N, a.H, a.L, a.batch) ||
+        !encode_4d_f32(&prm.tm_dC, a.ws_dC, N, a.H, a.L, a.batch))
         return cudaErrorInvalidValue;
     static std::atomic<uint8_t> ready[kMaxDevices];
     int dev = 0;

@@ -138,6 +138,8 @@ cudaError_t launch_split_scan(const FwdArgs& a, cudaStream_t st);
 // 4-D TMA map over a (batch, L, heads_or_groups, inner) bf16 tensor; box = one
 // 64-element x 128-row tile of one head (group), 128-byte swizzle.
 bool encode_4d(CUtensorMap* tm, const void* base, int64_t inner, int64_t mid, int64_t L, int64_t batch);
+// the same over an fp32 tensor; box = one 32-element x 128-row tile
+bool encode_4d_f32(CUtensorMap* tm, const void* base, int64_t inner, int64_t mid, int64_t L, int64_t batch);
 size_t tc_smem_bytes();
 bool tc_supported(int P, int N, int Q, int dtype);
 cudaError_t launch_tc(const FwdArgs& a, cudaStream_t st);
