@@ -188,11 +188,13 @@ bool bwd_layout(const ssd_params_t* p, BwdLayout* l) {
     const size_t bh = (size_t)p->batch * p->nheads;
     const size_t nch = (size_t)((p->seqlen + l->Qb - 1) / l->Qb);
     const size_t PN = (size_t)p->headdim * p->dstate;
+    // per-head shares of dB and dC: bf16 from the tensor-core backward, else fp32
+    const size_t share_elem = bwd_use_tc(p) ? 2 : 4;
     const size_t share = (size_t)p->batch * p->seqlen * p->nheads * p->dstate;
     size_t o = sizeof(WsHeader);
     l->ckpt = o;  o = align_up(o + bh * nch * PN * sizeof(float), 256);
-    l->dB = o;    o = align_up(o + share * sizeof(float), 256);
-    l->dC = o;    o = align_up(o + share * sizeof(float), 256);
+    l->dB = o;    o = align_up(o + share * share_elem, 256);
+    l->dC = o;    o = align_up(o + share * share_elem, 256);
     l->dA = o;    o = align_up(o + bh * sizeof(float), 256);
     l->dD = o;    o = align_up(o + bh * sizeof(float), 256);
     l->total = o;
@@ -522,6 +524,7 @@ int ssd_bwd(const ssd_params_t* p, const void* x, const float* dt, const float* 
     a.ws_dD = (float*)(ws + l.dD);
     a.ws = (WsHeader*)ws;
     a.wait_iters = kDefaultWaitIters;
+    a.shares_bf16 = bwd_use_tc(p) ? 1 : 0;
     // a fresh status word for this call's bounded device waits
     if (cudaMemsetAsync(ws, 0, sizeof(WsHeader), (cudaStream_t)stream) != cudaSuccess) return SSD_ERR_CUDA;
     if ((bwd_use_tc(p) ? launch_bwd_tc(a, (cudaStream_t)stream) : launch_bwd(a, (cudaStream_t)stream)) != cudaSuccess)

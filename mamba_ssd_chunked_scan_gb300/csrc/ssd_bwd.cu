@@ -679,10 +679,13 @@ __global__ void __launch_bounds__(kBwdThreads) ssd_bwd_chunk(BwdArgs a) {
     }
 }
 
-// dB, dC (batch, L, G, N) = sums over each group's heads of the per-head shares;
-// dA, dD (H) = sums over the batch rows.  Fixed summation order.
-template <typename T>
+// dB, dC (batch, L, G, N) = sums over each group's heads of the per-head shares
+// (fp32, or bf16 from the tensor-core backward), in fp32; dA, dD (H) = sums over
+// the batch rows.  Fixed summation order.
+template <typename T, typename S>
 __global__ void __launch_bounds__(256) ssd_bwd_reduce(BwdArgs a) {
+    const S* shB = reinterpret_cast<const S*>(a.ws_dB);
+    const S* shC = reinterpret_cast<const S*>(a.ws_dC);
     const int64_t total = a.batch * a.L * a.G * a.N;
     const int hpg = a.H / a.G;
     for (int64_t k = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; k < total; k += (int64_t)gridDim.x * blockDim.x) {
@@ -693,8 +696,8 @@ __global__ void __launch_bounds__(256) ssd_bwd_reduce(BwdArgs a) {
         float sb = 0.f, sc = 0.f;
         for (int hh = 0; hh < hpg; ++hh) {
             const size_t o = ((size_t)bt * a.H + g * hpg + hh) * a.N + n;
-            sb += a.ws_dB[o];
-            sc += a.ws_dC[o];
+            sb += Elem<S>::load(shB + o);
+            sc += Elem<S>::load(shC + o);
         }
         Elem<T>::store(static_cast<T*>(a.dB) + k, sb);
         Elem<T>::store(static_cast<T*>(a.dC) + k, sc);
@@ -747,7 +750,9 @@ cudaError_t launch_bwd_reduce(const BwdArgs& a, cudaStream_t st) {
     int64_t blocks = (total + 255) / 256;
     if (blocks > (int64_t)nsm * 8) blocks = (int64_t)nsm * 8;
     if (blocks < 1) blocks = 1;
-    auto k2 = a.dtype == SSD_BF16 ? ssd_bwd_reduce<__nv_bfloat16> : ssd_bwd_reduce<float>;
+    auto k2 = a.dtype == SSD_BF16
+                  ? (a.shares_bf16 ? ssd_bwd_reduce<__nv_bfloat16, __nv_bfloat16> : ssd_bwd_reduce<__nv_bfloat16, float>)
+                  : ssd_bwd_reduce<float, float>;
     k2<<<(unsigned)blocks, 256, 0, st>>>(a);
     return cudaGetLastError();
 }

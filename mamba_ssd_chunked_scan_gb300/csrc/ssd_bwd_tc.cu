@@ -74,7 +74,7 @@ static_assert(kSmemBytes <= 227 * 1024, "shared memory per CTA");
 struct BwdTcParams {
     CUtensorMap tm_x, tm_dy, tm_B, tm_C;   // loads (bf16)
     CUtensorMap tm_dx;                     // store (bf16)
-    CUtensorMap tm_dB, tm_dC;              // stores of this head's shares (fp32)
+    CUtensorMap tm_dB, tm_dC;              // stores of this head's shares (bf16)
     BwdArgs a;
 };
 
@@ -104,9 +104,6 @@ __device__ __forceinline__ float bf16hi(uint32_t w) { return __uint_as_float(w &
 
 // offset of element (row r, column j < 128) in a two-slab tile
 __device__ __forceinline__ uint32_t off2(int r, int j) { return (uint32_t)(j >> 6) * 16384u + sw128_off(r, j & 63); }
-// offset of the 16-byte chunk q < 8 (fp32 columns 4q .. 4q + 3) of row r in a
-// 128-row x 32-column fp32 box with the 128-byte swizzle
-__device__ __forceinline__ uint32_t offf(int r, int q) { return (uint32_t)(r * 128 + ((q ^ (r & 7)) << 4)); }
 
 __device__ __forceinline__ bool wait_bar(BwdTcSmall& sh, const BwdArgs& a, uint64_t* bar, uint32_t parity,
                                          uint32_t where) {
@@ -325,6 +322,7 @@ __global__ void __launch_bounds__(kThreads, 1) ssd_bwd_tc(const __grid_constant_
         sh.seg.a[r] = ex2_approx(start ? -INFINITY : d * A2);   // 0 at a document start, 1 past the end
         sh.dts[r] = d;
         d_next = (c > 0) ? __ldg(a.dt + ((size_t)b * L + t0 - Q + r) * a.H + h) : 0.f;
+        if (r == 0) ptx::bulk_wait_read0();   // the last chunk's stores have read S_in, A1 and A2
         __syncthreads();
         SegsumLinRow<4> row;
         segsum_lin_phase1<4>(sh.seg, row, warp, lane);
@@ -564,58 +562,54 @@ __global__ void __launch_bounds__(kThreads, 1) ssd_bwd_tc(const __grid_constant_
                 dxo[(32 * hf + k) / 2] = pack_bf16(fmaf(d, v0, Dh * y0), fmaf(d, v1v, Dh * y1));
             }
         }
-        // ---- this head's share of dB (row j = r), staged for TMA stores in tiles the
-        // dB contraction has finished reading: 2^s x (box 0), Lam (box 1), A2 (boxes 2, 3)
+        // ---- this head's share of dB (row j = r) as bf16, staged for a TMA store over A2
+        // (which the dB contraction has finished reading)
         wait_bar(sh, a, &sh.mmaDB, n1 & 1, kWhereDB);
         ptx::tc_fence_after();
-        {
-            uint8_t* box[4] = {sm + kTX, sm + kTLam, sm + kT2, sm + kT2 + 16384};
+#pragma unroll 1
+        for (int k = 0; k < 4; ++k) {
+            uint32_t v[32];
+            ptx::tmem_load32(lane_addr + kTmG + 32 * k, v);
 #pragma unroll
-            for (int k = 0; k < 4; ++k) {
-                uint32_t v[32];
-                ptx::tmem_load32(lane_addr + kTmG + 32 * k, v);
-#pragma unroll
-                for (int q = 0; q < 8; ++q)
-                    *reinterpret_cast<float4*>(box[k] + offf(r, q)) =
-                        make_float4(d * __uint_as_float(v[4 * q]), d * __uint_as_float(v[4 * q + 1]),
-                                    d * __uint_as_float(v[4 * q + 2]), d * __uint_as_float(v[4 * q + 3]));
-            }
+            for (int q = 0; q < 4; ++q)
+                *reinterpret_cast<uint4*>(sm + kT2 + off2(r, 32 * k + 8 * q)) = make_uint4(
+                    pack_bf16(d * __uint_as_float(v[8 * q]), d * __uint_as_float(v[8 * q + 1])),
+                    pack_bf16(d * __uint_as_float(v[8 * q + 2]), d * __uint_as_float(v[8 * q + 3])),
+                    pack_bf16(d * __uint_as_float(v[8 * q + 4]), d * __uint_as_float(v[8 * q + 5])),
+                    pack_bf16(d * __uint_as_float(v[8 * q + 6]), d * __uint_as_float(v[8 * q + 7])));
         }
-        // ---- dC (row i = r) over A2 o dt (boxes 0, 1) and B (boxes 2, 3), dx over
-        // S_in, once the dC and Lam contractions are done
+        // ---- dC (row i = r) as bf16 over A2 o dt, dx over S_in, once the dC and Lam
+        // contractions are done
         wait_bar(sh, a, &sh.mmaDC, n1 & 1, kWhereDC);
         ++n1;
         ptx::tc_fence_after();
-        {
-            uint8_t* box[4] = {sm + kT1, sm + kT1 + 16384, sm + kTB, sm + kTB + 16384};
+#pragma unroll 1
+        for (int k = 0; k < 4; ++k) {
+            uint32_t v[32];
+            ptx::tmem_load32(lane_addr + kTmX + 32 * k, v);
 #pragma unroll
-            for (int k = 0; k < 4; ++k) {
-                uint32_t v[32];
-                ptx::tmem_load32(lane_addr + kTmX + 32 * k, v);
-#pragma unroll
-                for (int q = 0; q < 8; ++q)
-                    *reinterpret_cast<float4*>(box[k] + offf(r, q)) =
-                        make_float4(__uint_as_float(v[4 * q]), __uint_as_float(v[4 * q + 1]),
-                                    __uint_as_float(v[4 * q + 2]), __uint_as_float(v[4 * q + 3]));
-            }
-#pragma unroll
-            for (int q = 0; q < 8; ++q)
-                *reinterpret_cast<uint4*>(sm + kTSin + sw128_off(r, 8 * q)) =
-                    make_uint4(dxo[4 * q], dxo[4 * q + 1], dxo[4 * q + 2], dxo[4 * q + 3]);
+            for (int q = 0; q < 4; ++q)
+                *reinterpret_cast<uint4*>(sm + kT1 + off2(r, 32 * k + 8 * q)) = make_uint4(
+                    pack_bf16(__uint_as_float(v[8 * q]), __uint_as_float(v[8 * q + 1])),
+                    pack_bf16(__uint_as_float(v[8 * q + 2]), __uint_as_float(v[8 * q + 3])),
+                    pack_bf16(__uint_as_float(v[8 * q + 4]), __uint_as_float(v[8 * q + 5])),
+                    pack_bf16(__uint_as_float(v[8 * q + 6]), __uint_as_float(v[8 * q + 7])));
         }
+#pragma unroll
+        for (int q = 0; q < 8; ++q)
+            *reinterpret_cast<uint4*>(sm + kTSin + sw128_off(r, 8 * q)) =
+                make_uint4(dxo[4 * q], dxo[4 * q + 1], dxo[4 * q + 2], dxo[4 * q + 3]);
         ptx::fence_proxy_async();
         ptx::tc_fence_before();
         __syncthreads();   // staged rows complete; sh.part complete
         if (r == 0) {
-            // rows past the sequence's end are clipped by the tensor maps
-            ptx::tma_store_4d(&prm.tm_dB, sm + kTX, 0, h, (int)t0, b);
-            ptx::tma_store_4d(&prm.tm_dB, sm + kTLam, 32, h, (int)t0, b);
-            ptx::tma_store_4d(&prm.tm_dB, sm + kT2, 64, h, (int)t0, b);
-            ptx::tma_store_4d(&prm.tm_dB, sm + kT2 + 16384, 96, h, (int)t0, b);
+            // (rows past the sequence's end are clipped by the tensor maps; the next
+            // chunk rewrites these tiles only after its segsum, by which time thread 0
+            // has waited for the stores to read them)
+            ptx::tma_store_4d(&prm.tm_dB, sm + kT2, 0, h, (int)t0, b);
+            ptx::tma_store_4d(&prm.tm_dB, sm + kT2 + 16384, 64, h, (int)t0, b);
             ptx::tma_store_4d(&prm.tm_dC, sm + kT1, 0, h, (int)t0, b);
-            ptx::tma_store_4d(&prm.tm_dC, sm + kT1 + 16384, 32, h, (int)t0, b);
-            ptx::tma_store_4d(&prm.tm_dC, sm + kTB, 64, h, (int)t0, b);
-            ptx::tma_store_4d(&prm.tm_dC, sm + kTB + 16384, 96, h, (int)t0, b);
+            ptx::tma_store_4d(&prm.tm_dC, sm + kT1 + 16384, 64, h, (int)t0, b);
             ptx::tma_store_4d(&prm.tm_dx, sm + kTSin, 0, h, (int)t0, b);
             ptx::bulk_commit();
         }
@@ -642,8 +636,7 @@ __global__ void __launch_bounds__(kThreads, 1) ssd_bwd_tc(const __grid_constant_
             dA_acc = fmaf(d, dl, dA_acc);
             dD_acc += ddv;
         }
-        if (r == 0) ptx::bulk_wait_read0();   // the stores have read their staged tiles
-        __syncthreads();   // the token scans' shared values are read; tiles and TMEM free
+        __syncthreads();   // the token scans' shared values are read; TMEM free
     }
     // ---- the adjoint of the initial state; this unit's dA and dD shares
     if (a.dinit && !*(volatile int*)&sh.abort) {
@@ -693,8 +686,7 @@ cudaError_t launch_bwd_tc(const BwdArgs& a, cudaStream_t st) {
     if (!encode_4d(&prm.tm_x, a.x, P, a.H, a.L, a.batch) || !encode_4d(&prm.tm_dy, a.dy, P, a.H, a.L, a.batch) ||
         !encode_4d(&prm.tm_B, a.B, N, a.G, a.L, a.batch) || !encode_4d(&prm.tm_C, a.C, N, a.G, a.L, a.batch) ||
         !encode_4d(&prm.tm_dx, a.dx, P, a.H, a.L, a.batch) ||
-        !encode_4d_f32(&prm.tm_dB, a.ws_dB, N, a.H, a.L, a.batch) ||
-        !encode_4d_f32(&prm.tm_dC, a.ws_dC, N, a.H, a.L, a.batch))
+        !encode_4d(&prm.tm_dB, a.ws_dB, N, a.H, a.L, a.batch) || !encode_4d(&prm.tm_dC, a.ws_dC, N, a.H, a.L, a.batch))
         return cudaErrorInvalidValue;
     static std::atomic<uint8_t> ready[kMaxDevices];
     int dev = 0;

@@ -95,8 +95,9 @@ struct BwdArgs {
     float* dD;
     float* dinit;
     float* ws_ckpt;        // [batch * H * nchunks * P * N] state entering each chunk
-    float* ws_dB;          // [batch * L * H * N] per-head shares of dB
+    float* ws_dB;          // [batch * L * H * N] per-head shares of dB (fp32, or bf16: shares_bf16)
     float* ws_dC;          // [batch * L * H * N] per-head shares of dC
+    int shares_bf16;       // the shares are bf16 (the tensor-core backward)
     float* ws_dA;          // [batch * H]
     float* ws_dD;          // [batch * H]
     WsHeader* ws;          // status word (the tensor-core kernel's bounded waits)
@@ -138,8 +139,6 @@ cudaError_t launch_split_scan(const FwdArgs& a, cudaStream_t st);
 // 4-D TMA map over a (batch, L, heads_or_groups, inner) bf16 tensor; box = one
 // 64-element x 128-row tile of one head (group), 128-byte swizzle.
 bool encode_4d(CUtensorMap* tm, const void* base, int64_t inner, int64_t mid, int64_t L, int64_t batch);
-// the same over an fp32 tensor; box = one 32-element x 128-row tile
-bool encode_4d_f32(CUtensorMap* tm, const void* base, int64_t inner, int64_t mid, int64_t L, int64_t batch);
 size_t tc_smem_bytes();
 bool tc_supported(int P, int N, int Q, int dtype);
 cudaError_t launch_tc(const FwdArgs& a, cudaStream_t st);

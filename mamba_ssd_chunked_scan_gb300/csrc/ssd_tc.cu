@@ -1147,22 +1147,6 @@ bool encode_4d(CUtensorMap* tm, const void* base, int64_t inner, int64_t mid, in
     return r == CUDA_SUCCESS;
 }
 
-// 4-D map over a (batch, L, heads, inner) fp32 tensor; box = one 32-element
-// (128-byte) x 128-row tile of one head, 128-byte swizzle.
-bool encode_4d_f32(CUtensorMap* tm, const void* base, int64_t inner, int64_t mid, int64_t L, int64_t batch) {
-    auto enc = get_encode();
-    if (!enc) return false;
-    cuuint64_t dims[4] = {(cuuint64_t)inner, (cuuint64_t)mid, (cuuint64_t)L, (cuuint64_t)batch};
-    cuuint64_t strides[3] = {(cuuint64_t)(inner * 4), (cuuint64_t)(inner * mid * 4),
-                             (cuuint64_t)(inner * mid * L * 4)};
-    cuuint32_t box[4] = {32, 1, 128, 1};
-    cuuint32_t es[4] = {1, 1, 1, 1};
-    CUresult r = enc(tm, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, const_cast<void*>(base), dims, strides, box, es,
-                     CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-                     CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
-    return r == CUDA_SUCCESS;
-}
-
 size_t tc_smem_bytes() { return kSmemBytes; }
 
 bool tc_supported(int P_, int N_, int Q_, int dtype) {

@@ -170,13 +170,13 @@ def test_step_invalid_args(L, kw, code):
 
 def test_bwd_workspace_size(L):
     # status header + chunk-entry states + dB, dC shares + dA, dD shares; the bf16
-    # Mamba-2 head shape runs the tensor-core backward (128-token chunks), fp32 the
-    # CUDA-core one (32-token chunks)
-    shares = 2 * 2 * 1000 * 4 * 128 * 4 + 2 * 8 * 4
+    # Mamba-2 head shape runs the tensor-core backward (128-token chunks, bf16
+    # shares), fp32 the CUDA-core one (32-token chunks, fp32 shares)
+    shares = 2 * 2 * 1000 * 4 * 128
     n = L.lib.ssd_bwd_workspace_size(ctypes.byref(params(L, batch=2, seqlen=1000, nheads=4)))
-    assert n >= 256 + 2 * 4 * 8 * 64 * 128 * 4 + shares
+    assert n >= 256 + 2 * 4 * 8 * 64 * 128 * 4 + 2 * shares + 2 * 8 * 4
     n = L.lib.ssd_bwd_workspace_size(ctypes.byref(params(L, batch=2, seqlen=1000, nheads=4, dtype=0)))
-    assert n >= 256 + 2 * 4 * 32 * 64 * 128 * 4 + shares
+    assert n >= 256 + 2 * 4 * 32 * 64 * 128 * 4 + 4 * shares + 2 * 8 * 4
     assert L.lib.ssd_bwd_workspace_size(ctypes.byref(params(L, ndocs=3, batch=1))) > 0    # packed documents
     assert L.lib.ssd_bwd_workspace_size(ctypes.byref(params(L, headdim=128, dstate=128))) == 0   # P * N > 8192
 

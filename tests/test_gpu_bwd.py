@@ -118,6 +118,7 @@ def test_bwd_packed_documents(lens, kw):
     dict(batch=1, seqlen=37, nheads=2, ngroups=1),                          # shorter than a chunk
     dict(batch=2, seqlen=128 * 3 + 5, nheads=6, ngroups=2),                 # ragged, 3 heads per group
     dict(batch=1, seqlen=512, nheads=4, ngroups=4, dt_dist="softplus_n22"),  # strong decay, one head per group
+    dict(batch=1, seqlen=256, nheads=32, ngroups=1),                        # 32 heads' shares summed per group
 ])
 def test_bwd_tensor_core_shapes(kw):
     """The tensor-core backward (bf16, P 64, N 128, 128-token chunks) with
