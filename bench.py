@@ -48,11 +48,12 @@ METRIC = "SSD fwd tokens/s and achieved HBM GB/s (% of GB300 roofline) vs L, 1 G
 # one sequence, 32 heads, split length 2048, initial and final states)
 DEFAULT_WORKLOAD = "long"
 FALLBACK_HBM_GBS = 6800.0
+FALLBACK_BF16_TFLOPS = 1900.0   # dense bf16, burst
 
 
 DECODE_METRIC = "SSD decode step tokens/s and achieved HBM GB/s on the resident state, 1 GPU"
 GATE_NORM_METRIC = "gated RMS norm of the scan output, tokens/s and achieved HBM GB/s, 1 GPU"
-BWD_METRIC = "SSD bwd tokens/s and achieved fp32 TFLOP/s (% of the CUDA-core fp32 peak), 1 GPU"
+BWD_METRIC = "SSD bwd tokens/s and achieved TFLOP/s against the kernel's peak, 1 GPU"
 # fp32 CUDA-core peak: 152 SMs x 128 fp32 lanes x 2 flop (FMA) x 2.07 GHz (maximum SM clock)
 FP32_PEAK_TFLOPS = 152 * 128 * 2 * 2.07e9 / 1e12
 
@@ -64,6 +65,22 @@ def bwd_flops(p, Qb=32) -> float:
     sum) + N (2P + Qb) (dB and dC)."""
     P, N = p.headdim, p.dstate
     mac = 2 * P * N + Qb * (N + P) / 2 + P * (2 * N + Qb / 2) + N * (2 * P + Qb)
+    return 2.0 * mac * p.batch * p.seqlen * p.nheads
+
+
+def bwd_uses_tensor_cores(p) -> bool:
+    """ssd_bwd runs on the tensor cores for the bf16 Mamba-2 head shape."""
+    return p.dtype == "bf16" and p.headdim == 64 and p.dstate == 128
+
+
+def bwd_tc_flops(p, Q=128) -> float:
+    """Algorithmic flops of the tensor-core backward's contractions (2 per
+    multiply-add, the causal lower triangles only): per token and head, 6PN
+    (the chunk-entry states, B Lam^T, C S_in^T, the two state terms of dB and
+    dC, the adjoint update) + Q (3N/2 + P) (C B^T, dy x^T, (L o G)^T dy and the
+    masked products of dB and dC)."""
+    P, N = p.headdim, p.dstate
+    mac = 6 * P * N + Q * (1.5 * N + P)
     return 2.0 * mac * p.batch * p.seqlen * p.nheads
 
 
@@ -107,6 +124,19 @@ def decode_bytes(p) -> int:
     e = 2 if p.dtype == "bf16" else 4
     bh = p.batch * p.nheads
     return bh * (2 * p.headdim * p.dstate * 4 + 2 * p.headdim * e + 4) + p.batch * p.ngroups * 2 * p.dstate * e
+
+
+def bf16_peak():
+    """Dense bf16 tensor TFLOP/s for a kernel timed alone (the burst figure)."""
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        try:
+            d = json.load(open(path))
+            if "bf16_tflops" in d:
+                return float(d["bf16_tflops"]), "measured (cuBLAS bf16 GEMM, burst)"
+        except Exception:
+            pass
+    return FALLBACK_BF16_TFLOPS, "fallback"
 
 
 def peaks():
@@ -632,21 +662,31 @@ def run_bwd(args, p, dev, rank, local_rank, world):
     ms_max, e2e_max = slowest_rank([ms, e2e_ms], dev)
     tokens = p.batch * p.seqlen
     if rank == 0:
-        fl = bwd_flops(p)
+        tc = bwd_uses_tensor_cores(p)
+        fl = bwd_tc_flops(p) if tc else bwd_flops(p)
         achieved = fl / (ms / 1e3) / 1e12
+        if tc:
+            pk, pk_kind = bf16_peak()
+            roof = {"bound": "tensor", "achieved": achieved, "peak": pk, "unit": "TFLOP/s", "frac": achieved / pk,
+                    "peak_source": pk_kind, "traffic": None,
+                    "scope": "algorithmic bf16 MMA flops of the whole ssd_bwd call (2 launches)"}
+            kern = "ssd_bwd_tc (tcgen05, bf16 operands, fp32 accumulation) + ssd_bwd_reduce"
+        else:
+            roof = {"bound": "alu", "achieved": achieved, "peak": FP32_PEAK_TFLOPS, "unit": "TFLOP/s",
+                    "frac": achieved / FP32_PEAK_TFLOPS,
+                    "peak_source": "derived: 152 SMs x 128 fp32 lanes x 2 x 2.07 GHz", "traffic": None,
+                    "scope": "algorithmic fp32 flops of the whole ssd_bwd call (2 launches)"}
+            kern = "ssd_bwd_chunk + ssd_bwd_reduce (CUDA cores, fp32)"
         line = {
             "metric": BWD_METRIC, "value": job_rate(tokens, world, ms_max), "unit": "tokens/s", "n_gpus": world,
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_max, "higher_is_better": True,
-            "scaling": "weak", "vs_baseline": None, "dtype": "f32", "data": "synthetic",
+            "scaling": "weak", "vs_baseline": None, "dtype": "bf16" if tc else "f32", "data": "synthetic",
             "config": {"workload": "bwd_" + p.name, "batch": p.batch, "seq_len": p.seqlen, "nheads": p.nheads,
                        "headdim": p.headdim, "dstate": p.dstate, "ngroups": p.ngroups, "storage": p.dtype,
-                       "kernel": "ssd_bwd_chunk + ssd_bwd_reduce (CUDA cores, fp32)",
+                       "kernel": kern,
                        "l2": "256 MiB write before every timed step; inputs larger than L2",
                        "algorithmic_flops": fl},
-            "roofline": {"bound": "alu", "achieved": achieved, "peak": FP32_PEAK_TFLOPS, "unit": "TFLOP/s",
-                         "frac": achieved / FP32_PEAK_TFLOPS,
-                         "peak_source": "derived: 152 SMs x 128 fp32 lanes x 2 x 2.07 GHz", "traffic": None,
-                         "scope": "algorithmic fp32 flops of the whole ssd_bwd call (2 launches)"},
+            "roofline": roof,
             "e2e": {"value": job_rate(tokens, world, e2e_max), "unit": "tokens/s", "h2d_bytes_per_step": h2d,
                     "d2h_bytes_per_step": d2h},
             "gpu_launches": 2 * args.steps,
