@@ -165,10 +165,11 @@ struct SegsumLinRow {
 // diagonal; the block's last row publishes its column factors and the block
 // total.  Needs sh.a complete (barrier before), a barrier after.  K
 // independent chunks (of different heads) at once: their product chains
-// interleave, each one multiply per column.
+// interleave, each one multiply per column.  publish = false: the row's
+// factors only (a second thread of the same row; the other publishes).
 template <int NW, int K>
 __device__ __forceinline__ void segsum_lin_phase1_k(SegsumLinShared<NW>* sh, SegsumLinRow<NW>* row, int w,
-                                                    int lane) {
+                                                    int lane, bool publish = true) {
     float e[K][32];
 #pragma unroll
     for (int h = 0; h < K; ++h) {
@@ -195,7 +196,7 @@ __device__ __forceinline__ void segsum_lin_phase1_k(SegsumLinShared<NW>* sh, Seg
             row[h].wl[c] = (c <= lane) ? r[h] : 0.f;
         }
     }
-    if (lane == 31) {
+    if (publish && lane == 31) {
 #pragma unroll
         for (int h = 0; h < K; ++h) {
             float4* dst = reinterpret_cast<float4*>(sh[h].colL + 32 * w);
@@ -210,8 +211,8 @@ __device__ __forceinline__ void segsum_lin_phase1_k(SegsumLinShared<NW>* sh, Seg
 
 template <int NW>
 __device__ __forceinline__ void segsum_lin_phase1(SegsumLinShared<NW>& sh, SegsumLinRow<NW>& row, int w,
-                                                  int lane) {
-    segsum_lin_phase1_k<NW, 1>(&sh, &row, w, lane);
+                                                  int lane, bool publish = true) {
+    segsum_lin_phase1_k<NW, 1>(&sh, &row, w, lane, publish);
 }
 
 // Phase 2: the rank-one row factors and the chunk prefix; the chunk's last
@@ -219,7 +220,7 @@ __device__ __forceinline__ void segsum_lin_phase1(SegsumLinShared<NW>& sh, Segsu
 // Needs the phase-1 barrier; a barrier after before segsum_lin_suffix().
 template <int NW>
 __device__ __forceinline__ void segsum_lin_phase2(SegsumLinShared<NW>& sh, SegsumLinRow<NW>& row, int w,
-                                                  int lane) {
+                                                  int lane, bool publish = true) {
     float acc = row.wl[0] * sh.a[32 * w];   // prod_{k=32w..i} a_k
 #pragma unroll
     for (int r = NW - 2; r >= 0; --r) {
@@ -227,7 +228,7 @@ __device__ __forceinline__ void segsum_lin_phase2(SegsumLinShared<NW>& sh, Segsu
         acc *= (r < w) ? sh.totL[r] : 1.f;   // 1: an exact no-op past the row's own block
     }
     row.pe = acc;
-    if (w == NW - 1 && lane == 31) {
+    if (publish && w == NW - 1 && lane == 31) {
 #pragma unroll
         for (int r = 0; r < NW - 1; ++r) sh.rlastL[r] = row.rf[r];
         sh.tauL = acc;

@@ -14,15 +14,18 @@
 //     SC = C S_in^T                      dx_j = dt_j v_j + D dy_j
 //     dB_j = dt_j [A2^T C + (2^s o x) Lam^T]_j        (one accumulator)
 //     dC_i = [(A2 o dt) B + (2^p o dy) S_in^T]_i       (one accumulator)
-//     Lam^T <- 2^tau Lam^T + C^T (2^p o dy)
+//     Lam^T <- 2^tau Lam^T + C^T (2^p o dy)           (in TMEM)
 //   and the per-token terms of ddt from row sums of those products and of
-//   W = A1 o dt o X (its corner sums by a warp transpose-reduction).
+//   W = A1 o dt o X (its corner sums by warp transpose-reductions).
 //
-// One CTA of 128 threads per (batch row, head): thread r owns chunk row r,
-// and state column n = r of S, Lam and the contractions whose rows are state
-// columns.  Thread 0 issues the TMA loads and the MMAs; every wait is bounded
-// and a wait that runs out records SSD_ERR_TIMEOUT in the workspace status
-// word, after which the CTA drains its MMAs, frees its TMEM and exits.
+// One CTA of 288 threads per (batch row, head).  Warps 0-7 compute: thread
+// (warp w, lane) owns chunk row (and state column) r = 32 (w % 4) + lane and
+// the column half w / 4 of that row; both halves of a row run its segsum.
+// Warp 8 issues: its lane 0 issues the TMA loads, the MMAs and the TMA stores,
+// handed over through mbarriers, so the next chunk's loads start as soon as
+// this chunk's last contraction is done.  Every wait is bounded; a wait that
+// runs out records SSD_ERR_TIMEOUT in the workspace status word, and the CTA
+// drains its MMAs and copies, frees its TMEM and exits.
 #include <cuda.h>
 #include <cuda_bf16.h>
 #include <stddef.h>
@@ -38,31 +41,37 @@ namespace ssd {
 namespace {
 
 constexpr int Q = 128, P = 64, N = 128;
-constexpr int kThreads = 128;
+constexpr int kCompute = 256;                 // compute threads (8 warps)
+constexpr int kThreads = kCompute + 32;       // and the issue warp
+constexpr int kBarCompute = 1;                // named barrier of the compute threads
 // shared tiles (each 1024-byte aligned for the 128-byte swizzle)
 constexpr uint32_t kTX = 0;           // x (row j, p); then 2^{s_j} x_j (phase 1: w_j x_j)
 constexpr uint32_t kTDY = 16384;      // dy (row i, p); then 2^{p_i} dy_i
 constexpr uint32_t kTB = 32768;       // B (row j, n in two 64-column slabs)
 constexpr uint32_t kTC = 65536;       // C
 constexpr uint32_t kTLam = 98304;     // Lam as (row n, p) bf16
-constexpr uint32_t kTSin = 114688;    // S_in as (row n, p) bf16
-constexpr uint32_t kT1 = 131072;      // A1 (row i, column j); then A2 o dt
-constexpr uint32_t kT2 = 163840;      // A2
+constexpr uint32_t kTSin = 114688;    // S_in as (row n, p) bf16; then dx, staged for its store
+constexpr uint32_t kT1 = 131072;      // A1 (row i, column j); then A2 o dt; then the dC share
+constexpr uint32_t kT2 = 163840;      // A2; then the dB share
 constexpr uint32_t kTiles = 196608;
-// TMEM columns
+// TMEM columns (phase 1: the state summary in columns 0-63 or 64-127, by chunk parity)
 constexpr uint32_t kTmG = 0, kTmX = 128, kTmV2 = 256, kTmSC = 320, kTmV1 = 384, kTmLU = 448, kTmCols = 512;
 
 // codes of the wait that gave up (WsHeader::where)
 enum : uint32_t { kWhereLoad = 31, kWhereMma1 = 32, kWhereV1 = 33, kWhereDB = 34, kWhereDC = 35,
-                  kWhereF = 36, kWhereDrain = 37 };
+                  kWhereF = 36, kWhereDrain = 37, kWhereReady = 38, kWhereStores = 39 };
 
 struct BwdTcSmall {
     SegsumLinShared<4> seg;
     alignas(16) float dts[Q];
-    float part[4][Q];       // per-warp partial corner sums of W
-    float red[8];
-    float carry[2][4];      // warp totals of the token scans
-    uint64_t full, mma1, mma2, mmaV1, mmaDB, mmaDC, mmaF, drain;
+    float part[4][Q];       // per row block: partial corner sums of W (column half 0: t < 64, half 1: t >= 64)
+    float F[Q];             // per row: the sum of W over column half 0
+    float qv[4][Q];         // column half 1's partial row sums (vx, lbx, scdy, dy . x)
+    float red[16];
+    float carry[3][4];      // warp totals of the token scans
+    uint64_t full, mmaF, mma1, mma2, mmaV1, mmaDB, mmaDC, drain;   // loads and MMAs complete
+    uint64_t rdyF, rdyA, rdyB, rdyC, rdyS;                          // compute warps -> issuer
+    uint64_t stFree;                                                // the stores have read their tiles
     uint32_t tmem_base;
     int abort;
     int never;
@@ -101,6 +110,11 @@ __device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
 }
 __device__ __forceinline__ float bf16lo(uint32_t w) { return __uint_as_float(w << 16); }
 __device__ __forceinline__ float bf16hi(uint32_t w) { return __uint_as_float(w & 0xFFFF0000u); }
+// eight bf16 values times s, rounded to bf16 again
+__device__ __forceinline__ uint4 scale_bf16x8(uint4 v, float s) {
+    return make_uint4(pack_bf16(bf16lo(v.x) * s, bf16hi(v.x) * s), pack_bf16(bf16lo(v.y) * s, bf16hi(v.y) * s),
+                      pack_bf16(bf16lo(v.z) * s, bf16hi(v.z) * s), pack_bf16(bf16lo(v.w) * s, bf16hi(v.w) * s));
+}
 
 // offset of element (row r, column j < 128) in a two-slab tile
 __device__ __forceinline__ uint32_t off2(int r, int j) { return (uint32_t)(j >> 6) * 16384u + sw128_off(r, j & 63); }
@@ -113,6 +127,15 @@ __device__ __forceinline__ bool wait_bar(BwdTcSmall& sh, const BwdArgs& a, uint6
         *(volatile int*)&sh.abort = 1;
     }
     return false;
+}
+
+// one arrival per compute warp, after the warp's shared-memory writes (for the
+// async proxy) and tensor-memory accesses
+__device__ __forceinline__ void warp_arrive(uint64_t* bar, int lane) {
+    ptx::fence_proxy_async();
+    ptx::tc_fence_before();
+    __syncwarp();
+    if (lane == 0) ptx::mbar_arrive(bar);
 }
 
 __device__ __forceinline__ float warp_sum(float v) {
@@ -157,7 +180,7 @@ __global__ void __launch_bounds__(kThreads, 1) ssd_bwd_tc(const __grid_constant_
     uint8_t* sm = (uint8_t*)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
     BwdTcSmall& sh = *reinterpret_cast<BwdTcSmall*>(sm + kTiles);
     const BwdArgs& a = prm.a;
-    const int r = threadIdx.x, warp = r >> 5, lane = r & 31;
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const uint32_t s0 = ptx::smem_u32(sm);
     const int64_t unit = blockIdx.x;   // b * H + h
     const int h = (int)(unit % a.H);
@@ -166,181 +189,273 @@ __global__ void __launch_bounds__(kThreads, 1) ssd_bwd_tc(const __grid_constant_
     const int64_t L = a.L;
     const int nch = (int)((L + Q - 1) / Q);
     const size_t PN = (size_t)P * N;
-    const float A2 = a.A[h] * kLog2e;
-    const float Ah = a.A[h];
-    const float Dh = a.D ? a.D[h] : 0.f;
     float* ckpt = a.ws_ckpt + (size_t)unit * nch * PN;
 
-    if (r == 0) {
+    if (threadIdx.x == 0) {
         ptx::mbar_init(&sh.full, 1);
+        ptx::mbar_init(&sh.mmaF, 1);
         ptx::mbar_init(&sh.mma1, 1);
         ptx::mbar_init(&sh.mma2, 1);
         ptx::mbar_init(&sh.mmaV1, 1);
         ptx::mbar_init(&sh.mmaDB, 1);
         ptx::mbar_init(&sh.mmaDC, 1);
-        ptx::mbar_init(&sh.mmaF, 1);
         ptx::mbar_init(&sh.drain, 1);
+        ptx::mbar_init(&sh.rdyF, 8);
+        ptx::mbar_init(&sh.rdyA, 8);
+        ptx::mbar_init(&sh.rdyB, 8);
+        ptx::mbar_init(&sh.rdyC, 8);
+        ptx::mbar_init(&sh.rdyS, 8);
+        ptx::mbar_init(&sh.stFree, 1);
         sh.abort = 0;
         sh.never = 0;
         ptx::mbar_fence_init();
-        ptx::prefetch_tmap(&prm.tm_x);
-        ptx::prefetch_tmap(&prm.tm_dy);
-        ptx::prefetch_tmap(&prm.tm_B);
-        ptx::prefetch_tmap(&prm.tm_C);
-        ptx::prefetch_tmap(&prm.tm_dx);
-        ptx::prefetch_tmap(&prm.tm_dB);
-        ptx::prefetch_tmap(&prm.tm_dC);
     }
     if (warp == 0) ptx::tmem_alloc(&sh.tmem_base, kTmCols);
     ptx::tc_fence_before();
     __syncthreads();
     ptx::tc_fence_after();
     const uint32_t tb = sh.tmem_base;
-    const uint32_t lane_addr = tb + ((uint32_t)(32 * warp) << 16);
-    uint32_t nfull = 0, nF = 0, n1 = 0;   // completed phases of the reused barriers
-    uint32_t nissue = 0;                  // loads issued (thread 0)
 
-    // log-decays of the chunk at t0 into the segsum input; dt into sh.dts
-    bool start = false;   // a document starts at this thread's token
-    auto chunk_decays = [&](int64_t t0) -> float {
-        const bool ok = t0 + r < L;
-        const float d = ok ? __ldg(a.dt + ((size_t)b * L + t0 + r) * a.H + h) : 0.f;
-        start = ok && doc_start_tc(a, t0 + r);
-        const float l2 = start ? -INFINITY : d * A2;
-        sh.seg.a[r] = ex2_approx(l2);   // 0 at a document start, 1 past the end
-        sh.dts[r] = d;
-        return d;
-    };
-
-    // ------------------------------------------------------------ phase 1
-    float S[P];
-#pragma unroll
-    for (int p = 0; p < P; ++p) S[p] = a.init ? a.init[unit * PN + (size_t)p * N + r] : 0.f;
-    for (int c = 0; c < nch && !*(volatile int*)&sh.abort; ++c) {
-        const int64_t t0 = (int64_t)c * Q;
-        if (r == 0) {
-            ++nissue;
-            ptx::mbar_expect_tx(&sh.full, 16384u + 32768u);
-            ptx::tma_load_4d(sm + kTX, &prm.tm_x, &sh.full, 0, h, (int)t0, b);
-            ptx::tma_load_4d(sm + kTB, &prm.tm_B, &sh.full, 0, g, (int)t0, b);
-            ptx::tma_load_4d(sm + kTB + 16384, &prm.tm_B, &sh.full, 64, g, (int)t0, b);
-        }
-        const float d = chunk_decays(t0);
-#pragma unroll
-        for (int p = 0; p < P; ++p) ckpt[(size_t)c * PN + (size_t)p * N + r] = S[p];
-        __syncthreads();
-        SegsumLinRow<4> row;
-        segsum_lin_phase1<4>(sh.seg, row, warp, lane);
-        __syncthreads();
-        segsum_lin_phase2<4>(sh.seg, row, warp, lane);
-        __syncthreads();
-        const float w = segsum_lin_suffix<4>(sh.seg, r) * d;
-        const float etau = sh.seg.tauL;
-        wait_bar(sh, a, &sh.full, nfull & 1, kWhereLoad);
-        ++nfull;
-        {   // w_j x_j in place (row j = r)
-            uint8_t* xr = sm + kTX;
-#pragma unroll
-            for (int q = 0; q < 8; ++q) {
-                uint4 v = *reinterpret_cast<const uint4*>(xr + sw128_off(r, 8 * q));
-                v.x = pack_bf16(bf16lo(v.x) * w, bf16hi(v.x) * w);
-                v.y = pack_bf16(bf16lo(v.y) * w, bf16hi(v.y) * w);
-                v.z = pack_bf16(bf16lo(v.z) * w, bf16hi(v.z) * w);
-                v.w = pack_bf16(bf16lo(v.w) * w, bf16hi(v.w) * w);
-                *reinterpret_cast<uint4*>(xr + sw128_off(r, 8 * q)) = v;
+    if (warp == 8) {
+        // ================================================================ issue warp
+        if (lane == 0) {
+            ptx::prefetch_tmap(&prm.tm_x);
+            ptx::prefetch_tmap(&prm.tm_dy);
+            ptx::prefetch_tmap(&prm.tm_B);
+            ptx::prefetch_tmap(&prm.tm_C);
+            ptx::prefetch_tmap(&prm.tm_dx);
+            ptx::prefetch_tmap(&prm.tm_dB);
+            ptx::prefetch_tmap(&prm.tm_dC);
+            uint32_t nfull = 0, nissue = 0;   // phases of `full` completed (and waited for), loads issued
+            auto load1 = [&](int c) {         // phase 1: x and B of chunk c
+                ++nissue;
+                const int t0 = c * Q;
+                ptx::mbar_expect_tx(&sh.full, 16384u + 32768u);
+                ptx::tma_load_4d(sm + kTX, &prm.tm_x, &sh.full, 0, h, t0, b);
+                ptx::tma_load_4d(sm + kTB, &prm.tm_B, &sh.full, 0, g, t0, b);
+                ptx::tma_load_4d(sm + kTB + 16384, &prm.tm_B, &sh.full, 64, g, t0, b);
+            };
+            auto load2 = [&](int c) {         // phase 2: x, dy, B and C of chunk c; chunk c - 1 towards L2
+                ++nissue;
+                const int t0 = c * Q;
+                ptx::mbar_expect_tx(&sh.full, 16384u * 2u + 32768u * 2u);
+                ptx::tma_load_4d(sm + kTX, &prm.tm_x, &sh.full, 0, h, t0, b);
+                ptx::tma_load_4d(sm + kTDY, &prm.tm_dy, &sh.full, 0, h, t0, b);
+                ptx::tma_load_4d(sm + kTB, &prm.tm_B, &sh.full, 0, g, t0, b);
+                ptx::tma_load_4d(sm + kTB + 16384, &prm.tm_B, &sh.full, 64, g, t0, b);
+                ptx::tma_load_4d(sm + kTC, &prm.tm_C, &sh.full, 0, g, t0, b);
+                ptx::tma_load_4d(sm + kTC + 16384, &prm.tm_C, &sh.full, 64, g, t0, b);
+                if (c > 0) {
+                    const int tp = t0 - Q;
+                    ptx::bulk_prefetch_l2(ckpt + (size_t)(c - 1) * PN, (uint32_t)(PN * 4));
+                    ptx::tma_prefetch_4d(&prm.tm_x, 0, h, tp, b);
+                    ptx::tma_prefetch_4d(&prm.tm_dy, 0, h, tp, b);
+                    ptx::tma_prefetch_4d(&prm.tm_B, 0, g, tp, b);
+                    ptx::tma_prefetch_4d(&prm.tm_B, 64, g, tp, b);
+                    ptx::tma_prefetch_4d(&prm.tm_C, 0, g, tp, b);
+                    ptx::tma_prefetch_4d(&prm.tm_C, 64, g, tp, b);
+                }
+            };
+            // ---- phase 1: the compute warps scale x once its load lands, then this
+            // chunk's state summary goes to the TMEM columns of its parity
+            if (nch > 0) load1(0);
+            for (int c = 0; c < nch; ++c) {
+                if (!wait_bar(sh, a, &sh.rdyF, c & 1, kWhereReady)) break;
+                ++nfull;   // (the compute warps waited for this load before arriving)
+                ptx::tc_fence_after();
+                constexpr uint32_t id = ptx::idesc_bf16(128, 64, 1, 1);
+#pragma unroll 1
+                for (int kk = 0; kk < 8; ++kk)
+                    ptx::mma_ss(tb + 64 * (c & 1), desc_mn2(s0 + kTB, kk), desc_mn1(s0 + kTX, kk), id, kk > 0);
+                ptx::mma_commit(&sh.mmaF);
+                if (!wait_bar(sh, a, &sh.mmaF, c & 1, kWhereF)) break;
+                if (c + 1 < nch) load1(c + 1);
             }
-            ptx::fence_proxy_async();
+            // ---- phase 2
+            if (nch > 0 && !*(volatile int*)&sh.abort) load2(nch - 1);
+            for (int k = 0; k < nch && !*(volatile int*)&sh.abort; ++k) {
+                const int c = nch - 1 - k;
+                const int t0 = c * Q;
+                if (!wait_bar(sh, a, &sh.full, nfull & 1, kWhereLoad)) break;
+                ++nfull;
+                // TMEM free: the last chunk's shares (or phase 1's state summaries) are read
+                if (!wait_bar(sh, a, &sh.rdyS, k & 1, kWhereReady)) break;
+                ptx::tc_fence_after();
+                constexpr uint32_t idQQ = ptx::idesc_bf16(128, 128, 0, 0);
+                constexpr uint32_t idQP = ptx::idesc_bf16(128, 64, 0, 1);
+#pragma unroll 1
+                for (int kk = 0; kk < 8; ++kk)
+                    ptx::mma_ss(tb + kTmG, desc_k2(s0 + kTC, kk), desc_k2(s0 + kTB, kk), idQQ, kk > 0);
+#pragma unroll 1
+                for (int kk = 0; kk < 4; ++kk)
+                    ptx::mma_ss(tb + kTmX, desc_k1(s0 + kTDY, kk), desc_k1(s0 + kTX, kk), idQQ, kk > 0);
+                ptx::mma_commit(&sh.mma1);
+                // B Lam^T and C S_in^T, once the Lam and S_in tiles are written
+                if (!wait_bar(sh, a, &sh.rdyA, k & 1, kWhereReady)) break;
+                ptx::tc_fence_after();
+#pragma unroll 1
+                for (int kk = 0; kk < 8; ++kk)
+                    ptx::mma_ss(tb + kTmV2, desc_k2(s0 + kTB, kk), desc_mn1(s0 + kTLam, kk), idQP, kk > 0);
+#pragma unroll 1
+                for (int kk = 0; kk < 8; ++kk)
+                    ptx::mma_ss(tb + kTmSC, desc_k2(s0 + kTC, kk), desc_mn1(s0 + kTSin, kk), idQP, kk > 0);
+                ptx::mma_commit(&sh.mma2);
+                // (L o G)^T dy; dB~ = A2^T C + (2^s o x) Lam^T
+                if (!wait_bar(sh, a, &sh.rdyB, k & 1, kWhereReady)) break;
+                ptx::tc_fence_after();
+                {
+                    constexpr uint32_t idV = ptx::idesc_bf16(128, 64, 1, 1);
+                    constexpr uint32_t idB1 = ptx::idesc_bf16(128, 128, 1, 1);
+                    constexpr uint32_t idB2 = ptx::idesc_bf16(128, 128, 0, 0);
+#pragma unroll 1
+                    for (int kk = 0; kk < 8; ++kk)
+                        ptx::mma_ss(tb + kTmV1, desc_mn2(s0 + kT1, kk), desc_mn1(s0 + kTDY, kk), idV, kk > 0);
+                    ptx::mma_commit(&sh.mmaV1);
+#pragma unroll 1
+                    for (int kk = 0; kk < 8; ++kk)
+                        ptx::mma_ss(tb + kTmG, desc_mn2(s0 + kT2, kk), desc_mn2(s0 + kTC, kk), idB1, kk > 0);
+#pragma unroll 1
+                    for (int kk = 0; kk < 4; ++kk)
+                        ptx::mma_ss(tb + kTmG, desc_k1(s0 + kTX, kk), desc_k1(s0 + kTLam, kk), idB2, 1);
+                    ptx::mma_commit(&sh.mmaDB);
+                }
+                // dC = (A2 o dt) B + (2^p o dy) S_in^T; Lam^T += C^T (2^p o dy)
+                if (!wait_bar(sh, a, &sh.rdyC, k & 1, kWhereReady)) break;
+                ptx::tc_fence_after();
+                {
+                    constexpr uint32_t idC1 = ptx::idesc_bf16(128, 128, 0, 1);
+                    constexpr uint32_t idC2 = ptx::idesc_bf16(128, 128, 0, 0);
+                    constexpr uint32_t idL = ptx::idesc_bf16(128, 64, 1, 1);
+#pragma unroll 1
+                    for (int kk = 0; kk < 8; ++kk)
+                        ptx::mma_ss(tb + kTmX, desc_k2(s0 + kT1, kk), desc_mn2(s0 + kTB, kk), idC1, kk > 0);
+#pragma unroll 1
+                    for (int kk = 0; kk < 4; ++kk)
+                        ptx::mma_ss(tb + kTmX, desc_k1(s0 + kTDY, kk), desc_k1(s0 + kTSin, kk), idC2, 1);
+#pragma unroll 1
+                    for (int kk = 0; kk < 8; ++kk)
+                        ptx::mma_ss(tb + kTmLU, desc_mn2(s0 + kTC, kk), desc_mn1(s0 + kTDY, kk), idL, 1);
+                    ptx::mma_commit(&sh.mmaDC);
+                }
+                // every contraction of the chunk is done: its tiles take the next chunk's loads
+                if (!wait_bar(sh, a, &sh.mmaDC, k & 1, kWhereDC)) break;
+                if (c > 0) load2(c - 1);
+                // the shares and dx staged: their stores (rows past the end are clipped)
+                if (!wait_bar(sh, a, &sh.rdyS, (k + 1) & 1, kWhereStores)) break;
+                ptx::tma_store_4d(&prm.tm_dB, sm + kT2, 0, h, t0, b);
+                ptx::tma_store_4d(&prm.tm_dB, sm + kT2 + 16384, 64, h, t0, b);
+                ptx::tma_store_4d(&prm.tm_dC, sm + kT1, 0, h, t0, b);
+                ptx::tma_store_4d(&prm.tm_dC, sm + kT1 + 16384, 64, h, t0, b);
+                ptx::tma_store_4d(&prm.tm_dx, sm + kTSin, 0, h, t0, b);
+                ptx::bulk_commit();
+                ptx::bulk_wait_read0();
+                ptx::mbar_arrive(&sh.stFree);
+            }
+            // drain: every MMA issued has completed, the last load issued has landed,
+            // and the stores are complete
+            ptx::mma_commit(&sh.drain);
+            if (!ptx::mbar_wait(&sh.drain, 0, &sh.never, a.wait_iters)) record_error(a.ws, SSD_ERR_TIMEOUT, kWhereDrain);
+            if (nissue > nfull && !ptx::mbar_wait(&sh.full, (nissue - 1) & 1, &sh.never, a.wait_iters))
+                record_error(a.ws, SSD_ERR_TIMEOUT, kWhereDrain);
+            ptx::bulk_wait0();
         }
-        __syncthreads();
-        if (r == 0) {
+        __syncwarp();
+    } else {
+        // ================================================================ compute warps
+        const int rb = warp & 3, hf = warp >> 2;   // row block (TMEM lane quarter), column half
+        const int r = 32 * rb + lane;              // chunk row = state column = TMEM lane
+        const uint32_t lane_addr = tb + ((uint32_t)(32 * rb) << 16);
+        const float A2 = a.A[h] * kLog2e;
+        const float Ah = a.A[h];
+        const float Dh = a.D ? a.D[h] : 0.f;
+        uint32_t nfull = 0;
+        auto dt_at = [&](int64_t t) { return t < L ? __ldg(a.dt + ((size_t)b * L + t) * a.H + h) : 0.f; };
+        // the chunk's log-decays into the segsum input, and dt (column half 0 writes them)
+        auto decays = [&](float d, bool start) {
+            if (hf == 0) {
+                sh.seg.a[r] = ex2_approx(start ? -INFINITY : d * A2);   // 0 at a document start, 1 past the end
+                sh.dts[r] = d;
+            }
+        };
+
+        // ------------------------------------------------------------ phase 1
+        float S[32];   // S^T[n = r][p], this half's p
+#pragma unroll
+        for (int p = 0; p < 32; ++p) S[p] = a.init ? a.init[unit * PN + (size_t)(32 * hf + p) * N + r] : 0.f;
+        for (int c = 0; c < nch; ++c) {
+            const int64_t t0 = (int64_t)c * Q;
+            const float d = dt_at(t0 + r);
+            decays(d, t0 + r < L && doc_start_tc(a, t0 + r));
+#pragma unroll
+            for (int p = 0; p < 32; ++p) ckpt[(size_t)c * PN + (size_t)(32 * hf + p) * N + r] = S[p];
+            ptx::named_bar(kBarCompute, kCompute);
+            SegsumLinRow<4> row;
+            segsum_lin_phase1<4>(sh.seg, row, rb, lane, hf == 0);
+            ptx::named_bar(kBarCompute, kCompute);
+            segsum_lin_phase2<4>(sh.seg, row, rb, lane, hf == 0);
+            ptx::named_bar(kBarCompute, kCompute);
+            const float w = segsum_lin_suffix<4>(sh.seg, r) * d;
+            const float etau = sh.seg.tauL;
+            wait_bar(sh, a, &sh.full, nfull & 1, kWhereLoad);
+            ++nfull;
+#pragma unroll
+            for (int q = 0; q < 4; ++q) {   // w_j x_j in place (row j = r, this half's p)
+                uint4* px = reinterpret_cast<uint4*>(sm + kTX + sw128_off(r, 32 * hf + 8 * q));
+                *px = scale_bf16x8(*px, w);
+            }
+            warp_arrive(&sh.rdyF, lane);
+            wait_bar(sh, a, &sh.mmaF, c & 1, kWhereF);
             ptx::tc_fence_after();
-            constexpr uint32_t id = ptx::idesc_bf16(128, 64, 1, 1);
-#pragma unroll 1
-            for (int kk = 0; kk < 8; ++kk)
-                ptx::mma_ss(tb + kTmG, desc_mn2(s0 + kTB, kk), desc_mn1(s0 + kTX, kk), id, kk > 0);
-            ptx::mma_commit(&sh.mmaF);
-        }
-        wait_bar(sh, a, &sh.mmaF, nF & 1, kWhereF);
-        ++nF;
-        ptx::tc_fence_after();
-        {
-            uint32_t d0[32], d1[32];
-            ptx::tmem_load32x2(lane_addr + kTmG, d0, lane_addr + kTmG + 32, d1);
+            uint32_t dd[32];
+            ptx::tmem_load32(lane_addr + 64 * (c & 1) + 32 * hf, dd);
 #pragma unroll
-            for (int p = 0; p < 32; ++p) {
-                S[p] = fmaf(etau, S[p], __uint_as_float(d0[p]));
-                S[p + 32] = fmaf(etau, S[p + 32], __uint_as_float(d1[p]));
-            }
+            for (int p = 0; p < 32; ++p) S[p] = fmaf(etau, S[p], __uint_as_float(dd[p]));
         }
-        ptx::tc_fence_before();
-        __syncthreads();   // tiles and TMEM free for the next chunk
-    }
+        warp_arrive(&sh.rdyS, lane);   // the state summaries are read: TMEM free for phase 2
 
-    // ------------------------------------------------------------ phase 2
-    // Lam^T (lane n, column p) lives in TMEM: each chunk scales it by 2^tau in
-    // place and the update contraction accumulates onto it
-    {
-#pragma unroll 1
-        for (int q = 0; q < 4; ++q) {
+        // ------------------------------------------------------------ phase 2
+        // Lam^T (lane n, column p) lives in TMEM: each chunk scales it by 2^tau in
+        // place and the update contraction accumulates onto it
+        {
             uint32_t v[16];
 #pragma unroll
-            for (int e = 0; e < 16; ++e)
-                v[e] = __float_as_uint(a.dfin ? a.dfin[unit * PN + (size_t)(16 * q + e) * N + r] : 0.f);
-            ptx::tmem_st16(lane_addr + kTmLU + 16 * q, v);
-        }
-        ptx::tmem_st_wait();
-    }
-    float dA_acc = 0.f, dD_acc = 0.f;
-    float d_next = (nch > 0 && (int64_t)(nch - 1) * Q + r < L)
-                       ? __ldg(a.dt + ((size_t)b * L + (int64_t)(nch - 1) * Q + r) * a.H + h) : 0.f;
-    for (int c = nch - 1; c >= 0 && !*(volatile int*)&sh.abort; --c) {
-        const int64_t t0 = (int64_t)c * Q;
-        const bool valid = t0 + r < L;
-        if (r == 0) {
-            ++nissue;
-            ptx::mbar_expect_tx(&sh.full, 16384u * 2u + 32768u * 2u);
-            ptx::tma_load_4d(sm + kTX, &prm.tm_x, &sh.full, 0, h, (int)t0, b);
-            ptx::tma_load_4d(sm + kTDY, &prm.tm_dy, &sh.full, 0, h, (int)t0, b);
-            ptx::tma_load_4d(sm + kTB, &prm.tm_B, &sh.full, 0, g, (int)t0, b);
-            ptx::tma_load_4d(sm + kTB + 16384, &prm.tm_B, &sh.full, 64, g, (int)t0, b);
-            ptx::tma_load_4d(sm + kTC, &prm.tm_C, &sh.full, 0, g, (int)t0, b);
-            ptx::tma_load_4d(sm + kTC + 16384, &prm.tm_C, &sh.full, 64, g, (int)t0, b);
-            if (c > 0) {   // the next chunk's tiles and incoming state on their way to L2
-                ptx::bulk_prefetch_l2(ckpt + (size_t)(c - 1) * PN, (uint32_t)(PN * 4));
-                const int tp = (int)(t0 - Q);
-                ptx::tma_prefetch_4d(&prm.tm_x, 0, h, tp, b);
-                ptx::tma_prefetch_4d(&prm.tm_dy, 0, h, tp, b);
-                ptx::tma_prefetch_4d(&prm.tm_B, 0, g, tp, b);
-                ptx::tma_prefetch_4d(&prm.tm_B, 64, g, tp, b);
-                ptx::tma_prefetch_4d(&prm.tm_C, 0, g, tp, b);
-                ptx::tma_prefetch_4d(&prm.tm_C, 64, g, tp, b);
+            for (int q = 0; q < 2; ++q) {
+#pragma unroll
+                for (int e = 0; e < 16; ++e)
+                    v[e] = __float_as_uint(a.dfin ? a.dfin[unit * PN + (size_t)(32 * hf + 16 * q + e) * N + r] : 0.f);
+                ptx::tmem_st16(lane_addr + kTmLU + 32 * hf + 16 * q, v);
             }
+            ptx::tmem_st_wait();
         }
-        // log-decays (dt was loaded a chunk earlier); the next chunk's dt
-        const float d = d_next;
-        start = valid && doc_start_tc(a, t0 + r);
-        sh.seg.a[r] = ex2_approx(start ? -INFINITY : d * A2);   // 0 at a document start, 1 past the end
-        sh.dts[r] = d;
-        d_next = (c > 0) ? __ldg(a.dt + ((size_t)b * L + t0 - Q + r) * a.H + h) : 0.f;
-        if (r == 0) ptx::bulk_wait_read0();   // the last chunk's stores have read S_in, A1 and A2
-        __syncthreads();
-        SegsumLinRow<4> row;
-        segsum_lin_phase1<4>(sh.seg, row, warp, lane);
-        __syncthreads();
-        segsum_lin_phase2<4>(sh.seg, row, warp, lane);
-        __syncthreads();
-        const float es_r = segsum_lin_suffix<4>(sh.seg, r);
-        const float ep_r = row.pe;
-        const float etau = sh.seg.tauL;
-        // S_in and Lam as bf16 (row n = r, p) operands; <Lam, S_in>; Lam^T <- 2^tau Lam^T in TMEM
-        float kdot = 0.f;
-        {
-            const float* src = ckpt + (size_t)c * PN + r;
-#pragma unroll 1
-            for (int hf = 0; hf < 2; ++hf) {
+        float dA_acc = 0.f, dD_acc = 0.f;
+        float d_next = nch > 0 ? dt_at((int64_t)(nch - 1) * Q + r) : 0.f;
+        for (int k = 0; k < nch; ++k) {
+            const int c = nch - 1 - k;
+            const int64_t t0 = (int64_t)c * Q;
+            const bool valid = t0 + r < L;
+            const float d = d_next;   // (loaded a chunk earlier)
+            const bool start = valid && doc_start_tc(a, t0 + r);
+            decays(d, start);
+            d_next = c > 0 ? dt_at(t0 - Q + r) : 0.f;
+            ptx::named_bar(kBarCompute, kCompute);
+            SegsumLinRow<4> row;
+            segsum_lin_phase1<4>(sh.seg, row, rb, lane, hf == 0);
+            ptx::named_bar(kBarCompute, kCompute);
+            segsum_lin_phase2<4>(sh.seg, row, rb, lane, hf == 0);
+            ptx::named_bar(kBarCompute, kCompute);
+            const float es_r = segsum_lin_suffix<4>(sh.seg, r);
+            const float ep_r = row.pe;
+            const float etau = sh.seg.tauL;
+            // the last chunk's stores have read S_in, A1 and A2
+            if (k > 0) wait_bar(sh, a, &sh.stFree, (k - 1) & 1, kWhereStores);
+            // S_in and Lam as bf16 (row n = r, this half's p) operands; <Lam, S_in>;
+            // Lam^T <- 2^tau Lam^T in TMEM (the last update contraction is done)
+            float kdot = 0.f;
+            {
+                const float* src = ckpt + (size_t)c * PN + (size_t)(32 * hf) * N + r;
                 float sv[32];
 #pragma unroll
-                for (int p = 0; p < 32; ++p) sv[p] = src[(size_t)(32 * hf + p) * N];
+                for (int p = 0; p < 32; ++p) sv[p] = src[(size_t)p * N];
                 uint32_t lv[32];
                 ptx::tmem_load32(lane_addr + kTmLU + 32 * hf, lv);
 #pragma unroll
@@ -366,307 +481,244 @@ __global__ void __launch_bounds__(kThreads, 1) ssd_bwd_tc(const __grid_constant_
                 }
                 ptx::tmem_st16(lane_addr + kTmLU + 32 * hf, lo);
                 ptx::tmem_st16(lane_addr + kTmLU + 32 * hf + 16, hi);
+                ptx::tmem_st_wait();
             }
-            ptx::tmem_st_wait();
-            ptx::fence_proxy_async();
-        }
-        kdot = warp_sum(kdot);
-        if (lane == 0) sh.red[warp] = kdot;
-        // ---- G, X (needed first), then V2, SC
-        wait_bar(sh, a, &sh.full, nfull & 1, kWhereLoad);
-        ++nfull;
-        ptx::tc_fence_before();
-        __syncthreads();
-        const float K = (sh.red[0] + sh.red[1]) + (sh.red[2] + sh.red[3]);
-        if (r == 0) {
+            warp_arrive(&sh.rdyA, lane);
+            kdot = warp_sum(kdot);
+            if (lane == 0) sh.red[warp] = kdot;
+            // this row's x and dy (this half's p), kept for the epilogue before the
+            // tiles are rescaled
+            wait_bar(sh, a, &sh.full, nfull & 1, kWhereLoad);
+            ++nfull;
+            uint4 xv[4], dv[4];
+#pragma unroll
+            for (int q = 0; q < 4; ++q) {
+                xv[q] = *reinterpret_cast<const uint4*>(sm + kTX + sw128_off(r, 32 * hf + 8 * q));
+                dv[q] = *reinterpret_cast<const uint4*>(sm + kTDY + sw128_off(r, 32 * hf + 8 * q));
+            }
+            wait_bar(sh, a, &sh.mma1, k & 1, kWhereMma1);
             ptx::tc_fence_after();
-            constexpr uint32_t idQQ = ptx::idesc_bf16(128, 128, 0, 0);
-            constexpr uint32_t idQP = ptx::idesc_bf16(128, 64, 0, 1);
+            // ---- this half's columns of A1 = L o G and A2 = L o X (bf16 tiles) and the
+            // corner sums of W.  Column block cb of 32: L_rj = rf[cb] colL[j] below the
+            // diagonal block (rank-one), wl[j - 32 cb] in it, 0 above it.  Half 1's row
+            // prefixes start at 0; the token pass adds half 0's row totals.
+            {
+                float zrun = 0.f;
 #pragma unroll 1
-            for (int kk = 0; kk < 8; ++kk)
-                ptx::mma_ss(tb + kTmG, desc_k2(s0 + kTC, kk), desc_k2(s0 + kTB, kk), idQQ, kk > 0);
-#pragma unroll 1
-            for (int kk = 0; kk < 4; ++kk)
-                ptx::mma_ss(tb + kTmX, desc_k1(s0 + kTDY, kk), desc_k1(s0 + kTX, kk), idQQ, kk > 0);
-            ptx::mma_commit(&sh.mma1);
-#pragma unroll 1
-            for (int kk = 0; kk < 8; ++kk)
-                ptx::mma_ss(tb + kTmV2, desc_k2(s0 + kTB, kk), desc_mn1(s0 + kTLam, kk), idQP, kk > 0);
-#pragma unroll 1
-            for (int kk = 0; kk < 8; ++kk)
-                ptx::mma_ss(tb + kTmSC, desc_k2(s0 + kTC, kk), desc_mn1(s0 + kTSin, kk), idQP, kk > 0);
-            ptx::mma_commit(&sh.mma2);
-        }
-        // this row's x and dy (bf16 pairs), kept for the epilogue before the tiles are rescaled
-        uint4 xv[8], dv[8];
+                for (int cb = 2 * hf; cb < 2 * hf + 2; ++cb) {
+                    const float rfc = (cb == 0) ? row.rf[0] : (cb == 1) ? row.rf[1] : row.rf[2];
+                    const bool below = cb < rb, diag = cb == rb;
+                    uint32_t gr[32], xr[32];
+                    ptx::tmem_load32x2(lane_addr + kTmG + 32 * cb, gr, lane_addr + kTmX + 32 * cb, xr);
 #pragma unroll
-        for (int q = 0; q < 8; ++q) {
-            xv[q] = *reinterpret_cast<const uint4*>(sm + kTX + sw128_off(r, 8 * q));
-            dv[q] = *reinterpret_cast<const uint4*>(sm + kTDY + sw128_off(r, 8 * q));
-        }
-        wait_bar(sh, a, &sh.mma1, n1 & 1, kWhereMma1);
-        ptx::tc_fence_after();
-        // ---- rows of A1 = L o G and A2 = L o X (bf16 tiles); corner sums of W.
-        // Column block cb of 32: L_rj = rf[cb] colL[j] below the diagonal block
-        // (rank-one), wl[j - 32 cb] in it, 0 above it.
-        {
-            float zrun = 0.f;   // sum of W_rj over the columns done
+                    for (int q16 = 0; q16 < 2; ++q16) {
+                        const int j0 = 32 * cb + 16 * q16;
+                        float z[16];
+                        uint32_t p1[8], p2[8];
+#pragma unroll
+                        for (int cc = 0; cc < 16; cc += 2) {
+                            const int kx = 16 * q16 + cc;
+                            const float l0 = below ? rfc * sh.seg.colL[j0 + cc] : diag ? row.wl[kx] : 0.f;
+                            const float l1 = below ? rfc * sh.seg.colL[j0 + cc + 1] : diag ? row.wl[kx + 1] : 0.f;
+                            const float x0 = __uint_as_float(xr[kx]), x1 = __uint_as_float(xr[kx + 1]);
+                            p1[cc / 2] = pack_bf16(l0 * __uint_as_float(gr[kx]), l1 * __uint_as_float(gr[kx + 1]));
+                            p2[cc / 2] = pack_bf16(l0 * x0, l1 * x1);
+                            // W from the bf16 A1 that V1 contracts: the token's own term of
+                            // <Lam_t, S_t> and of dt_t x_t . v_t then cancel in dl_t
+                            zrun += bf16lo(p1[cc / 2]) * sh.dts[j0 + cc] * x0;
+                            z[cc] = (j0 + cc <= r) ? zrun : 0.f;
+                            zrun += bf16hi(p1[cc / 2]) * sh.dts[j0 + cc + 1] * x1;
+                            z[cc + 1] = (j0 + cc + 1 <= r) ? zrun : 0.f;
+                        }
+#pragma unroll
+                        for (int q = 0; q < 2; ++q) {
+                            *reinterpret_cast<uint4*>(sm + kT1 + off2(r, j0 + 8 * q)) =
+                                make_uint4(p1[4 * q], p1[4 * q + 1], p1[4 * q + 2], p1[4 * q + 3]);
+                            *reinterpret_cast<uint4*>(sm + kT2 + off2(r, j0 + 8 * q)) =
+                                make_uint4(p2[4 * q], p2[4 * q + 1], p2[4 * q + 2], p2[4 * q + 3]);
+                        }
+                        const float zs = warp_transpose_sum16(z, lane);
+                        if (lane < 16) sh.part[rb][j0 + lane] = zs;
+                    }
+                }
+                if (hf == 0) sh.F[r] = zrun;
+            }
+            // x row j = r, this half's p, becomes 2^{s_j} x_j (the X contraction is done)
+#pragma unroll
+            for (int q = 0; q < 4; ++q)
+                *reinterpret_cast<uint4*>(sm + kTX + sw128_off(r, 32 * hf + 8 * q)) = scale_bf16x8(xv[q], es_r);
+            warp_arrive(&sh.rdyB, lane);
+            wait_bar(sh, a, &sh.mmaV1, k & 1, kWhereV1);
+            ptx::tc_fence_after();
+            // ---- this half's columns of A2 o dt (from X, still in TMEM) over A1; dy row
+            // i = r, this half's p, becomes 2^{p_i} dy_i
 #pragma unroll 1
-            for (int cb = 0; cb < 4; ++cb) {
+            for (int cb = 2 * hf; cb < 2 * hf + 2; ++cb) {
                 const float rfc = (cb == 0) ? row.rf[0] : (cb == 1) ? row.rf[1] : row.rf[2];
-                const bool below = cb < warp, diag = cb == warp;
-                uint32_t gr[32], xr[32];
-                ptx::tmem_load32x2(lane_addr + kTmG + 32 * cb, gr, lane_addr + kTmX + 32 * cb, xr);
+                const bool below = cb < rb, diag = cb == rb;
+                uint32_t xr[32];
+                ptx::tmem_load32(lane_addr + kTmX + 32 * cb, xr);
 #pragma unroll
-                for (int hf = 0; hf < 2; ++hf) {
-                    const int j0 = 32 * cb + 16 * hf;
-                    float z[16];
-                    uint32_t p1[8], p2[8];
+                for (int q16 = 0; q16 < 2; ++q16) {
+                    const int j0 = 32 * cb + 16 * q16;
+                    uint32_t p1[8];
 #pragma unroll
                     for (int cc = 0; cc < 16; cc += 2) {
-                        const int k = 16 * hf + cc;
-                        const float l0 = below ? rfc * sh.seg.colL[j0 + cc] : diag ? row.wl[k] : 0.f;
-                        const float l1 = below ? rfc * sh.seg.colL[j0 + cc + 1] : diag ? row.wl[k + 1] : 0.f;
-                        const float x0 = __uint_as_float(xr[k]), x1 = __uint_as_float(xr[k + 1]);
-                        p1[cc / 2] = pack_bf16(l0 * __uint_as_float(gr[k]), l1 * __uint_as_float(gr[k + 1]));
-                        p2[cc / 2] = pack_bf16(l0 * x0, l1 * x1);
-                        // W from the bf16 A1 that V1 contracts: the token's own term of
-                        // <Lam_t, S_t> and of dt_t x_t . v_t then cancel in dl_t
-                        zrun += bf16lo(p1[cc / 2]) * sh.dts[j0 + cc] * x0;
-                        z[cc] = (j0 + cc <= r) ? zrun : 0.f;
-                        zrun += bf16hi(p1[cc / 2]) * sh.dts[j0 + cc + 1] * x1;
-                        z[cc + 1] = (j0 + cc + 1 <= r) ? zrun : 0.f;
+                        const int kx = 16 * q16 + cc;
+                        const float l0 = below ? rfc * sh.seg.colL[j0 + cc] : diag ? row.wl[kx] : 0.f;
+                        const float l1 = below ? rfc * sh.seg.colL[j0 + cc + 1] : diag ? row.wl[kx + 1] : 0.f;
+                        p1[cc / 2] = pack_bf16(l0 * __uint_as_float(xr[kx]) * sh.dts[j0 + cc],
+                                               l1 * __uint_as_float(xr[kx + 1]) * sh.dts[j0 + cc + 1]);
                     }
 #pragma unroll
-                    for (int q = 0; q < 2; ++q) {
+                    for (int q = 0; q < 2; ++q)
                         *reinterpret_cast<uint4*>(sm + kT1 + off2(r, j0 + 8 * q)) =
                             make_uint4(p1[4 * q], p1[4 * q + 1], p1[4 * q + 2], p1[4 * q + 3]);
-                        *reinterpret_cast<uint4*>(sm + kT2 + off2(r, j0 + 8 * q)) =
-                            make_uint4(p2[4 * q], p2[4 * q + 1], p2[4 * q + 2], p2[4 * q + 3]);
+                }
+            }
+#pragma unroll
+            for (int q = 0; q < 4; ++q)
+                *reinterpret_cast<uint4*>(sm + kTDY + sw128_off(r, 32 * hf + 8 * q)) = scale_bf16x8(dv[q], ep_r);
+            warp_arrive(&sh.rdyC, lane);
+            // ---- dx (this half's p) and the per-token partial products (row j = r)
+            float vx = 0.f, lbx = 0.f, scdy = 0.f, ddv = 0.f;
+            uint32_t dxo[16];
+            wait_bar(sh, a, &sh.mma2, k & 1, kWhereMma1);
+            ptx::tc_fence_after();
+            {
+                uint32_t v1[32], v2[32], sc[32];
+                ptx::tmem_load32x2(lane_addr + kTmV1 + 32 * hf, v1, lane_addr + kTmV2 + 32 * hf, v2);
+                ptx::tmem_load32(lane_addr + kTmSC + 32 * hf, sc);
+#pragma unroll
+                for (int kx = 0; kx < 32; kx += 2) {
+                    const int q = kx >> 3, e = kx & 7;
+                    const uint32_t xw = e == 0 ? xv[q].x : e == 2 ? xv[q].y : e == 4 ? xv[q].z : xv[q].w;
+                    const uint32_t dw = e == 0 ? dv[q].x : e == 2 ? dv[q].y : e == 4 ? dv[q].z : dv[q].w;
+                    const float x0 = bf16lo(xw), x1 = bf16hi(xw), y0 = bf16lo(dw), y1 = bf16hi(dw);
+                    const float w0 = __uint_as_float(v2[kx]), w1 = __uint_as_float(v2[kx + 1]);
+                    const float v0 = fmaf(es_r, w0, __uint_as_float(v1[kx]));
+                    const float v1v = fmaf(es_r, w1, __uint_as_float(v1[kx + 1]));
+                    vx = fmaf(v0, x0, fmaf(v1v, x1, vx));
+                    lbx = fmaf(w0, x0, fmaf(w1, x1, lbx));
+                    scdy = fmaf(__uint_as_float(sc[kx]), y0, fmaf(__uint_as_float(sc[kx + 1]), y1, scdy));
+                    ddv = fmaf(y0, x0, fmaf(y1, x1, ddv));
+                    dxo[kx / 2] = pack_bf16(fmaf(d, v0, Dh * y0), fmaf(d, v1v, Dh * y1));
+                }
+            }
+            if (hf == 1) {
+                sh.qv[0][r] = vx;
+                sh.qv[1][r] = lbx;
+                sh.qv[2][r] = scdy;
+                sh.qv[3][r] = ddv;
+            }
+            // ---- this head's share of dB (row j = r, this half's columns) as bf16 over
+            // A2, which the dB contraction has finished reading
+            wait_bar(sh, a, &sh.mmaDB, k & 1, kWhereDB);
+            ptx::tc_fence_after();
+#pragma unroll 1
+            for (int cb = 2 * hf; cb < 2 * hf + 2; ++cb) {
+                uint32_t v[32];
+                ptx::tmem_load32(lane_addr + kTmG + 32 * cb, v);
+#pragma unroll
+                for (int q = 0; q < 4; ++q)
+                    *reinterpret_cast<uint4*>(sm + kT2 + off2(r, 32 * cb + 8 * q)) = make_uint4(
+                        pack_bf16(d * __uint_as_float(v[8 * q]), d * __uint_as_float(v[8 * q + 1])),
+                        pack_bf16(d * __uint_as_float(v[8 * q + 2]), d * __uint_as_float(v[8 * q + 3])),
+                        pack_bf16(d * __uint_as_float(v[8 * q + 4]), d * __uint_as_float(v[8 * q + 5])),
+                        pack_bf16(d * __uint_as_float(v[8 * q + 6]), d * __uint_as_float(v[8 * q + 7])));
+            }
+            // ---- dC (row i = r, this half's columns) as bf16 over A2 o dt, dx over S_in,
+            // once the dC and Lam contractions are done
+            wait_bar(sh, a, &sh.mmaDC, k & 1, kWhereDC);
+            ptx::tc_fence_after();
+#pragma unroll 1
+            for (int cb = 2 * hf; cb < 2 * hf + 2; ++cb) {
+                uint32_t v[32];
+                ptx::tmem_load32(lane_addr + kTmX + 32 * cb, v);
+#pragma unroll
+                for (int q = 0; q < 4; ++q)
+                    *reinterpret_cast<uint4*>(sm + kT1 + off2(r, 32 * cb + 8 * q)) = make_uint4(
+                        pack_bf16(__uint_as_float(v[8 * q]), __uint_as_float(v[8 * q + 1])),
+                        pack_bf16(__uint_as_float(v[8 * q + 2]), __uint_as_float(v[8 * q + 3])),
+                        pack_bf16(__uint_as_float(v[8 * q + 4]), __uint_as_float(v[8 * q + 5])),
+                        pack_bf16(__uint_as_float(v[8 * q + 6]), __uint_as_float(v[8 * q + 7])));
+            }
+#pragma unroll
+            for (int q = 0; q < 4; ++q)
+                *reinterpret_cast<uint4*>(sm + kTSin + sw128_off(r, 32 * hf + 8 * q)) =
+                    make_uint4(dxo[4 * q], dxo[4 * q + 1], dxo[4 * q + 2], dxo[4 * q + 3]);
+            warp_arrive(&sh.rdyS, lane);               // staged, and this chunk's TMEM is read
+            ptx::named_bar(kBarCompute, kCompute);     // sh.part, sh.F, sh.qv and sh.red complete
+            // ---- ddt of token t = r, dA and dD (column half 0 owns the token)
+            {
+                const float K = ((sh.red[0] + sh.red[1]) + (sh.red[2] + sh.red[3])) +
+                                ((sh.red[4] + sh.red[5]) + (sh.red[6] + sh.red[7]));
+                vx += sh.qv[0][r];
+                lbx += sh.qv[1][r];
+                scdy += sh.qv[2][r];
+                ddv += sh.qv[3][r];
+                // U_t = sum_{i >= t} 2^{p_i} scdy_i, V_t = sum_{j <= t} 2^{s_j} dt_j lbx_j,
+                // F_t = sum_{i >= t} F_i (the rows' totals of W over column half 0)
+                float u = ep_r * scdy, v = es_r * d * lbx, f = sh.F[r];
+#pragma unroll
+                for (int o = 1; o < 32; o <<= 1) {
+                    const float tu = __shfl_down_sync(0xffffffffu, u, o);
+                    const float tf = __shfl_down_sync(0xffffffffu, f, o);
+                    const float tv = __shfl_up_sync(0xffffffffu, v, o);
+                    if (lane + o < 32) {
+                        u += tu;
+                        f += tf;
                     }
-                    const float zs = warp_transpose_sum16(z, lane);
-                    if (lane < 16) sh.part[warp][j0 + lane] = zs;
+                    if (lane >= o) v += tv;
+                }
+                if (hf == 0) {
+                    if (lane == 0) {   // the warp's totals
+                        sh.carry[0][rb] = u;
+                        sh.carry[2][rb] = f;
+                    }
+                    if (lane == 31) sh.carry[1][rb] = v;
+                }
+                ptx::named_bar(kBarCompute, kCompute);
+                for (int w = rb + 1; w < 4; ++w) {
+                    u += sh.carry[0][w];
+                    f += sh.carry[2][w];
+                }
+                for (int w = rb - 1; w >= 0; --w) v += sh.carry[1][w];
+                // corner sums: column half 0's transposed sums hold t < 64 in full; for
+                // t >= 64 half 1's, plus the first-half totals F_i of the rows i >= t
+                const float rv = ((sh.part[0][r] + sh.part[1][r]) + (sh.part[2][r] + sh.part[3][r])) +
+                                 (r >= 64 ? f : 0.f);
+                // (a document start's decay is not dt A: it is 0, and so is its gradient)
+                const float dl = start ? 0.f : rv + u + v + etau * K - d * vx;
+                if (hf == 0) {
+                    if (valid) a.ddt[((size_t)b * L + t0 + r) * a.H + h] = fmaf(Ah, dl, vx);
+                    dA_acc = fmaf(d, dl, dA_acc);
+                    dD_acc += ddv;
                 }
             }
+            if (ptx::named_bar_any(kBarCompute, kCompute, *(volatile int*)&sh.abort != 0)) break;
         }
-        // x row j = r becomes 2^{s_j} x_j (the X contraction is done)
-#pragma unroll
-        for (int q = 0; q < 8; ++q) {
-            const uint4 v = xv[q];
-            *reinterpret_cast<uint4*>(sm + kTX + sw128_off(r, 8 * q)) =
-                make_uint4(pack_bf16(bf16lo(v.x) * es_r, bf16hi(v.x) * es_r),
-                           pack_bf16(bf16lo(v.y) * es_r, bf16hi(v.y) * es_r),
-                           pack_bf16(bf16lo(v.z) * es_r, bf16hi(v.z) * es_r),
-                           pack_bf16(bf16lo(v.w) * es_r, bf16hi(v.w) * es_r));
-        }
-        ptx::fence_proxy_async();
-        ptx::tc_fence_before();
-        __syncthreads();
-        // ---- V1 = A1^T dy; dB~ = A2^T C + (2^s o x) Lam^T
-        if (r == 0) {
+        // ---- the adjoint of the initial state; this unit's dA and dD shares
+        if (a.dinit && !*(volatile int*)&sh.abort) {
+            // (the last update contraction completed: its commit was waited for)
             ptx::tc_fence_after();
-            constexpr uint32_t idV = ptx::idesc_bf16(128, 64, 1, 1);
-            constexpr uint32_t idB1 = ptx::idesc_bf16(128, 128, 1, 1);
-            constexpr uint32_t idB2 = ptx::idesc_bf16(128, 128, 0, 0);
-#pragma unroll 1
-            for (int kk = 0; kk < 8; ++kk)
-                ptx::mma_ss(tb + kTmV1, desc_mn2(s0 + kT1, kk), desc_mn1(s0 + kTDY, kk), idV, kk > 0);
-            ptx::mma_commit(&sh.mmaV1);
-#pragma unroll 1
-            for (int kk = 0; kk < 8; ++kk)
-                ptx::mma_ss(tb + kTmG, desc_mn2(s0 + kT2, kk), desc_mn2(s0 + kTC, kk), idB1, kk > 0);
-#pragma unroll 1
-            for (int kk = 0; kk < 4; ++kk)
-                ptx::mma_ss(tb + kTmG, desc_k1(s0 + kTX, kk), desc_k1(s0 + kTLam, kk), idB2, 1);
-            ptx::mma_commit(&sh.mmaDB);
+            uint32_t l0[32];
+            ptx::tmem_load32(lane_addr + kTmLU + 32 * hf, l0);
+#pragma unroll
+            for (int p = 0; p < 32; ++p) a.dinit[unit * PN + (size_t)(32 * hf + p) * N + r] = __uint_as_float(l0[p]);
         }
-        wait_bar(sh, a, &sh.mmaV1, n1 & 1, kWhereV1);
-        ptx::tc_fence_after();
-        // ---- rows of A2 o dt (from X, still in TMEM) over A1; dy row i = r becomes 2^{p_i} dy_i
-#pragma unroll 1
-        for (int cb = 0; cb < 4; ++cb) {
-            const float rfc = (cb == 0) ? row.rf[0] : (cb == 1) ? row.rf[1] : row.rf[2];
-            const bool below = cb < warp, diag = cb == warp;
-            uint32_t xr[32];
-            ptx::tmem_load32(lane_addr + kTmX + 32 * cb, xr);
-#pragma unroll
-            for (int hf = 0; hf < 2; ++hf) {
-                const int j0 = 32 * cb + 16 * hf;
-                uint32_t p1[8];
-#pragma unroll
-                for (int cc = 0; cc < 16; cc += 2) {
-                    const int k = 16 * hf + cc;
-                    const float l0 = below ? rfc * sh.seg.colL[j0 + cc] : diag ? row.wl[k] : 0.f;
-                    const float l1 = below ? rfc * sh.seg.colL[j0 + cc + 1] : diag ? row.wl[k + 1] : 0.f;
-                    p1[cc / 2] = pack_bf16(l0 * __uint_as_float(xr[k]) * sh.dts[j0 + cc],
-                                           l1 * __uint_as_float(xr[k + 1]) * sh.dts[j0 + cc + 1]);
-                }
-#pragma unroll
-                for (int q = 0; q < 2; ++q)
-                    *reinterpret_cast<uint4*>(sm + kT1 + off2(r, j0 + 8 * q)) =
-                        make_uint4(p1[4 * q], p1[4 * q + 1], p1[4 * q + 2], p1[4 * q + 3]);
-            }
+        dA_acc = warp_sum(dA_acc);
+        dD_acc = warp_sum(dD_acc);
+        ptx::named_bar(kBarCompute, kCompute);
+        if (lane == 0) {
+            sh.red[warp] = dA_acc;
+            sh.red[8 + warp] = dD_acc;
         }
-#pragma unroll
-        for (int q = 0; q < 8; ++q) {
-            const uint4 v = dv[q];
-            *reinterpret_cast<uint4*>(sm + kTDY + sw128_off(r, 8 * q)) =
-                make_uint4(pack_bf16(bf16lo(v.x) * ep_r, bf16hi(v.x) * ep_r),
-                           pack_bf16(bf16lo(v.y) * ep_r, bf16hi(v.y) * ep_r),
-                           pack_bf16(bf16lo(v.z) * ep_r, bf16hi(v.z) * ep_r),
-                           pack_bf16(bf16lo(v.w) * ep_r, bf16hi(v.w) * ep_r));
+        ptx::named_bar(kBarCompute, kCompute);
+        if (threadIdx.x == 0) {
+            a.ws_dA[unit] = (sh.red[0] + sh.red[1]) + (sh.red[2] + sh.red[3]);
+            a.ws_dD[unit] = (sh.red[8] + sh.red[9]) + (sh.red[10] + sh.red[11]);
         }
-        ptx::fence_proxy_async();
-        ptx::tc_fence_before();
-        __syncthreads();
-        // ---- dC = (A2 o dt) B + (2^p o dy) S_in^T; Lam^T += C^T (2^p o dy)
-        if (r == 0) {
-            ptx::tc_fence_after();
-            constexpr uint32_t idC1 = ptx::idesc_bf16(128, 128, 0, 1);
-            constexpr uint32_t idC2 = ptx::idesc_bf16(128, 128, 0, 0);
-            constexpr uint32_t idL = ptx::idesc_bf16(128, 64, 1, 1);
-#pragma unroll 1
-            for (int kk = 0; kk < 8; ++kk)
-                ptx::mma_ss(tb + kTmX, desc_k2(s0 + kT1, kk), desc_mn2(s0 + kTB, kk), idC1, kk > 0);
-#pragma unroll 1
-            for (int kk = 0; kk < 4; ++kk)
-                ptx::mma_ss(tb + kTmX, desc_k1(s0 + kTDY, kk), desc_k1(s0 + kTSin, kk), idC2, 1);
-#pragma unroll 1
-            for (int kk = 0; kk < 8; ++kk)
-                ptx::mma_ss(tb + kTmLU, desc_mn2(s0 + kTC, kk), desc_mn1(s0 + kTDY, kk), idL, 1);
-            ptx::mma_commit(&sh.mmaDC);
-        }
-        // ---- dx and the per-token products (row j = r)
-        float vx = 0.f, lbx = 0.f, scdy = 0.f, ddv = 0.f;
-        uint32_t dxo[32];   // dx row, bf16 pairs
-        wait_bar(sh, a, &sh.mma2, n1 & 1, kWhereMma1);
-        ptx::tc_fence_after();
-#pragma unroll
-        for (int hf = 0; hf < 2; ++hf) {
-            uint32_t v1[32], v2[32], sc[32];
-            ptx::tmem_load32x2(lane_addr + kTmV1 + 32 * hf, v1, lane_addr + kTmV2 + 32 * hf, v2);
-            ptx::tmem_load32(lane_addr + kTmSC + 32 * hf, sc);
-#pragma unroll
-            for (int k = 0; k < 32; k += 2) {
-                const int q = (32 * hf + k) >> 3, e = (32 * hf + k) & 7;
-                const uint32_t xw = e == 0 ? xv[q].x : e == 2 ? xv[q].y : e == 4 ? xv[q].z : xv[q].w;
-                const uint32_t dw = e == 0 ? dv[q].x : e == 2 ? dv[q].y : e == 4 ? dv[q].z : dv[q].w;
-                const float x0 = bf16lo(xw), x1 = bf16hi(xw), y0 = bf16lo(dw), y1 = bf16hi(dw);
-                const float w0 = __uint_as_float(v2[k]), w1 = __uint_as_float(v2[k + 1]);
-                const float v0 = fmaf(es_r, w0, __uint_as_float(v1[k]));
-                const float v1v = fmaf(es_r, w1, __uint_as_float(v1[k + 1]));
-                vx = fmaf(v0, x0, fmaf(v1v, x1, vx));
-                lbx = fmaf(w0, x0, fmaf(w1, x1, lbx));
-                scdy = fmaf(__uint_as_float(sc[k]), y0, fmaf(__uint_as_float(sc[k + 1]), y1, scdy));
-                ddv = fmaf(y0, x0, fmaf(y1, x1, ddv));
-                dxo[(32 * hf + k) / 2] = pack_bf16(fmaf(d, v0, Dh * y0), fmaf(d, v1v, Dh * y1));
-            }
-        }
-        // ---- this head's share of dB (row j = r) as bf16, staged for a TMA store over A2
-        // (which the dB contraction has finished reading)
-        wait_bar(sh, a, &sh.mmaDB, n1 & 1, kWhereDB);
-        ptx::tc_fence_after();
-#pragma unroll 1
-        for (int k = 0; k < 4; ++k) {
-            uint32_t v[32];
-            ptx::tmem_load32(lane_addr + kTmG + 32 * k, v);
-#pragma unroll
-            for (int q = 0; q < 4; ++q)
-                *reinterpret_cast<uint4*>(sm + kT2 + off2(r, 32 * k + 8 * q)) = make_uint4(
-                    pack_bf16(d * __uint_as_float(v[8 * q]), d * __uint_as_float(v[8 * q + 1])),
-                    pack_bf16(d * __uint_as_float(v[8 * q + 2]), d * __uint_as_float(v[8 * q + 3])),
-                    pack_bf16(d * __uint_as_float(v[8 * q + 4]), d * __uint_as_float(v[8 * q + 5])),
-                    pack_bf16(d * __uint_as_float(v[8 * q + 6]), d * __uint_as_float(v[8 * q + 7])));
-        }
-        // ---- dC (row i = r) as bf16 over A2 o dt, dx over S_in, once the dC and Lam
-        // contractions are done
-        wait_bar(sh, a, &sh.mmaDC, n1 & 1, kWhereDC);
-        ++n1;
-        ptx::tc_fence_after();
-#pragma unroll 1
-        for (int k = 0; k < 4; ++k) {
-            uint32_t v[32];
-            ptx::tmem_load32(lane_addr + kTmX + 32 * k, v);
-#pragma unroll
-            for (int q = 0; q < 4; ++q)
-                *reinterpret_cast<uint4*>(sm + kT1 + off2(r, 32 * k + 8 * q)) = make_uint4(
-                    pack_bf16(__uint_as_float(v[8 * q]), __uint_as_float(v[8 * q + 1])),
-                    pack_bf16(__uint_as_float(v[8 * q + 2]), __uint_as_float(v[8 * q + 3])),
-                    pack_bf16(__uint_as_float(v[8 * q + 4]), __uint_as_float(v[8 * q + 5])),
-                    pack_bf16(__uint_as_float(v[8 * q + 6]), __uint_as_float(v[8 * q + 7])));
-        }
-#pragma unroll
-        for (int q = 0; q < 8; ++q)
-            *reinterpret_cast<uint4*>(sm + kTSin + sw128_off(r, 8 * q)) =
-                make_uint4(dxo[4 * q], dxo[4 * q + 1], dxo[4 * q + 2], dxo[4 * q + 3]);
-        ptx::fence_proxy_async();
-        ptx::tc_fence_before();
-        __syncthreads();   // staged rows complete; sh.part complete
-        if (r == 0) {
-            // (rows past the sequence's end are clipped by the tensor maps; the next
-            // chunk rewrites these tiles only after its segsum, by which time thread 0
-            // has waited for the stores to read them)
-            ptx::tma_store_4d(&prm.tm_dB, sm + kT2, 0, h, (int)t0, b);
-            ptx::tma_store_4d(&prm.tm_dB, sm + kT2 + 16384, 64, h, (int)t0, b);
-            ptx::tma_store_4d(&prm.tm_dC, sm + kT1, 0, h, (int)t0, b);
-            ptx::tma_store_4d(&prm.tm_dC, sm + kT1 + 16384, 64, h, (int)t0, b);
-            ptx::tma_store_4d(&prm.tm_dx, sm + kTSin, 0, h, (int)t0, b);
-            ptx::bulk_commit();
-        }
-        // ---- ddt of token t = r, dA and dD
-        {
-            const float rv = (sh.part[0][r] + sh.part[1][r]) + (sh.part[2][r] + sh.part[3][r]);
-            // U_t = sum_{i >= t} 2^{p_i} scdy_i, V_t = sum_{j <= t} 2^{s_j} dt_j lbx_j
-            float u = ep_r * scdy, v = es_r * d * lbx;
-#pragma unroll
-            for (int o = 1; o < 32; o <<= 1) {
-                const float tu = __shfl_down_sync(0xffffffffu, u, o);
-                const float tv = __shfl_up_sync(0xffffffffu, v, o);
-                if (lane + o < 32) u += tu;
-                if (lane >= o) v += tv;
-            }
-            if (lane == 0) sh.carry[0][warp] = u;    // the warp's total of u
-            if (lane == 31) sh.carry[1][warp] = v;   // the warp's total of v
-            __syncthreads();
-            for (int w = warp + 1; w < 4; ++w) u += sh.carry[0][w];
-            for (int w = warp - 1; w >= 0; --w) v += sh.carry[1][w];
-            // (a document start's decay is not dt A: it is 0, and so is its gradient)
-            const float dl = start ? 0.f : rv + u + v + etau * K - d * vx;
-            if (valid) a.ddt[((size_t)b * L + t0 + r) * a.H + h] = fmaf(Ah, dl, vx);
-            dA_acc = fmaf(d, dl, dA_acc);
-            dD_acc += ddv;
-        }
-        __syncthreads();   // the token scans' shared values are read; TMEM free
-    }
-    // ---- the adjoint of the initial state; this unit's dA and dD shares
-    if (a.dinit && !*(volatile int*)&sh.abort) {
-        ptx::tc_fence_after();
-        uint32_t l0[32], l1[32];
-        ptx::tmem_load32x2(lane_addr + kTmLU, l0, lane_addr + kTmLU + 32, l1);
-#pragma unroll
-        for (int p = 0; p < 32; ++p) {
-            a.dinit[unit * PN + (size_t)p * N + r] = __uint_as_float(l0[p]);
-            a.dinit[unit * PN + (size_t)(p + 32) * N + r] = __uint_as_float(l1[p]);
-        }
-    }
-    dA_acc = warp_sum(dA_acc);
-    dD_acc = warp_sum(dD_acc);
-    __syncthreads();
-    if (lane == 0) {
-        sh.red[warp] = dA_acc;
-        sh.red[4 + warp] = dD_acc;
-    }
-    __syncthreads();
-    if (r == 0) {
-        ptx::bulk_wait0();   // this CTA's stores are complete
-        a.ws_dA[unit] = (sh.red[0] + sh.red[1]) + (sh.red[2] + sh.red[3]);
-        a.ws_dD[unit] = (sh.red[4] + sh.red[5]) + (sh.red[6] + sh.red[7]);
-        // every MMA issued has completed before the tensor memory is freed, and (after
-        // a wait that ran out) the last load issued has landed before the CTA exits
-        ptx::mma_commit(&sh.drain);
-        if (!ptx::mbar_wait(&sh.drain, 0, &sh.never, a.wait_iters)) record_error(a.ws, SSD_ERR_TIMEOUT, kWhereDrain);
-        if (nissue > nfull && !ptx::mbar_wait(&sh.full, (nissue - 1) & 1, &sh.never, a.wait_iters))
-            record_error(a.ws, SSD_ERR_TIMEOUT, kWhereDrain);
     }
     ptx::tc_fence_before();
     __syncthreads();
