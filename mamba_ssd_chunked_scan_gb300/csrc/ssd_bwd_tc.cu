@@ -54,6 +54,8 @@ constexpr uint32_t kTSin = 114688;    // S_in as (row n, p) bf16; then dx, stage
 constexpr uint32_t kT1 = 131072;      // A1 (row i, column j); then A2 o dt; then the dC share
 constexpr uint32_t kT2 = 163840;      // A2; then the dB share
 constexpr uint32_t kTiles = 196608;
+// Phase 1 keeps two stages of (x, B): chunk c uses stage c & 1, stage 1's x in the
+// S_in tile and its B in the A1 tile, so each load runs two chunks ahead.
 // TMEM columns (phase 1: the state summary in columns 0-63 or 64-127, by chunk parity)
 constexpr uint32_t kTmG = 0, kTmX = 128, kTmV2 = 256, kTmSC = 320, kTmV1 = 384, kTmLU = 448, kTmCols = 512;
 
@@ -69,7 +71,7 @@ struct BwdTcSmall {
     float qv[4][Q];         // column half 1's partial row sums (vx, lbx, scdy, dy . x)
     float red[16];
     float carry[3][4];      // warp totals of the token scans
-    uint64_t full, mmaF, mma1, mma2, mmaV1, mmaDB, mmaDC, drain;   // loads and MMAs complete
+    uint64_t full, full1, mmaF, mma1, mma2, mmaV1, mmaDB, mmaDC, drain;   // loads and MMAs complete
     uint64_t rdyF, rdyA, rdyB, rdyC, rdyS;                          // compute warps -> issuer
     uint64_t stFree;                                                // the stores have read their tiles
     uint32_t tmem_base;
@@ -193,6 +195,7 @@ __global__ void __launch_bounds__(kThreads, 1) ssd_bwd_tc(const __grid_constant_
 
     if (threadIdx.x == 0) {
         ptx::mbar_init(&sh.full, 1);
+        ptx::mbar_init(&sh.full1, 1);
         ptx::mbar_init(&sh.mmaF, 1);
         ptx::mbar_init(&sh.mma1, 1);
         ptx::mbar_init(&sh.mma2, 1);
@@ -226,17 +229,22 @@ __global__ void __launch_bounds__(kThreads, 1) ssd_bwd_tc(const __grid_constant_
             ptx::prefetch_tmap(&prm.tm_dx);
             ptx::prefetch_tmap(&prm.tm_dB);
             ptx::prefetch_tmap(&prm.tm_dC);
-            uint32_t nfull = 0, nissue = 0;   // phases of `full` completed (and waited for), loads issued
-            auto load1 = [&](int c) {         // phase 1: x and B of chunk c
-                ++nissue;
+            // per stage: loads issued, and phases known complete (waited for by someone)
+            uint32_t nissue[2] = {0, 0}, ndone[2] = {0, 0};
+            auto load1 = [&](int c) {         // phase 1: x and B of chunk c, into stage c & 1
+                const int st = c & 1;
+                ++nissue[st];
+                uint64_t* bar = st ? &sh.full1 : &sh.full;
+                uint8_t* xt = sm + (st ? kTSin : kTX);
+                uint8_t* bt = sm + (st ? kT1 : kTB);
                 const int t0 = c * Q;
-                ptx::mbar_expect_tx(&sh.full, 16384u + 32768u);
-                ptx::tma_load_4d(sm + kTX, &prm.tm_x, &sh.full, 0, h, t0, b);
-                ptx::tma_load_4d(sm + kTB, &prm.tm_B, &sh.full, 0, g, t0, b);
-                ptx::tma_load_4d(sm + kTB + 16384, &prm.tm_B, &sh.full, 64, g, t0, b);
+                ptx::mbar_expect_tx(bar, 16384u + 32768u);
+                ptx::tma_load_4d(xt, &prm.tm_x, bar, 0, h, t0, b);
+                ptx::tma_load_4d(bt, &prm.tm_B, bar, 0, g, t0, b);
+                ptx::tma_load_4d(bt + 16384, &prm.tm_B, bar, 64, g, t0, b);
             };
             auto load2 = [&](int c) {         // phase 2: x, dy, B and C of chunk c; chunk c - 1 towards L2
-                ++nissue;
+                ++nissue[0];
                 const int t0 = c * Q;
                 ptx::mbar_expect_tx(&sh.full, 16384u * 2u + 32768u * 2u);
                 ptx::tma_load_4d(sm + kTX, &prm.tm_x, &sh.full, 0, h, t0, b);
@@ -259,25 +267,28 @@ __global__ void __launch_bounds__(kThreads, 1) ssd_bwd_tc(const __grid_constant_
             // ---- phase 1: the compute warps scale x once its load lands, then this
             // chunk's state summary goes to the TMEM columns of its parity
             if (nch > 0) load1(0);
+            if (nch > 1) load1(1);
             for (int c = 0; c < nch; ++c) {
+                const int st = c & 1;
                 if (!wait_bar(sh, a, &sh.rdyF, c & 1, kWhereReady)) break;
-                ++nfull;   // (the compute warps waited for this load before arriving)
+                ++ndone[st];   // (the compute warps waited for this load before arriving)
                 ptx::tc_fence_after();
                 constexpr uint32_t id = ptx::idesc_bf16(128, 64, 1, 1);
+                const uint32_t xt = s0 + (st ? kTSin : kTX), bt = s0 + (st ? kT1 : kTB);
 #pragma unroll 1
                 for (int kk = 0; kk < 8; ++kk)
-                    ptx::mma_ss(tb + 64 * (c & 1), desc_mn2(s0 + kTB, kk), desc_mn1(s0 + kTX, kk), id, kk > 0);
+                    ptx::mma_ss(tb + 64 * st, desc_mn2(bt, kk), desc_mn1(xt, kk), id, kk > 0);
                 ptx::mma_commit(&sh.mmaF);
                 if (!wait_bar(sh, a, &sh.mmaF, c & 1, kWhereF)) break;
-                if (c + 1 < nch) load1(c + 1);
+                if (c + 2 < nch) load1(c + 2);   // the stage is free again
             }
-            // ---- phase 2
+            // ---- phase 2 (stage 0's barrier only)
             if (nch > 0 && !*(volatile int*)&sh.abort) load2(nch - 1);
             for (int k = 0; k < nch && !*(volatile int*)&sh.abort; ++k) {
                 const int c = nch - 1 - k;
                 const int t0 = c * Q;
-                if (!wait_bar(sh, a, &sh.full, nfull & 1, kWhereLoad)) break;
-                ++nfull;
+                if (!wait_bar(sh, a, &sh.full, ndone[0] & 1, kWhereLoad)) break;
+                ++ndone[0];
                 // TMEM free: the last chunk's shares (or phase 1's state summaries) are read
                 if (!wait_bar(sh, a, &sh.rdyS, k & 1, kWhereReady)) break;
                 ptx::tc_fence_after();
@@ -355,8 +366,10 @@ __global__ void __launch_bounds__(kThreads, 1) ssd_bwd_tc(const __grid_constant_
             // and the stores are complete
             ptx::mma_commit(&sh.drain);
             if (!ptx::mbar_wait(&sh.drain, 0, &sh.never, a.wait_iters)) record_error(a.ws, SSD_ERR_TIMEOUT, kWhereDrain);
-            if (nissue > nfull && !ptx::mbar_wait(&sh.full, (nissue - 1) & 1, &sh.never, a.wait_iters))
-                record_error(a.ws, SSD_ERR_TIMEOUT, kWhereDrain);
+            for (int st = 0; st < 2; ++st)
+                if (nissue[st] > ndone[st] && !ptx::mbar_wait(st ? &sh.full1 : &sh.full, (nissue[st] - 1) & 1,
+                                                             &sh.never, a.wait_iters))
+                    record_error(a.ws, SSD_ERR_TIMEOUT, kWhereDrain);
             ptx::bulk_wait0();
         }
         __syncwarp();
@@ -379,15 +392,18 @@ __global__ void __launch_bounds__(kThreads, 1) ssd_bwd_tc(const __grid_constant_
         };
 
         // ------------------------------------------------------------ phase 1
+        // Chunk c's segsum runs while chunk c - 1's state summary is on the tensor
+        // cores; then S (the state entering chunk c) is updated and kept.
         float S[32];   // S^T[n = r][p], this half's p
 #pragma unroll
         for (int p = 0; p < 32; ++p) S[p] = a.init ? a.init[unit * PN + (size_t)(32 * hf + p) * N + r] : 0.f;
+        float etau_prev = 0.f;
+        float d1_next = dt_at(r);
         for (int c = 0; c < nch; ++c) {
             const int64_t t0 = (int64_t)c * Q;
-            const float d = dt_at(t0 + r);
+            const float d = d1_next;   // (loaded a chunk earlier)
             decays(d, t0 + r < L && doc_start_tc(a, t0 + r));
-#pragma unroll
-            for (int p = 0; p < 32; ++p) ckpt[(size_t)c * PN + (size_t)(32 * hf + p) * N + r] = S[p];
+            d1_next = c + 1 < nch ? dt_at(t0 + Q + r) : 0.f;
             ptx::named_bar(kBarCompute, kCompute);
             SegsumLinRow<4> row;
             segsum_lin_phase1<4>(sh.seg, row, rb, lane, hf == 0);
@@ -396,22 +412,29 @@ __global__ void __launch_bounds__(kThreads, 1) ssd_bwd_tc(const __grid_constant_
             ptx::named_bar(kBarCompute, kCompute);
             const float w = segsum_lin_suffix<4>(sh.seg, r) * d;
             const float etau = sh.seg.tauL;
-            wait_bar(sh, a, &sh.full, nfull & 1, kWhereLoad);
-            ++nfull;
+            if (c > 0) {   // S <- 2^tau S + the summary of chunk c - 1
+                wait_bar(sh, a, &sh.mmaF, (c - 1) & 1, kWhereF);
+                ptx::tc_fence_after();
+                uint32_t dd[32];
+                ptx::tmem_load32(lane_addr + 64 * ((c - 1) & 1) + 32 * hf, dd);
+#pragma unroll
+                for (int p = 0; p < 32; ++p) S[p] = fmaf(etau_prev, S[p], __uint_as_float(dd[p]));
+            }
+            etau_prev = etau;
+#pragma unroll
+            for (int p = 0; p < 32; ++p) ckpt[(size_t)c * PN + (size_t)(32 * hf + p) * N + r] = S[p];
+            wait_bar(sh, a, (c & 1) ? &sh.full1 : &sh.full, (c >> 1) & 1, kWhereLoad);
 #pragma unroll
             for (int q = 0; q < 4; ++q) {   // w_j x_j in place (row j = r, this half's p)
-                uint4* px = reinterpret_cast<uint4*>(sm + kTX + sw128_off(r, 32 * hf + 8 * q));
+                uint4* px = reinterpret_cast<uint4*>(sm + ((c & 1) ? kTSin : kTX) + sw128_off(r, 32 * hf + 8 * q));
                 *px = scale_bf16x8(*px, w);
             }
             warp_arrive(&sh.rdyF, lane);
-            wait_bar(sh, a, &sh.mmaF, c & 1, kWhereF);
-            ptx::tc_fence_after();
-            uint32_t dd[32];
-            ptx::tmem_load32(lane_addr + 64 * (c & 1) + 32 * hf, dd);
-#pragma unroll
-            for (int p = 0; p < 32; ++p) S[p] = fmaf(etau, S[p], __uint_as_float(dd[p]));
         }
+        // (the last chunk's summary is not needed; the issue warp waits for it before
+        // phase 2's loads)
         warp_arrive(&sh.rdyS, lane);   // the state summaries are read: TMEM free for phase 2
+        nfull = (uint32_t)(nch + 1) / 2;   // phase 1's uses of stage 0's barrier
 
         // ------------------------------------------------------------ phase 2
         // Lam^T (lane n, column p) lives in TMEM: each chunk scales it by 2^tau in
