@@ -18,12 +18,13 @@
 //   and the per-token terms of ddt from row sums of those products and of
 //   W = A1 o dt o X (its corner sums by warp transpose-reductions).
 //
-// One CTA of 288 threads per (batch row, head).  Warps 0-7 compute: thread
+// One CTA of 384 threads per (batch row, head).  Warps 0-7 compute: thread
 // (warp w, lane) owns chunk row (and state column) r = 32 (w % 4) + lane and
 // the column half w / 4 of that row; both halves of a row run its segsum.
 // Warp 8 issues: its lane 0 issues the TMA loads, the MMAs and the TMA stores,
 // handed over through mbarriers, so the next chunk's loads start as soon as
-// this chunk's last contraction is done.  Every wait is bounded; a wait that
+// this chunk's last contraction is done (warps 9-11 only complete its
+// warpgroup, whose registers go to the compute warps).  Every wait is bounded; a wait that
 // runs out records SSD_ERR_TIMEOUT in the workspace status word, and the CTA
 // drains its MMAs and copies, frees its TMEM and exits.
 #include <cuda.h>
@@ -41,8 +42,12 @@ namespace ssd {
 namespace {
 
 constexpr int Q = 128, P = 64, N = 128;
-constexpr int kCompute = 256;                 // compute threads (8 warps)
-constexpr int kThreads = kCompute + 32;       // and the issue warp
+constexpr int kCompute = 256;                 // compute threads (warpgroups 0 and 1)
+constexpr int kThreads = kCompute + 128;      // and the issue warpgroup (one lane issues)
+// setmaxnreg budgets: registers are allocated per warpgroup, so the issue group
+// hands its share to the compute groups
+constexpr int kRegsIssue = 56, kRegsCompute = 224;   // 128 * (56 + 2 * 224) = 64512 <= 384 * 168
+static_assert(128 * (kRegsIssue + 2 * kRegsCompute) <= kThreads * 168, "register split must fit the launch total");
 constexpr int kBarCompute = 1;                // named barrier of the compute threads
 // shared tiles (each 1024-byte aligned for the 128-byte swizzle)
 constexpr uint32_t kTX = 0;           // x (row j, p); then 2^{s_j} x_j (phase 1: w_j x_j)
@@ -66,12 +71,14 @@ enum : uint32_t { kWhereLoad = 31, kWhereMma1 = 32, kWhereV1 = 33, kWhereDB = 34
 struct BwdTcSmall {
     SegsumLinShared<4> seg;
     alignas(16) float dts[Q];
-    float part[4][Q];       // per row block: partial corner sums of W (column half 0: t < 64, half 1: t >= 64)
-    float F[Q];             // per row: the sum of W over column half 0
-    float qv[4][Q];         // column half 1's partial row sums (vx, lbx, scdy, dy . x)
+    // per chunk parity (a chunk's token pass runs during the next chunk):
+    float part[2][4][Q];    // per row block: partial corner sums of W (column half 0: t < 64, half 1: t >= 64)
+    float F[2][Q];          // per row: the sum of W over column half 0
+    float qv[2][4][Q];      // column half 1's partial row sums (vx, lbx, scdy, dy . x)
+    float kred[2][8];       // per warp: partial <Lam, S_in>
     float red[16];
     float carry[3][4];      // warp totals of the token scans
-    uint64_t full, full1, mmaF, mma1, mma2, mmaV1, mmaDB, mmaDC, drain;   // loads and MMAs complete
+    uint64_t full, full1, mmaF, mma1, mma2, mmaV1, mmaDB, mmaDC, mmaLU, drain;   // loads and MMAs complete
     uint64_t rdyF, rdyA, rdyB, rdyC, rdyS;                          // compute warps -> issuer
     uint64_t stFree;                                                // the stores have read their tiles
     uint32_t tmem_base;
@@ -202,6 +209,7 @@ __global__ void __launch_bounds__(kThreads, 1) ssd_bwd_tc(const __grid_constant_
         ptx::mbar_init(&sh.mmaV1, 1);
         ptx::mbar_init(&sh.mmaDB, 1);
         ptx::mbar_init(&sh.mmaDC, 1);
+        ptx::mbar_init(&sh.mmaLU, 1);
         ptx::mbar_init(&sh.drain, 1);
         ptx::mbar_init(&sh.rdyF, 8);
         ptx::mbar_init(&sh.rdyA, 8);
@@ -219,9 +227,10 @@ __global__ void __launch_bounds__(kThreads, 1) ssd_bwd_tc(const __grid_constant_
     ptx::tc_fence_after();
     const uint32_t tb = sh.tmem_base;
 
-    if (warp == 8) {
-        // ================================================================ issue warp
-        if (lane == 0) {
+    if (warp >= 8) {
+        // ================================================================ issue warpgroup
+        ptx::regs_dec<kRegsIssue>();
+        if (warp == 8 && lane == 0) {
             ptx::prefetch_tmap(&prm.tm_x);
             ptx::prefetch_tmap(&prm.tm_dy);
             ptx::prefetch_tmap(&prm.tm_B);
@@ -343,13 +352,14 @@ __global__ void __launch_bounds__(kThreads, 1) ssd_bwd_tc(const __grid_constant_
 #pragma unroll 1
                     for (int kk = 0; kk < 4; ++kk)
                         ptx::mma_ss(tb + kTmX, desc_k1(s0 + kTDY, kk), desc_k1(s0 + kTSin, kk), idC2, 1);
+                    ptx::mma_commit(&sh.mmaDC);
 #pragma unroll 1
                     for (int kk = 0; kk < 8; ++kk)
                         ptx::mma_ss(tb + kTmLU, desc_mn2(s0 + kTC, kk), desc_mn1(s0 + kTDY, kk), idL, 1);
-                    ptx::mma_commit(&sh.mmaDC);
+                    ptx::mma_commit(&sh.mmaLU);
                 }
                 // every contraction of the chunk is done: its tiles take the next chunk's loads
-                if (!wait_bar(sh, a, &sh.mmaDC, k & 1, kWhereDC)) break;
+                if (!wait_bar(sh, a, &sh.mmaLU, k & 1, kWhereDC)) break;
                 if (c > 0) load2(c - 1);
                 // the shares and dx staged: their stores (rows past the end are clipped)
                 if (!wait_bar(sh, a, &sh.rdyS, (k + 1) & 1, kWhereStores)) break;
@@ -375,6 +385,7 @@ __global__ void __launch_bounds__(kThreads, 1) ssd_bwd_tc(const __grid_constant_
         __syncwarp();
     } else {
         // ================================================================ compute warps
+        ptx::regs_inc<kRegsCompute>();
         const int rb = warp & 3, hf = warp >> 2;   // row block (TMEM lane quarter), column half
         const int r = 32 * rb + lane;              // chunk row = state column = TMEM lane
         const uint32_t lane_addr = tb + ((uint32_t)(32 * rb) << 16);
@@ -451,6 +462,59 @@ __global__ void __launch_bounds__(kThreads, 1) ssd_bwd_tc(const __grid_constant_
             ptx::tmem_st_wait();
         }
         float dA_acc = 0.f, dD_acc = 0.f;
+        // a chunk's per-token values, for its token pass
+        struct Tok {
+            float vx, lbx, scdy, ddv, es, ep, d, etau;
+            int64_t t0;
+            bool start, valid;
+        };
+        Tok prev{};
+        // ddt of token t = r, dA and dD (column half 0 owns the token), from the chunk's
+        // shared values in buffer pb
+        auto token_pass = [&](const Tok& T, int pb) {
+            const float K = ((sh.kred[pb][0] + sh.kred[pb][1]) + (sh.kred[pb][2] + sh.kred[pb][3])) +
+                            ((sh.kred[pb][4] + sh.kred[pb][5]) + (sh.kred[pb][6] + sh.kred[pb][7]));
+            const float vx = T.vx + sh.qv[pb][0][r], lbx = T.lbx + sh.qv[pb][1][r];
+            const float scdy = T.scdy + sh.qv[pb][2][r], ddv = T.ddv + sh.qv[pb][3][r];
+            // U_t = sum_{i >= t} 2^{p_i} scdy_i, V_t = sum_{j <= t} 2^{s_j} dt_j lbx_j,
+            // F_t = sum_{i >= t} F_i (the rows' totals of W over column half 0)
+            float u = T.ep * scdy, v = T.es * T.d * lbx, f = sh.F[pb][r];
+#pragma unroll
+            for (int o = 1; o < 32; o <<= 1) {
+                const float tu = __shfl_down_sync(0xffffffffu, u, o);
+                const float tf = __shfl_down_sync(0xffffffffu, f, o);
+                const float tv = __shfl_up_sync(0xffffffffu, v, o);
+                if (lane + o < 32) {
+                    u += tu;
+                    f += tf;
+                }
+                if (lane >= o) v += tv;
+            }
+            if (hf == 0) {
+                if (lane == 0) {   // the warp's totals
+                    sh.carry[0][rb] = u;
+                    sh.carry[2][rb] = f;
+                }
+                if (lane == 31) sh.carry[1][rb] = v;
+            }
+            ptx::named_bar(kBarCompute, kCompute);
+            for (int w = rb + 1; w < 4; ++w) {
+                u += sh.carry[0][w];
+                f += sh.carry[2][w];
+            }
+            for (int w = rb - 1; w >= 0; --w) v += sh.carry[1][w];
+            // corner sums: column half 0's transposed sums hold t < 64 in full; for
+            // t >= 64 half 1's, plus the first-half totals F_i of the rows i >= t
+            const float rv = ((sh.part[pb][0][r] + sh.part[pb][1][r]) + (sh.part[pb][2][r] + sh.part[pb][3][r])) +
+                             (r >= 64 ? f : 0.f);
+            // (a document start's decay is not dt A: it is 0, and so is its gradient)
+            const float dl = T.start ? 0.f : rv + u + v + T.etau * K - T.d * vx;
+            if (hf == 0) {
+                if (T.valid) a.ddt[((size_t)b * L + T.t0 + r) * a.H + h] = fmaf(Ah, dl, vx);
+                dA_acc = fmaf(T.d, dl, dA_acc);
+                dD_acc += ddv;
+            }
+        };
         float d_next = nch > 0 ? dt_at((int64_t)(nch - 1) * Q + r) : 0.f;
         for (int k = 0; k < nch; ++k) {
             const int c = nch - 1 - k;
@@ -472,7 +536,11 @@ __global__ void __launch_bounds__(kThreads, 1) ssd_bwd_tc(const __grid_constant_
             // the last chunk's stores have read S_in, A1 and A2
             if (k > 0) wait_bar(sh, a, &sh.stFree, (k - 1) & 1, kWhereStores);
             // S_in and Lam as bf16 (row n = r, this half's p) operands; <Lam, S_in>;
-            // Lam^T <- 2^tau Lam^T in TMEM (the last update contraction is done)
+            // Lam^T <- 2^tau Lam^T in TMEM, once the last update contraction is done
+            if (k > 0) {
+                wait_bar(sh, a, &sh.mmaLU, (k - 1) & 1, kWhereDC);
+                ptx::tc_fence_after();
+            }
             float kdot = 0.f;
             {
                 const float* src = ckpt + (size_t)c * PN + (size_t)(32 * hf) * N + r;
@@ -508,7 +576,9 @@ __global__ void __launch_bounds__(kThreads, 1) ssd_bwd_tc(const __grid_constant_
             }
             warp_arrive(&sh.rdyA, lane);
             kdot = warp_sum(kdot);
-            if (lane == 0) sh.red[warp] = kdot;
+            if (lane == 0) sh.kred[k & 1][warp] = kdot;
+            // the last chunk's token pass, while this chunk's first contractions run
+            if (k > 0) token_pass(prev, (k - 1) & 1);
             // this row's x and dy (this half's p), kept for the epilogue before the
             // tiles are rescaled
             wait_bar(sh, a, &sh.full, nfull & 1, kWhereLoad);
@@ -561,10 +631,10 @@ __global__ void __launch_bounds__(kThreads, 1) ssd_bwd_tc(const __grid_constant_
                                 make_uint4(p2[4 * q], p2[4 * q + 1], p2[4 * q + 2], p2[4 * q + 3]);
                         }
                         const float zs = warp_transpose_sum16(z, lane);
-                        if (lane < 16) sh.part[rb][j0 + lane] = zs;
+                        if (lane < 16) sh.part[k & 1][rb][j0 + lane] = zs;
                     }
                 }
-                if (hf == 0) sh.F[r] = zrun;
+                if (hf == 0) sh.F[k & 1][r] = zrun;
             }
             // x row j = r, this half's p, becomes 2^{s_j} x_j (the X contraction is done)
 #pragma unroll
@@ -629,10 +699,10 @@ __global__ void __launch_bounds__(kThreads, 1) ssd_bwd_tc(const __grid_constant_
                 }
             }
             if (hf == 1) {
-                sh.qv[0][r] = vx;
-                sh.qv[1][r] = lbx;
-                sh.qv[2][r] = scdy;
-                sh.qv[3][r] = ddv;
+                sh.qv[k & 1][0][r] = vx;
+                sh.qv[k & 1][1][r] = lbx;
+                sh.qv[k & 1][2][r] = scdy;
+                sh.qv[k & 1][3][r] = ddv;
             }
             // ---- this head's share of dB (row j = r, this half's columns) as bf16 over
             // A2, which the dB contraction has finished reading
@@ -670,60 +740,14 @@ __global__ void __launch_bounds__(kThreads, 1) ssd_bwd_tc(const __grid_constant_
             for (int q = 0; q < 4; ++q)
                 *reinterpret_cast<uint4*>(sm + kTSin + sw128_off(r, 32 * hf + 8 * q)) =
                     make_uint4(dxo[4 * q], dxo[4 * q + 1], dxo[4 * q + 2], dxo[4 * q + 3]);
-            warp_arrive(&sh.rdyS, lane);               // staged, and this chunk's TMEM is read
-            ptx::named_bar(kBarCompute, kCompute);     // sh.part, sh.F, sh.qv and sh.red complete
-            // ---- ddt of token t = r, dA and dD (column half 0 owns the token)
-            {
-                const float K = ((sh.red[0] + sh.red[1]) + (sh.red[2] + sh.red[3])) +
-                                ((sh.red[4] + sh.red[5]) + (sh.red[6] + sh.red[7]));
-                vx += sh.qv[0][r];
-                lbx += sh.qv[1][r];
-                scdy += sh.qv[2][r];
-                ddv += sh.qv[3][r];
-                // U_t = sum_{i >= t} 2^{p_i} scdy_i, V_t = sum_{j <= t} 2^{s_j} dt_j lbx_j,
-                // F_t = sum_{i >= t} F_i (the rows' totals of W over column half 0)
-                float u = ep_r * scdy, v = es_r * d * lbx, f = sh.F[r];
-#pragma unroll
-                for (int o = 1; o < 32; o <<= 1) {
-                    const float tu = __shfl_down_sync(0xffffffffu, u, o);
-                    const float tf = __shfl_down_sync(0xffffffffu, f, o);
-                    const float tv = __shfl_up_sync(0xffffffffu, v, o);
-                    if (lane + o < 32) {
-                        u += tu;
-                        f += tf;
-                    }
-                    if (lane >= o) v += tv;
-                }
-                if (hf == 0) {
-                    if (lane == 0) {   // the warp's totals
-                        sh.carry[0][rb] = u;
-                        sh.carry[2][rb] = f;
-                    }
-                    if (lane == 31) sh.carry[1][rb] = v;
-                }
-                ptx::named_bar(kBarCompute, kCompute);
-                for (int w = rb + 1; w < 4; ++w) {
-                    u += sh.carry[0][w];
-                    f += sh.carry[2][w];
-                }
-                for (int w = rb - 1; w >= 0; --w) v += sh.carry[1][w];
-                // corner sums: column half 0's transposed sums hold t < 64 in full; for
-                // t >= 64 half 1's, plus the first-half totals F_i of the rows i >= t
-                const float rv = ((sh.part[0][r] + sh.part[1][r]) + (sh.part[2][r] + sh.part[3][r])) +
-                                 (r >= 64 ? f : 0.f);
-                // (a document start's decay is not dt A: it is 0, and so is its gradient)
-                const float dl = start ? 0.f : rv + u + v + etau * K - d * vx;
-                if (hf == 0) {
-                    if (valid) a.ddt[((size_t)b * L + t0 + r) * a.H + h] = fmaf(Ah, dl, vx);
-                    dA_acc = fmaf(d, dl, dA_acc);
-                    dD_acc += ddv;
-                }
-            }
+            warp_arrive(&sh.rdyS, lane);   // staged, and this chunk's TMEM is read
+            prev = Tok{vx, lbx, scdy, ddv, es_r, ep_r, d, etau, t0, start, valid};
             if (ptx::named_bar_any(kBarCompute, kCompute, *(volatile int*)&sh.abort != 0)) break;
         }
+        if (nch > 0 && !*(volatile int*)&sh.abort) token_pass(prev, (nch - 1) & 1);
         // ---- the adjoint of the initial state; this unit's dA and dD shares
         if (a.dinit && !*(volatile int*)&sh.abort) {
-            // (the last update contraction completed: its commit was waited for)
+            wait_bar(sh, a, &sh.mmaLU, (nch - 1) & 1, kWhereDC);
             ptx::tc_fence_after();
             uint32_t l0[32];
             ptx::tmem_load32(lane_addr + kTmLU + 32 * hf, l0);
@@ -772,6 +796,11 @@ cudaError_t launch_bwd_tc(const BwdArgs& a, cudaStream_t st) {
         if ((e = cudaFuncSetAttribute(ssd_bwd_tc, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmemBytes)) !=
             cudaSuccess)
             return e;
+        // the warpgroup budgets must fit the registers the CTA is launched with
+        // (setmaxnreg.inc draws on that pool; a budget beyond it would wait forever)
+        cudaFuncAttributes fa;
+        if ((e = cudaFuncGetAttributes(&fa, ssd_bwd_tc)) != cudaSuccess) return e;
+        if (fa.numRegs * (kThreads / 128) < kRegsIssue + 2 * kRegsCompute) return cudaErrorInvalidConfiguration;
         ready[dev].store(1, std::memory_order_release);
     }
     ssd_bwd_tc<<<(unsigned)(a.batch * a.H), kThreads, kSmemBytes, st>>>(prm);
