@@ -476,7 +476,10 @@ struct Cursor {
 // for this kernel (its warps run several different loops at once).
 // kPersist: a persistent grid (one CTA per SM, each running several units),
 // used for short units, whose per-CTA start and pipeline ramp would dominate.
-template <bool kFull, bool kDocs, bool kPersist>
+// kEvents (with kFull and kDocs): the documents' initial or final states are
+// asked for, and the document events inside chunks are handled (their code
+// would otherwise cost registers in the plain packed-document kernel).
+template <bool kFull, bool kDocs, bool kPersist, bool kEvents = false>
 __global__ void __launch_bounds__(kThreads, 1) ssd_chunk_tc(const __grid_constant__ TcParams prm) {
     using Cursor = ssd::Cursor<kFull, kPersist>;
     extern __shared__ uint8_t smem_raw[];
@@ -689,7 +692,7 @@ __global__ void __launch_bounds__(kThreads, 1) ssd_chunk_tc(const __grid_constan
                     if (t + i + 1 == __ldg(a.cu + d + 1)) flag |= 2;
                     // the document's initial state, which the state group reads for this
                     // chunk, on its way to L2 a chunk ahead
-                    if (full_mode && (flag & 1) && a.init)
+                    if (kEvents && (flag & 1) && a.init)
                         ptx::bulk_prefetch_l2(a.init + ((size_t)d * a.H + h) * (P * N), P * N * 4);
                 } else if (t + i == a.L - 1) {
                     flag |= 2;
@@ -712,7 +715,7 @@ __global__ void __launch_bounds__(kThreads, 1) ssd_chunk_tc(const __grid_constan
             // packed documents with initial states: when one starts in this chunk, the
             // state group rewrites the chunk's Yoff rows, which the epilogue adds unscaled
             bool fix = false;
-            if (kDocs && full_mode)
+            if (kEvents)
                 fix = ptx::named_bar_any(nb, 128, (flag & 1) != 0) && a.init != nullptr;
             else
                 ptx::named_bar(nb, 128);
@@ -936,7 +939,7 @@ __global__ void __launch_bounds__(kThreads, 1) ssd_chunk_tc(const __grid_constan
             // ---- packed documents: final states of those that end inside this chunk,
             // and the state terms of the rows of those that start in it
             bool fix = false;
-            if (full_mode && kDocs && (a.fin || a.init)) {
+            if (kEvents) {
                 const int fl = m.rowflag[i];       // 0 past the chunk's last row
                 const float A2 = a.A[h] * kLog2e;
                 const bool end_row = i < nv - 1 && (fl & 2);
@@ -1017,7 +1020,7 @@ __global__ void __launch_bounds__(kThreads, 1) ssd_chunk_tc(const __grid_constan
                     ptx::f2_unpack(r1, S[32 + q], S[33 + q]);
                 }
             }
-            if (fix && sh.dlast >= 0) {
+            if (kEvents && fix && sh.dlast >= 0) {
                 // the initial state of the document open at the chunk's end, which started in it
                 const float ql = sh.qlast;
                 const float* src = a.init + ((size_t)sh.dlast * a.H + h) * PN + i;
@@ -1169,8 +1172,13 @@ cudaError_t launch_tc(const FwdArgs& a, cudaStream_t st) {
     const int nsm = device_sms();
     const bool persist = a.tail_units == 0 && (a.split_len + Q - 1) / Q <= kPersistChunks && nsm > 0 && grid > nsm;
     if (persist) grid = nsm;
+    // packed documents whose initial or final states are asked for: the kernel with
+    // the document events inside chunks
+    const bool events = full && docs && (a.init != nullptr || a.fin != nullptr);
     void (*kern)(TcParams);
-    if (persist)
+    if (events)
+        kern = persist ? ssd_chunk_tc<true, true, true, true> : ssd_chunk_tc<true, true, false, true>;
+    else if (persist)
         kern = full ? (docs ? ssd_chunk_tc<true, true, true> : ssd_chunk_tc<true, false, true>)
                     : (docs ? ssd_chunk_tc<false, true, true> : ssd_chunk_tc<false, false, true>);
     else
@@ -1179,12 +1187,12 @@ cudaError_t launch_tc(const FwdArgs& a, cudaStream_t st) {
     // once per device and variant: the shared-memory opt-in, and the check that the
     // warpgroup register budgets fit the registers the CTA is launched with
     // (setmaxnreg.inc draws on that pool; a budget beyond it would wait forever)
-    static std::atomic<uint8_t> ready[kMaxDevices][8];
+    static std::atomic<uint8_t> ready[kMaxDevices][16];
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess) return e;
     if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
-    std::atomic<uint8_t>& rd = ready[dev][(full ? 4 : 0) | (docs ? 2 : 0) | (persist ? 1 : 0)];
+    std::atomic<uint8_t>& rd = ready[dev][(events ? 8 : 0) | (full ? 4 : 0) | (docs ? 2 : 0) | (persist ? 1 : 0)];
     if (!rd.load(std::memory_order_acquire)) {
         if ((e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem)) != cudaSuccess)
             return e;
