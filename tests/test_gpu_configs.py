@@ -53,3 +53,11 @@ def test_config_varlen_stress():
     p = synth.config_varlen()
     y_o, f_o = oracle.ssd_recurrence(p)
     _check(p, y_o, f_o)
+
+
+def test_config_varlen_with_states():
+    """C5's packed row with every document's own initial state and every final
+    state asked for (the document-event kernel, 37 starts and ends per head)."""
+    p = synth.config_varlen(init_std=0.2)
+    y_o, f_o = oracle.ssd_recurrence(p)
+    _check(p, y_o, f_o)
