@@ -20,11 +20,17 @@
 namespace ssd {
 namespace {
 
-constexpr int kNormVecs = 4;   // 16-byte vectors of y (and of z) per thread
+constexpr int kNormVecs = 2;   // 16-byte vectors of y (and of z) per thread
 // group_size <= 8192: at most 1024 bf16 or 2048 fp32 vectors, so at most
-// 256 (bf16) or 512 (fp32) threads
+// 512 (bf16) or 1024 (fp32) threads
 template <typename T>
-constexpr int kNormMaxThreads = sizeof(T) == 2 ? 256 : 512;
+constexpr int kNormMaxThreads = sizeof(T) == 2 ? 512 : 1024;
+// CTAs per SM the bf16 kernel is compiled for: registers for 4 CTAs of 512
+// threads keep enough rows' loads in flight (2 vectors per thread and more
+// threads measured 84.6 us against 99.3 us for 4 vectors per thread at the
+// 2.7B-like layer's output; the loads' latency, not issue, is the bound)
+template <typename T>
+constexpr int kNormMinBlocks = sizeof(T) == 2 ? 4 : 1;
 
 // y silu(z) = y z / (1 + e^{-z}), with e^{-z} = 2^{-z log2 e} and the reciprocal
 // taken by the special-function unit (ex2.approx, rcp.approx: relative errors of a
@@ -75,7 +81,7 @@ struct Vec<__nv_bfloat16> {
 };
 
 template <typename T>
-__global__ void __launch_bounds__(kNormMaxThreads<T>) ssd_gate_norm_kernel(GateNormArgs a) {
+__global__ void __launch_bounds__(kNormMaxThreads<T>, kNormMinBlocks<T>) ssd_gate_norm_kernel(GateNormArgs a) {
     __shared__ float part[kNormMaxThreads<T> / 32];
     constexpr int V = Vec<T>::n;
     const int gs = a.group_size, nvec = gs / V;
