@@ -12,7 +12,8 @@
 //     G = C B^T, X = dy x^T              A1 = L o G, A2 = L o X (bf16 tiles)
 //     V1 = A1^T dy, V2 = B Lam^T         v_j = V1_j + 2^{s_j} V2_j
 //     SC = C S_in^T                      dx_j = dt_j v_j + D dy_j
-//     dB_j = dt_j [A2^T C + (2^s o x) Lam^T]_j        (one accumulator)
+//     dB_j = dt_j [A2^T C + (2^s o x) Lam^T]_j        (one accumulator, dt_j
+//                                                      folded into both operands)
 //     dC_i = [(A2 o dt) B + (2^p o dy) S_in^T]_i       (one accumulator)
 //     Lam^T <- 2^tau Lam^T + C^T (2^p o dy)           (in TMEM)
 //   and the per-token terms of ddt from row sums of those products and of
@@ -56,8 +57,8 @@ constexpr uint32_t kTB = 32768;       // B (row j, n in two 64-column slabs)
 constexpr uint32_t kTC = 65536;       // C
 constexpr uint32_t kTLam = 98304;     // Lam as (row n, p) bf16
 constexpr uint32_t kTSin = 114688;    // S_in as (row n, p) bf16; then dx, staged for its store
-constexpr uint32_t kT1 = 131072;      // A1 (row i, column j); then A2 o dt; then the dC share
-constexpr uint32_t kT2 = 163840;      // A2; then the dB share
+constexpr uint32_t kT1 = 131072;      // A1 (row i, column j); then the dB share
+constexpr uint32_t kT2 = 163840;      // A2 o dt (row i, column j); then the dC share
 constexpr uint32_t kTiles = 196608;
 // Phase 1 keeps two stages of (x, B): chunk c uses stage c & 1, stage 1's x in the
 // S_in tile and its B in the A1 tile, so each load runs two chunks ahead.
@@ -79,8 +80,8 @@ struct BwdTcSmall {
     float red[16];
     float carry[3][4];      // warp totals of the token scans
     uint64_t full, full1, mmaF, mma1, mma2, mmaV1, mmaDB, mmaDC, mmaLU, drain;   // loads and MMAs complete
-    uint64_t rdyF, rdyA, rdyB, rdyC, rdyS;                          // compute warps -> issuer
-    uint64_t stFree;                                                // the stores have read their tiles
+    uint64_t rdyF, rdyA, rdyB, rdyC, rdyDB, rdyS;                   // compute warps -> issuer
+    uint64_t stFreeS, stFreeT;   // the stores have read the S_in tile (dx), and the A1 / A2 tiles
     uint32_t tmem_base;
     int abort;
     int never;
@@ -215,8 +216,10 @@ __global__ void __launch_bounds__(kThreads, 1) ssd_bwd_tc(const __grid_constant_
         ptx::mbar_init(&sh.rdyA, 8);
         ptx::mbar_init(&sh.rdyB, 8);
         ptx::mbar_init(&sh.rdyC, 8);
+        ptx::mbar_init(&sh.rdyDB, 8);
         ptx::mbar_init(&sh.rdyS, 8);
-        ptx::mbar_init(&sh.stFree, 1);
+        ptx::mbar_init(&sh.stFreeS, 1);
+        ptx::mbar_init(&sh.stFreeT, 1);
         sh.abort = 0;
         sh.never = 0;
         ptx::mbar_fence_init();
@@ -310,6 +313,13 @@ __global__ void __launch_bounds__(kThreads, 1) ssd_bwd_tc(const __grid_constant_
                 for (int kk = 0; kk < 4; ++kk)
                     ptx::mma_ss(tb + kTmX, desc_k1(s0 + kTDY, kk), desc_k1(s0 + kTX, kk), idQQ, kk > 0);
                 ptx::mma_commit(&sh.mma1);
+                // the last chunk's stores (dB; dx | dC) have read their tiles
+                if (k > 0) {
+                    ptx::bulk_wait_read1();
+                    ptx::mbar_arrive(&sh.stFreeS);
+                    ptx::bulk_wait_read0();
+                    ptx::mbar_arrive(&sh.stFreeT);
+                }
                 // B Lam^T and C S_in^T, once the Lam and S_in tiles are written
                 if (!wait_bar(sh, a, &sh.rdyA, k & 1, kWhereReady)) break;
                 ptx::tc_fence_after();
@@ -320,7 +330,7 @@ __global__ void __launch_bounds__(kThreads, 1) ssd_bwd_tc(const __grid_constant_
                 for (int kk = 0; kk < 8; ++kk)
                     ptx::mma_ss(tb + kTmSC, desc_k2(s0 + kTC, kk), desc_mn1(s0 + kTSin, kk), idQP, kk > 0);
                 ptx::mma_commit(&sh.mma2);
-                // (L o G)^T dy; dB~ = A2^T C + (2^s o x) Lam^T
+                // (L o G)^T dy; dB = (A2 o dt)^T C + (2^s o dt o x) Lam^T
                 if (!wait_bar(sh, a, &sh.rdyB, k & 1, kWhereReady)) break;
                 ptx::tc_fence_after();
                 {
@@ -348,7 +358,7 @@ __global__ void __launch_bounds__(kThreads, 1) ssd_bwd_tc(const __grid_constant_
                     constexpr uint32_t idL = ptx::idesc_bf16(128, 64, 1, 1);
 #pragma unroll 1
                     for (int kk = 0; kk < 8; ++kk)
-                        ptx::mma_ss(tb + kTmX, desc_k2(s0 + kT1, kk), desc_mn2(s0 + kTB, kk), idC1, kk > 0);
+                        ptx::mma_ss(tb + kTmX, desc_k2(s0 + kT2, kk), desc_mn2(s0 + kTB, kk), idC1, kk > 0);
 #pragma unroll 1
                     for (int kk = 0; kk < 4; ++kk)
                         ptx::mma_ss(tb + kTmX, desc_k1(s0 + kTDY, kk), desc_k1(s0 + kTSin, kk), idC2, 1);
@@ -361,16 +371,18 @@ __global__ void __launch_bounds__(kThreads, 1) ssd_bwd_tc(const __grid_constant_
                 // every contraction of the chunk is done: its tiles take the next chunk's loads
                 if (!wait_bar(sh, a, &sh.mmaLU, k & 1, kWhereDC)) break;
                 if (c > 0) load2(c - 1);
-                // the shares and dx staged: their stores (rows past the end are clipped)
+                // the staged dB share, then dx and the dC share: their stores (rows past
+                // the end are clipped), in three groups
+                if (!wait_bar(sh, a, &sh.rdyDB, k & 1, kWhereStores)) break;
+                ptx::tma_store_4d(&prm.tm_dB, sm + kT1, 0, h, t0, b);
+                ptx::tma_store_4d(&prm.tm_dB, sm + kT1 + 16384, 64, h, t0, b);
+                ptx::bulk_commit();
                 if (!wait_bar(sh, a, &sh.rdyS, (k + 1) & 1, kWhereStores)) break;
-                ptx::tma_store_4d(&prm.tm_dB, sm + kT2, 0, h, t0, b);
-                ptx::tma_store_4d(&prm.tm_dB, sm + kT2 + 16384, 64, h, t0, b);
-                ptx::tma_store_4d(&prm.tm_dC, sm + kT1, 0, h, t0, b);
-                ptx::tma_store_4d(&prm.tm_dC, sm + kT1 + 16384, 64, h, t0, b);
                 ptx::tma_store_4d(&prm.tm_dx, sm + kTSin, 0, h, t0, b);
                 ptx::bulk_commit();
-                ptx::bulk_wait_read0();
-                ptx::mbar_arrive(&sh.stFree);
+                ptx::tma_store_4d(&prm.tm_dC, sm + kT2, 0, h, t0, b);
+                ptx::tma_store_4d(&prm.tm_dC, sm + kT2 + 16384, 64, h, t0, b);
+                ptx::bulk_commit();
             }
             // drain: every MMA issued has completed, the last load issued has landed,
             // and the stores are complete
@@ -530,11 +542,19 @@ __global__ void __launch_bounds__(kThreads, 1) ssd_bwd_tc(const __grid_constant_
             ptx::named_bar(kBarCompute, kCompute);
             segsum_lin_phase2<4>(sh.seg, row, rb, lane, hf == 0);
             ptx::named_bar(kBarCompute, kCompute);
+            // the state entering the chunk (row n = r, this half's p; written by this
+            // thread in phase 1), loaded while the last chunk's stores read their tiles
+            float sv[32];
+            {
+                const float* src = ckpt + (size_t)c * PN + (size_t)(32 * hf) * N + r;
+#pragma unroll
+                for (int p = 0; p < 32; ++p) sv[p] = src[(size_t)p * N];
+            }
             const float es_r = segsum_lin_suffix<4>(sh.seg, r);
             const float ep_r = row.pe;
             const float etau = sh.seg.tauL;
-            // the last chunk's stores have read S_in, A1 and A2
-            if (k > 0) wait_bar(sh, a, &sh.stFree, (k - 1) & 1, kWhereStores);
+            // the last chunk's dx store has read the S_in tile
+            if (k > 0) wait_bar(sh, a, &sh.stFreeS, (k - 1) & 1, kWhereStores);
             // S_in and Lam as bf16 (row n = r, this half's p) operands; <Lam, S_in>;
             // Lam^T <- 2^tau Lam^T in TMEM, once the last update contraction is done
             if (k > 0) {
@@ -543,10 +563,6 @@ __global__ void __launch_bounds__(kThreads, 1) ssd_bwd_tc(const __grid_constant_
             }
             float kdot = 0.f;
             {
-                const float* src = ckpt + (size_t)c * PN + (size_t)(32 * hf) * N + r;
-                float sv[32];
-#pragma unroll
-                for (int p = 0; p < 32; ++p) sv[p] = src[(size_t)p * N];
                 uint32_t lv[32];
                 ptx::tmem_load32(lane_addr + kTmLU + 32 * hf, lv);
 #pragma unroll
@@ -591,10 +607,12 @@ __global__ void __launch_bounds__(kThreads, 1) ssd_bwd_tc(const __grid_constant_
             }
             wait_bar(sh, a, &sh.mma1, k & 1, kWhereMma1);
             ptx::tc_fence_after();
-            // ---- this half's columns of A1 = L o G and A2 = L o X (bf16 tiles) and the
-            // corner sums of W.  Column block cb of 32: L_rj = rf[cb] colL[j] below the
-            // diagonal block (rank-one), wl[j - 32 cb] in it, 0 above it.  Half 1's row
-            // prefixes start at 0; the token pass adds half 0's row totals.
+            // the last chunk's share stores have read the A1 and A2 tiles
+            if (k > 0) wait_bar(sh, a, &sh.stFreeT, (k - 1) & 1, kWhereStores);
+            // ---- this half's columns of A1 = L o G and A2 o dt = L o X o dt (bf16 tiles)
+            // and the corner sums of W.  Column block cb of 32: L_rj = rf[cb] colL[j]
+            // below the diagonal block (rank-one), wl[j - 32 cb] in it, 0 above it.
+            // Half 1's row prefixes start at 0; the token pass adds half 0's row totals.
             {
                 float zrun = 0.f;
 #pragma unroll 1
@@ -615,7 +633,7 @@ __global__ void __launch_bounds__(kThreads, 1) ssd_bwd_tc(const __grid_constant_
                             const float l1 = below ? rfc * sh.seg.colL[j0 + cc + 1] : diag ? row.wl[kx + 1] : 0.f;
                             const float x0 = __uint_as_float(xr[kx]), x1 = __uint_as_float(xr[kx + 1]);
                             p1[cc / 2] = pack_bf16(l0 * __uint_as_float(gr[kx]), l1 * __uint_as_float(gr[kx + 1]));
-                            p2[cc / 2] = pack_bf16(l0 * x0, l1 * x1);
+                            p2[cc / 2] = pack_bf16(l0 * x0 * sh.dts[j0 + cc], l1 * x1 * sh.dts[j0 + cc + 1]);
                             // W from the bf16 A1 that V1 contracts: the token's own term of
                             // <Lam_t, S_t> and of dt_t x_t . v_t then cancel in dl_t
                             zrun += bf16lo(p1[cc / 2]) * sh.dts[j0 + cc] * x0;
@@ -636,65 +654,53 @@ __global__ void __launch_bounds__(kThreads, 1) ssd_bwd_tc(const __grid_constant_
                 }
                 if (hf == 0) sh.F[k & 1][r] = zrun;
             }
-            // x row j = r, this half's p, becomes 2^{s_j} x_j (the X contraction is done)
+            // x row j = r, this half's p, becomes 2^{s_j} dt_j x_j (the X contraction is done)
+            const float xs = es_r * d;
 #pragma unroll
             for (int q = 0; q < 4; ++q)
-                *reinterpret_cast<uint4*>(sm + kTX + sw128_off(r, 32 * hf + 8 * q)) = scale_bf16x8(xv[q], es_r);
+                *reinterpret_cast<uint4*>(sm + kTX + sw128_off(r, 32 * hf + 8 * q)) = scale_bf16x8(xv[q], xs);
             warp_arrive(&sh.rdyB, lane);
-            wait_bar(sh, a, &sh.mmaV1, k & 1, kWhereV1);
-            ptx::tc_fence_after();
-            // ---- this half's columns of A2 o dt (from X, still in TMEM) over A1; dy row
-            // i = r, this half's p, becomes 2^{p_i} dy_i
-#pragma unroll 1
-            for (int cb = 2 * hf; cb < 2 * hf + 2; ++cb) {
-                const float rfc = (cb == 0) ? row.rf[0] : (cb == 1) ? row.rf[1] : row.rf[2];
-                const bool below = cb < rb, diag = cb == rb;
-                uint32_t xr[32];
-                ptx::tmem_load32(lane_addr + kTmX + 32 * cb, xr);
-#pragma unroll
-                for (int q16 = 0; q16 < 2; ++q16) {
-                    const int j0 = 32 * cb + 16 * q16;
-                    uint32_t p1[8];
-#pragma unroll
-                    for (int cc = 0; cc < 16; cc += 2) {
-                        const int kx = 16 * q16 + cc;
-                        const float l0 = below ? rfc * sh.seg.colL[j0 + cc] : diag ? row.wl[kx] : 0.f;
-                        const float l1 = below ? rfc * sh.seg.colL[j0 + cc + 1] : diag ? row.wl[kx + 1] : 0.f;
-                        p1[cc / 2] = pack_bf16(l0 * __uint_as_float(xr[kx]) * sh.dts[j0 + cc],
-                                               l1 * __uint_as_float(xr[kx + 1]) * sh.dts[j0 + cc + 1]);
-                    }
-#pragma unroll
-                    for (int q = 0; q < 2; ++q)
-                        *reinterpret_cast<uint4*>(sm + kT1 + off2(r, j0 + 8 * q)) =
-                            make_uint4(p1[4 * q], p1[4 * q + 1], p1[4 * q + 2], p1[4 * q + 3]);
-                }
-            }
-#pragma unroll
-            for (int q = 0; q < 4; ++q)
-                *reinterpret_cast<uint4*>(sm + kTDY + sw128_off(r, 32 * hf + 8 * q)) = scale_bf16x8(dv[q], ep_r);
-            warp_arrive(&sh.rdyC, lane);
-            // ---- dx (this half's p) and the per-token partial products (row j = r)
+            // ---- the per-token partial products V1 does not enter (row j = r), while V1
+            // runs: <(B Lam^T)_j, x_j>, <(C S_in^T)_j, dy_j> and <dy_j, x_j>
             float vx = 0.f, lbx = 0.f, scdy = 0.f, ddv = 0.f;
-            uint32_t dxo[16];
+            uint32_t v2[32];
             wait_bar(sh, a, &sh.mma2, k & 1, kWhereMma1);
             ptx::tc_fence_after();
             {
-                uint32_t v1[32], v2[32], sc[32];
-                ptx::tmem_load32x2(lane_addr + kTmV1 + 32 * hf, v1, lane_addr + kTmV2 + 32 * hf, v2);
-                ptx::tmem_load32(lane_addr + kTmSC + 32 * hf, sc);
+                uint32_t sc[32];
+                ptx::tmem_load32x2(lane_addr + kTmV2 + 32 * hf, v2, lane_addr + kTmSC + 32 * hf, sc);
 #pragma unroll
                 for (int kx = 0; kx < 32; kx += 2) {
                     const int q = kx >> 3, e = kx & 7;
                     const uint32_t xw = e == 0 ? xv[q].x : e == 2 ? xv[q].y : e == 4 ? xv[q].z : xv[q].w;
                     const uint32_t dw = e == 0 ? dv[q].x : e == 2 ? dv[q].y : e == 4 ? dv[q].z : dv[q].w;
                     const float x0 = bf16lo(xw), x1 = bf16hi(xw), y0 = bf16lo(dw), y1 = bf16hi(dw);
-                    const float w0 = __uint_as_float(v2[kx]), w1 = __uint_as_float(v2[kx + 1]);
-                    const float v0 = fmaf(es_r, w0, __uint_as_float(v1[kx]));
-                    const float v1v = fmaf(es_r, w1, __uint_as_float(v1[kx + 1]));
-                    vx = fmaf(v0, x0, fmaf(v1v, x1, vx));
-                    lbx = fmaf(w0, x0, fmaf(w1, x1, lbx));
+                    lbx = fmaf(__uint_as_float(v2[kx]), x0, fmaf(__uint_as_float(v2[kx + 1]), x1, lbx));
                     scdy = fmaf(__uint_as_float(sc[kx]), y0, fmaf(__uint_as_float(sc[kx + 1]), y1, scdy));
                     ddv = fmaf(y0, x0, fmaf(y1, x1, ddv));
+                }
+            }
+            wait_bar(sh, a, &sh.mmaV1, k & 1, kWhereV1);
+            ptx::tc_fence_after();
+            // ---- dy row i = r, this half's p, becomes 2^{p_i} dy_i (V1 has read dy)
+#pragma unroll
+            for (int q = 0; q < 4; ++q)
+                *reinterpret_cast<uint4*>(sm + kTDY + sw128_off(r, 32 * hf + 8 * q)) = scale_bf16x8(dv[q], ep_r);
+            warp_arrive(&sh.rdyC, lane);
+            // ---- dx (this half's p) and <v_j, x_j>, v_j = V1_j + 2^{s_j} V2_j
+            uint32_t dxo[16];
+            {
+                uint32_t v1[32];
+                ptx::tmem_load32(lane_addr + kTmV1 + 32 * hf, v1);
+#pragma unroll
+                for (int kx = 0; kx < 32; kx += 2) {
+                    const int q = kx >> 3, e = kx & 7;
+                    const uint32_t xw = e == 0 ? xv[q].x : e == 2 ? xv[q].y : e == 4 ? xv[q].z : xv[q].w;
+                    const uint32_t dw = e == 0 ? dv[q].x : e == 2 ? dv[q].y : e == 4 ? dv[q].z : dv[q].w;
+                    const float x0 = bf16lo(xw), x1 = bf16hi(xw), y0 = bf16lo(dw), y1 = bf16hi(dw);
+                    const float v0 = fmaf(es_r, __uint_as_float(v2[kx]), __uint_as_float(v1[kx]));
+                    const float v1v = fmaf(es_r, __uint_as_float(v2[kx + 1]), __uint_as_float(v1[kx + 1]));
+                    vx = fmaf(v0, x0, fmaf(v1v, x1, vx));
                     dxo[kx / 2] = pack_bf16(fmaf(d, v0, Dh * y0), fmaf(d, v1v, Dh * y1));
                 }
             }
@@ -705,7 +711,7 @@ __global__ void __launch_bounds__(kThreads, 1) ssd_bwd_tc(const __grid_constant_
                 sh.qv[k & 1][3][r] = ddv;
             }
             // ---- this head's share of dB (row j = r, this half's columns) as bf16 over
-            // A2, which the dB contraction has finished reading
+            // A1, which V1 has finished reading
             wait_bar(sh, a, &sh.mmaDB, k & 1, kWhereDB);
             ptx::tc_fence_after();
 #pragma unroll 1
@@ -714,12 +720,13 @@ __global__ void __launch_bounds__(kThreads, 1) ssd_bwd_tc(const __grid_constant_
                 ptx::tmem_load32(lane_addr + kTmG + 32 * cb, v);
 #pragma unroll
                 for (int q = 0; q < 4; ++q)
-                    *reinterpret_cast<uint4*>(sm + kT2 + off2(r, 32 * cb + 8 * q)) = make_uint4(
-                        pack_bf16(d * __uint_as_float(v[8 * q]), d * __uint_as_float(v[8 * q + 1])),
-                        pack_bf16(d * __uint_as_float(v[8 * q + 2]), d * __uint_as_float(v[8 * q + 3])),
-                        pack_bf16(d * __uint_as_float(v[8 * q + 4]), d * __uint_as_float(v[8 * q + 5])),
-                        pack_bf16(d * __uint_as_float(v[8 * q + 6]), d * __uint_as_float(v[8 * q + 7])));
+                    *reinterpret_cast<uint4*>(sm + kT1 + off2(r, 32 * cb + 8 * q)) = make_uint4(
+                        pack_bf16(__uint_as_float(v[8 * q]), __uint_as_float(v[8 * q + 1])),
+                        pack_bf16(__uint_as_float(v[8 * q + 2]), __uint_as_float(v[8 * q + 3])),
+                        pack_bf16(__uint_as_float(v[8 * q + 4]), __uint_as_float(v[8 * q + 5])),
+                        pack_bf16(__uint_as_float(v[8 * q + 6]), __uint_as_float(v[8 * q + 7])));
             }
+            warp_arrive(&sh.rdyDB, lane);   // staged
             // ---- dC (row i = r, this half's columns) as bf16 over A2 o dt, dx over S_in,
             // once the dC and Lam contractions are done
             wait_bar(sh, a, &sh.mmaDC, k & 1, kWhereDC);
@@ -730,7 +737,7 @@ __global__ void __launch_bounds__(kThreads, 1) ssd_bwd_tc(const __grid_constant_
                 ptx::tmem_load32(lane_addr + kTmX + 32 * cb, v);
 #pragma unroll
                 for (int q = 0; q < 4; ++q)
-                    *reinterpret_cast<uint4*>(sm + kT1 + off2(r, 32 * cb + 8 * q)) = make_uint4(
+                    *reinterpret_cast<uint4*>(sm + kT2 + off2(r, 32 * cb + 8 * q)) = make_uint4(
                         pack_bf16(__uint_as_float(v[8 * q]), __uint_as_float(v[8 * q + 1])),
                         pack_bf16(__uint_as_float(v[8 * q + 2]), __uint_as_float(v[8 * q + 3])),
                         pack_bf16(__uint_as_float(v[8 * q + 4]), __uint_as_float(v[8 * q + 5])),

@@ -109,6 +109,10 @@ __device__ __forceinline__ void bulk_commit() { asm volatile("cp.async.bulk.comm
 __device__ __forceinline__ void bulk_wait_read0() {
     asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");
 }
+// every committed bulk group but the most recent one has read its shared memory
+__device__ __forceinline__ void bulk_wait_read1() {
+    asm volatile("cp.async.bulk.wait_group.read 1;" ::: "memory");
+}
 __device__ __forceinline__ void bulk_wait0() { asm volatile("cp.async.bulk.wait_group 0;" ::: "memory"); }
 // bulk prefetch of [p, p + bytes) from global memory into L2 (16-byte aligned, bytes a multiple of 16)
 __device__ __forceinline__ void bulk_prefetch_l2(const void* p, uint32_t bytes) {
