@@ -141,9 +141,8 @@ SSD_API int ssd_fwd_timed(const ssd_params_t* p,
  * caller still passes all inputs and outputs.
  * The first call on a device looks up the array's device address with that
  * device current (cudaGetSymbolAddress) and keeps it for the life of the
- * process; make that first call before any stream capture, and make no call
- * after resetting the device (cudaDeviceReset), which invalidates the kept
- * address.  Every call uses the same array: calls whose GPU work
+ * process; make no call after resetting the device (cudaDeviceReset), which
+ * invalidates the kept address.  Every call uses the same array: calls whose GPU work
  * overlaps (other streams or other host threads) race on it.  The call
  * clears the status word, enqueues the work on `stream`, then synchronises
  * the stream and returns the device status (SSD_OK or the first device
