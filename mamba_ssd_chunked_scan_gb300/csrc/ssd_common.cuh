@@ -43,7 +43,7 @@ struct SplitPlan {
 // Offsets (in bytes) of the split buffers inside the workspace.
 struct WsLayout {
     size_t tau_off;     // float   [batch * H * nsplit]
-    size_t state_off;   // float   [batch * H * nsplit * P * N]  aggregates, then incoming states
+    size_t state_off;   // float   [batch * H * nsplit * P * N]  aggregates, then incoming states (slot s - 1: split s)
     size_t total;
 };
 

@@ -37,7 +37,8 @@ struct FwdArgs {
     void* y;
     float* fin;
     float* ws_tau;         // [batch * H * nsplit] natural-log split decays
-    float* ws_state;       // [batch * H * nsplit * P * N] split states
+    float* ws_state;       // [batch * H * nsplit * P * N] split aggregates (slot s); after the
+                           // scan, slot s - 1 holds the state entering split s
     WsHeader* ws;
     // n / H, n / nsplit and n / (H / G) for 0 <= n < 2^31 as (mulhi(m, n) + n) >> l
     uint32_t divH_m, divH_l, divS_m, divS_l, divHG_m, divHG_l;

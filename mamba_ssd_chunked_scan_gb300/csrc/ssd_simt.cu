@@ -85,9 +85,9 @@ __global__ void __launch_bounds__(256) ssd_chunk_simt(FwdArgs a) {
     T* y = (T*)a.y;
     const size_t PN = (size_t)P * N;
 
-    // incoming state: from the split scan when this split continues a document
+    // incoming state: from the split scan (slot s - 1) when this split continues a document
     for (int k = tid; k < P * N; k += nt)
-        S[k] = (a.mode == kModeFull && a.nsplit > 1 && s > 0) ? a.ws_state[u * PN + k] : 0.f;
+        S[k] = (a.mode == kModeFull && a.nsplit > 1 && s > 0) ? a.ws_state[(u - 1) * PN + k] : 0.f;
     float tau = 0.f;  // natural-log decay applied to the split's incoming state
 
     for (int64_t c0 = t0; c0 < t1; c0 += Q) {
@@ -238,51 +238,55 @@ __global__ void __launch_bounds__(256) ssd_chunk_simt(FwdArgs a) {
 
 // Composition of split aggregates, left to right per (row, head):
 // (tau_1, S_1) then (tau_2, S_2) -> (tau_1 + tau_2, exp(tau_2) S_1 + S_2).
-// In place: slot s receives the state entering split s.
-// Exclusive scan over the splits of one (row, head): the incoming state of
-// split s is the composition of the aggregates of splits 0..s-1 (affine steps
-// S -> exp(tau_s) S + agg_s).  One thread owns 4 consecutive state elements;
-// the loads of the next kDepth splits are issued before the current ones are
-// combined, so the sequential chain waits on arithmetic, not on memory.
+// Slot s of a (row, head) holds the aggregate of split s (splits 0 .. nsplit-2;
+// split 0's includes the caller's initial state).  In place, slot s - 1
+// receives the state entering split s: slot 0 already is that of split 1, and
+// S_in(s + 1) = exp(tau_s) S_in(s) + agg_s goes over agg_s in slot s.  So the
+// scan reads nsplit - 1 slots and writes nsplit - 2 (nothing with two splits),
+// and no slot holds the zero state of split 0 or the unneeded aggregate of
+// the last split.  One thread owns 4 consecutive state elements; the loads of
+// the next kScanDepth slots are issued before the current ones are combined,
+// so the sequential chain waits on arithmetic, not on memory.
 constexpr int kScanDepth = 8;
 
 __global__ void ssd_split_scan(const float* __restrict__ tau, float* __restrict__ state,
                                int64_t units_bh, int nsplit, int PN) {
     const int PN4 = PN >> 2;
+    const int nagg = nsplit - 1;   // slots holding aggregates
     const int64_t k = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
-    if (k >= units_bh * PN4) return;
+    if (nagg < 2 || k >= units_bh * PN4) return;
     const int64_t bh = k / PN4;
     const int e4 = (int)(k % PN4);
     float4* st = reinterpret_cast<float4*>(state) + bh * nsplit * (int64_t)PN4 + e4;
     const float* tu = tau + bh * nsplit;
+    float4 run = st[0];   // S_in(1)
     float4 cur[kScanDepth];
     float ct[kScanDepth];
 #pragma unroll
     for (int d = 0; d < kScanDepth; ++d) {
-        if (d < nsplit) {
-            cur[d] = st[(int64_t)d * PN4];
-            ct[d] = tu[d];
+        if (1 + d < nagg) {
+            cur[d] = st[(int64_t)(1 + d) * PN4];
+            ct[d] = tu[1 + d];
         }
     }
-    float4 run = make_float4(0.f, 0.f, 0.f, 0.f);
-    for (int s0 = 0; s0 < nsplit; s0 += kScanDepth) {
+    for (int s0 = 1; s0 < nagg; s0 += kScanDepth) {
         float4 nxt[kScanDepth];
         float nt[kScanDepth];
 #pragma unroll
         for (int d = 0; d < kScanDepth; ++d) {
             const int sn = s0 + kScanDepth + d;
-            if (sn < nsplit) {
+            if (sn < nagg) {
                 nxt[d] = st[(int64_t)sn * PN4];
                 nt[d] = tu[sn];
             }
         }
 #pragma unroll
         for (int d = 0; d < kScanDepth; ++d) {
-            if (s0 + d < nsplit) {
-                st[(int64_t)(s0 + d) * PN4] = run;
+            if (s0 + d < nagg) {
                 const float e = expf(ct[d]);
                 run = make_float4(fmaf(e, run.x, cur[d].x), fmaf(e, run.y, cur[d].y), fmaf(e, run.z, cur[d].z),
                                   fmaf(e, run.w, cur[d].w));
+                st[(int64_t)(s0 + d) * PN4] = run;   // S_in(s0 + d + 1)
             }
         }
 #pragma unroll
@@ -356,7 +360,8 @@ cudaError_t launch_simt(const FwdArgs& a, cudaStream_t st) {
 
 cudaError_t launch_split_scan(const FwdArgs& a, cudaStream_t st) {
     const int PN = a.P * a.N;   // a multiple of 4: P * 4 bytes is a multiple of 16
-    const int64_t total = a.batch * a.H * (int64_t)(PN / 4);
+    // (with two splits there is nothing to compose: one block that returns at once)
+    const int64_t total = a.nsplit > 2 ? a.batch * a.H * (int64_t)(PN / 4) : 1;
     const int threads = 256;
     ssd_split_scan<<<(unsigned)((total + threads - 1) / threads), threads, 0, st>>>(
         a.ws_tau, a.ws_state, a.batch * a.H, a.nsplit, PN);

@@ -882,7 +882,7 @@ __global__ void __launch_bounds__(kThreads, 1) ssd_chunk_tc(const __grid_constan
         // caller's initial state, or zero
         auto enter_state = [&](const Unit& un) {
             const float* src = nullptr;
-            if (full_mode && a.nsplit > 1 && un.s > 0) src = a.ws_state + (size_t)un.ws * PN;
+            if (full_mode && a.nsplit > 1 && un.s > 0) src = a.ws_state + (size_t)(un.ws - 1) * PN;   // (slot s - 1)
             else if (un.s == 0 && a.init) src = a.init + ((size_t)un.b * a.H + un.h) * PN;   // (documents: d = 0 = b)
 #pragma unroll
             for (int p = 0; p < P; ++p) S[p] = src ? src[(size_t)p * N + i] : 0.f;
