@@ -157,6 +157,14 @@ SSD_API int ssd_fwd_static_scratch(const ssd_params_t* p,
  * parameters are invalid or the backward pass does not support them. */
 SSD_API size_t ssd_bwd_workspace_size(const ssd_params_t* p);
 
+/* Bytes of device workspace ssd_bwd() needs for packed documents (ndocs > 0)
+ * when the call passes initial_states, dfinal_states or dinitial_states: that
+ * call runs on CUDA cores with chunks of at most 32 tokens that start at every
+ * document start, so its layout is larger than ssd_bwd_workspace_size(p).
+ * 0 when the parameters are invalid, ndocs is 0 or the backward pass does not
+ * support them. */
+SSD_API size_t ssd_bwd_workspace_size_doc_states(const ssd_params_t* p);
+
 /* Backward pass of ssd_fwd(): the gradients of the scalar
  *     <dy, y> + <dfinal_states, final_states>
  * with respect to every input, where y and final_states are ssd_fwd()'s outputs
@@ -173,7 +181,9 @@ SSD_API size_t ssd_bwd_workspace_size(const ssd_params_t* p);
  *
  * Inputs: x, dt, A, B, C, D (optional), initial_states (optional: zeros) exactly
  * as for ssd_fwd(); dy (batch, seqlen, nheads, headdim) dtype;
- * dfinal_states (batch, nheads, headdim, dstate) fp32 or NULL (zeros).
+ * dfinal_states (batch, nheads, headdim, dstate) fp32 or NULL (zeros); with
+ * cu_seqlens, initial_states, dfinal_states and dinitial_states are per
+ * document, (ndocs, nheads, headdim, dstate).
  * Outputs (written, not accumulated into):
  *   dx               (batch, seqlen, nheads, headdim)   dtype
  *   ddt              (batch, seqlen, nheads)            fp32
@@ -182,14 +192,20 @@ SSD_API size_t ssd_bwd_workspace_size(const ssd_params_t* p);
  *   dD               (nheads) fp32, or NULL; written only when D is given
  *   dinitial_states  (batch, nheads, headdim, dstate)   fp32, or NULL
  * All pointers are device memory with 16-byte aligned bases; no output may equal
- * an input.  Packed documents (cu_seqlens with ndocs, batch 1) are supported
- * when every document starts from a zero state and carries no final-state
- * gradient: with cu_seqlens, a non-NULL initial_states, dfinal_states or
- * dinitial_states returns SSD_ERR_UNSUPPORTED.  So do headdim * dstate > 8192
- * and shapes whose tiles do not fit in shared memory.
+ * an input.  Packed documents (cu_seqlens with ndocs, batch 1; strictly
+ * increasing, from 0 to seqlen) are independent sequences: no state and no
+ * gradient crosses a document boundary.  Without per-document states they
+ * take the tensor-core path for its shape (a -inf log-decay at each document
+ * start); with initial_states, dfinal_states or dinitial_states they run on
+ * CUDA cores, whose chunks start at every document start: each document
+ * starts from its initial state (its first token's decay applied to it), its
+ * final state receives dfinal_states[d], and dinitial_states[d] is the
+ * gradient of initial_states[d].  headdim * dstate > 8192 and shapes whose
+ * tiles do not fit in shared memory return SSD_ERR_UNSUPPORTED.
  * `chunk` and `split_len` in p are validated but do not change the result.
- * `workspace`: at least ssd_bwd_workspace_size(p) bytes, 256-byte aligned
- * (else SSD_ERR_WORKSPACE).  Asynchronous on `stream`; a status-word reset
+ * `workspace`: at least ssd_bwd_workspace_size(p) bytes, or
+ * ssd_bwd_workspace_size_doc_states(p) for packed documents with any of the
+ * three states, 256-byte aligned (else SSD_ERR_WORKSPACE).  Asynchronous on `stream`; a status-word reset
  * and two launches.  The tensor-core path's device waits are bounded: one that
  * runs out records SSD_ERR_TIMEOUT (where codes 31-37) in the status word at
  * the start of `workspace`, read by ssd_check_status(); the CUDA-core path has

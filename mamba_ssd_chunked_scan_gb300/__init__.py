@@ -166,22 +166,23 @@ def ssd_fwd(x, dt, A, B, C, D=None, initial_states=None, cu_seqlens=None, *, chu
 def ssd_bwd(x, dt, A, B, C, dy, D=None, initial_states=None, dfinal_states=None, cu_seqlens=None, *,
             chunk=128, want_dinit=None, stream=None, check_status=False):
     """Gradients of <dy, y> + <dfinal_states, final_states> for one ssd_fwd
-    call's inputs.  Packed documents (cu_seqlens, batch 1) start from zero
-    states and take no dfinal_states.  Returns a dict with dx, ddt, dA, dB, dC,
-    dD (None without D) and dinit (by default for batch rows only).  With
-    check_status, also synchronises the stream and raises if a device-side
-    wait ran out (the workspace's status word)."""
+    call's inputs.  With packed documents (cu_seqlens, batch 1) the states
+    are per document: initial_states, dfinal_states and dinit are (ndocs, H,
+    P, N).  Returns a dict with dx, ddt, dA, dB, dC, dD (None without D) and
+    dinit (by default for batch rows, or for documents with initial_states).
+    With check_status, also synchronises the stream and raises if a
+    device-side wait ran out (the workspace's status word)."""
     batch, seqlen, nheads, headdim = x.shape
     ngroups, dstate = B.shape[2], B.shape[3]
     dev = x.device
     ndocs = 0 if cu_seqlens is None else cu_seqlens.numel() - 1
     if want_dinit is None:
-        want_dinit = cu_seqlens is None
+        want_dinit = cu_seqlens is None or initial_states is not None
     if cu_seqlens is not None and (cu_seqlens.dtype != torch.int32 or cu_seqlens.device != dev):
         raise ValueError("cu_seqlens: expected int32 (ndocs + 1) on the device")
     params = _lib.make_params(batch, seqlen, nheads, headdim, dstate, ngroups, chunk, 0, ndocs, _dtype_code(x))
     shp_x, shp_bc = (batch, seqlen, nheads, headdim), (batch, seqlen, ngroups, dstate)
-    shp_s = (batch, nheads, headdim, dstate)
+    shp_s = (batch if cu_seqlens is None else ndocs, nheads, headdim, dstate)
     for name, t, shp, dt_ in (("x", x, shp_x, x.dtype), ("dt", dt, shp_x[:3], torch.float32),
                               ("A", A, (nheads,), torch.float32), ("B", B, shp_bc, x.dtype),
                               ("C", C, shp_bc, x.dtype), ("dy", dy, shp_x, x.dtype),
@@ -193,7 +194,9 @@ def ssd_bwd(x, dt, A, B, C, dy, D=None, initial_states=None, dfinal_states=None,
         if tuple(t.shape) != shp or t.dtype != dt_ or not t.is_contiguous() or t.device != dev:
             raise ValueError(f"{name}: expected contiguous {dt_} {shp} on {dev}, got "
                              f"{t.dtype} {tuple(t.shape)} on {t.device}")
-    nbytes = int(_lib.lib.ssd_bwd_workspace_size(ctypes.byref(params)))
+    doc_states = cu_seqlens is not None and (initial_states is not None or dfinal_states is not None or want_dinit)
+    size_fn = _lib.lib.ssd_bwd_workspace_size_doc_states if doc_states else _lib.lib.ssd_bwd_workspace_size
+    nbytes = int(size_fn(ctypes.byref(params)))
     if nbytes == 0:
         raise _lib.SSDError(2, "ssd_bwd: unsupported parameters")
     ws = torch.empty(nbytes, dtype=torch.uint8, device=dev)

@@ -19,7 +19,7 @@ STATUS = {0: "SSD_OK", 1: "SSD_ERR_INVALID_ARG", 2: "SSD_ERR_UNSUPPORTED", 3: "S
 # every symbol include/ssd.h declares
 EXPORTS = ("ssd_fwd_workspace_size", "ssd_workspace_init", "ssd_fwd", "ssd_check_status",
            "ssd_status_string", "ssd_fwd_plan", "ssd_segsum_dump", "ssd_fwd_static_scratch", "ssd_step",
-           "ssd_bwd_workspace_size", "ssd_bwd", "ssd_fwd_timed",
+           "ssd_bwd_workspace_size", "ssd_bwd_workspace_size_doc_states", "ssd_bwd", "ssd_fwd_timed",
            "ssd_gate_norm", "ssd_check_status_where", "ssd_fwd_fault_inject")
 
 
@@ -66,6 +66,8 @@ def _load():
     lib.ssd_fwd_static_scratch.restype = ctypes.c_int
     lib.ssd_bwd_workspace_size.argtypes = [P]
     lib.ssd_bwd_workspace_size.restype = sz
+    lib.ssd_bwd_workspace_size_doc_states.argtypes = [P]
+    lib.ssd_bwd_workspace_size_doc_states.restype = sz
     lib.ssd_bwd.argtypes = [P] + [vp] * 18 + [sz, vp]
     lib.ssd_bwd.restype = ctypes.c_int
     lib.ssd_gate_norm.argtypes = [i64, i32, i32, i32, vp, vp, vp, ctypes.c_float, vp, vp]

@@ -173,26 +173,33 @@ WsLayout layout_for(const ssd_params_t* p, int ns, const TailPlan& tp) {
 // the per-head shares of dB and dC, and the per-row shares of dA and dD.
 struct BwdLayout {
     int Qb = 0;
-    size_t ckpt = 0, dB = 0, dC = 0, dA = 0, dD = 0, total = 0;
+    bool tc = false;
+    size_t ckpt = 0, cmap = 0, dB = 0, dC = 0, dA = 0, dD = 0, total = 0;
 };
 
-// The backward runs on the tensor cores for the bf16 Mamba-2 head shape.
-bool bwd_use_tc(const ssd_params_t* p) {
-    return bwd_tc_supported(p->headdim, p->dstate, p->dtype) && p->seqlen < ((int64_t)1 << 31) - 256;
+// The backward runs on the tensor cores for the bf16 Mamba-2 head shape, except
+// for packed documents with initial states or final-state gradients
+// (doc_states), which take the CUDA-core kernel's document-aligned chunks.
+bool bwd_use_tc(const ssd_params_t* p, bool doc_states) {
+    return !doc_states && bwd_tc_supported(p->headdim, p->dstate, p->dtype) &&
+           p->seqlen < ((int64_t)1 << 31) - 256;
 }
 
-bool bwd_layout(const ssd_params_t* p, BwdLayout* l) {
+bool bwd_layout(const ssd_params_t* p, bool doc_states, BwdLayout* l) {
     if (check_params(p) != SSD_OK) return false;
-    l->Qb = bwd_use_tc(p) ? kBwdTcChunk : bwd_chunk(p->headdim, p->dstate, kSmemLimit);
+    l->tc = bwd_use_tc(p, doc_states);
+    l->Qb = l->tc ? kBwdTcChunk : bwd_chunk(p->headdim, p->dstate, kSmemLimit);
     if (l->Qb == 0) return false;
     const size_t bh = (size_t)p->batch * p->nheads;
-    const size_t nch = (size_t)((p->seqlen + l->Qb - 1) / l->Qb);
+    // chunks per row: the CUDA-core kernel starts a chunk at every document start too
+    const size_t nch = (size_t)((p->seqlen + l->Qb - 1) / l->Qb) + (l->tc ? 0 : (size_t)p->ndocs);
     const size_t PN = (size_t)p->headdim * p->dstate;
     // per-head shares of dB and dC: bf16 from the tensor-core backward, else fp32
-    const size_t share_elem = bwd_use_tc(p) ? 2 : 4;
+    const size_t share_elem = l->tc ? 2 : 4;
     const size_t share = (size_t)p->batch * p->seqlen * p->nheads * p->dstate;
     size_t o = sizeof(WsHeader);
     l->ckpt = o;  o = align_up(o + bh * nch * PN * sizeof(float), 256);
+    l->cmap = o;  o = align_up(o + (l->tc ? 0 : bh * nch * 2 * sizeof(int)), 256);
     l->dB = o;    o = align_up(o + share * share_elem, 256);
     l->dC = o;    o = align_up(o + share * share_elem, 256);
     l->dA = o;    o = align_up(o + bh * sizeof(float), 256);
@@ -479,7 +486,12 @@ int ssd_fwd_static_scratch(const ssd_params_t* p, const void* x, const float* dt
 
 size_t ssd_bwd_workspace_size(const ssd_params_t* p) {
     BwdLayout l;
-    return bwd_layout(p, &l) ? l.total : 0;
+    return bwd_layout(p, false, &l) ? l.total : 0;
+}
+
+size_t ssd_bwd_workspace_size_doc_states(const ssd_params_t* p) {
+    BwdLayout l;
+    return p && p->ndocs > 0 && bwd_layout(p, true, &l) ? l.total : 0;
 }
 
 int ssd_bwd(const ssd_params_t* p, const void* x, const float* dt, const float* A, const void* B,
@@ -489,8 +501,9 @@ int ssd_bwd(const ssd_params_t* p, const void* x, const float* dt, const float* 
     int rc = check_params(p);
     if (rc != SSD_OK) return rc;
     if ((cu == nullptr) != (p->ndocs == 0)) return SSD_ERR_INVALID_ARG;
-    // packed documents: each starts from a zero state and has no final-state gradient
-    if (cu && (init || dfin || dinit)) return SSD_ERR_UNSUPPORTED;
+    // packed documents with initial states, final-state gradients or initial-state
+    // gradients: the CUDA-core kernel (its own, larger workspace layout)
+    const bool doc_states = cu && (init || dfin || dinit);
     if (cu && !aligned(cu, 4)) return SSD_ERR_INVALID_ARG;
     if (bwd_chunk(p->headdim, p->dstate, kSmemLimit) == 0) return SSD_ERR_UNSUPPORTED;
     if (p->batch * p->nheads >= ((int64_t)1 << 31)) return SSD_ERR_UNSUPPORTED;
@@ -505,7 +518,7 @@ int ssd_bwd(const ssd_params_t* p, const void* x, const float* dt, const float* 
             if (q && q == r) return SSD_ERR_INVALID_ARG;   // outputs never alias inputs
     }
     BwdLayout l;
-    if (!bwd_layout(p, &l)) return SSD_ERR_UNSUPPORTED;
+    if (!bwd_layout(p, doc_states, &l)) return SSD_ERR_UNSUPPORTED;
     if (!workspace || workspace_bytes < l.total || !aligned(workspace, 256)) return SSD_ERR_WORKSPACE;
     BwdArgs a;
     memset(&a, 0, sizeof(a));
@@ -518,16 +531,17 @@ int ssd_bwd(const ssd_params_t* p, const void* x, const float* dt, const float* 
     a.dx = dx; a.ddt = ddt; a.dA = dA; a.dB = dB; a.dC = dC; a.dD = D ? dD : nullptr; a.dinit = dinit;
     char* ws = static_cast<char*>(workspace);
     a.ws_ckpt = (float*)(ws + l.ckpt);
+    a.ws_cmap = (int*)(ws + l.cmap);
     a.ws_dB = (float*)(ws + l.dB);
     a.ws_dC = (float*)(ws + l.dC);
     a.ws_dA = (float*)(ws + l.dA);
     a.ws_dD = (float*)(ws + l.dD);
     a.ws = (WsHeader*)ws;
     a.wait_iters = kDefaultWaitIters;
-    a.shares_bf16 = bwd_use_tc(p) ? 1 : 0;
+    a.shares_bf16 = l.tc ? 1 : 0;
     // a fresh status word for this call's bounded device waits
     if (cudaMemsetAsync(ws, 0, sizeof(WsHeader), (cudaStream_t)stream) != cudaSuccess) return SSD_ERR_CUDA;
-    if ((bwd_use_tc(p) ? launch_bwd_tc(a, (cudaStream_t)stream) : launch_bwd(a, (cudaStream_t)stream)) != cudaSuccess)
+    if ((l.tc ? launch_bwd_tc(a, (cudaStream_t)stream) : launch_bwd(a, (cudaStream_t)stream)) != cudaSuccess)
         return SSD_ERR_CUDA;
     return SSD_OK;
 }

@@ -26,6 +26,13 @@
 //   ddt_t = x_t . v_t + A dl_t,  dA += dt_t dl_t,  dD += dy_t . x_t
 //   Lam  <- e^{tau} Lam + sum_i e^{p_i} dy_i C_i^T            (adjoint of S_in)
 // Every sum of log-decays is a direct sum (no prefix subtraction).
+//
+// Packed documents: no chunk straddles a document start (each document's
+// chunks begin at its start), so no state or adjoint crosses a boundary.  A
+// document's first chunk enters from the document's initial state (or zero)
+// and its start token's own decay applies to it; its last chunk leaves with
+// the document's final-state gradient (or zero) as Lam; the adjoint of its
+// first chunk's entering state is the initial state's gradient.
 #include "ssd_common.cuh"
 #include "ssd_kernels.h"
 
@@ -114,21 +121,6 @@ __device__ __forceinline__ float warp_suffix(float v) {
     return v;
 }
 
-// Packed documents: token t starts document d >= 1 (t == cu[d]).  Its log-decay
-// is taken as -inf, so no state and no adjoint cross the boundary (documents
-// start from a zero state and carry no final-state gradient here).
-__device__ __forceinline__ bool doc_start(const BwdArgs& a, int64_t t) {
-    if (!a.cu) return false;
-    int lo = 1, hi = a.ndocs - 1;
-    while (lo <= hi) {
-        const int mid = (lo + hi) >> 1;
-        const int64_t v = __ldg(a.cu + mid);
-        if (v == t) return true;
-        if (v < t) lo = mid + 1; else hi = mid - 1;
-    }
-    return false;
-}
-
 // Block-wide sum (every thread gets the result); `red` holds one float per warp.
 __device__ __forceinline__ float block_sum(float v, float* red) {
     v = warp_sum(v);
@@ -190,12 +182,18 @@ __global__ void __launch_bounds__(kBwdThreads) ssd_bwd_chunk(BwdArgs a) {
     const float Ah = a.A[h];
     const float Dh = a.D ? a.D[h] : 0.f;
     const int64_t Lseq = a.L;
-    const int nch = (int)((Lseq + Qb - 1) / Qb);
+    const bool docs = a.cu != nullptr;
+    // chunks per row at most: the Qb-token pieces, plus one per document boundary
+    const int nch_max = (int)((Lseq + Qb - 1) / Qb) + (docs ? a.ndocs : 0);
     const T* x = static_cast<const T*>(a.x);
     const T* Bg = static_cast<const T*>(a.B);
     const T* Cg = static_cast<const T*>(a.C);
     const T* dy = static_cast<const T*>(a.dy);
-    float* ckpt = a.ws_ckpt + (size_t)unit * nch * PN;
+    float* ckpt = a.ws_ckpt + (size_t)unit * nch_max * PN;
+    // chunk c: its first token, and (document << 2) | (ends its document << 1) | starts it
+    int* cmap = a.ws_cmap + (size_t)unit * nch_max * 2;
+    // the state index (of initial states, final-state gradients) of document d
+    auto sidx = [&](int d) -> size_t { return docs ? (size_t)d * H + h : (size_t)unit; };
 
     // token row k of this chunk: x / dy row, B / C row (zeros past the end)
     auto xrow = [&](int64_t t) { return x + ((size_t)(b * Lseq + t) * H + h) * P; };
@@ -208,13 +206,31 @@ __global__ void __launch_bounds__(kBwdThreads) ssd_bwd_chunk(BwdArgs a) {
     // ------------------------------------------------------------ phase 1
     // forward over the chunks: the state entering each chunk, kept in the workspace
     float S[kBwdOwn];
+    int nchunks = 0;
+    int doc = 0;
+    bool first = true;   // the next chunk starts a document (or the row)
+    for (int64_t t0 = 0; t0 < Lseq && nchunks < nch_max;) {
+        // this chunk: up to Qb tokens, ending at the document's end
+        int64_t dend = Lseq;
+        if (docs && doc + 1 < a.ndocs) {
+            const int64_t nx = __ldg(a.cu + doc + 1);
+            dend = nx <= t0 ? t0 + 1 : (nx < Lseq ? nx : Lseq);   // (documents are not empty)
+        }
+        const int64_t t1 = (t0 + Qb < dend) ? t0 + Qb : dend;
+        const int c = nchunks++;
+        if (first) {
 #pragma unroll
-    for (int r = 0; r < kBwdOwn; ++r) {
-        const int e = own(r);
-        S[r] = (e < PN && a.init) ? a.init[(size_t)unit * PN + e] : 0.f;
-    }
-    for (int c = 0; c < nch; ++c) {
-        const int64_t t0 = (int64_t)c * Qb;
+            for (int r = 0; r < kBwdOwn; ++r) {
+                const int e = own(r);
+                S[r] = (e < PN && a.init) ? a.init[sidx(doc) * PN + e] : 0.f;
+            }
+        }
+        if (tid == 0) {
+            cmap[2 * c] = (int)t0;
+            cmap[2 * c + 1] = (doc << 2) | (t1 == dend ? 2 : 0) | (first ? 1 : 0);
+        }
+        first = t1 == dend;
+        if (first) ++doc;
 #pragma unroll
         for (int r = 0; r < kBwdOwn; ++r) {
             const int e = own(r);
@@ -223,18 +239,18 @@ __global__ void __launch_bounds__(kBwdThreads) ssd_bwd_chunk(BwdArgs a) {
         __syncthreads();   // the previous chunk's tile reads are done
         for (int k = tid; k < Qb * P; k += kBwdThreads) {
             const int i = k / P, p = k - i * P;
-            const float v = (t0 + i < Lseq) ? Elem<T>::load(xrow(t0 + i) + p) : 0.f;
+            const float v = (t0 + i < t1) ? Elem<T>::load(xrow(t0 + i) + p) : 0.f;
             if (kT) dys[i * P + p] = v;    // x rows, 16-byte aligned (the dy buffer is free here)
             else xs[i * L.sx + p] = v;
         }
         for (int k = tid; k < Qb * N; k += kBwdThreads) {
             const int i = k / N, n = k - i * N;
-            Bs[i * L.sb + n] = (t0 + i < Lseq) ? Elem<T>::load(Bg + bcoff(t0 + i) + n) : 0.f;
+            Bs[i * L.sb + n] = (t0 + i < t1) ? Elem<T>::load(Bg + bcoff(t0 + i) + n) : 0.f;
         }
         if constexpr (kT) {
             if (tid < 32) {   // warp 0, lane = token: suffix sums by shuffles
-                const float d = (t0 + tid < Lseq) ? a.dt[(size_t)(b * Lseq + t0 + tid) * H + h] : 0.f;
-                const float l = doc_start(a, t0 + tid) ? -INFINITY : d * Ah;
+                const float d = (t0 + tid < t1) ? a.dt[(size_t)(b * Lseq + t0 + tid) * H + h] : 0.f;
+                const float l = d * Ah;
                 const float nxt = __shfl_down_sync(0xffffffffu, l, 1);
                 const float sfx = warp_suffix(tid < 31 ? nxt : 0.f);   // s_t: the log-decays after t
                 es[tid] = expf(sfx) * d;          // the weight of token t's input in the chunk's end state
@@ -243,9 +259,9 @@ __global__ void __launch_bounds__(kBwdThreads) ssd_bwd_chunk(BwdArgs a) {
             }
         } else {
             if (tid < Qb) {
-                const float d = (t0 + tid < Lseq) ? a.dt[(size_t)(b * Lseq + t0 + tid) * H + h] : 0.f;
+                const float d = (t0 + tid < t1) ? a.dt[(size_t)(b * Lseq + t0 + tid) * H + h] : 0.f;
                 dts[tid] = d;
-                ell[tid] = doc_start(a, t0 + tid) ? -INFINITY : d * Ah;
+                ell[tid] = d * Ah;
             }
             __syncthreads();
             if (tid < Qb) {
@@ -291,23 +307,28 @@ __global__ void __launch_bounds__(kBwdThreads) ssd_bwd_chunk(BwdArgs a) {
                 }
             }
         }
+        t0 = t1;
     }
 
     // ------------------------------------------------------------ phase 2
     // backward over the chunks, carrying Lam (the adjoint of the state leaving the chunk)
     float Lr[kBwdOwn];
-#pragma unroll
-    for (int r = 0; r < kBwdOwn; ++r) {
-        const int e = own(r);
-        Lr[r] = (e < PN && a.dfin) ? a.dfin[(size_t)unit * PN + e] : 0.f;
-    }
     float dA_acc = 0.f, dD_acc = 0.f;    // thread 0's running sums
-    for (int c = nch - 1; c >= 0; --c) {
-        const int64_t t0 = (int64_t)c * Qb;
+    for (int c = nchunks - 1; c >= 0; --c) {
+        const int64_t t0 = cmap[2 * c];
+        const int64_t t1 = c + 1 < nchunks ? cmap[2 * (c + 1)] : Lseq;
+        const int info = cmap[2 * c + 1];
+        if (info & 2) {   // the chunk ends its document (or the row): the final-state gradient
+#pragma unroll
+            for (int r = 0; r < kBwdOwn; ++r) {
+                const int e = own(r);
+                Lr[r] = (e < PN && a.dfin) ? a.dfin[sidx(info >> 2) * PN + e] : 0.f;
+            }
+        }
         __syncthreads();   // the previous chunk's shared-memory reads are done
         for (int k = tid; k < Qb * P; k += kBwdThreads) {
             const int i = k / P, p = k - i * P;
-            const bool ok = t0 + i < Lseq;
+            const bool ok = t0 + i < t1;
             const float xv = ok ? Elem<T>::load(xrow(t0 + i) + p) : 0.f;
             const float dv = ok ? Elem<T>::load(dyrow(t0 + i) + p) : 0.f;
             xs[i * L.sx + p] = xv;
@@ -319,7 +340,7 @@ __global__ void __launch_bounds__(kBwdThreads) ssd_bwd_chunk(BwdArgs a) {
         }
         for (int k = tid; k < Qb * N; k += kBwdThreads) {
             const int i = k / N, n = k - i * N;
-            const bool ok = t0 + i < Lseq;
+            const bool ok = t0 + i < t1;
             const float bv = ok ? Elem<T>::load(Bg + bcoff(t0 + i) + n) : 0.f;
             const float cv = ok ? Elem<T>::load(Cg + bcoff(t0 + i) + n) : 0.f;
             Bs[i * L.sb + n] = bv;
@@ -342,9 +363,9 @@ __global__ void __launch_bounds__(kBwdThreads) ssd_bwd_chunk(BwdArgs a) {
             }
         }
         if (tid < Qb) {
-            const float d = (t0 + tid < Lseq) ? a.dt[(size_t)(b * Lseq + t0 + tid) * H + h] : 0.f;
+            const float d = (t0 + tid < t1) ? a.dt[(size_t)(b * Lseq + t0 + tid) * H + h] : 0.f;
             dts[tid] = d;
-            ell[tid] = doc_start(a, t0 + tid) ? -INFINITY : d * Ah;
+            ell[tid] = d * Ah;
         }
         const float K = block_sum(kdot, red);   // (contains a barrier: the tiles are visible)
         if constexpr (kT) {
@@ -456,7 +477,7 @@ __global__ void __launch_bounds__(kBwdThreads) ssd_bwd_chunk(BwdArgs a) {
                         const float xv = xs[j * L.sx + p], dv = dys[j * 64 + p];
                         vx[q] = v[u] * xv;
                         lbx[q] = acc[u] * xv;
-                        if (t0 + j < Lseq)
+                        if (t0 + j < t1)
                             Elem<T>::store(static_cast<T*>(a.dx) + ((size_t)(b * Lseq + t0 + j) * H + h) * 64 + p,
                                            fmaf(dts[j], v[u], Dh * dv));
                     }
@@ -530,7 +551,7 @@ __global__ void __launch_bounds__(kBwdThreads) ssd_bwd_chunk(BwdArgs a) {
 #pragma unroll
                 for (int u = 0; u < 8; ++u) {
                     const int j = j0 + u;
-                    if (t0 + j < Lseq)
+                    if (t0 + j < t1)
                         out[((size_t)(b * Lseq + t0 + j) * H + h) * 128 + n] = half ? r[u] : dts[j] * r[u];
                 }
             }
@@ -551,14 +572,14 @@ __global__ void __launch_bounds__(kBwdThreads) ssd_bwd_chunk(BwdArgs a) {
 #pragma unroll 8
                 for (int n = 0; n < N; ++n) sc = fmaf(Sin[p * L.sb + n], Cs[j * N + n], sc);
                 scdy[q] = sc * dys[j * P + p];
-                if (t0 + j < Lseq)
+                if (t0 + j < t1)
                     Elem<T>::store(static_cast<T*>(a.dx) + ((size_t)(b * Lseq + t0 + j) * H + h) * P + p,
                                    fmaf(dts[j], v, Dh * dys[j * P + p]));
             }
             // this head's shares of dB and dC
             for (int q = tid; q < Qb * N; q += kBwdThreads) {
                 const int j = q / N, n = q - j * N;
-                if (t0 + j >= Lseq) continue;
+                if (t0 + j >= t1) continue;
                 float lx = 0.f, sd = 0.f;
 #pragma unroll 8
                 for (int p = 0; p < P; ++p) {
@@ -610,7 +631,7 @@ __global__ void __launch_bounds__(kBwdThreads) ssd_bwd_chunk(BwdArgs a) {
                 const int t = tid;
                 const float U = warp_suffix(uv[t]), V = warp_prefix(wv[t]);
                 const float dl = rv[t] + U + V + etau * K - dts[t] * ddta[t];
-                if (t0 + t < Lseq) a.ddt[(size_t)(b * Lseq + t0 + t) * H + h] = fmaf(Ah, dl, ddta[t]);
+                if (t0 + t < t1) a.ddt[(size_t)(b * Lseq + t0 + t) * H + h] = fmaf(Ah, dl, ddta[t]);
                 const float da = warp_sum(dts[t] * dl), dd = warp_sum(ddv[t]);
                 dA_acc += da;
                 dD_acc += dd;
@@ -622,7 +643,7 @@ __global__ void __launch_bounds__(kBwdThreads) ssd_bwd_chunk(BwdArgs a) {
                 for (int i = t; i < Qb; ++i) U += uv[i];
                 for (int j = 0; j <= t; ++j) V += wv[j];
                 const float dl = rv[t] + U + V + etau * K - dts[t] * ddta[t];
-                if (t0 + t < Lseq) a.ddt[(size_t)(b * Lseq + t0 + t) * H + h] = fmaf(Ah, dl, ddta[t]);
+                if (t0 + t < t1) a.ddt[(size_t)(b * Lseq + t0 + t) * H + h] = fmaf(Ah, dl, ddta[t]);
                 // thread 0 sums these in token order below
                 ddta[t] = dts[t] * dl;
             }
@@ -665,12 +686,13 @@ __global__ void __launch_bounds__(kBwdThreads) ssd_bwd_chunk(BwdArgs a) {
                 }
             }
         }
-    }
-    if (a.dinit) {
+        // the chunk starts its document (or the row): Lr is the initial state's gradient
+        if ((info & 1) && a.dinit) {
 #pragma unroll
-        for (int r = 0; r < kBwdOwn; ++r) {
-            const int e = own(r);
-            if (e < PN) a.dinit[(size_t)unit * PN + e] = Lr[r];
+            for (int r = 0; r < kBwdOwn; ++r) {
+                const int e = own(r);
+                if (e < PN) a.dinit[sidx(info >> 2) * PN + e] = Lr[r];
+            }
         }
     }
     if (tid == 0) {

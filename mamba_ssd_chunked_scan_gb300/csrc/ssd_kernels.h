@@ -96,6 +96,7 @@ struct BwdArgs {
     float* dD;
     float* dinit;
     float* ws_ckpt;        // [batch * H * nchunks * P * N] state entering each chunk
+    int* ws_cmap;          // [batch * H * nchunks * 2] chunk starts and document flags (CUDA-core backward)
     float* ws_dB;          // [batch * L * H * N] per-head shares of dB (fp32, or bf16: shares_bf16)
     float* ws_dC;          // [batch * L * H * N] per-head shares of dC
     int shares_bf16;       // the shares are bf16 (the tensor-core backward)

@@ -178,10 +178,17 @@ def test_bwd_workspace_size(L):
     n = L.lib.ssd_bwd_workspace_size(ctypes.byref(params(L, batch=2, seqlen=1000, nheads=4, dtype=0)))
     assert n >= 256 + 2 * 4 * 32 * 64 * 128 * 4 + 4 * shares + 2 * 8 * 4
     assert L.lib.ssd_bwd_workspace_size(ctypes.byref(params(L, ndocs=3, batch=1))) > 0    # packed documents
+    # packed documents with per-document states: CUDA-core chunks of 32 tokens that also start at
+    # every document start (one more chunk per document at most), fp32 shares, chunk map
+    pd = params(L, batch=1, seqlen=1000, nheads=4, ndocs=3)
+    nd = L.lib.ssd_bwd_workspace_size_doc_states(ctypes.byref(pd))
+    assert nd >= 256 + 4 * (32 + 3) * 64 * 128 * 4 + 2 * (1000 * 4 * 128 * 4) + 4 * (32 + 3) * 2 * 4
+    assert nd > L.lib.ssd_bwd_workspace_size(ctypes.byref(pd))
+    assert L.lib.ssd_bwd_workspace_size_doc_states(ctypes.byref(params(L, batch=2, seqlen=1000))) == 0   # no documents
     assert L.lib.ssd_bwd_workspace_size(ctypes.byref(params(L, headdim=128, dstate=128))) == 0   # P * N > 8192
 
 
-@pytest.mark.parametrize("case,code", [("docs_dinit", 2), ("docs_no_cu", 1), ("null_dx", 1), ("alias", 1),
+@pytest.mark.parametrize("case,code", [("docs_dinit", 3), ("docs_no_cu", 1), ("null_dx", 1), ("alias", 1),
                                        ("misaligned", 1), ("no_ws", 3)])
 def test_bwd_invalid_args(L, case, code):
     base = 1 << 40
@@ -189,7 +196,7 @@ def test_bwd_invalid_args(L, case, code):
         ("x", "dt", "A", "B", "C", "D", "dy", "dx", "ddt", "dA", "dB", "dC", "ws"))}
     p = params(L, batch=2, seqlen=256, nheads=4)
     cu, dinit = None, None
-    if case == "docs_dinit":     # packed documents take no initial-state gradient
+    if case == "docs_dinit":     # per-document states need ssd_bwd_workspace_size_doc_states() bytes
         p = params(L, batch=1, seqlen=256, nheads=4, ndocs=2)
         cu, dinit = base + (40 << 30), base + (41 << 30)
     if case == "docs_no_cu":     # ndocs without cu_seqlens

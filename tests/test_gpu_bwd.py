@@ -27,7 +27,7 @@ def cotangents(p, seed, with_dfin=True):
     dy = rng.standard_normal((p.batch, p.seqlen, p.nheads, p.headdim)).astype(np.float32)
     if p.dtype == "bf16":
         dy = synth.bf16_to_f32(synth.bf16_bits(dy))
-    dfin = rng.standard_normal((p.batch, p.nheads, p.headdim, p.dstate)).astype(np.float32) if with_dfin else None
+    dfin = rng.standard_normal((p.nstates, p.nheads, p.headdim, p.dstate)).astype(np.float32) if with_dfin else None
     return dy, dfin
 
 
@@ -112,6 +112,32 @@ def test_bwd_packed_documents(lens, kw):
     p = synth.make_problem(batch=1, seqlen=sum(lens), nheads=4, ngroups=2, chunk=128, seed=311,
                            doc_lengths=lens, dt_dist="softplus_n22", **kw)
     check(p, with_dfin=False)
+
+
+@pytest.mark.parametrize("lens,kw", [
+    ([3, 300, 128, 1, 257, 90, 500], dict(headdim=64, dstate=128, dtype="bf16")),    # tiled instance, bf16
+    ([32, 1, 31, 64, 33, 2], dict(headdim=64, dstate=128, dtype="f32")),             # ends on chunk edges
+    ([10, 1, 50, 39], dict(headdim=16, dstate=32, dtype="f32")),                    # generic instance
+])
+@pytest.mark.parametrize("with_dfin", [True, False])
+def test_bwd_packed_documents_with_states(lens, kw, with_dfin):
+    """Packed documents, each from its own initial state and with (or without)
+    its own final-state gradient: the CUDA-core kernel's chunks start at every
+    document start; dinit is per document."""
+    p = synth.make_problem(batch=1, seqlen=sum(lens), nheads=4, ngroups=2, chunk=128, seed=315,
+                           doc_lengths=lens, A_dist="exp", init_std=0.5, **kw)
+    got = check(p, with_dfin=with_dfin)
+    assert got["dinit"] is not None and got["dinit"].shape[0] == len(lens)
+
+
+def test_bwd_packed_documents_final_gradient_only():
+    """Documents from zero states with final-state gradients (no initial
+    states given): the same path, dinit not asked for."""
+    lens = [70, 1, 200, 33]
+    p = synth.make_problem(batch=1, seqlen=sum(lens), nheads=4, headdim=64, dstate=128, ngroups=1, chunk=128,
+                           dtype="f32", seed=317, doc_lengths=lens, A_dist="exp")
+    got = check(p)
+    assert got["dinit"] is None
 
 
 @pytest.mark.parametrize("kw", [
