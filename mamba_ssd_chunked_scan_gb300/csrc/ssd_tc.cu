@@ -821,6 +821,7 @@ __global__ void __launch_bounds__(kThreads, 1) ssd_chunk_tc(const __grid_constan
             ptx::tc_fence_before();
             __syncwarp();
             if (lane == 0) ptx::mbar_arrive(&sh.barM[X]);
+            bool stop;
             if (full_mode) {
                 // ---- epilogue of chunk c: y = Ydiag + 2^{p_i} Yoff  (D x is in Ydiag).
                 // The rows are staged in this group's scaled-X buffer (free once dS(c)
@@ -859,14 +860,18 @@ __global__ void __launch_bounds__(kThreads, 1) ssd_chunk_tc(const __grid_constan
                             make_uint4(ow[4 * q], ow[4 * q + 1], ow[4 * q + 2], ow[4 * q + 3]);
                 }
                 ptx::fence_proxy_async();
-                ptx::named_bar(nb, 128);
-                if (mt == 0) {
+                // every row is staged (and the group's last look at the abort flag
+                // this chunk: nothing after this barrier reads the group's scratch)
+                stop = ptx::named_bar_any(nb, 128, *(volatile int*)&sh.abort != 0);
+                if (mt == 0 && !stop) {
                     ptx::tma_store_4d(&prm.tm_y, ys, 0, h, (int)t, (int)b);
                     ptx::bulk_commit();
                 }
+            } else {
+                stop = ptx::named_bar_any(nb, 128, *(volatile int*)&sh.abort != 0);
             }
             cur.next2(a, nunits);                 // this group's next item
-            if (ptx::named_bar_any(nb, 128, *(volatile int*)&sh.abort != 0)) break;
+            if (stop) break;
         }
         if (mt == 0) ptx::bulk_wait0();
     } else {
