@@ -107,6 +107,7 @@ struct TcSmall {
     uint64_t barFix[2];            // the state group has rewritten the Yoff rows of a chunk
     uint32_t startmask[4];         // per warp: rows where a document starts (state group)
     uint32_t endmask[4];           // per warp: rows e < nv - 1 where a document ends (state group)
+    uint32_t evflags[4];           // per state-group warp: OR of (stale meta, a document end, a start)
     float segtot[4];               // per warp: log2-decay sum of the warp's last document segment
     float qlast, qend;             // initial-state decay at the chunk's last row / at a document end
     int dlast;                     // the document open at the chunk's last row, if it started in the chunk
@@ -190,9 +191,11 @@ __device__ __forceinline__ uint64_t desc_mn2(uint32_t base, int kk) {
 // spare TMEM columns (lane n, column p).  It also leaves in sh.qend the decay
 // q_e = 2^{seg(e, st) + l_st} of d's initial state when d started in this
 // chunk at row st and the call has initial states, else 0; the caller adds
-// 2^{p_e} S_in (its fp32 registers) and q_e init_d.  Rare path, kept out of
-// line: all 128 threads of the state group call it together (thread i = row i).
-__device__ __noinline__ void doc_end_mma(TcSmall& sh, const FwdArgs& a, const ChunkMeta& m, const uint8_t* stg,
+// 2^{p_e} S_in (its fp32 registers) and q_e init_d.  All 128 threads of the
+// state group call it together (thread i = row i).  Inlined, and only into the
+// kernel instance for document events: out of line, the caller's 64-register
+// state had to be saved around the call, which made every chunk slower.
+__device__ __forceinline__ void doc_end_mma(TcSmall& sh, const FwdArgs& a, const ChunkMeta& m, const uint8_t* stg,
                                          uint8_t* sin_tile, uint32_t tb, int e, float A2, int i, int& init_cnt) {
     constexpr uint32_t idDS = ptx::idesc_bf16(128, 64, 1, 1);
     const int lane = i & 31, rb = i >> 5;
@@ -253,10 +256,11 @@ __device__ __noinline__ void doc_end_mma(TcSmall& sh, const FwdArgs& a, const Ch
 // epilogue then adds them unscaled.  q_i comes from a segmented scan of the
 // log2-decays that restarts at each start (no prefix subtraction).  Also
 // leaves in sh.qlast / sh.dlast the decay and document of the initial state
-// that reaches the chunk's end (dlast = -1: none).  Rare path, kept out of
-// line: all 128 threads of the state group call it together (thread i =
+// that reaches the chunk's end (dlast = -1: none).  Inlined like doc_end_mma
+// (16-column pieces and 32 loads at a time beside the caller's live state):
+// all 128 threads of the state group call it together (thread i =
 // chunk row i = TMEM lane i).
-__device__ __noinline__ void doc_start_rows(TcSmall& sh, const FwdArgs& a, const ChunkMeta& m, uint32_t ctile,
+__device__ __forceinline__ void doc_start_rows(TcSmall& sh, const FwdArgs& a, const ChunkMeta& m, uint32_t ctile,
                                             uint8_t* sin_tile, uint32_t tb, int X, float A2, int h, int nv, int i,
                                             int& init_cnt) {
     constexpr uint32_t idYo = ptx::idesc_bf16(128, 64, 0, 1);
@@ -297,16 +301,12 @@ __device__ __noinline__ void doc_start_rows(TcSmall& sh, const FwdArgs& a, const
     {
         const float pe = m.pexp[i];
 #pragma unroll 1
-        for (int hf = 0; hf < 2; ++hf) {
-            uint32_t r[32], lo[16], hi[16];
-            ptx::tmem_load32(yo + 32 * hf, r);
+        for (int q16 = 0; q16 < 4; ++q16) {   // 16 columns at a time (the caller's state is live)
+            uint32_t r[16];
+            ptx::tmem_load16(yo + 16 * q16, r);
 #pragma unroll
-            for (int k = 0; k < 16; ++k) {
-                lo[k] = __float_as_uint(__uint_as_float(r[k]) * pe);
-                hi[k] = __float_as_uint(__uint_as_float(r[16 + k]) * pe);
-            }
-            ptx::tmem_st16(yo + 32 * hf, lo);
-            ptx::tmem_st16(yo + 32 * hf + 16, hi);
+            for (int k = 0; k < 16; ++k) r[k] = __float_as_uint(__uint_as_float(r[k]) * pe);
+            ptx::tmem_st16(yo + 16 * q16, r);
         }
         ptx::tmem_st_wait();
     }
@@ -319,16 +319,20 @@ __device__ __noinline__ void doc_start_rows(TcSmall& sh, const FwdArgs& a, const
             mk &= mk - 1;
             const int d = m.rowdoc[st];
             // init_d as the (n, p) bf16 operand; thread i writes state column n = i
-            // (all 64 loads in flight at once)
+            // (32 loads in flight at a time: the caller's state is live)
             const float* src = a.init + ((size_t)d * a.H + h) * (size_t)(P * N) + i;
-            float iv[P];
 #pragma unroll
-            for (int p = 0; p < P; ++p) iv[p] = __ldg(src + (size_t)p * N);
+            for (int hp = 0; hp < 2; ++hp) {
+                float iv[32];
 #pragma unroll
-            for (int q8 = 0; q8 < 8; ++q8)
-                *reinterpret_cast<uint4*>(sin_tile + sw128_off(i, 8 * q8)) =
-                    make_uint4(pack_bf16(iv[8 * q8], iv[8 * q8 + 1]), pack_bf16(iv[8 * q8 + 2], iv[8 * q8 + 3]),
-                               pack_bf16(iv[8 * q8 + 4], iv[8 * q8 + 5]), pack_bf16(iv[8 * q8 + 6], iv[8 * q8 + 7]));
+                for (int p = 0; p < 32; ++p) iv[p] = __ldg(src + (size_t)(32 * hp + p) * N);
+#pragma unroll
+                for (int q8 = 0; q8 < 4; ++q8)
+                    *reinterpret_cast<uint4*>(sin_tile + sw128_off(i, 32 * hp + 8 * q8)) =
+                        make_uint4(pack_bf16(iv[8 * q8], iv[8 * q8 + 1]), pack_bf16(iv[8 * q8 + 2], iv[8 * q8 + 3]),
+                                   pack_bf16(iv[8 * q8 + 4], iv[8 * q8 + 5]),
+                                   pack_bf16(iv[8 * q8 + 6], iv[8 * q8 + 7]));
+            }
             ptx::fence_proxy_async();
             ptx::named_bar(kBarState, 128);
             if (i == 0) {
@@ -345,16 +349,12 @@ __device__ __noinline__ void doc_start_rows(TcSmall& sh, const FwdArgs& a, const
             const bool mine = has && i < nv && m.rowdoc[i] == d;
             if (__any_sync(0xffffffffu, mine)) {
 #pragma unroll 1
-                for (int hf = 0; hf < 2; ++hf) {
-                    uint32_t sr[32], yr[32], lo[16], hi[16];
-                    ptx::tmem_load32x2(scr + 32 * hf, sr, yo + 32 * hf, yr);
+                for (int q16 = 0; q16 < 4; ++q16) {   // 16 columns at a time
+                    uint32_t sr[16], yr[16];
+                    ptx::tmem_load16x2(scr + 16 * q16, sr, yo + 16 * q16, yr);
 #pragma unroll
-                    for (int k = 0; k < 16; ++k) {
-                        lo[k] = mine ? __float_as_uint(q * __uint_as_float(sr[k])) : yr[k];
-                        hi[k] = mine ? __float_as_uint(q * __uint_as_float(sr[16 + k])) : yr[16 + k];
-                    }
-                    ptx::tmem_st16(yo + 32 * hf, lo);
-                    ptx::tmem_st16(yo + 32 * hf + 16, hi);
+                    for (int k = 0; k < 16; ++k) yr[k] = mine ? __float_as_uint(q * __uint_as_float(sr[k])) : yr[k];
+                    ptx::tmem_st16(yo + 16 * q16, yr);
                 }
                 ptx::tmem_st_wait();
             }
@@ -951,9 +951,14 @@ __global__ void __launch_bounds__(kThreads, 1) ssd_chunk_tc(const __grid_constan
                 // agreed by the whole group, and only on chunk values that are
                 // complete: the branches hold barriers, and after a wait that ran
                 // out the values may still be changing
-                const bool stale = ptx::named_bar_any(kBarState, 128, !meta_ok);
-                const bool any_end = ptx::named_bar_any(kBarState, 128, end_row) && !stale && a.fin != nullptr;
-                fix = ptx::named_bar_any(kBarState, 128, (fl & 1) != 0) && !stale && a.init != nullptr;
+                const uint32_t wf = __reduce_or_sync(
+                    0xffffffffu, (meta_ok ? 0u : 1u) | (end_row ? 2u : 0u) | ((fl & 1) ? 4u : 0u));
+                if (lane == 0) sh.evflags[rb] = wf;
+                ptx::named_bar(kBarState, 128);
+                const uint32_t gf = (sh.evflags[0] | sh.evflags[1]) | (sh.evflags[2] | sh.evflags[3]);
+                const bool stale = (gf & 1u) != 0;
+                const bool any_end = (gf & 2u) && !stale && a.fin != nullptr;
+                fix = (gf & 4u) && !stale && a.init != nullptr;
                 if (any_end || fix) {
                     // Yoff(c) is complete: the incoming-state tile and the spare TMEM
                     // columns are free for the rare paths below
@@ -972,25 +977,26 @@ __global__ void __launch_bounds__(kThreads, 1) ssd_chunk_tc(const __grid_constan
                             const int e = 32 * w + __ffs(mk) - 1;
                             mk &= mk - 1;
                             doc_end_mma(sh, a, m, stg, sm + kSin, tb, e, A2, i, init_cnt);
-                            uint32_t d0[32], d1[32];
-                            ptx::tmem_load32x2(lane_addr + kTmInit, d0, lane_addr + kTmInit + 32, d1);
                             const float pe = m.pexp[e], qe = sh.qend;
                             const size_t so = ((size_t)m.rowdoc[e] * a.H + h) * PN + i;
                             float* fo = a.fin + so;
-                            if (qe != 0.f) {
-                                const float* src = a.init + so;
+                            const float* src = a.init + so;
+                            // in two halves of 32 columns (32 registers beside the state's 64)
 #pragma unroll
-                                for (int p = 0; p < 32; ++p) {
-                                    fo[(size_t)p * N] = fmaf(qe, __ldg(src + (size_t)p * N),
-                                                             fmaf(pe, S[p], __uint_as_float(d0[p])));
-                                    fo[(size_t)(p + 32) * N] = fmaf(qe, __ldg(src + (size_t)(p + 32) * N),
-                                                                    fmaf(pe, S[p + 32], __uint_as_float(d1[p])));
-                                }
-                            } else {
+                            for (int half = 0; half < 2; ++half) {
+                                uint32_t dv[32];
+                                ptx::tmem_load32(lane_addr + kTmInit + 32 * half, dv);
+                                if (qe != 0.f) {
 #pragma unroll
-                                for (int p = 0; p < 32; ++p) {
-                                    fo[(size_t)p * N] = fmaf(pe, S[p], __uint_as_float(d0[p]));
-                                    fo[(size_t)(p + 32) * N] = fmaf(pe, S[p + 32], __uint_as_float(d1[p]));
+                                    for (int p = 0; p < 32; ++p)
+                                        fo[(size_t)(p + 32 * half) * N] =
+                                            fmaf(qe, __ldg(src + (size_t)(p + 32 * half) * N),
+                                                 fmaf(pe, S[p + 32 * half], __uint_as_float(dv[p])));
+                                } else {
+#pragma unroll
+                                    for (int p = 0; p < 32; ++p)
+                                        fo[(size_t)(p + 32 * half) * N] =
+                                            fmaf(pe, S[p + 32 * half], __uint_as_float(dv[p]));
                                 }
                             }
                             // the spare TMEM columns and the operand tile are free again
