@@ -32,7 +32,12 @@
  *   initial_states  (nstates, nheads, headdim, dstate)    fp32, optional (zeros)
  *   final_states    (nstates, nheads, headdim, dstate)    fp32, optional
  *   cu_seqlens      (ndocs + 1) int32, cu[0] = 0 < cu[1] < ... < cu[ndocs] = seqlen
- *                   (no empty document), optional
+ *                   (no empty document), optional.  The offsets are in device
+ *                   memory, so the host cannot check them; the last launch of
+ *                   ssd_fwd() / ssd_bwd() does, and records SSD_ERR_DEVICE_CHECK
+ *                   (where 40) in the workspace status word when they break
+ *                   this rule.  The kernels keep every index in bounds either
+ *                   way; the outputs are then undefined.
  *   nstates = ndocs when cu_seqlens is given (then batch must be 1), else batch.
  *
  * Ownership: the caller owns every buffer; the library keeps no pointer past
@@ -67,7 +72,7 @@ typedef enum {
     SSD_ERR_WORKSPACE = 3,     /* workspace missing or smaller than required */
     SSD_ERR_CUDA = 4,          /* a CUDA runtime call or launch failed */
     SSD_ERR_TIMEOUT = 5,       /* a device-side bounded wait ran out */
-    SSD_ERR_DEVICE_CHECK = 6   /* a device-side consistency check failed */
+    SSD_ERR_DEVICE_CHECK = 6   /* a device-side consistency check failed (cu_seqlens) */
 } ssd_status_t;
 
 typedef enum { SSD_F32 = 0, SSD_BF16 = 1 } ssd_dtype_t;
@@ -283,7 +288,8 @@ SSD_API int ssd_check_status(void* workspace, void* stream);
  * 14 C init_d^T done, 15 state terms of a chunk with document starts ready)
  * or of the split-aggregate kernel (21 stage free, 22 stage loaded, 23 scaled
  * tile ready, 24 split contraction done, 25 drain of copies in flight, 26 the
- * other scaling group's decay product ready). */
+ * other scaling group's decay product ready); with SSD_ERR_DEVICE_CHECK, 40:
+ * the packed-document offsets are not 0 = cu[0] < ... < cu[ndocs] = seqlen. */
 SSD_API int ssd_check_status_where(void* workspace, void* stream, uint32_t* where);
 
 /* Test aid for the device-side failure path: ssd_fwd() with an injected stall.

@@ -203,6 +203,8 @@ __global__ void __launch_bounds__(kBwdThreads) ssd_bwd_chunk(BwdArgs a) {
     const int own_n = kT ? (tid & 127) : 0, own_p0 = kT ? (tid >> 7) * 8 : 0;
     auto own = [&](int r) -> int { return kT ? (own_p0 + r) * N + own_n : tid + kBwdThreads * r; };
 
+    if (docs && unit == 0) check_cu_seqlens(a.cu, a.ndocs, Lseq, a.ws, tid, kBwdThreads);   // the call's offsets
+
     // ------------------------------------------------------------ phase 1
     // forward over the chunks: the state entering each chunk, kept in the workspace
     float S[kBwdOwn];

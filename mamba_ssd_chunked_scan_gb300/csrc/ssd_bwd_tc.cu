@@ -393,6 +393,9 @@ __global__ void __launch_bounds__(kThreads, 1) ssd_bwd_tc(const __grid_constant_
                                                              &sh.never, a.wait_iters))
                     record_error(a.ws, SSD_ERR_TIMEOUT, kWhereDrain);
             ptx::bulk_wait0();
+        } else if (warp == 9 && blockIdx.x == 0 && a.cu) {
+            // an idle warp checks the call's packed-document offsets
+            check_cu_seqlens(a.cu, a.ndocs, a.L, a.ws, lane, 32);
         }
         __syncwarp();
     } else {

@@ -23,6 +23,23 @@ __device__ __forceinline__ void record_error(WsHeader* ws, uint32_t code, uint32
     if (ws && atomicCAS(&ws->status, 0u, code) == 0u) ws->where = where;
 }
 
+// where code of a failed packed-document offset check
+constexpr uint32_t kWhereCuSeqlens = 40;
+
+// Packed-document offsets must run 0 = cu[0] < cu[1] < ... < cu[ndocs] = L (no
+// empty document).  The host cannot read them (device memory), so the last
+// launch of a call checks them: threads t = 0 .. stride - 1 of one CTA each
+// take every stride-th pair and record SSD_ERR_DEVICE_CHECK (where 40) on a
+// violation.  Every kernel that reads cu_seqlens keeps its indexes in bounds
+// whatever the offsets hold; the results are undefined when this check fails.
+__device__ __forceinline__ void check_cu_seqlens(const int32_t* cu, int ndocs, int64_t L, WsHeader* ws, int t,
+                                                 int stride) {
+    bool bad = t == 0 && (__ldg(cu) != 0 || (int64_t)__ldg(cu + ndocs) != L);
+    for (int k = t; k < ndocs; k += stride)
+        if (__ldg(cu + k) >= __ldg(cu + k + 1)) bad = true;
+    if (bad) record_error(ws, SSD_ERR_DEVICE_CHECK, kWhereCuSeqlens);
+}
+
 template <typename T> struct Elem;
 template <> struct Elem<float> {
     static __device__ __forceinline__ float load(const float* p) { return *p; }

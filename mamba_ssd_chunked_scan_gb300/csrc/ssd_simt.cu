@@ -85,6 +85,8 @@ __global__ void __launch_bounds__(256) ssd_chunk_simt(FwdArgs a) {
     T* y = (T*)a.y;
     const size_t PN = (size_t)P * N;
 
+    // the full pass checks the call's packed-document offsets (block 0)
+    if (a.cu && a.mode == kModeFull && u == 0) check_cu_seqlens(a.cu, a.ndocs, L, a.ws, tid, nt);
     // incoming state: from the split scan (slot s - 1) when this split continues a document
     for (int k = tid; k < P * N; k += nt)
         S[k] = (a.mode == kModeFull && a.nsplit > 1 && s > 0) ? a.ws_state[(u - 1) * PN + k] : 0.f;
@@ -114,7 +116,9 @@ __global__ void __launch_bounds__(256) ssd_chunk_simt(FwdArgs a) {
                 if (a.cu) {
                     doc = find_doc(a.cu, a.ndocs, t);
                     const int64_t ds = a.cu[doc];
-                    st = (ds > c0) ? (int)(ds - c0) : 0;
+                    // (clamped to the row: offsets that break their contract keep the
+                    // shared-memory indexes in bounds)
+                    st = (ds > c0) ? (int)((ds - c0 < i) ? ds - c0 : i) : 0;
                     if (ds >= c0) fl |= 1;
                     if (t + 1 == a.cu[doc + 1]) fl |= 2;
                 } else {

@@ -639,6 +639,9 @@ __global__ void __launch_bounds__(kThreads, 1) ssd_chunk_tc(const __grid_constan
             }
             ptx::mma_commit(&sh.drain[1]);
             if (!ptx::mbar_wait(&sh.drain[1], 0, &sh.never, a.wait_iters)) fail(sh, a, kWhereDrain);
+        } else if (warp == 1 && kDocs && full_mode && blockIdx.x == 0) {
+            // the dS issuer's idle lanes: the packed-document offsets of the call
+            check_cu_seqlens(a.cu, a.ndocs, a.L, a.ws, lane - 1, 31);
         }
     } else if (wg <= 2) {
         // ================================================================ mask groups
