@@ -164,14 +164,16 @@ def ssd_fwd(x, dt, A, B, C, D=None, initial_states=None, cu_seqlens=None, *, chu
 
 
 def ssd_bwd(x, dt, A, B, C, dy, D=None, initial_states=None, dfinal_states=None, cu_seqlens=None, *,
-            chunk=128, want_dinit=None, stream=None, check_status=False):
+            chunk=128, split_len=0, want_dinit=None, stream=None, check_status=False):
     """Gradients of <dy, y> + <dfinal_states, final_states> for one ssd_fwd
     call's inputs.  With packed documents (cu_seqlens, batch 1) the states
     are per document: initial_states, dfinal_states and dinit are (ndocs, H,
     P, N).  Returns a dict with dx, ddt, dA, dB, dC, dD (None without D) and
     dinit (by default for batch rows, or for documents with initial_states).
-    With check_status, also synchronises the stream and raises if a
-    device-side wait ran out (the workspace's status word)."""
+    split_len: tokens per sequence split of the tensor-core backward (0:
+    automatic); it changes only the rounding.  With check_status, also
+    synchronises the stream and raises if a device-side wait ran out (the
+    workspace's status word)."""
     batch, seqlen, nheads, headdim = x.shape
     ngroups, dstate = B.shape[2], B.shape[3]
     dev = x.device
@@ -180,7 +182,8 @@ def ssd_bwd(x, dt, A, B, C, dy, D=None, initial_states=None, dfinal_states=None,
         want_dinit = cu_seqlens is None or initial_states is not None
     if cu_seqlens is not None and (cu_seqlens.dtype != torch.int32 or cu_seqlens.device != dev):
         raise ValueError("cu_seqlens: expected int32 (ndocs + 1) on the device")
-    params = _lib.make_params(batch, seqlen, nheads, headdim, dstate, ngroups, chunk, 0, ndocs, _dtype_code(x))
+    params = _lib.make_params(batch, seqlen, nheads, headdim, dstate, ngroups, chunk, split_len, ndocs,
+                              _dtype_code(x))
     shp_x, shp_bc = (batch, seqlen, nheads, headdim), (batch, seqlen, ngroups, dstate)
     shp_s = (batch if cu_seqlens is None else ndocs, nheads, headdim, dstate)
     for name, t, shp, dt_ in (("x", x, shp_x, x.dtype), ("dt", dt, shp_x[:3], torch.float32),

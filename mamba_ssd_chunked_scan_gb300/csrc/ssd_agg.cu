@@ -23,6 +23,14 @@
 // item ahead), segsum, the scaled x rows written in place.
 // The running product of the later chunks' totals passes from one group to
 // the other through shared memory; group 1 writes the states at the end.
+//
+// Reverse mode (kRev, for the backward pass's sequence splits): the adjoint
+// entering split s from its right, V_s = sum_{i in split} 2^{P_i} dy_i C_i^T
+// with P_i = sum_{k=split start..i} l_k, is the same contraction with C in
+// place of B, dy in place of x, the chunks visited from the split's start
+// forwards and the row prefix 2^{p_i} times the running product of the
+// earlier chunks' totals in place of the suffix weight (no dt factor).  It is
+// formed for splits 1 .. nsplit - 1.
 #include <cuda.h>
 #include <cuda_bf16.h>
 #include <stddef.h>
@@ -99,7 +107,7 @@ __device__ __forceinline__ uint32_t scale_pair(uint32_t w, uint64_t f2) {
     return *reinterpret_cast<uint32_t*>(&v);
 }
 
-template <int K, bool kDocs>
+template <int K, bool kDocs, bool kRev>
 __global__ void __launch_bounds__(kThreads, 1) ssd_split_agg_tc(const __grid_constant__ AggParams prm) {
     using Cfg = AggCfg<K>;
     extern __shared__ uint8_t smem_raw[];
@@ -114,7 +122,7 @@ __global__ void __launch_bounds__(kThreads, 1) ssd_split_agg_tc(const __grid_con
     const int64_t u = blockIdx.x;
     const int hq = (int)(u % nhq);
     const int64_t bs = u / nhq;
-    const int s = (int)(bs % prm.nsplit_agg);
+    const int s = (int)(bs % prm.nsplit_agg) + (kRev ? 1 : 0);   // (reverse mode: splits 1 ..)
     const int b = (int)(bs / prm.nsplit_agg);
     const int h0 = hq * K;
     const int g = h0 / (a.H / a.G);
@@ -154,7 +162,7 @@ __global__ void __launch_bounds__(kThreads, 1) ssd_split_agg_tc(const __grid_con
             for (int r = 0; r < (a.stall_loads ? 0 : nch); ++r) {
                 const int st = r % NS;
                 if (r >= NS && !agg_wait(sh, a, &sh.empty[st], ((r / NS) - 1) & 1, kWhereAggEmpty)) break;
-                const int t = t0 + (nch - 1 - r) * Q;   // chunks from the split's end backwards
+                const int t = t0 + (kRev ? r : nch - 1 - r) * Q;   // chunks from the split's end backwards
                 uint8_t* stg = sm + st * Cfg::kStage;
                 ptx::mbar_expect_tx(&sh.full[st], Cfg::kStage);
                 ptx::tma_load_4d(stg, &prm.tm_B, &sh.full[st], 0, g, t, b);
@@ -204,10 +212,10 @@ __global__ void __launch_bounds__(kThreads, 1) ssd_split_agg_tc(const __grid_con
             Ls[h] = 0.f;
         }
         int doc = 0;   // document cursor (packed documents), moving backwards
-        if (kDocs) doc = find_doc_agg(a.cu, a.ndocs, (int64_t)t1 - 1);
+        if (kDocs && !kRev) doc = find_doc_agg(a.cu, a.ndocs, (int64_t)t1 - 1);
         // dt of item r for this thread's row (0 past the split), loaded one item ahead
         auto load_dt = [&](int r, float (&v)[K]) {
-            const int t = t0 + (nch - 1 - r) * Q;
+            const int t = t0 + (kRev ? r : nch - 1 - r) * Q;
             const bool ok = r < nch && t + i < t1;
             const float* dp = a.dt + ((size_t)b * a.L + t + i) * a.H + h0;
             if constexpr (K == 4) {
@@ -225,7 +233,7 @@ __global__ void __launch_bounds__(kThreads, 1) ssd_split_agg_tc(const __grid_con
         load_dt(X, dtn);
         for (int r = X; r < nch; r += 2) {
             const int j = r >> 1;
-            const int t = t0 + (nch - 1 - r) * Q;
+            const int t = t0 + (kRev ? r : nch - 1 - r) * Q;
             const bool valid = t + i < t1;
             float dtv[K];
 #pragma unroll
@@ -233,7 +241,9 @@ __global__ void __launch_bounds__(kThreads, 1) ssd_split_agg_tc(const __grid_con
             load_dt(r + 2, dtn);
             bool start = false;   // a document starts at this token (after the first)
             if (kDocs && valid) {
-                while (doc > 0 && __ldg(a.cu + doc) > t + i) --doc;
+                if (kRev) doc = find_doc_agg(a.cu, a.ndocs, (int64_t)t + i);   // (chunks forwards)
+                else
+                    while (doc > 0 && __ldg(a.cu + doc) > t + i) --doc;
                 start = doc > 0 && __ldg(a.cu + doc) == t + i;
             }
 #pragma unroll
@@ -253,11 +263,13 @@ __global__ void __launch_bounds__(kThreads, 1) ssd_split_agg_tc(const __grid_con
                 for (int h = 0; h < K; ++h) w0[h] = rows[h].wl[0];
             }
             ptx::named_bar(nb, 128);
+            float pe[K];   // 2^{p_i}: the row prefix (reverse mode's weight)
 #pragma unroll
             for (int h = 0; h < K; ++h) {
                 SegsumLinRow<4> row;
                 row.wl[0] = w0[h];
                 segsum_lin_phase2<4>(sh.seg[X][h], row, rb, lane);
+                pe[h] = row.pe;
             }
             ptx::named_bar(nb, 128);
             // the product of the later chunks' totals (from the other group); as soon
@@ -280,7 +292,7 @@ __global__ void __launch_bounds__(kThreads, 1) ssd_split_agg_tc(const __grid_con
             uint8_t* xs = sm + st * Cfg::kStage + kTileB;
 #pragma unroll
             for (int h = 0; h < K; ++h) {
-                const float wgt = segsum_lin_suffix<4>(sh.seg[X][h], i) * R[h] * dtv[h];
+                const float wgt = kRev ? pe[h] * R[h] : segsum_lin_suffix<4>(sh.seg[X][h], i) * R[h] * dtv[h];
                 const uint64_t wgt2 = ptx::f2_pack(wgt, wgt);
                 uint8_t* row = xs + h * kTileX;
                 uint4 v[8];   // the whole row's loads in flight before the first multiply
@@ -332,7 +344,7 @@ __global__ void __launch_bounds__(kThreads, 1) ssd_split_agg_tc(const __grid_con
                     // documents: the first document's, d = 0 = b; a later start in the
                     // split makes its decay 2^{-inf} = 0)
                     const float* init =
-                        (s == 0 && a.init) ? a.init + ((size_t)b * a.H + h0 + h) * PN + i : nullptr;
+                        (!kRev && s == 0 && a.init) ? a.init + ((size_t)b * a.H + h0 + h) * PN + i : nullptr;
                     if (init) {
                         // (read-only loads, so that all of them are issued before the stores)
                         const float dec = ex2_approx(lsum);
@@ -348,7 +360,7 @@ __global__ void __launch_bounds__(kThreads, 1) ssd_split_agg_tc(const __grid_con
                         out[(size_t)p * N] = __uint_as_float(d0[p]);
                         out[(size_t)(p + 32) * N] = __uint_as_float(d1[p]);
                     }
-                    if (mt == 0) a.ws_tau[ws] = lsum * kLn2;
+                    if (mt == 0) a.ws_tau[ws] = lsum * kLn2;   // (reverse mode: its own tau array)
                 }
             }
         }
@@ -359,7 +371,7 @@ __global__ void __launch_bounds__(kThreads, 1) ssd_split_agg_tc(const __grid_con
     if (warp == 2) ptx::tmem_dealloc(tb, Cfg::kCols);
 }
 
-template <int K, bool kDocs>
+template <int K, bool kDocs, bool kRev>
 cudaError_t launch_k(const AggParams& prm, int64_t grid, cudaStream_t st) {
     static std::atomic<uint8_t> ready[kMaxDevices];
     int dev = 0;
@@ -367,13 +379,33 @@ cudaError_t launch_k(const AggParams& prm, int64_t grid, cudaStream_t st) {
     if (e != cudaSuccess) return e;
     if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
     if (!ready[dev].load(std::memory_order_acquire)) {
-        e = cudaFuncSetAttribute(ssd_split_agg_tc<K, kDocs>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+        e = cudaFuncSetAttribute(ssd_split_agg_tc<K, kDocs, kRev>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                  (int)AggCfg<K>::kSmem);
         if (e != cudaSuccess) return e;
         ready[dev].store(1, std::memory_order_release);
     }
-    ssd_split_agg_tc<K, kDocs><<<(unsigned)grid, kThreads, AggCfg<K>::kSmem, st>>>(prm);
+    ssd_split_agg_tc<K, kDocs, kRev><<<(unsigned)grid, kThreads, AggCfg<K>::kSmem, st>>>(prm);
     return cudaGetLastError();
+}
+
+template <bool kRev>
+cudaError_t launch_agg(const FwdArgs& a, cudaStream_t st) {
+    AggParams prm;
+    memset(&prm, 0, sizeof(prm));
+    prm.a = a;
+    if (prm.a.wait_iters == 0) prm.a.wait_iters = kDefaultWaitIters;
+    // forwards: splits 0 .. nsplit - 2 (the last split's aggregate is never composed
+    // into a later split); reverse: splits 1 .. nsplit - 1 (nothing enters split 0's
+    // left side)
+    prm.nsplit_agg = a.nsplit - 1;
+    if (prm.nsplit_agg < 1) return cudaSuccess;
+    if (!encode_4d(&prm.tm_x, a.x, P, a.H, a.L, a.batch) || !encode_4d(&prm.tm_B, a.B, N, a.G, a.L, a.batch))
+        return cudaErrorInvalidValue;
+    const int K = agg_heads_per_cta(a.H, a.G);
+    const int64_t grid = a.batch * (int64_t)prm.nsplit_agg * (a.H / K);
+    const bool docs = a.cu != nullptr;
+    if (K == 2) return docs ? launch_k<2, true, kRev>(prm, grid, st) : launch_k<2, false, kRev>(prm, grid, st);
+    return docs ? launch_k<1, true, kRev>(prm, grid, st) : launch_k<1, false, kRev>(prm, grid, st);
 }
 
 }  // namespace
@@ -385,20 +417,11 @@ int agg_heads_per_cta(int H, int G) {
     return (hg % 2 == 0) ? 2 : 1;
 }
 
-cudaError_t launch_agg_tc(const FwdArgs& a, cudaStream_t st) {
-    AggParams prm;
-    memset(&prm, 0, sizeof(prm));
-    prm.a = a;
-    if (prm.a.wait_iters == 0) prm.a.wait_iters = kDefaultWaitIters;
-    prm.nsplit_agg = a.nsplit - 1;   // the last split's aggregate is never composed into a later split
-    if (prm.nsplit_agg < 1) return cudaSuccess;
-    if (!encode_4d(&prm.tm_x, a.x, P, a.H, a.L, a.batch) || !encode_4d(&prm.tm_B, a.B, N, a.G, a.L, a.batch))
-        return cudaErrorInvalidValue;
-    const int K = agg_heads_per_cta(a.H, a.G);
-    const int64_t grid = a.batch * (int64_t)prm.nsplit_agg * (a.H / K);
-    const bool docs = a.cu != nullptr;
-    if (K == 2) return docs ? launch_k<2, true>(prm, grid, st) : launch_k<2, false>(prm, grid, st);
-    return docs ? launch_k<1, true>(prm, grid, st) : launch_k<1, false>(prm, grid, st);
-}
+cudaError_t launch_agg_tc(const FwdArgs& a, cudaStream_t st) { return launch_agg<false>(a, st); }
+
+// The reverse aggregates V_s of the backward pass: a.x = dy, a.B = C,
+// a.ws_state the slots (split s in slot s of its (row, head)) and a.ws_tau the
+// splits' total log-decays (split s at s, for s >= 1).
+cudaError_t launch_agg_rev_tc(const FwdArgs& a, cudaStream_t st) { return launch_agg<true>(a, st); }
 
 }  // namespace ssd

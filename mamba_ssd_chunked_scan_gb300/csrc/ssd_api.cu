@@ -174,7 +174,11 @@ WsLayout layout_for(const ssd_params_t* p, int ns, const TailPlan& tp) {
 struct BwdLayout {
     int Qb = 0;
     bool tc = false;
-    size_t ckpt = 0, cmap = 0, dB = 0, dC = 0, dA = 0, dD = 0, total = 0;
+    int nsplit = 1;            // sequence splits of the tensor-core backward
+    int64_t split_len = 0;
+    size_t ckpt = 0, cmap = 0, dB = 0, dC = 0, dA = 0, dD = 0;
+    size_t tau_f = 0, tau_r = 0, sin = 0, lam = 0;   // split aggregates, forwards and reverse
+    size_t total = 0;
 };
 
 // The backward runs on the tensor cores for the bf16 Mamba-2 head shape, except
@@ -197,13 +201,36 @@ bool bwd_layout(const ssd_params_t* p, bool doc_states, BwdLayout* l) {
     // per-head shares of dB and dC: bf16 from the tensor-core backward, else fp32
     const size_t share_elem = l->tc ? 2 : 4;
     const size_t share = (size_t)p->batch * p->seqlen * p->nheads * p->dstate;
+    // the tensor-core backward splits sequences when rows x heads leave SMs idle,
+    // with the forward pass's automatic plan at its 128-token chunk; splits are
+    // 4 chunks at least (the split aggregates' tensor-core kernel)
+    l->nsplit = 1;
+    l->split_len = p->seqlen;
+    if (l->tc) {
+        ssd_params_t q = *p;
+        q.chunk = kBwdTcChunk;
+        if (q.split_len > 0) q.split_len = (int32_t)((q.split_len + kBwdTcChunk - 1) / kBwdTcChunk * kBwdTcChunk);
+        int64_t sl = plan_split_len(&q);
+        if (sl < 4 * kBwdTcChunk) sl = 4 * kBwdTcChunk;
+        if (sl < p->seqlen) {
+            l->split_len = sl;
+            l->nsplit = (int)((p->seqlen + sl - 1) / sl);
+        }
+    }
+    const size_t ns = (size_t)l->nsplit;
     size_t o = sizeof(WsHeader);
     l->ckpt = o;  o = align_up(o + bh * nch * PN * sizeof(float), 256);
     l->cmap = o;  o = align_up(o + (l->tc ? 0 : bh * nch * 2 * sizeof(int)), 256);
     l->dB = o;    o = align_up(o + share * share_elem, 256);
     l->dC = o;    o = align_up(o + share * share_elem, 256);
-    l->dA = o;    o = align_up(o + bh * sizeof(float), 256);
-    l->dD = o;    o = align_up(o + bh * sizeof(float), 256);
+    l->dA = o;    o = align_up(o + bh * ns * sizeof(float), 256);
+    l->dD = o;    o = align_up(o + bh * ns * sizeof(float), 256);
+    if (ns > 1) {
+        l->tau_f = o;  o = align_up(o + bh * ns * sizeof(float), 256);
+        l->tau_r = o;  o = align_up(o + bh * ns * sizeof(float), 256);
+        l->sin = o;    o = align_up(o + bh * ns * PN * sizeof(float), 256);
+        l->lam = o;    o = align_up(o + bh * ns * PN * sizeof(float), 256);
+    }
     l->total = o;
     return true;
 }
@@ -539,9 +566,41 @@ int ssd_bwd(const ssd_params_t* p, const void* x, const float* dt, const float* 
     a.ws = (WsHeader*)ws;
     a.wait_iters = kDefaultWaitIters;
     a.shares_bf16 = l.tc ? 1 : 0;
+    a.nsplit = l.nsplit;
+    a.split_len = l.split_len;
+    a.ws_sin = (const float*)(ws + l.sin);
+    a.ws_lam = (const float*)(ws + l.lam);
     // a fresh status word for this call's bounded device waits
-    if (cudaMemsetAsync(ws, 0, sizeof(WsHeader), (cudaStream_t)stream) != cudaSuccess) return SSD_ERR_CUDA;
-    if ((l.tc ? launch_bwd_tc(a, (cudaStream_t)stream) : launch_bwd(a, (cudaStream_t)stream)) != cudaSuccess)
+    cudaStream_t st = (cudaStream_t)stream;
+    if (cudaMemsetAsync(ws, 0, sizeof(WsHeader), st) != cudaSuccess) return SSD_ERR_CUDA;
+    if (l.nsplit > 1) {
+        // the state entering each split (the forward pass's split aggregates and
+        // their composition), then the adjoint leaving each split (the reverse
+        // aggregates V_s = sum 2^{P_i} dy_i C_i^T and their composition from dfin)
+        FwdArgs f;
+        memset(&f, 0, sizeof(f));
+        f.batch = p->batch; f.L = p->seqlen;
+        f.H = p->nheads; f.P = p->headdim; f.N = p->dstate; f.G = p->ngroups;
+        f.Q = kBwdTcChunk;
+        f.dtype = p->dtype;
+        f.x = x; f.dt = dt; f.A = A; f.B = B; f.C = C; f.D = D; f.init = init;
+        f.cu = cu; f.ndocs = p->ndocs;
+        f.mode = kModeAggregate;
+        f.split_len = l.split_len;
+        f.nsplit = l.nsplit;
+        f.ws = (WsHeader*)ws;
+        f.wait_iters = kDefaultWaitIters;
+        f.ws_tau = (float*)(ws + l.tau_f);
+        f.ws_state = (float*)(ws + l.sin);
+        if (launch_agg_tc(f, st) != cudaSuccess || launch_split_scan(f, st) != cudaSuccess) return SSD_ERR_CUDA;
+        FwdArgs r = f;
+        r.x = dy; r.B = C; r.init = nullptr;
+        r.ws_tau = (float*)(ws + l.tau_r);
+        r.ws_state = (float*)(ws + l.lam);
+        if (launch_agg_rev_tc(r, st) != cudaSuccess || launch_split_rscan(r, dfin, st) != cudaSuccess)
+            return SSD_ERR_CUDA;
+    }
+    if ((l.tc ? launch_bwd_tc(a, st) : launch_bwd(a, st)) != cudaSuccess)
         return SSD_ERR_CUDA;
     return SSD_OK;
 }

@@ -729,10 +729,12 @@ __global__ void __launch_bounds__(256) ssd_bwd_reduce(BwdArgs a) {
     if (blockIdx.x == 0) {
         for (int h = threadIdx.x; h < a.H; h += blockDim.x) {
             float sa = 0.f, sd = 0.f;
-            for (int64_t b = 0; b < a.batch; ++b) {
-                sa += a.ws_dA[b * a.H + h];
-                sd += a.ws_dD[b * a.H + h];
-            }
+            const int ns = a.nsplit > 0 ? a.nsplit : 1;   // (one share per unit: row, head, split)
+            for (int64_t b = 0; b < a.batch; ++b)
+                for (int sp = 0; sp < ns; ++sp) {
+                    sa += a.ws_dA[(b * a.H + h) * ns + sp];
+                    sd += a.ws_dD[(b * a.H + h) * ns + sp];
+                }
             a.dA[h] = sa;
             if (a.dD) a.dD[h] = sd;
         }

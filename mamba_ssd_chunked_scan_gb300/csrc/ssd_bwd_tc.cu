@@ -192,14 +192,24 @@ __global__ void __launch_bounds__(kThreads, 1) ssd_bwd_tc(const __grid_constant_
     const BwdArgs& a = prm.a;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const uint32_t s0 = ptx::smem_u32(sm);
-    const int64_t unit = blockIdx.x;   // b * H + h
-    const int h = (int)(unit % a.H);
-    const int b = (int)(unit / a.H);
+    // unit = (b * H + h) * nsplit + s: split s of row b, head h.  A split enters
+    // from the state the forward pass's split scan left in ws_sin (split 0: the
+    // initial state) and leaves with the adjoint the reverse scan left in ws_lam
+    // (the last split: dfin)
+    const int64_t unit = blockIdx.x;
+    const int nsplit = a.nsplit > 0 ? a.nsplit : 1;
+    const int s = (int)(unit % nsplit);
+    const int64_t bh = unit / nsplit;
+    const int h = (int)(bh % a.H);
+    const int b = (int)(bh / a.H);
     const int g = h / (a.H / a.G);
     const int64_t L = a.L;
-    const int nch = (int)((L + Q - 1) / Q);
+    const int nch_all = (int)((L + Q - 1) / Q);
+    const int cps = nsplit > 1 ? (int)(a.split_len / Q) : nch_all;   // chunks per split
+    const int c0 = s * cps;                                          // this split's first chunk
+    const int nch = (c0 + cps < nch_all ? c0 + cps : nch_all) - c0;  // and its chunks (local c = 0 ..)
     const size_t PN = (size_t)P * N;
-    float* ckpt = a.ws_ckpt + (size_t)unit * nch * PN;
+    float* ckpt = a.ws_ckpt + ((size_t)bh * nch_all + c0) * PN;
 
     if (threadIdx.x == 0) {
         ptx::mbar_init(&sh.full, 1);
@@ -249,7 +259,7 @@ __global__ void __launch_bounds__(kThreads, 1) ssd_bwd_tc(const __grid_constant_
                 uint64_t* bar = st ? &sh.full1 : &sh.full;
                 uint8_t* xt = sm + (st ? kTSin : kTX);
                 uint8_t* bt = sm + (st ? kT1 : kTB);
-                const int t0 = c * Q;
+                const int t0 = (c0 + c) * Q;
                 ptx::mbar_expect_tx(bar, 16384u + 32768u);
                 ptx::tma_load_4d(xt, &prm.tm_x, bar, 0, h, t0, b);
                 ptx::tma_load_4d(bt, &prm.tm_B, bar, 0, g, t0, b);
@@ -257,7 +267,7 @@ __global__ void __launch_bounds__(kThreads, 1) ssd_bwd_tc(const __grid_constant_
             };
             auto load2 = [&](int c) {         // phase 2: x, dy, B and C of chunk c; chunk c - 1 towards L2
                 ++nissue[0];
-                const int t0 = c * Q;
+                const int t0 = (c0 + c) * Q;
                 ptx::mbar_expect_tx(&sh.full, 16384u * 2u + 32768u * 2u);
                 ptx::tma_load_4d(sm + kTX, &prm.tm_x, &sh.full, 0, h, t0, b);
                 ptx::tma_load_4d(sm + kTDY, &prm.tm_dy, &sh.full, 0, h, t0, b);
@@ -298,7 +308,7 @@ __global__ void __launch_bounds__(kThreads, 1) ssd_bwd_tc(const __grid_constant_
             if (nch > 0 && !*(volatile int*)&sh.abort) load2(nch - 1);
             for (int k = 0; k < nch && !*(volatile int*)&sh.abort; ++k) {
                 const int c = nch - 1 - k;
-                const int t0 = c * Q;
+                const int t0 = (c0 + c) * Q;
                 if (!wait_bar(sh, a, &sh.full, ndone[0] & 1, kWhereLoad)) break;
                 ++ndone[0];
                 // TMEM free: the last chunk's shares (or phase 1's state summaries) are read
@@ -422,11 +432,16 @@ __global__ void __launch_bounds__(kThreads, 1) ssd_bwd_tc(const __grid_constant_
         // cores; then S (the state entering chunk c) is updated and kept.
         float S[32];   // S^T[n = r][p], this half's p
 #pragma unroll
-        for (int p = 0; p < 32; ++p) S[p] = a.init ? a.init[unit * PN + (size_t)(32 * hf + p) * N + r] : 0.f;
+        {
+            const float* s_in = s > 0 ? a.ws_sin + ((size_t)bh * nsplit + s - 1) * PN
+                                      : (a.init ? a.init + (size_t)bh * PN : nullptr);
+#pragma unroll
+            for (int p = 0; p < 32; ++p) S[p] = s_in ? s_in[(size_t)(32 * hf + p) * N + r] : 0.f;
+        }
         float etau_prev = 0.f;
-        float d1_next = dt_at(r);
+        float d1_next = dt_at((int64_t)c0 * Q + r);   // (the split's first chunk)
         for (int c = 0; c < nch; ++c) {
-            const int64_t t0 = (int64_t)c * Q;
+            const int64_t t0 = (int64_t)(c0 + c) * Q;
             const float d = d1_next;   // (loaded a chunk earlier)
             decays(d, t0 + r < L && doc_start_tc(a, t0 + r));
             d1_next = c + 1 < nch ? dt_at(t0 + Q + r) : 0.f;
@@ -464,14 +479,18 @@ __global__ void __launch_bounds__(kThreads, 1) ssd_bwd_tc(const __grid_constant_
 
         // ------------------------------------------------------------ phase 2
         // Lam^T (lane n, column p) lives in TMEM: each chunk scales it by 2^tau in
-        // place and the update contraction accumulates onto it
+        // place and the update contraction accumulates onto it.  It starts as the
+        // adjoint of the state leaving this split: dfin for the last split, else
+        // the reverse scan's slot s + 1
         {
+            const float* lam_out = s + 1 < nsplit ? a.ws_lam + ((size_t)bh * nsplit + s + 1) * PN
+                                                  : (a.dfin ? a.dfin + (size_t)bh * PN : nullptr);
             uint32_t v[16];
 #pragma unroll
             for (int q = 0; q < 2; ++q) {
 #pragma unroll
                 for (int e = 0; e < 16; ++e)
-                    v[e] = __float_as_uint(a.dfin ? a.dfin[unit * PN + (size_t)(32 * hf + 16 * q + e) * N + r] : 0.f);
+                    v[e] = __float_as_uint(lam_out ? lam_out[(size_t)(32 * hf + 16 * q + e) * N + r] : 0.f);
                 ptx::tmem_st16(lane_addr + kTmLU + 32 * hf + 16 * q, v);
             }
             ptx::tmem_st_wait();
@@ -530,10 +549,10 @@ __global__ void __launch_bounds__(kThreads, 1) ssd_bwd_tc(const __grid_constant_
                 dD_acc += ddv;
             }
         };
-        float d_next = nch > 0 ? dt_at((int64_t)(nch - 1) * Q + r) : 0.f;
+        float d_next = nch > 0 ? dt_at((int64_t)(c0 + nch - 1) * Q + r) : 0.f;
         for (int k = 0; k < nch; ++k) {
             const int c = nch - 1 - k;
-            const int64_t t0 = (int64_t)c * Q;
+            const int64_t t0 = (int64_t)(c0 + c) * Q;
             const bool valid = t0 + r < L;
             const float d = d_next;   // (loaded a chunk earlier)
             const bool start = valid && doc_start_tc(a, t0 + r);
@@ -756,13 +775,13 @@ __global__ void __launch_bounds__(kThreads, 1) ssd_bwd_tc(const __grid_constant_
         }
         if (nch > 0 && !*(volatile int*)&sh.abort) token_pass(prev, (nch - 1) & 1);
         // ---- the adjoint of the initial state; this unit's dA and dD shares
-        if (a.dinit && !*(volatile int*)&sh.abort) {
+        if (a.dinit && s == 0 && !*(volatile int*)&sh.abort) {
             wait_bar(sh, a, &sh.mmaLU, (nch - 1) & 1, kWhereDC);
             ptx::tc_fence_after();
             uint32_t l0[32];
             ptx::tmem_load32(lane_addr + kTmLU + 32 * hf, l0);
 #pragma unroll
-            for (int p = 0; p < 32; ++p) a.dinit[unit * PN + (size_t)(32 * hf + p) * N + r] = __uint_as_float(l0[p]);
+            for (int p = 0; p < 32; ++p) a.dinit[bh * PN + (size_t)(32 * hf + p) * N + r] = __uint_as_float(l0[p]);
         }
         dA_acc = warp_sum(dA_acc);
         dD_acc = warp_sum(dD_acc);
@@ -813,7 +832,7 @@ cudaError_t launch_bwd_tc(const BwdArgs& a, cudaStream_t st) {
         if (fa.numRegs * (kThreads / 128) < kRegsIssue + 2 * kRegsCompute) return cudaErrorInvalidConfiguration;
         ready[dev].store(1, std::memory_order_release);
     }
-    ssd_bwd_tc<<<(unsigned)(a.batch * a.H), kThreads, kSmemBytes, st>>>(prm);
+    ssd_bwd_tc<<<(unsigned)(a.batch * a.H * (a.nsplit > 0 ? a.nsplit : 1)), kThreads, kSmemBytes, st>>>(prm);
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
     return launch_bwd_reduce(a, st);
 }

@@ -103,6 +103,12 @@ struct BwdArgs {
     float* ws_dA;          // [batch * H]
     float* ws_dD;          // [batch * H]
     WsHeader* ws;          // status word (the tensor-core kernel's bounded waits)
+    // sequence splits of the tensor-core backward (nsplit 1: whole rows); units are
+    // (b * H + h) * nsplit + s, and ws_dA / ws_dD hold one share per unit
+    int nsplit;
+    int64_t split_len;     // tokens per split, a multiple of 128
+    const float* ws_sin;   // [batch * H * nsplit * P * N] slot s - 1: the state entering split s
+    const float* ws_lam;   // [batch * H * nsplit * P * N] slot s + 1: the adjoint of the state leaving split s
     uint32_t wait_iters;   // poll cap of each bounded wait (0: the default)
 };
 
@@ -149,6 +155,8 @@ cudaError_t launch_tc(const FwdArgs& a, cudaStream_t st);
 cudaError_t launch_doc_init_agg(const FwdArgs& a, cudaStream_t st);
 int agg_heads_per_cta(int H, int G);
 cudaError_t launch_agg_tc(const FwdArgs& a, cudaStream_t st);
+cudaError_t launch_agg_rev_tc(const FwdArgs& a, cudaStream_t st);
+cudaError_t launch_split_rscan(const FwdArgs& a, const float* dfin, cudaStream_t st);
 cudaError_t launch_gate_norm(const GateNormArgs& a, cudaStream_t st);
 size_t bwd_smem_bytes(int Qb, int P, int N);
 int bwd_chunk(int P, int N, size_t smem_limit);

@@ -301,6 +301,61 @@ __global__ void ssd_split_scan(const float* __restrict__ tau, float* __restrict_
     }
 }
 
+// Reverse composition for the backward pass's splits: the adjoint of the state
+// leaving split s, Lam_out(s) = e^{tau_{s+1}} Lam_out(s + 1) + V_{s+1}, from
+// Lam_out(nsplit - 1) = dfin (or zero).  In place: slot s + 1 (V_{s+1})
+// receives Lam_out(s), for s = nsplit - 2 down to 0.  tau: the splits' totals
+// (split s at s).  The loads of the next kScanDepth slots are in flight while
+// the current ones are combined.
+__global__ void ssd_split_rscan(const float* __restrict__ tau, float* __restrict__ state,
+                                const float* __restrict__ dfin, int64_t units_bh, int nsplit, int PN) {
+    const int PN4 = PN >> 2;
+    const int64_t k = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+    if (nsplit < 2 || k >= units_bh * PN4) return;
+    const int64_t bh = k / PN4;
+    const int e4 = (int)(k % PN4);
+    float4* st = reinterpret_cast<float4*>(state) + bh * nsplit * (int64_t)PN4 + e4;
+    const float* tu = tau + bh * nsplit;
+    float4 run = dfin ? reinterpret_cast<const float4*>(dfin)[bh * PN4 + e4] : make_float4(0.f, 0.f, 0.f, 0.f);
+    float4 cur[kScanDepth];
+    float ct[kScanDepth];
+#pragma unroll
+    for (int d = 0; d < kScanDepth; ++d) {
+        const int sn = nsplit - 1 - d;   // slots nsplit - 1, nsplit - 2, ..., 1
+        if (sn >= 1) {
+            cur[d] = st[(int64_t)sn * PN4];
+            ct[d] = tu[sn];
+        }
+    }
+    for (int s0 = nsplit - 1; s0 >= 1; s0 -= kScanDepth) {
+        float4 nxt[kScanDepth];
+        float nt[kScanDepth];
+#pragma unroll
+        for (int d = 0; d < kScanDepth; ++d) {
+            const int sn = s0 - kScanDepth - d;
+            if (sn >= 1) {
+                nxt[d] = st[(int64_t)sn * PN4];
+                nt[d] = tu[sn];
+            }
+        }
+#pragma unroll
+        for (int d = 0; d < kScanDepth; ++d) {
+            const int sc = s0 - d;
+            if (sc >= 1) {
+                const float e = expf(ct[d]);
+                run = make_float4(fmaf(e, run.x, cur[d].x), fmaf(e, run.y, cur[d].y), fmaf(e, run.z, cur[d].z),
+                                  fmaf(e, run.w, cur[d].w));
+                st[(int64_t)sc * PN4] = run;   // Lam_out(sc - 1)
+            }
+        }
+#pragma unroll
+        for (int d = 0; d < kScanDepth; ++d) {
+            cur[d] = nxt[d];
+            ct[d] = nt[d];
+        }
+    }
+}
+
 // Both forms of the segsum routine on rows of log2-decays: the log-domain
 // seg the SIMT kernel exponentiates, and the linear-domain mask, row prefix
 // and column suffix factors the tensor-core kernel multiplies in (the same
@@ -360,6 +415,15 @@ cudaError_t launch_simt(const FwdArgs& a, cudaStream_t st) {
         return a.Q == 128 ? launch_simt_q<__nv_bfloat16, 4>(a, smem, grid, st)
                           : launch_simt_q<__nv_bfloat16, 2>(a, smem, grid, st);
     return a.Q == 128 ? launch_simt_q<float, 4>(a, smem, grid, st) : launch_simt_q<float, 2>(a, smem, grid, st);
+}
+
+cudaError_t launch_split_rscan(const FwdArgs& a, const float* dfin, cudaStream_t st) {
+    const int PN = a.P * a.N;
+    const int64_t total = a.nsplit > 1 ? a.batch * a.H * (int64_t)(PN / 4) : 1;
+    const int threads = 256;
+    ssd_split_rscan<<<(unsigned)((total + threads - 1) / threads), threads, 0, st>>>(
+        a.ws_tau, a.ws_state, dfin, a.batch * a.H, a.nsplit, PN);
+    return cudaGetLastError();
 }
 
 cudaError_t launch_split_scan(const FwdArgs& a, cudaStream_t st) {

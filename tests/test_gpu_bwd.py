@@ -31,7 +31,7 @@ def cotangents(p, seed, with_dfin=True):
     return dy, dfin
 
 
-def run_bwd(p, dy, dfin):
+def run_bwd(p, dy, dfin, split_len=0):
     d = to_device(p)
     if p.dtype == "bf16":
         dyt = torch.from_numpy(synth.bf16_bits(dy).view(np.int16).copy()).cuda().view(torch.bfloat16)
@@ -39,15 +39,15 @@ def run_bwd(p, dy, dfin):
         dyt = torch.from_numpy(dy).cuda()
     dft = None if dfin is None else torch.from_numpy(dfin).cuda()
     g = ssd.ssd_bwd(d["x"], d["dt"], d["A"], d["B"], d["C"], dyt, d["D"], d["init"], dft, d["cu"],
-                    check_status=True)
+                    split_len=split_len, check_status=True)
     torch.cuda.synchronize()
     return {k: (None if v is None else v.float().cpu().numpy().astype(np.float64)) for k, v in g.items()}
 
 
-def check(p, seed=1, with_dfin=True):
+def check(p, seed=1, with_dfin=True, split_len=0):
     dy, dfin = cotangents(p, seed, with_dfin)
     want = oracle.ssd_backward(p, dy, dfin)
-    got = run_bwd(p, dy, dfin)
+    got = run_bwd(p, dy, dfin, split_len)
     tol = BWD_TOL[p.dtype]
     for k in ("dx", "ddt", "dA", "dB", "dC", "dD", "dinit"):
         if want[k] is None or got[k] is None:
@@ -152,3 +152,30 @@ def test_bwd_tensor_core_shapes(kw):
     p = synth.make_problem(headdim=64, dstate=128, chunk=128, dtype="bf16", seed=313, init_std=0.3, **kw)
     got = check(p)
     assert got["dinit"] is not None
+
+
+@pytest.mark.parametrize("split_len", [512, 1024, 0])
+@pytest.mark.parametrize("kw", [
+    dict(batch=1, seqlen=4096, nheads=4, ngroups=1),                    # one row in splits
+    dict(batch=2, seqlen=1000, nheads=2, ngroups=1, init_std=0.3),      # ragged last split, initial states
+    dict(batch=1, seqlen=2048, nheads=2, ngroups=2, dt_dist="softplus_n22", init_std=0.3),   # strong decay
+])
+def test_bwd_sequence_splits(kw, split_len):
+    """The tensor-core backward over sequence splits: each split enters from the
+    state the forward pass's split scan composes and leaves with the adjoint a
+    reverse scan composes from dfin (the reverse aggregates: the same
+    contraction with C, dy and prefix decays); the splits run in parallel."""
+    p = synth.make_problem(headdim=64, dstate=128, chunk=128, dtype="bf16", seed=319, **kw)
+    check(p, split_len=split_len)
+
+
+@pytest.mark.parametrize("lens", [
+    [700, 1, 1200, 300, 1895],     # starts inside splits
+    [512, 512, 3072],              # starts on split boundaries (split 512)
+])
+def test_bwd_sequence_splits_packed_documents(lens):
+    """Packed documents (from zero states) over sequence splits: the -inf decay
+    of a start also cuts the composed states and adjoints at split boundaries."""
+    p = synth.make_problem(batch=1, seqlen=sum(lens), nheads=4, headdim=64, dstate=128, ngroups=2, chunk=128,
+                           dtype="bf16", seed=321, doc_lengths=lens)
+    check(p, with_dfin=False, split_len=512)
