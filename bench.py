@@ -88,6 +88,8 @@ def workload(name: str):
     if name.startswith("decode"):
         parts = name.split(":")
         return synth.config_decode(int(parts[1]) if len(parts) > 1 else 256)
+    if name == "bwd_long":
+        return synth.config_long()
     if name.startswith("bwd"):
         parts = name.split(":")
         return synth.config_27b(batch=int(parts[1]) if len(parts) > 1 else 8)

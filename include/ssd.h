@@ -180,7 +180,14 @@ SSD_API size_t ssd_bwd_workspace_size_doc_states(const ssd_params_t* p);
  * shape) runs on the tensor cores: chunks of 128 tokens, every contraction a
  * bf16 x bf16 -> fp32 MMA (the decay-masked Q x Q products, the adjoint and
  * the incoming state are rounded to bf16 as MMA operands; sums, scans and
- * the adjoint recurrence stay fp32).  Every other shape, and fp32, runs on
+ * the adjoint recurrence stay fp32).  When rows x heads leave SMs idle it
+ * cuts each sequence into splits that run in parallel ("GPU Hierarchy Meets
+ * Structured Matrices": the split-sequence algorithm, here for the adjoint
+ * too): the forward pass's split aggregates and their composition give the
+ * state entering each split, and reverse aggregates (sum of 2^{P_i} dy_i C_i^T
+ * over a split, P_i the log-decays from the split's start through i) composed
+ * from dfinal_states give the adjoint leaving it.  split_len in p sets the
+ * split (0: automatic; rounded up to a multiple of 128, at least 512).  Every other shape, and fp32, runs on
  * CUDA cores in fp32 (bf16 inputs widened, bf16 gradients rounded once at the
  * end).
  *
@@ -207,12 +214,14 @@ SSD_API size_t ssd_bwd_workspace_size_doc_states(const ssd_params_t* p);
  * final state receives dfinal_states[d], and dinitial_states[d] is the
  * gradient of initial_states[d].  headdim * dstate > 8192 and shapes whose
  * tiles do not fit in shared memory return SSD_ERR_UNSUPPORTED.
- * `chunk` and `split_len` in p are validated but do not change the result.
+ * `chunk` and `split_len` in p are validated; they change only the rounding.
  * `workspace`: at least ssd_bwd_workspace_size(p) bytes, or
  * ssd_bwd_workspace_size_doc_states(p) for packed documents with any of the
  * three states, 256-byte aligned (else SSD_ERR_WORKSPACE).  Asynchronous on `stream`; a status-word reset
- * and two launches.  The tensor-core path's device waits are bounded: one that
- * runs out records SSD_ERR_TIMEOUT (where codes 31-37) in the status word at
+ * and two launches (six with splits: the two aggregate passes and their
+ * compositions first).  The tensor-core path's device waits are bounded: one that
+ * runs out records SSD_ERR_TIMEOUT (where codes 31-39, or 21-26 from the
+ * split aggregates) in the status word at
  * the start of `workspace`, read by ssd_check_status(); the CUDA-core path has
  * no device waits.  Bitwise deterministic (fixed summation orders). */
 SSD_API int ssd_bwd(const ssd_params_t* p,
