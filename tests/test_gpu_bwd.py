@@ -179,3 +179,18 @@ def test_bwd_sequence_splits_packed_documents(lens):
     p = synth.make_problem(batch=1, seqlen=sum(lens), nheads=4, headdim=64, dstate=128, ngroups=2, chunk=128,
                            dtype="bf16", seed=321, doc_lengths=lens)
     check(p, with_dfin=False, split_len=512)
+
+
+def test_bwd_splits_agree_with_whole_rows_on_a_long_sequence():
+    """A sequence too long for the oracle: the split plan and whole rows
+    (split_len = L) give the same gradients within bf16 rounding of the bf16
+    outputs and fp32 rounding of the fp32 ones."""
+    p = synth.make_problem(batch=1, seqlen=16384, nheads=4, headdim=64, dstate=128, ngroups=1, chunk=128,
+                           dtype="bf16", seed=323, A_dist="exp", init_std=0.2)
+    dy, dfin = cotangents(p, 5)
+    split = run_bwd(p, dy, dfin, split_len=1024)
+    whole = run_bwd(p, dy, dfin, split_len=p.seqlen)
+    for k, tol in (("dx", 1e-2), ("dB", 1e-2), ("dC", 1e-2), ("ddt", 1e-4), ("dA", 1e-4), ("dD", 1e-4),
+                   ("dinit", 1e-4)):
+        e = rel_err(split[k], whole[k])
+        assert e <= tol, f"{k}: {e:.3e} > {tol}"
