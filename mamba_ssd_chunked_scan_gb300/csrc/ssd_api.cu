@@ -176,7 +176,8 @@ struct BwdLayout {
     bool tc = false;
     int nsplit = 1;            // sequence splits of the tensor-core backward
     int64_t split_len = 0;
-    size_t ckpt = 0, cmap = 0, dB = 0, dC = 0, dA = 0, dD = 0;
+    int shares = 1;            // dA / dD shares per (row, head): splits, or documents (CUDA cores)
+    size_t ckpt = 0, dB = 0, dC = 0, dA = 0, dD = 0;
     size_t tau_f = 0, tau_r = 0, sin = 0, lam = 0;   // split aggregates, forwards and reverse
     size_t total = 0;
 };
@@ -218,13 +219,14 @@ bool bwd_layout(const ssd_params_t* p, bool doc_states, BwdLayout* l) {
         }
     }
     const size_t ns = (size_t)l->nsplit;
+    // the CUDA-core kernel runs packed documents as (head, document) units
+    l->shares = l->tc ? l->nsplit : (p->ndocs > 0 ? p->ndocs : 1);
     size_t o = sizeof(WsHeader);
     l->ckpt = o;  o = align_up(o + bh * nch * PN * sizeof(float), 256);
-    l->cmap = o;  o = align_up(o + (l->tc ? 0 : bh * nch * 2 * sizeof(int)), 256);
     l->dB = o;    o = align_up(o + share * share_elem, 256);
     l->dC = o;    o = align_up(o + share * share_elem, 256);
-    l->dA = o;    o = align_up(o + bh * ns * sizeof(float), 256);
-    l->dD = o;    o = align_up(o + bh * ns * sizeof(float), 256);
+    l->dA = o;    o = align_up(o + bh * (size_t)l->shares * sizeof(float), 256);
+    l->dD = o;    o = align_up(o + bh * (size_t)l->shares * sizeof(float), 256);
     if (ns > 1) {
         l->tau_f = o;  o = align_up(o + bh * ns * sizeof(float), 256);
         l->tau_r = o;  o = align_up(o + bh * ns * sizeof(float), 256);
@@ -558,7 +560,6 @@ int ssd_bwd(const ssd_params_t* p, const void* x, const float* dt, const float* 
     a.dx = dx; a.ddt = ddt; a.dA = dA; a.dB = dB; a.dC = dC; a.dD = D ? dD : nullptr; a.dinit = dinit;
     char* ws = static_cast<char*>(workspace);
     a.ws_ckpt = (float*)(ws + l.ckpt);
-    a.ws_cmap = (int*)(ws + l.cmap);
     a.ws_dB = (float*)(ws + l.dB);
     a.ws_dC = (float*)(ws + l.dC);
     a.ws_dA = (float*)(ws + l.dA);
@@ -566,7 +567,7 @@ int ssd_bwd(const ssd_params_t* p, const void* x, const float* dt, const float* 
     a.ws = (WsHeader*)ws;
     a.wait_iters = kDefaultWaitIters;
     a.shares_bf16 = l.tc ? 1 : 0;
-    a.nsplit = l.nsplit;
+    a.nsplit = l.shares;   // (the reduction sums this many dA / dD shares per (row, head))
     a.split_len = l.split_len;
     a.ws_sin = (const float*)(ws + l.sin);
     a.ws_lam = (const float*)(ws + l.lam);

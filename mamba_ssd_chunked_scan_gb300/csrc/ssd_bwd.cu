@@ -27,12 +27,12 @@
 //   Lam  <- e^{tau} Lam + sum_i e^{p_i} dy_i C_i^T            (adjoint of S_in)
 // Every sum of log-decays is a direct sum (no prefix subtraction).
 //
-// Packed documents: no chunk straddles a document start (each document's
-// chunks begin at its start), so no state or adjoint crosses a boundary.  A
-// document's first chunk enters from the document's initial state (or zero)
-// and its start token's own decay applies to it; its last chunk leaves with
-// the document's final-state gradient (or zero) as Lam; the adjoint of its
-// first chunk's entering state is the initial state's gradient.
+// Packed documents are independent sequences (no state or adjoint crosses a
+// boundary), so each (head, document) is its own unit, walked in chunks from
+// the document's start: its first chunk enters from the document's initial
+// state (or zero) and its start token's own decay applies to it; its last
+// chunk leaves with the document's final-state gradient (or zero) as Lam; the
+// adjoint of its first chunk's entering state is the initial state's gradient.
 #include "ssd_common.cuh"
 #include "ssd_kernels.h"
 
@@ -175,25 +175,52 @@ __global__ void __launch_bounds__(kBwdThreads) ssd_bwd_chunk(BwdArgs a) {
     float* A2dtT = sm + L.A2dtT;
 
     const int tid = threadIdx.x;
-    const int64_t unit = blockIdx.x;               // b * H + h
-    const int h = (int)(unit % H);
-    const int64_t b = unit / H;
+    const int64_t Lseq = a.L;
+    const bool docs = a.cu != nullptr;
+    // units: (batch row, head) = b * H + h, or with packed documents (head,
+    // document) = h * ndocs + d (batch 1), documents being independent sequences
+    const int64_t unit = blockIdx.x;
+    const int h = (int)(docs ? unit / a.ndocs : unit % H);
+    const int d = docs ? (int)(unit % a.ndocs) : 0;
+    const int64_t b = docs ? 0 : unit / H;
     const int g = h / (H / G);
     const float Ah = a.A[h];
     const float Dh = a.D ? a.D[h] : 0.f;
-    const int64_t Lseq = a.L;
-    const bool docs = a.cu != nullptr;
-    // chunks per row at most: the Qb-token pieces, plus one per document boundary
-    const int nch_max = (int)((Lseq + Qb - 1) / Qb) + (docs ? a.ndocs : 0);
     const T* x = static_cast<const T*>(a.x);
     const T* Bg = static_cast<const T*>(a.B);
     const T* Cg = static_cast<const T*>(a.C);
     const T* dy = static_cast<const T*>(a.dy);
-    float* ckpt = a.ws_ckpt + (size_t)unit * nch_max * PN;
-    // chunk c: its first token, and (document << 2) | (ends its document << 1) | starts it
-    int* cmap = a.ws_cmap + (size_t)unit * nch_max * 2;
-    // the state index (of initial states, final-state gradients) of document d
-    auto sidx = [&](int d) -> size_t { return docs ? (size_t)d * H + h : (size_t)unit; };
+    // the unit's tokens [T0, T1): the row, or the document (offsets clamped to the row)
+    auto clamp_t = [&](int64_t v, int64_t lo) { return v < lo ? lo : (v > Lseq ? Lseq : v); };
+    int64_t T0 = 0, T1 = Lseq;
+    if (docs) {
+        T0 = clamp_t(__ldg(a.cu + d), 0);
+        T1 = clamp_t(__ldg(a.cu + d + 1), T0);
+    }
+    const int nchunks = (int)((T1 - T0 + Qb - 1) / Qb);
+    // chunk-entry states: ceil(L / Qb) (+ ndocs with documents) slots per row or, with
+    // documents, per head; a document's slots follow those of the documents before it
+    const int nch_max = (int)((Lseq + Qb - 1) / Qb) + (docs ? a.ndocs : 0);
+    int64_t off = 0;
+    if (docs) {
+        float part = 0.f;   // (chunk counts: integers, exact in fp32 below 2^24)
+        for (int k = tid; k < d; k += kBwdThreads) {
+            const int64_t s0 = clamp_t(__ldg(a.cu + k), 0), s1 = clamp_t(__ldg(a.cu + k + 1), s0);
+            part += (float)((s1 - s0 + Qb - 1) / Qb);
+        }
+        off = (int64_t)block_sum(part, sm + L.red);
+        if (unit == 0) check_cu_seqlens(a.cu, a.ndocs, Lseq, a.ws, tid, kBwdThreads);   // the call's offsets
+        if (off + nchunks > nch_max) {
+            // only offsets that break their contract (reported by the check above) get here
+            if (tid == 0) {
+                a.ws_dA[unit] = 0.f;
+                a.ws_dD[unit] = 0.f;
+            }
+            return;
+        }
+    }
+    float* ckpt = a.ws_ckpt + ((size_t)(docs ? h : unit) * nch_max + off) * PN;
+    const size_t si = docs ? (size_t)d * H + h : (size_t)unit;   // state index: initial states, dfin, dinit
 
     // token row k of this chunk: x / dy row, B / C row (zeros past the end)
     auto xrow = [&](int64_t t) { return x + ((size_t)(b * Lseq + t) * H + h) * P; };
@@ -203,36 +230,17 @@ __global__ void __launch_bounds__(kBwdThreads) ssd_bwd_chunk(BwdArgs a) {
     const int own_n = kT ? (tid & 127) : 0, own_p0 = kT ? (tid >> 7) * 8 : 0;
     auto own = [&](int r) -> int { return kT ? (own_p0 + r) * N + own_n : tid + kBwdThreads * r; };
 
-    if (docs && unit == 0) check_cu_seqlens(a.cu, a.ndocs, Lseq, a.ws, tid, kBwdThreads);   // the call's offsets
-
     // ------------------------------------------------------------ phase 1
     // forward over the chunks: the state entering each chunk, kept in the workspace
     float S[kBwdOwn];
-    int nchunks = 0;
-    int doc = 0;
-    bool first = true;   // the next chunk starts a document (or the row)
-    for (int64_t t0 = 0; t0 < Lseq && nchunks < nch_max;) {
-        // this chunk: up to Qb tokens, ending at the document's end
-        int64_t dend = Lseq;
-        if (docs && doc + 1 < a.ndocs) {
-            const int64_t nx = __ldg(a.cu + doc + 1);
-            dend = nx <= t0 ? t0 + 1 : (nx < Lseq ? nx : Lseq);   // (documents are not empty)
-        }
-        const int64_t t1 = (t0 + Qb < dend) ? t0 + Qb : dend;
-        const int c = nchunks++;
-        if (first) {
 #pragma unroll
-            for (int r = 0; r < kBwdOwn; ++r) {
-                const int e = own(r);
-                S[r] = (e < PN && a.init) ? a.init[sidx(doc) * PN + e] : 0.f;
-            }
-        }
-        if (tid == 0) {
-            cmap[2 * c] = (int)t0;
-            cmap[2 * c + 1] = (doc << 2) | (t1 == dend ? 2 : 0) | (first ? 1 : 0);
-        }
-        first = t1 == dend;
-        if (first) ++doc;
+    for (int r = 0; r < kBwdOwn; ++r) {
+        const int e = own(r);
+        S[r] = (e < PN && a.init) ? a.init[si * PN + e] : 0.f;
+    }
+    for (int c = 0; c < nchunks; ++c) {
+        const int64_t t0 = T0 + (int64_t)c * Qb;
+        const int64_t t1 = (t0 + Qb < T1) ? t0 + Qb : T1;
 #pragma unroll
         for (int r = 0; r < kBwdOwn; ++r) {
             const int e = own(r);
@@ -309,24 +317,20 @@ __global__ void __launch_bounds__(kBwdThreads) ssd_bwd_chunk(BwdArgs a) {
                 }
             }
         }
-        t0 = t1;
     }
 
     // ------------------------------------------------------------ phase 2
     // backward over the chunks, carrying Lam (the adjoint of the state leaving the chunk)
     float Lr[kBwdOwn];
+#pragma unroll
+    for (int r = 0; r < kBwdOwn; ++r) {
+        const int e = own(r);
+        Lr[r] = (e < PN && a.dfin) ? a.dfin[si * PN + e] : 0.f;   // the final state's adjoint
+    }
     float dA_acc = 0.f, dD_acc = 0.f;    // thread 0's running sums
     for (int c = nchunks - 1; c >= 0; --c) {
-        const int64_t t0 = cmap[2 * c];
-        const int64_t t1 = c + 1 < nchunks ? cmap[2 * (c + 1)] : Lseq;
-        const int info = cmap[2 * c + 1];
-        if (info & 2) {   // the chunk ends its document (or the row): the final-state gradient
-#pragma unroll
-            for (int r = 0; r < kBwdOwn; ++r) {
-                const int e = own(r);
-                Lr[r] = (e < PN && a.dfin) ? a.dfin[sidx(info >> 2) * PN + e] : 0.f;
-            }
-        }
+        const int64_t t0 = T0 + (int64_t)c * Qb;
+        const int64_t t1 = (t0 + Qb < T1) ? t0 + Qb : T1;
         __syncthreads();   // the previous chunk's shared-memory reads are done
         for (int k = tid; k < Qb * P; k += kBwdThreads) {
             const int i = k / P, p = k - i * P;
@@ -688,13 +692,13 @@ __global__ void __launch_bounds__(kBwdThreads) ssd_bwd_chunk(BwdArgs a) {
                 }
             }
         }
-        // the chunk starts its document (or the row): Lr is the initial state's gradient
-        if ((info & 1) && a.dinit) {
+    }
+    // Lr is the adjoint of the state entering the unit: the initial state's gradient
+    if (a.dinit) {
 #pragma unroll
-            for (int r = 0; r < kBwdOwn; ++r) {
-                const int e = own(r);
-                if (e < PN) a.dinit[sidx(info >> 2) * PN + e] = Lr[r];
-            }
+        for (int r = 0; r < kBwdOwn; ++r) {
+            const int e = own(r);
+            if (e < PN) a.dinit[si * PN + e] = Lr[r];
         }
     }
     if (tid == 0) {
@@ -763,7 +767,8 @@ cudaError_t launch_bwd(const BwdArgs& a, cudaStream_t st) {
                                   : (mamba_shape ? ssd_bwd_chunk<float, 64, 128, 32> : ssd_bwd_chunk<float, 0, 0, 0>);
     cudaError_t e = cudaFuncSetAttribute(k1, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
-    k1<<<(unsigned)(a.batch * a.H), kBwdThreads, smem, st>>>(a);
+    // (units: rows x heads, or heads x documents)
+    k1<<<(unsigned)(a.cu ? (int64_t)a.H * a.ndocs : a.batch * a.H), kBwdThreads, smem, st>>>(a);
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
     return launch_bwd_reduce(a, st);
 }

@@ -96,7 +96,6 @@ struct BwdArgs {
     float* dD;
     float* dinit;
     float* ws_ckpt;        // [batch * H * nchunks * P * N] state entering each chunk
-    int* ws_cmap;          // [batch * H * nchunks * 2] chunk starts and document flags (CUDA-core backward)
     float* ws_dB;          // [batch * L * H * N] per-head shares of dB (fp32, or bf16: shares_bf16)
     float* ws_dC;          // [batch * L * H * N] per-head shares of dC
     int shares_bf16;       // the shares are bf16 (the tensor-core backward)
@@ -104,7 +103,8 @@ struct BwdArgs {
     float* ws_dD;          // [batch * H]
     WsHeader* ws;          // status word (the tensor-core kernel's bounded waits)
     // sequence splits of the tensor-core backward (nsplit 1: whole rows); units are
-    // (b * H + h) * nsplit + s, and ws_dA / ws_dD hold one share per unit
+    // (b * H + h) * nsplit + s, and ws_dA / ws_dD hold one share per unit (the
+    // CUDA-core kernel with packed documents: nsplit = ndocs, units h * ndocs + d)
     int nsplit;
     int64_t split_len;     // tokens per split, a multiple of 128
     const float* ws_sin;   // [batch * H * nsplit * P * N] slot s - 1: the state entering split s
