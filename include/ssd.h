@@ -164,8 +164,9 @@ SSD_API size_t ssd_bwd_workspace_size(const ssd_params_t* p);
 
 /* Bytes of device workspace ssd_bwd() needs for packed documents (ndocs > 0)
  * when the call passes initial_states, dfinal_states or dinitial_states: that
- * call runs on CUDA cores with chunks of at most 32 tokens that start at every
- * document start, so its layout is larger than ssd_bwd_workspace_size(p).
+ * call runs on CUDA cores, one block per (head, document), with chunks of at
+ * most 32 tokens from each document's start, so its layout is larger than
+ * ssd_bwd_workspace_size(p).
  * 0 when the parameters are invalid, ndocs is 0 or the backward pass does not
  * support them. */
 SSD_API size_t ssd_bwd_workspace_size_doc_states(const ssd_params_t* p);
@@ -209,7 +210,8 @@ SSD_API size_t ssd_bwd_workspace_size_doc_states(const ssd_params_t* p);
  * gradient crosses a document boundary.  Without per-document states they
  * take the tensor-core path for its shape (a -inf log-decay at each document
  * start); with initial_states, dfinal_states or dinitial_states they run on
- * CUDA cores, whose chunks start at every document start: each document
+ * CUDA cores, one block per (head, document), walking the document's own
+ * chunks of at most 32 tokens from its start: each document
  * starts from its initial state (its first token's decay applied to it), its
  * final state receives dfinal_states[d], and dinitial_states[d] is the
  * gradient of initial_states[d].  headdim * dstate > 8192 and shapes whose
