@@ -115,6 +115,7 @@ __global__ void __launch_bounds__(kThreads, 1) ssd_split_agg_tc(const __grid_con
     __shared__ AggSmall sh;
     const FwdArgs& a = prm.a;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    pdl_trigger();                                // the split scan may start on SMs this grid leaves free
 
     // unit: (batch row, split, group of K heads), head groups fastest so that
     // CTAs running together share B in L2

@@ -415,6 +415,9 @@ int fwd_impl(const ssd_params_t* p, const void* x, const float* dt, const float*
         return e;
     };
     auto launch = [&](const FwdArgs& aa) { return timed(tc ? launch_tc : launch_simt, aa); };
+    // the launches after the first start as programmatic dependents of the one before
+    // (not when each launch is timed: the events between them serialise the launches)
+    const int pdl = (tc && !tm) ? 1 : 0;
     if (tc && tp.T > 0) {
         // leftover-unit plan: aggregates of the pieces, their composition, then the
         // whole units and the pieces in one launch
@@ -427,6 +430,7 @@ int fwd_impl(const ssd_params_t* p, const void* x, const float* dt, const float*
         a.mode = kModeAggregate;
         a.grid_units = (int64_t)tp.T * tp.m;
         if (launch(a) != cudaSuccess) return SSD_ERR_CUDA;
+        a.pdl = pdl;
         if (doc_init && timed(launch_doc_init_agg, a) != cudaSuccess) return SSD_ERR_CUDA;
         FwdArgs sa = a;   // the scan runs over T "rows" of m splits
         sa.batch = 1;
@@ -446,6 +450,9 @@ int fwd_impl(const ssd_params_t* p, const void* x, const float* dt, const float*
         a.mode = kModeAggregate;
         const bool agg_tc = tc && a.split_len >= (int64_t)kAggMinChunks * p->chunk;
         if ((agg_tc ? timed(launch_agg_tc, a) : launch(a)) != cudaSuccess) return SSD_ERR_CUDA;
+        // (not after the persistent aggregate grid of short splits: the scan's blocks,
+        // launched as soon as that grid starts, measured slower there)
+        a.pdl = agg_tc ? pdl : 0;
         if (doc_init && timed(launch_doc_init_agg, a) != cudaSuccess) return SSD_ERR_CUDA;
         if (timed(launch_split_scan, a) != cudaSuccess) return SSD_ERR_CUDA;
     }

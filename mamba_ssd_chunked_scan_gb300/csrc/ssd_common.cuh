@@ -64,6 +64,35 @@ struct WsLayout {
     size_t total;
 };
 
+// Programmatic dependent launch.  A forward call's launches after its first are
+// programmatic dependents of the one before: they may start on SMs the earlier
+// kernel leaves free, and wait for its completion (and the visibility of its
+// writes) only where they read its output.  Every kernel of the call triggers its
+// dependent at its start; a dependent waits before its first read of earlier
+// output, and also before it exits, so that its completion implies the
+// completion of every earlier launch.  Without the launch attribute both are
+// no-ops.
+__device__ __forceinline__ void pdl_trigger() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+
+// Launch kern<<<grid, block, smem, st>>>(args...), as a programmatic dependent of
+// the previous launch on st when dep is set.
+template <typename... KArgs, typename... Args>
+inline cudaError_t launch_kernel(void (*kern)(KArgs...), unsigned grid, unsigned block, size_t smem, cudaStream_t st,
+                                 bool dep, Args... args) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(grid);
+    cfg.blockDim = dim3(block);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = st;
+    cudaLaunchAttribute at[1];
+    at[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    at[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = at;
+    cfg.numAttrs = dep ? 1 : 0;
+    return cudaLaunchKernelEx(&cfg, kern, args...);
+}
+
 __host__ __device__ inline size_t align_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
 
 __host__ __device__ inline WsLayout ws_layout(int64_t batch, int H, int P, int N, int nsplit) {

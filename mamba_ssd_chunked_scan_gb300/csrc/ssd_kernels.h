@@ -53,6 +53,9 @@ struct FwdArgs {
     // fault injection (test aid, 0 otherwise): the TMA producer issues no loads,
     // so every wait that depends on them runs out
     int stall_loads;
+    // launched as a programmatic dependent of the call's previous launch (tensor-core
+    // full pass, split scan, document-start aggregates)
+    int pdl;
 };
 
 // One decode step (ssd_step): everything the launch needs.

@@ -258,6 +258,9 @@ __global__ void ssd_split_scan(const float* __restrict__ tau, float* __restrict_
     const int PN4 = PN >> 2;
     const int nagg = nsplit - 1;   // slots holding aggregates
     const int64_t k = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+    // (no early trigger: the full pass starts as this grid's blocks exit, so it does not
+    // compete for bandwidth with the scan, which is bandwidth-bound at short splits)
+    pdl_wait();                    // the aggregates are complete (also on the early return)
     if (nagg < 2 || k >= units_bh * PN4) return;
     const int64_t bh = k / PN4;
     const int e4 = (int)(k % PN4);
@@ -431,9 +434,8 @@ cudaError_t launch_split_scan(const FwdArgs& a, cudaStream_t st) {
     // (with two splits there is nothing to compose: one block that returns at once)
     const int64_t total = a.nsplit > 2 ? a.batch * a.H * (int64_t)(PN / 4) : 1;
     const int threads = 256;
-    ssd_split_scan<<<(unsigned)((total + threads - 1) / threads), threads, 0, st>>>(
-        a.ws_tau, a.ws_state, a.batch * a.H, a.nsplit, PN);
-    return cudaGetLastError();
+    return launch_kernel(ssd_split_scan, (unsigned)((total + threads - 1) / threads), threads, 0, st, a.pdl != 0,
+                         (const float*)a.ws_tau, a.ws_state, a.batch * a.H, a.nsplit, PN);
 }
 
 cudaError_t launch_segsum_dump(const float* l2, int64_t nrows, int chunk, float* seg, float* L, float* pexp,

@@ -489,6 +489,7 @@ __global__ void __launch_bounds__(kThreads, 1) ssd_chunk_tc(const __grid_constan
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int wg = warp >> 2;
     constexpr bool full_mode = kFull;
+    pdl_trigger();
 
     // items of this CTA: the chunks of units blockIdx.x, blockIdx.x + gridDim.x, ...
     const int nunits = (int)(a.batch * a.H * a.nsplit);
@@ -890,7 +891,10 @@ __global__ void __launch_bounds__(kThreads, 1) ssd_chunk_tc(const __grid_constan
         // caller's initial state, or zero
         auto enter_state = [&](const Unit& un) {
             const float* src = nullptr;
-            if (full_mode && a.nsplit > 1 && un.s > 0) src = a.ws_state + (size_t)(un.ws - 1) * PN;   // (slot s - 1)
+            if (full_mode && a.nsplit > 1 && un.s > 0) {
+                pdl_wait();                       // the split scan (and everything before it) is complete
+                src = a.ws_state + (size_t)(un.ws - 1) * PN;   // (slot s - 1)
+            }
             else if (un.s == 0 && a.init) src = a.init + ((size_t)un.b * a.H + un.h) * PN;   // (documents: d = 0 = b)
 #pragma unroll
             for (int p = 0; p < P; ++p) S[p] = src ? src[(size_t)p * N + i] : 0.f;
@@ -1074,6 +1078,7 @@ __global__ void __launch_bounds__(kThreads, 1) ssd_chunk_tc(const __grid_constan
             if (!ptx::mbar_wait(&sh.drain[2], 0, &sh.never, a.wait_iters)) fail(sh, a, kWhereDrain);
         }
     }
+    pdl_wait();                                   // (the call's earlier launches end before this one)
     ptx::tc_fence_before();
     __syncthreads();
     ptx::tc_fence_after();
@@ -1094,6 +1099,8 @@ constexpr int kDocInitThreads = 128;
 
 __global__ void __launch_bounds__(kDocInitThreads) ssd_doc_init_agg(const FwdArgs a) {
     __shared__ float part[kDocInitThreads / 32];
+    pdl_trigger();
+    pdl_wait();                                // the split aggregates are complete
     const Unit un = unit_at<false>(a, blockIdx.x);
     if (un.s == (int)a.nsplit - 1) return;   // the last split's aggregate is never composed
     const int d = find_doc_tc(a.cu, a.ndocs, un.t1 - 1);
@@ -1131,8 +1138,7 @@ static_assert(kDocInitThreads == 128, "the reduction above sums four warps");
 cudaError_t launch_doc_init_agg(const FwdArgs& a, cudaStream_t st) {
     const int64_t grid = a.grid_units > 0 ? a.grid_units : a.batch * a.H * a.nsplit;
     if (grid <= 0 || !a.cu || !a.init) return cudaSuccess;
-    ssd_doc_init_agg<<<(unsigned)grid, kDocInitThreads, 0, st>>>(a);
-    return cudaGetLastError();
+    return launch_kernel(ssd_doc_init_agg, (unsigned)grid, kDocInitThreads, 0, st, a.pdl != 0, a);
 }
 
 static PFN_cuTensorMapEncodeTiled_v12000 get_encode() {
@@ -1216,8 +1222,7 @@ cudaError_t launch_tc(const FwdArgs& a, cudaStream_t st) {
         if (fa.numRegs * 4 < need) return cudaErrorInvalidConfiguration;
         rd.store(1, std::memory_order_release);
     }
-    kern<<<(unsigned)grid, kThreads, smem, st>>>(prm);
-    return cudaGetLastError();
+    return launch_kernel(kern, (unsigned)grid, kThreads, smem, st, a.pdl != 0, prm);
 }
 
 }  // namespace ssd
