@@ -176,18 +176,19 @@ struct BwdLayout {
     bool tc = false;
     int nsplit = 1;            // sequence splits of the tensor-core backward
     int64_t split_len = 0;
-    int shares = 1;            // dA / dD shares per (row, head): splits, or documents (CUDA cores)
+    int shares = 1;            // dA / dD shares per (row, head): splits, or documents
+    bool doc_units = false;    // tensor cores: packed documents with their own states as (head, document) units
     size_t ckpt = 0, dB = 0, dC = 0, dA = 0, dD = 0;
     size_t tau_f = 0, tau_r = 0, sin = 0, lam = 0;   // split aggregates, forwards and reverse
     size_t total = 0;
 };
 
-// The backward runs on the tensor cores for the bf16 Mamba-2 head shape, except
-// for packed documents with initial states or final-state gradients
-// (doc_states), which take the CUDA-core kernel's document-aligned chunks.
+// The backward runs on the tensor cores for the bf16 Mamba-2 head shape (packed
+// documents with initial states or final-state gradients, doc_states, as
+// (head, document) units), and on CUDA cores otherwise.
 bool bwd_use_tc(const ssd_params_t* p, bool doc_states) {
-    return !doc_states && bwd_tc_supported(p->headdim, p->dstate, p->dtype) &&
-           p->seqlen < ((int64_t)1 << 31) - 256;
+    (void)doc_states;
+    return bwd_tc_supported(p->headdim, p->dstate, p->dtype) && p->seqlen < ((int64_t)1 << 31) - 256;
 }
 
 bool bwd_layout(const ssd_params_t* p, bool doc_states, BwdLayout* l) {
@@ -196,8 +197,12 @@ bool bwd_layout(const ssd_params_t* p, bool doc_states, BwdLayout* l) {
     l->Qb = l->tc ? kBwdTcChunk : bwd_chunk(p->headdim, p->dstate, kSmemLimit);
     if (l->Qb == 0) return false;
     const size_t bh = (size_t)p->batch * p->nheads;
-    // chunks per row: the CUDA-core kernel starts a chunk at every document start too
-    const size_t nch = (size_t)((p->seqlen + l->Qb - 1) / l->Qb) + (l->tc ? 0 : (size_t)p->ndocs);
+    // (head, document) units, each document in chunks from its first token (one more
+    // chunk per document at most): packed documents on CUDA cores, and on the tensor
+    // cores those with their own states (without, they run as whole rows there)
+    const bool per_doc = p->ndocs > 0 && (!l->tc || doc_states);
+    l->doc_units = l->tc && per_doc;
+    const size_t nch = (size_t)((p->seqlen + l->Qb - 1) / l->Qb) + (per_doc ? (size_t)p->ndocs : 0);
     const size_t PN = (size_t)p->headdim * p->dstate;
     // per-head shares of dB and dC: bf16 from the tensor-core backward, else fp32
     const size_t share_elem = l->tc ? 2 : 4;
@@ -207,7 +212,7 @@ bool bwd_layout(const ssd_params_t* p, bool doc_states, BwdLayout* l) {
     // 4 chunks at least (the split aggregates' tensor-core kernel)
     l->nsplit = 1;
     l->split_len = p->seqlen;
-    if (l->tc) {
+    if (l->tc && !l->doc_units) {
         ssd_params_t q = *p;
         q.chunk = kBwdTcChunk;
         if (q.split_len > 0) q.split_len = (int32_t)((q.split_len + kBwdTcChunk - 1) / kBwdTcChunk * kBwdTcChunk);
@@ -219,8 +224,8 @@ bool bwd_layout(const ssd_params_t* p, bool doc_states, BwdLayout* l) {
         }
     }
     const size_t ns = (size_t)l->nsplit;
-    // the CUDA-core kernel runs packed documents as (head, document) units
-    l->shares = l->tc ? l->nsplit : (p->ndocs > 0 ? p->ndocs : 1);
+    // document units give one dA / dD share per (head, document)
+    l->shares = per_doc ? p->ndocs : l->nsplit;
     size_t o = sizeof(WsHeader);
     l->ckpt = o;  o = align_up(o + bh * nch * PN * sizeof(float), 256);
     l->dB = o;    o = align_up(o + share * share_elem, 256);
@@ -578,6 +583,7 @@ int ssd_bwd(const ssd_params_t* p, const void* x, const float* dt, const float* 
     a.split_len = l.split_len;
     a.ws_sin = (const float*)(ws + l.sin);
     a.ws_lam = (const float*)(ws + l.lam);
+    a.doc_units = l.doc_units ? 1 : 0;
     // a fresh status word for this call's bounded device waits
     cudaStream_t st = (cudaStream_t)stream;
     if (cudaMemsetAsync(ws, 0, sizeof(WsHeader), st) != cudaSuccess) return SSD_ERR_CUDA;

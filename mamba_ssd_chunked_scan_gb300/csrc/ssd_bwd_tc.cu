@@ -79,6 +79,7 @@ struct BwdTcSmall {
     float kred[2][8];       // per warp: partial <Lam, S_in>
     float red[16];
     float carry[3][4];      // warp totals of the token scans
+    int docoff[12];         // per warp: chunks of the earlier documents (document units)
     uint64_t full, full1, mmaF, mma1, mma2, mmaV1, mmaDB, mmaDC, mmaLU, drain;   // loads and MMAs complete
     uint64_t rdyF, rdyA, rdyB, rdyC, rdyDB, rdyS;                   // compute warps -> issuer
     uint64_t stFreeS, stFreeT;   // the stores have read the S_in tile (dx), and the A1 / A2 tiles
@@ -185,6 +186,10 @@ __device__ __forceinline__ bool doc_start_tc(const BwdArgs& a, int64_t t) {
     return false;
 }
 
+// kDocu: document units (packed documents with their own states; BwdArgs::doc_units),
+// a kernel instance of its own so that the whole-row and split units keep their
+// register allocation.
+template <bool kDocu>
 __global__ void __launch_bounds__(kThreads, 1) ssd_bwd_tc(const __grid_constant__ BwdTcParams prm) {
     extern __shared__ uint8_t smem_raw[];
     uint8_t* sm = (uint8_t*)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
@@ -207,9 +212,35 @@ __global__ void __launch_bounds__(kThreads, 1) ssd_bwd_tc(const __grid_constant_
     const int nch_all = (int)((L + Q - 1) / Q);
     const int cps = nsplit > 1 ? (int)(a.split_len / Q) : nch_all;   // chunks per split
     const int c0 = s * cps;                                          // this split's first chunk
-    const int nch = (c0 + cps < nch_all ? c0 + cps : nch_all) - c0;  // and its chunks (local c = 0 ..)
+    int nch = (c0 + cps < nch_all ? c0 + cps : nch_all) - c0;        // and its chunks (local c = 0 ..)
     const size_t PN = (size_t)P * N;
     float* ckpt = a.ws_ckpt + ((size_t)bh * nch_all + c0) * PN;
+    // Document units (packed documents with their own states; batch 1, s = the document):
+    // the document's tokens [T0, tend) in chunks from T0, entering from its initial
+    // state and leaving with its final-state gradient.  The rows of its last chunk past
+    // tend are padding: dt 0 (no decay, no input), their rows of the masks and of the
+    // scaled dy zero, and that chunk's outputs written row by row (its tiles overlap
+    // the next document's first rows).  Offsets are clamped, so invalid ones (which the
+    // device check reports) keep every index in bounds.
+    constexpr bool docu = kDocu;
+    int64_t T0 = (int64_t)c0 * Q, tend = L;
+    if (docu) {
+        auto clampL = [&](int64_t v) { return v < 0 ? (int64_t)0 : v > L ? L : v; };
+        T0 = clampL(__ldg(a.cu + s));
+        tend = clampL(__ldg(a.cu + s + 1));
+        if (tend < T0) tend = T0;
+        nch = (int)((tend - T0 + Q - 1) / Q);
+        // this document's first checkpoint slot: after the chunks of the head's earlier
+        // documents (a block sum, completed after the barrier below)
+        int part = 0;
+        for (int e = (int)threadIdx.x; e < s; e += (int)blockDim.x) {
+            const int64_t u0 = clampL(__ldg(a.cu + e)), u1 = clampL(__ldg(a.cu + e + 1));
+            part += u1 > u0 ? (int)((u1 - u0 + Q - 1) / Q) : 0;
+        }
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) part += __shfl_xor_sync(0xffffffffu, part, o);
+        if (lane == 0) sh.docoff[warp] = part;
+    }
 
     if (threadIdx.x == 0) {
         ptx::mbar_init(&sh.full, 1);
@@ -239,6 +270,13 @@ __global__ void __launch_bounds__(kThreads, 1) ssd_bwd_tc(const __grid_constant_
     __syncthreads();
     ptx::tc_fence_after();
     const uint32_t tb = sh.tmem_base;
+    if (docu) {
+        int64_t off = 0;
+        for (int w = 0; w < kThreads / 32; ++w) off += sh.docoff[w];
+        const int64_t cap = (int64_t)nch_all + a.ndocs;   // checkpoint slots per head
+        if (off + nch > cap) nch = 0;                     // (inconsistent offsets: no work)
+        ckpt = a.ws_ckpt + ((size_t)h * cap + (size_t)off) * PN;
+    }
 
     if (warp >= 8) {
         // ================================================================ issue warpgroup
@@ -259,7 +297,7 @@ __global__ void __launch_bounds__(kThreads, 1) ssd_bwd_tc(const __grid_constant_
                 uint64_t* bar = st ? &sh.full1 : &sh.full;
                 uint8_t* xt = sm + (st ? kTSin : kTX);
                 uint8_t* bt = sm + (st ? kT1 : kTB);
-                const int t0 = (c0 + c) * Q;
+                const int t0 = docu ? (int)(T0 + (int64_t)c * Q) : (c0 + c) * Q;
                 ptx::mbar_expect_tx(bar, 16384u + 32768u);
                 ptx::tma_load_4d(xt, &prm.tm_x, bar, 0, h, t0, b);
                 ptx::tma_load_4d(bt, &prm.tm_B, bar, 0, g, t0, b);
@@ -267,7 +305,7 @@ __global__ void __launch_bounds__(kThreads, 1) ssd_bwd_tc(const __grid_constant_
             };
             auto load2 = [&](int c) {         // phase 2: x, dy, B and C of chunk c; chunk c - 1 towards L2
                 ++nissue[0];
-                const int t0 = (c0 + c) * Q;
+                const int t0 = docu ? (int)(T0 + (int64_t)c * Q) : (c0 + c) * Q;
                 ptx::mbar_expect_tx(&sh.full, 16384u * 2u + 32768u * 2u);
                 ptx::tma_load_4d(sm + kTX, &prm.tm_x, &sh.full, 0, h, t0, b);
                 ptx::tma_load_4d(sm + kTDY, &prm.tm_dy, &sh.full, 0, h, t0, b);
@@ -308,7 +346,10 @@ __global__ void __launch_bounds__(kThreads, 1) ssd_bwd_tc(const __grid_constant_
             if (nch > 0 && !*(volatile int*)&sh.abort) load2(nch - 1);
             for (int k = 0; k < nch && !*(volatile int*)&sh.abort; ++k) {
                 const int c = nch - 1 - k;
-                const int t0 = (c0 + c) * Q;
+                const int t0 = docu ? (int)(T0 + (int64_t)c * Q) : (c0 + c) * Q;
+                // a document's last chunk when it ends before the chunk does: the compute
+                // threads write its rows (the groups stay, empty, for the counts below)
+                const bool partial = docu && (int64_t)t0 + Q > tend;
                 if (!wait_bar(sh, a, &sh.full, ndone[0] & 1, kWhereLoad)) break;
                 ++ndone[0];
                 // TMEM free: the last chunk's shares (or phase 1's state summaries) are read
@@ -384,14 +425,18 @@ __global__ void __launch_bounds__(kThreads, 1) ssd_bwd_tc(const __grid_constant_
                 // the staged dB share, then dx and the dC share: their stores (rows past
                 // the end are clipped), in three groups
                 if (!wait_bar(sh, a, &sh.rdyDB, k & 1, kWhereStores)) break;
-                ptx::tma_store_4d(&prm.tm_dB, sm + kT1, 0, h, t0, b);
-                ptx::tma_store_4d(&prm.tm_dB, sm + kT1 + 16384, 64, h, t0, b);
+                if (!partial) {
+                    ptx::tma_store_4d(&prm.tm_dB, sm + kT1, 0, h, t0, b);
+                    ptx::tma_store_4d(&prm.tm_dB, sm + kT1 + 16384, 64, h, t0, b);
+                }
                 ptx::bulk_commit();
                 if (!wait_bar(sh, a, &sh.rdyS, (k + 1) & 1, kWhereStores)) break;
-                ptx::tma_store_4d(&prm.tm_dx, sm + kTSin, 0, h, t0, b);
+                if (!partial) ptx::tma_store_4d(&prm.tm_dx, sm + kTSin, 0, h, t0, b);
                 ptx::bulk_commit();
-                ptx::tma_store_4d(&prm.tm_dC, sm + kT2, 0, h, t0, b);
-                ptx::tma_store_4d(&prm.tm_dC, sm + kT2 + 16384, 64, h, t0, b);
+                if (!partial) {
+                    ptx::tma_store_4d(&prm.tm_dC, sm + kT2, 0, h, t0, b);
+                    ptx::tma_store_4d(&prm.tm_dC, sm + kT2 + 16384, 64, h, t0, b);
+                }
                 ptx::bulk_commit();
             }
             // drain: every MMA issued has completed, the last load issued has landed,
@@ -418,7 +463,7 @@ __global__ void __launch_bounds__(kThreads, 1) ssd_bwd_tc(const __grid_constant_
         const float Ah = a.A[h];
         const float Dh = a.D ? a.D[h] : 0.f;
         uint32_t nfull = 0;
-        auto dt_at = [&](int64_t t) { return t < L ? __ldg(a.dt + ((size_t)b * L + t) * a.H + h) : 0.f; };
+        auto dt_at = [&](int64_t t) { return t < (docu ? tend : L) ? __ldg(a.dt + ((size_t)b * L + t) * a.H + h) : 0.f; };
         // the chunk's log-decays into the segsum input, and dt (column half 0 writes them)
         auto decays = [&](float d, bool start) {
             if (hf == 0) {
@@ -431,19 +476,19 @@ __global__ void __launch_bounds__(kThreads, 1) ssd_bwd_tc(const __grid_constant_
         // Chunk c's segsum runs while chunk c - 1's state summary is on the tensor
         // cores; then S (the state entering chunk c) is updated and kept.
         float S[32];   // S^T[n = r][p], this half's p
-#pragma unroll
         {
-            const float* s_in = s > 0 ? a.ws_sin + ((size_t)bh * nsplit + s - 1) * PN
-                                      : (a.init ? a.init + (size_t)bh * PN : nullptr);
+            const float* s_in = docu  ? (a.init ? a.init + ((size_t)s * a.H + h) * PN : nullptr)
+                                : s > 0 ? a.ws_sin + ((size_t)bh * nsplit + s - 1) * PN
+                                        : (a.init ? a.init + (size_t)bh * PN : nullptr);
 #pragma unroll
             for (int p = 0; p < 32; ++p) S[p] = s_in ? s_in[(size_t)(32 * hf + p) * N + r] : 0.f;
         }
         float etau_prev = 0.f;
-        float d1_next = dt_at((int64_t)c0 * Q + r);   // (the split's first chunk)
+        float d1_next = dt_at((docu ? T0 : (int64_t)c0 * Q) + r);   // (the split's first chunk)
         for (int c = 0; c < nch; ++c) {
-            const int64_t t0 = (int64_t)(c0 + c) * Q;
+            const int64_t t0 = docu ? T0 + (int64_t)c * Q : (int64_t)(c0 + c) * Q;
             const float d = d1_next;   // (loaded a chunk earlier)
-            decays(d, t0 + r < L && doc_start_tc(a, t0 + r));
+            decays(d, !docu && t0 + r < L && doc_start_tc(a, t0 + r));
             d1_next = c + 1 < nch ? dt_at(t0 + Q + r) : 0.f;
             ptx::named_bar(kBarCompute, kCompute);
             SegsumLinRow<4> row;
@@ -483,8 +528,9 @@ __global__ void __launch_bounds__(kThreads, 1) ssd_bwd_tc(const __grid_constant_
         // adjoint of the state leaving this split: dfin for the last split, else
         // the reverse scan's slot s + 1
         {
-            const float* lam_out = s + 1 < nsplit ? a.ws_lam + ((size_t)bh * nsplit + s + 1) * PN
-                                                  : (a.dfin ? a.dfin + (size_t)bh * PN : nullptr);
+            const float* lam_out = docu ? (a.dfin ? a.dfin + ((size_t)s * a.H + h) * PN : nullptr)
+                                   : s + 1 < nsplit ? a.ws_lam + ((size_t)bh * nsplit + s + 1) * PN
+                                                    : (a.dfin ? a.dfin + (size_t)bh * PN : nullptr);
             uint32_t v[16];
 #pragma unroll
             for (int q = 0; q < 2; ++q) {
@@ -545,17 +591,21 @@ __global__ void __launch_bounds__(kThreads, 1) ssd_bwd_tc(const __grid_constant_
             const float dl = T.start ? 0.f : rv + u + v + T.etau * K - T.d * vx;
             if (hf == 0) {
                 if (T.valid) a.ddt[((size_t)b * L + T.t0 + r) * a.H + h] = fmaf(Ah, dl, vx);
-                dA_acc = fmaf(T.d, dl, dA_acc);
-                dD_acc += ddv;
+                if (!docu || T.valid) {   // (document units: a padding row's dy . x is not zero)
+                    dA_acc = fmaf(T.d, dl, dA_acc);
+                    dD_acc += ddv;
+                }
             }
         };
-        float d_next = nch > 0 ? dt_at((int64_t)(c0 + nch - 1) * Q + r) : 0.f;
+        float d_next = nch > 0 ? dt_at((docu ? T0 + (int64_t)(nch - 1) * Q : (int64_t)(c0 + nch - 1) * Q) + r) : 0.f;
         for (int k = 0; k < nch; ++k) {
             const int c = nch - 1 - k;
-            const int64_t t0 = (int64_t)(c0 + c) * Q;
-            const bool valid = t0 + r < L;
+            // (the whole-row and split instance keeps its own expressions: fewer live registers)
+            const int64_t t0 = docu ? T0 + (int64_t)c * Q : (int64_t)(c0 + c) * Q;
+            const bool valid = t0 + r < (docu ? tend : L);
+            const bool partial = docu && t0 + Q > tend;   // (its rows are written by this thread)
             const float d = d_next;   // (loaded a chunk earlier)
-            const bool start = valid && doc_start_tc(a, t0 + r);
+            const bool start = valid && !docu && doc_start_tc(a, t0 + r);
             decays(d, start);
             d_next = c > 0 ? dt_at(t0 - Q + r) : 0.f;
             ptx::named_bar(kBarCompute, kCompute);
@@ -573,7 +623,7 @@ __global__ void __launch_bounds__(kThreads, 1) ssd_bwd_tc(const __grid_constant_
                 for (int p = 0; p < 32; ++p) sv[p] = src[(size_t)p * N];
             }
             const float es_r = segsum_lin_suffix<4>(sh.seg, r);
-            const float ep_r = row.pe;
+            const float ep_r = (docu && !valid) ? 0.f : row.pe;   // (a padding row's dy enters nothing)
             const float etau = sh.seg.tauL;
             // the last chunk's dx store has read the S_in tile
             if (k > 0) wait_bar(sh, a, &sh.stFreeS, (k - 1) & 1, kWhereStores);
@@ -651,8 +701,16 @@ __global__ void __launch_bounds__(kThreads, 1) ssd_bwd_tc(const __grid_constant_
 #pragma unroll
                         for (int cc = 0; cc < 16; cc += 2) {
                             const int kx = 16 * q16 + cc;
-                            const float l0 = below ? rfc * sh.seg.colL[j0 + cc] : diag ? row.wl[kx] : 0.f;
-                            const float l1 = below ? rfc * sh.seg.colL[j0 + cc + 1] : diag ? row.wl[kx + 1] : 0.f;
+                            // (document units: a padding row of A1 and A2 is zero; past the
+                            // row's end the loads are zero-filled instead)
+                            const float l0 = (docu && !valid) ? 0.f
+                                             : below          ? rfc * sh.seg.colL[j0 + cc]
+                                             : diag           ? row.wl[kx]
+                                                              : 0.f;
+                            const float l1 = (docu && !valid) ? 0.f
+                                             : below          ? rfc * sh.seg.colL[j0 + cc + 1]
+                                             : diag           ? row.wl[kx + 1]
+                                                              : 0.f;
                             const float x0 = __uint_as_float(xr[kx]), x1 = __uint_as_float(xr[kx + 1]);
                             p1[cc / 2] = pack_bf16(l0 * __uint_as_float(gr[kx]), l1 * __uint_as_float(gr[kx + 1]));
                             p2[cc / 2] = pack_bf16(l0 * x0 * sh.dts[j0 + cc], l1 * x1 * sh.dts[j0 + cc + 1]);
@@ -741,12 +799,17 @@ __global__ void __launch_bounds__(kThreads, 1) ssd_bwd_tc(const __grid_constant_
                 uint32_t v[32];
                 ptx::tmem_load32(lane_addr + kTmG + 32 * cb, v);
 #pragma unroll
-                for (int q = 0; q < 4; ++q)
-                    *reinterpret_cast<uint4*>(sm + kT1 + off2(r, 32 * cb + 8 * q)) = make_uint4(
+                for (int q = 0; q < 4; ++q) {
+                    const uint4 u = make_uint4(
                         pack_bf16(__uint_as_float(v[8 * q]), __uint_as_float(v[8 * q + 1])),
                         pack_bf16(__uint_as_float(v[8 * q + 2]), __uint_as_float(v[8 * q + 3])),
                         pack_bf16(__uint_as_float(v[8 * q + 4]), __uint_as_float(v[8 * q + 5])),
                         pack_bf16(__uint_as_float(v[8 * q + 6]), __uint_as_float(v[8 * q + 7])));
+                    *reinterpret_cast<uint4*>(sm + kT1 + off2(r, 32 * cb + 8 * q)) = u;
+                    if (partial && valid)
+                        *reinterpret_cast<uint4*>(reinterpret_cast<uint16_t*>(a.ws_dB) +
+                                                  ((size_t)(t0 + r) * a.H + h) * N + 32 * cb + 8 * q) = u;
+                }
             }
             warp_arrive(&sh.rdyDB, lane);   // staged
             // ---- dC (row i = r, this half's columns) as bf16 over A2 o dt, dx over S_in,
@@ -758,30 +821,40 @@ __global__ void __launch_bounds__(kThreads, 1) ssd_bwd_tc(const __grid_constant_
                 uint32_t v[32];
                 ptx::tmem_load32(lane_addr + kTmX + 32 * cb, v);
 #pragma unroll
-                for (int q = 0; q < 4; ++q)
-                    *reinterpret_cast<uint4*>(sm + kT2 + off2(r, 32 * cb + 8 * q)) = make_uint4(
+                for (int q = 0; q < 4; ++q) {
+                    const uint4 u = make_uint4(
                         pack_bf16(__uint_as_float(v[8 * q]), __uint_as_float(v[8 * q + 1])),
                         pack_bf16(__uint_as_float(v[8 * q + 2]), __uint_as_float(v[8 * q + 3])),
                         pack_bf16(__uint_as_float(v[8 * q + 4]), __uint_as_float(v[8 * q + 5])),
                         pack_bf16(__uint_as_float(v[8 * q + 6]), __uint_as_float(v[8 * q + 7])));
+                    *reinterpret_cast<uint4*>(sm + kT2 + off2(r, 32 * cb + 8 * q)) = u;
+                    if (partial && valid)
+                        *reinterpret_cast<uint4*>(reinterpret_cast<uint16_t*>(a.ws_dC) +
+                                                  ((size_t)(t0 + r) * a.H + h) * N + 32 * cb + 8 * q) = u;
+                }
             }
 #pragma unroll
-            for (int q = 0; q < 4; ++q)
-                *reinterpret_cast<uint4*>(sm + kTSin + sw128_off(r, 32 * hf + 8 * q)) =
-                    make_uint4(dxo[4 * q], dxo[4 * q + 1], dxo[4 * q + 2], dxo[4 * q + 3]);
+            for (int q = 0; q < 4; ++q) {
+                const uint4 u = make_uint4(dxo[4 * q], dxo[4 * q + 1], dxo[4 * q + 2], dxo[4 * q + 3]);
+                *reinterpret_cast<uint4*>(sm + kTSin + sw128_off(r, 32 * hf + 8 * q)) = u;
+                if (partial && valid)
+                    *reinterpret_cast<uint4*>(reinterpret_cast<uint16_t*>(a.dx) + ((size_t)(t0 + r) * a.H + h) * P +
+                                              32 * hf + 8 * q) = u;
+            }
             warp_arrive(&sh.rdyS, lane);   // staged, and this chunk's TMEM is read
             prev = Tok{vx, lbx, scdy, ddv, es_r, ep_r, d, etau, t0, start, valid};
             if (ptx::named_bar_any(kBarCompute, kCompute, *(volatile int*)&sh.abort != 0)) break;
         }
         if (nch > 0 && !*(volatile int*)&sh.abort) token_pass(prev, (nch - 1) & 1);
         // ---- the adjoint of the initial state; this unit's dA and dD shares
-        if (a.dinit && s == 0 && !*(volatile int*)&sh.abort) {
+        if (a.dinit && (docu ? nch > 0 : s == 0) && !*(volatile int*)&sh.abort) {
             wait_bar(sh, a, &sh.mmaLU, (nch - 1) & 1, kWhereDC);
             ptx::tc_fence_after();
             uint32_t l0[32];
             ptx::tmem_load32(lane_addr + kTmLU + 32 * hf, l0);
+            const size_t di = docu ? (size_t)s * a.H + h : (size_t)bh;
 #pragma unroll
-            for (int p = 0; p < 32; ++p) a.dinit[bh * PN + (size_t)(32 * hf + p) * N + r] = __uint_as_float(l0[p]);
+            for (int p = 0; p < 32; ++p) a.dinit[di * PN + (size_t)(32 * hf + p) * N + r] = __uint_as_float(l0[p]);
         }
         dA_acc = warp_sum(dA_acc);
         dD_acc = warp_sum(dD_acc);
@@ -816,23 +889,25 @@ cudaError_t launch_bwd_tc(const BwdArgs& a, cudaStream_t st) {
         !encode_4d(&prm.tm_dx, a.dx, P, a.H, a.L, a.batch) ||
         !encode_4d(&prm.tm_dB, a.ws_dB, N, a.H, a.L, a.batch) || !encode_4d(&prm.tm_dC, a.ws_dC, N, a.H, a.L, a.batch))
         return cudaErrorInvalidValue;
-    static std::atomic<uint8_t> ready[kMaxDevices];
+    void (*kern)(BwdTcParams) = a.doc_units ? ssd_bwd_tc<true> : ssd_bwd_tc<false>;
+    static std::atomic<uint8_t> ready[kMaxDevices][2];
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess) return e;
     if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
-    if (!ready[dev].load(std::memory_order_acquire)) {
-        if ((e = cudaFuncSetAttribute(ssd_bwd_tc, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmemBytes)) !=
+    std::atomic<uint8_t>& rd = ready[dev][a.doc_units ? 1 : 0];
+    if (!rd.load(std::memory_order_acquire)) {
+        if ((e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmemBytes)) !=
             cudaSuccess)
             return e;
         // the warpgroup budgets must fit the registers the CTA is launched with
         // (setmaxnreg.inc draws on that pool; a budget beyond it would wait forever)
         cudaFuncAttributes fa;
-        if ((e = cudaFuncGetAttributes(&fa, ssd_bwd_tc)) != cudaSuccess) return e;
+        if ((e = cudaFuncGetAttributes(&fa, kern)) != cudaSuccess) return e;
         if (fa.numRegs * (kThreads / 128) < kRegsIssue + 2 * kRegsCompute) return cudaErrorInvalidConfiguration;
-        ready[dev].store(1, std::memory_order_release);
+        rd.store(1, std::memory_order_release);
     }
-    ssd_bwd_tc<<<(unsigned)(a.batch * a.H * (a.nsplit > 0 ? a.nsplit : 1)), kThreads, kSmemBytes, st>>>(prm);
+    kern<<<(unsigned)(a.batch * a.H * (a.nsplit > 0 ? a.nsplit : 1)), kThreads, kSmemBytes, st>>>(prm);
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
     return launch_bwd_reduce(a, st);
 }

@@ -113,6 +113,10 @@ struct BwdArgs {
     const float* ws_sin;   // [batch * H * nsplit * P * N] slot s - 1: the state entering split s
     const float* ws_lam;   // [batch * H * nsplit * P * N] slot s + 1: the adjoint of the state leaving split s
     uint32_t wait_iters;   // poll cap of each bounded wait (0: the default)
+    // packed documents with their own states on the tensor cores: units h * ndocs + d
+    // (nsplit = ndocs), each document in chunks from its first token; ws_ckpt holds
+    // L / 128 + ndocs chunks per head
+    int doc_units;
 };
 
 // Gated RMS normalisation (ssd_gate_norm): everything its launch needs.

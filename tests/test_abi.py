@@ -178,13 +178,17 @@ def test_bwd_workspace_size(L):
     n = L.lib.ssd_bwd_workspace_size(ctypes.byref(params(L, batch=2, seqlen=1000, nheads=4, dtype=0)))
     assert n >= 256 + 2 * 4 * 32 * 64 * 128 * 4 + 4 * shares + 2 * 8 * 4
     assert L.lib.ssd_bwd_workspace_size(ctypes.byref(params(L, ndocs=3, batch=1))) > 0    # packed documents
-    # packed documents with per-document states: (head, document) units on CUDA cores, chunks of
-    # 32 tokens from each document's start (one more chunk per document at most), fp32 shares, a dA
-    # and a dD share per unit
+    # packed documents with per-document states: (head, document) units, each document in chunks
+    # from its first token (one more chunk per document at most), a dA and a dD share per unit; the
+    # bf16 Mamba-2 head shape on the tensor cores (128-token chunks, bf16 shares), fp32 on CUDA
+    # cores (32-token chunks, fp32 shares)
     pd = params(L, batch=1, seqlen=1000, nheads=4, ndocs=3)
     nd = L.lib.ssd_bwd_workspace_size_doc_states(ctypes.byref(pd))
-    assert nd >= 256 + 4 * (32 + 3) * 64 * 128 * 4 + 2 * (1000 * 4 * 128 * 4) + 2 * 4 * 3 * 4
-    assert nd > L.lib.ssd_bwd_workspace_size(ctypes.byref(pd))
+    assert nd >= 256 + 4 * (8 + 3) * 64 * 128 * 4 + 2 * (1000 * 4 * 128 * 2) + 2 * 4 * 3 * 4
+    pf = params(L, batch=1, seqlen=1000, nheads=4, ndocs=3, dtype=0)
+    nf = L.lib.ssd_bwd_workspace_size_doc_states(ctypes.byref(pf))
+    assert nf >= 256 + 4 * (32 + 3) * 64 * 128 * 4 + 2 * (1000 * 4 * 128 * 4) + 2 * 4 * 3 * 4
+    assert nf == L.lib.ssd_bwd_workspace_size(ctypes.byref(pf))   # (CUDA cores: document units either way)
     assert L.lib.ssd_bwd_workspace_size_doc_states(ctypes.byref(params(L, batch=2, seqlen=1000))) == 0   # no documents
     assert L.lib.ssd_bwd_workspace_size(ctypes.byref(params(L, headdim=128, dstate=128))) == 0   # P * N > 8192
 

@@ -115,27 +115,31 @@ def test_bwd_packed_documents(lens, kw):
 
 
 @pytest.mark.parametrize("lens,kw", [
-    ([3, 300, 128, 1, 257, 90, 500], dict(headdim=64, dstate=128, dtype="bf16")),    # tiled instance, bf16
+    ([3, 300, 128, 1, 257, 90, 500], dict(headdim=64, dstate=128, dtype="bf16")),    # tensor cores, bf16
+    ([700, 129, 1000, 255, 384, 383], dict(headdim=64, dstate=128, dtype="bf16")),   # several chunks each
     ([32, 1, 31, 64, 33, 2], dict(headdim=64, dstate=128, dtype="f32")),             # ends on chunk edges
     ([10, 1, 50, 39], dict(headdim=16, dstate=32, dtype="f32")),                    # generic instance
 ])
 @pytest.mark.parametrize("with_dfin", [True, False])
 def test_bwd_packed_documents_with_states(lens, kw, with_dfin):
     """Packed documents, each from its own initial state and with (or without)
-    its own final-state gradient: the CUDA-core kernel's chunks start at every
-    document start; dinit is per document."""
+    its own final-state gradient, run as (head, document) units whose chunks
+    start at the document's first token (bf16 on the tensor cores: a document's
+    last chunk runs past its end into padding rows and is written row by row);
+    dinit is per document."""
     p = synth.make_problem(batch=1, seqlen=sum(lens), nheads=4, ngroups=2, chunk=128, seed=315,
                            doc_lengths=lens, A_dist="exp", init_std=0.5, **kw)
     got = check(p, with_dfin=with_dfin)
     assert got["dinit"] is not None and got["dinit"].shape[0] == len(lens)
 
 
-def test_bwd_packed_documents_final_gradient_only():
+@pytest.mark.parametrize("dtype", ["f32", "bf16"])
+def test_bwd_packed_documents_final_gradient_only(dtype):
     """Documents from zero states with final-state gradients (no initial
     states given): the same path, dinit not asked for."""
     lens = [70, 1, 200, 33]
     p = synth.make_problem(batch=1, seqlen=sum(lens), nheads=4, headdim=64, dstate=128, ngroups=1, chunk=128,
-                           dtype="f32", seed=317, doc_lengths=lens, A_dist="exp")
+                           dtype=dtype, seed=317, doc_lengths=lens, A_dist="exp")
     got = check(p)
     assert got["dinit"] is None
 
