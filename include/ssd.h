@@ -164,9 +164,10 @@ SSD_API size_t ssd_bwd_workspace_size(const ssd_params_t* p);
 
 /* Bytes of device workspace ssd_bwd() needs for packed documents (ndocs > 0)
  * when the call passes initial_states, dfinal_states or dinitial_states: that
- * call runs on CUDA cores, one block per (head, document), with chunks of at
- * most 32 tokens from each document's start, so its layout is larger than
- * ssd_bwd_workspace_size(p).
+ * call runs one unit per (head, document), in chunks from each document's first
+ * token (on the tensor cores for their shape, 128 tokens; else on CUDA cores,
+ * at most 32), so its chunk-state layout holds up to ndocs more chunks per head
+ * than whole rows need.
  * 0 when the parameters are invalid, ndocs is 0 or the backward pass does not
  * support them. */
 SSD_API size_t ssd_bwd_workspace_size_doc_states(const ssd_params_t* p);
@@ -207,11 +208,11 @@ SSD_API size_t ssd_bwd_workspace_size_doc_states(const ssd_params_t* p);
  * All pointers are device memory with 16-byte aligned bases; no output may equal
  * an input.  Packed documents (cu_seqlens with ndocs, batch 1; strictly
  * increasing, from 0 to seqlen) are independent sequences: no state and no
- * gradient crosses a document boundary.  Without per-document states they
- * take the tensor-core path for its shape (a -inf log-decay at each document
- * start); with initial_states, dfinal_states or dinitial_states they run on
- * CUDA cores, one block per (head, document), walking the document's own
- * chunks of at most 32 tokens from its start: each document
+ * gradient crosses a document boundary.  Without per-document states the
+ * tensor-core path for its shape runs whole rows (a -inf log-decay at each
+ * document start); with initial_states, dfinal_states or dinitial_states every
+ * path runs one unit per (head, document), walking the document's own chunks
+ * from its first token: each document
  * starts from its initial state (its first token's decay applied to it), its
  * final state receives dfinal_states[d], and dinitial_states[d] is the
  * gradient of initial_states[d].  headdim * dstate > 8192 and shapes whose
