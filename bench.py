@@ -90,6 +90,8 @@ def workload(name: str):
         return synth.config_decode(int(parts[1]) if len(parts) > 1 else 256)
     if name == "bwd_long":
         return synth.config_long()
+    if name == "bwd_varlen_states":
+        return synth.config_varlen(init_std=0.2)
     if name.startswith("bwd"):
         parts = name.split(":")
         return synth.config_27b(batch=int(parts[1]) if len(parts) > 1 else 8)
@@ -596,8 +598,9 @@ def run_gate_norm(args, p, dev, rank, local_rank, world):
 
 
 def run_bwd(args, p, dev, rank, local_rank, world):
-    """Backward workload: a step is one ssd_bwd call over the 2.7B-like layer
-    (the forward's inputs, random dy and dfinal_states)."""
+    """Backward workload: a step is one ssd_bwd call over the configuration's
+    inputs, random dy and dfinal_states (packed documents: every document's
+    initial state and final-state gradient, and its dinit)."""
     import torch
     import torch.distributed as dist
     import mamba_ssd_chunked_scan_gb300 as ssd
@@ -611,12 +614,16 @@ def run_bwd(args, p, dev, rank, local_rank, world):
     dt = torch.from_numpy(p.dt).to(dev)
     A = torch.from_numpy(p.A).to(dev)
     D = torch.from_numpy(p.D).to(dev)
-    dfin = torch.from_numpy(rng.standard_normal((p.batch, p.nheads, p.headdim, p.dstate)).astype(np.float32)).to(dev)
+    docs = p.cu_seqlens is not None
+    nst = p.nstates if docs else p.batch
+    dfin = torch.from_numpy(rng.standard_normal((nst, p.nheads, p.headdim, p.dstate)).astype(np.float32)).to(dev)
+    init = torch.from_numpy(p.initial_states).to(dev) if p.initial_states is not None else None
+    cu = torch.from_numpy(p.cu_seqlens).to(dev) if docs else None
     flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
     stream = torch.cuda.current_stream()
 
-    def step(xx=x, dd=dt, bb=B, cc=C, yy=dy):
-        return ssd.ssd_bwd(xx, dd, A, bb, cc, yy, D, None, dfin, want_dinit=False, stream=stream)
+    def step(xx=x, dd=dt, bb=B, cc=C, yy=dy, ii=init, ff=dfin):
+        return ssd.ssd_bwd(xx, dd, A, bb, cc, yy, D, ii, ff, cu, want_dinit=docs, stream=stream)
 
     for _ in range(args.warmup):
         flush.zero_()
@@ -636,9 +643,10 @@ def run_bwd(args, p, dev, rank, local_rank, world):
     ms = sum(a.elapsed_time(b) for a, b in ev) / args.steps
 
     # end to end: inputs from pinned host memory, the gradients back to pinned host memory
-    hin = [t.cpu().pin_memory() for t in (x, dt, B, C, dy)]
+    ins = (x, dt, B, C, dy) + ((init, dfin) if docs else ())
+    hin = [t.cpu().pin_memory() for t in ins]
     h2d = sum(t.numel() * t.element_size() for t in hin)
-    din = [torch.empty_like(t) for t in (x, dt, B, C, dy)]
+    din = [torch.empty_like(t) for t in ins]
     g0 = step()
     hout = {k: torch.empty(v.shape, dtype=v.dtype).pin_memory() for k, v in g0.items() if v is not None}
     d2h = sum(t.numel() * t.element_size() for t in hout.values())

@@ -198,3 +198,28 @@ def test_bwd_splits_agree_with_whole_rows_on_a_long_sequence():
                    ("dinit", 1e-4)):
         e = rel_err(split[k], whole[k])
         assert e <= tol, f"{k}: {e:.3e} > {tol}"
+
+
+def test_bwd_documents_with_states_full_size_sampled():
+    """C5's full size (32,768 tokens in 37 packed documents, 48 heads, bf16)
+    with every document's initial state and final-state gradient.  Documents
+    are independent sequences, so each sampled one (the first, one in the
+    middle, the last) is run by the oracle on its own, from its initial state
+    and with its final-state gradient, and gives every gradient of its tokens
+    and its dinit.  (dA and dD sum over all documents; the smaller cases above
+    check them.)"""
+    p = synth.config_varlen(init_std=0.2)
+    dy, dfin = cotangents(p, 17)
+    got = run_bwd(p, dy, dfin)
+    cu = p.cu_seqlens
+    for d in (0, p.ndocs // 2, p.ndocs - 1):
+        t0, t1 = int(cu[d]), int(cu[d + 1])
+        q = synth.SSDProblem(1, t1 - t0, p.nheads, p.headdim, p.dstate, p.ngroups, p.chunk, 0, p.dtype,
+                             p.x[:, t0:t1].copy(), p.dt[:, t0:t1].copy(), p.A, p.B[:, t0:t1].copy(),
+                             p.C[:, t0:t1].copy(), p.D, p.initial_states[d:d + 1].copy(), None, f"doc{d}")
+        want = oracle.ssd_backward(q, dy[:, t0:t1].copy(), dfin[d:d + 1].copy())
+        for k, g in (("dx", got["dx"][:, t0:t1]), ("ddt", got["ddt"][:, t0:t1]), ("dB", got["dB"][:, t0:t1]),
+                     ("dC", got["dC"][:, t0:t1]), ("dinit", got["dinit"][d:d + 1])):
+            assert np.isfinite(g).all(), (d, k)
+            e = rel_err(g, want[k])
+            assert e <= BWD_TOL["bf16"], f"document {d} {k}: {e:.3e}"
