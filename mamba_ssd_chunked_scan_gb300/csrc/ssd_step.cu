@@ -14,8 +14,10 @@
 // The step reads and writes the P x N fp32 state once and touches little
 // else, so it is bound by HBM bandwidth on the state: one CTA per (b, h)
 // streams the state rows as float4 vectors (each row owned by a segment of
-// SEG lanes, VPL vectors per lane), several rows in flight per thread, and
-// reduces y_p within the segment by shuffles.
+// SEG lanes, VPL vectors per lane), 16 / VPL rows in flight per segment (64
+// state registers per thread: all 64 rows of a Mamba-2 head in one pass, so
+// that small batches, whose CTAs are all resident at once, keep enough bytes
+// in flight), and reduces y_p within the segment by shuffles.
 #include "ssd_common.cuh"
 #include "ssd_kernels.h"
 
@@ -23,10 +25,10 @@ namespace ssd {
 namespace {
 
 constexpr int kStepThreads = 128;
-constexpr int kStepRows = 4;   // rows each segment has in flight
 
 template <typename T, int SEG, int VPL>
 __global__ void __launch_bounds__(kStepThreads) ssd_step_kernel(StepArgs a) {
+    constexpr int kStepRows = 16 / VPL;   // rows each segment has in flight
     extern __shared__ float sm[];
     const int P = a.P, N = a.N, N4 = a.N >> 2;
     float* sB = sm;            // [N]  B_n
