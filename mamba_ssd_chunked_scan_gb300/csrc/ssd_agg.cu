@@ -73,6 +73,31 @@ struct AggSmall {
     int never;
 };
 
+// L2 policies: x streams through once (evicted first), while the split states stay
+// for the split scan that reads them next (evicted last); without them the x
+// stream pushed the states out of L2 and the scan read them back from HBM.
+__device__ __forceinline__ uint64_t l2_evict_first() {
+    uint64_t p;
+    asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(p));
+    return p;
+}
+__device__ __forceinline__ uint64_t l2_evict_last() {
+    uint64_t p;
+    asm volatile("createpolicy.fractional.L2::evict_last.b64 %0, 1.0;" : "=l"(p));
+    return p;
+}
+__device__ __forceinline__ void tma_load_4d_hint(void* smem_dst, const CUtensorMap* tm, uint64_t* bar, int c0, int c1,
+                                                 int c2, int c3, uint64_t pol) {
+    asm volatile(
+        "cp.async.bulk.tensor.4d.shared::cluster.global.mbarrier::complete_tx::bytes.L2::cache_hint [%0], [%1, {%3, "
+        "%4, %5, %6}], [%2], %7;" ::"r"(ptx::smem_u32(smem_dst)),
+        "l"(tm), "r"(ptx::smem_u32(bar)), "r"(c0), "r"(c1), "r"(c2), "r"(c3), "l"(pol)
+        : "memory");
+}
+__device__ __forceinline__ void st_hint(float* p, float v, uint64_t pol) {
+    asm volatile("st.global.L2::cache_hint.f32 [%0], %1, %2;" ::"l"(p), "f"(v), "l"(pol) : "memory");
+}
+
 struct AggParams {
     CUtensorMap tm_x, tm_B;
     FwdArgs a;
@@ -160,6 +185,7 @@ __global__ void __launch_bounds__(kThreads, 1) ssd_split_agg_tc(const __grid_con
             // ============================================================ TMA producer
             int issued = 0;
             constexpr int NS = Cfg::kStages;
+            const uint64_t stream_pol = l2_evict_first();
             for (int r = 0; r < (a.stall_loads ? 0 : nch); ++r) {
                 const int st = r % NS;
                 if (r >= NS && !agg_wait(sh, a, &sh.empty[st], ((r / NS) - 1) & 1, kWhereAggEmpty)) break;
@@ -170,7 +196,7 @@ __global__ void __launch_bounds__(kThreads, 1) ssd_split_agg_tc(const __grid_con
                 ptx::tma_load_4d(stg + 16384, &prm.tm_B, &sh.full[st], 64, g, t, b);
 #pragma unroll
                 for (int h = 0; h < K; ++h)
-                    ptx::tma_load_4d(stg + kTileB + h * kTileX, &prm.tm_x, &sh.full[st], 0, h0 + h, t, b);
+                    tma_load_4d_hint(stg + kTileB + h * kTileX, &prm.tm_x, &sh.full[st], 0, h0 + h, t, b, stream_pol);
                 ++issued;
             }
             for (int st = 0; st < NS && st < issued; ++st) {
@@ -356,10 +382,11 @@ __global__ void __launch_bounds__(kThreads, 1) ssd_split_agg_tc(const __grid_con
                                 fmaf(dec, __ldg(init + (size_t)(p + 32) * N), __uint_as_float(d1[p])));
                         }
                     }
+                    const uint64_t keep = l2_evict_last();
 #pragma unroll
                     for (int p = 0; p < 32; ++p) {
-                        out[(size_t)p * N] = __uint_as_float(d0[p]);
-                        out[(size_t)(p + 32) * N] = __uint_as_float(d1[p]);
+                        st_hint(out + (size_t)p * N, __uint_as_float(d0[p]), keep);
+                        st_hint(out + (size_t)(p + 32) * N, __uint_as_float(d1[p]), keep);
                     }
                     if (mt == 0) a.ws_tau[ws] = lsum * kLn2;   // (reverse mode: its own tau array)
                 }
